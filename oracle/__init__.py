@@ -1,0 +1,153 @@
+"""The oracle: plain float64 CPU restatement of paged decode attention.
+
+TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import it; the library
+``paged_kv_decode_slot_gb300`` never does, and the two share no code.
+
+The C implementation is ``pkv_oracle.c``; this module compiles it with gcc
+and exposes numpy-facing wrappers (argument marshalling only).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "pkv_oracle.c")
+LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_D = ctypes.c_double
+
+
+def compile_oracle(source: str = SOURCE, out: str = LIB_PATH, extra_flags=()) -> str:
+    """gcc -O2 the oracle into a shared library (plain C11, libm, pthreads)."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread",
+                           "-I", _HERE, *extra_flags, "-o", tmp, source, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
+def build_oracle(force: bool = False) -> str:
+    hdr = os.path.join(_HERE, "pkv_oracle.h")
+    newest = max(os.path.getmtime(SOURCE), os.path.getmtime(hdr))
+    if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < newest:
+        compile_oracle()
+    return LIB_PATH
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data
+
+
+class Oracle:
+    """numpy wrappers over one compiled copy of the oracle library."""
+
+    def __init__(self, lib_path: str | None = None):
+        if lib_path is None:
+            lib_path = build_oracle()
+        lib = ctypes.CDLL(lib_path)
+        lib.oracle_kv_bytes.argtypes = [_I64] * 5
+        lib.oracle_kv_bytes.restype = ctypes.c_uint64
+        lib.oracle_slot_mapping.argtypes = [_P, _I32, _P, _I32, _I32, _P]
+        lib.oracle_append.argtypes = [_P, _P, _P, _I32, _P, _P, _I32, _I32]
+        lib.oracle_gather.argtypes = [_P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P]
+        lib.oracle_decode.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
+                                      _D, _P, _P, ctypes.c_int]
+        lib.oracle_decode_partitions.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32,
+                                                 _I32, _D, _I32, _I32, _P, _P, ctypes.c_int]
+        lib.oracle_lse_merge.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P]
+        self.lib = lib
+
+    # -- KV size -------------------------------------------------------------------
+    def kv_bytes(self, layers, kv_heads, head_dim, tokens, bytes_per_elem) -> int:
+        return int(self.lib.oracle_kv_bytes(layers, kv_heads, head_dim, tokens, bytes_per_elem))
+
+    # -- slot mapping / append / gather --------------------------------------------
+    def slot_mapping(self, block_tables, context_lens, bs=16) -> np.ndarray:
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        out = np.empty(cl.shape[0], dtype=np.int64)
+        self.lib.oracle_slot_mapping(_ptr(bt), bt.shape[1], _ptr(cl), cl.shape[0], bs, _ptr(out))
+        return out
+
+    def append(self, k_new, v_new, slots, k_cache, v_cache):
+        """Writes into (and returns) k_cache, v_cache, which must be C-contiguous uint16."""
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        kn = np.ascontiguousarray(k_new, dtype=np.uint16)
+        vn = np.ascontiguousarray(v_new, dtype=np.uint16)
+        sl = np.ascontiguousarray(slots, dtype=np.int64)
+        K, H = kn.shape[1], kn.shape[2]
+        self.lib.oracle_append(_ptr(kn), _ptr(vn), _ptr(sl), sl.shape[0], _ptr(k_cache),
+                               _ptr(v_cache), K, H)
+        return k_cache, v_cache
+
+    def gather(self, k_cache, v_cache, block_tables, context_lens, bs=16):
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        cu = np.zeros(cl.shape[0] + 1, dtype=np.int64)
+        cu[1:] = np.cumsum(cl.astype(np.int64))
+        K, H = k_cache.shape[2], k_cache.shape[3]
+        ko = np.empty((int(cu[-1]), K, H), dtype=np.uint16)
+        vo = np.empty((int(cu[-1]), K, H), dtype=np.uint16)
+        self.lib.oracle_gather(_ptr(np.ascontiguousarray(k_cache)), _ptr(np.ascontiguousarray(v_cache)),
+                               _ptr(bt), bt.shape[1], _ptr(cl), _ptr(cu), cl.shape[0], bs, K, H,
+                               _ptr(ko), _ptr(vo))
+        return ko, vo, cu
+
+    # -- attention -------------------------------------------------------------------
+    def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale, bs=16, threads=0):
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        kc = np.ascontiguousarray(k_cache, dtype=np.uint16)
+        vc = np.ascontiguousarray(v_cache, dtype=np.uint16)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        B, N, H = q.shape
+        K = kc.shape[2]
+        assert N % K == 0 and kc.shape[3] == H
+        out = np.empty((B, N, H), dtype=np.float64)
+        lse = np.empty((B, N), dtype=np.float64)
+        self.lib.oracle_decode(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cl),
+                               B, N, K, H, bs, float(scale), _ptr(out), _ptr(lse), threads)
+        return out, lse
+
+    def decode_partitions(self, q, k_cache, v_cache, block_tables, context_lens, scale,
+                          partition_tokens, max_parts, bs=16, threads=0):
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        kc = np.ascontiguousarray(k_cache, dtype=np.uint16)
+        vc = np.ascontiguousarray(v_cache, dtype=np.uint16)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        B, N, H = q.shape
+        K = kc.shape[2]
+        po = np.empty((B, N, max_parts, H), dtype=np.float64)
+        pl = np.empty((B, N, max_parts), dtype=np.float64)
+        self.lib.oracle_decode_partitions(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
+                                          _ptr(cl), B, N, K, H, bs, float(scale),
+                                          partition_tokens, max_parts, _ptr(po), _ptr(pl), threads)
+        return po, pl
+
+    def lse_merge(self, part_out, part_lse):
+        po = np.ascontiguousarray(part_out, dtype=np.float64)
+        pl = np.ascontiguousarray(part_lse, dtype=np.float64)
+        B, N, P, H = po.shape
+        out = np.empty((B, N, H), dtype=np.float64)
+        lse = np.empty((B, N), dtype=np.float64)
+        self.lib.oracle_lse_merge(_ptr(po), _ptr(pl), B, N, H, P, _ptr(out), _ptr(lse))
+        return out, lse
+
+
+_default = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default

@@ -1,0 +1,265 @@
+/*
+ * pkv_oracle.c - the oracle: decode-step attention over a paged KV cache,
+ * restated plainly in float64 on the CPU.
+ *
+ * TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
+ * CPU-baseline leg call it; the product path never does.  It shares no code
+ * with the CUDA library.
+ *
+ * What it follows:
+ *  - KV cache size: "Optimización de la inferencia", section "Cache de KV",
+ *    memory formula 2 * num_layers * num_kv_heads * head_dim * seq_len *
+ *    bytes; also Week 11 "Inference", Step 2 (2 * B * S * L * K * H * bytes).
+ *  - Paged layout: "Optimización de la inferencia", section "Página Atención"
+ *    (fixed 16-token pages anywhere in memory, a page table mapping logical
+ *    positions to physical pages); CS336 Lecture 10 notes, "分页注意力".
+ *  - Appending the new token's K/V: "Optimización de la inferencia", section
+ *    "Cache de KV" (compute K, V only for token N and join it to the cache),
+ *    and Step 1 (KVCache.update writes the new keys/values after the cached
+ *    ones and returns the cache up to and including them).
+ *  - Attention: Step 2, scaled_dot_product_attention: scores = q . k / sqrt(d)
+ *    (here an explicit scale), subtract the row maximum, exponentiate,
+ *    normalise by the sum, multiply by V.  With one query token no mask
+ *    applies (the mask there is built only when there is more than one query
+ *    row; Week 11 "Inference", Common mistakes, warns against a causal mask
+ *    at T = 1).
+ *  - GQA: each KV head serves N/K query heads (CS336 Lecture 10 notes,
+ *    "分组查询注意力"); query head n uses KV head n / (N/K).
+ */
+#include "pkv_oracle.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+static double bf16_to_double(uint16_t bits16)
+{
+    uint32_t bits = (uint32_t)bits16 << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+uint64_t oracle_kv_bytes(int64_t layers, int64_t kv_heads, int64_t head_dim, int64_t tokens,
+                         int64_t bytes_per_elem)
+{
+    return 2u * (uint64_t)layers * (uint64_t)kv_heads * (uint64_t)head_dim * (uint64_t)tokens *
+           (uint64_t)bytes_per_elem;
+}
+
+/* Physical slot of logical token t of sequence b: the block table entry of
+   block t / bs, and offset t % bs inside it. */
+static int64_t physical_slot(const int32_t *block_tables, int32_t max_nb, int32_t b, int64_t t,
+                             int32_t bs)
+{
+    int64_t block = block_tables[(int64_t)b * max_nb + t / bs];
+    return block * bs + t % bs;
+}
+
+void oracle_slot_mapping(const int32_t *block_tables, int32_t max_nb, const int32_t *context_lens,
+                         int32_t B, int32_t bs, int64_t *slots)
+{
+    for (int32_t b = 0; b < B; ++b) {
+        int64_t pos = (int64_t)context_lens[b] - 1; /* the newest token */
+        slots[b] = pos < 0 ? -1 : physical_slot(block_tables, max_nb, b, pos, bs);
+    }
+}
+
+void oracle_append(const uint16_t *k_new, const uint16_t *v_new, const int64_t *slots, int32_t T,
+                   uint16_t *k_cache, uint16_t *v_cache, int32_t K, int32_t H)
+{
+    size_t row = (size_t)K * (size_t)H; /* all KV heads of one token */
+    for (int32_t i = 0; i < T; ++i) {
+        if (slots[i] < 0) continue;
+        memcpy(k_cache + (size_t)slots[i] * row, k_new + (size_t)i * row, row * sizeof(uint16_t));
+        memcpy(v_cache + (size_t)slots[i] * row, v_new + (size_t)i * row, row * sizeof(uint16_t));
+    }
+}
+
+void oracle_gather(const uint16_t *k_cache, const uint16_t *v_cache, const int32_t *block_tables,
+                   int32_t max_nb, const int32_t *context_lens, const int64_t *cu_seqlens,
+                   int32_t B, int32_t bs, int32_t K, int32_t H, uint16_t *k_out, uint16_t *v_out)
+{
+    size_t row = (size_t)K * (size_t)H;
+    for (int32_t b = 0; b < B; ++b) {
+        for (int64_t t = 0; t < context_lens[b]; ++t) {
+            int64_t slot = physical_slot(block_tables, max_nb, b, t, bs);
+            memcpy(k_out + (size_t)(cu_seqlens[b] + t) * row, k_cache + (size_t)slot * row,
+                   row * sizeof(uint16_t));
+            memcpy(v_out + (size_t)(cu_seqlens[b] + t) * row, v_cache + (size_t)slot * row,
+                   row * sizeof(uint16_t));
+        }
+    }
+}
+
+/* Attention of one query vector over ntok contiguous keys/values [ntok][H]. */
+static void attend(const double *q, const double *keys, const double *values, int64_t ntok,
+                   int32_t H, double scale, double *scores, double *out, double *lse)
+{
+    if (ntok <= 0) { /* nothing to attend to: empty sum */
+        for (int32_t h = 0; h < H; ++h) out[h] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    for (int64_t t = 0; t < ntok; ++t) { /* scores = scale * q . k_t */
+        double dot = 0.0;
+        for (int32_t h = 0; h < H; ++h) dot += q[h] * keys[t * H + h];
+        scores[t] = scale * dot;
+    }
+    double mx = scores[0]; /* subtract the maximum before exponentiating */
+    for (int64_t t = 1; t < ntok; ++t)
+        if (scores[t] > mx) mx = scores[t];
+    double sum = 0.0;
+    for (int64_t t = 0; t < ntok; ++t) {
+        scores[t] = exp(scores[t] - mx);
+        sum += scores[t];
+    }
+    for (int64_t t = 0; t < ntok; ++t) scores[t] /= sum; /* attention weights */
+    for (int32_t h = 0; h < H; ++h) {                    /* weights times V */
+        double acc = 0.0;
+        for (int64_t t = 0; t < ntok; ++t) acc += scores[t] * values[t * H + h];
+        out[h] = acc;
+    }
+    *lse = mx + log(sum);
+}
+
+typedef struct {
+    const uint16_t *q, *k_cache, *v_cache;
+    const int32_t *block_tables, *context_lens;
+    int32_t max_nb, B, N, K, H, bs;
+    double scale;
+    int32_t partition_tokens, max_parts; /* partition_tokens <= 0: whole sequence */
+    double *out, *lse;
+    int nthreads, tid;
+} decode_job;
+
+/* One (sequence, KV head) unit: gather its K/V rows through the block table into
+   contiguous float64 arrays, then attend for each query head of the group. */
+static void decode_unit(const decode_job *j, int32_t b, int32_t kvh)
+{
+    const int32_t H = j->H, G = j->N / j->K;
+    const int64_t ctx = j->context_lens[b] > 0 ? j->context_lens[b] : 0;
+    double *keys = malloc(sizeof(double) * (size_t)(ctx > 0 ? ctx : 1) * (size_t)H);
+    double *values = malloc(sizeof(double) * (size_t)(ctx > 0 ? ctx : 1) * (size_t)H);
+    double *scores = malloc(sizeof(double) * (size_t)(ctx > 0 ? ctx : 1));
+    double *qv = malloc(sizeof(double) * (size_t)H);
+    for (int64_t t = 0; t < ctx; ++t) {
+        int64_t slot = physical_slot(j->block_tables, j->max_nb, b, t, j->bs);
+        const uint16_t *krow = j->k_cache + ((size_t)slot * j->K + kvh) * H;
+        const uint16_t *vrow = j->v_cache + ((size_t)slot * j->K + kvh) * H;
+        for (int32_t h = 0; h < H; ++h) {
+            keys[t * H + h] = bf16_to_double(krow[h]);
+            values[t * H + h] = bf16_to_double(vrow[h]);
+        }
+    }
+    for (int32_t g = 0; g < G; ++g) {
+        int32_t n = kvh * G + g;
+        const uint16_t *qrow = j->q + ((size_t)b * j->N + n) * H;
+        for (int32_t h = 0; h < H; ++h) qv[h] = bf16_to_double(qrow[h]);
+        size_t bn = (size_t)b * j->N + n;
+        if (j->partition_tokens <= 0) {
+            attend(qv, keys, values, ctx, H, j->scale, scores, j->out + bn * H, j->lse + bn);
+        } else {
+            for (int32_t p = 0; p < j->max_parts; ++p) {
+                int64_t t0 = (int64_t)p * j->partition_tokens;
+                int64_t t1 = t0 + j->partition_tokens;
+                if (t1 > ctx) t1 = ctx;
+                if (t0 > ctx) t0 = ctx;
+                size_t bnp = bn * j->max_parts + p;
+                attend(qv, keys + t0 * H, values + t0 * H, t1 - t0, H, j->scale, scores,
+                       j->out + bnp * H, j->lse + bnp);
+            }
+        }
+    }
+    free(keys);
+    free(values);
+    free(scores);
+    free(qv);
+}
+
+static void *decode_worker(void *arg)
+{
+    const decode_job *j = (const decode_job *)arg;
+    int64_t units = (int64_t)j->B * j->K;
+    for (int64_t u = j->tid; u < units; u += j->nthreads)
+        decode_unit(j, (int32_t)(u / j->K), (int32_t)(u % j->K));
+    return 0;
+}
+
+static void run_decode(decode_job proto)
+{
+    int nt = proto.nthreads;
+    if (nt <= 0) {
+        long c = sysconf(_SC_NPROCESSORS_ONLN);
+        nt = c > 0 ? (int)c : 1;
+    }
+    if (nt > 512) nt = 512;
+    if (nt > proto.B * proto.K) nt = proto.B * proto.K > 0 ? proto.B * proto.K : 1;
+    decode_job jobs[512];
+    pthread_t tids[512];
+    int started[512];
+    for (int t = 0; t < nt; ++t) {
+        jobs[t] = proto;
+        jobs[t].nthreads = nt;
+        jobs[t].tid = t;
+        started[t] = t > 0 && pthread_create(&tids[t], 0, decode_worker, &jobs[t]) == 0;
+    }
+    decode_worker(&jobs[0]);
+    for (int t = 1; t < nt; ++t) {
+        if (started[t])
+            pthread_join(tids[t], 0);
+        else
+            decode_worker(&jobs[t]);
+    }
+}
+
+void oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                   const int32_t *block_tables, int32_t max_nb, const int32_t *context_lens,
+                   int32_t B, int32_t N, int32_t K, int32_t H, int32_t bs, double scale,
+                   double *out, double *lse, int nthreads)
+{
+    decode_job j = {q, k_cache, v_cache, block_tables, context_lens, max_nb, B, N, K, H, bs,
+                    scale, 0, 1, out, lse, nthreads, 0};
+    run_decode(j);
+}
+
+void oracle_decode_partitions(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                              const int32_t *block_tables, int32_t max_nb,
+                              const int32_t *context_lens, int32_t B, int32_t N, int32_t K,
+                              int32_t H, int32_t bs, double scale, int32_t partition_tokens,
+                              int32_t max_parts, double *part_out, double *part_lse, int nthreads)
+{
+    decode_job j = {q, k_cache, v_cache, block_tables, context_lens, max_nb, B, N, K, H, bs,
+                    scale, partition_tokens, max_parts, part_out, part_lse, nthreads, 0};
+    run_decode(j);
+}
+
+/* Softmax over a union of disjoint key sets: each part's (out_p, lse_p) is its own
+   normalised attention; the whole is the lse-weighted combination. */
+void oracle_lse_merge(const double *part_out, const double *part_lse, int32_t B, int32_t N,
+                      int32_t H, int32_t max_parts, double *out, double *lse)
+{
+    for (int64_t bn = 0; bn < (int64_t)B * N; ++bn) {
+        const double *pl = part_lse + bn * max_parts;
+        double mx = -INFINITY;
+        for (int32_t p = 0; p < max_parts; ++p)
+            if (pl[p] > mx) mx = pl[p];
+        if (mx == -INFINITY) { /* no tokens at all */
+            for (int32_t h = 0; h < H; ++h) out[bn * H + h] = 0.0;
+            lse[bn] = -INFINITY;
+            continue;
+        }
+        double sum = 0.0;
+        for (int32_t p = 0; p < max_parts; ++p) sum += exp(pl[p] - mx);
+        double total = mx + log(sum);
+        for (int32_t h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int32_t p = 0; p < max_parts; ++p)
+                acc += exp(pl[p] - total) * part_out[(bn * max_parts + p) * H + h];
+            out[bn * H + h] = acc;
+        }
+        lse[bn] = total;
+    }
+}

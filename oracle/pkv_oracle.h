@@ -1,0 +1,65 @@
+/*
+ * pkv_oracle.h - the oracle for paged decode attention: a plain, slow,
+ * obviously correct CPU restatement in float64.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may call it.  It shares no code, header,
+ * table or helper with the CUDA library; it reads the same input bytes.
+ *
+ * Layouts (bf16 passed as uint16 bit patterns):
+ *   q            [B][N][H]
+ *   k/v cache    [num_blocks][bs][K][H]   row (block*bs + off)*K + kvh holds H values
+ *   block_tables [B][max_nb]               int32 physical block ids
+ *   context_lens [B]                       tokens attended, including the new one
+ *   out          [B][N][H] double,  lse [B][N] double (natural log)
+ * Query head n reads KV head n / (N/K)  (contiguous query groups).
+ */
+#ifndef PKV_ORACLE_H
+#define PKV_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* KV cache bytes = 2 * layers * kv_heads * head_dim * tokens * bytes_per_elem. */
+uint64_t oracle_kv_bytes(int64_t layers, int64_t kv_heads, int64_t head_dim, int64_t tokens,
+                         int64_t bytes_per_elem);
+
+/* slot of each sequence's newest token (logical position ctx-1); -1 when ctx <= 0. */
+void oracle_slot_mapping(const int32_t *block_tables, int32_t max_nb, const int32_t *context_lens,
+                         int32_t B, int32_t bs, int64_t *slots);
+
+/* copy k_new[i], v_new[i] ([T][K][H]) into cache slot slots[i]; negative slots are skipped. */
+void oracle_append(const uint16_t *k_new, const uint16_t *v_new, const int64_t *slots, int32_t T,
+                   uint16_t *k_cache, uint16_t *v_cache, int32_t K, int32_t H);
+
+/* contiguous copy of each sequence's K/V rows: out[(cu_seqlens[b] + t)][K][H] for t < ctx_b. */
+void oracle_gather(const uint16_t *k_cache, const uint16_t *v_cache, const int32_t *block_tables,
+                   int32_t max_nb, const int32_t *context_lens, const int64_t *cu_seqlens,
+                   int32_t B, int32_t bs, int32_t K, int32_t H, uint16_t *k_out, uint16_t *v_out);
+
+/* decode attention for every (b, n); nthreads <= 0 means all online cores. */
+void oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                   const int32_t *block_tables, int32_t max_nb, const int32_t *context_lens,
+                   int32_t B, int32_t N, int32_t K, int32_t H, int32_t bs, double scale,
+                   double *out, double *lse, int nthreads);
+
+/* the same attention restricted to each partition of partition_tokens logical tokens:
+   part_out [B][N][max_parts][H], part_lse [B][N][max_parts]; an empty partition has
+   out 0 and lse -inf. */
+void oracle_decode_partitions(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                              const int32_t *block_tables, int32_t max_nb,
+                              const int32_t *context_lens, int32_t B, int32_t N, int32_t K,
+                              int32_t H, int32_t bs, double scale, int32_t partition_tokens,
+                              int32_t max_parts, double *part_out, double *part_lse, int nthreads);
+
+/* combine partitions: lse = log sum_p exp(lse_p); out = sum_p exp(lse_p - lse) out_p. */
+void oracle_lse_merge(const double *part_out, const double *part_lse, int32_t B, int32_t N,
+                      int32_t H, int32_t max_parts, double *out, double *lse);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
