@@ -1,0 +1,194 @@
+/*
+ * pkv.h - libpagedkv: decode-step attention over a paged KV cache, for one
+ * NVIDIA GB300 (sm_103a).  Plain C ABI: device pointers, sizes and a CUDA
+ * stream; no framework types.
+ *
+ * The method.  In a continuously batched decode step each sequence b has one
+ * new query token with N query heads that share K KV heads (GQA; query head
+ * n reads KV head n / (N/K)).  The token's own key and value are first
+ * appended to the cache, then it attends to its whole history:
+ *     s_t      = scale * q[b,n,:] . K[b,t,kvh,:]       t in [0, ctx_b)
+ *     out[b,n] = sum_t softmax(s)_t V[b,t,kvh,:],      lse[b,n] = ln sum_t e^{s_t}
+ * Sources: "Optimización de la inferencia" (aiengineeringfromscratch.com),
+ * sections "Cache de KV" (append only the new token's K/V), "Página
+ * Atención" (fixed-size pages anywhere in GPU memory, a page table from
+ * logical positions to physical pages) and "Construye el mismo", Step 2
+ * (max-subtracted scaled dot-product attention); CS336 Lecture 10 notes
+ * "注意力层的算术强度分析" (decode attention intensity S/(S+1) < 1) and
+ * "分页注意力（PagedAttention）" ("融合块读取和注意力的内核", FlashDecoding).
+ *
+ * Layouts (row-major, bf16 passed as 16-bit storage):
+ *   k_cache, v_cache  [num_blocks][block_size=16][K][H]   separate K and V pools
+ *   block_tables      [num_seqs][max_blocks_per_seq] int32; entry j of sequence b is
+ *                     the physical block of its logical tokens 16j .. 16j+15
+ *   context_lens      [num_seqs] int32: tokens attended, INCLUDING the token
+ *                     appended this step (its logical position is ctx-1)
+ *   q, out            [num_seqs][N][H] bf16;   lse [num_seqs][N] float (natural log)
+ *   k_new, v_new      [num_tokens][K][H] bf16; slot_mapping [num_tokens] int64,
+ *                     slot = block * 16 + offset, negative = skip the token
+ * Supported shapes: block_size 16, H in {64, 128}, G = N/K in {1, 2, 4, 8}.
+ *
+ * Ownership: every pointer is caller-owned device memory (k_new/v_new/q etc.
+ * must be in the same device's global memory); the library allocates nothing
+ * and keeps no state between calls besides cached device attributes.  Calls
+ * are asynchronous on the given stream (0 = the legacy default stream).
+ *
+ * Errors: each call returns a pkv_status.  Host-side validation happens
+ * before anything is launched.  Bad values that only the device sees (a
+ * block id outside [0, num_blocks), a slot beyond the pool, ctx beyond the
+ * table width) set bits in the caller's err_flag (a device int32, nullable,
+ * sticky: the caller zeroes it, synchronises and reads it, e.g. with
+ * pkv_read_err_flag); the offending work is skipped, never a fault.  Every
+ * wait inside a kernel is bounded; an expired wait sets PKV_FLAG_TIMEOUT.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pkv_bf16;                   /* bf16 bit pattern */
+typedef struct CUstream_st *pkv_stream_t;   /* identical to cudaStream_t */
+
+enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_NULL = -1,        /* a required pointer is NULL */
+    PKV_ERR_SHAPE = -2,       /* inconsistent sizes (N % K != 0, partitions too few, ...) */
+    PKV_ERR_UNSUPPORTED = -3, /* H not in {64,128}, G not in {1,2,4,8}, block_size != 16 */
+    PKV_ERR_RANGE = -4,       /* device-detected out-of-range value (err_flag non-zero) */
+    PKV_ERR_CUDA = -5,        /* a CUDA call failed; pkv_last_error() has the text */
+    PKV_ERR_ALIGN = -6,       /* a pointer lacks the alignment the layout needs */
+    PKV_ERR_WORKSPACE = -7    /* workspace missing or smaller than required */
+};
+
+/* err_flag bits */
+#define PKV_FLAG_BLOCK_RANGE 1 /* a block table entry outside [0, num_blocks) */
+#define PKV_FLAG_SLOT_RANGE 2  /* a slot >= num_blocks * 16 */
+#define PKV_FLAG_CTX_RANGE 4   /* context_len < 0 or > max_blocks_per_seq * 16 */
+#define PKV_FLAG_TIMEOUT 8     /* a bounded in-kernel wait expired; the unit's result is void */
+#define PKV_FLAG_OUT_RANGE 16  /* pkv_gather: a row beyond out_rows */
+
+typedef struct {
+    int32_t num_blocks;   /* physical blocks in each pool */
+    int32_t block_size;   /* tokens per block; must be 16 */
+    int32_t num_kv_heads; /* K */
+    int32_t head_dim;     /* H */
+} pkv_cache_desc;
+
+/*
+ * KV cache bytes = 2 * layers * kv_heads * head_dim * tokens * bytes_per_elem
+ * ("Optimización de la inferencia", section "Cache de KV", memory formula;
+ * Week 11 "Inference", Step 2).  Host only.
+ */
+uint64_t pkv_kv_bytes(int64_t layers, int64_t kv_heads, int64_t head_dim, int64_t tokens,
+                      int64_t bytes_per_elem);
+
+/*
+ * Slot mapping: slot_mapping[b] = block_tables[b][p / 16] * 16 + p % 16 for the
+ * newest token p = context_lens[b] - 1 (the page table maps logical positions
+ * to physical pages: "Optimización de la inferencia", "Página Atención").
+ * ctx <= 0 gives -1.  num_blocks bounds the ids (out of range: flag, slot -1).
+ */
+int pkv_slot_mapping(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                     const int32_t *context_lens, int32_t num_seqs, int32_t num_blocks,
+                     int64_t *slot_mapping, int32_t *err_flag, pkv_stream_t stream);
+
+/*
+ * Append: k_cache[slot / 16][slot % 16][:][:] = k_new[i] (and v), bit for bit,
+ * for each token i with slot_mapping[i] >= 0 ("Optimización de la
+ * inferencia", "Cache de KV": only the new token's key and value are computed
+ * and joined to the cache).  Slots within one call must be distinct.
+ * k_new/v_new/k_cache/v_cache must be 16-byte aligned.
+ */
+int pkv_append(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const int64_t *slot_mapping,
+               int32_t num_tokens, pkv_bf16 *k_cache, pkv_bf16 *v_cache, pkv_cache_desc cache,
+               int32_t *err_flag, pkv_stream_t stream);
+
+/*
+ * Single-pass decode attention: one CTA per (sequence, KV head) reads each
+ * K/V block once through the block table and serves the whole query group
+ * from it (CS336 Lecture 10 notes: fused block-read + attention kernel).
+ * out [num_seqs][N][H] bf16 (round-to-nearest-even of an fp32 result);
+ * lse_out [num_seqs][N] float, nullable.  ctx = 0 gives out 0, lse -inf.
+ * k_cache/v_cache 16-byte aligned; q and out 4-byte aligned.
+ */
+int pkv_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                    float scale, pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
+                    int32_t *err_flag, pkv_stream_t stream);
+
+/*
+ * Workspace for pkv_decode_attn_splitk: part_out float [num_seqs][N][max_partitions][H]
+ * followed (256-byte aligned) by part_lse float [num_seqs][N][max_partitions].
+ */
+size_t pkv_splitk_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                  int32_t max_partitions);
+
+/*
+ * Split-KV decode attention (FlashDecoding, named in CS336 Lecture 10 notes,
+ * "其他优化"): partition p of sequence b covers logical blocks
+ * [p * partition_blocks, (p+1) * partition_blocks) of its table.  One CTA per
+ * (partition, KV head, sequence) writes its normalised partial output and
+ * lse into the workspace, then pkv_lse_merge combines them (two launches,
+ * stream-ordered).  max_partitions must be >= ceil(max_blocks_per_seq /
+ * partition_blocks).  The workspace is caller-owned device memory of at
+ * least pkv_splitk_workspace_bytes(...) bytes, 256-byte aligned.
+ */
+int pkv_decode_attn_splitk(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                           float scale, pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
+                           int32_t partition_blocks, int32_t max_partitions, void *workspace,
+                           size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream);
+
+/*
+ * The partition step alone: writes part_out [num_seqs][N][max_partitions][H] and
+ * part_lse [num_seqs][N][max_partitions] (float, natural log) for the partitions
+ * that hold tokens; partitions past a sequence's last block are not written.
+ */
+int pkv_decode_attn_partitions(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                               const pkv_bf16 *v_cache, const int32_t *block_tables,
+                               int32_t max_blocks_per_seq, const int32_t *context_lens,
+                               int32_t num_seqs, int32_t num_q_heads, float scale,
+                               pkv_cache_desc cache, int32_t partition_blocks,
+                               int32_t max_partitions, float *part_out, float *part_lse,
+                               int32_t *err_flag, pkv_stream_t stream);
+
+/*
+ * Log-sum-exp merge of disjoint partitions (softmax over a union of disjoint
+ * key sets):  lse = ln sum_p e^{lse_p};  out = sum_p e^{lse_p - lse} out_p.
+ * Sequence b has ceil(ceil(ctx_b / 16) / partition_blocks) partitions; only
+ * those are read.  out bf16 [num_seqs][N][H]; lse_out nullable.
+ */
+int pkv_lse_merge(const float *part_out, const float *part_lse, const int32_t *context_lens,
+                  int32_t num_seqs, int32_t num_q_heads, int32_t head_dim, int32_t max_partitions,
+                  int32_t partition_blocks, pkv_bf16 *out, float *lse_out, pkv_stream_t stream);
+
+/*
+ * Block-table gather (test and debug export): k_out[(cu_seqlens[b] + t)][K][H] =
+ * k_cache[table[b][t / 16]][t % 16][K][H] for t < ctx_b (and v).  out_rows bounds
+ * the output (rows beyond it: flag, skipped).  All buffers 16-byte aligned.
+ */
+int pkv_gather(const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *block_tables,
+               int32_t max_blocks_per_seq, const int32_t *context_lens, const int64_t *cu_seqlens,
+               int32_t num_seqs, pkv_bf16 *k_out, pkv_bf16 *v_out, int64_t out_rows,
+               pkv_cache_desc cache, int32_t *err_flag, pkv_stream_t stream);
+
+/* Synchronise the stream, copy *err_flag to *host_value; PKV_ERR_RANGE if it is non-zero. */
+int pkv_read_err_flag(const int32_t *err_flag, int32_t *host_value, pkv_stream_t stream);
+
+/* Static text for a status code. */
+const char *pkv_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+const char *pkv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

@@ -1,0 +1,274 @@
+"""ctypes binding of libpagedkv: the C ABI's entry points under the same names.
+
+Argument marshalling only: each function checks dtypes, shapes and devices of
+its torch tensors, takes their device pointers and the current CUDA stream,
+and calls the library.  Every step of the computation runs in the library's
+CUDA kernels.  Functions return the C status code (0 = PKV_OK); ``check``
+turns a non-zero status into a ``PkvError``.
+
+The library must be built (``paged_kv_decode_slot_gb300.build``); importing
+this module without it raises ImportError -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libpagedkv.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+PKV_OK = 0
+PKV_ERR_NULL = -1
+PKV_ERR_SHAPE = -2
+PKV_ERR_UNSUPPORTED = -3
+PKV_ERR_RANGE = -4
+PKV_ERR_CUDA = -5
+PKV_ERR_ALIGN = -6
+PKV_ERR_WORKSPACE = -7
+
+PKV_FLAG_BLOCK_RANGE = 1
+PKV_FLAG_SLOT_RANGE = 2
+PKV_FLAG_CTX_RANGE = 4
+PKV_FLAG_TIMEOUT = 8
+PKV_FLAG_OUT_RANGE = 16
+
+BLOCK_SIZE = 16
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+
+_lib.pkv_kv_bytes.argtypes = [_I64] * 5
+_lib.pkv_kv_bytes.restype = ctypes.c_uint64
+_lib.pkv_slot_mapping.argtypes = [_P, _I32, _P, _I32, _I32, _P, _P, _P]
+_lib.pkv_append.argtypes = [_P, _P, _P, _I32, _P, _P, CacheDesc, _P, _P]
+_lib.pkv_decode_attn.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P, _P,
+                                 CacheDesc, _P, _P]
+_lib.pkv_splitk_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32]
+_lib.pkv_splitk_workspace_bytes.restype = ctypes.c_size_t
+_lib.pkv_decode_attn_splitk.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P,
+                                        _P, CacheDesc, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
+_lib.pkv_decode_attn_partitions.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float,
+                                            CacheDesc, _I32, _I32, _P, _P, _P, _P]
+_lib.pkv_lse_merge.argtypes = [_P, _P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P]
+_lib.pkv_gather.argtypes = [_P, _P, _P, _I32, _P, _P, _I32, _P, _P, _I64, CacheDesc, _P, _P]
+_lib.pkv_read_err_flag.argtypes = [_P, _P, _P]
+_lib.pkv_status_string.argtypes = [ctypes.c_int]
+_lib.pkv_status_string.restype = ctypes.c_char_p
+_lib.pkv_last_error.argtypes = []
+_lib.pkv_last_error.restype = ctypes.c_char_p
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int):
+        msg = _lib.pkv_status_string(status).decode()
+        if status == PKV_ERR_CUDA:
+            msg += ": " + _lib.pkv_last_error().decode()
+        super().__init__(f"libpagedkv status {status}: {msg}")
+        self.status = status
+
+
+def check(status: int) -> None:
+    if status != PKV_OK:
+        raise PkvError(status)
+
+
+def library():
+    """The loaded ctypes library (for tests that inspect exports)."""
+    return _lib
+
+
+# ---------------------------------------------------------------------------------------------
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, ndim, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _opt(t, dtype, ndim, name):
+    if t is not None:
+        _need(t, dtype, ndim, name)
+
+
+def cache_desc(k_cache: torch.Tensor) -> CacheDesc:
+    nb, bs, K, H = k_cache.shape
+    return CacheDesc(nb, bs, K, H)
+
+
+# ---------------------------------------------------------------------------------------------
+def pkv_kv_bytes(layers: int, kv_heads: int, head_dim: int, tokens: int, bytes_per_elem: int) -> int:
+    return int(_lib.pkv_kv_bytes(layers, kv_heads, head_dim, tokens, bytes_per_elem))
+
+
+def pkv_slot_mapping(block_tables, context_lens, num_blocks: int, slot_mapping, err_flag=None,
+                     stream=None) -> int:
+    _need(block_tables, torch.int32, 2, "block_tables")
+    _need(context_lens, torch.int32, 1, "context_lens")
+    _need(slot_mapping, torch.int64, 1, "slot_mapping")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    B = context_lens.shape[0]
+    if block_tables.shape[0] != B or slot_mapping.shape[0] != B:
+        raise ValueError("batch sizes differ")
+    return _lib.pkv_slot_mapping(_ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B,
+                                 num_blocks, _ptr(slot_mapping), _ptr(err_flag), _stream(stream))
+
+
+def pkv_append(k_new, v_new, slot_mapping, k_cache, v_cache, err_flag=None, stream=None) -> int:
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, torch.bfloat16, 3, n)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, 4, n)
+    _need(slot_mapping, torch.int64, 1, "slot_mapping")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    T = k_new.shape[0]
+    if slot_mapping.shape[0] != T or tuple(k_new.shape[1:]) != tuple(k_cache.shape[2:]):
+        raise ValueError("k_new [T, K, H] must match slot_mapping [T] and k_cache [nb, 16, K, H]")
+    if v_new.shape != k_new.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("K and V shapes differ")
+    return _lib.pkv_append(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T, _ptr(k_cache),
+                           _ptr(v_cache), cache_desc(k_cache), _ptr(err_flag), _stream(stream))
+
+
+def _attn_common(q, k_cache, v_cache, block_tables, context_lens):
+    _need(q, torch.bfloat16, 3, "q")
+    _need(k_cache, torch.bfloat16, 4, "k_cache")
+    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    _need(block_tables, torch.int32, 2, "block_tables")
+    _need(context_lens, torch.int32, 1, "context_lens")
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("K and V pools differ in shape")
+    B = q.shape[0]
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("batch sizes differ")
+    if q.shape[2] != k_cache.shape[3]:
+        raise ValueError("head_dim of q and the cache differ")
+
+
+def pkv_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale: float, out, lse_out=None,
+                    err_flag=None, stream=None) -> int:
+    _attn_common(q, k_cache, v_cache, block_tables, context_lens)
+    _need(out, torch.bfloat16, 3, "out")
+    _opt(lse_out, torch.float32, 2, "lse_out")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    B, N, _ = q.shape
+    return _lib.pkv_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                block_tables.shape[1], _ptr(context_lens), B, N, float(scale),
+                                _ptr(out), _ptr(lse_out), cache_desc(k_cache), _ptr(err_flag),
+                                _stream(stream))
+
+
+def pkv_splitk_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_partitions: int) -> int:
+    return int(_lib.pkv_splitk_workspace_bytes(num_seqs, num_q_heads, head_dim, max_partitions))
+
+
+def max_partitions_for(max_blocks_per_seq: int, partition_blocks: int) -> int:
+    return max(1, -(-max_blocks_per_seq // partition_blocks))
+
+
+def pkv_decode_attn_splitk(q, k_cache, v_cache, block_tables, context_lens, scale: float, out,
+                           partition_blocks: int, max_partitions: int, workspace, lse_out=None,
+                           err_flag=None, stream=None) -> int:
+    _attn_common(q, k_cache, v_cache, block_tables, context_lens)
+    _need(out, torch.bfloat16, 3, "out")
+    _opt(lse_out, torch.float32, 2, "lse_out")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    _need(workspace, torch.uint8, 1, "workspace")
+    B, N, _ = q.shape
+    return _lib.pkv_decode_attn_splitk(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                       block_tables.shape[1], _ptr(context_lens), B, N, float(scale),
+                                       _ptr(out), _ptr(lse_out), cache_desc(k_cache),
+                                       partition_blocks, max_partitions, _ptr(workspace),
+                                       workspace.numel(), _ptr(err_flag), _stream(stream))
+
+
+def pkv_decode_attn_partitions(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                               partition_blocks: int, part_out, part_lse, err_flag=None,
+                               stream=None) -> int:
+    _attn_common(q, k_cache, v_cache, block_tables, context_lens)
+    _need(part_out, torch.float32, 4, "part_out")
+    _need(part_lse, torch.float32, 3, "part_lse")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    B, N, H = q.shape
+    P = part_out.shape[2]
+    if tuple(part_out.shape) != (B, N, P, H) or tuple(part_lse.shape) != (B, N, P):
+        raise ValueError("part_out must be [B, N, P, H] and part_lse [B, N, P]")
+    return _lib.pkv_decode_attn_partitions(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                           block_tables.shape[1], _ptr(context_lens), B, N,
+                                           float(scale), cache_desc(k_cache), partition_blocks, P,
+                                           _ptr(part_out), _ptr(part_lse), _ptr(err_flag),
+                                           _stream(stream))
+
+
+def pkv_lse_merge(part_out, part_lse, context_lens, partition_blocks: int, out, lse_out=None,
+                  stream=None) -> int:
+    _need(part_out, torch.float32, 4, "part_out")
+    _need(part_lse, torch.float32, 3, "part_lse")
+    _need(context_lens, torch.int32, 1, "context_lens")
+    _need(out, torch.bfloat16, 3, "out")
+    _opt(lse_out, torch.float32, 2, "lse_out")
+    B, N, P, H = part_out.shape
+    return _lib.pkv_lse_merge(_ptr(part_out), _ptr(part_lse), _ptr(context_lens), B, N, H, P,
+                              partition_blocks, _ptr(out), _ptr(lse_out), _stream(stream))
+
+
+def pkv_gather(k_cache, v_cache, block_tables, context_lens, cu_seqlens, k_out, v_out, err_flag=None,
+               stream=None) -> int:
+    _need(k_cache, torch.bfloat16, 4, "k_cache")
+    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    _need(block_tables, torch.int32, 2, "block_tables")
+    _need(context_lens, torch.int32, 1, "context_lens")
+    _need(cu_seqlens, torch.int64, 1, "cu_seqlens")
+    _need(k_out, torch.bfloat16, 3, "k_out")
+    _need(v_out, torch.bfloat16, 3, "v_out")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    B = context_lens.shape[0]
+    return _lib.pkv_gather(_ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                           _ptr(context_lens), _ptr(cu_seqlens), B, _ptr(k_out), _ptr(v_out),
+                           k_out.shape[0], cache_desc(k_cache), _ptr(err_flag), _stream(stream))
+
+
+def pkv_read_err_flag(err_flag, stream=None) -> tuple[int, int]:
+    """(status, flag value): synchronises the stream and reads the device flag."""
+    _need(err_flag, torch.int32, 1, "err_flag")
+    host = ctypes.c_int32(0)
+    st = _lib.pkv_read_err_flag(_ptr(err_flag), ctypes.byref(host), _stream(stream))
+    return st, host.value
+
+
+def pkv_status_string(status: int) -> str:
+    return _lib.pkv_status_string(status).decode()
+
+
+def pkv_last_error() -> str:
+    return _lib.pkv_last_error().decode()

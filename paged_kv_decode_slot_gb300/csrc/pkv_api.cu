@@ -1,0 +1,377 @@
+// pkv_api.cu - the C ABI of libpagedkv: host-side validation, TMA descriptor encoding and
+// kernel launches.  Every entry point validates its arguments before launching anything and
+// returns a pkv_status; device-detected errors go to the caller's err_flag.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <string>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+#define PKV_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int cuda_fail(cudaError_t e, const char *where)
+{
+    g_last_error = std::string(where) + ": " + cudaGetErrorName(e) + ": " + cudaGetErrorString(e);
+    return PKV_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_attn_desc(const pkv_cache_desc &d, int32_t num_q_heads)
+{
+    if (d.block_size != 16) return PKV_ERR_UNSUPPORTED;
+    if (d.num_blocks <= 0 || d.num_kv_heads <= 0 || num_q_heads <= 0) return PKV_ERR_SHAPE;
+    if (d.head_dim != 64 && d.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_q_heads % d.num_kv_heads != 0) return PKV_ERR_SHAPE;
+    const int G = num_q_heads / d.num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+int check_copy_desc(const pkv_cache_desc &d)
+{
+    if (d.block_size != 16) return PKV_ERR_UNSUPPORTED;
+    if (d.num_blocks <= 0 || d.num_kv_heads <= 0 || d.head_dim <= 0) return PKV_ERR_SHAPE;
+    if (d.head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;  // rows move as 16-byte vectors
+    return PKV_OK;
+}
+
+// ---- TMA descriptors for the K and V pools -----------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The box of one (physical block, KV head) tile: 16 token rows x H elements, split into
+// 64-element (128-byte) rows so the 128-byte swizzle applies.  Half-major order
+// (dims h_lo, token, half, head, block) lands in shared memory as [half][token][64], which
+// makes the MMA fragment loads bank-conflict free; token-major order (h_lo, half, head,
+// token, block) is the fallback with monotone strides.
+CUresult encode_kv_map(CUtensorMap *map, const void *base, const pkv_cache_desc &d, int tok_major)
+{
+    const cuuint64_t H = (cuuint64_t)d.head_dim, K = (cuuint64_t)d.num_kv_heads;
+    const cuuint64_t halves = H / 64;
+    const cuuint64_t tok_stride = K * H * 2, half_stride = 128, head_stride = H * 2;
+    const cuuint64_t blk_stride = 16 * K * H * 2;
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5];
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    if (!tok_major) {
+        const cuuint64_t d5[5] = {64, 16, halves, K, (cuuint64_t)d.num_blocks};
+        const cuuint64_t s4[4] = {tok_stride, half_stride, head_stride, blk_stride};
+        const cuuint32_t b5[5] = {64, 16, (cuuint32_t)halves, 1, 1};
+        for (int i = 0; i < 5; ++i) dims[i] = d5[i], box[i] = b5[i];
+        for (int i = 0; i < 4; ++i) strides[i] = s4[i];
+    } else {
+        const cuuint64_t d5[5] = {64, halves, K, 16, (cuuint64_t)d.num_blocks};
+        const cuuint64_t s4[4] = {half_stride, head_stride, tok_stride, blk_stride};
+        const cuuint32_t b5[5] = {64, (cuuint32_t)halves, 1, 16, 1};
+        for (int i = 0; i < 5; ++i) dims[i] = d5[i], box[i] = b5[i];
+        for (int i = 0; i < 4; ++i) strides[i] = s4[i];
+    }
+    return encode_fn()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims,
+                       strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int g_tok_major = -1;  // layout the driver accepted first (-1: not yet known)
+std::mutex g_layout_mu;
+
+int make_kv_maps(CUtensorMap *tk, CUtensorMap *tv, const void *k, const void *v,
+                 const pkv_cache_desc &d, int *tok_major)
+{
+    if (!encode_fn()) {
+        g_last_error = "cuTensorMapEncodeTiled is unavailable from the driver";
+        return PKV_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_layout_mu);
+    const int first = g_tok_major < 0 ? 0 : g_tok_major;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        const int mode = attempt == 0 ? first : 1 - first;
+        CUresult rk = encode_kv_map(tk, k, d, mode);
+        CUresult rv = rk == CUDA_SUCCESS ? encode_kv_map(tv, v, d, mode) : rk;
+        if (rk == CUDA_SUCCESS && rv == CUDA_SUCCESS) {
+            g_tok_major = mode;
+            *tok_major = mode;
+            return PKV_OK;
+        }
+        if (g_tok_major >= 0) break;  // a layout worked before: this failure is the arguments'
+        g_last_error = "cuTensorMapEncodeTiled failed (CUresult " + std::to_string((int)rk) + "/" +
+                       std::to_string((int)rv) + ")";
+    }
+    return PKV_ERR_CUDA;
+}
+
+struct AttnArgs {
+    const pkv_bf16 *q, *k_cache, *v_cache;
+    const int32_t *block_tables;
+    int32_t max_nb;
+    const int32_t *context_lens;
+    int32_t B, N;
+    float scale;
+    pkv_cache_desc d;
+    int32_t *err_flag;
+};
+
+int validate_attn(const AttnArgs &a)
+{
+    if (!a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens) return PKV_ERR_NULL;
+    if (a.B < 0 || a.max_nb <= 0) return PKV_ERR_SHAPE;
+    int st = check_attn_desc(a.d, a.N);
+    if (st != PKV_OK) return st;
+    if (a.B > 65535 || a.d.num_kv_heads > 65535) return PKV_ERR_SHAPE;  // grid limits
+    if ((int64_t)a.max_nb * 16 > INT32_MAX) return PKV_ERR_SHAPE;
+    if (!aligned(a.k_cache, 16) || !aligned(a.v_cache, 16) || !aligned(a.q, 4)) return PKV_ERR_ALIGN;
+    return PKV_OK;
+}
+
+pkv::AttnParams params_of(const AttnArgs &a, int tok_major)
+{
+    pkv::AttnParams p{};
+    p.q = a.q;
+    p.block_tables = a.block_tables;
+    p.context_lens = a.context_lens;
+    p.max_nb = a.max_nb;
+    p.B = a.B;
+    p.N = a.N;
+    p.K = a.d.num_kv_heads;
+    p.G = a.N / a.d.num_kv_heads;
+    p.num_blocks = a.d.num_blocks;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.tok_major = tok_major;
+    p.err_flag = a.err_flag;
+    return p;
+}
+
+int64_t splitk_lse_offset(int32_t B, int32_t N, int32_t H, int32_t P)
+{
+    const int64_t out_bytes = (int64_t)B * N * P * H * 4;
+    return (out_bytes + 255) / 256 * 256;
+}
+
+int run_partitions(const AttnArgs &a, int32_t part_blocks, int32_t max_parts, float *part_out,
+                   float *part_lse, cudaStream_t s)
+{
+    if (part_blocks <= 0 || max_parts <= 0) return PKV_ERR_SHAPE;
+    if ((int64_t)max_parts * part_blocks < a.max_nb) return PKV_ERR_SHAPE;
+    if (!aligned(part_out, 16) || !aligned(part_lse, 4)) return PKV_ERR_ALIGN;
+    CUtensorMap tk, tv;
+    int tok_major = 0;
+    int st = make_kv_maps(&tk, &tv, a.k_cache, a.v_cache, a.d, &tok_major);
+    if (st != PKV_OK) return st;
+    pkv::AttnParams p = params_of(a, tok_major);
+    p.part_blocks = part_blocks;
+    p.max_parts = max_parts;
+    p.part_out = part_out;
+    p.part_lse = part_lse;
+    cudaError_t e = pkv::launch_attn(a.d.head_dim, true, tk, tv, p, s);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "attn partitions launch");
+}
+
+}  // namespace
+
+PKV_EXPORT uint64_t pkv_kv_bytes(int64_t layers, int64_t kv_heads, int64_t head_dim, int64_t tokens,
+                                 int64_t bytes_per_elem)
+{
+    return 2ull * (uint64_t)layers * (uint64_t)kv_heads * (uint64_t)head_dim * (uint64_t)tokens *
+           (uint64_t)bytes_per_elem;
+}
+
+PKV_EXPORT int pkv_slot_mapping(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                const int32_t *context_lens, int32_t num_seqs, int32_t num_blocks,
+                                int64_t *slot_mapping, int32_t *err_flag, pkv_stream_t stream)
+{
+    if (!block_tables || !context_lens || !slot_mapping) return PKV_ERR_NULL;
+    if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PKV_ERR_SHAPE;
+    if ((int64_t)max_blocks_per_seq * 16 > INT32_MAX) return PKV_ERR_SHAPE;
+    if (num_seqs == 0) return PKV_OK;
+    cudaError_t e = pkv::launch_slot_mapping(block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                             num_blocks, slot_mapping, err_flag, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "slot mapping launch");
+}
+
+PKV_EXPORT int pkv_append(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const int64_t *slot_mapping,
+                          int32_t num_tokens, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                          pkv_cache_desc cache, int32_t *err_flag, pkv_stream_t stream)
+{
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_NULL;
+    if (num_tokens < 0) return PKV_ERR_SHAPE;
+    int st = check_copy_desc(cache);
+    if (st != PKV_OK) return st;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PKV_ERR_ALIGN;
+    if (num_tokens == 0) return PKV_OK;
+    if ((int64_t)num_tokens * cache.num_kv_heads * cache.head_dim / 8 > ((int64_t)1 << 40))
+        return PKV_ERR_SHAPE;
+    cudaError_t e = pkv::launch_append(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache,
+                                       cache.num_blocks, cache.num_kv_heads, cache.head_dim, err_flag,
+                                       stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "append launch");
+}
+
+PKV_EXPORT int pkv_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                               const int32_t *block_tables, int32_t max_blocks_per_seq,
+                               const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                               float scale, pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
+                               int32_t *err_flag, pkv_stream_t stream)
+{
+    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+               num_q_heads, scale, cache, err_flag};
+    if (!out) return PKV_ERR_NULL;
+    int st = validate_attn(a);
+    if (st != PKV_OK) return st;
+    if (!aligned(out, 4) || !aligned(lse_out, 4)) return PKV_ERR_ALIGN;
+    if (num_seqs == 0) return PKV_OK;
+    CUtensorMap tk, tv;
+    int tok_major = 0;
+    st = make_kv_maps(&tk, &tv, k_cache, v_cache, cache, &tok_major);
+    if (st != PKV_OK) return st;
+    pkv::AttnParams p = params_of(a, tok_major);
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.lse_out = lse_out;
+    cudaError_t e = pkv::launch_attn(cache.head_dim, false, tk, tv, p, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "decode attention launch");
+}
+
+PKV_EXPORT size_t pkv_splitk_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                             int32_t max_partitions)
+{
+    if (num_seqs < 0 || num_q_heads < 0 || head_dim < 0 || max_partitions < 0) return 0;
+    return (size_t)(splitk_lse_offset(num_seqs, num_q_heads, head_dim, max_partitions) +
+                    (int64_t)num_seqs * num_q_heads * max_partitions * 4);
+}
+
+PKV_EXPORT int pkv_decode_attn_partitions(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                          const pkv_bf16 *v_cache, const int32_t *block_tables,
+                                          int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                          int32_t num_seqs, int32_t num_q_heads, float scale,
+                                          pkv_cache_desc cache, int32_t partition_blocks,
+                                          int32_t max_partitions, float *part_out, float *part_lse,
+                                          int32_t *err_flag, pkv_stream_t stream)
+{
+    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+               num_q_heads, scale, cache, err_flag};
+    if (!part_out || !part_lse) return PKV_ERR_NULL;
+    int st = validate_attn(a);
+    if (st != PKV_OK) return st;
+    if (num_seqs == 0) return PKV_OK;
+    return run_partitions(a, partition_blocks, max_partitions, part_out, part_lse, stream);
+}
+
+PKV_EXPORT int pkv_lse_merge(const float *part_out, const float *part_lse, const int32_t *context_lens,
+                             int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                             int32_t max_partitions, int32_t partition_blocks, pkv_bf16 *out,
+                             float *lse_out, pkv_stream_t stream)
+{
+    if (!part_out || !part_lse || !context_lens || !out) return PKV_ERR_NULL;
+    if (num_seqs < 0 || num_q_heads <= 0 || max_partitions <= 0 || partition_blocks <= 0)
+        return PKV_ERR_SHAPE;
+    if (head_dim <= 0 || head_dim > 1024) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || num_q_heads > INT32_MAX / 2) return PKV_ERR_SHAPE;
+    if (!aligned(part_out, 4) || !aligned(part_lse, 4) || !aligned(out, 2) || !aligned(lse_out, 4))
+        return PKV_ERR_ALIGN;
+    if (num_seqs == 0) return PKV_OK;
+    cudaError_t e = pkv::launch_lse_merge(part_out, part_lse, context_lens, num_seqs, num_q_heads,
+                                          head_dim, max_partitions, partition_blocks, out, lse_out,
+                                          stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "lse merge launch");
+}
+
+PKV_EXPORT int pkv_decode_attn_splitk(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                      const pkv_bf16 *v_cache, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                      int32_t num_seqs, int32_t num_q_heads, float scale,
+                                      pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
+                                      int32_t partition_blocks, int32_t max_partitions,
+                                      void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                                      pkv_stream_t stream)
+{
+    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+               num_q_heads, scale, cache, err_flag};
+    if (!out) return PKV_ERR_NULL;
+    int st = validate_attn(a);
+    if (st != PKV_OK) return st;
+    if (partition_blocks <= 0 || max_partitions <= 0) return PKV_ERR_SHAPE;
+    if (!workspace) return PKV_ERR_WORKSPACE;
+    if (workspace_bytes < pkv_splitk_workspace_bytes(num_seqs, num_q_heads, cache.head_dim,
+                                                     max_partitions))
+        return PKV_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
+    if (!aligned(out, 4) || !aligned(lse_out, 4)) return PKV_ERR_ALIGN;
+    if (num_seqs == 0) return PKV_OK;
+    float *part_out = static_cast<float *>(workspace);
+    float *part_lse = reinterpret_cast<float *>(
+        static_cast<char *>(workspace) +
+        splitk_lse_offset(num_seqs, num_q_heads, cache.head_dim, max_partitions));
+    st = run_partitions(a, partition_blocks, max_partitions, part_out, part_lse, stream);
+    if (st != PKV_OK) return st;
+    return pkv_lse_merge(part_out, part_lse, context_lens, num_seqs, num_q_heads, cache.head_dim,
+                         max_partitions, partition_blocks, out, lse_out, stream);
+}
+
+PKV_EXPORT int pkv_gather(const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *context_lens, const int64_t *cu_seqlens, int32_t num_seqs,
+                          pkv_bf16 *k_out, pkv_bf16 *v_out, int64_t out_rows, pkv_cache_desc cache,
+                          int32_t *err_flag, pkv_stream_t stream)
+{
+    if (!k_cache || !v_cache || !block_tables || !context_lens || !cu_seqlens || !k_out || !v_out)
+        return PKV_ERR_NULL;
+    if (num_seqs < 0 || max_blocks_per_seq <= 0 || out_rows < 0) return PKV_ERR_SHAPE;
+    int st = check_copy_desc(cache);
+    if (st != PKV_OK) return st;
+    if (num_seqs > 65535) return PKV_ERR_SHAPE;
+    if ((int64_t)max_blocks_per_seq * 16 > INT32_MAX) return PKV_ERR_SHAPE;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_out, 16) || !aligned(v_out, 16))
+        return PKV_ERR_ALIGN;
+    if (num_seqs == 0) return PKV_OK;
+    cudaError_t e = pkv::launch_gather(k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                       context_lens, cu_seqlens, num_seqs, cache.num_blocks,
+                                       cache.num_kv_heads, cache.head_dim, k_out, v_out, out_rows,
+                                       err_flag, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "gather launch");
+}
+
+PKV_EXPORT int pkv_read_err_flag(const int32_t *err_flag, int32_t *host_value, pkv_stream_t stream)
+{
+    if (!err_flag || !host_value) return PKV_ERR_NULL;
+    cudaError_t e = cudaMemcpyAsync(host_value, err_flag, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                    stream);
+    if (e != cudaSuccess) return cuda_fail(e, "err_flag copy");
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "err_flag sync");
+    return *host_value != 0 ? PKV_ERR_RANGE : PKV_OK;
+}
+
+PKV_EXPORT const char *pkv_status_string(int status)
+{
+    switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_NULL: return "a required pointer is NULL";
+    case PKV_ERR_SHAPE: return "inconsistent or out-of-range sizes";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape (H in {64,128}, G in {1,2,4,8}, block_size 16)";
+    case PKV_ERR_RANGE: return "device-detected out-of-range value (see err_flag bits)";
+    case PKV_ERR_CUDA: return "CUDA error (see pkv_last_error)";
+    case PKV_ERR_ALIGN: return "pointer misaligned for the layout";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+PKV_EXPORT const char *pkv_last_error(void) { return g_last_error.c_str(); }

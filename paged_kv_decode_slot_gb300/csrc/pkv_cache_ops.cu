@@ -1,0 +1,135 @@
+// pkv_cache_ops.cu - byte-moving kernels of the paged KV cache: slot mapping, append of the
+// new token's K/V into its slot, and the block-table gather to a contiguous copy.
+//
+// The cache is [num_blocks][16][K][H] bf16, so all K heads of one token form one contiguous
+// row of K*H elements and the 16 rows of a block are contiguous too.  Both copies therefore
+// move whole 16-byte vectors with coalesced loads and stores.
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// slot[b] = table[b][p / 16] * 16 + p % 16 for the newest token p = ctx_b - 1
+// ("Optimización de la inferencia", "Página Atención": the page table maps logical positions
+// to physical pages).
+__global__ void slot_mapping_kernel(const int32_t *__restrict__ block_tables, int max_nb,
+                                    const int32_t *__restrict__ context_lens, int B, int num_blocks,
+                                    int64_t *__restrict__ slots, int32_t *err_flag)
+{
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int ctx = context_lens[b];
+    int64_t slot = -1;
+    if (ctx > max_nb * kBlockSize) {
+        set_flag(err_flag, PKV_FLAG_CTX_RANGE);
+    } else if (ctx > 0) {
+        const int pos = ctx - 1;
+        const int blk = block_tables[(size_t)b * max_nb + pos / kBlockSize];
+        if (blk < 0 || blk >= num_blocks)
+            set_flag(err_flag, PKV_FLAG_BLOCK_RANGE);
+        else
+            slot = (int64_t)blk * kBlockSize + pos % kBlockSize;
+    }
+    slots[b] = slot;
+}
+
+// One thread per 16-byte vector of one token's [K][H] row: k_cache row `slot` <- k_new row i.
+__global__ void append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                              const int64_t *__restrict__ slots, int T, uint4 *__restrict__ k_cache,
+                              uint4 *__restrict__ v_cache, int64_t capacity, int vec_per_row,
+                              int32_t *err_flag)
+{
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)T * vec_per_row) return;
+    const int i = (int)(idx / vec_per_row);
+    const int r = (int)(idx - (int64_t)i * vec_per_row);
+    const int64_t slot = slots[i];
+    if (slot < 0) return;  // skipped token
+    if (slot >= capacity) {
+        if (r == 0) set_flag(err_flag, PKV_FLAG_SLOT_RANGE);
+        return;
+    }
+    const int64_t src = (int64_t)i * vec_per_row + r;
+    const int64_t dst = slot * vec_per_row + r;
+    k_cache[dst] = __ldg(k_new + src);
+    v_cache[dst] = __ldg(v_new + src);
+}
+
+// One CTA per (logical block j, sequence b): its tokens are one contiguous run of rows in
+// the pool and one contiguous run in the output.
+__global__ void gather_kernel(const uint4 *__restrict__ k_cache, const uint4 *__restrict__ v_cache,
+                              const int32_t *__restrict__ block_tables, int max_nb,
+                              const int32_t *__restrict__ context_lens,
+                              const int64_t *__restrict__ cu_seqlens, int num_blocks, int vec_per_row,
+                              uint4 *__restrict__ k_out, uint4 *__restrict__ v_out, int64_t out_rows,
+                              int32_t *err_flag)
+{
+    const int j = blockIdx.x, b = blockIdx.y;
+    const int ctx = context_lens[b];
+    if (ctx > max_nb * kBlockSize) {
+        if (j == 0 && threadIdx.x == 0) set_flag(err_flag, PKV_FLAG_CTX_RANGE);
+        return;
+    }
+    const int t0 = j * kBlockSize;
+    if (t0 >= ctx) return;
+    const int ntok = min(kBlockSize, ctx - t0);
+    const int blk = block_tables[(size_t)b * max_nb + j];
+    if (blk < 0 || blk >= num_blocks) {
+        if (threadIdx.x == 0) set_flag(err_flag, PKV_FLAG_BLOCK_RANGE);
+        return;
+    }
+    const int64_t row0 = cu_seqlens[b] + t0;
+    if (row0 < 0 || row0 + ntok > out_rows) {
+        if (threadIdx.x == 0) set_flag(err_flag, PKV_FLAG_OUT_RANGE);
+        return;
+    }
+    const int64_t n = (int64_t)ntok * vec_per_row;
+    const uint4 *ks = k_cache + (int64_t)blk * kBlockSize * vec_per_row;
+    const uint4 *vs = v_cache + (int64_t)blk * kBlockSize * vec_per_row;
+    uint4 *kd = k_out + row0 * vec_per_row;
+    uint4 *vd = v_out + row0 * vec_per_row;
+    for (int64_t x = threadIdx.x; x < n; x += blockDim.x) {
+        kd[x] = __ldg(ks + x);
+        vd[x] = __ldg(vs + x);
+    }
+}
+
+cudaError_t launch_slot_mapping(const int32_t *block_tables, int max_nb, const int32_t *context_lens,
+                                int B, int num_blocks, int64_t *slots, int32_t *err_flag,
+                                cudaStream_t stream)
+{
+    const int threads = 128;
+    slot_mapping_kernel<<<(B + threads - 1) / threads, threads, 0, stream>>>(
+        block_tables, max_nb, context_lens, B, num_blocks, slots, err_flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, const int64_t *slots, int T,
+                          uint16_t *k_cache, uint16_t *v_cache, int num_blocks, int K, int H,
+                          int32_t *err_flag, cudaStream_t stream)
+{
+    const int vec_per_row = K * H / 8;
+    const int64_t total = (int64_t)T * vec_per_row;
+    const int threads = 256;
+    const int64_t blocks = (total + threads - 1) / threads;
+    append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+        reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), slots, T,
+        reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache),
+        (int64_t)num_blocks * kBlockSize, vec_per_row, err_flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const uint16_t *k_cache, const uint16_t *v_cache,
+                          const int32_t *block_tables, int max_nb, const int32_t *context_lens,
+                          const int64_t *cu_seqlens, int B, int num_blocks, int K, int H,
+                          uint16_t *k_out, uint16_t *v_out, int64_t out_rows, int32_t *err_flag,
+                          cudaStream_t stream)
+{
+    gather_kernel<<<dim3(max_nb, B), 256, 0, stream>>>(
+        reinterpret_cast<const uint4 *>(k_cache), reinterpret_cast<const uint4 *>(v_cache),
+        block_tables, max_nb, context_lens, cu_seqlens, num_blocks, K * H / 8,
+        reinterpret_cast<uint4 *>(k_out), reinterpret_cast<uint4 *>(v_out), out_rows, err_flag);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,54 @@
+// pkv_internal.h - kernel parameter blocks and launchers shared by the libpagedkv
+// translation units (not part of the public C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+struct AttnParams {
+    const uint16_t *q;             // [B][N][H] bf16
+    const int32_t *block_tables;   // [B][max_nb]
+    const int32_t *context_lens;   // [B]
+    int32_t max_nb;
+    int32_t B, N, K, G;
+    int32_t num_blocks;
+    float scale_log2;              // scale * log2(e)
+    int32_t tok_major;             // smem tile layout chosen by the tensor map (see pkv_attn.cu)
+    int32_t part_blocks;           // split-KV: blocks per partition
+    int32_t max_parts;             // split-KV: partition stride of part_out / part_lse
+    __nv_bfloat16 *out;            // single pass: [B][N][H]
+    float *lse_out;                // single pass: [B][N] (nullable)
+    float *part_out;               // split-KV: [B][N][max_parts][H]
+    float *part_lse;               // split-KV: [B][N][max_parts]
+    int32_t *err_flag;             // nullable
+};
+
+template <int H>
+int attn_smem_bytes();
+
+cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensorMap &tv,
+                        const AttnParams &p, cudaStream_t stream);
+
+cudaError_t launch_lse_merge(const float *part_out, const float *part_lse,
+                             const int32_t *context_lens, int B, int N, int H, int max_parts,
+                             int part_blocks, uint16_t *out, float *lse_out, cudaStream_t stream);
+
+cudaError_t launch_slot_mapping(const int32_t *block_tables, int max_nb, const int32_t *context_lens,
+                                int B, int num_blocks, int64_t *slots, int32_t *err_flag,
+                                cudaStream_t stream);
+
+cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, const int64_t *slots, int T,
+                          uint16_t *k_cache, uint16_t *v_cache, int num_blocks, int K, int H,
+                          int32_t *err_flag, cudaStream_t stream);
+
+cudaError_t launch_gather(const uint16_t *k_cache, const uint16_t *v_cache,
+                          const int32_t *block_tables, int max_nb, const int32_t *context_lens,
+                          const int64_t *cu_seqlens, int B, int num_blocks, int K, int H,
+                          uint16_t *k_out, uint16_t *v_out, int64_t out_rows, int32_t *err_flag,
+                          cudaStream_t stream);
+
+}  // namespace pkv

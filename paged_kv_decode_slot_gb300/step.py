@@ -1,0 +1,101 @@
+"""One decode step through libpagedkv: slot mapping, append into the slot, then attention.
+
+``DecodeStep`` owns the per-step device buffers (slot mapping, output, lse, split-KV
+workspace) and issues, on one stream, the library calls that make a decode step:
+
+1. ``pkv_slot_mapping``  -- the new token's slot from its block table and context length;
+2. ``pkv_append``         -- its K/V written into that slot of the paged pools;
+3. ``pkv_decode_attn`` (one CTA per sequence and KV head) or ``pkv_decode_attn_splitk``
+   (partitions of the block table, then the log-sum-exp merge), as ``plan_attention`` picks.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import binding as B
+
+
+@dataclass
+class AttentionPlan:
+    split: bool
+    partition_blocks: int
+    max_partitions: int
+
+    def describe(self) -> str:
+        if not self.split:
+            return "single-pass"
+        return f"split-KV, {self.partition_blocks}-block partitions (max {self.max_partitions})"
+
+
+def plan_attention(num_seqs: int, num_kv_heads: int, max_blocks_per_seq: int, num_sms: int,
+                   partition_blocks: int | None = None) -> AttentionPlan:
+    """Single pass when (sequence, KV head) units fill the GPU, else split-KV.
+
+    The single-pass kernel runs one CTA per unit and up to 3 CTAs per SM, so fewer than
+    ~2 units per SM leaves bandwidth idle; the split path multiplies the units by the
+    number of partitions.  An explicit ``partition_blocks`` forces the split path.
+    """
+    units = num_seqs * num_kv_heads
+    if partition_blocks is None:
+        if units >= 2 * num_sms:
+            return AttentionPlan(False, max_blocks_per_seq, 1)
+        want_parts = -(-2 * num_sms // max(units, 1))
+        partition_blocks = max(4, -(-max_blocks_per_seq // want_parts))
+    max_parts = B.max_partitions_for(max_blocks_per_seq, partition_blocks)
+    return AttentionPlan(True, partition_blocks, max_parts)
+
+
+class DecodeStep:
+    """Device-resident state of one decode step over a paged cache (all torch CUDA tensors).
+
+    q [B, N, H] bf16; k_new/v_new [B, K, H] bf16; k_cache/v_cache [nb, 16, K, H] bf16;
+    block_tables [B, max_blocks] int32; context_lens [B] int32 (including the new token).
+    """
+
+    def __init__(self, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
+                 plan: AttentionPlan | None = None, err_flag=None):
+        self.q, self.k_new, self.v_new = q, k_new, v_new
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.block_tables, self.context_lens = block_tables, context_lens
+        self.scale = float(scale)
+        dev = q.device
+        nseq = q.shape[0]
+        self.num_blocks = k_cache.shape[0]
+        if plan is None:
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            plan = plan_attention(nseq, k_cache.shape[2], block_tables.shape[1], sms)
+        self.plan = plan
+        self.slot_mapping = torch.empty(nseq, dtype=torch.int64, device=dev)
+        self.out = torch.empty_like(q)
+        self.lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev)
+        self.err_flag = err_flag
+        self.workspace = None
+        if plan.split:
+            nbytes = B.pkv_splitk_workspace_bytes(nseq, q.shape[1], q.shape[2], plan.max_partitions)
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def slot_and_append(self, stream=None) -> None:
+        B.check(B.pkv_slot_mapping(self.block_tables, self.context_lens, self.num_blocks,
+                                   self.slot_mapping, self.err_flag, stream))
+        B.check(B.pkv_append(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
+                             self.err_flag, stream))
+
+    def attention(self, stream=None) -> None:
+        if self.plan.split:
+            B.check(B.pkv_decode_attn_splitk(self.q, self.k_cache, self.v_cache, self.block_tables,
+                                             self.context_lens, self.scale, self.out,
+                                             self.plan.partition_blocks, self.plan.max_partitions,
+                                             self.workspace, self.lse, self.err_flag, stream))
+        else:
+            B.check(B.pkv_decode_attn(self.q, self.k_cache, self.v_cache, self.block_tables,
+                                      self.context_lens, self.scale, self.out, self.lse,
+                                      self.err_flag, stream))
+
+    def run(self, stream=None) -> None:
+        self.slot_and_append(stream)
+        self.attention(stream)
+
+    def launches_per_step(self) -> int:
+        return 2 + (2 if self.plan.split else 1)

@@ -1,0 +1,145 @@
+"""The C-ABI library on the CPU: it loads, exports every declared symbol, and validates
+arguments on the host before any CUDA call (no GPU is touched by these tests)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import pins
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_decode_slot_gb300.build import build_library
+    path = build_library()
+    return ctypes.CDLL(path), path
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("pkv_append", "pkv_decode_attn", "pkv_decode_attn_splitk", "pkv_lse_merge",
+                 "pkv_gather", "pkv_slot_mapping", "pkv_kv_bytes", "pkv_splitk_workspace_bytes",
+                 "pkv_decode_attn_partitions", "pkv_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    cdll, path = lib
+    for name in declared_functions():
+        assert hasattr(cdll, name), f"{name} declared in pkv.h but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True)
+    if out.returncode == 0:
+        exported = set(re.findall(r"\s[TW]\s+(pkv_\w+)$", out.stdout, flags=re.M))
+        assert exported == set(declared_functions()), exported ^ set(declared_functions())
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+P = ctypes.c_void_p
+FAKE = 0x10000          # an aligned stand-in device address; host validation never dereferences it
+
+
+def _attn(cdll, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, ctx=FAKE, out=FAKE, B=4, N=8, max_nb=4,
+          desc=(64, 16, 2, 64), lse=None):
+    f = cdll.pkv_decode_attn
+    f.argtypes = [P, P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, P, P,
+                  Desc, P, P]
+    return f(q, k, v, bt, max_nb, ctx, B, N, 0.125, out, lse, Desc(*desc), None, None)
+
+
+def test_host_validation_of_decode_attn(lib):
+    cdll, _ = lib
+    assert _attn(cdll, q=None) == -1
+    assert _attn(cdll, out=None) == -1
+    assert _attn(cdll, desc=(64, 16, 2, 96)) == -3        # head_dim
+    assert _attn(cdll, desc=(64, 8, 2, 64)) == -3         # block size
+    assert _attn(cdll, N=6, desc=(64, 16, 4, 64)) == -2    # N % K
+    assert _attn(cdll, N=32, desc=(64, 16, 2, 64)) == -3   # G = 16
+    assert _attn(cdll, k=FAKE + 8) == -6                  # TMA needs 16-byte alignment
+    assert _attn(cdll, B=-1) == -2
+    assert _attn(cdll, max_nb=0) == -2
+    assert _attn(cdll, B=0) == 0                          # nothing to do, nothing launched
+
+
+def test_host_validation_of_splitk_and_merge(lib):
+    cdll, _ = lib
+    f = cdll.pkv_decode_attn_splitk
+    f.argtypes = [P, P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, P, P,
+                  Desc, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_size_t, P, P]
+    cdll.pkv_splitk_workspace_bytes.restype = ctypes.c_size_t
+    need = cdll.pkv_splitk_workspace_bytes(4, 8, 64, 2)
+    assert need == 256 * ((4 * 8 * 2 * 64 * 4 + 255) // 256) + 4 * 8 * 2 * 4
+    args = lambda ws, wsb, pb=2, P_=2, B=4: (FAKE, FAKE, FAKE, FAKE, 4, FAKE, B, 8, 0.125, FAKE, None,
+                                            Desc(64, 16, 2, 64), pb, P_, ws, wsb, None, None)
+    assert f(*args(None, need)) == -7
+    assert f(*args(FAKE, need - 1)) == -7
+    assert f(*args(FAKE + 16, need)) == -6                # workspace alignment 256
+    assert f(*args(FAKE, need, pb=0)) == -2
+    assert f(*args(FAKE, need, B=0)) == 0
+    g = cdll.pkv_lse_merge
+    g.argtypes = [P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_int32, P, P, P]
+    assert g(None, FAKE, FAKE, 4, 8, 64, 2, 2, FAKE, None, None) == -1
+    assert g(FAKE, FAKE, FAKE, 4, 8, 64, 0, 2, FAKE, None, None) == -2
+    assert g(FAKE, FAKE, FAKE, 0, 8, 64, 2, 2, FAKE, None, None) == 0
+
+
+def test_host_validation_of_cache_ops(lib):
+    cdll, _ = lib
+    a = cdll.pkv_append
+    a.argtypes = [P, P, P, ctypes.c_int32, P, P, Desc, P, P]
+    assert a(FAKE, FAKE, None, 4, FAKE, FAKE, Desc(64, 16, 2, 64), None, None) == -1
+    assert a(FAKE, FAKE, FAKE, 4, FAKE + 2, FAKE, Desc(64, 16, 2, 64), None, None) == -6
+    assert a(FAKE, FAKE, FAKE, 4, FAKE, FAKE, Desc(64, 16, 2, 60), None, None) == -3
+    assert a(FAKE, FAKE, FAKE, 0, FAKE, FAKE, Desc(64, 16, 2, 64), None, None) == 0
+    s = cdll.pkv_slot_mapping
+    s.argtypes = [P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, P, P, P]
+    assert s(FAKE, 4, FAKE, 3, 64, None, None, None) == -1
+    assert s(FAKE, 0, FAKE, 3, 64, FAKE, None, None) == -2
+    assert s(FAKE, 4, FAKE, 0, 64, FAKE, None, None) == 0
+    gth = cdll.pkv_gather
+    gth.argtypes = [P, P, P, ctypes.c_int32, P, P, ctypes.c_int32, P, P, ctypes.c_int64, Desc, P, P]
+    assert gth(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, FAKE, FAKE, -1, Desc(64, 16, 2, 64), None, None) == -2
+    assert gth(FAKE, FAKE, FAKE, 4, FAKE, None, 2, FAKE, FAKE, 9, Desc(64, 16, 2, 64), None, None) == -1
+
+
+def test_status_strings(lib):
+    cdll, _ = lib
+    cdll.pkv_status_string.restype = ctypes.c_char_p
+    for st in range(-7, 1):
+        assert cdll.pkv_status_string(st) and cdll.pkv_status_string(st) != b"unknown status"
+
+
+def test_library_kv_bytes_matches_pages(lib):
+    cdll, _ = lib
+    f = cdll.pkv_kv_bytes
+    f.argtypes = [ctypes.c_int64] * 5
+    f.restype = ctypes.c_uint64
+    for (L, K, H, S, nbytes), expected, cite in pins.read_kv_bytes_golden():
+        assert f(L, K, H, S, nbytes) == expected, cite
+
+
+def test_attention_plan():
+    from paged_kv_decode_slot_gb300.step import plan_attention
+    assert not plan_attention(64, 8, 512, 152).split                # 512 units fill 152 SMs
+    p = plan_attention(1, 40, 64, 152)                              # 40 units: split
+    assert p.split and p.max_partitions * p.partition_blocks >= 64
+    assert 40 * p.max_partitions >= 2 * 152
+    p = plan_attention(2, 8, 8192, 152, partition_blocks=256)
+    assert p.split and p.partition_blocks == 256 and p.max_partitions == 32
