@@ -1,0 +1,404 @@
+"""Benchmark of one decode step of paged KV-cache attention on GB300.
+
+A step is the whole hot path over one batch: slot mapping of each sequence's new token,
+append of its K/V into the paged pools, then decode attention (single pass, or split-KV
+partitions plus the log-sum-exp merge, as the attention plan picks).  Inputs are seeded
+synthetic workloads resident in HBM; between timed steps L2 is flushed by writing a buffer
+twice its size (outside the timed events).
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the float64 CPU oracle on the
+host cores instead (bounded samples of the same workload).  Multi-GPU runs are independent
+replicas (one per rank, no collective on the data path; weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attention KV GB/s and % of GB300 HBM roofline; µs per decode step"
+NORTH_STAR_TBS = 8.0          # the HBM roofline the method's target is quoted against (TB/s)
+FALLBACK_HBM_GBS = 6800.0     # copy bandwidth of an earlier GB300 measurement
+DEFAULT_CONFIG = "l3_8b_b64"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+ATTN_SOURCES = [os.path.join(ROOT, "paged_kv_decode_slot_gb300", "csrc", f)
+                for f in ("pkv_attn.cu", "pkv_device.cuh", "pkv_internal.h")]
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def attn_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in ATTN_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str):
+    """dram bytes per attention launch from an ncu capture of the current kernel source, else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    want = attn_source_hash()
+    with open(TRAFFIC_FILE, encoding="utf-8") as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == want and parts[1] == config:
+                return int(parts[2])
+    return None
+
+
+def step_bytes(w) -> dict:
+    """Algorithmic bytes of one step (what the method must move, padding not counted)."""
+    tables = int(sum(-(-int(c) // 16) for c in w.context_lens)) * 4
+    attn = w.kv_bytes() + w.qo_bytes()
+    meta = w.B * 4 + tables + w.B * 8 * 2          # context lens, table entries, slots (write+read)
+    return {"attn": attn, "attn_unique": w.unique_kv_bytes() + w.qo_bytes(),
+            "append": w.append_bytes(), "meta": meta,
+            "step": attn + w.append_bytes() + meta}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------------
+def oracle_step_seconds(orc, w, rows, kc, vc, threads):
+    """Time the oracle's decode step (slot mapping, append, attention) on sequences `rows`."""
+    sub_t = w.block_tables[rows]
+    sub_c = w.context_lens[rows]
+    t0 = time.perf_counter()
+    slots = orc.slot_mapping(sub_t, sub_c)
+    orc.append(w.k_new[rows], w.v_new[rows], slots, kc, vc)
+    orc.decode(w.q[rows], kc, vc, sub_t, sub_c, w.scale, threads=threads)
+    return time.perf_counter() - t0
+
+
+def pick_sample(w, budget_s, orc, kc, vc, threads):
+    """Sequences (a contiguous run from the start, wrapping) sized to about budget_s of oracle work."""
+    probe = [0]
+    t = oracle_step_seconds(orc, w, probe, kc, vc, threads)
+    per_token = max(t, 1e-4) / max(int(w.context_lens[0]), 1)
+    rows, tok = [], 0
+    budget_tok = budget_s / per_token
+    for b in range(w.B):
+        if rows and tok + int(w.context_lens[b]) > budget_tok:
+            break
+        rows.append(b)
+        tok += int(w.context_lens[b])
+    return rows
+
+
+def sample_bytes(w, rows):
+    tok = int(w.context_lens[rows].astype(np.int64).sum())
+    n = len(rows)
+    attn = tok * w.K * w.H * 4 + 2 * n * w.N * w.H * 2
+    app = 2 * 2 * n * w.K * w.H * 2
+    meta = n * 4 + int(sum(-(-int(w.context_lens[b]) // 16) for b in rows)) * 4 + n * 16
+    return attn + app + meta
+
+
+def run_cpu_baseline(w, budget_s=12.0):
+    import oracle
+    orc = oracle.default()
+    threads = os.cpu_count() or 1
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    rows = pick_sample(w, budget_s, orc, kc, vc, threads)
+    secs = oracle_step_seconds(orc, w, rows, kc, vc, threads)
+    gbs = sample_bytes(w, rows) / secs / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} of {w.B} sequences ({int(w.context_lens[rows].sum())} tokens) of "
+                      f"{w.name}, one decode step (slot mapping, append, float64 attention), "
+                      f"{secs:.2f} s"}
+
+
+def run_reference(args):
+    """The oracle on the host cores, on bounded samples of the workload."""
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_decode_slot_gb300 import inputs as gen
+    w = gen.make_config(args.config)
+    orc = oracle.default()
+    threads = os.cpu_count() or 1
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    per_step = max(1.0, min(10.0, 150.0 / max(args.steps + args.warmup, 1)))
+    rows = pick_sample(w, per_step, orc, kc, vc, threads)
+    for _ in range(args.warmup):
+        oracle_step_seconds(orc, w, rows, kc, vc, threads)
+    times = [oracle_step_seconds(orc, w, rows, kc, vc, threads) for _ in range(args.steps)]
+    nbytes = sample_bytes(w, rows)
+    mean_s = sum(times) / len(times)
+    gbs = nbytes / mean_s / 1e9
+    sample = (f"{len(rows)} of {w.B} sequences ({int(w.context_lens[rows].sum())} tokens) of {w.name} "
+              f"per step")
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": config_dict(w, "none (host run)"),
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w, flush: str, plan=None) -> dict:
+    d = {"workload": w.name, "batch": w.B, "q_heads": w.N, "kv_heads": w.K, "head_dim": w.H,
+         "block_size": 16, "total_context_tokens": w.total_tokens,
+         "max_context": int(w.context_lens.max()), "pool_blocks": w.num_blocks,
+         "l2": flush, "parallelism": "replicas"}
+    if plan is not None:
+        d["attention"] = plan.describe()
+    return d
+
+
+# ----------------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    ws, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    from paged_kv_decode_slot_gb300.build import build_library
+    build_library()
+    import paged_kv_decode_slot_gb300 as pkv
+    from paged_kv_decode_slot_gb300 import inputs as gen
+    from paged_kv_decode_slot_gb300.step import DecodeStep, plan_attention
+
+    w = gen.make_config(args.config)
+    dev = torch.device("cuda", local)
+
+    def d16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def d32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    q, kn, vn = d16(w.q), d16(w.k_new), d16(w.v_new)
+    kc, vc = d16(w.k_cache), d16(w.v_cache)
+    bt, cl = d32(w.block_tables), d32(w.context_lens)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    pb = args.partition_blocks or (w.partition_blocks if args.config == "long_splitk" else None)
+    plan = plan_attention(w.B, w.K, w.max_blocks, sms, partition_blocks=pb)
+    if args.single:
+        from paged_kv_decode_slot_gb300.step import AttentionPlan
+        plan = AttentionPlan(False, w.max_blocks, 1)
+    step = DecodeStep(q, kn, vn, kc, vc, bt, cl, w.scale, plan=plan, err_flag=err)
+    stream = torch.cuda.Stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    nbytes = step_bytes(w)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.add_(1.0)
+            step.run(stream)
+    torch.cuda.synchronize(dev)
+    st, flag = pkv.pkv_read_err_flag(err, stream)
+    if st != pkv.PKV_OK:
+        raise RuntimeError(f"device error flag {flag:#x} during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.add_(1.0)                      # evict L2 (outside the events)
+                ev[i][0].record(stream)
+                step.slot_and_append(stream)
+                ev[i][1].record(stream)
+                step.attention(stream)
+                ev[i][2].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    if dist is not None:
+        dist.barrier()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    mean_step = sum(step_ms) / len(step_ms)
+    mean_attn = sum(attn_ms) / len(attn_ms)
+    if dist is not None:
+        t = torch.tensor([mean_step, mean_attn], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_step, mean_attn = t.tolist()
+
+    st, flag = pkv.pkv_read_err_flag(err, stream)
+    if st != pkv.PKV_OK:
+        raise RuntimeError(f"device error flag {flag:#x} during the timed steps")
+
+    # -- end to end through the public API with host buffers (pinned), copies inside the timing
+    hq = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hkn = torch.from_numpy(w.k_new.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hvn = torch.from_numpy(w.v_new.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hbt = torch.from_numpy(np.ascontiguousarray(w.block_tables)).pin_memory()
+    hcl = torch.from_numpy(np.ascontiguousarray(w.context_lens)).pin_memory()
+    hout = torch.empty(tuple(q.shape), dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hkn, hvn, hbt, hcl))
+    d2h = hout.numel() * hout.element_size()
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            flush.add_(1.0)
+            k = i - args.warmup
+            if k >= 0:
+                e2e_ev[k][0].record(stream)
+            q.copy_(hq, non_blocking=True)
+            kn.copy_(hkn, non_blocking=True)
+            vn.copy_(hvn, non_blocking=True)
+            bt.copy_(hbt, non_blocking=True)
+            cl.copy_(hcl, non_blocking=True)
+            step.run(stream)
+            hout.copy_(step.out, non_blocking=True)
+            if k >= 0:
+                e2e_ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / args.steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = t.item()
+
+    peak, peak_kind = load_peak()
+    attn_bytes = nbytes["attn_unique"] if w.unique_tokens is not None else nbytes["attn"]
+    achieved = attn_bytes / (mean_attn * 1e-3) / 1e9
+    value = ws * nbytes["step"] / (mean_step * 1e-3) / 1e9
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "config": config_dict(w, "flushed between steps (write of 2x L2 outside the timed events)", plan),
+        "us_per_step": mean_step * 1e3,
+        "attn_us": mean_attn * 1e3,
+        "attn_calls_per_s": 1e3 / mean_attn,
+        "kv_gbs": w.kv_bytes() / (mean_attn * 1e-3) / 1e9,
+        "frac_of_8tbs": achieved / (NORTH_STAR_TBS * 1e3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                     "kernel": "attn_kernel" + (" + lse_merge_kernel" if plan.split else ""),
+                     "bytes_per_launch": attn_bytes,
+                     "traffic": recorded_traffic(args.config)},
+        "e2e": {"value": ws * nbytes["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * step.launches_per_step(),
+        "clocks": clocks,
+        "wall_s_timed_region": t_wall,
+        "step_bytes": nbytes["step"],
+    }
+    if w.unique_tokens is not None:
+        line["kv_gbs_logical"] = w.kv_bytes() / (mean_attn * 1e-3) / 1e9
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = run_cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--partition-blocks", type=int, default=None)
+    ap.add_argument("--single", action="store_true", help="force the single-pass kernel")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -3,13 +3,17 @@
 The compute path is the C-ABI library ``libpagedkv.so`` (hand-written sm_103a CUDA, declared
 in ``include/pkv.h``); ``binding`` exposes its entry points under the same names with torch
 tensors as arguments (PyTorch supplies device memory and streams only).  ``inputs`` draws
-seeded synthetic workloads.
+seeded synthetic workloads; ``step`` runs a whole decode step.
+
+The binding is loaded on first use of one of its names, so that ``build`` can be imported
+before the library exists; using any entry point without the built library raises
+ImportError (there is no fallback path).
 """
-from .binding import (BLOCK_SIZE, PKV_ERR_ALIGN, PKV_ERR_CUDA, PKV_ERR_NULL, PKV_ERR_RANGE,  # noqa: F401
-                      PKV_ERR_SHAPE, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_FLAG_BLOCK_RANGE,
-                      PKV_FLAG_CTX_RANGE, PKV_FLAG_OUT_RANGE, PKV_FLAG_SLOT_RANGE, PKV_FLAG_TIMEOUT,
-                      PKV_OK, CacheDesc, PkvError, cache_desc, check, library, max_partitions_for,
-                      pkv_append, pkv_decode_attn, pkv_decode_attn_partitions,
-                      pkv_decode_attn_splitk, pkv_gather, pkv_kv_bytes, pkv_last_error,
-                      pkv_lse_merge, pkv_read_err_flag, pkv_slot_mapping,
-                      pkv_splitk_workspace_bytes, pkv_status_string)
+
+
+def __getattr__(name):
+    if name.startswith(("pkv_", "PKV_")) or name in ("BLOCK_SIZE", "CacheDesc", "PkvError", "cache_desc",
+                                                    "check", "library", "max_partitions_for"):
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(f"module {__name__!r} has no attribute {name!r}")

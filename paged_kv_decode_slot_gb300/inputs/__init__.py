@@ -278,7 +278,7 @@ def make_prefix_workload(name: str, seed: int, N: int, K: int, H: int, B: int, p
 # Lecture 10's worked example, and Llama-3-70B's head shape (64 / 8).
 # --------------------------------------------------------------------------------------
 
-CONFIG_NAMES = ("tiny", "l3_8b_b64", "l2_13b_mha_b1", "l2_13b_mha_b8", "l2_13b_mha_b64",
+CONFIG_NAMES = ("tiny", "l3_8b_b64", "l3_8b_b16", "l2_13b_mha_b1", "l2_13b_mha_b8", "l2_13b_mha_b64",
                 "l2_13b_mha_b128", "prefix_l3_70b", "long_splitk")
 
 
@@ -290,6 +290,11 @@ def make_config(name: str, threads: int = 0) -> Workload:
     if name == "l3_8b_b64":
         ctx = uniform_int(2, _S_CTX, 64, 512, 8192)
         return make_workload("l3_8b_b64", 2, 32, 8, 128, ctx, threads=threads)
+    if name == "l3_8b_b16":
+        # A quarter of l3_8b_b64 (its first 16 context lengths; K/V still larger than L2),
+        # small enough for full profiler captures.
+        ctx = uniform_int(2, _S_CTX, 16, 512, 8192)
+        return make_workload("l3_8b_b16", 2, 32, 8, 128, ctx, threads=threads)
     if name.startswith("l2_13b_mha_b"):
         B = int(name[len("l2_13b_mha_b"):])
         assert B in (1, 8, 64, 128)
