@@ -30,7 +30,8 @@
  *
  * Ownership: every pointer is caller-owned device memory (k_new/v_new/q etc.
  * must be in the same device's global memory); the library allocates nothing
- * and keeps no state between calls besides cached device attributes.  Calls
+ * and keeps no state between calls besides cached device attributes (and the
+ * static scratch of pkv_decode_attn_splitk_noalloc, described there).  Calls
  * are asynchronous on the given stream (0 = the legacy default stream).
  *
  * Errors: each call returns a pkv_status.  Host-side validation happens
@@ -145,6 +146,36 @@ int pkv_decode_attn_splitk(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
                            float scale, pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
                            int32_t partition_blocks, int32_t max_partitions, void *workspace,
                            size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream);
+
+/*
+ * Size of the static scratch used by pkv_decode_attn_splitk_noalloc (8 MiB).
+ */
+#define PKV_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * Split-KV decode attention that allocates nothing and takes no workspace.  The pages have
+ * no counterpart: this entry point exists for callers that cannot call cudaMalloc where they
+ * run attention (while a CUDA graph is being captured, inside an allocator's own callback, or
+ * under a framework that owns the whole device heap).  Same arguments and result as
+ * pkv_decode_attn_splitk without workspace/workspace_bytes; the partial outputs go to a
+ * PKV_STATIC_SCRATCH_BYTES array built into the library, which every GPU that loads the
+ * library holds until the process exits.
+ *  - If pkv_splitk_workspace_bytes(num_seqs, N, H, max_partitions) exceeds
+ *    PKV_STATIC_SCRATCH_BYTES the call returns PKV_ERR_WORKSPACE (pkv_last_error() says
+ *    how much was needed) and launches nothing.
+ *  - The first call on a device looks up the scratch's device address with that device
+ *    current (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents; nothing in it has
+ *    to start at zero.  Calls that overlap on the GPU (e.g. on two streams) race on it: order
+ *    them on one stream or with events.
+ */
+int pkv_decode_attn_splitk_noalloc(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                   const pkv_bf16 *v_cache, const int32_t *block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                   int32_t num_seqs, int32_t num_q_heads, float scale,
+                                   pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
+                                   int32_t partition_blocks, int32_t max_partitions,
+                                   int32_t *err_flag, pkv_stream_t stream);
 
 /*
  * The partition step alone: writes part_out [num_seqs][N][max_partitions][H] and

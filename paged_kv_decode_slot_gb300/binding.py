@@ -272,3 +272,32 @@ def pkv_status_string(status: int) -> str:
 
 def pkv_last_error() -> str:
     return _lib.pkv_last_error().decode()
+
+
+# ---------------------------------------------------------------------------------------------
+# Split-KV attention without a workspace, for callers that cannot allocate device memory where
+# they run attention (graph capture, allocator callbacks, frameworks that own the heap).
+STATIC_SCRATCH_BYTES = 8 << 20
+
+_lib.pkv_decode_attn_splitk_noalloc.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float,
+                                                _P, _P, CacheDesc, _I32, _I32, _P, _P]
+
+
+def pkv_decode_attn_splitk_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float, out,
+                                   partition_blocks: int, max_partitions: int, lse_out=None,
+                                   err_flag=None, stream=None) -> int:
+    """pkv_decode_attn_splitk with the partials in the library's static scratch.
+
+    Needs pkv_splitk_workspace_bytes(B, N, H, max_partitions) <= STATIC_SCRATCH_BYTES, else
+    returns PKV_ERR_WORKSPACE.  Calls share the scratch: do not overlap them on the GPU.
+    """
+    _attn_common(q, k_cache, v_cache, block_tables, context_lens)
+    _need(out, torch.bfloat16, 3, "out")
+    _opt(lse_out, torch.float32, 2, "lse_out")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    B, N, _ = q.shape
+    return _lib.pkv_decode_attn_splitk_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                               block_tables.shape[1], _ptr(context_lens), B, N,
+                                               float(scale), _ptr(out), _ptr(lse_out),
+                                               cache_desc(k_cache), partition_blocks, max_partitions,
+                                               _ptr(err_flag), _stream(stream))

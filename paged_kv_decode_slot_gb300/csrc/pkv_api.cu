@@ -375,3 +375,85 @@ PKV_EXPORT const char *pkv_status_string(int status)
 }
 
 PKV_EXPORT const char *pkv_last_error(void) { return g_last_error.c_str(); }
+
+// ---- split-KV attention for callers that cannot allocate device memory ---------------------
+//
+// Some callers cannot call cudaMalloc at the point where they run attention: code running
+// while a CUDA graph is being captured, inside a custom allocator's own callback, or under a
+// serving framework that owns every byte of the device heap and forbids allocations on the
+// decode path.  For them, pkv_decode_attn_splitk_noalloc keeps its partial results in the
+// file-scope array below instead of a caller-provided workspace.  The array is part of this
+// library's device image: every GPU that loads it holds PKV_STATIC_SCRATCH_BYTES of device
+// memory until the process exits.  All calls share it, and it keeps the previous call's
+// contents; calls that overlap on the GPU (for example on two streams) race on it.
+static __device__ __align__(256) unsigned char g_splitk_scratch[PKV_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxScratchDevices = 64;
+void *g_scratch_addr[kMaxScratchDevices] = {};
+std::mutex g_scratch_mu;
+
+// Host code cannot use g_splitk_scratch's name as a device address (on the host it names a
+// stand-in).  The device address is looked up once per device, with that device current.
+int scratch_address(void **addr)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxScratchDevices) {
+        g_last_error = "device ordinal beyond the static scratch table";
+        return PKV_ERR_UNSUPPORTED;
+    }
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_splitk_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static split-KV scratch)");
+        g_scratch_addr[dev] = p;
+    }
+    *addr = g_scratch_addr[dev];
+    return PKV_OK;
+}
+
+}  // namespace
+
+PKV_EXPORT int pkv_decode_attn_splitk_noalloc(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                              const pkv_bf16 *v_cache, const int32_t *block_tables,
+                                              int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                              int32_t num_seqs, int32_t num_q_heads, float scale,
+                                              pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
+                                              int32_t partition_blocks, int32_t max_partitions,
+                                              int32_t *err_flag, pkv_stream_t stream)
+{
+    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+               num_q_heads, scale, cache, err_flag};
+    if (!out) return PKV_ERR_NULL;
+    int st = validate_attn(a);
+    if (st != PKV_OK) return st;
+    if (partition_blocks <= 0 || max_partitions <= 0) return PKV_ERR_SHAPE;
+    if (!aligned(out, 4) || !aligned(lse_out, 4)) return PKV_ERR_ALIGN;
+    const size_t need = pkv_splitk_workspace_bytes(num_seqs, num_q_heads, cache.head_dim,
+                                                   max_partitions);
+    if (need > (size_t)PKV_STATIC_SCRATCH_BYTES) {
+        g_last_error = "split-KV partials need " + std::to_string(need) +
+                       " bytes; the static scratch holds " +
+                       std::to_string((size_t)PKV_STATIC_SCRATCH_BYTES) +
+                       " (use pkv_decode_attn_splitk with a workspace, or fewer partitions)";
+        return PKV_ERR_WORKSPACE;
+    }
+    if (num_seqs == 0) return PKV_OK;
+    void *scratch = nullptr;
+    st = scratch_address(&scratch);
+    if (st != PKV_OK) return st;
+    // Nothing in the scratch has to start at zero: the partition step writes every partial
+    // output and lse that the merge then reads, within this call.
+    float *part_out = static_cast<float *>(scratch);
+    float *part_lse = reinterpret_cast<float *>(
+        static_cast<char *>(scratch) +
+        splitk_lse_offset(num_seqs, num_q_heads, cache.head_dim, max_partitions));
+    st = run_partitions(a, partition_blocks, max_partitions, part_out, part_lse, stream);
+    if (st != PKV_OK) return st;
+    return pkv_lse_merge(part_out, part_lse, context_lens, num_seqs, num_q_heads, cache.head_dim,
+                         max_partitions, partition_blocks, out, lse_out, stream);
+}
