@@ -266,9 +266,9 @@ def run_ours(args):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     pb = args.partition_blocks or (w.partition_blocks if args.config == "long_splitk" else None)
     plan = plan_attention(w.B, w.K, w.max_blocks, sms, partition_blocks=pb)
-    if args.single:
+    if args.mode:
         from paged_kv_decode_slot_gb300.step import AttentionPlan
-        plan = AttentionPlan(False, w.max_blocks, 1)
+        plan = AttentionPlan(args.mode) if args.mode != "split" else plan
     step = DecodeStep(q, kn, vn, kc, vc, bt, cl, w.scale, plan=plan, err_flag=err)
     stream = torch.cuda.Stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -382,7 +382,9 @@ def run_ours(args):
         "frac_of_8tbs": achieved / (NORTH_STAR_TBS * 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "kernel": "attn_kernel" + (" + lse_merge_kernel" if plan.split else ""),
+                     "kernel": {"single": "attn_kernel<128,0>",
+                                "split": "attn_kernel<128,1> + lse_merge_kernel",
+                                "balanced": "attn_balanced_kernel + balanced_merge_kernel"}[plan.mode],
                      "bytes_per_launch": attn_bytes,
                      "traffic": recorded_traffic(args.config)},
         "e2e": {"value": ws * nbytes["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
@@ -410,7 +412,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--partition-blocks", type=int, default=None)
-    ap.add_argument("--single", action="store_true", help="force the single-pass kernel")
+    ap.add_argument("--mode", choices=("single", "balanced", "split"), default=None,
+                    help="force an attention mode (split needs --partition-blocks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -148,6 +148,32 @@ int pkv_decode_attn_splitk(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
                            size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream);
 
 /*
+ * Workspace for pkv_decode_attn_balanced: two partial-output slots per CTA of the persistent
+ * grid (about 2 CTAs per SM of the current device, a multiple of num_kv_heads) and a
+ * per-sequence block prefix.  Queries the current device's SM count; returns 0 on error.
+ */
+size_t pkv_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim);
+
+/*
+ * Split-KV decode attention with balanced partitions (FlashDecoding's split, CS336 Lecture 10
+ * notes "其他优化", cut so every SM gets the same work).  For each KV head the (sequence,
+ * block) tiles are numbered in order and split into equal shares, one per CTA of a persistent
+ * grid (about 2 CTAs per SM; CTA c serves head c % K); a unit (sequence, KV head) that falls
+ * inside one share is finished there, one cut by share
+ * boundaries is merged from its pieces' (partial output, lse) by a second, stream-ordered
+ * launch with the log-sum-exp formula of pkv_lse_merge.  Same arguments and results as
+ * pkv_decode_attn plus a caller-owned, 256-byte aligned workspace of at least
+ * pkv_balanced_workspace_bytes(num_seqs, H) bytes.  num_seqs <= 1024 (PKV_ERR_UNSUPPORTED
+ * otherwise).
+ */
+int pkv_decode_attn_balanced(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                             const int32_t *block_tables, int32_t max_blocks_per_seq,
+                             const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                             float scale, pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
+                             void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                             pkv_stream_t stream);
+
+/*
  * Size of the static scratch used by pkv_decode_attn_splitk_noalloc (8 MiB).
  */
 #define PKV_STATIC_SCRATCH_BYTES (8u << 20)

@@ -16,7 +16,11 @@ import os
 
 import torch
 
-from .build import LIB_PATH
+from .build import LIB_PATH as _BUILT_LIB
+
+# PKV_LIBRARY selects another build of the same library (for example one compiled with other
+# pipeline depths); by default the in-tree build is loaded.
+LIB_PATH = os.environ.get("PKV_LIBRARY") or _BUILT_LIB
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libpagedkv.so is not built ({LIB_PATH}); run __graft_entry__.build()")
@@ -210,6 +214,31 @@ def pkv_decode_attn_splitk(q, k_cache, v_cache, block_tables, context_lens, scal
                                        _ptr(out), _ptr(lse_out), cache_desc(k_cache),
                                        partition_blocks, max_partitions, _ptr(workspace),
                                        workspace.numel(), _ptr(err_flag), _stream(stream))
+
+
+_lib.pkv_balanced_workspace_bytes.argtypes = [_I32, _I32, _I32]
+_lib.pkv_balanced_workspace_bytes.restype = ctypes.c_size_t
+_lib.pkv_decode_attn_balanced.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P,
+                                          _P, CacheDesc, _P, ctypes.c_size_t, _P, _P]
+MAX_BALANCED_SEQS = 1024
+
+
+def pkv_balanced_workspace_bytes(num_seqs: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(_lib.pkv_balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim))
+
+
+def pkv_decode_attn_balanced(q, k_cache, v_cache, block_tables, context_lens, scale: float, out,
+                             workspace, lse_out=None, err_flag=None, stream=None) -> int:
+    _attn_common(q, k_cache, v_cache, block_tables, context_lens)
+    _need(out, torch.bfloat16, 3, "out")
+    _opt(lse_out, torch.float32, 2, "lse_out")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    _need(workspace, torch.uint8, 1, "workspace")
+    B, N, _ = q.shape
+    return _lib.pkv_decode_attn_balanced(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                         block_tables.shape[1], _ptr(context_lens), B, N, float(scale),
+                                         _ptr(out), _ptr(lse_out), cache_desc(k_cache), _ptr(workspace),
+                                         workspace.numel(), _ptr(err_flag), _stream(stream))
 
 
 def pkv_decode_attn_partitions(q, k_cache, v_cache, block_tables, context_lens, scale: float,

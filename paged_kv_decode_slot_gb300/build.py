@@ -33,20 +33,28 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile every .cu to an object in _build/, link libpagedkv.so next to this file."""
-    if not force and not _stale():
+def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+                  out: str | None = None, defines=(), build_dir: str | None = None) -> str:
+    """Compile every .cu to an object in _build/, link libpagedkv.so next to this file.
+
+    ``out``/``defines``/``build_dir`` build a variant elsewhere (e.g. other pipeline depths via
+    -DPKV_STAGES=...); the default build is the in-tree library the package loads.
+    """
+    variant = out is not None
+    out = out or LIB_PATH
+    bdir = build_dir or BUILD_DIR
+    if not variant and not force and not _stale():
         return LIB_PATH
     nvcc = nvcc_path()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
     common = [nvcc, "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
-              "-I", INCLUDE, "-I", CSRC]
+              "-I", INCLUDE, "-I", CSRC, *[f"-D{d}" for d in defines]]
     if ptxas_info:
         common += ["-Xptxas", "-v"]
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmd = common + ["-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
@@ -55,21 +63,21 @@ def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool =
     logs = []
     failed = []
     for src, p in procs:
-        out, _ = p.communicate()
-        logs.append(out.decode(errors="replace"))
+        text, _ = p.communicate()
+        logs.append(text.decode(errors="replace"))
         if p.returncode != 0:
             failed.append(src)
     log_text = "".join(logs)
-    with open(os.path.join(BUILD_DIR, "compile.log"), "w") as f:
+    with open(os.path.join(bdir, "compile.log"), "w") as f:
         f.write(log_text)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}:\n{log_text}")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, out)
     if verbose:
         print(log_text, file=sys.stderr)
-    return LIB_PATH
+    return out
 
 
 if __name__ == "__main__":

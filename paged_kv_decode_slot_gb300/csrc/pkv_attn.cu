@@ -1,53 +1,112 @@
 // pkv_attn.cu - paged decode attention for sm_103a.
 //
-// One CTA per work unit (sequence b, KV head kvh[, partition p]).  A producer warp walks the
-// unit's slice of the block table and streams each physical block's K and V tiles
-// (16 tokens x H bf16 for head kvh) into a ring of shared-memory stages with TMA, one
-// mbarrier pair per stage.  Four consumer warps take the stages round-robin; each keeps its
-// own online-softmax state for the whole query group (the G = N/K query heads that share
-// kvh), so every K/V byte fetched from HBM serves all G heads:
+// Work is cut into tiles: one tile = one physical block (16 tokens) of one KV head.  A CTA has
+// a producer warp and four consumer warps.  The producer walks the CTA's tiles, looks each one
+// up in the block table, and streams its K and V (16 x H bf16 each) into a ring of shared-memory
+// stages with TMA, one mbarrier pair per stage.  The consumer warps take the stages round-robin;
+// each keeps an online-softmax state for the whole query group (the G = N/K query heads that share
+// the KV head), so every K/V byte fetched from HBM serves all G heads:
 //     S^T[16 tok x 8] = K_tile[16 x H] . Q^T[H x 8]        (mma.sync m16n8k16, G padded to 8)
 //     P^T            = exp2(S^T * scale*log2e - m)         (fp32, lazily rescaled running max)
 //     O^T[H x 8]    += V_tile^T[H x 16] . P^T[16 x 8]      (P^T moved to the B operand with
 //                                                          movmatrix; V^T via ldmatrix.trans)
-// At the end the warps' partial states are merged in shared memory and the CTA writes the
-// bf16 output and lse (single pass) or the fp32 normalised partial output and lse of its
-// partition (split-KV, merged afterwards by lse_merge_kernel).
+// When a unit (sequence, KV head) ends, the four warps' states are merged in shared memory.
 //
-// This fuses the block-table gather with attention ("融合块读取和注意力的内核" and
-// FlashDecoding in CS336 Lecture 10's notes) and computes, for one query token,
-// softmax(q K^T * scale) V with the maximum subtracted ("Optimización de la inferencia",
-// "Construye el mismo", Step 2).  The softmax is the online (running max / running sum)
-// form of the same quantity; the LSE merge is exact for disjoint key sets.
+// Three ways to cut the work:
+//  * attn_kernel<H, false>: one CTA per (KV head, sequence), whole sequence (single pass).
+//  * attn_kernel<H, true>:  one CTA per (partition, KV head, sequence), partitions of a fixed
+//    number of blocks (FlashDecoding); partial results are merged by lse_merge_kernel.
+//  * attn_balanced_kernel<H>: a persistent grid (about two CTAs per SM, a multiple of K) in which
+//    CTA c serves KV head c % K and takes the (c / K)-th equal share of that head's tiles in
+//    (sequence, block) order, keeping its TMA ring streaming across unit boundaries.  The K CTAs
+//    of one share read the same physical blocks at the same time (one per head), as the K CTAs of
+//    a sequence do in the single pass.  Units that lie inside one share are finished in place;
+//    units cut by a share boundary leave fp32 partials (at most two per CTA) for
+//    balanced_merge_kernel.
+//
+// This fuses the block-table gather with attention ("融合块读取和注意力的内核" and FlashDecoding
+// in CS336 Lecture 10's notes) and computes, for one query token, softmax(q K^T * scale) V with
+// the maximum subtracted ("Optimización de la inferencia", "Construye el mismo", Step 2), in its
+// online (running max / running sum) form; the log-sum-exp merge of disjoint key sets is exact.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 
+// Pipeline depth (K+V tile pairs in flight per CTA), CTAs per SM and producer warps per CTA.  The
+// bytes in flight per SM (stages x 8 KiB x CTAs at H = 128) must cover HBM latency under full
+// load, and one producer warp issues only about 2.6 M tiles/s (two TMA tile loads each), so a CTA
+// needs more than one to keep its ring full.
+#ifndef PKV_STAGES
+#define PKV_STAGES 8
+#endif
+#ifndef PKV_CTAS_PER_SM
+#define PKV_CTAS_PER_SM 3
+#endif
+#ifndef PKV_BAL_STAGES
+#define PKV_BAL_STAGES 8
+#endif
+#ifndef PKV_BAL_WARPS
+#define PKV_BAL_WARPS 4
+#endif
+#ifndef PKV_BAL_CTAS_PER_SM
+#define PKV_BAL_CTAS_PER_SM 2
+#endif
+
+#ifndef PKV_PRODUCERS
+#define PKV_PRODUCERS 2
+#endif
+#ifndef PKV_BAL_PRODUCERS
+#define PKV_BAL_PRODUCERS 2
+#endif
+
 constexpr int kConsumerWarps = 4;
-constexpr int kStages = 8;
-constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = PKV_STAGES;
+constexpr int kProducers = PKV_PRODUCERS;
+constexpr int kAttnThreads = (kConsumerWarps + kProducers) * 32;
+constexpr int kBalStages = PKV_BAL_STAGES;
+constexpr int kBalWarps = PKV_BAL_WARPS;
+constexpr int kBalProducers = PKV_BAL_PRODUCERS;
+constexpr int kBalThreads = (kBalWarps + kBalProducers) * 32;
+// Stage s is reused by tiles s, s+S, s+2S, ... and tile i goes to consumer warp i % W.  With
+// S a multiple of W every use of a stage belongs to the same warp, so a warp only waits for a
+// stage's next phase after it consumed the previous one and mbarrier parities cannot alias.
+// The same holds for the producer warps (producer p issues tiles i = p mod P).
+static_assert(kStages % kConsumerWarps == 0, "pipeline depth must be a multiple of the consumer warps");
+static_assert(kBalStages % kBalWarps == 0, "pipeline depth must be a multiple of the consumer warps");
+static_assert(kStages % kProducers == 0, "pipeline depth must be a multiple of the producer warps");
+static_assert(kBalStages % kBalProducers == 0, "pipeline depth must be a multiple of the producer warps");
+
+int balanced_ctas_per_sm() { return PKV_BAL_CTAS_PER_SM; }
 // Lazy rescaling: keep the running maximum until a new logit exceeds it by this much
 // (log2 units), so exponentials stay <= 2^8 and the accumulator is rarely rescaled.
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int H>
+template <int H, int S = kStages, int W = kConsumerWarps, int P = kProducers>
 struct AttnLayout {
     static constexpr int kHalves = H / 64;                  // 128-byte rows per token row
     static constexpr int kTileBytes = kBlockSize * H * 2;   // one K or V tile
     static constexpr int kStageBytes = 2 * kTileBytes;      // K tile then V tile
-    static constexpr int kPipeBytes = kStages * kStageBytes;
-    static constexpr int kMergeBytes = kConsumerWarps * 8 * (H + 2) * 4;
+    static constexpr int kPipeBytes = S * kStageBytes;
+    static constexpr int kMergeBytes = W * 8 * (H + 2) * 4;
+    // single-pass / partition kernel: the merge area reuses the drained pipeline
     static constexpr int kDataBytes = kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes;
-    static constexpr int kBarOffset = kDataBytes;           // full[kStages], empty[kStages]
-    static constexpr int kMiscOffset = kBarOffset + 2 * kStages * 8;  // slot_ok[], abort, issued
-    static constexpr int kBytes = kMiscOffset + (kStages + 4) * 4;
+    static constexpr int kBarOffset = kDataBytes;           // full[S], empty[S]
+    static constexpr int kMiscOffset = kBarOffset + 2 * S * 8;  // slot_ok[S], abort, issued[P]
+    static constexpr int kBytes = kMiscOffset + (S + 1 + P) * 4;
     static constexpr int kAlloc = kBytes + 1024;             // slack for 1024-byte alignment
+    // balanced kernel: pipeline, its own merge area, barriers, misc, then the block prefix
+    static constexpr int kBalMergeOffset = kPipeBytes;
+    static constexpr int kBalBarOffset = kBalMergeOffset + kMergeBytes;
+    static constexpr int kBalMiscOffset = kBalBarOffset + 2 * S * 8;
+    // misc: int64 issued[P], abort flag (padded to 8 bytes), slot_ok[S]
+    static constexpr int kBalSeqOffset = (kBalMiscOffset + 8 * P + 8 + S * 4 + 15) / 16 * 16;
+    static int balanced_alloc(int B) { return kBalSeqOffset + (B + 1) * 8 + 1024; }
+    static_assert(kBalMiscOffset % 8 == 0, "the balanced kernel's int64 counter needs 8-byte alignment");
+    static_assert(kBalSeqOffset % 16 == 0 && kPipeBytes % 1024 == 0, "shared-memory layout alignment");
+    static_assert(kStageBytes % 1024 == 0, "TMA destinations with 128B swizzle need 1024-byte alignment");
 };
-
-template <int H>
-int attn_smem_bytes() { return AttnLayout<H>::kAlloc; }
 
 // Byte offset inside a TMA-written, 128B-swizzled tile of the 16-byte chunk holding
 // elements h .. h+7 of token row tok.  Tile rows are 128 bytes; with half-major tiles the
@@ -63,13 +122,272 @@ __device__ __forceinline__ uint32_t tile_chunk_offset(int tok, int h, int tok_ma
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// ----------------------------- per-warp online-softmax state -----------------------------
+template <int H>
+struct WarpAcc {
+    float o[H / 16][4];  // O^T fragments: rows h (16 per m-tile), columns g = c0, c0+1
+    float m[2];          // running max of columns c0, c0+1 (log2 units)
+    float l[2];          // this lane's share of the running sums
+};
+
+template <int H>
+__device__ __forceinline__ void acc_reset(WarpAcc<H> &a)
+{
+#pragma unroll
+    for (int mt = 0; mt < H / 16; ++mt) a.o[mt][0] = a.o[mt][1] = a.o[mt][2] = a.o[mt][3] = 0.f;
+    a.m[0] = a.m[1] = -INFINITY;
+    a.l[0] = a.l[1] = 0.f;
+}
+
+// Q^T as the B operand of S^T = K . Q^T: lane l holds q[g = l/4][16kk + 2(l%4) + {0,1}] and
+// the same +8; rows g >= G are zero.
+template <int H>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[H / 16][2], const uint16_t *q, int N,
+                                             int b, int kvh, int G, int lane)
+{
+    const int g_row = lane >> 2, c0 = (lane & 3) * 2;
+    const bool live = g_row < G;
+    const uint16_t *qrow = q + ((size_t)b * N + (size_t)kvh * G + (live ? g_row : 0)) * H;
+#pragma unroll
+    for (int kk = 0; kk < H / 16; ++kk) {
+        qf[kk][0] = live ? __ldg(reinterpret_cast<const unsigned int *>(qrow + 16 * kk + c0)) : 0u;
+        qf[kk][1] = live ? __ldg(reinterpret_cast<const unsigned int *>(qrow + 16 * kk + c0 + 8)) : 0u;
+    }
+}
+
+// One 16-token tile (the first `valid` tokens count) folded into a warp's state.
+template <int H>
+__device__ __forceinline__ void tile_update(WarpAcc<H> &a, const uint32_t (&qf)[H / 16][2],
+                                            uint32_t kt, uint32_t vt, int valid, float sl2,
+                                            int tok_major, int lane)
+{
+    constexpr int kKSteps = H / 16;
+    const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: lane feeds matrix mi, row ri
+    const int k_tok = ri + 8 * (mi & 1), k_hoff = 8 * (mi >> 1);  // K as A (non-trans)
+    const int v_tok = ri + 8 * (mi >> 1), v_hoff = 8 * (mi & 1);  // V^T as A (trans)
+
+    // S^T = K . Q^T, two independent accumulation chains
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < kKSteps; kk += 2) {
+        uint32_t a0[4], a1[4];
+        ldsm_x4(a0, kt + tile_chunk_offset<H>(k_tok, 16 * kk + k_hoff, tok_major));
+        ldsm_x4(a1, kt + tile_chunk_offset<H>(k_tok, 16 * kk + 16 + k_hoff, tok_major));
+        mma_bf16_16816(sa, a0, qf[kk][0], qf[kk][1]);
+        mma_bf16_16816(sb, a1, qf[kk + 1][0], qf[kk + 1][1]);
+    }
+    // rows: tokens t0 = lane/4 and t1 = t0 + 8; columns: g = c0, c0+1
+    const int t0 = lane >> 2, t1 = t0 + 8;
+    const float x0 = t0 < valid ? (sa[0] + sb[0]) * sl2 : -INFINITY;
+    const float x1 = t0 < valid ? (sa[1] + sb[1]) * sl2 : -INFINITY;
+    const float x2 = t1 < valid ? (sa[2] + sb[2]) * sl2 : -INFINITY;
+    const float x3 = t1 < valid ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+    float mA = fmaxf(x0, x2), mB = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mA = fmaxf(mA, __shfl_xor_sync(0xFFFFFFFFu, mA, off));
+        mB = fmaxf(mB, __shfl_xor_sync(0xFFFFFFFFu, mB, off));
+    }
+    const bool needA = mA > a.m[0] + kRescaleThreshold;
+    const bool needB = mB > a.m[1] + kRescaleThreshold;
+    if (__any_sync(0xFFFFFFFFu, needA || needB)) {
+        const float alphaA = needA ? exp2f(a.m[0] - mA) : 1.f;
+        const float alphaB = needB ? exp2f(a.m[1] - mB) : 1.f;
+        if (needA) a.m[0] = mA;
+        if (needB) a.m[1] = mB;
+        a.l[0] *= alphaA;
+        a.l[1] *= alphaB;
+#pragma unroll
+        for (int mt = 0; mt < kKSteps; ++mt) {
+            a.o[mt][0] *= alphaA;
+            a.o[mt][1] *= alphaB;
+            a.o[mt][2] *= alphaA;
+            a.o[mt][3] *= alphaB;
+        }
+    }
+    const uint32_t p01 = pack_bf16x2(exp2f(x0 - a.m[0]), exp2f(x1 - a.m[1]));
+    const uint32_t p23 = pack_bf16x2(exp2f(x2 - a.m[0]), exp2f(x3 - a.m[1]));
+    a.l[0] += bf16x2_lo(p01) + bf16x2_lo(p23);  // sums of the rounded weights
+    a.l[1] += bf16x2_hi(p01) + bf16x2_hi(p23);
+    const uint32_t pb0 = movmatrix_trans(p01);    // P^T rows tok 0-7 -> B fragment
+    const uint32_t pb1 = movmatrix_trans(p23);    // tok 8-15
+
+    // O^T += V^T . P^T
+    const bool partial = valid < kBlockSize;
+    const int tc = (lane & 3) * 2;  // token columns of this lane's A fragment
+#pragma unroll
+    for (int mt = 0; mt < kKSteps; ++mt) {
+        uint32_t av[4];
+        ldsm_x4_trans(av, vt + tile_chunk_offset<H>(v_tok, 16 * mt + v_hoff, tok_major));
+        if (partial) {  // zero V of tokens past the context (they may be NaN poison)
+            const uint32_t lo0 = tc < valid ? 0x0000FFFFu : 0u;
+            const uint32_t hi0 = tc + 1 < valid ? 0xFFFF0000u : 0u;
+            const uint32_t lo1 = tc + 8 < valid ? 0x0000FFFFu : 0u;
+            const uint32_t hi1 = tc + 9 < valid ? 0xFFFF0000u : 0u;
+            av[0] &= lo0 | hi0;
+            av[1] &= lo0 | hi0;
+            av[2] &= lo1 | hi1;
+            av[3] &= lo1 | hi1;
+        }
+        mma_bf16_16816(a.o[mt], av, pb0, pb1);
+    }
+}
+
+// Finish a warp's sums (across the lanes that share a column) and store its state in the
+// merge area: mo[W][8][H], mm[W][8] (running max), ml[W][8] (running sum).
+template <int H>
+__device__ __forceinline__ void deposit(WarpAcc<H> &a, float *mo, float *mm, float *ml, int warp,
+                                        int lane)
+{
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        a.l[0] += __shfl_xor_sync(0xFFFFFFFFu, a.l[0], off);
+        a.l[1] += __shfl_xor_sync(0xFFFFFFFFu, a.l[1], off);
+    }
+    const int c0 = (lane & 3) * 2;
+    if (lane < 4) {
+        mm[warp * 8 + c0] = a.m[0];
+        mm[warp * 8 + c0 + 1] = a.m[1];
+        ml[warp * 8 + c0] = a.l[0];
+        ml[warp * 8 + c0 + 1] = a.l[1];
+    }
+    const int hr = lane >> 2;
+#pragma unroll
+    for (int mt = 0; mt < H / 16; ++mt) {
+        const int h = 16 * mt + hr;
+        mo[(warp * 8 + c0) * H + h] = a.o[mt][0];
+        mo[(warp * 8 + c0 + 1) * H + h] = a.o[mt][1];
+        mo[(warp * 8 + c0) * H + h + 8] = a.o[mt][2];
+        mo[(warp * 8 + c0 + 1) * H + h + 8] = a.o[mt][3];
+    }
+}
+
+// Combine the deposited states for column g, element h: normalised output and lse (natural).
+template <int H, int W = kConsumerWarps>
+__device__ __forceinline__ void combine(const float *mo, const float *mm, const float *ml, int g,
+                                        int h, float &val, float &lse)
+{
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) M = fmaxf(M, mm[w * 8 + g]);
+    float acc = 0.f, lsum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            const float sc = exp2f(mm[w * 8 + g] - M);
+            lsum += sc * ml[w * 8 + g];
+            acc += sc * mo[(w * 8 + g) * H + h];
+        }
+    }
+    // No key at all (M = -inf) gives 0 and -inf; a NaN anywhere in the inputs stays NaN.
+    val = M != -INFINITY ? acc / lsum : 0.f;
+    lse = M != -INFINITY ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+}
+
+template <int S>
+__device__ __forceinline__ void init_ring(uint32_t bar_full, uint32_t bar_empty)
+{
+    for (int s = 0; s < S; ++s) {
+        mbar_init(bar_full + 8 * s, 1);
+        mbar_init(bar_empty + 8 * s, 1);
+    }
+    fence_barrier_init();
+}
+
+// Producer side of one tile: wait for the stage to be free, then load the tile (or mark it
+// skipped).  Runs on one lane.  Returns false when the wait expired.
+template <int H, int S>
+__device__ __forceinline__ bool produce_tile(int64_t i, int kvh, int bid, bool ok, uint32_t base_u32,
+                                             uint32_t bar_full, uint32_t bar_empty,
+                                             volatile int *slot_ok, volatile int *abort_flag,
+                                             const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                                             int tok_major, int32_t *err_flag)
+{
+    using L = AttnLayout<H, S>;
+    const int s = (int)(i % S);
+    if (i >= S &&
+        !mbar_wait_bounded(bar_empty + 8 * s, (uint32_t)(((i / S) & 1) ^ 1), abort_flag,
+                           kWaitLimitNs)) {
+        if (!*abort_flag) set_flag(err_flag, PKV_FLAG_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+    }
+    if (ok) {
+        slot_ok[s] = 1;
+        const uint32_t dst = base_u32 + s * L::kStageBytes;
+        mbar_arrive_expect_tx(bar_full + 8 * s, L::kStageBytes);
+        if (tok_major) {
+            tma_load_5d(dst, tm_k, bar_full + 8 * s, 0, 0, kvh, 0, bid);
+            tma_load_5d(dst + L::kTileBytes, tm_v, bar_full + 8 * s, 0, 0, kvh, 0, bid);
+        } else {
+            tma_load_5d(dst, tm_k, bar_full + 8 * s, 0, 0, 0, kvh, bid);
+            tma_load_5d(dst + L::kTileBytes, tm_v, bar_full + 8 * s, 0, 0, 0, kvh, bid);
+        }
+    } else {
+        slot_ok[s] = 0;  // out-of-range block id: the tile is skipped
+        mbar_arrive(bar_full + 8 * s);
+    }
+    return true;
+}
+
+// Producer warp p of P issues the CTA's tiles i = p, p + P, p + 2P, ... in order (each: wait for
+// its stage, then TMA its K and V).  `lookup(i)` gives tile i's physical block id; lanes look up
+// 32 tiles at a time, the next 32 while the current ones are issued.  Returns the number of
+// tiles this producer issued.
+template <int H, int S, int P, typename Lookup>
+__device__ __forceinline__ int64_t run_producer(int pw, int lane, int64_t n, int kvh, Lookup lookup,
+                                                int num_blocks, uint32_t base_u32, uint32_t bar_full,
+                                                uint32_t bar_empty, volatile int *slot_ok,
+                                                volatile int *abort_flag, const CUtensorMap *tm_k,
+                                                const CUtensorMap *tm_v, int tok_major,
+                                                int32_t *err_flag)
+{
+    const int64_t mine = n > pw ? (n - pw + P - 1) / P : 0;
+    int cur = lane < mine ? lookup(pw + (int64_t)P * lane) : 0;
+    int64_t issued = 0;
+    bool aborted = false;
+    for (int64_t k0 = 0; k0 < mine && !aborted; k0 += 32) {
+        const int nxt = (k0 + 32 + lane < mine) ? lookup(pw + (int64_t)P * (k0 + 32 + lane)) : 0;
+        const int cnt = (int)min((int64_t)32, mine - k0);
+        const bool bad = lane < cnt && (cur < 0 || cur >= num_blocks);
+        const unsigned badmask = __ballot_sync(0xFFFFFFFFu, bad);
+        if (badmask && lane == 0) set_flag(err_flag, PKV_FLAG_BLOCK_RANGE);
+        for (int k = 0; k < cnt; ++k) {
+            const int bid = __shfl_sync(0xFFFFFFFFu, cur, k);
+            int lane0_abort = 0;
+            if (lane == 0) {
+                if (produce_tile<H, S>(pw + (int64_t)P * (k0 + k), kvh, bid, !((badmask >> k) & 1u),
+                                       base_u32, bar_full, bar_empty, slot_ok, abort_flag, tm_k,
+                                       tm_v, tok_major, err_flag))
+                    ++issued;
+                else
+                    lane0_abort = 1;
+            }
+            aborted = __shfl_sync(0xFFFFFFFFu, lane0_abort, 0) != 0;
+            if (aborted) break;
+        }
+        cur = nxt;
+    }
+    return issued;  // meaningful on lane 0
+}
+
+// Drain after an expired wait: producer pw waits (bounded) for its copies that may still land.
+template <int S, int P>
+__device__ __forceinline__ void drain_ring(uint32_t bar_full, int pw, int64_t issued)
+{
+    for (int64_t k = issued > S / P ? issued - S / P : 0; k < issued; ++k) {
+        const int64_t i = pw + (int64_t)P * k;
+        mbar_wait_bounded(bar_full + 8 * (int)(i % S), (uint32_t)((i / S) & 1), nullptr, kDrainLimitNs);
+    }
+}
+
+// ------------------------ single pass and fixed partitions --------------------------------
 template <int H, bool kSplit>
-__global__ void __launch_bounds__(kAttnThreads)
+__global__ void __launch_bounds__(kAttnThreads, PKV_CTAS_PER_SM)
 attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
             const AttnParams p)
 {
     using L = AttnLayout<H>;
-    constexpr int kKSteps = H / 16;  // k-steps of the QK^T contraction, m-tiles of PV
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -94,12 +412,15 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     const int nblk = blk_end - blk_begin;
 
     if (nblk <= 0) {
-        if (kSplit) return;  // an empty partition is never read by the merge
-        for (int idx = threadIdx.x; idx < G * H; idx += kAttnThreads) {
-            const int g = idx / H, h = idx - g * H;
-            const size_t bn = (size_t)b * p.N + (size_t)kvh * G + g;
-            p.out[bn * H + h] = __float2bfloat16_rn(0.0f);
-            if (h == 0 && p.lse_out) p.lse_out[bn] = -INFINITY;
+        // A single pass over an empty sequence writes 0 / -inf; an empty partition is never
+        // read by the merge and writes nothing.
+        if (!kSplit) {
+            for (int idx = threadIdx.x; idx < G * H; idx += kAttnThreads) {
+                const int g = idx / H, h = idx - g * H;
+                const size_t bn = (size_t)b * p.N + (size_t)kvh * G + g;
+                p.out[bn * H + h] = __float2bfloat16_rn(0.0f);
+                if (h == 0 && p.lse_out) p.lse_out[bn] = -INFINITY;
+            }
         }
         return;
     }
@@ -108,100 +429,34 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     const uint32_t bar_empty = bar_full + 8 * kStages;
     volatile int *slot_ok = reinterpret_cast<volatile int *>(base + L::kMiscOffset);
     volatile int *abort_flag = slot_ok + kStages;
-    volatile int *issued_count = abort_flag + 1;
+    volatile int *issued_count = abort_flag + 1;  // [kProducers]
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, 1);
-        }
         *abort_flag = 0;
-        *issued_count = 0;
-        fence_barrier_init();
+        for (int q = 0; q < kProducers; ++q) issued_count[q] = 0;
+        init_ring<kStages>(bar_full, bar_empty);
     }
     __syncthreads();
 
-    float o[kKSteps][4];  // O^T fragments: rows h (16 per m-tile), cols g
-    float m_run[2] = {-INFINITY, -INFINITY};
-    float l_run[2] = {0.f, 0.f};
+    WarpAcc<H> acc;
 
-    if (warp == kConsumerWarps) {
-        // ------------------------------ producer warp ------------------------------
-        if (lane == 0) {
+    if (warp >= kConsumerWarps) {
+        // ------------------------------ producer warps ------------------------------
+        const int pw = warp - kConsumerWarps;
+        if (lane == 0 && pw == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
         }
         const int32_t *tbl = p.block_tables + (size_t)b * p.max_nb + blk_begin;
-        int cur = lane < nblk ? __ldg(tbl + lane) : 0;
-        bool aborted = false;
-        int issued = 0;
-        for (int i0 = 0; i0 < nblk && !aborted; i0 += 32) {
-            const int nxt = (i0 + 32 + lane < nblk) ? __ldg(tbl + i0 + 32 + lane) : 0;
-            const int cnt = min(32, nblk - i0);
-            const bool bad = lane < cnt && (cur < 0 || cur >= p.num_blocks);
-            const unsigned badmask = __ballot_sync(0xFFFFFFFFu, bad);
-            if (badmask && lane == 0) set_flag(p.err_flag, PKV_FLAG_BLOCK_RANGE);
-            for (int k = 0; k < cnt; ++k) {
-                const int bid = __shfl_sync(0xFFFFFFFFu, cur, k);
-                int lane0_abort = 0;
-                if (lane == 0) {
-                    const int i = i0 + k;
-                    const int s = i % kStages;
-                    bool ok = true;
-                    if (i >= kStages)
-                        ok = mbar_wait_bounded(bar_empty + 8 * s, ((i / kStages) & 1) ^ 1,
-                                               abort_flag, kWaitLimitNs);
-                    if (!ok) {
-                        if (!*abort_flag) set_flag(p.err_flag, PKV_FLAG_TIMEOUT);
-                        *abort_flag = 1;
-                        lane0_abort = 1;
-                    } else if (!((badmask >> k) & 1u)) {
-                        slot_ok[s] = 1;
-                        const uint32_t dst = base_u32 + s * L::kStageBytes;
-                        mbar_arrive_expect_tx(bar_full + 8 * s, L::kStageBytes);
-                        if (p.tok_major) {
-                            tma_load_5d(dst, &tm_k, bar_full + 8 * s, 0, 0, kvh, 0, bid);
-                            tma_load_5d(dst + L::kTileBytes, &tm_v, bar_full + 8 * s, 0, 0, kvh, 0, bid);
-                        } else {
-                            tma_load_5d(dst, &tm_k, bar_full + 8 * s, 0, 0, 0, kvh, bid);
-                            tma_load_5d(dst + L::kTileBytes, &tm_v, bar_full + 8 * s, 0, 0, 0, kvh, bid);
-                        }
-                        ++issued;
-                    } else {
-                        slot_ok[s] = 0;  // out-of-range block id: the tile is skipped
-                        mbar_arrive(bar_full + 8 * s);
-                        ++issued;
-                    }
-                }
-                aborted = __shfl_sync(0xFFFFFFFFu, lane0_abort, 0) != 0;
-                if (aborted) break;
-            }
-            cur = nxt;
-        }
-        if (lane == 0) *issued_count = issued;
+        const int64_t issued = run_producer<H, kStages, kProducers>(
+            pw, lane, nblk, kvh, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, base_u32,
+            bar_full, bar_empty, slot_ok, abort_flag, &tm_k, &tm_v, p.tok_major, p.err_flag);
+        if (lane == 0) issued_count[pw] = (int)issued;
     } else {
         // ------------------------------ consumer warps ------------------------------
-        const int g_row = lane >> 2;        // Q^T column / fragment row owned by this lane
-        const int c0 = (lane & 3) * 2;      // first of the two columns this lane accumulates
-        uint32_t qf[kKSteps][2];            // Q^T as the B operand of S^T = K . Q^T
-        {
-            const bool live = g_row < G;
-            const uint16_t *qrow = p.q + ((size_t)b * p.N + (size_t)kvh * G + (live ? g_row : 0)) * H;
-#pragma unroll
-            for (int kk = 0; kk < kKSteps; ++kk) {
-                qf[kk][0] = live ? __ldg(reinterpret_cast<const unsigned int *>(qrow + 16 * kk + c0)) : 0u;
-                qf[kk][1] = live ? __ldg(reinterpret_cast<const unsigned int *>(qrow + 16 * kk + c0 + 8)) : 0u;
-            }
-        }
-#pragma unroll
-        for (int mt = 0; mt < kKSteps; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-
-        // ldmatrix source rows: lane l feeds matrix l/8, row l%8.
-        const int mi = lane >> 3, ri = lane & 7;
-        const int k_tok = ri + 8 * (mi & 1), k_hoff = 8 * (mi >> 1);  // K as A (non-trans)
-        const int v_tok = ri + 8 * (mi >> 1), v_hoff = 8 * (mi & 1);  // V^T as A (trans)
-        const float sl2 = p.scale_log2;
-
+        uint32_t qf[H / 16][2];
+        load_q_frags<H>(qf, p.q, p.N, b, kvh, G, lane);
+        acc_reset<H>(acc);
         for (int i = warp; i < nblk; i += kConsumerWarps) {
             const int s = i % kStages;
             if (!mbar_wait_bounded(bar_full + 8 * s, (i / kStages) & 1, abort_flag, kWaitLimitNs)) {
@@ -212,73 +467,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
             if (slot_ok[s]) {
                 const int valid = min(kBlockSize, ctx - (blk_begin + i) * kBlockSize);
                 const uint32_t kt = base_u32 + s * L::kStageBytes;
-                const uint32_t vt = kt + L::kTileBytes;
-
-                // S^T = K . Q^T, two independent accumulation chains
-                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int kk = 0; kk < kKSteps; kk += 2) {
-                    uint32_t a0[4], a1[4];
-                    ldsm_x4(a0, kt + tile_chunk_offset<H>(k_tok, 16 * kk + k_hoff, p.tok_major));
-                    ldsm_x4(a1, kt + tile_chunk_offset<H>(k_tok, 16 * kk + 16 + k_hoff, p.tok_major));
-                    mma_bf16_16816(sa, a0, qf[kk][0], qf[kk][1]);
-                    mma_bf16_16816(sb, a1, qf[kk + 1][0], qf[kk + 1][1]);
-                }
-                // rows: tokens t0 = lane/4 and t1 = t0 + 8; columns: g = c0, c0+1
-                const int t0 = lane >> 2, t1 = t0 + 8;
-                const float x0 = t0 < valid ? (sa[0] + sb[0]) * sl2 : -INFINITY;
-                const float x1 = t0 < valid ? (sa[1] + sb[1]) * sl2 : -INFINITY;
-                const float x2 = t1 < valid ? (sa[2] + sb[2]) * sl2 : -INFINITY;
-                const float x3 = t1 < valid ? (sa[3] + sb[3]) * sl2 : -INFINITY;
-                float mA = fmaxf(x0, x2), mB = fmaxf(x1, x3);
-#pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    mA = fmaxf(mA, __shfl_xor_sync(0xFFFFFFFFu, mA, off));
-                    mB = fmaxf(mB, __shfl_xor_sync(0xFFFFFFFFu, mB, off));
-                }
-                const bool needA = mA > m_run[0] + kRescaleThreshold;
-                const bool needB = mB > m_run[1] + kRescaleThreshold;
-                if (__any_sync(0xFFFFFFFFu, needA || needB)) {
-                    const float alphaA = needA ? exp2f(m_run[0] - mA) : 1.f;
-                    const float alphaB = needB ? exp2f(m_run[1] - mB) : 1.f;
-                    if (needA) m_run[0] = mA;
-                    if (needB) m_run[1] = mB;
-                    l_run[0] *= alphaA;
-                    l_run[1] *= alphaB;
-#pragma unroll
-                    for (int mt = 0; mt < kKSteps; ++mt) {
-                        o[mt][0] *= alphaA;
-                        o[mt][1] *= alphaB;
-                        o[mt][2] *= alphaA;
-                        o[mt][3] *= alphaB;
-                    }
-                }
-                const uint32_t p01 = pack_bf16x2(exp2f(x0 - m_run[0]), exp2f(x1 - m_run[1]));
-                const uint32_t p23 = pack_bf16x2(exp2f(x2 - m_run[0]), exp2f(x3 - m_run[1]));
-                l_run[0] += bf16x2_lo(p01) + bf16x2_lo(p23);  // sums of the rounded weights
-                l_run[1] += bf16x2_hi(p01) + bf16x2_hi(p23);
-                const uint32_t pb0 = movmatrix_trans(p01);    // P^T rows tok 0-7 -> B frag
-                const uint32_t pb1 = movmatrix_trans(p23);    // tok 8-15
-
-                // O^T += V^T . P^T
-                const bool partial = valid < kBlockSize;
-                const int tc = (lane & 3) * 2;  // token columns of this lane's A fragment
-#pragma unroll
-                for (int mt = 0; mt < kKSteps; ++mt) {
-                    uint32_t a[4];
-                    ldsm_x4_trans(a, vt + tile_chunk_offset<H>(v_tok, 16 * mt + v_hoff, p.tok_major));
-                    if (partial) {  // zero V of tokens past the context (they may be NaN poison)
-                        const uint32_t lo0 = tc < valid ? 0x0000FFFFu : 0u;
-                        const uint32_t hi0 = tc + 1 < valid ? 0xFFFF0000u : 0u;
-                        const uint32_t lo1 = tc + 8 < valid ? 0x0000FFFFu : 0u;
-                        const uint32_t hi1 = tc + 9 < valid ? 0xFFFF0000u : 0u;
-                        a[0] &= lo0 | hi0;
-                        a[1] &= lo0 | hi0;
-                        a[2] &= lo1 | hi1;
-                        a[3] &= lo1 | hi1;
-                    }
-                    mma_bf16_16816(o[mt], a, pb0, pb1);
-                }
+                tile_update<H>(acc, qf, kt, kt + L::kTileBytes, valid, p.scale_log2, p.tok_major, lane);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);
@@ -287,61 +476,23 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
 
     __syncthreads();
     if (*abort_flag) {
-        // Drain: wait (bounded) for copies that were issued and may still be landing.
-        if (threadIdx.x == kConsumerWarps * 32) {
-            const int issued = *issued_count;
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                mbar_wait_bounded(bar_full + 8 * (i % kStages), (i / kStages) & 1, nullptr,
-                                  kDrainLimitNs);
-        }
+        if (warp >= kConsumerWarps && lane == 0)
+            drain_ring<kStages, kProducers>(bar_full, warp - kConsumerWarps,
+                                            issued_count[warp - kConsumerWarps]);
         __syncthreads();
         return;
     }
 
     // ------------------------- merge the consumer warps' states -------------------------
     float *mo = reinterpret_cast<float *>(base);              // [W][8][H]
-    float *mm = mo + kConsumerWarps * 8 * H;                 // [W][8] running max (log2 units)
-    float *ml = mm + kConsumerWarps * 8;                     // [W][8] running sum
-    if (warp < kConsumerWarps) {
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l_run[0] += __shfl_xor_sync(0xFFFFFFFFu, l_run[0], off);
-            l_run[1] += __shfl_xor_sync(0xFFFFFFFFu, l_run[1], off);
-        }
-        const int c0 = (lane & 3) * 2;
-        if (lane < 4) {
-            mm[warp * 8 + c0] = m_run[0];
-            mm[warp * 8 + c0 + 1] = m_run[1];
-            ml[warp * 8 + c0] = l_run[0];
-            ml[warp * 8 + c0 + 1] = l_run[1];
-        }
-        const int hr = lane >> 2;
-#pragma unroll
-        for (int mt = 0; mt < kKSteps; ++mt) {
-            const int h = 16 * mt + hr;
-            mo[(warp * 8 + c0) * H + h] = o[mt][0];
-            mo[(warp * 8 + c0 + 1) * H + h] = o[mt][1];
-            mo[(warp * 8 + c0) * H + h + 8] = o[mt][2];
-            mo[(warp * 8 + c0 + 1) * H + h + 8] = o[mt][3];
-        }
-    }
+    float *mm = mo + kConsumerWarps * 8 * H;                 // [W][8]
+    float *ml = mm + kConsumerWarps * 8;                     // [W][8]
+    if (warp < kConsumerWarps) deposit<H>(acc, mo, mm, ml, warp, lane);
     __syncthreads();
     for (int idx = threadIdx.x; idx < G * H; idx += kAttnThreads) {
         const int g = idx / H, h = idx - g * H;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * 8 + g]);
-        float acc = 0.f, lsum = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float sc = exp2f(mm[w * 8 + g] - M);
-                lsum += sc * ml[w * 8 + g];
-                acc += sc * mo[(w * 8 + g) * H + h];
-            }
-        }
-        const float val = lsum > 0.f ? acc / lsum : 0.f;
-        const float lse = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+        float val, lse;
+        combine<H>(mo, mm, ml, g, h, val, lse);
         const size_t bn = (size_t)b * p.N + (size_t)kvh * G + g;
         if (kSplit) {
             const size_t bnp = bn * p.max_parts + part;
@@ -351,6 +502,275 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
             p.out[bn * H + h] = __float2bfloat16_rn(val);
             if (h == 0 && p.lse_out) p.lse_out[bn] = lse;
         }
+    }
+}
+
+// ------------------------------ balanced (stream-K) split ---------------------------------
+// For each KV head the tiles are numbered in (sequence b, block j) order; sequence b owns
+// tiles [pre[b], pre[b+1]) with pre[b+1] - pre[b] = nb_b.  Of the grid's S = gridDim.x / K
+// shares per head, share s takes tiles [floor(T*s/S), floor(T*(s+1)/S)); CTA c = s*K + kvh.
+struct TileLoc {
+    int b, j, nb;
+    int64_t unit_start;  // first tile of sequence b
+};
+
+__device__ __forceinline__ TileLoc locate_tile(const int64_t *pre, int B, int64_t t)
+{
+    int lo = 0, hi = B - 1;  // largest b with pre[b] <= t (it has tiles since pre[b+1] > t)
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    TileLoc L;
+    L.b = lo;
+    L.nb = (int)(pre[lo + 1] - pre[lo]);
+    L.j = (int)(t - pre[lo]);
+    L.unit_start = pre[lo];
+    return L;
+}
+
+__device__ __forceinline__ int64_t share_start(int64_t T, int G, int c)
+{
+    return T * c / G;  // the host bounds T * grid below 2^62
+}
+
+template <int W>
+__device__ __forceinline__ void consumer_bar()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
+}
+
+template <int H>
+__global__ void __launch_bounds__(kBalThreads, PKV_BAL_CTAS_PER_SM)
+attn_balanced_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const AttnParams p)
+{
+    constexpr int S = kBalStages, W = kBalWarps, P = kBalProducers;
+    using L = AttnLayout<H, S, W, P>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_u32 - raw_u32);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int B = p.B, K = p.K, G = p.G;
+    int64_t *pre = reinterpret_cast<int64_t *>(base + L::kBalSeqOffset);   // [B + 1]
+
+    // Per-sequence block counts and their prefix, by warp 0 (B <= 1024: 32 sequences a lane).
+    // An out-of-range context length counts as empty (and is flagged once).
+    auto blocks_of = [&](int s) {
+        const int c = p.context_lens[s];
+        return (c < 0 || c > p.max_nb * kBlockSize) ? 0 : (c + kBlockSize - 1) / kBlockSize;
+    };
+    if (warp == 0) {
+        const int per = (B + 31) / 32;
+        const int s0 = min(B, lane * per), s1 = min(B, s0 + per);
+        int64_t local = 0;
+        for (int s = s0; s < s1; ++s) {
+            const int c = p.context_lens[s];
+            if ((c < 0 || c > p.max_nb * kBlockSize) && blockIdx.x == 0)
+                set_flag(p.err_flag, PKV_FLAG_CTX_RANGE);
+            local += blocks_of(s);
+        }
+        int64_t incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        int64_t run = incl - local;
+        for (int s = s0; s < s1; ++s) {
+            pre[s] = run;
+            run += blocks_of(s);
+        }
+        if (lane == 31) pre[B] = incl;
+    }
+    __syncthreads();
+    const int64_t T = pre[B];
+    const int c = blockIdx.x, kvh = c % K, shares = gridDim.x / K, sh = c / K;
+    if (c == 0 && p.prefix_out)
+        for (int s = threadIdx.x; s <= B; s += kBalThreads) p.prefix_out[s] = pre[s];
+    const int64_t t0 = share_start(T, shares, sh), t1 = share_start(T, shares, sh + 1);
+    if (t0 >= t1) return;
+    const int64_t n = t1 - t0;
+
+    const uint32_t bar_full = base_u32 + L::kBalBarOffset;
+    const uint32_t bar_empty = bar_full + 8 * S;
+    volatile int64_t *issued_count = reinterpret_cast<volatile int64_t *>(base + L::kBalMiscOffset);  // [P]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + L::kBalMiscOffset + 8 * P);
+    volatile int *slot_ok = abort_flag + 2;
+    float *mo = reinterpret_cast<float *>(base + L::kBalMergeOffset);
+    float *mm = mo + W * 8 * H;
+    float *ml = mm + W * 8;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int q = 0; q < P; ++q) issued_count[q] = 0;
+        init_ring<S>(bar_full, bar_empty);
+    }
+    __syncthreads();
+
+    if (warp >= W) {
+        // ------------------------------ producer warps ------------------------------
+        const int pw = warp - W;
+        if (lane == 0 && pw == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
+        auto lookup = [&](int64_t i) -> int {
+            const TileLoc tl = locate_tile(pre, B, t0 + i);
+            return __ldg(p.block_tables + (size_t)tl.b * p.max_nb + tl.j);
+        };
+        const int64_t issued = run_producer<H, S, P>(pw, lane, n, kvh, lookup, p.num_blocks, base_u32,
+                                                      bar_full, bar_empty, slot_ok, abort_flag, &tm_k,
+                                                      &tm_v, p.tok_major, p.err_flag);
+        if (lane == 0) issued_count[pw] = issued;
+    } else {
+        // ------------------------------ consumer warps ------------------------------
+        // Every consumer warp walks the same units in order and meets the others at two
+        // consumer-only barriers per unit (also after an expired wait, so nobody is stranded).
+        WarpAcc<H> acc;
+        uint32_t qf[H / 16][2];
+        bool aborted = false;
+        bool first_unit = true;
+        int64_t t = t0;
+        while (t < t1) {
+            const TileLoc u = locate_tile(pre, B, t);
+            const int64_t ue = min(t1, u.unit_start + u.nb);   // end of this unit's part here
+            const bool whole = u.unit_start >= t0 && u.unit_start + u.nb <= t1;
+            const int ctx = p.context_lens[u.b];
+            load_q_frags<H>(qf, p.q, p.N, u.b, kvh, G, lane);
+            acc_reset<H>(acc);
+            const int64_t ibeg = t - t0, iend = ue - t0;
+            int64_t i = ibeg + (int64_t)((warp - (int)(ibeg % W) + W) % W);
+            for (; i < iend && !aborted; i += W) {
+                const int s = (int)(i % S);
+                if (!mbar_wait_bounded(bar_full + 8 * s, (uint32_t)((i / S) & 1), abort_flag,
+                                       kWaitLimitNs)) {
+                    if (!*abort_flag) set_flag(p.err_flag, PKV_FLAG_TIMEOUT);
+                    *abort_flag = 1;
+                    aborted = true;
+                    break;
+                }
+                if (slot_ok[s]) {
+                    const int j = u.j + (int)(i - ibeg);
+                    const int valid = min(kBlockSize, ctx - j * kBlockSize);
+                    const uint32_t kt = base_u32 + s * L::kStageBytes;
+                    tile_update<H>(acc, qf, kt, kt + L::kTileBytes, valid, p.scale_log2, p.tok_major, lane);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+            }
+            deposit<H>(acc, mo, mm, ml, warp, lane);
+            consumer_bar<W>();
+            if (!*abort_flag) {
+                const int slot = first_unit ? 0 : 1;
+                for (int idx = threadIdx.x; idx < G * H; idx += W * 32) {
+                    const int g = idx / H, h = idx - g * H;
+                    float val, lse;
+                    combine<H, W>(mo, mm, ml, g, h, val, lse);
+                    if (whole) {
+                        const size_t bn = (size_t)u.b * p.N + (size_t)kvh * G + g;
+                        p.out[bn * H + h] = __float2bfloat16_rn(val);
+                        if (h == 0 && p.lse_out) p.lse_out[bn] = lse;
+                    } else {
+                        const size_t cs = ((size_t)c * 2 + slot) * 8 + g;
+                        p.part_out[cs * H + h] = val;
+                        if (h == 0) p.part_lse[cs] = lse;
+                    }
+                }
+            }
+            consumer_bar<W>();
+            first_unit = false;
+            t = ue;
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag) {
+        if (warp >= W && lane == 0) drain_ring<S, P>(bar_full, warp - W, issued_count[warp - W]);
+        __syncthreads();
+    }
+}
+
+// Merge of the units the balanced kernel left split: one CTA per (KV head, sequence).  A unit
+// whose tiles all fell into one share is already final.  The pieces' lse are loaded in
+// parallel, their weights e^{lse_q - lse} computed once, then every (g, h) output element
+// sums its pieces.
+constexpr int kMergeThreads = 128;
+constexpr int kMaxPieces = 512;  // pieces of one unit held in shared memory per pass
+
+__global__ void __launch_bounds__(kMergeThreads)
+balanced_merge_kernel(const float *__restrict__ part_out, const float *__restrict__ part_lse,
+                      const int64_t *__restrict__ pre, int B, int N, int K, int H, int grid,
+                      __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out)
+{
+    __shared__ int piece_cs[kMaxPieces];        // (CTA, slot) index of each non-empty piece
+    __shared__ float wgt[kMaxPieces][8];        // lse of piece q, column g, then its weight
+    __shared__ float tot[8];
+    const int kvh = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+    const int G = N / K, shares = grid / K;
+    const int64_t T = pre[B];
+    const int nb = (int)(pre[b + 1] - pre[b]);
+    if (nb == 0) {  // empty sequence: no CTA touched it
+        for (int idx = tid; idx < G * H; idx += kMergeThreads) {
+            const int g = idx / H, h = idx - g * H;
+            const size_t bn = (size_t)b * N + (size_t)kvh * G + g;
+            out[bn * H + h] = __float2bfloat16_rn(0.f);
+            if (h == 0 && lse_out) lse_out[bn] = -INFINITY;
+        }
+        return;
+    }
+    const int64_t s = pre[b], e = s + nb;
+    auto share_of = [&](int64_t t) {
+        int c = (int)(t * shares / T);
+        while (c + 1 < shares && share_start(T, shares, c + 1) <= t) ++c;
+        while (c > 0 && share_start(T, shares, c) > t) --c;
+        return c;
+    };
+    const int q0 = share_of(s), q1 = share_of(e - 1);
+    if (q0 == q1) return;
+    const int slot0 = share_start(T, shares, q0) == s ? 0 : 1;
+    // Non-empty shares between q0 and q1 hold one piece each (shares with no tiles wrote nothing).
+    int np = 0;
+    if (tid == 0) {
+        for (int q = q0; q <= q1 && np < kMaxPieces; ++q)
+            if (share_start(T, shares, q) != share_start(T, shares, q + 1))
+                piece_cs[np++] = (q * K + kvh) * 2 + (q == q0 ? slot0 : 0);
+        tot[0] = __int_as_float(np);
+    }
+    __syncthreads();
+    np = __float_as_int(tot[0]);
+    __syncthreads();
+    for (int idx = tid; idx < np * G; idx += kMergeThreads) {
+        const int q = idx / G, g = idx - q * G;
+        wgt[q][g] = part_lse[(size_t)piece_cs[q] * 8 + g];
+    }
+    __syncthreads();
+    if (tid < G) {
+        float M = -INFINITY;
+        for (int q = 0; q < np; ++q) M = fmaxf(M, wgt[q][tid]);
+        float total = -INFINITY;
+        if (M != -INFINITY) {
+            float sum = 0.f;
+            for (int q = 0; q < np; ++q) sum += expf(wgt[q][tid] - M);
+            total = M + logf(sum);
+            for (int q = 0; q < np; ++q) wgt[q][tid] = expf(wgt[q][tid] - total);
+        } else {
+            for (int q = 0; q < np; ++q) wgt[q][tid] = 0.f;
+        }
+        tot[tid] = total;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < G * H; idx += kMergeThreads) {
+        const int g = idx / H, h = idx - g * H;
+        float val = 0.f;
+#pragma unroll 4
+        for (int q = 0; q < np; ++q)
+            val += wgt[q][g] * part_out[((size_t)piece_cs[q] * 8 + g) * H + h];
+        const size_t bn = (size_t)b * N + (size_t)kvh * G + g;
+        out[bn * H + h] = __float2bfloat16_rn(val);
+        if (h == 0 && lse_out) lse_out[bn] = tot[g];
     }
 }
 
@@ -384,20 +804,26 @@ __global__ void lse_merge_kernel(const float *__restrict__ part_out, const float
 }
 
 // ---------------------------------- launchers ----------------------------------------------
+template <typename Kern>
+static cudaError_t ensure_smem(Kern kern, int smem, int *cached)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (cached[dev] >= smem) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) cached[dev] = smem;
+    return e;
+}
+
 template <int H, bool kSplit>
 static cudaError_t launch_attn_t(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
                                  dim3 grid, cudaStream_t stream)
 {
-    constexpr int smem = AttnLayout<H>::kAlloc;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attn_kernel<H, kSplit>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
+    constexpr int smem = AttnLayout<H, kStages>::kAlloc;
+    static int cached[64] = {};
+    cudaError_t e = ensure_smem(attn_kernel<H, kSplit>, smem, cached);
+    if (e != cudaSuccess) return e;
     attn_kernel<H, kSplit><<<grid, kAttnThreads, smem, stream>>>(tk, tv, p);
     return cudaGetLastError();
 }
@@ -411,6 +837,35 @@ cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensor
                      : launch_attn_t<128, false>(tk, tv, p, grid, stream);
     return split ? launch_attn_t<64, true>(tk, tv, p, grid, stream)
                  : launch_attn_t<64, false>(tk, tv, p, grid, stream);
+}
+
+template <int H>
+static cudaError_t launch_balanced_t(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
+                                     int grid, cudaStream_t stream)
+{
+    using L = AttnLayout<H, kBalStages, kBalWarps, kBalProducers>;
+    const int smem = L::balanced_alloc(p.B);
+    static int cached[64] = {};
+    cudaError_t e = ensure_smem(attn_balanced_kernel<H>, L::balanced_alloc(kMaxBalancedSeqs), cached);
+    if (e != cudaSuccess) return e;
+    attn_balanced_kernel<H><<<grid, kBalThreads, smem, stream>>>(tk, tv, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_balanced(int H, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const AttnParams &p, int grid, cudaStream_t stream)
+{
+    return H == 128 ? launch_balanced_t<128>(tk, tv, p, grid, stream)
+                    : launch_balanced_t<64>(tk, tv, p, grid, stream);
+}
+
+cudaError_t launch_balanced_merge(const float *part_out, const float *part_lse, const int64_t *pre,
+                                  int B, int N, int K, int H, int grid, uint16_t *out, float *lse_out,
+                                  cudaStream_t stream)
+{
+    balanced_merge_kernel<<<dim3(K, B), kMergeThreads, 0, stream>>>(
+        part_out, part_lse, pre, B, N, K, H, grid, reinterpret_cast<__nv_bfloat16 *>(out), lse_out);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_lse_merge(const float *part_out, const float *part_lse, const int32_t *context_lens,

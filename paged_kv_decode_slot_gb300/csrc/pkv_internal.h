@@ -9,6 +9,10 @@
 
 namespace pkv {
 
+// The balanced kernel keeps per-sequence tile prefixes in shared memory: at most this many
+// sequences per call.
+constexpr int kMaxBalancedSeqs = 1024;
+
 struct AttnParams {
     const uint16_t *q;             // [B][N][H] bf16
     const int32_t *block_tables;   // [B][max_nb]
@@ -24,14 +28,23 @@ struct AttnParams {
     float *lse_out;                // single pass: [B][N] (nullable)
     float *part_out;               // split-KV: [B][N][max_parts][H]
     float *part_lse;               // split-KV: [B][N][max_parts]
+                                   // balanced: part_out [grid][2][8][H], part_lse [grid][2][8]
+    int64_t *prefix_out;           // balanced: tile prefix per sequence [B + 1], for the merge
     int32_t *err_flag;             // nullable
 };
 
-template <int H>
-int attn_smem_bytes();
-
 cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensorMap &tv,
                         const AttnParams &p, cudaStream_t stream);
+
+// CTAs per SM of the balanced kernel's persistent grid (a compile-time choice).
+int balanced_ctas_per_sm();
+
+cudaError_t launch_attn_balanced(int H, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const AttnParams &p, int grid, cudaStream_t stream);
+
+cudaError_t launch_balanced_merge(const float *part_out, const float *part_lse, const int64_t *pre,
+                                  int B, int N, int K, int H, int grid, uint16_t *out, float *lse_out,
+                                  cudaStream_t stream);
 
 cudaError_t launch_lse_merge(const float *part_out, const float *part_lse,
                              const int32_t *context_lens, int B, int N, int H, int max_parts,

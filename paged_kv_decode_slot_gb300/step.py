@@ -5,8 +5,10 @@ workspace) and issues, on one stream, the library calls that make a decode step:
 
 1. ``pkv_slot_mapping``  -- the new token's slot from its block table and context length;
 2. ``pkv_append``         -- its K/V written into that slot of the paged pools;
-3. ``pkv_decode_attn`` (one CTA per sequence and KV head) or ``pkv_decode_attn_splitk``
-   (partitions of the block table, then the log-sum-exp merge), as ``plan_attention`` picks.
+3. attention, in the mode ``plan_attention`` picks:
+   ``balanced`` -- ``pkv_decode_attn_balanced`` (persistent grid, equal tile shares, merge);
+   ``single``   -- ``pkv_decode_attn`` (one CTA per sequence and KV head, no workspace);
+   ``split``    -- ``pkv_decode_attn_splitk`` (fixed partitions of the block table, merge).
 """
 from __future__ import annotations
 
@@ -19,32 +21,43 @@ from . import binding as B
 
 @dataclass
 class AttentionPlan:
-    split: bool
-    partition_blocks: int
-    max_partitions: int
+    mode: str                      # "balanced" | "single" | "split"
+    partition_blocks: int = 0      # split only
+    max_partitions: int = 1        # split only
+
+    @property
+    def split(self) -> bool:
+        return self.mode != "single"
 
     def describe(self) -> str:
-        if not self.split:
-            return "single-pass"
-        return f"split-KV, {self.partition_blocks}-block partitions (max {self.max_partitions})"
+        if self.mode == "split":
+            return f"split-KV, {self.partition_blocks}-block partitions (max {self.max_partitions})"
+        if self.mode == "balanced":
+            return "balanced split-KV (persistent grid, equal tile shares)"
+        return "single-pass"
 
 
 def plan_attention(num_seqs: int, num_kv_heads: int, max_blocks_per_seq: int, num_sms: int,
                    partition_blocks: int | None = None) -> AttentionPlan:
-    """Single pass when (sequence, KV head) units fill the GPU, else split-KV.
+    """Single pass when (sequence, KV head) units cover every SM, else the balanced split.
 
-    The single-pass kernel runs one CTA per unit and up to 3 CTAs per SM, so fewer than
-    ~2 units per SM leaves bandwidth idle; the split path multiplies the units by the
-    number of partitions.  An explicit ``partition_blocks`` forces the split path.
+    Measured on GB300: with at least one unit per SM the single pass (up to three CTAs per SM,
+    no merge) is fastest; with fewer units it leaves SMs idle and the balanced split (every SM
+    gets the same number of tiles) is.  The balanced split keeps a per-sequence prefix in
+    shared memory and takes at most 1024 sequences; a larger batch with few units per SM falls
+    back to fixed partitions.  An explicit ``partition_blocks`` forces fixed partitions.
     """
+    if partition_blocks is not None:
+        return AttentionPlan("split", partition_blocks,
+                             B.max_partitions_for(max_blocks_per_seq, partition_blocks))
     units = num_seqs * num_kv_heads
-    if partition_blocks is None:
-        if units >= 2 * num_sms:
-            return AttentionPlan(False, max_blocks_per_seq, 1)
-        want_parts = -(-2 * num_sms // max(units, 1))
-        partition_blocks = max(4, -(-max_blocks_per_seq // want_parts))
-    max_parts = B.max_partitions_for(max_blocks_per_seq, partition_blocks)
-    return AttentionPlan(True, partition_blocks, max_parts)
+    if units >= num_sms:
+        return AttentionPlan("single", max_blocks_per_seq, 1)
+    if num_seqs <= B.MAX_BALANCED_SEQS:
+        return AttentionPlan("balanced")
+    want_parts = -(-2 * num_sms // max(units, 1))
+    pb = max(4, -(-max_blocks_per_seq // want_parts))
+    return AttentionPlan("split", pb, B.max_partitions_for(max_blocks_per_seq, pb))
 
 
 class DecodeStep:
@@ -72,8 +85,12 @@ class DecodeStep:
         self.lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev)
         self.err_flag = err_flag
         self.workspace = None
-        if plan.split:
+        if plan.mode == "split":
             nbytes = B.pkv_splitk_workspace_bytes(nseq, q.shape[1], q.shape[2], plan.max_partitions)
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        elif plan.mode == "balanced":
+            with torch.cuda.device(dev):
+                nbytes = B.pkv_balanced_workspace_bytes(nseq, k_cache.shape[2], q.shape[2])
             self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
 
     def slot_and_append(self, stream=None) -> None:
@@ -83,11 +100,15 @@ class DecodeStep:
                              self.err_flag, stream))
 
     def attention(self, stream=None) -> None:
-        if self.plan.split:
+        if self.plan.mode == "split":
             B.check(B.pkv_decode_attn_splitk(self.q, self.k_cache, self.v_cache, self.block_tables,
                                              self.context_lens, self.scale, self.out,
                                              self.plan.partition_blocks, self.plan.max_partitions,
                                              self.workspace, self.lse, self.err_flag, stream))
+        elif self.plan.mode == "balanced":
+            B.check(B.pkv_decode_attn_balanced(self.q, self.k_cache, self.v_cache, self.block_tables,
+                                               self.context_lens, self.scale, self.out, self.workspace,
+                                               self.lse, self.err_flag, stream))
         else:
             B.check(B.pkv_decode_attn(self.q, self.k_cache, self.v_cache, self.block_tables,
                                       self.context_lens, self.scale, self.out, self.lse,

@@ -137,9 +137,26 @@ def test_library_kv_bytes_matches_pages(lib):
 
 def test_attention_plan():
     from paged_kv_decode_slot_gb300.step import plan_attention
-    assert not plan_attention(64, 8, 512, 152).split                # 512 units fill 152 SMs
-    p = plan_attention(1, 40, 64, 152)                              # 40 units: split
-    assert p.split and p.max_partitions * p.partition_blocks >= 64
-    assert 40 * p.max_partitions >= 2 * 152
+    assert plan_attention(64, 8, 512, 152).mode == "single"            # units cover the SMs
+    assert plan_attention(16, 8, 512, 152).mode == "balanced"          # 128 units < 152 SMs
+    assert plan_attention(2, 8, 8192, 152).mode == "balanced"
+    assert plan_attention(1024, 8, 512, 152).mode == "single"
+    p = plan_attention(2000, 1, 64, 4096)                               # few units, many sequences
+    assert p.mode == "split"
+    assert p.max_partitions * p.partition_blocks >= 64 and 2000 * p.max_partitions >= 2 * 4096
     p = plan_attention(2, 8, 8192, 152, partition_blocks=256)
-    assert p.split and p.partition_blocks == 256 and p.max_partitions == 32
+    assert p.mode == "split" and p.partition_blocks == 256 and p.max_partitions == 32
+
+
+def test_balanced_host_validation(lib):
+    cdll, _ = lib
+    f = cdll.pkv_decode_attn_balanced
+    f.argtypes = [P, P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, P, P,
+                  Desc, P, ctypes.c_size_t, P, P]
+    args = lambda B=4, ws=FAKE, q=FAKE: (q, FAKE, FAKE, FAKE, 4, FAKE, B, 8, 0.125, FAKE, None,
+                                         Desc(64, 16, 2, 64), ws, 1 << 20, None, None)
+    assert f(*args(q=None)) == -1
+    assert f(*args(B=1025)) == -3                                     # beyond the shared-memory prefix
+    assert f(*args(ws=None)) == -7
+    assert f(*args(ws=FAKE + 64)) == -6
+    assert f(*args(B=0)) == 0

@@ -58,6 +58,15 @@ def _single(pkv, w, d, err=None):
     return out, lse
 
 
+def _balanced(pkv, w, d, err=None):
+    ws = torch.empty(pkv.pkv_balanced_workspace_bytes(w.B, w.K, w.H), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(w.B, w.N, dtype=torch.float32, device="cuda")
+    pkv.check(pkv.pkv_decode_attn_balanced(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                           d["context_lens"], w.scale, out, ws, lse, err))
+    return out, lse
+
+
 def _splitk(pkv, w, d, part_blocks, err=None):
     P = pkv.max_partitions_for(w.max_blocks, part_blocks)
     ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
@@ -136,6 +145,10 @@ def test_decode_attn_vs_oracle(pkv, oracle, name, make):
         _no_flags(pkv, err)
         assert_close(out_f64(out_s), ref, f"{name} split-KV {part_blocks}")
         assert_lse_close(lse_s.cpu().numpy(), ref_lse, f"{name} split-KV {part_blocks}")
+    out_b, lse_b = _balanced(pkv, w, d, err)
+    _no_flags(pkv, err)
+    assert_close(out_f64(out_b), ref, f"{name} balanced")
+    assert_lse_close(lse_b.cpu().numpy(), ref_lse, f"{name} balanced")
 
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
@@ -152,6 +165,9 @@ def test_decode_sweep_every_tail(pkv, oracle, G, H):
     assert_lse_close(lse.cpu().numpy(), ref_lse, f"sweep G={G} H={H}")
     out_s, _ = _splitk(pkv, w, d, 2)
     assert_close(out_f64(out_s), ref, f"sweep split G={G} H={H}")
+    out_b, lse_b = _balanced(pkv, w, d)
+    assert_close(out_f64(out_b), ref, f"sweep balanced G={G} H={H}")
+    assert_lse_close(lse_b.cpu().numpy(), ref_lse, f"sweep balanced G={G} H={H}")
 
 
 def test_partitions_vs_oracle(pkv, oracle):
@@ -181,6 +197,22 @@ def test_partitions_vs_oracle(pkv, oracle):
                                 d["context_lens"], pb, out, lse))
     assert_close(out_f64(out), ref, "merge of oracle partials")
     assert_lse_close(lse.cpu().numpy(), ref_lse, "merge of oracle partials")
+
+
+@pytest.mark.parametrize("ctxs", [[5000, 3, 0, 17, 2000, 1, 900], [1] * 700, [16 * 4096, 16]],
+                         ids=["mixed_with_empty", "many_tiny", "one_long"])
+def test_balanced_shares_vs_oracle(pkv, oracle, ctxs):
+    """Units cut by many shares, shares cut inside one unit, empty sequences, more CTAs than tiles."""
+    w = gen.make_workload("bal", 16, 16, 4, 128, ctxs)
+    d = _post_append_device(pkv, oracle, w)
+    kc, vc = appended_host_cache(oracle, w)
+    rows = list(range(w.B)) if w.B <= 16 else [0, 1, 2, 350, 699]
+    ref, ref_lse = oracle.decode(w.q[rows], kc, vc, w.block_tables[rows], w.context_lens[rows], w.scale)
+    err = _err()
+    out, lse = _balanced(pkv, w, d, err)
+    _no_flags(pkv, err)
+    assert_close(out_f64(out)[rows], ref, "balanced")
+    assert_lse_close(lse.cpu().numpy()[rows], ref_lse, "balanced")
 
 
 def test_single_partition_split_is_bit_identical(pkv, oracle):
@@ -220,11 +252,14 @@ def test_block_permutation_bit_identical(pkv, oracle):
 
 def test_ctx0_gives_zero_and_neg_inf(pkv, oracle):
     w = gen.make_workload("ctx0", 15, 8, 2, 64, [0, 20])
-    d = upload(w)
+    d = _post_append_device(pkv, oracle, w)
     out, lse = _single(pkv, w, d)
     assert torch.all(out[0].float() == 0) and torch.all(torch.isneginf(lse[0]))
     out_s, lse_s = _splitk(pkv, w, d, 1)
     assert torch.all(out_s[0].float() == 0) and torch.all(torch.isneginf(lse_s[0]))
+    out_b, lse_b = _balanced(pkv, w, d)
+    assert torch.all(out_b[0].float() == 0) and torch.all(torch.isneginf(lse_b[0]))
+    assert float((out_b[1].float() - out[1].float()).abs().max()) <= 2e-2
 
 
 # ------------------------------------ device-detected errors -------------------------------

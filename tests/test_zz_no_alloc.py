@@ -30,6 +30,10 @@ def pkv():
 
 def _both(pkv, w, part_blocks):
     d = upload(w)
+    # the decode step's append first: each sequence's newest slot holds a NaN poison until then
+    slots = torch.empty(w.B, dtype=torch.int64, device="cuda")
+    pkv.check(pkv.pkv_slot_mapping(d["block_tables"], d["context_lens"], w.num_blocks, slots))
+    pkv.check(pkv.pkv_append(d["k_new"], d["v_new"], slots, d["k_cache"], d["v_cache"]))
     P = pkv.max_partitions_for(w.max_blocks, part_blocks)
     assert pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P) <= pkv.binding.STATIC_SCRATCH_BYTES
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
