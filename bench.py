@@ -264,11 +264,9 @@ def run_ours(args):
     bt, cl = d32(w.block_tables), d32(w.context_lens)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    pb = args.partition_blocks or (w.partition_blocks if args.config == "long_splitk" else None)
-    plan = plan_attention(w.B, w.K, w.max_blocks, sms, partition_blocks=pb)
-    if args.mode:
-        from paged_kv_decode_slot_gb300.step import AttentionPlan
-        plan = AttentionPlan(args.mode) if args.mode != "split" else plan
+    plan = plan_attention(w.B, w.K, w.max_blocks, sms, partition_blocks=args.partition_blocks)
+    if args.mode and args.partition_blocks is None:
+        plan = plan_attention(w.B, w.K, w.max_blocks, sms, mode=args.mode)
     step = DecodeStep(q, kn, vn, kc, vc, bt, cl, w.scale, plan=plan, err_flag=err)
     stream = torch.cuda.Stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size

@@ -328,9 +328,7 @@ PKV_EXPORT int pkv_decode_attn_splitk(const pkv_bf16 *q, const pkv_bf16 *k_cache
 // ---- balanced split (persistent grid, equal tile shares) -----------------------------------
 namespace {
 
-// The balanced kernel's CTAs per SM times the SM count, rounded down to a multiple of the KV
-// head count (at least K).
-int balanced_grid(int32_t num_kv_heads, int *grid)
+int sm_count(int *sms)
 {
     static int cache[64] = {};
     int dev = 0;
@@ -338,28 +336,35 @@ int balanced_grid(int32_t num_kv_heads, int *grid)
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= 64) return PKV_ERR_UNSUPPORTED;
     if (!cache[dev]) {
-        int sms = 0;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        e = cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-        cache[dev] = pkv::balanced_ctas_per_sm() * sms;
     }
-    const int K = num_kv_heads > 0 ? num_kv_heads : 1;
-    int shares = cache[dev] >= K ? cache[dev] / K : 1;
-    if (shares > 512) shares = 512;  // the merge holds at most 512 pieces of one unit
-    *grid = shares * K;
+    *sms = cache[dev];
     return PKV_OK;
+}
+
+// The balanced kernel's CTAs per SM times the SM count, rounded down to a multiple of the KV
+// head count: CTA c = share * K + head.  The merge holds at most 512 pieces of one unit.
+int balanced_grid(int sms, int32_t K)
+{
+    int shares = pkv::balanced_ctas_per_sm() * sms / K;
+    if (shares < 1) shares = 1;
+    if (shares > 512) shares = 512;
+    return shares * K;
 }
 
 struct BalancedWs {
     int64_t lse_off, pre_off, bytes;
 };
 
+// part_out [grid][2][8][H] float, part_lse [grid][2][8] float, prefix int64 [B + 1]
 BalancedWs balanced_ws_layout(int grid, int32_t B, int32_t H)
 {
     auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
+    const int64_t slots = (int64_t)grid * 2 * 8;
     BalancedWs w;
-    w.lse_off = up((int64_t)grid * 2 * 8 * H * 4);
-    w.pre_off = w.lse_off + up((int64_t)grid * 2 * 8 * 4);
+    w.lse_off = up(slots * H * 4);
+    w.pre_off = w.lse_off + up(slots * 4);
     w.bytes = w.pre_off + (int64_t)(B + 1) * 8;
     return w;
 }
@@ -369,11 +374,9 @@ BalancedWs balanced_ws_layout(int grid, int32_t B, int32_t H)
 PKV_EXPORT size_t pkv_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads,
                                                int32_t head_dim)
 {
-    int grid = 0;
-    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-        balanced_grid(num_kv_heads, &grid) != PKV_OK)
-        return 0;
-    return (size_t)balanced_ws_layout(grid, num_seqs, head_dim).bytes;
+    int sms = 0;
+    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || sm_count(&sms) != PKV_OK) return 0;
+    return (size_t)balanced_ws_layout(balanced_grid(sms, num_kv_heads), num_seqs, head_dim).bytes;
 }
 
 PKV_EXPORT int pkv_decode_attn_balanced(const pkv_bf16 *q, const pkv_bf16 *k_cache,
@@ -394,18 +397,20 @@ PKV_EXPORT int pkv_decode_attn_balanced(const pkv_bf16 *q, const pkv_bf16 *k_cac
     if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
     if (!aligned(out, 4) || !aligned(lse_out, 4)) return PKV_ERR_ALIGN;
     if (num_seqs == 0) return PKV_OK;
-    int grid = 0;
-    st = balanced_grid(cache.num_kv_heads, &grid);
+    int sms = 0;
+    st = sm_count(&sms);
     if (st != PKV_OK) return st;
-    const BalancedWs lay = balanced_ws_layout(grid, num_seqs, cache.head_dim);
-    if (workspace_bytes < (size_t)lay.bytes) return PKV_ERR_WORKSPACE;
-    // tile indices times the grid size must stay within int64 inside the kernels
+    if (workspace_bytes < pkv_balanced_workspace_bytes(num_seqs, cache.num_kv_heads, cache.head_dim))
+        return PKV_ERR_WORKSPACE;
+    // tile indices times the share count must stay within int64 inside the kernels
     const double tiles_max = (double)num_seqs * max_blocks_per_seq;
-    if (tiles_max * grid > 4.0e18) return PKV_ERR_SHAPE;
+    if (tiles_max * 1024.0 > 4.0e18) return PKV_ERR_SHAPE;
     CUtensorMap tk, tv;
     int tok_major = 0;
     st = make_kv_maps(&tk, &tv, k_cache, v_cache, cache, &tok_major);
     if (st != PKV_OK) return st;
+    const int grid = balanced_grid(sms, cache.num_kv_heads);
+    const BalancedWs lay = balanced_ws_layout(grid, num_seqs, cache.head_dim);
     char *ws = static_cast<char *>(workspace);
     pkv::AttnParams p = params_of(a, tok_major);
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
@@ -416,7 +421,7 @@ PKV_EXPORT int pkv_decode_attn_balanced(const pkv_bf16 *q, const pkv_bf16 *k_cac
     cudaError_t e = pkv::launch_attn_balanced(cache.head_dim, tk, tv, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "balanced attention launch");
     e = pkv::launch_balanced_merge(p.part_out, p.part_lse, p.prefix_out, num_seqs, num_q_heads,
-                                   cache.num_kv_heads, cache.head_dim, grid, out, lse_out, stream);
+                                   cache.num_kv_heads, cache.head_dim, grid, 1, out, lse_out, stream);
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "balanced merge launch");
 }
 

@@ -14,8 +14,9 @@
 //
 // Three ways to cut the work:
 //  * attn_kernel<H, false>: one CTA per (KV head, sequence), whole sequence (single pass).
-//  * attn_kernel<H, true>:  one CTA per (partition, KV head, sequence), partitions of a fixed
-//    number of blocks (FlashDecoding); partial results are merged by lse_merge_kernel.
+//  * attn_kernel<H, true>:  one CTA per (KV head, sequence, partition), partitions of a fixed
+//    number of blocks (FlashDecoding), highest partition first; partial results are merged by
+//    lse_merge_kernel.
 //  * attn_balanced_kernel<H>: a persistent grid (about two CTAs per SM, a multiple of K) in which
 //    CTA c serves KV head c % K and takes the (c / K)-th equal share of that head's tiles in
 //    (sequence, block) order, keeping its TMA ring streaming across unit boundaries.  The K CTAs
@@ -330,17 +331,13 @@ __device__ __forceinline__ bool produce_tile(int64_t i, int kvh, int bid, bool o
     return true;
 }
 
-// Producer warp p of P issues the CTA's tiles i = p, p + P, p + 2P, ... in order (each: wait for
-// its stage, then TMA its K and V).  `lookup(i)` gives tile i's physical block id; lanes look up
-// 32 tiles at a time, the next 32 while the current ones are issued.  Returns the number of
-// tiles this producer issued.
-template <int H, int S, int P, typename Lookup>
-__device__ __forceinline__ int64_t run_producer(int pw, int lane, int64_t n, int kvh, Lookup lookup,
-                                                int num_blocks, uint32_t base_u32, uint32_t bar_full,
-                                                uint32_t bar_empty, volatile int *slot_ok,
-                                                volatile int *abort_flag, const CUtensorMap *tm_k,
-                                                const CUtensorMap *tm_v, int tok_major,
-                                                int32_t *err_flag)
+// Producer warp p of P issues the CTA's tiles i = p, p + P, p + 2P, ... in order: `lookup(i)`
+// gives tile i's physical block id (lanes look up 32 tiles at a time, the next 32 while the
+// current ones are issued) and `issue(i, bid, ok)` waits for the stage and loads it, returning
+// false when its wait expired.  Returns the number of tiles this producer issued (on lane 0).
+template <int P, typename Lookup, typename Issue>
+__device__ __forceinline__ int64_t run_producer(int pw, int lane, int64_t n, Lookup lookup,
+                                                int num_blocks, int32_t *err_flag, Issue issue)
 {
     const int64_t mine = n > pw ? (n - pw + P - 1) / P : 0;
     int cur = lane < mine ? lookup(pw + (int64_t)P * lane) : 0;
@@ -356,9 +353,7 @@ __device__ __forceinline__ int64_t run_producer(int pw, int lane, int64_t n, int
             const int bid = __shfl_sync(0xFFFFFFFFu, cur, k);
             int lane0_abort = 0;
             if (lane == 0) {
-                if (produce_tile<H, S>(pw + (int64_t)P * (k0 + k), kvh, bid, !((badmask >> k) & 1u),
-                                       base_u32, bar_full, bar_empty, slot_ok, abort_flag, tm_k,
-                                       tm_v, tok_major, err_flag))
+                if (issue(pw + (int64_t)P * (k0 + k), bid, !((badmask >> k) & 1u)))
                     ++issued;
                 else
                     lane0_abort = 1;
@@ -368,7 +363,7 @@ __device__ __forceinline__ int64_t run_producer(int pw, int lane, int64_t n, int
         }
         cur = nxt;
     }
-    return issued;  // meaningful on lane 0
+    return issued;
 }
 
 // Drain after an expired wait: producer pw waits (bounded) for its copies that may still land.
@@ -394,9 +389,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_u32 - raw_u32);
 
-    const int kvh = kSplit ? blockIdx.y : blockIdx.x;
-    const int b = kSplit ? blockIdx.z : blockIdx.y;
-    const int part = kSplit ? blockIdx.x : 0;
+    // Split grid (K, B, P): partitions are the slowest dimension and the highest runs first, so
+    // the extra partitions of the longest sequences start before the rest (longest-first).
+    const int kvh = blockIdx.x;
+    const int b = blockIdx.y;
+    const int part = kSplit ? (int)gridDim.z - 1 - (int)blockIdx.z : 0;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = p.G;
@@ -448,9 +445,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
             prefetch_tensormap(&tm_v);
         }
         const int32_t *tbl = p.block_tables + (size_t)b * p.max_nb + blk_begin;
-        const int64_t issued = run_producer<H, kStages, kProducers>(
-            pw, lane, nblk, kvh, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, base_u32,
-            bar_full, bar_empty, slot_ok, abort_flag, &tm_k, &tm_v, p.tok_major, p.err_flag);
+        const int64_t issued = run_producer<kProducers>(
+            pw, lane, nblk, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, p.err_flag,
+            [&](int64_t i, int bid, bool ok) {
+                return produce_tile<H, kStages>(i, kvh, bid, ok, base_u32, bar_full, bar_empty, slot_ok,
+                                                abort_flag, &tm_k, &tm_v, p.tok_major, p.err_flag);
+            });
         if (lane == 0) issued_count[pw] = (int)issued;
     } else {
         // ------------------------------ consumer warps ------------------------------
@@ -621,9 +621,11 @@ attn_balanced_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             const TileLoc tl = locate_tile(pre, B, t0 + i);
             return __ldg(p.block_tables + (size_t)tl.b * p.max_nb + tl.j);
         };
-        const int64_t issued = run_producer<H, S, P>(pw, lane, n, kvh, lookup, p.num_blocks, base_u32,
-                                                      bar_full, bar_empty, slot_ok, abort_flag, &tm_k,
-                                                      &tm_v, p.tok_major, p.err_flag);
+        const int64_t issued = run_producer<P>(
+            pw, lane, n, lookup, p.num_blocks, p.err_flag, [&](int64_t i, int bid, bool ok) {
+                return produce_tile<H, S>(i, kvh, bid, ok, base_u32, bar_full, bar_empty, slot_ok,
+                                          abort_flag, &tm_k, &tm_v, p.tok_major, p.err_flag);
+            });
         if (lane == 0) issued_count[pw] = issued;
     } else {
         // ------------------------------ consumer warps ------------------------------
@@ -702,14 +704,17 @@ constexpr int kMaxPieces = 512;  // pieces of one unit held in shared memory per
 
 __global__ void __launch_bounds__(kMergeThreads)
 balanced_merge_kernel(const float *__restrict__ part_out, const float *__restrict__ part_lse,
-                      const int64_t *__restrict__ pre, int B, int N, int K, int H, int grid,
+                      const int64_t *__restrict__ pre, int B, int N, int K, int H, int grid, int KG,
                       __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out)
 {
     __shared__ int piece_cs[kMaxPieces];        // (CTA, slot) index of each non-empty piece
     __shared__ float wgt[kMaxPieces][8];        // lse of piece q, column g, then its weight
     __shared__ float tot[8];
+    // Pieces come from CTA c = share * (K / KG) + kvh / KG, slot (first/last unit of its share),
+    // head kvh % KG of its group: entry ((c * 2 + slot) * KG + kvh % KG) * 8 + g.
     const int kvh = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-    const int G = N / K, shares = grid / K;
+    const int G = N / K, groups = K / KG, shares = grid / groups;
+    const int grp = kvh / KG, kh = kvh - grp * KG;
     const int64_t T = pre[B];
     const int nb = (int)(pre[b + 1] - pre[b]);
     if (nb == 0) {  // empty sequence: no CTA touched it
@@ -736,7 +741,7 @@ balanced_merge_kernel(const float *__restrict__ part_out, const float *__restric
     if (tid == 0) {
         for (int q = q0; q <= q1 && np < kMaxPieces; ++q)
             if (share_start(T, shares, q) != share_start(T, shares, q + 1))
-                piece_cs[np++] = (q * K + kvh) * 2 + (q == q0 ? slot0 : 0);
+                piece_cs[np++] = ((q * groups + grp) * 2 + (q == q0 ? slot0 : 0)) * KG + kh;
         tot[0] = __int_as_float(np);
     }
     __syncthreads();
@@ -831,7 +836,7 @@ static cudaError_t launch_attn_t(const CUtensorMap &tk, const CUtensorMap &tv, c
 cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensorMap &tv,
                         const AttnParams &p, cudaStream_t stream)
 {
-    dim3 grid = split ? dim3(p.max_parts, p.K, p.B) : dim3(p.K, p.B, 1);
+    dim3 grid = split ? dim3(p.K, p.B, p.max_parts) : dim3(p.K, p.B, 1);
     if (H == 128)
         return split ? launch_attn_t<128, true>(tk, tv, p, grid, stream)
                      : launch_attn_t<128, false>(tk, tv, p, grid, stream);
@@ -860,11 +865,11 @@ cudaError_t launch_attn_balanced(int H, const CUtensorMap &tk, const CUtensorMap
 }
 
 cudaError_t launch_balanced_merge(const float *part_out, const float *part_lse, const int64_t *pre,
-                                  int B, int N, int K, int H, int grid, uint16_t *out, float *lse_out,
-                                  cudaStream_t stream)
+                                  int B, int N, int K, int H, int grid, int KG, uint16_t *out,
+                                  float *lse_out, cudaStream_t stream)
 {
     balanced_merge_kernel<<<dim3(K, B), kMergeThreads, 0, stream>>>(
-        part_out, part_lse, pre, B, N, K, H, grid, reinterpret_cast<__nv_bfloat16 *>(out), lse_out);
+        part_out, part_lse, pre, B, N, K, H, grid, KG, reinterpret_cast<__nv_bfloat16 *>(out), lse_out);
     return cudaGetLastError();
 }
 

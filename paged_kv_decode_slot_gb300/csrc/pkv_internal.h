@@ -42,9 +42,11 @@ int balanced_ctas_per_sm();
 cudaError_t launch_attn_balanced(int H, const CUtensorMap &tk, const CUtensorMap &tv,
                                  const AttnParams &p, int grid, cudaStream_t stream);
 
+// Partials are indexed ((c * 2 + slot) * KG + head-in-group) * 8 + g; attn_balanced_kernel
+// writes them with KG = 1.
 cudaError_t launch_balanced_merge(const float *part_out, const float *part_lse, const int64_t *pre,
-                                  int B, int N, int K, int H, int grid, uint16_t *out, float *lse_out,
-                                  cudaStream_t stream);
+                                  int B, int N, int K, int H, int grid, int KG, uint16_t *out,
+                                  float *lse_out, cudaStream_t stream);
 
 cudaError_t launch_lse_merge(const float *part_out, const float *part_lse,
                              const int32_t *context_lens, int B, int N, int H, int max_parts,

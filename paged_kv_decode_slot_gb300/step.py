@@ -6,9 +6,9 @@ workspace) and issues, on one stream, the library calls that make a decode step:
 1. ``pkv_slot_mapping``  -- the new token's slot from its block table and context length;
 2. ``pkv_append``         -- its K/V written into that slot of the paged pools;
 3. attention, in the mode ``plan_attention`` picks:
-   ``balanced`` -- ``pkv_decode_attn_balanced`` (persistent grid, equal tile shares, merge);
    ``single``   -- ``pkv_decode_attn`` (one CTA per sequence and KV head, no workspace);
-   ``split``    -- ``pkv_decode_attn_splitk`` (fixed partitions of the block table, merge).
+   ``split``    -- ``pkv_decode_attn_splitk`` (fixed partitions of the block table, merge);
+   ``balanced`` -- ``pkv_decode_attn_balanced`` (persistent grid, equal tile shares, merge).
 """
 from __future__ import annotations
 
@@ -38,26 +38,30 @@ class AttentionPlan:
 
 
 def plan_attention(num_seqs: int, num_kv_heads: int, max_blocks_per_seq: int, num_sms: int,
-                   partition_blocks: int | None = None) -> AttentionPlan:
-    """Single pass when (sequence, KV head) units cover every SM, else the balanced split.
+                   partition_blocks: int | None = None, mode: str | None = None) -> AttentionPlan:
+    """Single pass when (sequence, KV head) units cover every SM, else fixed partitions.
 
-    Measured on GB300: with at least one unit per SM the single pass (up to three CTAs per SM,
-    no merge) is fastest; with fewer units it leaves SMs idle and the balanced split (every SM
-    gets the same number of tiles) is.  The balanced split keeps a per-sequence prefix in
-    shared memory and takes at most 1024 sequences; a larger batch with few units per SM falls
-    back to fixed partitions.  An explicit ``partition_blocks`` forces fixed partitions.
+    Measured on GB300 (Llama-3-8B / Llama-2-13B / long-context shapes): with at least one unit
+    per SM the single pass (three CTAs per SM, no merge) is fastest; with fewer units it leaves
+    SMs idle, and partitions sized so the grid holds about 512 partition CTAs when every
+    sequence is as long as the table allows (at least 8 blocks each) are fastest -- 256 blocks
+    for two sequences of 128K/32K tokens, 128 for 16 sequences of up to 7.4K tokens.  The
+    persistent balanced split is available with ``mode="balanced"``.
     """
-    if partition_blocks is not None:
-        return AttentionPlan("split", partition_blocks,
-                             B.max_partitions_for(max_blocks_per_seq, partition_blocks))
-    units = num_seqs * num_kv_heads
-    if units >= num_sms:
-        return AttentionPlan("single", max_blocks_per_seq, 1)
-    if num_seqs <= B.MAX_BALANCED_SEQS:
+    if mode == "balanced":
         return AttentionPlan("balanced")
-    want_parts = -(-2 * num_sms // max(units, 1))
-    pb = max(4, -(-max_blocks_per_seq // want_parts))
-    return AttentionPlan("split", pb, B.max_partitions_for(max_blocks_per_seq, pb))
+    if mode == "single":
+        return AttentionPlan("single", max_blocks_per_seq, 1)
+    units = num_seqs * num_kv_heads
+    if partition_blocks is None:
+        if units >= num_sms and mode is None:
+            return AttentionPlan("single", max_blocks_per_seq, 1)
+        want = -(-max_blocks_per_seq * units // 512)
+        partition_blocks = 8
+        while partition_blocks < want:
+            partition_blocks *= 2
+    return AttentionPlan("split", partition_blocks,
+                         B.max_partitions_for(max_blocks_per_seq, partition_blocks))
 
 
 class DecodeStep:

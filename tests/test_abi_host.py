@@ -137,15 +137,17 @@ def test_library_kv_bytes_matches_pages(lib):
 
 def test_attention_plan():
     from paged_kv_decode_slot_gb300.step import plan_attention
-    assert plan_attention(64, 8, 512, 152).mode == "single"            # units cover the SMs
-    assert plan_attention(16, 8, 512, 152).mode == "balanced"          # 128 units < 152 SMs
-    assert plan_attention(2, 8, 8192, 152).mode == "balanced"
-    assert plan_attention(1024, 8, 512, 152).mode == "single"
-    p = plan_attention(2000, 1, 64, 4096)                               # few units, many sequences
-    assert p.mode == "split"
-    assert p.max_partitions * p.partition_blocks >= 64 and 2000 * p.max_partitions >= 2 * 4096
-    p = plan_attention(2, 8, 8192, 152, partition_blocks=256)
+    assert plan_attention(64, 8, 512, 152).mode == "single"            # 512 units cover 152 SMs
+    assert plan_attention(20, 8, 95, 152).mode == "single"
+    p = plan_attention(2, 8, 8192, 152)                                 # long context: 256 blocks
     assert p.mode == "split" and p.partition_blocks == 256 and p.max_partitions == 32
+    p = plan_attention(16, 8, 464, 152)                                 # 128 units: 128 blocks
+    assert p.mode == "split" and p.partition_blocks == 128 and p.max_partitions == 4
+    p = plan_attention(1, 40, 64, 152)                                  # at least 8 blocks
+    assert p.mode == "split" and p.partition_blocks == 8
+    assert plan_attention(64, 8, 512, 152, mode="balanced").mode == "balanced"
+    p = plan_attention(64, 8, 512, 152, partition_blocks=64)
+    assert p.mode == "split" and p.max_partitions == 8
 
 
 def test_balanced_host_validation(lib):
