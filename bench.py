@@ -267,7 +267,8 @@ def run_ours(args):
     plan = plan_attention(w.B, w.K, w.max_blocks, sms, partition_blocks=args.partition_blocks)
     if args.mode and args.partition_blocks is None:
         plan = plan_attention(w.B, w.K, w.max_blocks, sms, mode=args.mode)
-    step = DecodeStep(q, kn, vn, kc, vc, bt, cl, w.scale, plan=plan, err_flag=err)
+    step = DecodeStep(q, kn, vn, kc, vc, bt, cl, w.scale, plan=plan, err_flag=err,
+                      fused=not args.unfused)
     stream = torch.cuda.Stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.zeros(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
@@ -301,9 +302,13 @@ def run_ours(args):
             for i in range(args.steps):
                 flush_l2()                           # evict L2 (outside the events)
                 ev[i][0].record(stream)
-                step.slot_and_append(stream)
+                if step.fused:
+                    step.run(stream)                 # slot mapping + append + attention, fused
+                else:
+                    step.slot_and_append(stream)
                 ev[i][1].record(stream)
-                step.attention(stream)
+                if not step.fused:
+                    step.attention(stream)
                 ev[i][2].record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
@@ -319,7 +324,8 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    attn_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    # the fused step is one attention launch (plus the merge); it is the "dominant kernel" too
+    attn_ms = step_ms if step.fused else [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     mean_step = sum(step_ms) / len(step_ms)
     mean_attn = sum(attn_ms) / len(attn_ms)
     if dist is not None:
@@ -330,6 +336,30 @@ def run_ours(args):
     st, flag = pkv.pkv_read_err_flag(err, stream)
     if st != pkv.PKV_OK:
         raise RuntimeError(f"device error flag {flag:#x} during the timed steps")
+
+    # -- the same step replayed from a CUDA graph (one graph launch per step, no host gaps)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step.run(stream)
+    g_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            flush_l2()
+            k = i - args.warmup
+            if k >= 0:
+                g_ev[k][0].record(stream)
+            graph.replay()
+            if k >= 0:
+                g_ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    graph_ms = sum(e[0].elapsed_time(e[1]) for e in g_ev) / args.steps
+    if dist is not None:
+        t = torch.tensor([graph_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        graph_ms = t.item()
+    st, flag = pkv.pkv_read_err_flag(err, stream)
+    if st != pkv.PKV_OK:
+        raise RuntimeError(f"device error flag {flag:#x} during the graph replays")
 
     # -- end to end through the public API with host buffers (pinned), copies inside the timing
     hq = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -382,11 +412,16 @@ def run_ours(args):
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
                      "kernel": {"single": "attn_kernel<128,0>",
                                 "split": "attn_kernel<128,1> + lse_merge_kernel",
-                                "balanced": "attn_balanced_kernel + balanced_merge_kernel"}[plan.mode],
+                                "balanced": "attn_balanced_kernel + balanced_merge_kernel"}[plan.mode]
+                               + (" (append fused)" if step.fused else ""),
                      "bytes_per_launch": attn_bytes,
                      "traffic": recorded_traffic(args.config)},
         "e2e": {"value": ws * nbytes["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "graph": {"us_per_step": graph_ms * 1e3,
+                  "value": ws * nbytes["step"] / (graph_ms * 1e-3) / 1e9,
+                  "note": "the same step captured once in a CUDA graph and replayed per step"},
+        "step_launches": step.launches_per_step(),
         "gpu_launches": args.steps * step.launches_per_step(),
         "clocks": dict(clocks, window="timed steps plus ~1 s of the same steps right after"),
         "wall_s_timed_region": t_wall,
@@ -413,6 +448,8 @@ def main():
     ap.add_argument("--mode", choices=("single", "balanced", "split"), default=None,
                     help="force an attention mode (split needs --partition-blocks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="separate slot-mapping, append and attention launches")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

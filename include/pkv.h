@@ -148,6 +148,27 @@ int pkv_decode_attn_splitk(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
                            size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream);
 
 /*
+ * One whole decode step in one launch (two with partitions): for each sequence the new token's
+ * K and V (k_new/v_new [num_seqs][K][H]) are written into the slot of its logical position
+ * ctx-1 (slot_mapping_out[b] = that slot, or -1 for ctx 0; nullable) and the token attends to
+ * its context including itself -- pkv_slot_mapping + pkv_append + pkv_decode_attn (or
+ * pkv_decode_attn_splitk) fused.  The kernel that reads a sequence's last block replaces that
+ * block's row ctx-1 with the new K/V on chip and writes it to the pools, so no separate append
+ * pass runs ("Optimización de la inferencia", "Cache de KV": only the new token's K/V is
+ * computed and joined to the cache; CUDA graphs / fused kernels: CS336 Lecture 10 notes,
+ * "其他优化").  partition_blocks 0 = single pass (workspace unused, may be NULL); > 0 = fixed
+ * partitions with the workspace of pkv_decode_attn_splitk.  k_new/v_new 16-byte aligned.
+ * Results are bit-identical to the three separate calls.
+ */
+int pkv_decode_step(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                    pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *block_tables,
+                    int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                    int32_t num_q_heads, float scale, pkv_bf16 *out, float *lse_out,
+                    int64_t *slot_mapping_out, pkv_cache_desc cache, int32_t partition_blocks,
+                    int32_t max_partitions, void *workspace, size_t workspace_bytes,
+                    int32_t *err_flag, pkv_stream_t stream);
+
+/*
  * Workspace for pkv_decode_attn_balanced: two partial-output slots per CTA of the persistent
  * grid (about 2 CTAs per SM of the current device, a multiple of num_kv_heads) and a
  * per-sequence block prefix.  Queries the current device's SM count; returns 0 on error.

@@ -241,6 +241,32 @@ def pkv_decode_attn_balanced(q, k_cache, v_cache, block_tables, context_lens, sc
                                          workspace.numel(), _ptr(err_flag), _stream(stream))
 
 
+_lib.pkv_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P, _P,
+                                 _P, CacheDesc, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
+
+
+def pkv_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale: float, out,
+                    lse_out=None, slot_mapping_out=None, partition_blocks: int = 0,
+                    max_partitions: int = 0, workspace=None, err_flag=None, stream=None) -> int:
+    _attn_common(q, k_cache, v_cache, block_tables, context_lens)
+    _need(k_new, torch.bfloat16, 3, "k_new")
+    _need(v_new, torch.bfloat16, 3, "v_new")
+    _need(out, torch.bfloat16, 3, "out")
+    _opt(lse_out, torch.float32, 2, "lse_out")
+    _opt(slot_mapping_out, torch.int64, 1, "slot_mapping_out")
+    _opt(workspace, torch.uint8, 1, "workspace")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    B, N, _ = q.shape
+    if tuple(k_new.shape) != (B, k_cache.shape[2], k_cache.shape[3]) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [B, K, H]")
+    return _lib.pkv_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, N,
+                                float(scale), _ptr(out), _ptr(lse_out), _ptr(slot_mapping_out),
+                                cache_desc(k_cache), partition_blocks, max_partitions, _ptr(workspace),
+                                0 if workspace is None else workspace.numel(), _ptr(err_flag),
+                                _stream(stream))
+
+
 def pkv_decode_attn_partitions(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                                partition_blocks: int, part_out, part_lse, err_flag=None,
                                stream=None) -> int:

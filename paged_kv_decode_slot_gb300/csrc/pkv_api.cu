@@ -325,6 +325,66 @@ PKV_EXPORT int pkv_decode_attn_splitk(const pkv_bf16 *q, const pkv_bf16 *k_cache
                          max_partitions, partition_blocks, out, lse_out, stream);
 }
 
+// ---- fused decode step: slot mapping + append + attention -----------------------------------
+PKV_EXPORT int pkv_decode_step(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                               pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *block_tables,
+                               int32_t max_blocks_per_seq, const int32_t *context_lens,
+                               int32_t num_seqs, int32_t num_q_heads, float scale, pkv_bf16 *out,
+                               float *lse_out, int64_t *slot_mapping_out, pkv_cache_desc cache,
+                               int32_t partition_blocks, int32_t max_partitions, void *workspace,
+                               size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream)
+{
+    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+               num_q_heads, scale, cache, err_flag};
+    if (!out || !k_new || !v_new) return PKV_ERR_NULL;
+    int st = validate_attn(a);
+    if (st != PKV_OK) return st;
+    if (!aligned(out, 4) || !aligned(lse_out, 4) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+        !aligned(slot_mapping_out, 8))
+        return PKV_ERR_ALIGN;
+    const bool split = partition_blocks > 0;
+    float *part_out = nullptr, *part_lse = nullptr;
+    if (split) {
+        if (max_partitions <= 0 || (int64_t)max_partitions * partition_blocks < max_blocks_per_seq)
+            return PKV_ERR_SHAPE;
+        if (!workspace) return PKV_ERR_WORKSPACE;
+        if (workspace_bytes < pkv_splitk_workspace_bytes(num_seqs, num_q_heads, cache.head_dim,
+                                                         max_partitions))
+            return PKV_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
+        part_out = static_cast<float *>(workspace);
+        part_lse = reinterpret_cast<float *>(
+            static_cast<char *>(workspace) +
+            splitk_lse_offset(num_seqs, num_q_heads, cache.head_dim, max_partitions));
+    } else if (partition_blocks < 0) {
+        return PKV_ERR_SHAPE;
+    }
+    if (num_seqs == 0) return PKV_OK;
+    CUtensorMap tk, tv;
+    int tok_major = 0;
+    st = make_kv_maps(&tk, &tv, k_cache, v_cache, cache, &tok_major);
+    if (st != PKV_OK) return st;
+    pkv::AttnParams p = params_of(a, tok_major);
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.lse_out = lse_out;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache_w = k_cache;
+    p.v_cache_w = v_cache;
+    p.slot_out = slot_mapping_out;
+    if (split) {
+        p.part_blocks = partition_blocks;
+        p.max_parts = max_partitions;
+        p.part_out = part_out;
+        p.part_lse = part_lse;
+    }
+    cudaError_t e = pkv::launch_attn(cache.head_dim, split, tk, tv, p, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
+    if (!split) return PKV_OK;
+    return pkv_lse_merge(part_out, part_lse, context_lens, num_seqs, num_q_heads, cache.head_dim,
+                         max_partitions, partition_blocks, out, lse_out, stream);
+}
+
 // ---- balanced split (persistent grid, equal tile shares) -----------------------------------
 namespace {
 

@@ -376,6 +376,29 @@ __device__ __forceinline__ void drain_ring(uint32_t bar_full, int pw, int64_t is
     }
 }
 
+// Fused decode step: the consumer warp that holds a sequence's last block writes the new token's
+// K and V (k_new/v_new row of this KV head) into that tile's row ctx-1 in shared memory -- so
+// attention sees it in the same pass -- and into its slot of the pools in global memory.  Lanes
+// [0, H/8) move the K row, [H/8, H/4) the V row, 16 bytes each.  Each writer then fences its
+// shared-memory stores against the TMA that later refills the stage.
+template <int H>
+__device__ __forceinline__ void append_new_token(const AttnParams &p, int b, int kvh, int ctx, int bid,
+                                                 uint32_t kt, uint32_t vt, int lane)
+{
+    constexpr int kChunks = H / 8;
+    if (lane >= 2 * kChunks) return;
+    const int tok = (ctx - 1) % kBlockSize;
+    const bool is_v = lane >= kChunks;
+    const int c = is_v ? lane - kChunks : lane;
+    const size_t row = ((size_t)b * p.K + kvh) * H + 8 * c;
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>((is_v ? p.v_new : p.k_new) + row));
+    st_shared_v4((is_v ? vt : kt) + tile_chunk_offset<H>(tok, 8 * c, p.tok_major), v);
+    uint16_t *dst = (is_v ? p.v_cache_w : p.k_cache_w) +
+                    (((size_t)bid * kBlockSize + tok) * p.K + kvh) * H + 8 * c;
+    *reinterpret_cast<uint4 *>(dst) = v;
+    fence_proxy_async_shared();
+}
+
 // ------------------------ single pass and fixed partitions --------------------------------
 template <int H, bool kSplit>
 __global__ void __launch_bounds__(kAttnThreads, PKV_CTAS_PER_SM)
@@ -410,7 +433,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
 
     if (nblk <= 0) {
         // A single pass over an empty sequence writes 0 / -inf; an empty partition is never
-        // read by the merge and writes nothing.
+        // read by the merge and writes nothing.  An empty sequence appends nothing.
+        if (p.slot_out && nb == 0 && kvh == 0 && part == 0 && threadIdx.x == 0) p.slot_out[b] = -1;
         if (!kSplit) {
             for (int idx = threadIdx.x; idx < G * H; idx += kAttnThreads) {
                 const int g = idx / H, h = idx - g * H;
@@ -457,6 +481,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
         uint32_t qf[H / 16][2];
         load_q_frags<H>(qf, p.q, p.N, b, kvh, G, lane);
         acc_reset<H>(acc);
+        // fused append: the warp that will hold the last block warms the new K/V rows in L2
+        if (p.k_new && blk_end == nb && warp == (nb - 1 - blk_begin) % kConsumerWarps && lane < 2) {
+            const size_t row = ((size_t)b * p.K + kvh) * H;
+            prefetch_l2((lane ? p.v_new : p.k_new) + row);
+        }
         for (int i = warp; i < nblk; i += kConsumerWarps) {
             const int s = i % kStages;
             if (!mbar_wait_bounded(bar_full + 8 * s, (i / kStages) & 1, abort_flag, kWaitLimitNs)) {
@@ -464,11 +493,20 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
                 *abort_flag = 1;
                 break;
             }
+            // fused append: the tile of the sequence's last block holds the new token
+            const bool newest = p.k_new && blk_begin + i == nb - 1;
+            const int last_bid = newest ? __ldg(p.block_tables + (size_t)b * p.max_nb + nb - 1) : -1;
             if (slot_ok[s]) {
                 const int valid = min(kBlockSize, ctx - (blk_begin + i) * kBlockSize);
                 const uint32_t kt = base_u32 + s * L::kStageBytes;
+                if (newest) {
+                    append_new_token<H>(p, b, kvh, ctx, last_bid, kt, kt + L::kTileBytes, lane);
+                    __syncwarp();
+                }
                 tile_update<H>(acc, qf, kt, kt + L::kTileBytes, valid, p.scale_log2, p.tok_major, lane);
             }
+            if (newest && p.slot_out && kvh == 0 && lane == 0)
+                p.slot_out[b] = slot_ok[s] ? (int64_t)last_bid * kBlockSize + (ctx - 1) % kBlockSize : -1;
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);
         }

@@ -30,6 +30,12 @@ struct AttnParams {
     float *part_lse;               // split-KV: [B][N][max_parts]
                                    // balanced: part_out [grid][2][8][H], part_lse [grid][2][8]
     int64_t *prefix_out;           // balanced: tile prefix per sequence [B + 1], for the merge
+    // fused decode step (single pass / partitions): append the new token while attending
+    const uint16_t *k_new;         // [B][K][H], nullable: no append
+    const uint16_t *v_new;
+    uint16_t *k_cache_w;           // the pools, written at each sequence's newest slot
+    uint16_t *v_cache_w;
+    int64_t *slot_out;             // [B] slot of the newest token (-1 none), nullable
     int32_t *err_flag;             // nullable
 };
 

@@ -1,7 +1,9 @@
 """One decode step through libpagedkv: slot mapping, append into the slot, then attention.
 
 ``DecodeStep`` owns the per-step device buffers (slot mapping, output, lse, split-KV
-workspace) and issues, on one stream, the library calls that make a decode step:
+workspace).  By default one ``pkv_decode_step`` call does the whole step (the attention kernel
+appends the new token as it reads the sequence's last block); ``fused=False`` issues the
+separate library calls instead:
 
 1. ``pkv_slot_mapping``  -- the new token's slot from its block table and context length;
 2. ``pkv_append``         -- its K/V written into that slot of the paged pools;
@@ -72,7 +74,7 @@ class DecodeStep:
     """
 
     def __init__(self, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
-                 plan: AttentionPlan | None = None, err_flag=None):
+                 plan: AttentionPlan | None = None, err_flag=None, fused: bool = True):
         self.q, self.k_new, self.v_new = q, k_new, v_new
         self.k_cache, self.v_cache = k_cache, v_cache
         self.block_tables, self.context_lens = block_tables, context_lens
@@ -88,6 +90,8 @@ class DecodeStep:
         self.out = torch.empty_like(q)
         self.lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev)
         self.err_flag = err_flag
+        # fused: one pkv_decode_step call (single pass or fixed partitions) does it all
+        self.fused = fused and plan.mode != "balanced"
         self.workspace = None
         if plan.mode == "split":
             nbytes = B.pkv_splitk_workspace_bytes(nseq, q.shape[1], q.shape[2], plan.max_partitions)
@@ -119,8 +123,18 @@ class DecodeStep:
                                       self.err_flag, stream))
 
     def run(self, stream=None) -> None:
+        if self.fused:
+            split = self.plan.mode == "split"
+            B.check(B.pkv_decode_step(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
+                                      self.block_tables, self.context_lens, self.scale, self.out,
+                                      self.lse, self.slot_mapping,
+                                      self.plan.partition_blocks if split else 0,
+                                      self.plan.max_partitions if split else 0,
+                                      self.workspace, self.err_flag, stream))
+            return
         self.slot_and_append(stream)
         self.attention(stream)
 
     def launches_per_step(self) -> int:
-        return 2 + (2 if self.plan.split else 1)
+        attn = 2 if self.plan.split else 1
+        return attn if self.fused else 2 + attn

@@ -162,3 +162,20 @@ def test_balanced_host_validation(lib):
     assert f(*args(ws=None)) == -7
     assert f(*args(ws=FAKE + 64)) == -6
     assert f(*args(B=0)) == 0
+
+
+def test_decode_step_host_validation(lib):
+    cdll, _ = lib
+    f = cdll.pkv_decode_step
+    f.argtypes = [P, P, P, P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                  P, P, P, Desc, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_size_t, P, P]
+    args = lambda kn=FAKE, pb=0, P_=0, ws=None, wsb=0, B=4, slot=None: (
+        FAKE, kn, FAKE, FAKE, FAKE, FAKE, 4, FAKE, B, 8, 0.125, FAKE, None, slot, Desc(64, 16, 2, 64),
+        pb, P_, ws, wsb, None, None)
+    assert f(*args(kn=None)) == -1
+    assert f(*args(kn=FAKE + 8)) == -6                  # k_new rows move as 16-byte vectors
+    assert f(*args(slot=FAKE + 4)) == -6
+    assert f(*args(pb=-1)) == -2
+    assert f(*args(pb=2, P_=1)) == -2                   # 1 partition of 2 blocks < 4 blocks
+    assert f(*args(pb=2, P_=2)) == -7                   # partitions need the workspace
+    assert f(*args(B=0)) == 0

@@ -1,0 +1,119 @@
+"""The fused decode step (pkv_decode_step) against the separate calls and the oracle (GPU).
+
+One launch (two with partitions) must give bit for bit what slot mapping, append and attention
+give as separate calls: the same output and lse, the same bytes in both pools, the same slots.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from devutil import appended_host_cache, assert_close, bf16_host, out_f64, upload
+from paged_kv_decode_slot_gb300 import inputs as gen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_decode_slot_gb300.build import build_library
+    build_library()
+    import paged_kv_decode_slot_gb300 as pkv
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return pkv
+
+
+def _separate(pkv, w, part_blocks):
+    d = upload(w)
+    slots = torch.empty(w.B, dtype=torch.int64, device="cuda")
+    pkv.check(pkv.pkv_slot_mapping(d["block_tables"], d["context_lens"], w.num_blocks, slots))
+    pkv.check(pkv.pkv_append(d["k_new"], d["v_new"], slots, d["k_cache"], d["v_cache"]))
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(w.B, w.N, dtype=torch.float32, device="cuda")
+    if part_blocks:
+        P = pkv.max_partitions_for(w.max_blocks, part_blocks)
+        ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+        pkv.check(pkv.pkv_decode_attn_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                             d["context_lens"], w.scale, out, part_blocks, P, ws, lse))
+    else:
+        pkv.check(pkv.pkv_decode_attn(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                      d["context_lens"], w.scale, out, lse))
+    return d, out, lse, slots
+
+
+def _fused(pkv, w, part_blocks, err=None):
+    d = upload(w)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(w.B, w.N, dtype=torch.float32, device="cuda")
+    slots = torch.full((w.B,), -7, dtype=torch.int64, device="cuda")
+    P, ws = 0, None
+    if part_blocks:
+        P = pkv.max_partitions_for(w.max_blocks, part_blocks)
+        ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+    pkv.check(pkv.pkv_decode_step(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
+                                  d["block_tables"], d["context_lens"], w.scale, out, lse, slots,
+                                  part_blocks, P, ws, err))
+    return d, out, lse, slots
+
+
+CASES = [
+    ("tiny", lambda: gen.make_config("tiny")),
+    ("ragged_gqa4", lambda: gen.make_workload("f_ragged", 41, 32, 8, 128, gen.uniform_int(41, 9, 10, 1, 1500))),
+    ("mha", lambda: gen.make_workload("f_mha", 42, 8, 8, 128, [1, 16, 17, 200])),
+    ("gqa8_h64", lambda: gen.make_workload("f_gqa8", 43, 16, 2, 64, [31, 32, 33, 500])),
+    ("prefix", lambda: gen.make_config("prefix_l3_70b")),
+]
+
+
+@pytest.mark.parametrize("part_blocks", [0, 2, 5])
+@pytest.mark.parametrize("name,make", CASES, ids=[c[0] for c in CASES])
+def test_fused_step_equals_separate_calls(pkv, oracle, name, make, part_blocks):
+    w = make()
+    d1, out1, lse1, slots1 = _separate(pkv, w, part_blocks)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d2, out2, lse2, slots2 = _fused(pkv, w, part_blocks, err)
+    st, flag = pkv.pkv_read_err_flag(err)
+    assert st == pkv.PKV_OK, f"err_flag {flag:#x}"
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+    assert torch.equal(slots1, slots2)
+    assert torch.equal(d1["k_cache"].view(torch.int16), d2["k_cache"].view(torch.int16))
+    assert torch.equal(d1["v_cache"].view(torch.int16), d2["v_cache"].view(torch.int16))
+    # and against the oracle: the pools byte for byte, the output within tolerance
+    kc, vc = appended_host_cache(oracle, w)
+    assert np.array_equal(bf16_host(d2["k_cache"]), kc) and np.array_equal(bf16_host(d2["v_cache"]), vc)
+    assert np.array_equal(slots2.cpu().numpy(), oracle.slot_mapping(w.block_tables, w.context_lens))
+    ref, _ = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    assert_close(out_f64(out2), ref, f"fused {name} pb={part_blocks}")
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_fused_step_every_tail(pkv, oracle, G):
+    """The new token at every in-block position 0..15 and across the first blocks."""
+    w = gen.make_workload(f"f_tail{G}", 50 + G, 2 * G, 2, 128, list(range(1, 50)))
+    _, out1, lse1, _ = _separate(pkv, w, 0)
+    _, out2, lse2, _ = _fused(pkv, w, 0)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16)) and torch.equal(lse1, lse2)
+
+
+def test_fused_step_empty_sequence_and_bad_last_block(pkv):
+    w = gen.make_workload("f_edge", 60, 8, 2, 64, [0, 20, 33])
+    d = upload(w)
+    bt = d["block_tables"].clone()
+    bt[2, 2] = w.num_blocks + 5               # sequence 2's last block (tokens 32..) is out of range
+    d["block_tables"] = bt
+    out = torch.empty_like(d["q"])
+    slots = torch.full((w.B,), -7, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    before = bf16_host(d["k_cache"])
+    pkv.check(pkv.pkv_decode_step(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], bt,
+                                  d["context_lens"], w.scale, out, None, slots, 0, 0, None, err))
+    st, flag = pkv.pkv_read_err_flag(err)
+    assert st == pkv.PKV_ERR_RANGE and flag & pkv.PKV_FLAG_BLOCK_RANGE
+    s = slots.cpu().numpy()
+    assert s[0] == -1 and s[2] == -1 and s[1] == int(w.block_tables[1, 1]) * 16 + 3
+    assert torch.all(out[0].float() == 0)
+    after = bf16_host(d["k_cache"])
+    changed = np.argwhere(np.any(after != before, axis=(2, 3)))
+    assert [tuple(x) for x in changed] == [(int(w.block_tables[1, 1]), 3)]   # only sequence 1's slot
