@@ -63,6 +63,14 @@ class Oracle:
         lib.oracle_decode_partitions.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                                  _I32, _D, _I32, _I32, _P, _P, ctypes.c_int]
         lib.oracle_lse_merge.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P]
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = _D
+        lib.oracle_quantize_fp8.argtypes = [_P, _I64, _I32, _I32, _P, _P]
+        lib.oracle_append_fp8.argtypes = [_P, _P, _P, _P, _P, _I32, _P, _P, _I32, _I32]
+        lib.oracle_decode_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32,
+                                          _I32, _D, _P, _P, ctypes.c_int]
         self.lib = lib
 
     # -- KV size -------------------------------------------------------------------
@@ -140,6 +148,54 @@ class Oracle:
         out = np.empty((B, N, H), dtype=np.float64)
         lse = np.empty((B, N), dtype=np.float64)
         self.lib.oracle_lse_merge(_ptr(po), _ptr(pl), B, N, H, P, _ptr(out), _ptr(lse))
+        return out, lse
+
+
+    # -- FP8 (e4m3) cache --------------------------------------------------------------
+    def e4m3_encode(self, x: float) -> int:
+        return int(self.lib.oracle_e4m3_encode(float(x)))
+
+    def e4m3_decode_table(self) -> np.ndarray:
+        return np.array([self.lib.oracle_e4m3_decode(c) for c in range(256)], dtype=np.float64)
+
+    def quantize_fp8(self, src, scale) -> np.ndarray:
+        """e4m3 codes of a bf16 array [..., K, H] with per-KV-head scales [K]."""
+        x = np.ascontiguousarray(src, dtype=np.uint16)
+        sc = np.ascontiguousarray(scale, dtype=np.float32)
+        K, H = x.shape[-2], x.shape[-1]
+        rows = x.size // (K * H)
+        out = np.empty(x.shape, dtype=np.uint8)
+        self.lib.oracle_quantize_fp8(_ptr(x), rows, K, H, _ptr(sc), _ptr(out))
+        return out
+
+    def append_fp8(self, k_new, v_new, k_scale, v_scale, slots, k_cache8, v_cache8):
+        assert k_cache8.flags.c_contiguous and v_cache8.flags.c_contiguous
+        kn = np.ascontiguousarray(k_new, dtype=np.uint16)
+        vn = np.ascontiguousarray(v_new, dtype=np.uint16)
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+        sl = np.ascontiguousarray(slots, dtype=np.int64)
+        K, H = kn.shape[1], kn.shape[2]
+        self.lib.oracle_append_fp8(_ptr(kn), _ptr(vn), _ptr(ks), _ptr(vs), _ptr(sl), sl.shape[0],
+                                   _ptr(k_cache8), _ptr(v_cache8), K, H)
+        return k_cache8, v_cache8
+
+    def decode_fp8(self, q, k_cache8, v_cache8, k_scale, v_scale, block_tables, context_lens, scale,
+                   bs=16, threads=0):
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        kc = np.ascontiguousarray(k_cache8, dtype=np.uint8)
+        vc = np.ascontiguousarray(v_cache8, dtype=np.uint8)
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        B, N, H = q.shape
+        K = kc.shape[2]
+        out = np.empty((B, N, H), dtype=np.float64)
+        lse = np.empty((B, N), dtype=np.float64)
+        self.lib.oracle_decode_fp8(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
+                                   bt.shape[1], _ptr(cl), B, N, K, H, bs, float(scale), _ptr(out),
+                                   _ptr(lse), threads)
         return out, lse
 
 

@@ -127,6 +127,8 @@ static void attend(const double *q, const double *keys, const double *values, in
 
 typedef struct {
     const uint16_t *q, *k_cache, *v_cache;
+    const uint8_t *k8, *v8;             /* e4m3 pools instead of bf16 ones, when set */
+    const float *k_scale, *v_scale;
     const int32_t *block_tables, *context_lens;
     int32_t max_nb, B, N, K, H, bs;
     double scale;
@@ -147,11 +149,15 @@ static void decode_unit(const decode_job *j, int32_t b, int32_t kvh)
     double *qv = malloc(sizeof(double) * (size_t)H);
     for (int64_t t = 0; t < ctx; ++t) {
         int64_t slot = physical_slot(j->block_tables, j->max_nb, b, t, j->bs);
-        const uint16_t *krow = j->k_cache + ((size_t)slot * j->K + kvh) * H;
-        const uint16_t *vrow = j->v_cache + ((size_t)slot * j->K + kvh) * H;
+        const size_t row = ((size_t)slot * j->K + kvh) * H;
         for (int32_t h = 0; h < H; ++h) {
-            keys[t * H + h] = bf16_to_double(krow[h]);
-            values[t * H + h] = bf16_to_double(vrow[h]);
+            if (j->k8) { /* dequantize: decode(code) * per-head scale */
+                keys[t * H + h] = oracle_e4m3_decode(j->k8[row + h]) * (double)j->k_scale[kvh];
+                values[t * H + h] = oracle_e4m3_decode(j->v8[row + h]) * (double)j->v_scale[kvh];
+            } else {
+                keys[t * H + h] = bf16_to_double(j->k_cache[row + h]);
+                values[t * H + h] = bf16_to_double(j->v_cache[row + h]);
+            }
         }
     }
     for (int32_t g = 0; g < G; ++g) {
@@ -220,8 +226,8 @@ void oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v
                    int32_t B, int32_t N, int32_t K, int32_t H, int32_t bs, double scale,
                    double *out, double *lse, int nthreads)
 {
-    decode_job j = {q, k_cache, v_cache, block_tables, context_lens, max_nb, B, N, K, H, bs,
-                    scale, 0, 1, out, lse, nthreads, 0};
+    decode_job j = {q, k_cache, v_cache, 0, 0, 0, 0, block_tables, context_lens, max_nb, B, N, K,
+                    H, bs, scale, 0, 1, out, lse, nthreads, 0};
     run_decode(j);
 }
 
@@ -231,8 +237,8 @@ void oracle_decode_partitions(const uint16_t *q, const uint16_t *k_cache, const 
                               int32_t H, int32_t bs, double scale, int32_t partition_tokens,
                               int32_t max_parts, double *part_out, double *part_lse, int nthreads)
 {
-    decode_job j = {q, k_cache, v_cache, block_tables, context_lens, max_nb, B, N, K, H, bs,
-                    scale, partition_tokens, max_parts, part_out, part_lse, nthreads, 0};
+    decode_job j = {q, k_cache, v_cache, 0, 0, 0, 0, block_tables, context_lens, max_nb, B, N, K,
+                    H, bs, scale, partition_tokens, max_parts, part_out, part_lse, nthreads, 0};
     run_decode(j);
 }
 
@@ -262,4 +268,74 @@ void oracle_lse_merge(const double *part_out, const double *part_lse, int32_t B,
         }
         lse[bn] = total;
     }
+}
+
+/* ---- FP8 (e4m3) -------------------------------------------------------------------------
+   The format as the OCP 8-bit floating point specification defines E4M3: exponent bias 7,
+   normal values (1 + m/8) * 2^(e-7) for exponent fields 1..15 (except S.1111.111, NaN),
+   subnormals (m/8) * 2^-6, no infinities. */
+double oracle_e4m3_decode(uint8_t code)
+{
+    const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* Nearest e4m3 value (ties to the even code), saturating at +-448. */
+uint8_t oracle_e4m3_encode(float x)
+{
+    const uint8_t sign = signbit(x) ? 0x80 : 0;
+    if (isnan(x)) return (uint8_t)(sign | 0x7F);
+    double a = fabs((double)x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    /* binade of a (exponents below -6 share the subnormal spacing 2^-9) */
+    int e = -6;
+    if (a >= ldexp(1.0, -6)) {
+        int ex;
+        frexp(a, &ex);       /* a = f * 2^ex, f in [0.5, 1) */
+        e = ex - 1;
+    }
+    const double quantum = ldexp(1.0, e - 3);
+    double r = nearbyint(a / quantum); /* a / quantum is exact; ties to even */
+    if (e == -6 && r < 8.0) return (uint8_t)(sign | (uint8_t)r); /* subnormal (or zero) */
+    if (r >= 16.0) {         /* rounded up into the next binade */
+        r = 8.0;
+        e += 1;
+    }
+    return (uint8_t)(sign | ((e + 7) << 3) | ((int)r - 8));
+}
+
+void oracle_quantize_fp8(const uint16_t *src, int64_t rows, int32_t K, int32_t H,
+                         const float *scale, uint8_t *dst)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int32_t kvh = 0; kvh < K; ++kvh)
+            for (int32_t h = 0; h < H; ++h) {
+                size_t i = ((size_t)r * K + kvh) * H + h;
+                float x = (float)bf16_to_double(src[i]);
+                dst[i] = oracle_e4m3_encode(x / scale[kvh]);
+            }
+}
+
+void oracle_append_fp8(const uint16_t *k_new, const uint16_t *v_new, const float *k_scale,
+                       const float *v_scale, const int64_t *slots, int32_t T, uint8_t *k_cache,
+                       uint8_t *v_cache, int32_t K, int32_t H)
+{
+    size_t row = (size_t)K * (size_t)H;
+    for (int32_t i = 0; i < T; ++i) {
+        if (slots[i] < 0) continue;
+        oracle_quantize_fp8(k_new + (size_t)i * row, 1, K, H, k_scale, k_cache + (size_t)slots[i] * row);
+        oracle_quantize_fp8(v_new + (size_t)i * row, 1, K, H, v_scale, v_cache + (size_t)slots[i] * row);
+    }
+}
+
+void oracle_decode_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                       const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                       int32_t max_nb, const int32_t *context_lens, int32_t B, int32_t N, int32_t K,
+                       int32_t H, int32_t bs, double scale, double *out, double *lse, int nthreads)
+{
+    decode_job j = {q, 0, 0, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, max_nb,
+                    B, N, K, H, bs, scale, 0, 1, out, lse, nthreads, 0};
+    run_decode(j);
 }

@@ -262,8 +262,96 @@ def check_gather_inverts_scatter(orc):
     assert np.array_equal(ko, np.concatenate(ks)) and np.array_equal(vo, np.concatenate(vs))
 
 
+# ---------------------------------------- FP8 -------------------------------------------
+def check_e4m3_decode_table(orc):
+    """Values the E4M3 format definition fixes (OCP 8-bit floating point, E4M3)."""
+    t = orc.e4m3_decode_table()
+    fixed = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+             0x39: 1.125, 0x3F: 1.875, 0x40: 2.0, 0x7E: 448.0, 0x77: 240.0, 0x80: -0.0,
+             0xB8: -1.0, 0xFE: -448.0}
+    for c, v in fixed.items():
+        assert t[c] == v and np.signbit(t[c]) == np.signbit(v), (hex(c), t[c], v)
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    finite = t[np.isfinite(t)]
+    assert finite.size == 254 and len(set(finite[finite > 0].tolist())) == 126
+
+
+def check_e4m3_encode_nearest_even(orc):
+    """Brute force: the code of x is the nearest finite e4m3 value, ties to the even code."""
+    t = orc.e4m3_decode_table()
+    codes = [c for c in range(256) if np.isfinite(t[c])]
+    rng = np.random.default_rng(9)
+    xs = np.concatenate([rng.normal(0, 1, 400), rng.normal(0, 100, 200), rng.uniform(-520, 520, 200),
+                         [464.0, -470.0, 479.9, 1000.0, -1e30],                # beyond the largest code
+                         rng.uniform(-2.0 ** -6, 2.0 ** -6, 200),
+                         [(t[c] + t[c + 1]) / 2 for c in range(0x00, 0x7D)]])   # exact midpoints
+    for x in xs.astype(np.float32):
+        got = orc.e4m3_encode(float(x))
+        if abs(x) >= 448:
+            assert t[got] == np.copysign(448.0, x), (x, hex(got))
+            continue
+        d = [abs(t[c] - float(x)) for c in codes]
+        best = min(d)
+        cands = [c for c, dc in zip(codes, d) if dc == best]
+        if len(cands) > 1:                       # a tie: the even code (zero: keep the sign)
+            cands = [c for c in cands if c & 1 == 0] or cands
+            if float(x) == 0.0:
+                cands = [0x80 if np.signbit(x) else 0x00]
+        assert got in cands, (float(x), hex(got), [hex(c) for c in cands])
+    for c in codes:                              # representable values encode to themselves
+        assert t[orc.e4m3_encode(float(t[c]))] == t[c]
+
+
+def check_fp8_attention_is_dequantized_attention(orc):
+    """decode_fp8 == the bf16-path oracle's definition on the dequantized K/V (torch SDPA)."""
+    q, ks, vs = random_case(95, 8, 2, 128, [1, 17, 70])
+    k_scale = np.array([0.011, 0.013], dtype=np.float32)     # 448 * scale > every |value| here
+    v_scale = np.array([0.013, 0.0125], dtype=np.float32)
+    k8 = [orc.quantize_fp8(k, k_scale) for k in ks]
+    v8 = [orc.quantize_fp8(v, v_scale) for v in vs]
+    kc, vc, tables, ctx = paged_from_contiguous(ks, vs, 10)
+    kc8 = orc.quantize_fp8(kc, k_scale)
+    vc8 = orc.quantize_fp8(vc, v_scale)
+    out, lse = orc.decode_fp8(q, kc8, vc8, k_scale, v_scale, tables, ctx, 1 / math.sqrt(128))
+    t = orc.e4m3_decode_table()
+    import torch
+    for b in range(3):
+        kd = (t[k8[b]] * k_scale[None, :, None]).astype(np.float64)      # [ctx, K, H]
+        vd = (t[v8[b]] * v_scale[None, :, None]).astype(np.float64)
+        qt = torch.from_numpy(to_f64(q[b])).reshape(1, 8, 1, 128)
+        kt = torch.from_numpy(kd).permute(1, 0, 2).unsqueeze(0).repeat_interleave(4, dim=1)
+        vt = torch.from_numpy(vd).permute(1, 0, 2).unsqueeze(0).repeat_interleave(4, dim=1)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=1 / math.sqrt(128))
+        assert np.max(np.abs(out[b] - ref.reshape(8, 128).numpy())) < 1e-12
+    # context 1: the output is that token's dequantized V, within e4m3 rounding of the bf16 V
+    # (half a unit of the 3-bit mantissa: 2^-4 relative, or half the subnormal step 2^-10 * scale)
+    v0 = to_f64(vs[0][0])                                        # [K, H]
+    for n in range(8):
+        kvh = n // 4
+        bound = np.maximum(np.abs(v0[kvh]) * 2.0 ** -4, 2.0 ** -10 * float(v_scale[kvh])) * (1 + 1e-6)
+        assert np.all(np.abs(out[0, n] - v0[kvh]) <= bound)
+
+
+def check_fp8_append_roundtrip(orc):
+    w = gen.make_config("tiny")
+    k_scale = np.array([0.01, 0.02], dtype=np.float32)
+    v_scale = np.array([0.015, 0.005], dtype=np.float32)
+    kc8 = orc.quantize_fp8(w.k_cache, k_scale)
+    vc8 = orc.quantize_fp8(w.v_cache, v_scale)
+    slots = orc.slot_mapping(w.block_tables, w.context_lens)
+    before_k = kc8.copy()
+    orc.append_fp8(w.k_new, w.v_new, k_scale, v_scale, slots, kc8, vc8)
+    for b, s_ in enumerate(slots.tolist()):
+        assert np.array_equal(kc8[s_ // 16, s_ % 16], orc.quantize_fp8(w.k_new[b:b + 1], k_scale)[0])
+        assert np.array_equal(vc8[s_ // 16, s_ % 16], orc.quantize_fp8(w.v_new[b:b + 1], v_scale)[0])
+    changed = np.any(kc8 != before_k, axis=(2, 3))
+    assert sorted(map(tuple, np.argwhere(changed))) == sorted((s_ // 16, s_ % 16) for s_ in slots.tolist())
+
+
 ALL_CHECKS = [check_kv_bytes_golden, check_paged_equals_contiguous,
               check_block_permutation_invariance, check_ctx1_returns_v, check_constant_v,
               check_zero_query_is_uniform_mean, check_brute_force_mpmath, check_large_logits,
               check_partitions_merge_to_unsplit, check_ctx0, check_slot_mapping,
-              check_append_gather_roundtrip, check_gather_inverts_scatter]
+              check_append_gather_roundtrip, check_gather_inverts_scatter,
+              check_e4m3_decode_table, check_e4m3_encode_nearest_even,
+              check_fp8_attention_is_dequantized_attention, check_fp8_append_roundtrip]

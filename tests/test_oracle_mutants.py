@@ -37,6 +37,13 @@ MUTANTS = {
     "partition_drops_token": [("int64_t t1 = t0 + j->partition_tokens;",
                                "int64_t t1 = t0 + j->partition_tokens - 1;")],
     "kv_bytes_factor": [("return 2u * (uint64_t)layers", "return 1u * (uint64_t)layers")],
+    "e4m3_bias": [("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)")],
+    "e4m3_round_half_up": [("double r = nearbyint(a / quantum);", "double r = floor(a / quantum + 0.5);")],
+    "e4m3_no_saturation": [("if (a >= 448.0) return (uint8_t)(sign | 0x7E);", "if (a >= 480.0) return (uint8_t)(sign | 0x7E);")],
+    "e4m3_subnormal_quantum": [("const double quantum = ldexp(1.0, e - 3);", "const double quantum = ldexp(1.0, e - 3 + (e == -6));")],
+    "fp8_scale_multiplies": [("dst[i] = oracle_e4m3_encode(x / scale[kvh]);", "dst[i] = oracle_e4m3_encode(x * scale[kvh]);")],
+    "fp8_v_scale_for_k": [("keys[t * H + h] = oracle_e4m3_decode(j->k8[row + h]) * (double)j->k_scale[kvh];",
+                           "keys[t * H + h] = oracle_e4m3_decode(j->k8[row + h]) * (double)j->v_scale[kvh];")],
     "weights_not_normalised": [("for (int64_t t = 0; t < ntok; ++t) scores[t] /= sum;",
                                 "for (int64_t t = 0; t < ntok; ++t) scores[t] /= (double)ntok;")],
 }
