@@ -74,14 +74,25 @@ def recorded_traffic(config: str):
     return None
 
 
-def step_bytes(w) -> dict:
-    """Algorithmic bytes of one step (what the method must move, padding not counted)."""
+def step_bytes(w, kv: str = "bf16") -> dict:
+    """Algorithmic bytes of one step (what the method must move, padding not counted).
+
+    With an e4m3 cache the K/V history is one byte per element (half the bf16 bytes), the
+    append reads the new bf16 rows and writes one-byte codes, and attention also reads the
+    2 x K per-head scales."""
     tables = int(sum(-(-int(c) // 16) for c in w.context_lens)) * 4
-    attn = w.kv_bytes() + w.qo_bytes()
     meta = w.B * 4 + tables + w.B * 8 * 2          # context lens, table entries, slots (write+read)
-    return {"attn": attn, "attn_unique": w.unique_kv_bytes() + w.qo_bytes(),
-            "append": w.append_bytes(), "meta": meta,
-            "step": attn + w.append_bytes() + meta}
+    if kv == "fp8":
+        scales = 2 * w.K * 4
+        attn = w.kv_bytes() // 2 + w.qo_bytes() + scales
+        attn_unique = w.unique_kv_bytes() // 2 + w.qo_bytes() + scales
+        append = w.append_bytes() * 3 // 4
+    else:
+        attn = w.kv_bytes() + w.qo_bytes()
+        attn_unique = w.unique_kv_bytes() + w.qo_bytes()
+        append = w.append_bytes()
+    return {"attn": attn, "attn_unique": attn_unique, "append": append, "meta": meta,
+            "step": attn + append + meta}
 
 
 class ClockSampler:
@@ -248,7 +259,7 @@ def run_ours(args):
     build_library()
     import paged_kv_decode_slot_gb300 as pkv
     from paged_kv_decode_slot_gb300 import inputs as gen
-    from paged_kv_decode_slot_gb300.step import DecodeStep, plan_attention
+    from paged_kv_decode_slot_gb300.step import DecodeStep, DecodeStepFp8, plan_attention
 
     w = gen.make_config(args.config)
     dev = torch.device("cuda", local)
@@ -267,8 +278,25 @@ def run_ours(args):
     plan = plan_attention(w.B, w.K, w.max_blocks, sms, partition_blocks=args.partition_blocks)
     if args.mode and args.partition_blocks is None:
         plan = plan_attention(w.B, w.K, w.max_blocks, sms, mode=args.mode)
-    step = DecodeStep(q, kn, vn, kc, vc, bt, cl, w.scale, plan=plan, err_flag=err,
-                      fused=not args.unfused)
+    if args.kv == "fp8":
+        if args.unfused or plan.mode == "balanced":
+            raise SystemExit("--kv fp8 runs the fused single-pass or split step only")
+        # per-KV-head scales from the cache's own absolute maxima (NaN tail poison ignored)
+        def head_scale(c):
+            amax = torch.nan_to_num(c.float(), nan=0.0).abs().amax(dim=(0, 1, 3))
+            return (torch.where(amax > 0, amax, torch.ones_like(amax)) / 448.0).contiguous()
+        ks, vs = head_scale(kc), head_scale(vc)
+        kc8 = torch.empty(kc.shape, dtype=torch.uint8, device=dev)
+        vc8 = torch.empty(vc.shape, dtype=torch.uint8, device=dev)
+        pkv.check(pkv.pkv_quantize_fp8(kc, ks, kc8))
+        pkv.check(pkv.pkv_quantize_fp8(vc, vs, vc8))
+        del kc, vc
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        step = DecodeStepFp8(q, kn, vn, kc8, vc8, ks, vs, bt, cl, w.scale, plan=plan, err_flag=err)
+    else:
+        step = DecodeStep(q, kn, vn, kc, vc, bt, cl, w.scale, plan=plan, err_flag=err,
+                          fused=not args.unfused)
     stream = torch.cuda.Stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.zeros(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
@@ -281,7 +309,7 @@ def run_ours(args):
         # timed step starts with an L2 that holds neither its inputs nor write-back debt.
         flush_w.add_(1.0)
         torch.sum(flush_r, dim=0, keepdim=True, out=flush_sink)
-    nbytes = step_bytes(w)
+    nbytes = step_bytes(w, args.kv)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -401,7 +429,9 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": mean_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if args.kv == "bf16" else "e4m3 KV (f16 mma, fp32 softmax)",
+        "data": "synthetic (seeded)",
         "config": config_dict(w, "flushed between steps: write of one 2x-L2 buffer, then read of another, outside the timed events", plan),
         "us_per_step": mean_step * 1e3,
         "attn_us": mean_attn * 1e3,
@@ -410,12 +440,13 @@ def run_ours(args):
         "frac_of_8tbs": achieved / (NORTH_STAR_TBS * 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "kernel": {"single": "attn_kernel<128,0>",
-                                "split": "attn_kernel<128,1> + lse_merge_kernel",
+                     "kernel": {"single": "attn_kernel<128,0,%d>",
+                                "split": "attn_kernel<128,1,%d> + lse_merge_kernel",
                                 "balanced": "attn_balanced_kernel + balanced_merge_kernel"}[plan.mode]
+                               .replace("%d", "1" if args.kv == "fp8" else "0")
                                + (" (append fused)" if step.fused else ""),
                      "bytes_per_launch": attn_bytes,
-                     "traffic": recorded_traffic(args.config)},
+                     "traffic": recorded_traffic(args.config + ("" if args.kv == "bf16" else "+fp8"))},
         "e2e": {"value": ws * nbytes["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "graph": {"us_per_step": graph_ms * 1e3,
@@ -427,6 +458,10 @@ def run_ours(args):
         "wall_s_timed_region": t_wall,
         "step_bytes": nbytes["step"],
     }
+    if args.kv == "fp8":
+        line["config"]["kv_cache"] = "e4m3, per-KV-head scales (amax / 448)"
+        line["kv_gbs"] = w.kv_bytes() / 2 / (mean_attn * 1e-3) / 1e9
+        line["kv_gbs_bf16_equivalent"] = w.kv_bytes() / (mean_attn * 1e-3) / 1e9
     if w.unique_tokens is not None:
         line["kv_gbs_logical"] = w.kv_bytes() / (mean_attn * 1e-3) / 1e9
     if rank == 0 and not args.no_cpu_baseline:
@@ -448,6 +483,8 @@ def main():
     ap.add_argument("--mode", choices=("single", "balanced", "split"), default=None,
                     help="force an attention mode (split needs --partition-blocks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv", choices=("bf16", "fp8"), default="bf16",
+                    help="KV cache element type (fp8 = e4m3 codes with per-KV-head scales)")
     ap.add_argument("--unfused", action="store_true",
                     help="separate slot-mapping, append and attention launches")
     args = ap.parse_args()

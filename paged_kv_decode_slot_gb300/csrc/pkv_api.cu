@@ -385,6 +385,173 @@ PKV_EXPORT int pkv_decode_step(const pkv_bf16 *q, const pkv_bf16 *k_new, const p
                          max_partitions, partition_blocks, out, lse_out, stream);
 }
 
+// ---- FP8 (e4m3) pools with per-KV-head scales --------------------------------------------
+namespace {
+
+// e4m3 pool [num_blocks][16][K][H] bytes, H = 128: dims (h, head, token, block) with monotone
+// strides; the box is one (block, head) tile, 16 rows of 128 bytes, 128B-swizzled.
+int make_kv_maps_fp8(CUtensorMap *tk, CUtensorMap *tv, const void *k, const void *v,
+                     const pkv_cache_desc &d)
+{
+    if (!encode_fn()) {
+        g_last_error = "cuTensorMapEncodeTiled is unavailable from the driver";
+        return PKV_ERR_CUDA;
+    }
+    const cuuint64_t H = (cuuint64_t)d.head_dim, K = (cuuint64_t)d.num_kv_heads;
+    const cuuint64_t dims[4] = {H, K, 16, (cuuint64_t)d.num_blocks};
+    const cuuint64_t strides[3] = {H, K * H, 16 * K * H};
+    const cuuint32_t box[4] = {(cuuint32_t)H, 1, 16, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    for (int t = 0; t < 2; ++t) {
+        CUresult r = encode_fn()(t ? tv : tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                                 const_cast<void *>(t ? v : k), dims, strides, box, es,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            g_last_error = "cuTensorMapEncodeTiled failed for the e4m3 pool (CUresult " +
+                           std::to_string((int)r) + ")";
+            return PKV_ERR_CUDA;
+        }
+    }
+    return PKV_OK;
+}
+
+int check_fp8_desc(const pkv_cache_desc &d)
+{
+    if (d.block_size != 16) return PKV_ERR_UNSUPPORTED;
+    if (d.num_blocks <= 0 || d.num_kv_heads <= 0) return PKV_ERR_SHAPE;
+    if (d.head_dim != 128) return PKV_ERR_UNSUPPORTED;  // one 128-byte swizzle row per token
+    return PKV_OK;
+}
+
+int fp8_attention(const AttnArgs &a, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                  const float *k_scale, const float *v_scale, pkv_bf16 *out, float *lse_out,
+                  int64_t *slot_out, int32_t partition_blocks, int32_t max_partitions,
+                  void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    if (!out || !k_scale || !v_scale) return PKV_ERR_NULL;
+    if (!a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens) return PKV_ERR_NULL;
+    if (a.B < 0 || a.max_nb <= 0 || a.N <= 0) return PKV_ERR_SHAPE;
+    int st = check_fp8_desc(a.d);
+    if (st != PKV_OK) return st;
+    if (a.N % a.d.num_kv_heads != 0) return PKV_ERR_SHAPE;
+    const int G = a.N / a.d.num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
+    if (a.B > 65535 || a.d.num_kv_heads > 65535 || (int64_t)a.max_nb * 16 > INT32_MAX)
+        return PKV_ERR_SHAPE;
+    if (!aligned(a.k_cache, 16) || !aligned(a.v_cache, 16) || !aligned(a.q, 8) || !aligned(out, 4) ||
+        !aligned(lse_out, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(k_new, 16) ||
+        !aligned(v_new, 16) || !aligned(slot_out, 8))
+        return PKV_ERR_ALIGN;
+    const bool split = partition_blocks > 0;
+    float *part_out = nullptr, *part_lse = nullptr;
+    if (split) {
+        if (max_partitions <= 0 || (int64_t)max_partitions * partition_blocks < a.max_nb)
+            return PKV_ERR_SHAPE;
+        if (!workspace ||
+            workspace_bytes < pkv_splitk_workspace_bytes(a.B, a.N, a.d.head_dim, max_partitions))
+            return PKV_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
+        part_out = static_cast<float *>(workspace);
+        part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                             splitk_lse_offset(a.B, a.N, a.d.head_dim, max_partitions));
+    } else if (partition_blocks < 0) {
+        return PKV_ERR_SHAPE;
+    }
+    if (a.B == 0) return PKV_OK;
+    CUtensorMap tk, tv;
+    st = make_kv_maps_fp8(&tk, &tv, a.k_cache, a.v_cache, a.d);
+    if (st != PKV_OK) return st;
+    pkv::AttnParams p = params_of(a, 0);
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.lse_out = lse_out;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache_w = const_cast<pkv_bf16 *>(a.k_cache);
+    p.v_cache_w = const_cast<pkv_bf16 *>(a.v_cache);
+    p.slot_out = slot_out;
+    if (split) {
+        p.part_blocks = partition_blocks;
+        p.max_parts = max_partitions;
+        p.part_out = part_out;
+        p.part_lse = part_lse;
+    }
+    cudaError_t e = pkv::launch_attn(a.d.head_dim, split, tk, tv, p, stream, true);
+    if (e != cudaSuccess) return cuda_fail(e, "e4m3 attention launch");
+    if (!split) return PKV_OK;
+    return pkv_lse_merge(part_out, part_lse, a.context_lens, a.B, a.N, a.d.head_dim, max_partitions,
+                         partition_blocks, out, lse_out, stream);
+}
+
+}  // namespace
+
+PKV_EXPORT int pkv_quantize_fp8(const pkv_bf16 *src, int64_t rows, int32_t num_kv_heads,
+                                int32_t head_dim, const float *scale, uint8_t *dst,
+                                pkv_stream_t stream)
+{
+    if (!src || !scale || !dst) return PKV_ERR_NULL;
+    if (rows < 0 || num_kv_heads <= 0 || head_dim <= 0) return PKV_ERR_SHAPE;
+    if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(src, 16) || !aligned(dst, 8) || !aligned(scale, 4)) return PKV_ERR_ALIGN;
+    if (rows == 0) return PKV_OK;
+    cudaError_t e = pkv::launch_quantize_fp8(src, rows, num_kv_heads, head_dim, scale, dst, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "e4m3 quantize launch");
+}
+
+PKV_EXPORT int pkv_append_fp8(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const float *k_scale,
+                              const float *v_scale, const int64_t *slot_mapping, int32_t num_tokens,
+                              uint8_t *k_cache, uint8_t *v_cache, pkv_cache_desc cache,
+                              int32_t *err_flag, pkv_stream_t stream)
+{
+    if (!k_new || !v_new || !k_scale || !v_scale || !slot_mapping || !k_cache || !v_cache)
+        return PKV_ERR_NULL;
+    if (num_tokens < 0) return PKV_ERR_SHAPE;
+    int st = check_copy_desc(cache);
+    if (st != PKV_OK) return st;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 8) || !aligned(v_cache, 8))
+        return PKV_ERR_ALIGN;
+    if (num_tokens == 0) return PKV_OK;
+    cudaError_t e = pkv::launch_append_fp8(k_new, v_new, k_scale, v_scale, slot_mapping, num_tokens,
+                                           k_cache, v_cache, cache.num_blocks, cache.num_kv_heads,
+                                           cache.head_dim, err_flag, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "e4m3 append launch");
+}
+
+PKV_EXPORT int pkv_decode_attn_fp8(const pkv_bf16 *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                   const float *k_scale, const float *v_scale,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *context_lens, int32_t num_seqs,
+                                   int32_t num_q_heads, float scale, pkv_bf16 *out, float *lse_out,
+                                   pkv_cache_desc cache, int32_t partition_blocks,
+                                   int32_t max_partitions, void *workspace, size_t workspace_bytes,
+                                   int32_t *err_flag, pkv_stream_t stream)
+{
+    AttnArgs a{q, reinterpret_cast<const pkv_bf16 *>(k_cache), reinterpret_cast<const pkv_bf16 *>(v_cache),
+               block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale, cache,
+               err_flag};
+    return fp8_attention(a, nullptr, nullptr, k_scale, v_scale, out, lse_out, nullptr,
+                         partition_blocks, max_partitions, workspace, workspace_bytes, stream);
+}
+
+PKV_EXPORT int pkv_decode_step_fp8(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                                   uint8_t *k_cache, uint8_t *v_cache, const float *k_scale,
+                                   const float *v_scale, const int32_t *block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                   int32_t num_seqs, int32_t num_q_heads, float scale, pkv_bf16 *out,
+                                   float *lse_out, int64_t *slot_mapping_out, pkv_cache_desc cache,
+                                   int32_t partition_blocks, int32_t max_partitions, void *workspace,
+                                   size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream)
+{
+    if (!k_new || !v_new) return PKV_ERR_NULL;
+    AttnArgs a{q, reinterpret_cast<const pkv_bf16 *>(k_cache), reinterpret_cast<const pkv_bf16 *>(v_cache),
+               block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale, cache,
+               err_flag};
+    return fp8_attention(a, k_new, v_new, k_scale, v_scale, out, lse_out, slot_mapping_out,
+                         partition_blocks, max_partitions, workspace, workspace_bytes, stream);
+}
+
 // ---- balanced split (persistent grid, equal tile shares) -----------------------------------
 namespace {
 

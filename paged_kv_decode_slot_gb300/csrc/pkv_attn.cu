@@ -61,8 +61,13 @@ namespace pkv {
 #define PKV_BAL_PRODUCERS 2
 #endif
 
+#ifndef PKV_FP8_STAGES
+#define PKV_FP8_STAGES 16
+#endif
+
 constexpr int kConsumerWarps = 4;
 constexpr int kStages = PKV_STAGES;
+constexpr int kStagesFp8 = PKV_FP8_STAGES;  // e4m3 tiles are half the bytes: twice the depth
 constexpr int kProducers = PKV_PRODUCERS;
 constexpr int kAttnThreads = (kConsumerWarps + kProducers) * 32;
 constexpr int kBalStages = PKV_BAL_STAGES;
@@ -76,6 +81,8 @@ constexpr int kBalThreads = (kBalWarps + kBalProducers) * 32;
 static_assert(kStages % kConsumerWarps == 0, "pipeline depth must be a multiple of the consumer warps");
 static_assert(kBalStages % kBalWarps == 0, "pipeline depth must be a multiple of the consumer warps");
 static_assert(kStages % kProducers == 0, "pipeline depth must be a multiple of the producer warps");
+static_assert(kStagesFp8 % kConsumerWarps == 0 && kStagesFp8 % kProducers == 0,
+              "pipeline depth must be a multiple of the consumer and producer warps");
 static_assert(kBalStages % kBalProducers == 0, "pipeline depth must be a multiple of the producer warps");
 
 int balanced_ctas_per_sm() { return PKV_BAL_CTAS_PER_SM; }
@@ -84,10 +91,10 @@ int balanced_ctas_per_sm() { return PKV_BAL_CTAS_PER_SM; }
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int H, int S = kStages, int W = kConsumerWarps, int P = kProducers>
+template <int H, int S = kStages, int W = kConsumerWarps, int P = kProducers, int EB = 2>
 struct AttnLayout {
-    static constexpr int kHalves = H / 64;                  // 128-byte rows per token row
-    static constexpr int kTileBytes = kBlockSize * H * 2;   // one K or V tile
+    static constexpr int kHalves = H / 64;                  // 128-byte rows per bf16 token row
+    static constexpr int kTileBytes = kBlockSize * H * EB;  // one K or V tile (EB bytes/element)
     static constexpr int kStageBytes = 2 * kTileBytes;      // K tile then V tile
     static constexpr int kPipeBytes = S * kStageBytes;
     static constexpr int kMergeBytes = W * 8 * (H + 2) * 4;
@@ -106,7 +113,7 @@ struct AttnLayout {
     static int balanced_alloc(int B) { return kBalSeqOffset + (B + 1) * 8 + 1024; }
     static_assert(kBalMiscOffset % 8 == 0, "the balanced kernel's int64 counter needs 8-byte alignment");
     static_assert(kBalSeqOffset % 16 == 0 && kPipeBytes % 1024 == 0, "shared-memory layout alignment");
-    static_assert(kStageBytes % 1024 == 0, "TMA destinations with 128B swizzle need 1024-byte alignment");
+    static_assert(kTileBytes % 1024 == 0, "TMA destinations with 128B swizzle need 1024-byte alignment");
 };
 
 // Byte offset inside a TMA-written, 128B-swizzled tile of the 16-byte chunk holding
@@ -234,9 +241,136 @@ __device__ __forceinline__ void tile_update(WarpAcc<H> &a, const uint32_t (&qf)[
     }
 }
 
+// ------------------------------------ FP8 (e4m3) tiles ------------------------------------
+// An e4m3 tile is 16 token rows of H = 128 bytes (128B-swizzled).  ldmatrix reads it as b16
+// pairs and cvt widens pairs to f16 exactly, so the contractions run as f16 mma.sync.  Reading
+// b16 pairs permutes the head dimension inside each 16-element step; q (the other operand of
+// QK^T) is loaded in the same order, and in P.V the accumulator rows come out as
+// h = 16*mt + 2*(lane/4) (+1 for the upper 8 rows) instead of 16*mt + lane/4 (+8).
+__device__ __forceinline__ uint32_t fp8_chunk_offset(int tok, int chunk)
+{
+    return static_cast<uint32_t>(tok * 128 + ((chunk ^ (tok & 7)) << 4));
+}
+
+// q as f16 B fragments: k-step kk, lane (g = lane/4, m = lane%4): b0 = q[16kk + 4m .. +1],
+// b1 = q[16kk + 4m + 2 .. +3]; rows g >= G are zero.
+template <int H>
+__device__ __forceinline__ void load_q_frags_fp8(uint32_t (&qf)[H / 16][2], const uint16_t *q, int N,
+                                                 int b, int kvh, int G, int lane)
+{
+    const int g_row = lane >> 2, m = lane & 3;
+    const bool live = g_row < G;
+    const uint16_t *qrow = q + ((size_t)b * N + (size_t)kvh * G + (live ? g_row : 0)) * H;
+#pragma unroll
+    for (int kk = 0; kk < H / 16; ++kk) {
+        if (live) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(qrow + 16 * kk + 4 * m));
+            qf[kk][0] = pack_f16x2(bf16_to_f32((uint16_t)(v.x & 0xFFFFu)), bf16_to_f32((uint16_t)(v.x >> 16)));
+            qf[kk][1] = pack_f16x2(bf16_to_f32((uint16_t)(v.y & 0xFFFFu)), bf16_to_f32((uint16_t)(v.y >> 16)));
+        } else {
+            qf[kk][0] = qf[kk][1] = 0u;
+        }
+    }
+}
+
+// One 16-token e4m3 tile folded into a warp's state (the codes only; the per-head scales are
+// folded into sl2 and into the final normalisation).
+template <int H>
+__device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&qf)[H / 16][2],
+                                                uint32_t kt, uint32_t vt, int valid, float sl2, int lane)
+{
+    constexpr int kKSteps = H / 16;
+    const int mi = lane >> 3, ri = lane & 7;
+    const int tok = ri + 8 * (mi & 1), coff = mi >> 1;  // ldmatrix row address of this lane
+
+    // S^T = K . Q^T
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < kKSteps; kk += 2) {
+        uint32_t r[4];
+        ldsm_x4(r, kt + fp8_chunk_offset(tok, kk + coff));
+        uint32_t a0[4], a1[4];
+        a0[0] = e4m3x2_to_f16x2((uint16_t)(r[0] & 0xFFFFu));
+        a0[1] = e4m3x2_to_f16x2((uint16_t)(r[1] & 0xFFFFu));
+        a0[2] = e4m3x2_to_f16x2((uint16_t)(r[0] >> 16));
+        a0[3] = e4m3x2_to_f16x2((uint16_t)(r[1] >> 16));
+        a1[0] = e4m3x2_to_f16x2((uint16_t)(r[2] & 0xFFFFu));
+        a1[1] = e4m3x2_to_f16x2((uint16_t)(r[3] & 0xFFFFu));
+        a1[2] = e4m3x2_to_f16x2((uint16_t)(r[2] >> 16));
+        a1[3] = e4m3x2_to_f16x2((uint16_t)(r[3] >> 16));
+        mma_f16_16816(sa, a0, qf[kk][0], qf[kk][1]);
+        mma_f16_16816(sb, a1, qf[kk + 1][0], qf[kk + 1][1]);
+    }
+    const int t0 = lane >> 2, t1 = t0 + 8;
+    const float x0 = t0 < valid ? (sa[0] + sb[0]) * sl2 : -INFINITY;
+    const float x1 = t0 < valid ? (sa[1] + sb[1]) * sl2 : -INFINITY;
+    const float x2 = t1 < valid ? (sa[2] + sb[2]) * sl2 : -INFINITY;
+    const float x3 = t1 < valid ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+    float mA = fmaxf(x0, x2), mB = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mA = fmaxf(mA, __shfl_xor_sync(0xFFFFFFFFu, mA, off));
+        mB = fmaxf(mB, __shfl_xor_sync(0xFFFFFFFFu, mB, off));
+    }
+    const bool needA = mA > a.m[0] + kRescaleThreshold;
+    const bool needB = mB > a.m[1] + kRescaleThreshold;
+    if (__any_sync(0xFFFFFFFFu, needA || needB)) {
+        const float alphaA = needA ? exp2f(a.m[0] - mA) : 1.f;
+        const float alphaB = needB ? exp2f(a.m[1] - mB) : 1.f;
+        if (needA) a.m[0] = mA;
+        if (needB) a.m[1] = mB;
+        a.l[0] *= alphaA;
+        a.l[1] *= alphaB;
+#pragma unroll
+        for (int mt = 0; mt < kKSteps; ++mt) {
+            a.o[mt][0] *= alphaA;
+            a.o[mt][1] *= alphaB;
+            a.o[mt][2] *= alphaA;
+            a.o[mt][3] *= alphaB;
+        }
+    }
+    const uint32_t p01 = pack_f16x2(exp2f(x0 - a.m[0]), exp2f(x1 - a.m[1]));
+    const uint32_t p23 = pack_f16x2(exp2f(x2 - a.m[0]), exp2f(x3 - a.m[1]));
+    a.l[0] += f16x2_lo(p01) + f16x2_lo(p23);
+    a.l[1] += f16x2_hi(p01) + f16x2_hi(p23);
+    const uint32_t pb0 = movmatrix_trans(p01);
+    const uint32_t pb1 = movmatrix_trans(p23);
+
+    // O^T += V^T . P^T: ldmatrix.trans gives lane bytes (tok 2m, h 2c'), (tok 2m, h 2c'+1),
+    // (tok 2m+1, h 2c'), (tok 2m+1, h 2c'+1) with c' = lane/4; prmt regroups them per h.
+    const bool partial = valid < kBlockSize;
+    const int tc = (lane & 3) * 2;
+#pragma unroll
+    for (int mt = 0; mt < kKSteps; mt += 2) {
+        uint32_t r[4];
+        ldsm_x4_trans(r, vt + fp8_chunk_offset(tok, mt + coff));
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const uint32_t lo = byte_perm(r[2 * hf], 0u, 0x3120u);      // tokens 0-7 of the tile
+            const uint32_t hi = byte_perm(r[2 * hf + 1], 0u, 0x3120u);  // tokens 8-15
+            uint32_t av[4];
+            av[0] = e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu));
+            av[1] = e4m3x2_to_f16x2((uint16_t)(lo >> 16));
+            av[2] = e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu));
+            av[3] = e4m3x2_to_f16x2((uint16_t)(hi >> 16));
+            if (partial) {
+                const uint32_t lo0 = tc < valid ? 0x0000FFFFu : 0u;
+                const uint32_t hi0 = tc + 1 < valid ? 0xFFFF0000u : 0u;
+                const uint32_t lo1 = tc + 8 < valid ? 0x0000FFFFu : 0u;
+                const uint32_t hi1 = tc + 9 < valid ? 0xFFFF0000u : 0u;
+                av[0] &= lo0 | hi0;
+                av[1] &= lo0 | hi0;
+                av[2] &= lo1 | hi1;
+                av[3] &= lo1 | hi1;
+            }
+            mma_f16_16816(a.o[mt + hf], av, pb0, pb1);
+        }
+    }
+}
+
 // Finish a warp's sums (across the lanes that share a column) and store its state in the
 // merge area: mo[W][8][H], mm[W][8] (running max), ml[W][8] (running sum).
-template <int H>
+template <int H, bool kFp8 = false>
 __device__ __forceinline__ void deposit(WarpAcc<H> &a, float *mo, float *mm, float *ml, int warp,
                                         int lane)
 {
@@ -255,11 +389,13 @@ __device__ __forceinline__ void deposit(WarpAcc<H> &a, float *mo, float *mm, flo
     const int hr = lane >> 2;
 #pragma unroll
     for (int mt = 0; mt < H / 16; ++mt) {
-        const int h = 16 * mt + hr;
-        mo[(warp * 8 + c0) * H + h] = a.o[mt][0];
-        mo[(warp * 8 + c0 + 1) * H + h] = a.o[mt][1];
-        mo[(warp * 8 + c0) * H + h + 8] = a.o[mt][2];
-        mo[(warp * 8 + c0 + 1) * H + h + 8] = a.o[mt][3];
+        // rows of the accumulator: h0 for o[mt][0..1], h1 for o[mt][2..3]
+        const int h0 = kFp8 ? 16 * mt + 2 * hr : 16 * mt + hr;
+        const int h1 = kFp8 ? h0 + 1 : h0 + 8;
+        mo[(warp * 8 + c0) * H + h0] = a.o[mt][0];
+        mo[(warp * 8 + c0 + 1) * H + h0] = a.o[mt][1];
+        mo[(warp * 8 + c0) * H + h1] = a.o[mt][2];
+        mo[(warp * 8 + c0 + 1) * H + h1] = a.o[mt][3];
     }
 }
 
@@ -296,15 +432,16 @@ __device__ __forceinline__ void init_ring(uint32_t bar_full, uint32_t bar_empty)
 }
 
 // Producer side of one tile: wait for the stage to be free, then load the tile (or mark it
-// skipped).  Runs on one lane.  Returns false when the wait expired.
-template <int H, int S>
+// skipped).  Runs on one lane.  Returns false when the wait expired.  bf16 tiles come through
+// 5-D maps (half-major or token-major), e4m3 tiles through a 4-D map (h, head, token, block).
+template <int H, int S, bool kFp8 = false>
 __device__ __forceinline__ bool produce_tile(int64_t i, int kvh, int bid, bool ok, uint32_t base_u32,
                                              uint32_t bar_full, uint32_t bar_empty,
                                              volatile int *slot_ok, volatile int *abort_flag,
                                              const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                                              int tok_major, int32_t *err_flag)
 {
-    using L = AttnLayout<H, S>;
+    using L = AttnLayout<H, S, kConsumerWarps, kProducers, kFp8 ? 1 : 2>;
     const int s = (int)(i % S);
     if (i >= S &&
         !mbar_wait_bounded(bar_empty + 8 * s, (uint32_t)(((i / S) & 1) ^ 1), abort_flag,
@@ -316,13 +453,17 @@ __device__ __forceinline__ bool produce_tile(int64_t i, int kvh, int bid, bool o
     if (ok) {
         slot_ok[s] = 1;
         const uint32_t dst = base_u32 + s * L::kStageBytes;
-        mbar_arrive_expect_tx(bar_full + 8 * s, L::kStageBytes);
-        if (tok_major) {
-            tma_load_5d(dst, tm_k, bar_full + 8 * s, 0, 0, kvh, 0, bid);
-            tma_load_5d(dst + L::kTileBytes, tm_v, bar_full + 8 * s, 0, 0, kvh, 0, bid);
+        const uint32_t bar = bar_full + 8 * s;
+        mbar_arrive_expect_tx(bar, L::kStageBytes);
+        if (kFp8) {
+            tma_load_4d(dst, tm_k, bar, 0, kvh, 0, bid);
+            tma_load_4d(dst + L::kTileBytes, tm_v, bar, 0, kvh, 0, bid);
+        } else if (tok_major) {
+            tma_load_5d(dst, tm_k, bar, 0, 0, kvh, 0, bid);
+            tma_load_5d(dst + L::kTileBytes, tm_v, bar, 0, 0, kvh, 0, bid);
         } else {
-            tma_load_5d(dst, tm_k, bar_full + 8 * s, 0, 0, 0, kvh, bid);
-            tma_load_5d(dst + L::kTileBytes, tm_v, bar_full + 8 * s, 0, 0, 0, kvh, bid);
+            tma_load_5d(dst, tm_k, bar, 0, 0, 0, kvh, bid);
+            tma_load_5d(dst + L::kTileBytes, tm_v, bar, 0, 0, 0, kvh, bid);
         }
     } else {
         slot_ok[s] = 0;  // out-of-range block id: the tile is skipped
@@ -393,19 +534,54 @@ __device__ __forceinline__ void append_new_token(const AttnParams &p, int b, int
     const size_t row = ((size_t)b * p.K + kvh) * H + 8 * c;
     const uint4 v = __ldg(reinterpret_cast<const uint4 *>((is_v ? p.v_new : p.k_new) + row));
     st_shared_v4((is_v ? vt : kt) + tile_chunk_offset<H>(tok, 8 * c, p.tok_major), v);
-    uint16_t *dst = (is_v ? p.v_cache_w : p.k_cache_w) +
+    uint16_t *dst = static_cast<uint16_t *>(is_v ? p.v_cache_w : p.k_cache_w) +
                     (((size_t)bid * kBlockSize + tok) * p.K + kvh) * H + 8 * c;
     *reinterpret_cast<uint4 *>(dst) = v;
     fence_proxy_async_shared();
 }
 
+// The same for an e4m3 cache: the new token's bf16 K/V rows are quantized with the head's scale
+// (code = e4m3(x / scale), the division rounded to nearest) while being written.  Lanes
+// [0, H/16) handle the K row, [H/16, H/8) the V row, 16 codes each.
+template <int H>
+__device__ __forceinline__ void append_new_token_fp8(const AttnParams &p, int b, int kvh, int ctx,
+                                                     int bid, uint32_t kt, uint32_t vt, int lane)
+{
+    constexpr int kChunks = H / 16;
+    if (lane >= 2 * kChunks) return;
+    const int tok = (ctx - 1) % kBlockSize;
+    const bool is_v = lane >= kChunks;
+    const int c = is_v ? lane - kChunks : lane;
+    const float sc = (is_v ? p.v_scale : p.k_scale)[kvh];
+    const uint4 *src = reinterpret_cast<const uint4 *>((is_v ? p.v_new : p.k_new) +
+                                                        ((size_t)b * p.K + kvh) * H + 16 * c);
+    const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
+    auto q2 = [&](uint32_t pair) -> uint32_t {  // two bf16 -> two e4m3 codes (low first)
+        return f32x2_to_e4m3x2(__fdiv_rn(bf16_to_f32((uint16_t)(pair & 0xFFFFu)), sc),
+                               __fdiv_rn(bf16_to_f32((uint16_t)(pair >> 16)), sc));
+    };
+    uint4 v;
+    v.x = q2(x0.x) | (q2(x0.y) << 16);
+    v.y = q2(x0.z) | (q2(x0.w) << 16);
+    v.z = q2(x1.x) | (q2(x1.y) << 16);
+    v.w = q2(x1.z) | (q2(x1.w) << 16);
+    st_shared_v4((is_v ? vt : kt) + fp8_chunk_offset(tok, c), v);
+    uint8_t *dst = reinterpret_cast<uint8_t *>(is_v ? p.v_cache_w : p.k_cache_w) +
+                   (((size_t)bid * kBlockSize + tok) * p.K + kvh) * H + 16 * c;
+    *reinterpret_cast<uint4 *>(dst) = v;
+    fence_proxy_async_shared();
+}
+
 // ------------------------ single pass and fixed partitions --------------------------------
-template <int H, bool kSplit>
+// kFp8: the pools hold e4m3 codes with per-KV-head scales (H = 128); the K scale is folded into
+// the logit multiplier, the V scale into the final normalisation.
+template <int H, bool kSplit, bool kFp8 = false>
 __global__ void __launch_bounds__(kAttnThreads, PKV_CTAS_PER_SM)
 attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
             const AttnParams p)
 {
-    using L = AttnLayout<H>;
+    constexpr int S = kFp8 ? kStagesFp8 : kStages;
+    using L = AttnLayout<H, S, kConsumerWarps, kProducers, kFp8 ? 1 : 2>;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -447,15 +623,15 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     }
 
     const uint32_t bar_full = base_u32 + L::kBarOffset;
-    const uint32_t bar_empty = bar_full + 8 * kStages;
+    const uint32_t bar_empty = bar_full + 8 * S;
     volatile int *slot_ok = reinterpret_cast<volatile int *>(base + L::kMiscOffset);
-    volatile int *abort_flag = slot_ok + kStages;
+    volatile int *abort_flag = slot_ok + S;
     volatile int *issued_count = abort_flag + 1;  // [kProducers]
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int q = 0; q < kProducers; ++q) issued_count[q] = 0;
-        init_ring<kStages>(bar_full, bar_empty);
+        init_ring<S>(bar_full, bar_empty);
     }
     __syncthreads();
 
@@ -472,23 +648,28 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
         const int64_t issued = run_producer<kProducers>(
             pw, lane, nblk, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, p.err_flag,
             [&](int64_t i, int bid, bool ok) {
-                return produce_tile<H, kStages>(i, kvh, bid, ok, base_u32, bar_full, bar_empty, slot_ok,
-                                                abort_flag, &tm_k, &tm_v, p.tok_major, p.err_flag);
+                return produce_tile<H, S, kFp8>(i, kvh, bid, ok, base_u32, bar_full, bar_empty,
+                                                slot_ok, abort_flag, &tm_k, &tm_v, p.tok_major,
+                                                p.err_flag);
             });
         if (lane == 0) issued_count[pw] = (int)issued;
     } else {
         // ------------------------------ consumer warps ------------------------------
         uint32_t qf[H / 16][2];
-        load_q_frags<H>(qf, p.q, p.N, b, kvh, G, lane);
+        if constexpr (kFp8)
+            load_q_frags_fp8<H>(qf, p.q, p.N, b, kvh, G, lane);
+        else
+            load_q_frags<H>(qf, p.q, p.N, b, kvh, G, lane);
         acc_reset<H>(acc);
+        const float sl2 = kFp8 ? p.scale_log2 * p.k_scale[kvh] : p.scale_log2;
         // fused append: the warp that will hold the last block warms the new K/V rows in L2
         if (p.k_new && blk_end == nb && warp == (nb - 1 - blk_begin) % kConsumerWarps && lane < 2) {
             const size_t row = ((size_t)b * p.K + kvh) * H;
             prefetch_l2((lane ? p.v_new : p.k_new) + row);
         }
         for (int i = warp; i < nblk; i += kConsumerWarps) {
-            const int s = i % kStages;
-            if (!mbar_wait_bounded(bar_full + 8 * s, (i / kStages) & 1, abort_flag, kWaitLimitNs)) {
+            const int s = i % S;
+            if (!mbar_wait_bounded(bar_full + 8 * s, (i / S) & 1, abort_flag, kWaitLimitNs)) {
                 if (!*abort_flag) set_flag(p.err_flag, PKV_FLAG_TIMEOUT);
                 *abort_flag = 1;
                 break;
@@ -500,10 +681,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
                 const int valid = min(kBlockSize, ctx - (blk_begin + i) * kBlockSize);
                 const uint32_t kt = base_u32 + s * L::kStageBytes;
                 if (newest) {
-                    append_new_token<H>(p, b, kvh, ctx, last_bid, kt, kt + L::kTileBytes, lane);
+                    if constexpr (kFp8)
+                        append_new_token_fp8<H>(p, b, kvh, ctx, last_bid, kt, kt + L::kTileBytes, lane);
+                    else
+                        append_new_token<H>(p, b, kvh, ctx, last_bid, kt, kt + L::kTileBytes, lane);
                     __syncwarp();
                 }
-                tile_update<H>(acc, qf, kt, kt + L::kTileBytes, valid, p.scale_log2, p.tok_major, lane);
+                if constexpr (kFp8)
+                    tile_update_fp8<H>(acc, qf, kt, kt + L::kTileBytes, valid, sl2, lane);
+                else
+                    tile_update<H>(acc, qf, kt, kt + L::kTileBytes, valid, sl2, p.tok_major, lane);
             }
             if (newest && p.slot_out && kvh == 0 && lane == 0)
                 p.slot_out[b] = slot_ok[s] ? (int64_t)last_bid * kBlockSize + (ctx - 1) % kBlockSize : -1;
@@ -515,7 +702,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     __syncthreads();
     if (*abort_flag) {
         if (warp >= kConsumerWarps && lane == 0)
-            drain_ring<kStages, kProducers>(bar_full, warp - kConsumerWarps,
+            drain_ring<S, kProducers>(bar_full, warp - kConsumerWarps,
                                             issued_count[warp - kConsumerWarps]);
         __syncthreads();
         return;
@@ -525,12 +712,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     float *mo = reinterpret_cast<float *>(base);              // [W][8][H]
     float *mm = mo + kConsumerWarps * 8 * H;                 // [W][8]
     float *ml = mm + kConsumerWarps * 8;                     // [W][8]
-    if (warp < kConsumerWarps) deposit<H>(acc, mo, mm, ml, warp, lane);
+    if (warp < kConsumerWarps) deposit<H, kFp8>(acc, mo, mm, ml, warp, lane);
     __syncthreads();
+    const float vscale = kFp8 ? p.v_scale[kvh] : 1.f;
     for (int idx = threadIdx.x; idx < G * H; idx += kAttnThreads) {
         const int g = idx / H, h = idx - g * H;
         float val, lse;
         combine<H>(mo, mm, ml, g, h, val, lse);
+        val *= vscale;
         const size_t bn = (size_t)b * p.N + (size_t)kvh * G + g;
         if (kSplit) {
             const size_t bnp = bn * p.max_parts + part;
@@ -859,27 +1048,31 @@ static cudaError_t ensure_smem(Kern kern, int smem, int *cached)
     return e;
 }
 
-template <int H, bool kSplit>
+template <int H, bool kSplit, bool kFp8>
 static cudaError_t launch_attn_t(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
                                  dim3 grid, cudaStream_t stream)
 {
-    constexpr int smem = AttnLayout<H, kStages>::kAlloc;
+    constexpr int smem = AttnLayout<H, kFp8 ? kStagesFp8 : kStages, kConsumerWarps, kProducers,
+                                    kFp8 ? 1 : 2>::kAlloc;
     static int cached[64] = {};
-    cudaError_t e = ensure_smem(attn_kernel<H, kSplit>, smem, cached);
+    cudaError_t e = ensure_smem(attn_kernel<H, kSplit, kFp8>, smem, cached);
     if (e != cudaSuccess) return e;
-    attn_kernel<H, kSplit><<<grid, kAttnThreads, smem, stream>>>(tk, tv, p);
+    attn_kernel<H, kSplit, kFp8><<<grid, kAttnThreads, smem, stream>>>(tk, tv, p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const AttnParams &p, cudaStream_t stream)
+                        const AttnParams &p, cudaStream_t stream, bool fp8)
 {
     dim3 grid = split ? dim3(p.K, p.B, p.max_parts) : dim3(p.K, p.B, 1);
+    if (fp8)  // e4m3 pools: H = 128 only
+        return split ? launch_attn_t<128, true, true>(tk, tv, p, grid, stream)
+                     : launch_attn_t<128, false, true>(tk, tv, p, grid, stream);
     if (H == 128)
-        return split ? launch_attn_t<128, true>(tk, tv, p, grid, stream)
-                     : launch_attn_t<128, false>(tk, tv, p, grid, stream);
-    return split ? launch_attn_t<64, true>(tk, tv, p, grid, stream)
-                 : launch_attn_t<64, false>(tk, tv, p, grid, stream);
+        return split ? launch_attn_t<128, true, false>(tk, tv, p, grid, stream)
+                     : launch_attn_t<128, false, false>(tk, tv, p, grid, stream);
+    return split ? launch_attn_t<64, true, false>(tk, tv, p, grid, stream)
+                 : launch_attn_t<64, false, false>(tk, tv, p, grid, stream);
 }
 
 template <int H>

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -124,6 +125,70 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
         : "memory");
 }
+
+// 4-D tiled bulk tensor copy global -> this CTA's shared memory (see tma_load_5d).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// ---- FP8 (e4m3) <-> f16 / f32 -----------------------------------------------------------
+// Two e4m3 codes (low byte first) -> f16x2 (low half first).  Exact: every e4m3 value is an
+// f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes)
+{
+    uint32_t out;
+    asm volatile("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(codes));
+    return out;
+}
+
+// Two floats -> two e4m3 codes, round to nearest even, saturating at +-448 (lo in the low byte).
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi)
+{
+    uint16_t out;
+    asm volatile("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(hi), "f"(lo));
+    return out;
+}
+
+// Select bytes of (a, b) into a 32-bit value (PTX prmt; selector nibble i picks byte i).
+__device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float f16x2_lo(uint32_t v)
+{
+    return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16x2_hi(uint32_t v)
+{
+    return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
 
 // ---- warp-level bf16 MMA (m16n8k16, fp32 accumulate) -----------------------------------
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)

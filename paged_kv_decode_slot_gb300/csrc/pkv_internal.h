@@ -33,14 +33,24 @@ struct AttnParams {
     // fused decode step (single pass / partitions): append the new token while attending
     const uint16_t *k_new;         // [B][K][H], nullable: no append
     const uint16_t *v_new;
-    uint16_t *k_cache_w;           // the pools, written at each sequence's newest slot
-    uint16_t *v_cache_w;
+    void *k_cache_w;               // the pools (bf16 or e4m3), written at the newest slot
+    void *v_cache_w;
+    const float *k_scale;          // e4m3 pools: per-KV-head scales [K] (value = code * scale)
+    const float *v_scale;
     int64_t *slot_out;             // [B] slot of the newest token (-1 none), nullable
     int32_t *err_flag;             // nullable
 };
 
 cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const AttnParams &p, cudaStream_t stream);
+                        const AttnParams &p, cudaStream_t stream, bool fp8 = false);
+
+cudaError_t launch_quantize_fp8(const uint16_t *src, int64_t rows, int K, int H, const float *scale,
+                                uint8_t *dst, cudaStream_t stream);
+
+cudaError_t launch_append_fp8(const uint16_t *k_new, const uint16_t *v_new, const float *k_scale,
+                              const float *v_scale, const int64_t *slots, int T, uint8_t *k_cache,
+                              uint8_t *v_cache, int num_blocks, int K, int H, int32_t *err_flag,
+                              cudaStream_t stream);
 
 // CTAs per SM of the balanced kernel's persistent grid (a compile-time choice).
 int balanced_ctas_per_sm();

@@ -138,3 +138,43 @@ class DecodeStep:
     def launches_per_step(self) -> int:
         attn = 2 if self.plan.split else 1
         return attn if self.fused else 2 + attn
+
+
+class DecodeStepFp8:
+    """A decode step over e4m3 pools with per-KV-head scales: one ``pkv_decode_step_fp8`` call
+    (single pass or fixed partitions, as ``plan_attention`` picks; never the balanced path)."""
+
+    def __init__(self, q, k_new, v_new, k_cache8, v_cache8, k_scale, v_scale, block_tables,
+                 context_lens, scale, plan: AttentionPlan | None = None, err_flag=None):
+        self.q, self.k_new, self.v_new = q, k_new, v_new
+        self.k_cache, self.v_cache = k_cache8, v_cache8
+        self.k_scale, self.v_scale = k_scale, v_scale
+        self.block_tables, self.context_lens = block_tables, context_lens
+        self.scale = float(scale)
+        dev = q.device
+        nseq = q.shape[0]
+        if plan is None or plan.mode == "balanced":
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            plan = plan_attention(nseq, k_cache8.shape[2], block_tables.shape[1], sms)
+        self.plan = plan
+        self.fused = True
+        self.slot_mapping = torch.empty(nseq, dtype=torch.int64, device=dev)
+        self.out = torch.empty_like(q)
+        self.lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev)
+        self.err_flag = err_flag
+        self.workspace = None
+        if plan.mode == "split":
+            nbytes = B.pkv_splitk_workspace_bytes(nseq, q.shape[1], q.shape[2], plan.max_partitions)
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def run(self, stream=None) -> None:
+        split = self.plan.mode == "split"
+        B.check(B.pkv_decode_step_fp8(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
+                                      self.k_scale, self.v_scale, self.block_tables, self.context_lens,
+                                      self.scale, self.out, self.lse, self.slot_mapping,
+                                      self.plan.partition_blocks if split else 0,
+                                      self.plan.max_partitions if split else 0, self.workspace,
+                                      self.err_flag, stream))
+
+    def launches_per_step(self) -> int:
+        return 2 if self.plan.mode == "split" else 1
