@@ -63,6 +63,10 @@ class Oracle:
         lib.oracle_decode_partitions.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                                  _I32, _D, _I32, _I32, _P, _P, ctypes.c_int]
         lib.oracle_lse_merge.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _P, _P]
+        lib.oracle_slot_mapping_multi.argtypes = [_P, _I32, _P, _I32, _I32, _I32, _P]
+        lib.oracle_decode_multi.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32, _I32,
+                                            _I32, _D, _P, _P, ctypes.c_int]
+        lib.oracle_copy_blocks.argtypes = [_P, _P, _P, _I32, _I64]
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
@@ -150,6 +154,42 @@ class Oracle:
         self.lib.oracle_lse_merge(_ptr(po), _ptr(pl), B, N, H, P, _ptr(out), _ptr(lse))
         return out, lse
 
+
+    # -- several query tokens per sequence -----------------------------------------------
+    def slot_mapping_multi(self, block_tables, context_lens, T, bs=16) -> np.ndarray:
+        """Slots [B, T] of the last T logical positions of each sequence (-1 below position 0)."""
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        out = np.empty((cl.shape[0], T), dtype=np.int64)
+        self.lib.oracle_slot_mapping_multi(_ptr(bt), bt.shape[1], _ptr(cl), cl.shape[0], T, bs,
+                                           _ptr(out))
+        return out
+
+    def decode_multi(self, q, k_cache, v_cache, block_tables, context_lens, scale, bs=16, threads=0):
+        """q [B, T, N, H] bf16 bits; query token t attends to tokens [0, ctx - T + t]."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        kc = np.ascontiguousarray(k_cache, dtype=np.uint16)
+        vc = np.ascontiguousarray(v_cache, dtype=np.uint16)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        B, T, N, H = q.shape
+        K = kc.shape[2]
+        out = np.empty((B, T, N, H), dtype=np.float64)
+        lse = np.empty((B, T, N), dtype=np.float64)
+        self.lib.oracle_decode_multi(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cl),
+                                     B, T, N, K, H, bs, float(scale), _ptr(out), _ptr(lse), threads)
+        return out, lse
+
+    # -- copy-on-write -----------------------------------------------------------------
+    def copy_blocks(self, k_cache, v_cache, src_dst):
+        """In place: block dst of both pools becomes a copy of block src, pair by pair."""
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        assert k_cache.shape == v_cache.shape and k_cache.dtype == v_cache.dtype
+        pairs = np.ascontiguousarray(src_dst, dtype=np.int32).reshape(-1, 2)
+        block_bytes = k_cache[0].nbytes
+        self.lib.oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), pairs.shape[0],
+                                    block_bytes)
+        return k_cache, v_cache
 
     # -- FP8 (e4m3) cache --------------------------------------------------------------
     def e4m3_encode(self, x: float) -> int:

@@ -25,6 +25,15 @@
  *    at T = 1).
  *  - GQA: each KV head serves N/K query heads (CS336 Lecture 10 notes,
  *    "分组查询注意力"); query head n uses KV head n / (N/K).
+ *  - Several query tokens per sequence: Week 11 "Inference", Step 3 (the target
+ *    model verifies gamma + 1 tokens in one pass) and Common mistakes (the causal
+ *    mask of the new tokens must line up with the end of the cached keys, not
+ *    its start); Step 2 of "Optimización de la inferencia" masks future
+ *    positions when there is more than one query row.
+ *  - Copy-on-write: "Optimización de la inferencia", "Página Atención" (shared
+ *    pages are stored once; a request that diverges gets its own pages);
+ *    CS336 Lecture 10 transcript 01:21:58-01:23:17 (share the prompt's blocks,
+ *    split a block when the samples differ).
  */
 #include "pkv_oracle.h"
 
@@ -135,10 +144,14 @@ typedef struct {
     int32_t partition_tokens, max_parts; /* partition_tokens <= 0: whole sequence */
     double *out, *lse;
     int nthreads, tid;
+    int32_t T; /* query tokens per sequence (0 means 1) */
 } decode_job;
 
 /* One (sequence, KV head) unit: gather its K/V rows through the block table into
-   contiguous float64 arrays, then attend for each query head of the group. */
+   contiguous float64 arrays, then attend for each query head of the group.  With T > 1
+   query tokens per sequence (the last T of its ctx tokens), query token t sits at logical
+   position ctx - T + t and attends to tokens [0, ctx - T + t]: the whole cache and the new
+   tokens up to itself (the causal mask aligned to the end of the keys, not to their start). */
 static void decode_unit(const decode_job *j, int32_t b, int32_t kvh)
 {
     const int32_t H = j->H, G = j->N / j->K;
@@ -160,19 +173,24 @@ static void decode_unit(const decode_job *j, int32_t b, int32_t kvh)
             }
         }
     }
+    const int32_t T = j->T > 0 ? j->T : 1;
+    for (int32_t t = 0; t < T; ++t)
     for (int32_t g = 0; g < G; ++g) {
         int32_t n = kvh * G + g;
-        const uint16_t *qrow = j->q + ((size_t)b * j->N + n) * H;
+        size_t bn = ((size_t)b * T + t) * j->N + n;
+        const uint16_t *qrow = j->q + bn * H;
         for (int32_t h = 0; h < H; ++h) qv[h] = bf16_to_double(qrow[h]);
-        size_t bn = (size_t)b * j->N + n;
+        int64_t visible = ctx - T + t + 1; /* keys this query token may see */
+        if (visible < 0) visible = 0;
+        if (visible > ctx) visible = ctx;
         if (j->partition_tokens <= 0) {
-            attend(qv, keys, values, ctx, H, j->scale, scores, j->out + bn * H, j->lse + bn);
+            attend(qv, keys, values, visible, H, j->scale, scores, j->out + bn * H, j->lse + bn);
         } else {
             for (int32_t p = 0; p < j->max_parts; ++p) {
                 int64_t t0 = (int64_t)p * j->partition_tokens;
                 int64_t t1 = t0 + j->partition_tokens;
-                if (t1 > ctx) t1 = ctx;
-                if (t0 > ctx) t0 = ctx;
+                if (t1 > visible) t1 = visible;
+                if (t0 > visible) t0 = visible;
                 size_t bnp = bn * j->max_parts + p;
                 attend(qv, keys + t0 * H, values + t0 * H, t1 - t0, H, j->scale, scores,
                        j->out + bnp * H, j->lse + bnp);
@@ -240,6 +258,39 @@ void oracle_decode_partitions(const uint16_t *q, const uint16_t *k_cache, const 
     decode_job j = {q, k_cache, v_cache, 0, 0, 0, 0, block_tables, context_lens, max_nb, B, N, K,
                     H, bs, scale, partition_tokens, max_parts, part_out, part_lse, nthreads, 0};
     run_decode(j);
+}
+
+void oracle_slot_mapping_multi(const int32_t *block_tables, int32_t max_nb,
+                               const int32_t *context_lens, int32_t B, int32_t T, int32_t bs,
+                               int64_t *slots)
+{
+    for (int32_t b = 0; b < B; ++b)
+        for (int32_t t = 0; t < T; ++t) {
+            int64_t pos = (int64_t)context_lens[b] - T + t;
+            slots[(size_t)b * T + t] = pos >= 0 ? physical_slot(block_tables, max_nb, b, pos, bs) : -1;
+        }
+}
+
+void oracle_decode_multi(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                         const int32_t *block_tables, int32_t max_nb, const int32_t *context_lens,
+                         int32_t B, int32_t T, int32_t N, int32_t K, int32_t H, int32_t bs,
+                         double scale, double *out, double *lse, int nthreads)
+{
+    decode_job j = {q, k_cache, v_cache, 0, 0, 0, 0, block_tables, context_lens, max_nb, B, N, K,
+                    H, bs, scale, 0, 1, out, lse, nthreads, 0, T};
+    run_decode(j);
+}
+
+void oracle_copy_blocks(uint8_t *k_cache, uint8_t *v_cache, const int32_t *src_dst, int32_t n,
+                        int64_t block_bytes)
+{
+    for (int32_t i = 0; i < n; ++i) {
+        const int64_t src = src_dst[2 * i], dst = src_dst[2 * i + 1];
+        for (int64_t x = 0; x < block_bytes; ++x) {
+            k_cache[dst * block_bytes + x] = k_cache[src * block_bytes + x];
+            v_cache[dst * block_bytes + x] = v_cache[src * block_bytes + x];
+        }
+    }
 }
 
 /* Softmax over a union of disjoint key sets: each part's (out_p, lse_p) is its own

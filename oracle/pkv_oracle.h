@@ -59,6 +59,24 @@ void oracle_decode_partitions(const uint16_t *q, const uint16_t *k_cache, const 
 void oracle_lse_merge(const double *part_out, const double *part_lse, int32_t B, int32_t N,
                       int32_t H, int32_t max_parts, double *out, double *lse);
 
+/* ---- several query tokens per sequence (speculative verification) ------------------
+   The last T of each sequence's ctx tokens are new: query token t ([B][T][N][H]) sits at
+   logical position ctx - T + t and attends to the tokens [0, ctx - T + t] -- the whole cache
+   and the new tokens up to itself.  out [B][T][N][H], lse [B][T][N]. */
+void oracle_slot_mapping_multi(const int32_t *block_tables, int32_t max_nb,
+                               const int32_t *context_lens, int32_t B, int32_t T, int32_t bs,
+                               int64_t *slots);
+void oracle_decode_multi(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                         const int32_t *block_tables, int32_t max_nb, const int32_t *context_lens,
+                         int32_t B, int32_t T, int32_t N, int32_t K, int32_t H, int32_t bs,
+                         double scale, double *out, double *lse, int nthreads);
+
+/* ---- copy-on-write -----------------------------------------------------------------
+   For each pair i: physical block src_dst[2i+1] of both pools becomes a byte copy of block
+   src_dst[2i] (block_bytes = 16 * K * H * element bytes), in pair order. */
+void oracle_copy_blocks(uint8_t *k_cache, uint8_t *v_cache, const int32_t *src_dst, int32_t n,
+                        int64_t block_bytes);
+
 /* ---- FP8 (e4m3) KV cache ----------------------------------------------------------
    Codes: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent field 0 holds
    subnormals m * 2^-9; S.1111.111 is NaN; no infinities; largest finite 448.

@@ -348,10 +348,98 @@ def check_fp8_append_roundtrip(orc):
     assert sorted(map(tuple, np.argwhere(changed))) == sorted((s_ // 16, s_ % 16) for s_ in slots.tolist())
 
 
+# ------------------------------- several query tokens ------------------------------------
+def masked_sdpa_reference(q, ks, vs, scale):
+    """torch SDPA (float64) with an explicit boolean mask: the T query rows of a sequence of
+    ctx keys are its last T positions; row t may see keys 0 .. ctx - T + t."""
+    import torch
+    B, T, N, H = q.shape
+    K = ks[0].shape[1]
+    G = N // K
+    out = np.zeros((B, T, N, H))
+    for b in range(B):
+        ctx = ks[b].shape[0]
+        qt = torch.from_numpy(to_f64(q[b])).permute(1, 0, 2).unsqueeze(0)   # [1, N, T, H]
+        kt = torch.from_numpy(to_f64(ks[b])).permute(1, 0, 2).unsqueeze(0).repeat_interleave(G, dim=1)
+        vt = torch.from_numpy(to_f64(vs[b])).permute(1, 0, 2).unsqueeze(0).repeat_interleave(G, dim=1)
+        rows = torch.arange(T).unsqueeze(1) + (ctx - T)
+        mask = torch.arange(ctx).unsqueeze(0) <= rows                        # [T, ctx]
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
+        out[b] = o[0].permute(1, 0, 2).numpy()
+    return out
+
+
+def check_multi_query_equals_masked_sdpa(orc):
+    for N, K, H, ctxs, T, seed in [(8, 2, 64, [4, 17, 40], 4, 21), (16, 2, 128, [2, 33], 2, 22),
+                                   (4, 4, 64, [16, 31], 3, 23)]:
+        _, ks, vs = random_case(seed, N, K, H, ctxs)
+        q = gen.normal_bf16(seed, 400, (len(ctxs), T, N, H))
+        kc, vc, tables, ctx = paged_from_contiguous(ks, vs, seed)
+        scale = 1.0 / math.sqrt(H)
+        out, lse = orc.decode_multi(q, kc, vc, tables, ctx, scale)
+        ref = masked_sdpa_reference(q, ks, vs, scale)
+        assert np.all(np.isfinite(out))
+        assert np.max(np.abs(out - ref)) < 1e-12, (N, K, H, ctxs, T)
+
+
+def check_multi_query_is_a_sequence_of_decode_steps(orc):
+    """Verifying T tokens at once gives, for token t, exactly what a one-token decode step at
+    its position gives (the context cut after that token)."""
+    w = gen.make_workload("pin_multi", 24, 8, 2, 64, [5, 16, 17, 50])
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    T = 4
+    slots = orc.slot_mapping_multi(w.block_tables, w.context_lens, T)
+    new_k = gen.normal_bf16(24, 500, (w.B, T, w.K, w.H))
+    new_v = gen.normal_bf16(24, 501, (w.B, T, w.K, w.H))
+    orc.append(new_k.reshape(-1, w.K, w.H), new_v.reshape(-1, w.K, w.H), slots.reshape(-1), kc, vc)
+    q = gen.normal_bf16(24, 502, (w.B, T, w.N, w.H))
+    out, lse = orc.decode_multi(q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    for t in range(T):
+        cut = np.maximum(w.context_lens - T + t + 1, 0).astype(np.int32)
+        o1, l1 = orc.decode(q[:, t], kc, vc, w.block_tables, cut, w.scale)
+        assert np.array_equal(out[:, t], o1) and np.array_equal(lse[:, t], l1), t
+
+
+def check_slot_mapping_multi(orc):
+    B, T, max_nb = 3, 5, 4
+    tables = np.arange(B * max_nb, dtype=np.int32).reshape(B, max_nb)[:, ::-1].copy()
+    ctx = np.array([3, 16, 40], dtype=np.int32)
+    got = orc.slot_mapping_multi(tables, ctx, T)
+    for b in range(B):
+        for t in range(T):
+            pos = int(ctx[b]) - T + t
+            want = -1 if pos < 0 else int(tables[b, pos // BS]) * BS + pos % BS
+            assert got[b, t] == want, (b, t, got[b, t], want)
+
+
+def check_copy_blocks(orc):
+    """The copy equals numpy's; a sequence whose shared partial block is replaced by a private
+    copy (copy-on-write) attends exactly as before."""
+    w = gen.make_workload("pin_cow", 25, 8, 2, 64, [20, 40, 9], pool_blocks=10)
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    ref_k, ref_v = kc.copy(), vc.copy()
+    used = set(w.block_tables[w.block_tables >= 0].tolist())
+    free = [x for x in range(w.num_blocks) if x not in used]
+    pairs = np.array([[w.block_tables[0, 1], free[0]], [w.block_tables[1, 2], free[1]]], dtype=np.int32)
+    orc.copy_blocks(kc, vc, pairs)
+    for src, dst in pairs:
+        ref_k[dst] = ref_k[src]
+        ref_v[dst] = ref_v[src]
+    assert np.array_equal(kc.view(np.uint16), ref_k.view(np.uint16))
+    assert np.array_equal(vc.view(np.uint16), ref_v.view(np.uint16))
+    before, lse_b = orc.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    tables = w.block_tables.copy()
+    tables[0, 1], tables[1, 2] = pairs[0, 1], pairs[1, 1]
+    after, lse_a = orc.decode(w.q, kc, vc, tables, w.context_lens, w.scale)
+    assert np.array_equal(np.nan_to_num(before, nan=7.0), np.nan_to_num(after, nan=7.0))
+
+
 ALL_CHECKS = [check_kv_bytes_golden, check_paged_equals_contiguous,
               check_block_permutation_invariance, check_ctx1_returns_v, check_constant_v,
               check_zero_query_is_uniform_mean, check_brute_force_mpmath, check_large_logits,
               check_partitions_merge_to_unsplit, check_ctx0, check_slot_mapping,
               check_append_gather_roundtrip, check_gather_inverts_scatter,
               check_e4m3_decode_table, check_e4m3_encode_nearest_even,
-              check_fp8_attention_is_dequantized_attention, check_fp8_append_roundtrip]
+              check_fp8_attention_is_dequantized_attention, check_fp8_append_roundtrip,
+              check_multi_query_equals_masked_sdpa, check_multi_query_is_a_sequence_of_decode_steps,
+              check_slot_mapping_multi, check_copy_blocks]

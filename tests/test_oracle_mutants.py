@@ -44,6 +44,15 @@ MUTANTS = {
     "fp8_scale_multiplies": [("dst[i] = oracle_e4m3_encode(x / scale[kvh]);", "dst[i] = oracle_e4m3_encode(x * scale[kvh]);")],
     "fp8_v_scale_for_k": [("keys[t * H + h] = oracle_e4m3_decode(j->k8[row + h]) * (double)j->k_scale[kvh];",
                            "keys[t * H + h] = oracle_e4m3_decode(j->k8[row + h]) * (double)j->v_scale[kvh];")],
+    "multi_mask_top_left": [("int64_t visible = ctx - T + t + 1;", "int64_t visible = t + 1;")],
+    "multi_mask_off_by_one": [("int64_t visible = ctx - T + t + 1;", "int64_t visible = ctx - T + t;")],
+    "multi_query_row": [("const uint16_t *qrow = j->q + bn * H;",
+                         "const uint16_t *qrow = j->q + ((size_t)b * T * j->N + n) * H;")],
+    "slot_multi_offset": [("int64_t pos = (int64_t)context_lens[b] - T + t;",
+                           "int64_t pos = (int64_t)context_lens[b] - T + t + 1;")],
+    "copy_blocks_reversed": [("const int64_t src = src_dst[2 * i], dst = src_dst[2 * i + 1];",
+                              "const int64_t dst = src_dst[2 * i], src = src_dst[2 * i + 1];")],
+    "copy_blocks_k_only": [("v_cache[dst * block_bytes + x] = v_cache[src * block_bytes + x];", "")],
     "weights_not_normalised": [("for (int64_t t = 0; t < ntok; ++t) scores[t] /= sum;",
                                 "for (int64_t t = 0; t < ntok; ++t) scores[t] /= (double)ntok;")],
 }
