@@ -33,7 +33,7 @@ FALLBACK_HBM_GBS = 6800.0     # copy bandwidth of an earlier GB300 measurement
 DEFAULT_CONFIG = "l3_8b_b64"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 ATTN_SOURCES = [os.path.join(ROOT, "paged_kv_decode_slot_gb300", "csrc", f)
-                for f in ("pkv_attn.cu", "pkv_device.cuh", "pkv_internal.h")]
+                for f in ("pkv_attn.cu", "pkv_attn_common.cuh", "pkv_device.cuh", "pkv_internal.h")]
 
 
 def _dist_env():
@@ -74,12 +74,13 @@ def recorded_traffic(config: str):
     return None
 
 
-def step_bytes(w, kv: str = "bf16") -> dict:
+def step_bytes(w, kv: str = "bf16", tokens: int = 1) -> dict:
     """Algorithmic bytes of one step (what the method must move, padding not counted).
 
     With an e4m3 cache the K/V history is one byte per element (half the bf16 bytes), the
     append reads the new bf16 rows and writes one-byte codes, and attention also reads the
-    2 x K per-head scales."""
+    2 x K per-head scales.  With T new tokens per sequence (verification) q, out and the
+    append are T times larger and the block tables are read once per 32-row chunk."""
     tables = int(sum(-(-int(c) // 16) for c in w.context_lens)) * 4
     meta = w.B * 4 + tables + w.B * 8 * 2          # context lens, table entries, slots (write+read)
     if kv == "fp8":
@@ -91,6 +92,12 @@ def step_bytes(w, kv: str = "bf16") -> dict:
         attn = w.kv_bytes() + w.qo_bytes()
         attn_unique = w.unique_kv_bytes() + w.qo_bytes()
         append = w.append_bytes()
+    if tokens > 1:
+        extra_qo = (tokens - 1) * w.qo_bytes()
+        attn += extra_qo
+        attn_unique += extra_qo
+        append *= tokens
+        meta += w.B * 8 * 2 * (tokens - 1)
     return {"attn": attn, "attn_unique": attn_unique, "append": append, "meta": meta,
             "step": attn + append + meta}
 
@@ -234,6 +241,17 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def kernel_label(args, plan, step) -> str:
+    if args.tokens > 1:
+        return "attn_cols_kernel<128>" + (" + lse_merge_kernel" if plan.mode == "split" else "")
+    if args.attn == "prefix":
+        return "attn_cols_kernel<128> (prefix + suffix passes) + cascade_merge_kernel"
+    fp8 = "1" if args.kv == "fp8" else "0"
+    return {"single": f"attn_kernel<128,0,{fp8}>",
+            "split": f"attn_kernel<128,1,{fp8}> + lse_merge_kernel",
+            "balanced": "attn_balanced_kernel + balanced_merge_kernel"}[plan.mode]
+
+
 def config_dict(w, flush: str, plan=None) -> dict:
     d = {"workload": w.name, "batch": w.B, "q_heads": w.N, "kv_heads": w.K, "head_dim": w.H,
          "block_size": 16, "total_context_tokens": w.total_tokens,
@@ -259,7 +277,8 @@ def run_ours(args):
     build_library()
     import paged_kv_decode_slot_gb300 as pkv
     from paged_kv_decode_slot_gb300 import inputs as gen
-    from paged_kv_decode_slot_gb300.step import DecodeStep, DecodeStepFp8, plan_attention
+    from paged_kv_decode_slot_gb300.step import (DecodeStep, DecodeStepFp8, MultiTokenStep, PrefixDecodeStep,
+                                                 plan_attention)
 
     w = gen.make_config(args.config)
     dev = torch.device("cuda", local)
@@ -278,7 +297,26 @@ def run_ours(args):
     plan = plan_attention(w.B, w.K, w.max_blocks, sms, partition_blocks=args.partition_blocks)
     if args.mode and args.partition_blocks is None:
         plan = plan_attention(w.B, w.K, w.max_blocks, sms, mode=args.mode)
-    if args.kv == "fp8":
+    if args.tokens > 1:
+        if args.kv != "bf16" or args.attn != "auto":
+            raise SystemExit("--tokens > 1 runs the bf16 cache without --attn prefix")
+        T = args.tokens
+        qm = d16(gen.normal_bf16(w.seed, 900, (w.B, T, w.N, w.H)))
+        knm = d16(gen.normal_bf16(w.seed, 901, (w.B, T, w.K, w.H)))
+        vnm = d16(gen.normal_bf16(w.seed, 902, (w.B, T, w.K, w.H)))
+        step = MultiTokenStep(qm, knm, vnm, kc, vc, bt, cl, w.scale,
+                              partition_blocks=args.partition_blocks, err_flag=err)
+        plan = step.plan
+    elif args.attn == "prefix":
+        groups = w.prefix_groups()
+        if groups is None or args.kv != "bf16":
+            raise SystemExit("--attn prefix needs a shared-prefix workload and the bf16 cache")
+        gs, pb = groups
+        step = PrefixDecodeStep(q, kn, vn, kc, vc, bt, cl, w.scale, d32(gs), d32(pb),
+                                int(np.max(np.diff(gs))), int(pb.max()),
+                                partition_blocks=args.partition_blocks or 16, err_flag=err)
+        plan = step.plan
+    elif args.kv == "fp8":
         if args.unfused or plan.mode == "balanced":
             raise SystemExit("--kv fp8 runs the fused single-pass or split step only")
         # per-KV-head scales from the cache's own absolute maxima (NaN tail poison ignored)
@@ -309,7 +347,7 @@ def run_ours(args):
         # timed step starts with an L2 that holds neither its inputs nor write-back debt.
         flush_w.add_(1.0)
         torch.sum(flush_r, dim=0, keepdim=True, out=flush_sink)
-    nbytes = step_bytes(w, args.kv)
+    nbytes = step_bytes(w, args.kv, args.tokens)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -390,13 +428,10 @@ def run_ours(args):
         raise RuntimeError(f"device error flag {flag:#x} during the graph replays")
 
     # -- end to end through the public API with host buffers (pinned), copies inside the timing
-    hq = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hkn = torch.from_numpy(w.k_new.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hvn = torch.from_numpy(w.v_new.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hbt = torch.from_numpy(np.ascontiguousarray(w.block_tables)).pin_memory()
-    hcl = torch.from_numpy(np.ascontiguousarray(w.context_lens)).pin_memory()
-    hout = torch.empty(tuple(q.shape), dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hkn, hvn, hbt, hcl))
+    dev_inputs = step.inputs()
+    host_inputs = [t.detach().cpu().pin_memory() for t in dev_inputs]
+    hout = torch.empty(tuple(step.out.shape), dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_inputs)
     d2h = hout.numel() * hout.element_size()
     e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     with torch.cuda.stream(stream):
@@ -405,11 +440,8 @@ def run_ours(args):
             k = i - args.warmup
             if k >= 0:
                 e2e_ev[k][0].record(stream)
-            q.copy_(hq, non_blocking=True)
-            kn.copy_(hkn, non_blocking=True)
-            vn.copy_(hvn, non_blocking=True)
-            bt.copy_(hbt, non_blocking=True)
-            cl.copy_(hcl, non_blocking=True)
+            for dst, src in zip(dev_inputs, host_inputs):
+                dst.copy_(src, non_blocking=True)
             step.run(stream)
             hout.copy_(step.out, non_blocking=True)
             if k >= 0:
@@ -440,10 +472,7 @@ def run_ours(args):
         "frac_of_8tbs": achieved / (NORTH_STAR_TBS * 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "kernel": {"single": "attn_kernel<128,0,%d>",
-                                "split": "attn_kernel<128,1,%d> + lse_merge_kernel",
-                                "balanced": "attn_balanced_kernel + balanced_merge_kernel"}[plan.mode]
-                               .replace("%d", "1" if args.kv == "fp8" else "0")
+                     "kernel": kernel_label(args, plan, step)
                                + (" (append fused)" if step.fused else ""),
                      "bytes_per_launch": attn_bytes,
                      "traffic": recorded_traffic(args.config + ("" if args.kv == "bf16" else "+fp8"))},
@@ -458,6 +487,10 @@ def run_ours(args):
         "wall_s_timed_region": t_wall,
         "step_bytes": nbytes["step"],
     }
+    if args.tokens > 1:
+        line["config"]["new_tokens_per_seq"] = args.tokens
+    if args.attn == "prefix":
+        line["config"]["prefix_groups"] = "one group of the whole batch sharing its full prefix blocks"
     if args.kv == "fp8":
         line["config"]["kv_cache"] = "e4m3, per-KV-head scales (amax / 448)"
         line["kv_gbs"] = w.kv_bytes() / 2 / (mean_attn * 1e-3) / 1e9
@@ -485,6 +518,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv", choices=("bf16", "fp8"), default="bf16",
                     help="KV cache element type (fp8 = e4m3 codes with per-KV-head scales)")
+    ap.add_argument("--tokens", type=int, default=1,
+                    help="new tokens per sequence (> 1: speculative verification of that many)")
+    ap.add_argument("--attn", choices=("auto", "prefix"), default="auto",
+                    help="prefix: shared-prefix decode on a workload whose sequences share blocks")
     ap.add_argument("--unfused", action="store_true",
                     help="separate slot-mapping, append and attention launches")
     args = ap.parse_args()

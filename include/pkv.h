@@ -72,6 +72,8 @@ enum pkv_status {
 #define PKV_FLAG_CTX_RANGE 4   /* context_len < 0 or > max_blocks_per_seq * 16 */
 #define PKV_FLAG_TIMEOUT 8     /* a bounded in-kernel wait expired; the unit's result is void */
 #define PKV_FLAG_OUT_RANGE 16  /* pkv_gather: a row beyond out_rows */
+#define PKV_FLAG_GROUP_RANGE 32 /* pkv_decode_attn_prefix: a group or prefix beyond its declared
+                                   bound, or a member shorter than its group's prefix */
 
 typedef struct {
     int32_t num_blocks;   /* physical blocks in each pool */
@@ -301,6 +303,86 @@ int pkv_gather(const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *
                int32_t max_blocks_per_seq, const int32_t *context_lens, const int64_t *cu_seqlens,
                int32_t num_seqs, pkv_bf16 *k_out, pkv_bf16 *v_out, int64_t out_rows,
                pkv_cache_desc cache, int32_t *err_flag, pkv_stream_t stream);
+
+/*
+ * ---- several new tokens per sequence (speculative verification) ---------------------------
+ * The target model checks gamma + 1 drafted tokens in one pass ("Week 11. Inference", Step 3):
+ * each sequence carries T = num_new new tokens, the last T of its ctx tokens (context_lens
+ * counts them).  Token t sits at logical position ctx - T + t and attends to the tokens
+ * [0, ctx - T + t]: the whole cache and the new tokens up to itself.  The causal mask lines up
+ * with the end of the keys, not with their start (Week 11, "Common mistakes"; the masked
+ * softmax of "Optimización de la inferencia", Step 2).  A token with no visible key (ctx < T)
+ * gets out 0 and lse -inf.
+ */
+
+/* Slots of the last T logical positions of each sequence: slot_mapping int64 [num_seqs][T],
+   -1 below position 0; a block id outside [0, num_blocks) or a context beyond the table sets a
+   flag and gives -1.  Feed it to pkv_append with num_tokens = num_seqs * T and the new rows
+   [num_seqs][T][K][H]. */
+int pkv_slot_mapping_multi(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t num_seqs, int32_t num_new,
+                           int32_t num_blocks, int64_t *slot_mapping, int32_t *err_flag,
+                           pkv_stream_t stream);
+
+/* Attention of T = num_new (1..64) query tokens per sequence after they were appended.
+   q bf16 [num_seqs][T][N][H] (4-byte aligned), out bf16 [num_seqs][T][N][H], lse_out fp32
+   [num_seqs][T][N] (nullable).  partition_blocks 0: one pass (no workspace); > 0: fixed
+   partitions of that many blocks and a log-sum-exp merge, with max_partitions as for
+   pkv_decode_attn_splitk and a workspace of pkv_splitk_workspace_bytes(num_seqs * T, N, H,
+   max_partitions) bytes (256-byte aligned).  Each CTA loads a K/V tile once for up to 32 of a
+   sequence's (token, head) rows of one KV head.  H in {64, 128}; G in {1, 2, 4, 8}. */
+int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *context_lens, int32_t num_seqs, int32_t num_new,
+                          int32_t num_q_heads, float scale, pkv_bf16 *out, float *lse_out,
+                          pkv_cache_desc cache, int32_t partition_blocks, int32_t max_partitions,
+                          void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                          pkv_stream_t stream);
+
+/*
+ * ---- shared prefixes and copy-on-write ------------------------------------------------------
+ * Requests that share a prompt reference the same physical blocks; a request that diverges gets
+ * its own copy of the block it writes into ("Optimización de la inferencia", "Página Atención",
+ * copy-on-write; CS336 Lecture 10 transcript 01:21:58-01:23:17: share the prompt's KV cache,
+ * split the block when the samples differ).
+ */
+
+/* Copy-on-write: for each pair i, physical block src_dst[2i+1] of both pools becomes a byte copy
+   of block src_dst[2i] (whole blocks of 16 x K x H elements of elem_bytes, 1 for e4m3 pools or 2
+   for bf16).  src_dst int32 [num_pairs][2] (device).  Pairs run concurrently: no destination
+   may be another pair's source or destination.  An id outside [0, num_blocks) sets
+   PKV_FLAG_BLOCK_RANGE and that pair is skipped.  Pools 16-byte aligned. */
+int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_dst, int32_t num_pairs,
+                    pkv_cache_desc cache, int32_t elem_bytes, int32_t *err_flag, pkv_stream_t stream);
+
+/* Workspace bytes of pkv_decode_attn_prefix. */
+size_t pkv_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                  int32_t max_blocks_per_seq, int32_t max_prefix_blocks,
+                                  int32_t partition_blocks);
+
+/* Decode attention (one token per sequence, the result of pkv_decode_attn) for a batch whose
+   sequences form groups that share their leading blocks.  group_starts int32 [num_groups + 1]
+   (device, non-decreasing, within [0, num_seqs]): group g = sequences [group_starts[g],
+   group_starts[g+1]); prefix_blocks int32 [num_groups] (device): the number of leading logical
+   blocks that every member's table shares with the group's first member (full blocks: a partly
+   filled prefix block is copied on write and belongs to each member).  Sequences outside every
+   group have no shared prefix.  The shared blocks are attended once per KV head for all the
+   group's queries (up to 32 query rows per loaded tile), each sequence's own blocks separately
+   in partitions of partition_blocks, and the partials are merged by their log-sum-exp.
+   Host-side bounds: every group has at most max_group_size members and at most
+   max_prefix_blocks (<= max_blocks_per_seq) shared blocks; a group beyond them, or a member
+   shorter than its prefix, sets PKV_FLAG_GROUP_RANGE (that member's result is then void).  The
+   members' tables are not compared: if they do not share the prefix, the result is attention
+   over the first member's prefix blocks followed by the member's own blocks.  workspace of
+   pkv_prefix_workspace_bytes(...) bytes, 256-byte aligned. */
+int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                           float scale, const int32_t *group_starts, const int32_t *prefix_blocks,
+                           int32_t num_groups, int32_t max_group_size, int32_t max_prefix_blocks,
+                           pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
+                           int32_t partition_blocks, void *workspace, size_t workspace_bytes,
+                           int32_t *err_flag, pkv_stream_t stream);
 
 /* Synchronise the stream, copy *err_flag to *host_value; PKV_ERR_RANGE if it is non-zero. */
 int pkv_read_err_flag(const int32_t *err_flag, int32_t *host_value, pkv_stream_t stream);

@@ -41,6 +41,7 @@ PKV_FLAG_SLOT_RANGE = 2
 PKV_FLAG_CTX_RANGE = 4
 PKV_FLAG_TIMEOUT = 8
 PKV_FLAG_OUT_RANGE = 16
+PKV_FLAG_GROUP_RANGE = 32
 
 BLOCK_SIZE = 16
 
@@ -387,6 +388,100 @@ def pkv_lse_merge(part_out, part_lse, context_lens, partition_blocks: int, out, 
     B, N, P, H = part_out.shape
     return _lib.pkv_lse_merge(_ptr(part_out), _ptr(part_lse), _ptr(context_lens), B, N, H, P,
                               partition_blocks, _ptr(out), _ptr(lse_out), _stream(stream))
+
+
+# ---------------------------- several new tokens per sequence ----------------------------
+_lib.pkv_slot_mapping_multi.argtypes = [_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P]
+_lib.pkv_decode_attn_multi.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, ctypes.c_float, _P,
+                                       _P, CacheDesc, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
+_lib.pkv_copy_blocks.argtypes = [_P, _P, _P, _I32, CacheDesc, _I32, _P, _P]
+_lib.pkv_prefix_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32]
+_lib.pkv_prefix_workspace_bytes.restype = ctypes.c_size_t
+_lib.pkv_decode_attn_prefix.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P, _P,
+                                        _I32, _I32, _I32, _P, _P, CacheDesc, _I32, _P, ctypes.c_size_t,
+                                        _P, _P]
+
+
+def pkv_slot_mapping_multi(block_tables, context_lens, num_blocks: int, slot_mapping, err_flag=None,
+                           stream=None) -> int:
+    """slot_mapping int64 [B, T]: slots of each sequence's last T logical positions."""
+    _need(block_tables, torch.int32, 2, "block_tables")
+    _need(context_lens, torch.int32, 1, "context_lens")
+    _need(slot_mapping, torch.int64, 2, "slot_mapping")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    B, T = slot_mapping.shape
+    return _lib.pkv_slot_mapping_multi(_ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, T,
+                                       num_blocks, _ptr(slot_mapping), _ptr(err_flag), _stream(stream))
+
+
+def pkv_decode_attn_multi(q, k_cache, v_cache, block_tables, context_lens, scale: float, out, lse_out=None,
+                          partition_blocks: int = 0, max_partitions: int = 0, workspace=None,
+                          err_flag=None, stream=None) -> int:
+    """q, out bf16 [B, T, N, H]; lse_out float32 [B, T, N]."""
+    _need(q, torch.bfloat16, 4, "q")
+    _need(k_cache, torch.bfloat16, 4, "k_cache")
+    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    _need(block_tables, torch.int32, 2, "block_tables")
+    _need(context_lens, torch.int32, 1, "context_lens")
+    _need(out, torch.bfloat16, 4, "out")
+    _opt(lse_out, torch.float32, 3, "lse_out")
+    _opt(workspace, torch.uint8, 1, "workspace")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    B, T, N, _ = q.shape
+    return _lib.pkv_decode_attn_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                      block_tables.shape[1], _ptr(context_lens), B, T, N, float(scale),
+                                      _ptr(out), _ptr(lse_out), cache_desc(k_cache), partition_blocks,
+                                      max_partitions, _ptr(workspace),
+                                      0 if workspace is None else workspace.numel(), _ptr(err_flag),
+                                      _stream(stream))
+
+
+def pkv_copy_blocks(k_cache, v_cache, src_dst, err_flag=None, stream=None) -> int:
+    """Copy-on-write: block src_dst[i, 1] of both pools becomes a copy of block src_dst[i, 0]."""
+    if k_cache.dtype not in (torch.bfloat16, torch.uint8) or v_cache.dtype != k_cache.dtype:
+        raise TypeError("pools must both be bf16 or both uint8 (e4m3)")
+    _need(k_cache, k_cache.dtype, 4, "k_cache")
+    _need(v_cache, k_cache.dtype, 4, "v_cache")
+    _need(src_dst, torch.int32, 2, "src_dst")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    if src_dst.shape[1] != 2 or v_cache.shape != k_cache.shape:
+        raise ValueError("src_dst must be [n, 2]; pools must have one shape")
+    return _lib.pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src_dst), src_dst.shape[0],
+                                cache_desc(k_cache), k_cache.element_size(), _ptr(err_flag),
+                                _stream(stream))
+
+
+def pkv_prefix_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_blocks_per_seq: int,
+                               max_prefix_blocks: int, partition_blocks: int) -> int:
+    return int(_lib.pkv_prefix_workspace_bytes(num_seqs, num_q_heads, head_dim, max_blocks_per_seq,
+                                               max_prefix_blocks, partition_blocks))
+
+
+def pkv_decode_attn_prefix(q, k_cache, v_cache, block_tables, context_lens, scale: float, group_starts,
+                           prefix_blocks, max_group_size: int, max_prefix_blocks: int, out, lse_out=None,
+                           partition_blocks: int = 16, workspace=None, err_flag=None, stream=None) -> int:
+    """Decode attention with each group's shared leading blocks attended once per KV head."""
+    _need(q, torch.bfloat16, 3, "q")
+    _need(k_cache, torch.bfloat16, 4, "k_cache")
+    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    _need(block_tables, torch.int32, 2, "block_tables")
+    _need(context_lens, torch.int32, 1, "context_lens")
+    _need(group_starts, torch.int32, 1, "group_starts")
+    _need(prefix_blocks, torch.int32, 1, "prefix_blocks")
+    _need(out, torch.bfloat16, 3, "out")
+    _opt(lse_out, torch.float32, 2, "lse_out")
+    _opt(workspace, torch.uint8, 1, "workspace")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    if group_starts.numel() != prefix_blocks.numel() + 1:
+        raise ValueError("group_starts needs one more entry than prefix_blocks")
+    B, N, _ = q.shape
+    return _lib.pkv_decode_attn_prefix(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                       block_tables.shape[1], _ptr(context_lens), B, N, float(scale),
+                                       _ptr(group_starts), _ptr(prefix_blocks), prefix_blocks.numel(),
+                                       max_group_size, max_prefix_blocks, _ptr(out), _ptr(lse_out),
+                                       cache_desc(k_cache), partition_blocks, _ptr(workspace),
+                                       0 if workspace is None else workspace.numel(), _ptr(err_flag),
+                                       _stream(stream))
 
 
 def pkv_gather(k_cache, v_cache, block_tables, context_lens, cu_seqlens, k_out, v_out, err_flag=None,

@@ -784,3 +784,204 @@ PKV_EXPORT int pkv_decode_attn_splitk_noalloc(const pkv_bf16 *q, const pkv_bf16 
     return pkv_lse_merge(part_out, part_lse, context_lens, num_seqs, num_q_heads, cache.head_dim,
                          max_partitions, partition_blocks, out, lse_out, stream);
 }
+
+// ---- several new tokens per sequence, shared prefixes, copy-on-write ------------------------
+namespace {
+
+pkv::ColsParams cols_params_of(const AttnArgs &a, int tok_major)
+{
+    pkv::ColsParams p{};
+    p.q = a.q;
+    p.block_tables = a.block_tables;
+    p.context_lens = a.context_lens;
+    p.max_nb = a.max_nb;
+    p.B = a.B;
+    p.N = a.N;
+    p.K = a.d.num_kv_heads;
+    p.G = a.N / a.d.num_kv_heads;
+    p.T = 1;
+    p.num_blocks = a.d.num_blocks;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.tok_major = tok_major;
+    p.err_flag = a.err_flag;
+    return p;
+}
+
+constexpr int kColsPerCta = 32;  // query rows per CTA of the column-parallel kernel
+
+int32_t prefix_parts_for(int32_t max_prefix_blocks, int32_t partition_blocks)
+{
+    const int32_t n = (max_prefix_blocks + partition_blocks - 1) / partition_blocks;
+    return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+PKV_EXPORT int pkv_slot_mapping_multi(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t *context_lens, int32_t num_seqs, int32_t num_new,
+                                      int32_t num_blocks, int64_t *slot_mapping, int32_t *err_flag,
+                                      pkv_stream_t stream)
+{
+    if (!block_tables || !context_lens || !slot_mapping) return PKV_ERR_NULL;
+    if (num_seqs < 0 || num_new <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PKV_ERR_SHAPE;
+    if ((int64_t)max_blocks_per_seq * 16 > INT32_MAX || (int64_t)num_seqs * num_new > INT32_MAX)
+        return PKV_ERR_SHAPE;
+    if (!aligned(slot_mapping, 8)) return PKV_ERR_ALIGN;
+    if (num_seqs == 0) return PKV_OK;
+    cudaError_t e = pkv::launch_slot_mapping_multi(block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                                   num_new, num_blocks, slot_mapping, err_flag, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "multi-token slot mapping launch");
+}
+
+PKV_EXPORT int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_dst, int32_t num_pairs,
+                               pkv_cache_desc cache, int32_t elem_bytes, int32_t *err_flag,
+                               pkv_stream_t stream)
+{
+    if (!k_cache || !v_cache || (num_pairs > 0 && !src_dst)) return PKV_ERR_NULL;
+    if (num_pairs < 0) return PKV_ERR_SHAPE;
+    if (elem_bytes != 1 && elem_bytes != 2) return PKV_ERR_UNSUPPORTED;
+    int st = check_copy_desc(cache);
+    if (st != PKV_OK) return st;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(src_dst, 4)) return PKV_ERR_ALIGN;
+    if (num_pairs == 0) return PKV_OK;
+    const int64_t block_bytes = (int64_t)cache.block_size * cache.num_kv_heads * cache.head_dim * elem_bytes;
+    cudaError_t e = pkv::launch_copy_blocks(static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache),
+                                            src_dst, num_pairs, cache.num_blocks, block_bytes, err_flag,
+                                            stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "copy-blocks launch");
+}
+
+PKV_EXPORT int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t *context_lens, int32_t num_seqs, int32_t num_new,
+                                     int32_t num_q_heads, float scale, pkv_bf16 *out, float *lse_out,
+                                     pkv_cache_desc cache, int32_t partition_blocks,
+                                     int32_t max_partitions, void *workspace, size_t workspace_bytes,
+                                     int32_t *err_flag, pkv_stream_t stream)
+{
+    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+               num_q_heads, scale, cache, err_flag};
+    int st = validate_attn(a);
+    if (st != PKV_OK) return st;
+    if (!out) return PKV_ERR_NULL;
+    if (num_new <= 0 || num_new > 64) return PKV_ERR_SHAPE;
+    if (!aligned(out, 4) || !aligned(lse_out, 4)) return PKV_ERR_ALIGN;
+    const int32_t G = num_q_heads / cache.num_kv_heads;
+    const int32_t chunks = (num_new * G + kColsPerCta - 1) / kColsPerCta;
+    const bool split = partition_blocks > 0;
+    int32_t parts = 1, pb = max_blocks_per_seq;
+    float *part_out = nullptr, *part_lse = nullptr;
+    if (split) {
+        if (max_partitions <= 0 || (int64_t)max_partitions * partition_blocks < max_blocks_per_seq)
+            return PKV_ERR_SHAPE;
+        const int64_t rows = (int64_t)num_seqs * num_new;
+        if (rows > INT32_MAX) return PKV_ERR_SHAPE;
+        if (!workspace || workspace_bytes < pkv_splitk_workspace_bytes((int32_t)rows, num_q_heads,
+                                                                       cache.head_dim, max_partitions))
+            return PKV_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
+        parts = max_partitions;
+        pb = partition_blocks;
+        part_out = static_cast<float *>(workspace);
+        part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                             splitk_lse_offset((int32_t)rows, num_q_heads, cache.head_dim,
+                                                               max_partitions));
+    } else if (partition_blocks < 0) {
+        return PKV_ERR_SHAPE;
+    }
+    const int64_t grid = (int64_t)cache.num_kv_heads * num_seqs * chunks * parts;
+    if (grid > INT32_MAX) return PKV_ERR_SHAPE;
+    if (num_seqs == 0) return PKV_OK;
+    CUtensorMap tk, tv;
+    int tok_major = 0;
+    st = make_kv_maps(&tk, &tv, k_cache, v_cache, cache, &tok_major);
+    if (st != PKV_OK) return st;
+    pkv::ColsParams p = cols_params_of(a, tok_major);
+    p.T = num_new;
+    p.part_blocks = pb;
+    p.parts = parts;
+    p.split = split ? 1 : 0;
+    p.max_parts = split ? max_partitions : 1;
+    p.chunks = chunks;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.lse_out = lse_out;
+    p.part_out = part_out;
+    p.part_lse = part_lse;
+    cudaError_t e = pkv::launch_attn_cols(cache.head_dim, tk, tv, p, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "multi-token attention launch");
+    if (!split) return PKV_OK;
+    // rows of one sequence: its T tokens x N heads, all with the sequence's context length
+    return pkv_lse_merge(part_out, part_lse, context_lens, num_seqs, num_new * num_q_heads,
+                         cache.head_dim, max_partitions, partition_blocks, out, lse_out, stream);
+}
+
+PKV_EXPORT size_t pkv_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                             int32_t max_blocks_per_seq, int32_t max_prefix_blocks,
+                                             int32_t partition_blocks)
+{
+    if (num_seqs < 0 || num_q_heads < 0 || head_dim < 0 || max_blocks_per_seq <= 0 ||
+        max_prefix_blocks < 0 || partition_blocks <= 0)
+        return 0;
+    const int32_t parts = prefix_parts_for(max_prefix_blocks, partition_blocks) +
+                          (max_blocks_per_seq + partition_blocks - 1) / partition_blocks;
+    return pkv_splitk_workspace_bytes(num_seqs, num_q_heads, head_dim, parts);
+}
+
+PKV_EXPORT int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                      float scale, const int32_t *group_starts,
+                                      const int32_t *prefix_blocks, int32_t num_groups,
+                                      int32_t max_group_size, int32_t max_prefix_blocks, pkv_bf16 *out,
+                                      float *lse_out, pkv_cache_desc cache, int32_t partition_blocks,
+                                      void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                                      pkv_stream_t stream)
+{
+    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+               num_q_heads, scale, cache, err_flag};
+    int st = validate_attn(a);
+    if (st != PKV_OK) return st;
+    if (!out || !workspace) return PKV_ERR_NULL;
+    if (num_groups < 0 || partition_blocks <= 0 || max_prefix_blocks < 0 ||
+        max_prefix_blocks > max_blocks_per_seq)
+        return PKV_ERR_SHAPE;
+    if (num_groups > 0 && (!group_starts || !prefix_blocks)) return PKV_ERR_NULL;
+    if (num_groups > 0 && (max_group_size <= 0 || max_group_size > num_seqs)) return PKV_ERR_SHAPE;
+    if (!aligned(out, 4) || !aligned(lse_out, 4) || !aligned(workspace, 256)) return PKV_ERR_ALIGN;
+    if (workspace_bytes < pkv_prefix_workspace_bytes(num_seqs, num_q_heads, cache.head_dim,
+                                                     max_blocks_per_seq, max_prefix_blocks,
+                                                     partition_blocks))
+        return PKV_ERR_WORKSPACE;
+    const int32_t G = num_q_heads / cache.num_kv_heads;
+    const int32_t prefix_parts = prefix_parts_for(max_prefix_blocks, partition_blocks);
+    const int32_t suffix_parts = (max_blocks_per_seq + partition_blocks - 1) / partition_blocks;
+    const int32_t max_parts = prefix_parts + suffix_parts;
+    const int32_t chunks = num_groups > 0 ? (max_group_size * G + kColsPerCta - 1) / kColsPerCta : 1;
+    const int64_t prefix_ctas = (int64_t)cache.num_kv_heads * num_groups * chunks * prefix_parts;
+    const int64_t grid = prefix_ctas + (int64_t)cache.num_kv_heads * num_seqs * suffix_parts;
+    if (grid > INT32_MAX) return PKV_ERR_SHAPE;
+    if (num_seqs == 0) return PKV_OK;
+    CUtensorMap tk, tv;
+    int tok_major = 0;
+    st = make_kv_maps(&tk, &tv, k_cache, v_cache, cache, &tok_major);
+    if (st != PKV_OK) return st;
+    pkv::ColsParams p = cols_params_of(a, tok_major);
+    p.part_blocks = partition_blocks;
+    p.parts = max_parts;
+    p.split = 1;
+    p.max_parts = max_parts;
+    p.chunks = chunks;
+    p.part_out = static_cast<float *>(workspace);
+    p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                           splitk_lse_offset(num_seqs, num_q_heads, cache.head_dim, max_parts));
+    p.group_starts = group_starts;
+    p.prefix_blocks = prefix_blocks;
+    p.num_groups = num_groups;
+    p.max_group = max_group_size;
+    p.prefix_parts = prefix_parts;
+    p.prefix_ctas = (int32_t)prefix_ctas;
+    cudaError_t e = pkv::launch_attn_cols(cache.head_dim, tk, tv, p, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "shared-prefix attention launch");
+    e = pkv::launch_cascade_merge(p, cache.head_dim, reinterpret_cast<__nv_bfloat16 *>(out), lse_out, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "shared-prefix merge launch");
+}

@@ -1,0 +1,497 @@
+// pkv_attn_common.cuh - building blocks shared by the attention kernels: ring and tile
+// constants, the shared-memory layout, the swizzled tile addressing, the per-warp online-softmax
+// state and its tile update (QK^T and PV with mma.sync), the merge of warp states, and the TMA
+// producer side of the full/empty mbarrier ring.
+#pragma once
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// Pipeline depth (K+V tile pairs in flight per CTA), CTAs per SM and producer warps per CTA.  The
+// bytes in flight per SM (stages x 8 KiB x CTAs at H = 128) must cover HBM latency under full
+// load, and one producer warp issues only about 2.6 M tiles/s (two TMA tile loads each), so a CTA
+// needs more than one to keep its ring full.
+#ifndef PKV_STAGES
+#define PKV_STAGES 8
+#endif
+#ifndef PKV_CTAS_PER_SM
+#define PKV_CTAS_PER_SM 3
+#endif
+#ifndef PKV_BAL_STAGES
+#define PKV_BAL_STAGES 8
+#endif
+#ifndef PKV_BAL_WARPS
+#define PKV_BAL_WARPS 4
+#endif
+#ifndef PKV_BAL_CTAS_PER_SM
+#define PKV_BAL_CTAS_PER_SM 2
+#endif
+
+#ifndef PKV_PRODUCERS
+#define PKV_PRODUCERS 2
+#endif
+#ifndef PKV_BAL_PRODUCERS
+#define PKV_BAL_PRODUCERS 2
+#endif
+
+#ifndef PKV_FP8_STAGES
+#define PKV_FP8_STAGES 16
+#endif
+
+#ifndef PKV_CONSUMERS
+#define PKV_CONSUMERS 4
+#endif
+constexpr int kConsumerWarps = PKV_CONSUMERS;
+constexpr int kStages = PKV_STAGES;
+constexpr int kStagesFp8 = PKV_FP8_STAGES;  // e4m3 tiles are half the bytes: twice the depth
+constexpr int kProducers = PKV_PRODUCERS;
+constexpr int kAttnThreads = (kConsumerWarps + kProducers) * 32;
+constexpr int kBalStages = PKV_BAL_STAGES;
+constexpr int kBalWarps = PKV_BAL_WARPS;
+constexpr int kBalProducers = PKV_BAL_PRODUCERS;
+constexpr int kBalThreads = (kBalWarps + kBalProducers) * 32;
+// Stage s is reused by tiles s, s+S, s+2S, ... and tile i goes to consumer warp i % W.  With
+// S a multiple of W every use of a stage belongs to the same warp, so a warp only waits for a
+// stage's next phase after it consumed the previous one and mbarrier parities cannot alias.
+// The same holds for the producer warps (producer p issues tiles i = p mod P).
+static_assert(kStages % kConsumerWarps == 0, "pipeline depth must be a multiple of the consumer warps");
+static_assert(kBalStages % kBalWarps == 0, "pipeline depth must be a multiple of the consumer warps");
+static_assert(kStages % kProducers == 0, "pipeline depth must be a multiple of the producer warps");
+static_assert(kStagesFp8 % kConsumerWarps == 0 && kStagesFp8 % kProducers == 0,
+              "pipeline depth must be a multiple of the consumer and producer warps");
+static_assert(kBalStages % kBalProducers == 0, "pipeline depth must be a multiple of the producer warps");
+
+// Lazy rescaling: keep the running maximum until a new logit exceeds it by this much
+// (log2 units), so exponentials stay <= 2^8 and the accumulator is rarely rescaled.
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int H, int S = kStages, int W = kConsumerWarps, int P = kProducers, int EB = 2>
+struct AttnLayout {
+    static constexpr int kHalves = H / 64;                  // 128-byte rows per bf16 token row
+    static constexpr int kTileBytes = kBlockSize * H * EB;  // one K or V tile (EB bytes/element)
+    static constexpr int kStageBytes = 2 * kTileBytes;      // K tile then V tile
+    static constexpr int kPipeBytes = S * kStageBytes;
+    static constexpr int kMergeBytes = W * 8 * (H + 2) * 4;
+    // single-pass / partition kernel: the merge area reuses the drained pipeline
+    static constexpr int kDataBytes = kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes;
+    static constexpr int kBarOffset = kDataBytes;           // full[S], empty[S]
+    static constexpr int kMiscOffset = kBarOffset + 2 * S * 8;  // slot_ok[S], abort, issued[P]
+    static constexpr int kBytes = kMiscOffset + (S + 1 + P) * 4;
+    static constexpr int kAlloc = kBytes + 1024;             // slack for 1024-byte alignment
+    // balanced kernel: pipeline, its own merge area, barriers, misc, then the block prefix
+    static constexpr int kBalMergeOffset = kPipeBytes;
+    static constexpr int kBalBarOffset = kBalMergeOffset + kMergeBytes;
+    static constexpr int kBalMiscOffset = kBalBarOffset + 2 * S * 8;
+    // misc: int64 issued[P], abort flag (padded to 8 bytes), slot_ok[S]
+    static constexpr int kBalSeqOffset = (kBalMiscOffset + 8 * P + 8 + S * 4 + 15) / 16 * 16;
+    static int balanced_alloc(int B) { return kBalSeqOffset + (B + 1) * 8 + 1024; }
+    static_assert(kBalMiscOffset % 8 == 0, "the balanced kernel's int64 counter needs 8-byte alignment");
+    static_assert(kBalSeqOffset % 16 == 0 && kPipeBytes % 1024 == 0, "shared-memory layout alignment");
+    static_assert(kTileBytes % 1024 == 0, "TMA destinations with 128B swizzle need 1024-byte alignment");
+};
+
+// Byte offset inside a TMA-written, 128B-swizzled tile of the 16-byte chunk holding
+// elements h .. h+7 of token row tok.  Tile rows are 128 bytes; with half-major tiles the
+// row of (tok, half) is half*16 + tok, with token-major tiles tok*kHalves + half.  The
+// swizzle XORs the chunk index with the row index mod 8 (tile base 1024-byte aligned).
+template <int H>
+__device__ __forceinline__ uint32_t tile_chunk_offset(int tok, int h, int tok_major)
+{
+    constexpr int kHalves = AttnLayout<H>::kHalves;
+    const int half = h >> 6;
+    const int chunk = (h & 63) >> 3;
+    const int row = tok_major ? tok * kHalves + half : half * kBlockSize + tok;
+    return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// ----------------------------- per-warp online-softmax state -----------------------------
+template <int H>
+struct WarpAcc {
+    float o[H / 16][4];  // O^T fragments: rows h (16 per m-tile), columns g = c0, c0+1
+    float m[2];          // running max of columns c0, c0+1 (log2 units)
+    float l[2];          // this lane's share of the running sums
+};
+
+template <int H>
+__device__ __forceinline__ void acc_reset(WarpAcc<H> &a)
+{
+#pragma unroll
+    for (int mt = 0; mt < H / 16; ++mt) a.o[mt][0] = a.o[mt][1] = a.o[mt][2] = a.o[mt][3] = 0.f;
+    a.m[0] = a.m[1] = -INFINITY;
+    a.l[0] = a.l[1] = 0.f;
+}
+
+// Q^T as the B operand of S^T = K . Q^T: lane l holds q[g = l/4][16kk + 2(l%4) + {0,1}] and
+// the same +8; rows g >= G are zero.
+template <int H>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[H / 16][2], const uint16_t *q, int N,
+                                             int b, int kvh, int G, int lane)
+{
+    const int g_row = lane >> 2, c0 = (lane & 3) * 2;
+    const bool live = g_row < G;
+    const uint16_t *qrow = q + ((size_t)b * N + (size_t)kvh * G + (live ? g_row : 0)) * H;
+#pragma unroll
+    for (int kk = 0; kk < H / 16; ++kk) {
+        qf[kk][0] = live ? __ldg(reinterpret_cast<const unsigned int *>(qrow + 16 * kk + c0)) : 0u;
+        qf[kk][1] = live ? __ldg(reinterpret_cast<const unsigned int *>(qrow + 16 * kk + c0 + 8)) : 0u;
+    }
+}
+
+// One 16-token tile (the first `valid` tokens count) folded into a warp's state.
+template <int H>
+__device__ __forceinline__ void tile_update(WarpAcc<H> &a, const uint32_t (&qf)[H / 16][2],
+                                            uint32_t kt, uint32_t vt, int valid, float sl2,
+                                            int tok_major, int lane)
+{
+    constexpr int kKSteps = H / 16;
+    const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: lane feeds matrix mi, row ri
+    const int k_tok = ri + 8 * (mi & 1), k_hoff = 8 * (mi >> 1);  // K as A (non-trans)
+    const int v_tok = ri + 8 * (mi >> 1), v_hoff = 8 * (mi & 1);  // V^T as A (trans)
+
+    // S^T = K . Q^T, two independent accumulation chains
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < kKSteps; kk += 2) {
+        uint32_t a0[4], a1[4];
+        ldsm_x4(a0, kt + tile_chunk_offset<H>(k_tok, 16 * kk + k_hoff, tok_major));
+        ldsm_x4(a1, kt + tile_chunk_offset<H>(k_tok, 16 * kk + 16 + k_hoff, tok_major));
+        mma_bf16_16816(sa, a0, qf[kk][0], qf[kk][1]);
+        mma_bf16_16816(sb, a1, qf[kk + 1][0], qf[kk + 1][1]);
+    }
+    // rows: tokens t0 = lane/4 and t1 = t0 + 8; columns: g = c0, c0+1
+    const int t0 = lane >> 2, t1 = t0 + 8;
+    const float x0 = t0 < valid ? (sa[0] + sb[0]) * sl2 : -INFINITY;
+    const float x1 = t0 < valid ? (sa[1] + sb[1]) * sl2 : -INFINITY;
+    const float x2 = t1 < valid ? (sa[2] + sb[2]) * sl2 : -INFINITY;
+    const float x3 = t1 < valid ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+    float mA = fmaxf(x0, x2), mB = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mA = fmaxf(mA, __shfl_xor_sync(0xFFFFFFFFu, mA, off));
+        mB = fmaxf(mB, __shfl_xor_sync(0xFFFFFFFFu, mB, off));
+    }
+    const bool needA = mA > a.m[0] + kRescaleThreshold;
+    const bool needB = mB > a.m[1] + kRescaleThreshold;
+    if (__any_sync(0xFFFFFFFFu, needA || needB)) {
+        const float alphaA = needA ? exp2f(a.m[0] - mA) : 1.f;
+        const float alphaB = needB ? exp2f(a.m[1] - mB) : 1.f;
+        if (needA) a.m[0] = mA;
+        if (needB) a.m[1] = mB;
+        a.l[0] *= alphaA;
+        a.l[1] *= alphaB;
+#pragma unroll
+        for (int mt = 0; mt < kKSteps; ++mt) {
+            a.o[mt][0] *= alphaA;
+            a.o[mt][1] *= alphaB;
+            a.o[mt][2] *= alphaA;
+            a.o[mt][3] *= alphaB;
+        }
+    }
+    const uint32_t p01 = pack_bf16x2(exp2f(x0 - a.m[0]), exp2f(x1 - a.m[1]));
+    const uint32_t p23 = pack_bf16x2(exp2f(x2 - a.m[0]), exp2f(x3 - a.m[1]));
+    a.l[0] += bf16x2_lo(p01) + bf16x2_lo(p23);  // sums of the rounded weights
+    a.l[1] += bf16x2_hi(p01) + bf16x2_hi(p23);
+    const uint32_t pb0 = movmatrix_trans(p01);    // P^T rows tok 0-7 -> B fragment
+    const uint32_t pb1 = movmatrix_trans(p23);    // tok 8-15
+
+    // O^T += V^T . P^T
+    const bool partial = valid < kBlockSize;
+    const int tc = (lane & 3) * 2;  // token columns of this lane's A fragment
+#pragma unroll
+    for (int mt = 0; mt < kKSteps; ++mt) {
+        uint32_t av[4];
+        ldsm_x4_trans(av, vt + tile_chunk_offset<H>(v_tok, 16 * mt + v_hoff, tok_major));
+        if (partial) {  // zero V of tokens past the context (they may be NaN poison)
+            const uint32_t lo0 = tc < valid ? 0x0000FFFFu : 0u;
+            const uint32_t hi0 = tc + 1 < valid ? 0xFFFF0000u : 0u;
+            const uint32_t lo1 = tc + 8 < valid ? 0x0000FFFFu : 0u;
+            const uint32_t hi1 = tc + 9 < valid ? 0xFFFF0000u : 0u;
+            av[0] &= lo0 | hi0;
+            av[1] &= lo0 | hi0;
+            av[2] &= lo1 | hi1;
+            av[3] &= lo1 | hi1;
+        }
+        mma_bf16_16816(a.o[mt], av, pb0, pb1);
+    }
+}
+
+// ------------------------------------ FP8 (e4m3) tiles ------------------------------------
+// An e4m3 tile is 16 token rows of H = 128 bytes (128B-swizzled).  ldmatrix reads it as b16
+// pairs and cvt widens pairs to f16 exactly, so the contractions run as f16 mma.sync.  Reading
+// b16 pairs permutes the head dimension inside each 16-element step; q (the other operand of
+// QK^T) is loaded in the same order, and in P.V the accumulator rows come out as
+// h = 16*mt + 2*(lane/4) (+1 for the upper 8 rows) instead of 16*mt + lane/4 (+8).
+__device__ __forceinline__ uint32_t fp8_chunk_offset(int tok, int chunk)
+{
+    return static_cast<uint32_t>(tok * 128 + ((chunk ^ (tok & 7)) << 4));
+}
+
+// q as f16 B fragments: k-step kk, lane (g = lane/4, m = lane%4): b0 = q[16kk + 4m .. +1],
+// b1 = q[16kk + 4m + 2 .. +3]; rows g >= G are zero.
+template <int H>
+__device__ __forceinline__ void load_q_frags_fp8(uint32_t (&qf)[H / 16][2], const uint16_t *q, int N,
+                                                 int b, int kvh, int G, int lane)
+{
+    const int g_row = lane >> 2, m = lane & 3;
+    const bool live = g_row < G;
+    const uint16_t *qrow = q + ((size_t)b * N + (size_t)kvh * G + (live ? g_row : 0)) * H;
+#pragma unroll
+    for (int kk = 0; kk < H / 16; ++kk) {
+        if (live) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(qrow + 16 * kk + 4 * m));
+            qf[kk][0] = pack_f16x2(bf16_to_f32((uint16_t)(v.x & 0xFFFFu)), bf16_to_f32((uint16_t)(v.x >> 16)));
+            qf[kk][1] = pack_f16x2(bf16_to_f32((uint16_t)(v.y & 0xFFFFu)), bf16_to_f32((uint16_t)(v.y >> 16)));
+        } else {
+            qf[kk][0] = qf[kk][1] = 0u;
+        }
+    }
+}
+
+// One 16-token e4m3 tile folded into a warp's state (the codes only; the per-head scales are
+// folded into sl2 and into the final normalisation).
+template <int H>
+__device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&qf)[H / 16][2],
+                                                uint32_t kt, uint32_t vt, int valid, float sl2, int lane)
+{
+    constexpr int kKSteps = H / 16;
+    const int mi = lane >> 3, ri = lane & 7;
+    const int tok = ri + 8 * (mi & 1), coff = mi >> 1;  // ldmatrix row address of this lane
+
+    // S^T = K . Q^T
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < kKSteps; kk += 2) {
+        uint32_t r[4];
+        ldsm_x4(r, kt + fp8_chunk_offset(tok, kk + coff));
+        uint32_t a0[4], a1[4];
+        a0[0] = e4m3x2_to_f16x2((uint16_t)(r[0] & 0xFFFFu));
+        a0[1] = e4m3x2_to_f16x2((uint16_t)(r[1] & 0xFFFFu));
+        a0[2] = e4m3x2_to_f16x2((uint16_t)(r[0] >> 16));
+        a0[3] = e4m3x2_to_f16x2((uint16_t)(r[1] >> 16));
+        a1[0] = e4m3x2_to_f16x2((uint16_t)(r[2] & 0xFFFFu));
+        a1[1] = e4m3x2_to_f16x2((uint16_t)(r[3] & 0xFFFFu));
+        a1[2] = e4m3x2_to_f16x2((uint16_t)(r[2] >> 16));
+        a1[3] = e4m3x2_to_f16x2((uint16_t)(r[3] >> 16));
+        mma_f16_16816(sa, a0, qf[kk][0], qf[kk][1]);
+        mma_f16_16816(sb, a1, qf[kk + 1][0], qf[kk + 1][1]);
+    }
+    const int t0 = lane >> 2, t1 = t0 + 8;
+    const float x0 = t0 < valid ? (sa[0] + sb[0]) * sl2 : -INFINITY;
+    const float x1 = t0 < valid ? (sa[1] + sb[1]) * sl2 : -INFINITY;
+    const float x2 = t1 < valid ? (sa[2] + sb[2]) * sl2 : -INFINITY;
+    const float x3 = t1 < valid ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+    float mA = fmaxf(x0, x2), mB = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mA = fmaxf(mA, __shfl_xor_sync(0xFFFFFFFFu, mA, off));
+        mB = fmaxf(mB, __shfl_xor_sync(0xFFFFFFFFu, mB, off));
+    }
+    const bool needA = mA > a.m[0] + kRescaleThreshold;
+    const bool needB = mB > a.m[1] + kRescaleThreshold;
+    if (__any_sync(0xFFFFFFFFu, needA || needB)) {
+        const float alphaA = needA ? exp2f(a.m[0] - mA) : 1.f;
+        const float alphaB = needB ? exp2f(a.m[1] - mB) : 1.f;
+        if (needA) a.m[0] = mA;
+        if (needB) a.m[1] = mB;
+        a.l[0] *= alphaA;
+        a.l[1] *= alphaB;
+#pragma unroll
+        for (int mt = 0; mt < kKSteps; ++mt) {
+            a.o[mt][0] *= alphaA;
+            a.o[mt][1] *= alphaB;
+            a.o[mt][2] *= alphaA;
+            a.o[mt][3] *= alphaB;
+        }
+    }
+    const uint32_t p01 = pack_f16x2(exp2f(x0 - a.m[0]), exp2f(x1 - a.m[1]));
+    const uint32_t p23 = pack_f16x2(exp2f(x2 - a.m[0]), exp2f(x3 - a.m[1]));
+    a.l[0] += f16x2_lo(p01) + f16x2_lo(p23);
+    a.l[1] += f16x2_hi(p01) + f16x2_hi(p23);
+    const uint32_t pb0 = movmatrix_trans(p01);
+    const uint32_t pb1 = movmatrix_trans(p23);
+
+    // O^T += V^T . P^T: ldmatrix.trans gives lane bytes (tok 2m, h 2c'), (tok 2m, h 2c'+1),
+    // (tok 2m+1, h 2c'), (tok 2m+1, h 2c'+1) with c' = lane/4; prmt regroups them per h.
+    const bool partial = valid < kBlockSize;
+    const int tc = (lane & 3) * 2;
+#pragma unroll
+    for (int mt = 0; mt < kKSteps; mt += 2) {
+        uint32_t r[4];
+        ldsm_x4_trans(r, vt + fp8_chunk_offset(tok, mt + coff));
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const uint32_t lo = byte_perm(r[2 * hf], 0u, 0x3120u);      // tokens 0-7 of the tile
+            const uint32_t hi = byte_perm(r[2 * hf + 1], 0u, 0x3120u);  // tokens 8-15
+            uint32_t av[4];
+            av[0] = e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu));
+            av[1] = e4m3x2_to_f16x2((uint16_t)(lo >> 16));
+            av[2] = e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu));
+            av[3] = e4m3x2_to_f16x2((uint16_t)(hi >> 16));
+            if (partial) {
+                const uint32_t lo0 = tc < valid ? 0x0000FFFFu : 0u;
+                const uint32_t hi0 = tc + 1 < valid ? 0xFFFF0000u : 0u;
+                const uint32_t lo1 = tc + 8 < valid ? 0x0000FFFFu : 0u;
+                const uint32_t hi1 = tc + 9 < valid ? 0xFFFF0000u : 0u;
+                av[0] &= lo0 | hi0;
+                av[1] &= lo0 | hi0;
+                av[2] &= lo1 | hi1;
+                av[3] &= lo1 | hi1;
+            }
+            mma_f16_16816(a.o[mt + hf], av, pb0, pb1);
+        }
+    }
+}
+
+// Finish a warp's sums (across the lanes that share a column) and store its state in the
+// merge area: mo[W][8][H], mm[W][8] (running max), ml[W][8] (running sum).
+template <int H, bool kFp8 = false>
+__device__ __forceinline__ void deposit(WarpAcc<H> &a, float *mo, float *mm, float *ml, int warp,
+                                        int lane)
+{
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        a.l[0] += __shfl_xor_sync(0xFFFFFFFFu, a.l[0], off);
+        a.l[1] += __shfl_xor_sync(0xFFFFFFFFu, a.l[1], off);
+    }
+    const int c0 = (lane & 3) * 2;
+    if (lane < 4) {
+        mm[warp * 8 + c0] = a.m[0];
+        mm[warp * 8 + c0 + 1] = a.m[1];
+        ml[warp * 8 + c0] = a.l[0];
+        ml[warp * 8 + c0 + 1] = a.l[1];
+    }
+    const int hr = lane >> 2;
+#pragma unroll
+    for (int mt = 0; mt < H / 16; ++mt) {
+        // rows of the accumulator: h0 for o[mt][0..1], h1 for o[mt][2..3]
+        const int h0 = kFp8 ? 16 * mt + 2 * hr : 16 * mt + hr;
+        const int h1 = kFp8 ? h0 + 1 : h0 + 8;
+        mo[(warp * 8 + c0) * H + h0] = a.o[mt][0];
+        mo[(warp * 8 + c0 + 1) * H + h0] = a.o[mt][1];
+        mo[(warp * 8 + c0) * H + h1] = a.o[mt][2];
+        mo[(warp * 8 + c0 + 1) * H + h1] = a.o[mt][3];
+    }
+}
+
+// Combine the deposited states for column g, element h: normalised output and lse (natural).
+template <int H, int W = kConsumerWarps>
+__device__ __forceinline__ void combine(const float *mo, const float *mm, const float *ml, int g,
+                                        int h, float &val, float &lse)
+{
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) M = fmaxf(M, mm[w * 8 + g]);
+    float acc = 0.f, lsum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            const float sc = exp2f(mm[w * 8 + g] - M);
+            lsum += sc * ml[w * 8 + g];
+            acc += sc * mo[(w * 8 + g) * H + h];
+        }
+    }
+    // No key at all (M = -inf) gives 0 and -inf; a NaN anywhere in the inputs stays NaN.
+    val = M != -INFINITY ? acc / lsum : 0.f;
+    lse = M != -INFINITY ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+}
+
+template <int S>
+__device__ __forceinline__ void init_ring(uint32_t bar_full, uint32_t bar_empty)
+{
+    for (int s = 0; s < S; ++s) {
+        mbar_init(bar_full + 8 * s, 1);
+        mbar_init(bar_empty + 8 * s, 1);
+    }
+    fence_barrier_init();
+}
+
+// Producer side of one tile: wait for the stage to be free, then load the tile (or mark it
+// skipped).  Runs on one lane.  Returns false when the wait expired.  bf16 tiles come through
+// 5-D maps (half-major or token-major), e4m3 tiles through a 4-D map (h, head, token, block).
+template <int H, int S, bool kFp8 = false>
+__device__ __forceinline__ bool produce_tile(int64_t i, int kvh, int bid, bool ok, uint32_t base_u32,
+                                             uint32_t bar_full, uint32_t bar_empty,
+                                             volatile int *slot_ok, volatile int *abort_flag,
+                                             const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                                             int tok_major, int32_t *err_flag)
+{
+    using L = AttnLayout<H, S, kConsumerWarps, kProducers, kFp8 ? 1 : 2>;
+    const int s = (int)(i % S);
+    if (i >= S &&
+        !mbar_wait_bounded(bar_empty + 8 * s, (uint32_t)(((i / S) & 1) ^ 1), abort_flag,
+                           kWaitLimitNs)) {
+        if (!*abort_flag) set_flag(err_flag, PKV_FLAG_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+    }
+    if (ok) {
+        slot_ok[s] = 1;
+        const uint32_t dst = base_u32 + s * L::kStageBytes;
+        const uint32_t bar = bar_full + 8 * s;
+        mbar_arrive_expect_tx(bar, L::kStageBytes);
+        if (kFp8) {
+            tma_load_4d(dst, tm_k, bar, 0, kvh, 0, bid);
+            tma_load_4d(dst + L::kTileBytes, tm_v, bar, 0, kvh, 0, bid);
+        } else if (tok_major) {
+            tma_load_5d(dst, tm_k, bar, 0, 0, kvh, 0, bid);
+            tma_load_5d(dst + L::kTileBytes, tm_v, bar, 0, 0, kvh, 0, bid);
+        } else {
+            tma_load_5d(dst, tm_k, bar, 0, 0, 0, kvh, bid);
+            tma_load_5d(dst + L::kTileBytes, tm_v, bar, 0, 0, 0, kvh, bid);
+        }
+    } else {
+        slot_ok[s] = 0;  // out-of-range block id: the tile is skipped
+        mbar_arrive(bar_full + 8 * s);
+    }
+    return true;
+}
+
+// Producer warp p of P issues the CTA's tiles i = p, p + P, p + 2P, ... in order: `lookup(i)`
+// gives tile i's physical block id (lanes look up 32 tiles at a time, the next 32 while the
+// current ones are issued) and `issue(i, bid, ok)` waits for the stage and loads it, returning
+// false when its wait expired.  Returns the number of tiles this producer issued (on lane 0).
+template <int P, typename Lookup, typename Issue>
+__device__ __forceinline__ int64_t run_producer(int pw, int lane, int64_t n, Lookup lookup,
+                                                int num_blocks, int32_t *err_flag, Issue issue)
+{
+    const int64_t mine = n > pw ? (n - pw + P - 1) / P : 0;
+    int cur = lane < mine ? lookup(pw + (int64_t)P * lane) : 0;
+    int64_t issued = 0;
+    bool aborted = false;
+    for (int64_t k0 = 0; k0 < mine && !aborted; k0 += 32) {
+        const int nxt = (k0 + 32 + lane < mine) ? lookup(pw + (int64_t)P * (k0 + 32 + lane)) : 0;
+        const int cnt = (int)min((int64_t)32, mine - k0);
+        const bool bad = lane < cnt && (cur < 0 || cur >= num_blocks);
+        const unsigned badmask = __ballot_sync(0xFFFFFFFFu, bad);
+        if (badmask && lane == 0) set_flag(err_flag, PKV_FLAG_BLOCK_RANGE);
+        for (int k = 0; k < cnt; ++k) {
+            const int bid = __shfl_sync(0xFFFFFFFFu, cur, k);
+            int lane0_abort = 0;
+            if (lane == 0) {
+                if (issue(pw + (int64_t)P * (k0 + k), bid, !((badmask >> k) & 1u)))
+                    ++issued;
+                else
+                    lane0_abort = 1;
+            }
+            aborted = __shfl_sync(0xFFFFFFFFu, lane0_abort, 0) != 0;
+            if (aborted) break;
+        }
+        cur = nxt;
+    }
+    return issued;
+}
+
+// Drain after an expired wait: producer pw waits (bounded) for its copies that may still land.
+template <int S, int P>
+__device__ __forceinline__ void drain_ring(uint32_t bar_full, int pw, int64_t issued)
+{
+    for (int64_t k = issued > S / P ? issued - S / P : 0; k < issued; ++k) {
+        const int64_t i = pw + (int64_t)P * k;
+        mbar_wait_bounded(bar_full + 8 * (int)(i % S), (uint32_t)((i / S) & 1), nullptr, kDrainLimitNs);
+    }
+}
+
+}  // namespace pkv

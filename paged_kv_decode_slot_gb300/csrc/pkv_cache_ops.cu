@@ -94,6 +94,75 @@ __global__ void gather_kernel(const uint4 *__restrict__ k_cache, const uint4 *__
     }
 }
 
+// Slots of the last T logical positions of each sequence (several new tokens per step):
+// slot[b][t] for position ctx_b - T + t; -1 below position 0.
+__global__ void slot_mapping_multi_kernel(const int32_t *__restrict__ block_tables, int max_nb,
+                                          const int32_t *__restrict__ context_lens, int B, int T,
+                                          int num_blocks, int64_t *__restrict__ slots, int32_t *err_flag)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)B * T) return;
+    const int b = (int)(i / T), t = (int)(i - (int64_t)b * T);
+    const int ctx = context_lens[b];
+    int64_t slot = -1;
+    if (ctx > max_nb * kBlockSize) {
+        if (t == 0) set_flag(err_flag, PKV_FLAG_CTX_RANGE);
+    } else {
+        const int pos = ctx - T + t;
+        if (pos >= 0) {
+            const int blk = block_tables[(size_t)b * max_nb + pos / kBlockSize];
+            if (blk < 0 || blk >= num_blocks)
+                set_flag(err_flag, PKV_FLAG_BLOCK_RANGE);
+            else
+                slot = (int64_t)blk * kBlockSize + pos % kBlockSize;
+        }
+    }
+    slots[i] = slot;
+}
+
+// Copy-on-write: block dst of both pools becomes a byte copy of block src, one CTA per pair
+// ("Optimización de la inferencia", "Página Atención": a request that diverges from a shared
+// prefix gets its own pages; CS336 Lecture 10 transcript 01:23:17: split the block).
+__global__ void copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                                   const int32_t *__restrict__ src_dst, int num_blocks,
+                                   int64_t vec_per_block, int32_t *err_flag)
+{
+    const int i = blockIdx.x;
+    const int src = src_dst[2 * i], dst = src_dst[2 * i + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (threadIdx.x == 0) set_flag(err_flag, PKV_FLAG_BLOCK_RANGE);
+        return;
+    }
+    if (src == dst) return;
+    const uint4 *ks = k_cache + (int64_t)src * vec_per_block, *vs = v_cache + (int64_t)src * vec_per_block;
+    uint4 *kd = k_cache + (int64_t)dst * vec_per_block, *vd = v_cache + (int64_t)dst * vec_per_block;
+    for (int64_t x = threadIdx.x; x < vec_per_block; x += blockDim.x) {
+        kd[x] = ks[x];
+        vd[x] = vs[x];
+    }
+}
+
+cudaError_t launch_slot_mapping_multi(const int32_t *block_tables, int max_nb,
+                                      const int32_t *context_lens, int B, int T, int num_blocks,
+                                      int64_t *slots, int32_t *err_flag, cudaStream_t stream)
+{
+    const int threads = 128;
+    const int64_t n = (int64_t)B * T;
+    slot_mapping_multi_kernel<<<(unsigned)((n + threads - 1) / threads), threads, 0, stream>>>(
+        block_tables, max_nb, context_lens, B, T, num_blocks, slots, err_flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(uint8_t *k_cache, uint8_t *v_cache, const int32_t *src_dst, int n,
+                               int num_blocks, int64_t block_bytes, int32_t *err_flag,
+                               cudaStream_t stream)
+{
+    copy_blocks_kernel<<<n, 256, 0, stream>>>(reinterpret_cast<uint4 *>(k_cache),
+                                              reinterpret_cast<uint4 *>(v_cache), src_dst, num_blocks,
+                                              block_bytes / 16, err_flag);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_slot_mapping(const int32_t *block_tables, int max_nb, const int32_t *context_lens,
                                 int B, int num_blocks, int64_t *slots, int32_t *err_flag,
                                 cudaStream_t stream)

@@ -44,6 +44,54 @@ struct AttnParams {
 cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensorMap &tv,
                         const AttnParams &p, cudaStream_t stream, bool fp8 = false);
 
+// Column-parallel attention (pkv_attn_cols.cu): a CTA serves up to 32 query rows ("columns")
+// of one KV head over one list of logical blocks; each consumer warp owns 8 columns, and every
+// column has its own visibility limit.  Two uses:
+//  * several new tokens per sequence (group_starts == nullptr): work unit = (sequence, KV head,
+//    column chunk, partition); column j of a sequence is token t = j / G, head g = j % G, and
+//    sees the tokens [0, ctx - T + t];
+//  * shared prefixes (group_starts != nullptr): the first prefix_ctas CTAs run the prefix pass
+//    (work unit = (group, KV head, column chunk, prefix partition); columns are the group's
+//    members x G heads, blocks come from the group's first member's table), the rest run each
+//    sequence's suffix (work unit = (sequence, KV head, suffix partition)).  All write partials.
+struct ColsParams {
+    const uint16_t *q;             // multi: [B][T][N][H]; prefix: [B][N][H]
+    const int32_t *block_tables;   // [B][max_nb]
+    const int32_t *context_lens;   // [B]
+    int32_t max_nb;
+    int32_t B, N, K, G, T;
+    int32_t num_blocks;
+    float scale_log2;
+    int32_t tok_major;
+    int32_t part_blocks;           // blocks per partition
+    int32_t parts;                 // multi: partitions per sequence
+    int32_t split;                 // multi: write partials (1) or final outputs (0, parts == 1)
+    int32_t max_parts;             // partition stride of part_out / part_lse
+    int32_t chunks;                // column chunks of 32 per work unit
+    __nv_bfloat16 *out;            // multi, one pass: [rows][H]
+    float *lse_out;                // nullable
+    float *part_out;               // [rows][max_parts][H]
+    float *part_lse;               // [rows][max_parts]
+    const int32_t *group_starts;   // prefix mode: [num_groups + 1]
+    const int32_t *prefix_blocks;  // prefix mode: [num_groups] shared leading blocks per group
+    int32_t num_groups;
+    int32_t max_group;             // prefix mode: declared bound on the members of a group
+    int32_t prefix_parts;          // prefix mode: partition slots of the prefix pass
+    int32_t prefix_ctas;           // prefix mode: CTAs of the prefix pass
+    int32_t *err_flag;
+};
+
+cudaError_t launch_attn_cols(int H, const CUtensorMap &tk, const CUtensorMap &tv, const ColsParams &p,
+                             int64_t grid, cudaStream_t stream);
+cudaError_t launch_cascade_merge(const ColsParams &p, int H, __nv_bfloat16 *out, float *lse_out,
+                                 cudaStream_t stream);
+cudaError_t launch_slot_mapping_multi(const int32_t *block_tables, int max_nb,
+                                      const int32_t *context_lens, int B, int T, int num_blocks,
+                                      int64_t *slots, int32_t *err_flag, cudaStream_t stream);
+cudaError_t launch_copy_blocks(uint8_t *k_cache, uint8_t *v_cache, const int32_t *src_dst, int n,
+                               int num_blocks, int64_t block_bytes, int32_t *err_flag,
+                               cudaStream_t stream);
+
 cudaError_t launch_quantize_fp8(const uint16_t *src, int64_t rows, int K, int H, const float *scale,
                                 uint8_t *dst, cudaStream_t stream);
 

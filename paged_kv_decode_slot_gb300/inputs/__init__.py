@@ -149,6 +149,14 @@ class Workload:
         t = self.unique_tokens if self.unique_tokens is not None else self.total_tokens
         return t * self.K * self.H * 2 * 2
 
+    def prefix_groups(self):
+        """(group_starts int32 [G+1], prefix_blocks int32 [G]) of the sequences that share leading
+        blocks: one group of the whole batch for the shared-prefix workloads, else None."""
+        full = self.notes.get("shared_blocks")
+        if full is None:
+            return None
+        return (np.array([0, self.B], dtype=np.int32), np.array([full], dtype=np.int32))
+
     def qo_bytes(self) -> int:
         return 2 * self.B * self.N * self.H * 2
 

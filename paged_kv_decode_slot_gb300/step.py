@@ -32,6 +32,8 @@ class AttentionPlan:
         return self.mode != "single"
 
     def describe(self) -> str:
+        if self.mode == "prefix":
+            return f"shared-prefix pass + {self.partition_blocks}-block suffix partitions, merged"
         if self.mode == "split":
             return f"split-KV, {self.partition_blocks}-block partitions (max {self.max_partitions})"
         if self.mode == "balanced":
@@ -139,6 +141,10 @@ class DecodeStep:
         attn = 2 if self.plan.split else 1
         return attn if self.fused else 2 + attn
 
+    def inputs(self):
+        """The tensors a caller refreshes every step (the pools are state)."""
+        return [self.q, self.k_new, self.v_new, self.block_tables, self.context_lens]
+
 
 class DecodeStepFp8:
     """A decode step over e4m3 pools with per-KV-head scales: one ``pkv_decode_step_fp8`` call
@@ -178,3 +184,127 @@ class DecodeStepFp8:
 
     def launches_per_step(self) -> int:
         return 2 if self.plan.mode == "split" else 1
+
+    def inputs(self):
+        return [self.q, self.k_new, self.v_new, self.block_tables, self.context_lens]
+
+
+class MultiTokenStep:
+    """Verification of T new tokens per sequence (speculative decoding): the slots of the last T
+    positions (``pkv_slot_mapping_multi``), the append of the B*T new K/V rows (``pkv_append``),
+    then ``pkv_decode_attn_multi`` -- one pass when the (sequence, KV head, 32-row chunk) units
+    cover the SMs, else fixed partitions sized like ``plan_attention``'s.
+
+    q [B, T, N, H] bf16; k_new/v_new [B, T, K, H]; pools, tables and lengths as ``DecodeStep``
+    (context_lens counts the T new tokens).
+    """
+
+    def __init__(self, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
+                 partition_blocks: int | None = None, err_flag=None):
+        self.q, self.k_new, self.v_new = q, k_new, v_new
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.block_tables, self.context_lens = block_tables, context_lens
+        self.scale = float(scale)
+        dev = q.device
+        nseq, T, N, H = q.shape
+        K = k_cache.shape[2]
+        self.T = T
+        self.num_blocks = k_cache.shape[0]
+        chunks = -(-T * (N // K) // 32)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.plan = plan_attention(nseq * chunks, K, block_tables.shape[1], sms,
+                                   partition_blocks=partition_blocks)
+        self.fused = False
+        self.slot_mapping = torch.empty(nseq, T, dtype=torch.int64, device=dev)
+        self.out = torch.empty_like(q)
+        self.lse = torch.empty(nseq, T, N, dtype=torch.float32, device=dev)
+        self.err_flag = err_flag
+        self.workspace = None
+        if self.plan.mode == "split":
+            nbytes = B.pkv_splitk_workspace_bytes(nseq * T, N, H, self.plan.max_partitions)
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def slot_and_append(self, stream=None) -> None:
+        nseq, T = self.q.shape[0], self.T
+        K, H = self.k_cache.shape[2], self.k_cache.shape[3]
+        B.check(B.pkv_slot_mapping_multi(self.block_tables, self.context_lens, self.num_blocks,
+                                         self.slot_mapping, self.err_flag, stream))
+        B.check(B.pkv_append(self.k_new.view(nseq * T, K, H), self.v_new.view(nseq * T, K, H),
+                             self.slot_mapping.view(-1), self.k_cache, self.v_cache, self.err_flag,
+                             stream))
+
+    def attention(self, stream=None) -> None:
+        split = self.plan.mode == "split"
+        B.check(B.pkv_decode_attn_multi(self.q, self.k_cache, self.v_cache, self.block_tables,
+                                        self.context_lens, self.scale, self.out, self.lse,
+                                        self.plan.partition_blocks if split else 0,
+                                        self.plan.max_partitions if split else 0, self.workspace,
+                                        self.err_flag, stream))
+
+    def run(self, stream=None) -> None:
+        self.slot_and_append(stream)
+        self.attention(stream)
+
+    def launches_per_step(self) -> int:
+        return 3 + (1 if self.plan.mode == "split" else 0)
+
+    def inputs(self):
+        return [self.q, self.k_new, self.v_new, self.block_tables, self.context_lens]
+
+
+class PrefixDecodeStep:
+    """A decode step of a batch whose sequences share leading blocks (copy-on-write prefix
+    sharing): slot mapping and append of the new token, then ``pkv_decode_attn_prefix`` -- each
+    group's shared blocks attended once per KV head for all its members, each sequence's own
+    blocks in partitions of ``partition_blocks``, merged by log-sum-exp.
+
+    group_starts int32 [G+1] and prefix_blocks int32 [G] on the device; max_group_size and
+    max_prefix_blocks are host-side bounds on them.
+    """
+
+    def __init__(self, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
+                 group_starts, prefix_blocks, max_group_size: int, max_prefix_blocks: int,
+                 partition_blocks: int = 16, err_flag=None):
+        self.q, self.k_new, self.v_new = q, k_new, v_new
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.block_tables, self.context_lens = block_tables, context_lens
+        self.group_starts, self.prefix_blocks = group_starts, prefix_blocks
+        self.max_group_size, self.max_prefix_blocks = int(max_group_size), int(max_prefix_blocks)
+        self.partition_blocks = int(partition_blocks)
+        self.scale = float(scale)
+        dev = q.device
+        nseq, N, H = q.shape
+        self.num_blocks = k_cache.shape[0]
+        self.plan = AttentionPlan("prefix", self.partition_blocks, 0)
+        self.fused = False
+        self.slot_mapping = torch.empty(nseq, dtype=torch.int64, device=dev)
+        self.out = torch.empty_like(q)
+        self.lse = torch.empty(nseq, N, dtype=torch.float32, device=dev)
+        self.err_flag = err_flag
+        nbytes = B.pkv_prefix_workspace_bytes(nseq, N, H, block_tables.shape[1], self.max_prefix_blocks,
+                                              self.partition_blocks)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def slot_and_append(self, stream=None) -> None:
+        B.check(B.pkv_slot_mapping(self.block_tables, self.context_lens, self.num_blocks,
+                                   self.slot_mapping, self.err_flag, stream))
+        B.check(B.pkv_append(self.k_new, self.v_new, self.slot_mapping, self.k_cache, self.v_cache,
+                             self.err_flag, stream))
+
+    def attention(self, stream=None) -> None:
+        B.check(B.pkv_decode_attn_prefix(self.q, self.k_cache, self.v_cache, self.block_tables,
+                                         self.context_lens, self.scale, self.group_starts,
+                                         self.prefix_blocks, self.max_group_size,
+                                         self.max_prefix_blocks, self.out, self.lse,
+                                         self.partition_blocks, self.workspace, self.err_flag, stream))
+
+    def run(self, stream=None) -> None:
+        self.slot_and_append(stream)
+        self.attention(stream)
+
+    def launches_per_step(self) -> int:
+        return 4
+
+    def inputs(self):
+        return [self.q, self.k_new, self.v_new, self.block_tables, self.context_lens,
+                self.group_starts, self.prefix_blocks]

@@ -1,0 +1,295 @@
+"""Several new tokens per sequence, shared-prefix decode and copy-on-write, on the GPU.
+
+Multi-token decode (speculative verification): slots bit-exact, attention within the bf16
+tolerance of the oracle's masked attention, T = 1 bit-identical to the one-token kernel.
+Shared-prefix decode: within tolerance of the oracle's plain decode (the prefix pass plus suffix
+pass plus merge reach the same definition).  Block copies: bit-exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from devutil import (appended_host_cache, assert_close, assert_lse_close, bf16_dev, bf16_host, i32_dev,
+                     out_f64, upload)
+from paged_kv_decode_slot_gb300 import inputs as gen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_decode_slot_gb300.build import build_library
+    build_library()
+    import paged_kv_decode_slot_gb300 as pkv
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return pkv
+
+
+class MultiCase:
+    """A workload whose sequences each end with T new tokens, appended by the oracle."""
+
+    def __init__(self, oracle, w: gen.Workload, T: int, seed: int):
+        self.w, self.T = w, T
+        self.k_new = gen.normal_bf16(seed, 700, (w.B, T, w.K, w.H))
+        self.v_new = gen.normal_bf16(seed, 701, (w.B, T, w.K, w.H))
+        self.q = gen.normal_bf16(seed, 702, (w.B, T, w.N, w.H))
+        self.slots = oracle.slot_mapping_multi(w.block_tables, w.context_lens, T)
+        self.kc, self.vc = w.k_cache.copy(), w.v_cache.copy()
+        oracle.append(self.k_new.reshape(-1, w.K, w.H), self.v_new.reshape(-1, w.K, w.H),
+                      self.slots.reshape(-1), self.kc, self.vc)
+
+    def reference(self, oracle):
+        w = self.w
+        return oracle.decode_multi(self.q, self.kc, self.vc, w.block_tables, w.context_lens, w.scale)
+
+
+def run_multi(pkv, c: MultiCase, kc, vc, part_blocks, err=None):
+    w = c.w
+    q = bf16_dev(c.q)
+    out = torch.empty_like(q)
+    lse = torch.empty(w.B, c.T, w.N, dtype=torch.float32, device="cuda")
+    P, ws = 0, None
+    if part_blocks:
+        P = pkv.max_partitions_for(w.max_blocks, part_blocks)
+        ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B * c.T, w.N, w.H, P), dtype=torch.uint8,
+                         device="cuda")
+    pkv.check(pkv.pkv_decode_attn_multi(q, kc, vc, i32_dev(w.block_tables), i32_dev(w.context_lens),
+                                        w.scale, out, lse, part_blocks, P, ws, err))
+    return out, lse
+
+
+MULTI_CASES = [
+    # (name, N, K, H, context lengths) -- lengths below T, at block edges and long ones
+    ("gqa4_h128", 16, 4, 128, [1, 2, 3, 4, 5, 15, 16, 17, 33, 250, 700]),
+    ("gqa8_h128", 16, 2, 128, [3, 8, 16, 31, 64, 300]),
+    ("mha_h64", 4, 4, 64, [2, 9, 16, 17, 129]),
+    ("gqa2_h64", 8, 4, 64, [4, 20, 47]),
+]
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
+def test_slot_mapping_multi_matches_oracle(pkv, oracle, T):
+    w = gen.make_workload("m_slots", 70 + T, 8, 2, 64, [1, 2, 15, 16, 17, 40, 100])
+    slots = torch.full((w.B, T), -7, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.check(pkv.pkv_slot_mapping_multi(i32_dev(w.block_tables), i32_dev(w.context_lens), w.num_blocks,
+                                         slots, err))
+    assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
+    assert np.array_equal(slots.cpu().numpy(), oracle.slot_mapping_multi(w.block_tables, w.context_lens, T))
+
+
+@pytest.mark.parametrize("part_blocks", [0, 2, 5])
+@pytest.mark.parametrize("T", [1, 2, 4, 8])
+@pytest.mark.parametrize("name,N,K,H,ctx", MULTI_CASES, ids=[c[0] for c in MULTI_CASES])
+def test_decode_attn_multi_matches_oracle(pkv, oracle, name, N, K, H, ctx, T, part_blocks):
+    w = gen.make_workload(f"m_{name}", 80 + T, N, K, H, ctx)
+    c = MultiCase(oracle, w, T, 90 + T)
+    # the device append path: multi-token slot mapping, then the ordinary append
+    d = upload(w)
+    slots = torch.empty(w.B, T, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.check(pkv.pkv_slot_mapping_multi(d["block_tables"], d["context_lens"], w.num_blocks, slots, err))
+    pkv.check(pkv.pkv_append(bf16_dev(c.k_new.reshape(-1, K, H)), bf16_dev(c.v_new.reshape(-1, K, H)),
+                             slots.reshape(-1), d["k_cache"], d["v_cache"], err))
+    assert np.array_equal(bf16_host(d["k_cache"]), c.kc) and np.array_equal(bf16_host(d["v_cache"]), c.vc)
+    out, lse = run_multi(pkv, c, d["k_cache"], d["v_cache"], part_blocks, err)
+    assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
+    ref, ref_lse = c.reference(oracle)
+    assert_close(out_f64(out), ref, f"multi {name} T={T} pb={part_blocks}")
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), ref_lse, f"multi {name} T={T} pb={part_blocks}")
+
+
+@pytest.mark.parametrize("part_blocks", [0, 3])
+def test_multi_with_one_token_is_the_decode_kernel(pkv, oracle, part_blocks):
+    """T = 1 through the column-parallel kernel equals pkv_decode_attn / _splitk bit for bit."""
+    w = gen.make_workload("m_t1", 99, 32, 8, 128, gen.uniform_int(99, 9, 10, 1, 900))
+    kc, vc = appended_host_cache(oracle, w)
+    dk, dv = bf16_dev(kc), bf16_dev(vc)
+    q = bf16_dev(w.q)
+    bt, cl = i32_dev(w.block_tables), i32_dev(w.context_lens)
+    out1 = torch.empty_like(q)
+    lse1 = torch.empty(w.B, w.N, dtype=torch.float32, device="cuda")
+    out2 = torch.empty(w.B, 1, w.N, w.H, dtype=torch.bfloat16, device="cuda")
+    lse2 = torch.empty(w.B, 1, w.N, dtype=torch.float32, device="cuda")
+    if part_blocks:
+        P = pkv.max_partitions_for(w.max_blocks, part_blocks)
+        ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+        pkv.check(pkv.pkv_decode_attn_splitk(q, dk, dv, bt, cl, w.scale, out1, part_blocks, P, ws, lse1))
+        ws2 = torch.empty_like(ws)
+        pkv.check(pkv.pkv_decode_attn_multi(q.view(w.B, 1, w.N, w.H), dk, dv, bt, cl, w.scale, out2, lse2,
+                                            part_blocks, P, ws2))
+    else:
+        pkv.check(pkv.pkv_decode_attn(q, dk, dv, bt, cl, w.scale, out1, lse1))
+        pkv.check(pkv.pkv_decode_attn_multi(q.view(w.B, 1, w.N, w.H), dk, dv, bt, cl, w.scale, out2, lse2))
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(w.B, w.N, w.H).view(torch.int16))
+    assert torch.equal(lse1, lse2.view(w.B, w.N))
+
+
+def test_multi_full_size_sampled(pkv, oracle):
+    """Llama-3-8B-shaped batch of 64 verifying 4 tokens each (gamma = 3), one pass and partitions."""
+    w = gen.make_config("l3_8b_b64")
+    T = 4
+    c = MultiCase(oracle, w, T, 123)
+    kc, vc = bf16_dev(c.kc), bf16_dev(c.vc)
+    out, _ = run_multi(pkv, c, kc, vc, 0)
+    out_s, _ = run_multi(pkv, c, kc, vc, 64)
+    sample = [0, 5, 31, 62]
+    bt = np.ascontiguousarray(w.block_tables[sample])
+    cl = np.ascontiguousarray(w.context_lens[sample])
+    ref, _ = oracle.decode_multi(c.q[sample], c.kc, c.vc, bt, cl, w.scale)
+    assert_close(out_f64(out[sample]), ref, "multi l3_8b_b64 one pass")
+    assert_close(out_f64(out_s[sample]), ref, "multi l3_8b_b64 partitions")
+
+
+# ------------------------------------ copy-on-write ----------------------------------------
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_copy_blocks_matches_oracle(pkv, oracle, dtype):
+    w = gen.make_workload("cow", 111, 8, 2, 128, [20, 40, 9, 70], pool_blocks=40)
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    if dtype == "e4m3":
+        kc = (kc & 0xFF).astype(np.uint8)
+        vc = (vc >> 8).astype(np.uint8)
+    rng = np.random.default_rng(3)
+    perm = rng.permutation(w.num_blocks)
+    pairs = np.stack([perm[:10], perm[10:20]], axis=1).astype(np.int32)  # sources and distinct targets
+    ref_k, ref_v = kc.copy(), vc.copy()
+    oracle.copy_blocks(ref_k, ref_v, pairs)
+    if dtype == "bf16":
+        dk, dv = bf16_dev(kc), bf16_dev(vc)
+    else:
+        dk, dv = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.check(pkv.pkv_copy_blocks(dk, dv, i32_dev(pairs), err))
+    assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
+    got_k = bf16_host(dk) if dtype == "bf16" else dk.cpu().numpy()
+    got_v = bf16_host(dv) if dtype == "bf16" else dv.cpu().numpy()
+    assert np.array_equal(got_k, ref_k) and np.array_equal(got_v, ref_v)
+    # an id outside the pool is flagged and skipped
+    bad = i32_dev(np.array([[0, w.num_blocks]], dtype=np.int32))
+    pkv.check(pkv.pkv_copy_blocks(dk, dv, bad, err))
+    st, flag = pkv.pkv_read_err_flag(err)
+    assert st == pkv.PKV_ERR_RANGE and flag & pkv.PKV_FLAG_BLOCK_RANGE
+
+
+def test_copy_on_write_split_keeps_attention(pkv, oracle):
+    """Give every sequence of the shared-prefix batch a private copy of one shared block and point
+    its table there: attention is bit-identical."""
+    w = gen.make_config("prefix_l3_70b")
+    kc, vc = appended_host_cache(oracle, w)
+    dk, dv = bf16_dev(kc), bf16_dev(vc)
+    q = bf16_dev(w.q)
+    bt, cl = i32_dev(w.block_tables), i32_dev(w.context_lens)
+    out1 = torch.empty_like(q)
+    pkv.check(pkv.pkv_decode_attn(q, dk, dv, bt, cl, w.scale, out1))
+    used = set(w.block_tables[w.block_tables >= 0].tolist()) | {w.notes["orig_partial_block"]}
+    free = [x for x in range(w.num_blocks) if x not in used][:w.B]
+    assert len(free) == w.B
+    src = int(w.block_tables[0, 5])
+    pairs = np.array([[src, f] for f in free], dtype=np.int32)
+    pkv.check(pkv.pkv_copy_blocks(dk, dv, i32_dev(pairs)))
+    tables = w.block_tables.copy()
+    tables[:, 5] = free
+    out2 = torch.empty_like(q)
+    pkv.check(pkv.pkv_decode_attn(q, dk, dv, i32_dev(tables), cl, w.scale, out2))
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+# ------------------------------------ shared prefixes --------------------------------------
+def share_prefixes(w: gen.Workload, groups):
+    """Rewrite the tables so that each group's members use the first member's leading blocks.
+    groups: (start, end, prefix_blocks); every member keeps prefix_blocks * 16 < ctx."""
+    tables = w.block_tables.copy()
+    starts, pblocks = [0], []
+    for s, e, p in groups:
+        assert starts[-1] <= s
+        if starts[-1] < s:                 # sequences between groups form a group without prefix
+            pblocks.append(0)
+            starts.append(s)
+        for b in range(s, e):
+            assert p * 16 < int(w.context_lens[b])
+            tables[b, :p] = tables[s, :p]
+        pblocks.append(p)
+        starts.append(e)
+    if starts[-1] < w.B:
+        pblocks.append(0)
+        starts.append(w.B)
+    return tables, np.array(starts, dtype=np.int32), np.array(pblocks, dtype=np.int32)
+
+
+def run_prefix(pkv, w, kc, vc, tables, starts, pblocks, part_blocks, max_group=None, max_prefix=None,
+               err=None):
+    q = bf16_dev(w.q)
+    out = torch.empty_like(q)
+    lse = torch.empty(w.B, w.N, dtype=torch.float32, device="cuda")
+    max_group = max_group or int(np.max(np.diff(starts)))
+    max_prefix = int(pblocks.max()) if max_prefix is None else max_prefix
+    ws = torch.empty(pkv.pkv_prefix_workspace_bytes(w.B, w.N, w.H, tables.shape[1], max_prefix, part_blocks),
+                     dtype=torch.uint8, device="cuda")
+    pkv.check(pkv.pkv_decode_attn_prefix(q, kc, vc, i32_dev(tables), i32_dev(w.context_lens), w.scale,
+                                         i32_dev(starts), i32_dev(pblocks), max_group, max_prefix, out, lse,
+                                         part_blocks, ws, err))
+    return out, lse
+
+
+@pytest.mark.parametrize("part_blocks", [4, 8, 16, 64])
+def test_prefix_workload_matches_oracle(pkv, oracle, part_blocks):
+    w = gen.make_config("prefix_l3_70b")
+    starts, pblocks = w.prefix_groups()
+    kc, vc = appended_host_cache(oracle, w)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_prefix(pkv, w, bf16_dev(kc), bf16_dev(vc), w.block_tables, starts, pblocks, part_blocks,
+                          err=err)
+    assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    assert_close(out_f64(out), ref, f"prefix pb={part_blocks}")
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), ref_lse, f"prefix pb={part_blocks}")
+
+
+PREFIX_CASES = [
+    # name, N, K, H, context lengths, groups (start, end, shared blocks)
+    ("two_groups_gqa4", 32, 8, 128, [200, 300, 180, 500, 90, 64, 700, 40],
+     [(0, 3, 11), (3, 7, 3)]),
+    ("singles_between", 16, 2, 128, [100, 120, 17, 300, 260, 33, 35], [(0, 2, 6), (3, 5, 16)]),
+    ("mha_h64", 8, 8, 64, [70, 90, 110, 130, 150], [(0, 5, 4)]),
+    ("big_group_g8", 64, 8, 128, [130 + 7 * i for i in range(12)], [(0, 12, 8)]),  # 96 rows: 3 chunks
+]
+
+
+@pytest.mark.parametrize("part_blocks", [2, 5, 16])
+@pytest.mark.parametrize("name,N,K,H,ctx,groups", PREFIX_CASES, ids=[c[0] for c in PREFIX_CASES])
+def test_prefix_groups_match_oracle(pkv, oracle, name, N, K, H, ctx, groups, part_blocks):
+    w = gen.make_workload(f"p_{name}", 131, N, K, H, ctx)
+    tables, starts, pblocks = share_prefixes(w, groups)
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    slots = oracle.slot_mapping(tables, w.context_lens)
+    oracle.append(w.k_new, w.v_new, slots, kc, vc)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_prefix(pkv, w, bf16_dev(kc), bf16_dev(vc), tables, starts, pblocks, part_blocks, err=err)
+    assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, tables, w.context_lens, w.scale)
+    assert_close(out_f64(out), ref, f"prefix {name} pb={part_blocks}")
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), ref_lse, f"prefix {name} pb={part_blocks}")
+
+
+def test_prefix_bounds_are_flagged(pkv, oracle):
+    w = gen.make_workload("p_bounds", 141, 16, 4, 128, [100, 120, 140, 160])
+    tables, starts, pblocks = share_prefixes(w, [(0, 4, 5)])
+    kc, vc = appended_host_cache(oracle, w)
+    dk, dv = bf16_dev(kc), bf16_dev(vc)
+    # a group larger than the declared bound
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run_prefix(pkv, w, dk, dv, tables, starts, pblocks, 4, max_group=1, err=err)
+    st, flag = pkv.pkv_read_err_flag(err)
+    assert st == pkv.PKV_ERR_RANGE and flag & pkv.PKV_FLAG_GROUP_RANGE
+    # a member shorter than its group's prefix
+    err.zero_()
+    bad = pblocks.copy()
+    bad[0] = 7                         # 112 tokens > ctx of sequence 0 (100)
+    out, _ = run_prefix(pkv, w, dk, dv, tables, starts, bad, 4, err=err)
+    st, flag = pkv.pkv_read_err_flag(err)
+    assert st == pkv.PKV_ERR_RANGE and flag & pkv.PKV_FLAG_GROUP_RANGE
+    assert torch.all(out[0].float() == 0)
