@@ -126,8 +126,12 @@ int pkv_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *
                     int32_t *err_flag, pkv_stream_t stream);
 
 /*
- * Workspace for pkv_decode_attn_splitk: part_out float [num_seqs][N][max_partitions][H]
- * followed (256-byte aligned) by part_lse float [num_seqs][N][max_partitions].
+ * Workspace for pkv_decode_attn_splitk (and the partitioned forms of pkv_decode_step,
+ * pkv_decode_attn_fp8, pkv_decode_step_fp8): part_out float [num_seqs][N][max_partitions][H],
+ * then (256-byte aligned) part_lse float [num_seqs][N][max_partitions], then (256-byte aligned)
+ * merge counters int32 [num_seqs][N].  ZERO THE WORKSPACE ONCE before its first use: each call
+ * leaves the counters at zero again, so a workspace can be reused (and captured in a CUDA graph)
+ * without clearing it.  Calls that share a workspace must not overlap on the GPU.
  */
 size_t pkv_splitk_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                   int32_t max_partitions);
@@ -136,11 +140,14 @@ size_t pkv_splitk_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
  * Split-KV decode attention (FlashDecoding, named in CS336 Lecture 10 notes,
  * "其他优化"): partition p of sequence b covers logical blocks
  * [p * partition_blocks, (p+1) * partition_blocks) of its table.  One CTA per
- * (partition, KV head, sequence) writes its normalised partial output and
- * lse into the workspace, then pkv_lse_merge combines them (two launches,
- * stream-ordered).  max_partitions must be >= ceil(max_blocks_per_seq /
- * partition_blocks).  The workspace is caller-owned device memory of at
- * least pkv_splitk_workspace_bytes(...) bytes, 256-byte aligned.
+ * (partition, KV head, sequence), highest partition first, in one launch: a
+ * sequence that fits in one partition is written to out directly; the others
+ * leave normalised partial outputs and lse in the workspace, and the last CTA of
+ * each (sequence, KV head) to finish merges them by log-sum-exp (the same
+ * arithmetic as pkv_lse_merge, bit for bit).  max_partitions must be >=
+ * ceil(max_blocks_per_seq / partition_blocks).  The workspace is caller-owned
+ * device memory of at least pkv_splitk_workspace_bytes(...) bytes, 256-byte
+ * aligned and zeroed before its first use.
  */
 int pkv_decode_attn_splitk(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
                            const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -150,7 +157,7 @@ int pkv_decode_attn_splitk(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
                            size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream);
 
 /*
- * One whole decode step in one launch (two with partitions): for each sequence the new token's
+ * One whole decode step in one launch: for each sequence the new token's
  * K and V (k_new/v_new [num_seqs][K][H]) are written into the slot of its logical position
  * ctx-1 (slot_mapping_out[b] = that slot, or -1 for ctx 0; nullable) and the token attends to
  * its context including itself -- pkv_slot_mapping + pkv_append + pkv_decode_attn (or

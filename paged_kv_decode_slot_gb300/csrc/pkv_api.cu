@@ -165,8 +165,40 @@ int64_t splitk_lse_offset(int32_t B, int32_t N, int32_t H, int32_t P)
     return (out_bytes + 255) / 256 * 256;
 }
 
+// Split-KV workspace: part_out fp32 [B][N][P][H], part_lse fp32 [B][N][P], then the merge counters
+// int32 [B][N] (one per (sequence, KV head) is used; zero between calls).
+int64_t splitk_counter_offset(int32_t B, int32_t N, int32_t H, int32_t P)
+{
+    const int64_t lse_end = splitk_lse_offset(B, N, H, P) + (int64_t)B * N * P * 4;
+    return (lse_end + 255) / 256 * 256;
+}
+
+struct SplitWs {
+    float *part_out, *part_lse;
+    int32_t *counters;
+};
+
+// The in-kernel merge keeps G x max_parts weights in the attention kernel's drained ring (32 KiB
+// at least); larger splits merge in pkv_lse_merge.  pkv_lse_merge keeps max_parts weights.
+constexpr int64_t kInKernelMergeWeights = 8192;
+constexpr int32_t kMaxMergeParts = 12288;
+
+bool merge_in_kernel(int32_t N, int32_t K, int32_t max_parts)
+{
+    return (int64_t)(N / K) * max_parts <= kInKernelMergeWeights;
+}
+
+SplitWs split_ws(void *ws, int32_t B, int32_t N, int32_t H, int32_t P)
+{
+    char *base = static_cast<char *>(ws);
+    return {reinterpret_cast<float *>(base), reinterpret_cast<float *>(base + splitk_lse_offset(B, N, H, P)),
+            reinterpret_cast<int32_t *>(base + splitk_counter_offset(B, N, H, P))};
+}
+
+// counters != nullptr: the merge runs in the attention kernel (out, lse_out written there);
+// otherwise every partition's partial is written for a separate merge.
 int run_partitions(const AttnArgs &a, int32_t part_blocks, int32_t max_parts, float *part_out,
-                   float *part_lse, cudaStream_t s)
+                   float *part_lse, int32_t *counters, pkv_bf16 *out, float *lse_out, cudaStream_t s)
 {
     if (part_blocks <= 0 || max_parts <= 0) return PKV_ERR_SHAPE;
     if ((int64_t)max_parts * part_blocks < a.max_nb) return PKV_ERR_SHAPE;
@@ -180,6 +212,9 @@ int run_partitions(const AttnArgs &a, int32_t part_blocks, int32_t max_parts, fl
     p.max_parts = max_parts;
     p.part_out = part_out;
     p.part_lse = part_lse;
+    p.counters = counters;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.lse_out = lse_out;
     cudaError_t e = pkv::launch_attn(a.d.head_dim, true, tk, tv, p, s);
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "attn partitions launch");
 }
@@ -253,8 +288,8 @@ PKV_EXPORT size_t pkv_splitk_workspace_bytes(int32_t num_seqs, int32_t num_q_hea
                                              int32_t max_partitions)
 {
     if (num_seqs < 0 || num_q_heads < 0 || head_dim < 0 || max_partitions < 0) return 0;
-    return (size_t)(splitk_lse_offset(num_seqs, num_q_heads, head_dim, max_partitions) +
-                    (int64_t)num_seqs * num_q_heads * max_partitions * 4);
+    return (size_t)(splitk_counter_offset(num_seqs, num_q_heads, head_dim, max_partitions) +
+                    (int64_t)num_seqs * num_q_heads * 4);
 }
 
 PKV_EXPORT int pkv_decode_attn_partitions(const pkv_bf16 *q, const pkv_bf16 *k_cache,
@@ -271,7 +306,8 @@ PKV_EXPORT int pkv_decode_attn_partitions(const pkv_bf16 *q, const pkv_bf16 *k_c
     int st = validate_attn(a);
     if (st != PKV_OK) return st;
     if (num_seqs == 0) return PKV_OK;
-    return run_partitions(a, partition_blocks, max_partitions, part_out, part_lse, stream);
+    return run_partitions(a, partition_blocks, max_partitions, part_out, part_lse, nullptr, nullptr,
+                          nullptr, stream);
 }
 
 PKV_EXPORT int pkv_lse_merge(const float *part_out, const float *part_lse, const int32_t *context_lens,
@@ -282,7 +318,7 @@ PKV_EXPORT int pkv_lse_merge(const float *part_out, const float *part_lse, const
     if (!part_out || !part_lse || !context_lens || !out) return PKV_ERR_NULL;
     if (num_seqs < 0 || num_q_heads <= 0 || max_partitions <= 0 || partition_blocks <= 0)
         return PKV_ERR_SHAPE;
-    if (head_dim <= 0 || head_dim > 1024) return PKV_ERR_UNSUPPORTED;
+    if (head_dim <= 0 || head_dim > 1024 || max_partitions > kMaxMergeParts) return PKV_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || num_q_heads > INT32_MAX / 2) return PKV_ERR_SHAPE;
     if (!aligned(part_out, 4) || !aligned(part_lse, 4) || !aligned(out, 2) || !aligned(lse_out, 4))
         return PKV_ERR_ALIGN;
@@ -315,13 +351,14 @@ PKV_EXPORT int pkv_decode_attn_splitk(const pkv_bf16 *q, const pkv_bf16 *k_cache
     if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
     if (!aligned(out, 4) || !aligned(lse_out, 4)) return PKV_ERR_ALIGN;
     if (num_seqs == 0) return PKV_OK;
-    float *part_out = static_cast<float *>(workspace);
-    float *part_lse = reinterpret_cast<float *>(
-        static_cast<char *>(workspace) +
-        splitk_lse_offset(num_seqs, num_q_heads, cache.head_dim, max_partitions));
-    st = run_partitions(a, partition_blocks, max_partitions, part_out, part_lse, stream);
+    const SplitWs w = split_ws(workspace, num_seqs, num_q_heads, cache.head_dim, max_partitions);
+    if (merge_in_kernel(num_q_heads, cache.num_kv_heads, max_partitions))
+        return run_partitions(a, partition_blocks, max_partitions, w.part_out, w.part_lse, w.counters, out,
+                              lse_out, stream);
+    st = run_partitions(a, partition_blocks, max_partitions, w.part_out, w.part_lse, nullptr, nullptr,
+                        nullptr, stream);
     if (st != PKV_OK) return st;
-    return pkv_lse_merge(part_out, part_lse, context_lens, num_seqs, num_q_heads, cache.head_dim,
+    return pkv_lse_merge(w.part_out, w.part_lse, context_lens, num_seqs, num_q_heads, cache.head_dim,
                          max_partitions, partition_blocks, out, lse_out, stream);
 }
 
@@ -343,7 +380,7 @@ PKV_EXPORT int pkv_decode_step(const pkv_bf16 *q, const pkv_bf16 *k_new, const p
         !aligned(slot_mapping_out, 8))
         return PKV_ERR_ALIGN;
     const bool split = partition_blocks > 0;
-    float *part_out = nullptr, *part_lse = nullptr;
+    SplitWs sw{nullptr, nullptr, nullptr};
     if (split) {
         if (max_partitions <= 0 || (int64_t)max_partitions * partition_blocks < max_blocks_per_seq)
             return PKV_ERR_SHAPE;
@@ -352,10 +389,7 @@ PKV_EXPORT int pkv_decode_step(const pkv_bf16 *q, const pkv_bf16 *k_new, const p
                                                          max_partitions))
             return PKV_ERR_WORKSPACE;
         if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
-        part_out = static_cast<float *>(workspace);
-        part_lse = reinterpret_cast<float *>(
-            static_cast<char *>(workspace) +
-            splitk_lse_offset(num_seqs, num_q_heads, cache.head_dim, max_partitions));
+        sw = split_ws(workspace, num_seqs, num_q_heads, cache.head_dim, max_partitions);
     } else if (partition_blocks < 0) {
         return PKV_ERR_SHAPE;
     }
@@ -375,13 +409,14 @@ PKV_EXPORT int pkv_decode_step(const pkv_bf16 *q, const pkv_bf16 *k_new, const p
     if (split) {
         p.part_blocks = partition_blocks;
         p.max_parts = max_partitions;
-        p.part_out = part_out;
-        p.part_lse = part_lse;
+        p.part_out = sw.part_out;
+        p.part_lse = sw.part_lse;
+        p.counters = merge_in_kernel(num_q_heads, cache.num_kv_heads, max_partitions) ? sw.counters : nullptr;
     }
     cudaError_t e = pkv::launch_attn(cache.head_dim, split, tk, tv, p, stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
-    if (!split) return PKV_OK;
-    return pkv_lse_merge(part_out, part_lse, context_lens, num_seqs, num_q_heads, cache.head_dim,
+    if (!split || p.counters) return PKV_OK;
+    return pkv_lse_merge(sw.part_out, sw.part_lse, context_lens, num_seqs, num_q_heads, cache.head_dim,
                          max_partitions, partition_blocks, out, lse_out, stream);
 }
 
@@ -444,7 +479,7 @@ int fp8_attention(const AttnArgs &a, const pkv_bf16 *k_new, const pkv_bf16 *v_ne
         !aligned(v_new, 16) || !aligned(slot_out, 8))
         return PKV_ERR_ALIGN;
     const bool split = partition_blocks > 0;
-    float *part_out = nullptr, *part_lse = nullptr;
+    SplitWs sw{nullptr, nullptr, nullptr};
     if (split) {
         if (max_partitions <= 0 || (int64_t)max_partitions * partition_blocks < a.max_nb)
             return PKV_ERR_SHAPE;
@@ -452,9 +487,7 @@ int fp8_attention(const AttnArgs &a, const pkv_bf16 *k_new, const pkv_bf16 *v_ne
             workspace_bytes < pkv_splitk_workspace_bytes(a.B, a.N, a.d.head_dim, max_partitions))
             return PKV_ERR_WORKSPACE;
         if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
-        part_out = static_cast<float *>(workspace);
-        part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                             splitk_lse_offset(a.B, a.N, a.d.head_dim, max_partitions));
+        sw = split_ws(workspace, a.B, a.N, a.d.head_dim, max_partitions);
     } else if (partition_blocks < 0) {
         return PKV_ERR_SHAPE;
     }
@@ -475,13 +508,14 @@ int fp8_attention(const AttnArgs &a, const pkv_bf16 *k_new, const pkv_bf16 *v_ne
     if (split) {
         p.part_blocks = partition_blocks;
         p.max_parts = max_partitions;
-        p.part_out = part_out;
-        p.part_lse = part_lse;
+        p.part_out = sw.part_out;
+        p.part_lse = sw.part_lse;
+        p.counters = merge_in_kernel(a.N, a.d.num_kv_heads, max_partitions) ? sw.counters : nullptr;
     }
     cudaError_t e = pkv::launch_attn(a.d.head_dim, split, tk, tv, p, stream, true);
     if (e != cudaSuccess) return cuda_fail(e, "e4m3 attention launch");
-    if (!split) return PKV_OK;
-    return pkv_lse_merge(part_out, part_lse, a.context_lens, a.B, a.N, a.d.head_dim, max_partitions,
+    if (!split || p.counters) return PKV_OK;
+    return pkv_lse_merge(sw.part_out, sw.part_lse, a.context_lens, a.B, a.N, a.d.head_dim, max_partitions,
                          partition_blocks, out, lse_out, stream);
 }
 
@@ -779,7 +813,8 @@ PKV_EXPORT int pkv_decode_attn_splitk_noalloc(const pkv_bf16 *q, const pkv_bf16 
     float *part_lse = reinterpret_cast<float *>(
         static_cast<char *>(scratch) +
         splitk_lse_offset(num_seqs, num_q_heads, cache.head_dim, max_partitions));
-    st = run_partitions(a, partition_blocks, max_partitions, part_out, part_lse, stream);
+    st = run_partitions(a, partition_blocks, max_partitions, part_out, part_lse, nullptr, nullptr, nullptr,
+                        stream);
     if (st != PKV_OK) return st;
     return pkv_lse_merge(part_out, part_lse, context_lens, num_seqs, num_q_heads, cache.head_dim,
                          max_partitions, partition_blocks, out, lse_out, stream);

@@ -1,8 +1,8 @@
 // pkv_attn.cu - paged decode attention for sm_103a.
 //
 // Work is cut into tiles: one tile = one physical block (16 tokens) of one KV head.  A CTA has
-// a producer warp and four consumer warps.  The producer walks the CTA's tiles, looks each one
-// up in the block table, and streams its K and V (16 x H bf16 each) into a ring of shared-memory
+// two producer warps and four consumer warps.  The producers walk the CTA's tiles, look each one
+// up in the block table, and stream its K and V (16 x H bf16 each) into a ring of shared-memory
 // stages with TMA, one mbarrier pair per stage.  The consumer warps take the stages round-robin;
 // each keeps an online-softmax state for the whole query group (the G = N/K query heads that share
 // the KV head), so every K/V byte fetched from HBM serves all G heads:
@@ -15,8 +15,10 @@
 // Three ways to cut the work:
 //  * attn_kernel<H, false>: one CTA per (KV head, sequence), whole sequence (single pass).
 //  * attn_kernel<H, true>:  one CTA per (KV head, sequence, partition), partitions of a fixed
-//    number of blocks (FlashDecoding), highest partition first; partial results are merged by
-//    lse_merge_kernel.
+//    number of blocks (FlashDecoding), highest partition first.  A sequence that fits in one
+//    partition is written out directly; the partial results of a longer one are merged by the
+//    last of its CTAs to finish (a per-unit counter that the merger resets), or -- when the caller
+//    asks for the partials themselves -- by lse_merge_kernel.
 //  * attn_balanced_kernel<H>: a persistent grid (about two CTAs per SM, a multiple of K) in which
 //    CTA c serves KV head c % K and takes the (c / K)-th equal share of that head's tiles in
 //    (sequence, block) order, keeping its TMA ring streaming across unit boundaries.  The K CTAs
@@ -124,12 +126,19 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     const int blk_begin = kSplit ? part * p.part_blocks : 0;
     const int blk_end = kSplit ? min(nb, blk_begin + p.part_blocks) : nb;
     const int nblk = blk_end - blk_begin;
+    // In-kernel merge (split with counters): a sequence held by one partition is written out
+    // directly; one held by several leaves partials, and the last of its CTAs to finish (per KV
+    // head, counted in p.counters) merges them and resets the count to zero.
+    const int nparts = kSplit ? (nb + p.part_blocks - 1) / p.part_blocks : 1;
+    const bool merge_here = kSplit && p.counters != nullptr;
+    const bool direct = !kSplit || (merge_here && nparts <= 1);
 
     if (nblk <= 0) {
-        // A single pass over an empty sequence writes 0 / -inf; an empty partition is never
-        // read by the merge and writes nothing.  An empty sequence appends nothing.
+        // A single pass over an empty sequence writes 0 / -inf (so does partition 0 of an empty
+        // sequence when the merge runs in the kernel); an empty partition is never read by the
+        // merge and writes nothing.  An empty sequence appends nothing.
         if (p.slot_out && nb == 0 && kvh == 0 && part == 0 && threadIdx.x == 0) p.slot_out[b] = -1;
-        if (!kSplit) {
+        if (!kSplit || (merge_here && nb == 0 && part == 0)) {
             for (int idx = threadIdx.x; idx < G * H; idx += kAttnThreads) {
                 const int g = idx / H, h = idx - g * H;
                 const size_t bn = (size_t)b * p.N + (size_t)kvh * G + g;
@@ -218,28 +227,34 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     }
 
     __syncthreads();
-    if (*abort_flag) {
+    const bool aborted = *abort_flag != 0;
+    if (aborted) {
         if (warp >= kConsumerWarps && lane == 0)
             drain_ring<S, kProducers>(bar_full, warp - kConsumerWarps,
                                             issued_count[warp - kConsumerWarps]);
         __syncthreads();
-        return;
+        // the sequence's other partitions still count on this one: it leaves a void partial
+        if (!(merge_here && nparts > 1)) return;
     }
 
     // ------------------------- merge the consumer warps' states -------------------------
     float *mo = reinterpret_cast<float *>(base);              // [W][8][H]
     float *mm = mo + kConsumerWarps * 8 * H;                 // [W][8]
     float *ml = mm + kConsumerWarps * 8;                     // [W][8]
-    if (warp < kConsumerWarps) deposit<H, kFp8>(acc, mo, mm, ml, warp, lane);
-    __syncthreads();
+    if (!aborted) {
+        if (warp < kConsumerWarps) deposit<H, kFp8>(acc, mo, mm, ml, warp, lane);
+        __syncthreads();
+    }
     const float vscale = kFp8 ? p.v_scale[kvh] : 1.f;
     for (int idx = threadIdx.x; idx < G * H; idx += kAttnThreads) {
         const int g = idx / H, h = idx - g * H;
-        float val, lse;
-        combine<H>(mo, mm, ml, g, h, val, lse);
-        val *= vscale;
+        float val = __int_as_float(0x7FC00000), lse = __int_as_float(0x7FC00000);  // NaN: void
+        if (!aborted) {
+            combine<H>(mo, mm, ml, g, h, val, lse);
+            val *= vscale;
+        }
         const size_t bn = (size_t)b * p.N + (size_t)kvh * G + g;
-        if (kSplit) {
+        if (!direct) {
             const size_t bnp = bn * p.max_parts + part;
             p.part_out[bnp * H + h] = val;
             if (h == 0) p.part_lse[bnp] = lse;
@@ -248,6 +263,30 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
             if (h == 0 && p.lse_out) p.lse_out[bn] = lse;
         }
     }
+    if (!merge_here || nparts <= 1) return;
+
+    // ----------------- in-kernel log-sum-exp merge by the last partition -----------------
+    // The host only asks for it when G * max_parts weights fit in the (drained) ring.
+    __shared__ int last_one;
+    __syncthreads();  // every partial of this CTA is written
+    int32_t *count = p.counters + (size_t)b * p.K + kvh;
+    if (threadIdx.x == 0) last_one = atomic_add_acq_rel_gpu(count, 1) == nparts - 1;
+    __syncthreads();
+    if (!last_one) return;
+    float *wts = reinterpret_cast<float *>(base);  // [G][nparts]
+    for (int g = warp; g < G; g += kAttnThreads / 32) {
+        const size_t bn = (size_t)b * p.N + (size_t)kvh * G + g;
+        const float L = lse_merge_weights(p.part_lse + bn * p.max_parts, nparts, wts + g * nparts, lane);
+        if (lane == 0 && p.lse_out) p.lse_out[bn] = L;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * H; idx += kAttnThreads) {
+        const int g = idx / H, h = idx - g * H;
+        const size_t bn = (size_t)b * p.N + (size_t)kvh * G + g;
+        const float val = lse_merge_value(wts + g * nparts, p.part_out + bn * p.max_parts * H + h, nparts, H);
+        p.out[bn * H + h] = __float2bfloat16_rn(val);
+    }
+    if (threadIdx.x == 0) *count = 0;  // ready for the next call
 }
 
 // ------------------------------ balanced (stream-K) split ---------------------------------
@@ -530,27 +569,21 @@ __global__ void lse_merge_kernel(const float *__restrict__ part_out, const float
                                  const int32_t *__restrict__ context_lens, int N, int H, int max_parts,
                                  int part_blocks, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out)
 {
+    extern __shared__ float wts[];  // [max_parts]
+    __shared__ float row_lse;
     const int n = blockIdx.x, b = blockIdx.y, h = threadIdx.x;
     const size_t bn = (size_t)b * N + n;
     int ctx = context_lens[b];
     const int nb = ctx > 0 ? (ctx + kBlockSize - 1) / kBlockSize : 0;
     int np = (nb + part_blocks - 1) / part_blocks;
     if (np > max_parts) np = max_parts;
-    const float *lp = part_lse + bn * max_parts;
-    float M = -INFINITY;
-    for (int q = 0; q < np; ++q) M = fmaxf(M, lp[q]);
-    float total = -INFINITY, val = 0.f;
-    if (M != -INFINITY) {
-        float sum = 0.f;
-        for (int q = 0; q < np; ++q) sum += expf(lp[q] - M);
-        total = M + logf(sum);
-        if (h < H) {
-            const float *po = part_out + bn * max_parts * H + h;
-            for (int q = 0; q < np; ++q) val += expf(lp[q] - total) * po[(size_t)q * H];
-        }
+    if (h < 32) {
+        const float L = lse_merge_weights(part_lse + bn * max_parts, np, wts, h);
+        if (h == 0) row_lse = L;
     }
-    if (h < H) out[bn * H + h] = __float2bfloat16_rn(val);
-    if (h == 0 && lse_out) lse_out[bn] = total;
+    __syncthreads();
+    if (h < H) out[bn * H + h] = __float2bfloat16_rn(lse_merge_value(wts, part_out + bn * max_parts * H + h, np, H));
+    if (h == 0 && lse_out) lse_out[bn] = row_lse;
 }
 
 // ---------------------------------- launchers ----------------------------------------------
@@ -627,7 +660,7 @@ cudaError_t launch_lse_merge(const float *part_out, const float *part_lse, const
                              float *lse_out, cudaStream_t stream)
 {
     const int threads = H < 32 ? 32 : H;
-    lse_merge_kernel<<<dim3(N, B), threads, 0, stream>>>(
+    lse_merge_kernel<<<dim3(N, B), threads, (size_t)max_parts * sizeof(float), stream>>>(
         part_out, part_lse, context_lens, N, H, max_parts, part_blocks,
         reinterpret_cast<__nv_bfloat16 *>(out), lse_out);
     return cudaGetLastError();

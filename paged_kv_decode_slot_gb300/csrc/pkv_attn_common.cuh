@@ -398,6 +398,38 @@ __device__ __forceinline__ void combine(const float *mo, const float *mm, const 
     lse = M != -INFINITY ? (M + log2f(lsum)) * kLn2 : -INFINITY;
 }
 
+// Log-sum-exp weights of one output row's n partial results (natural-log lse_q; -inf for a part
+// without keys): M = max_q lse_q, L = M + ln sum_q exp(lse_q - M), w_q = exp(lse_q - L), all
+// zero and L = -inf when M = -inf.  Called by one whole warp (lanes stride the parts, shuffles
+// reduce); writes w[0..n) and returns L on every lane.  The merged output is sum_q w_q o_q.
+__device__ __forceinline__ float lse_merge_weights(const float *lp, int n, float *w, int lane)
+{
+    float M = -INFINITY;
+    for (int q = lane; q < n; q += 32) M = fmaxf(M, __ldcg(lp + q));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+    float L = -INFINITY;
+    if (M != -INFINITY) {
+        float sum = 0.f;
+        for (int q = lane; q < n; q += 32) sum += expf(__ldcg(lp + q) - M);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+        L = M + logf(sum);
+    }
+    for (int q = lane; q < n; q += 32) w[q] = L == -INFINITY ? 0.f : expf(__ldcg(lp + q) - L);
+    __syncwarp();
+    return L;
+}
+
+// sum_q w_q o_q for one element h of a row whose partials are po[q * stride] (independent loads).
+__device__ __forceinline__ float lse_merge_value(const float *w, const float *po, int n, size_t stride)
+{
+    float val = 0.f;
+#pragma unroll 4
+    for (int q = 0; q < n; ++q) val += w[q] * __ldcg(po + (size_t)q * stride);
+    return val;
+}
+
 template <int S>
 __device__ __forceinline__ void init_ring(uint32_t bar_full, uint32_t bar_empty)
 {

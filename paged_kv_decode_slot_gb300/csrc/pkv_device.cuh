@@ -89,6 +89,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Atomic add at GPU scope with acquire-release semantics; returns the previous value.  Issued by
+// one thread after a CTA barrier, the release publishes the whole CTA's earlier writes (the
+// barrier orders them before it), and the acquire makes the writes released by earlier adders
+// visible to this CTA after its next barrier.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 // Order this thread's earlier generic-proxy shared-memory writes before later async-proxy
 // (TMA) accesses to the same memory.
 __device__ __forceinline__ void fence_proxy_async_shared()

@@ -38,6 +38,8 @@ struct AttnParams {
     const float *k_scale;          // e4m3 pools: per-KV-head scales [K] (value = code * scale)
     const float *v_scale;
     int64_t *slot_out;             // [B] slot of the newest token (-1 none), nullable
+    int32_t *counters;             // split-KV with the merge in the kernel: [B][K], zero between
+                                   // calls (nullptr: write every partial, merge separately)
     int32_t *err_flag;             // nullable
 };
 

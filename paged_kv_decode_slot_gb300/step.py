@@ -41,16 +41,24 @@ class AttentionPlan:
         return "single-pass"
 
 
+LONG_PARTITION_BLOCKS = 128
+
+
 def plan_attention(num_seqs: int, num_kv_heads: int, max_blocks_per_seq: int, num_sms: int,
                    partition_blocks: int | None = None, mode: str | None = None) -> AttentionPlan:
-    """Single pass when (sequence, KV head) units cover every SM, else fixed partitions.
+    """Partitions sized by how well the (sequence, KV head) units cover the SMs.
 
-    Measured on GB300 (Llama-3-8B / Llama-2-13B / long-context shapes): with at least one unit
-    per SM the single pass (three CTAs per SM, no merge) is fastest; with fewer units it leaves
-    SMs idle, and partitions sized so the grid holds about 512 partition CTAs when every
-    sequence is as long as the table allows (at least 8 blocks each) are fastest -- 256 blocks
-    for two sequences of 128K/32K tokens, 128 for 16 sequences of up to 7.4K tokens.  The
-    persistent balanced split is available with ``mode="balanced"``.
+    Measured on GB300 (Llama-3-8B / Llama-2-13B / long-context shapes):
+      * with at least one unit per SM, one CTA per unit keeps HBM busy until the short sequences
+        finish; then the longest ones stream alone, one CTA each at about 30 GB/s.  Tables longer
+        than 128 blocks therefore get 128-block partitions (2K tokens): a sequence that fits in
+        one partition is still a single pass (the split kernel writes it out directly and merges
+        longer ones in the same launch), and the long ones are spread over more SMs -- 185 vs
+        188 us on the ragged Llama-3-8B batch of 64, equal on uniform 1K-token batches;
+      * with fewer units than SMs, partitions sized so the grid holds about 512 partition CTAs
+        when every sequence is as long as the table allows (at least 8 blocks each) are fastest:
+        256 blocks for two sequences of 128K/32K tokens, 128 for 16 sequences of up to 7.4K.
+    The persistent balanced split is available with ``mode="balanced"``.
     """
     if mode == "balanced":
         return AttentionPlan("balanced")
@@ -59,7 +67,11 @@ def plan_attention(num_seqs: int, num_kv_heads: int, max_blocks_per_seq: int, nu
     units = num_seqs * num_kv_heads
     if partition_blocks is None:
         if units >= num_sms and mode is None:
-            return AttentionPlan("single", max_blocks_per_seq, 1)
+            if max_blocks_per_seq <= LONG_PARTITION_BLOCKS:
+                return AttentionPlan("single", max_blocks_per_seq, 1)
+            partition_blocks = LONG_PARTITION_BLOCKS
+            return AttentionPlan("split", partition_blocks,
+                                 B.max_partitions_for(max_blocks_per_seq, partition_blocks))
         want = -(-max_blocks_per_seq * units // 512)
         partition_blocks = 8
         while partition_blocks < want:
@@ -97,11 +109,11 @@ class DecodeStep:
         self.workspace = None
         if plan.mode == "split":
             nbytes = B.pkv_splitk_workspace_bytes(nseq, q.shape[1], q.shape[2], plan.max_partitions)
-            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         elif plan.mode == "balanced":
             with torch.cuda.device(dev):
                 nbytes = B.pkv_balanced_workspace_bytes(nseq, k_cache.shape[2], q.shape[2])
-            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def slot_and_append(self, stream=None) -> None:
         B.check(B.pkv_slot_mapping(self.block_tables, self.context_lens, self.num_blocks,
@@ -171,7 +183,7 @@ class DecodeStepFp8:
         self.workspace = None
         if plan.mode == "split":
             nbytes = B.pkv_splitk_workspace_bytes(nseq, q.shape[1], q.shape[2], plan.max_partitions)
-            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def run(self, stream=None) -> None:
         split = self.plan.mode == "split"
@@ -222,7 +234,7 @@ class MultiTokenStep:
         self.workspace = None
         if self.plan.mode == "split":
             nbytes = B.pkv_splitk_workspace_bytes(nseq * T, N, H, self.plan.max_partitions)
-            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def slot_and_append(self, stream=None) -> None:
         nseq, T = self.q.shape[0], self.T
@@ -283,7 +295,7 @@ class PrefixDecodeStep:
         self.err_flag = err_flag
         nbytes = B.pkv_prefix_workspace_bytes(nseq, N, H, block_tables.shape[1], self.max_prefix_blocks,
                                               self.partition_blocks)
-        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def slot_and_append(self, stream=None) -> None:
         B.check(B.pkv_slot_mapping(self.block_tables, self.context_lens, self.num_blocks,

@@ -84,7 +84,10 @@ def test_host_validation_of_splitk_and_merge(lib):
                   Desc, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_size_t, P, P]
     cdll.pkv_splitk_workspace_bytes.restype = ctypes.c_size_t
     need = cdll.pkv_splitk_workspace_bytes(4, 8, 64, 2)
-    assert need == 256 * ((4 * 8 * 2 * 64 * 4 + 255) // 256) + 4 * 8 * 2 * 4
+    # part_out, then part_lse, then the merge counters, each region 256-byte aligned
+    lse_off = 256 * ((4 * 8 * 2 * 64 * 4 + 255) // 256)
+    cnt_off = 256 * ((lse_off + 4 * 8 * 2 * 4 + 255) // 256)
+    assert need == cnt_off + 4 * 8 * 4
     args = lambda ws, wsb, pb=2, P_=2, B=4: (FAKE, FAKE, FAKE, FAKE, 4, FAKE, B, 8, 0.125, FAKE, None,
                                             Desc(64, 16, 2, 64), pb, P_, ws, wsb, None, None)
     assert f(*args(None, need)) == -7
@@ -137,8 +140,10 @@ def test_library_kv_bytes_matches_pages(lib):
 
 def test_attention_plan():
     from paged_kv_decode_slot_gb300.step import plan_attention
-    assert plan_attention(64, 8, 512, 152).mode == "single"            # 512 units cover 152 SMs
+    p = plan_attention(64, 8, 512, 152)                                 # 512 units cover 152 SMs,
+    assert (p.mode, p.partition_blocks, p.max_partitions) == ("split", 128, 4)   # long tables split
     assert plan_attention(20, 8, 95, 152).mode == "single"
+    assert plan_attention(128, 40, 64, 152).mode == "single"
     p = plan_attention(2, 8, 8192, 152)                                 # long context: 256 blocks
     assert p.mode == "split" and p.partition_blocks == 256 and p.max_partitions == 32
     p = plan_attention(16, 8, 464, 152)                                 # 128 units: 128 blocks

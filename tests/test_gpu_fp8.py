@@ -85,7 +85,7 @@ def _attn(pkv, c: Fp8Case, d, part_blocks, err=None):
     P, ws = 0, None
     if part_blocks:
         P = pkv.max_partitions_for(w.max_blocks, part_blocks)
-        ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
     pkv.check(pkv.pkv_decode_attn_fp8(d["q"], d["k_cache"], d["v_cache"], d["k_scale"], d["v_scale"],
                                       d["block_tables"], d["context_lens"], w.scale, out, lse,
                                       part_blocks, P, ws, err))
@@ -100,7 +100,7 @@ def _step(pkv, c: Fp8Case, d, part_blocks, err=None):
     P, ws = 0, None
     if part_blocks:
         P = pkv.max_partitions_for(w.max_blocks, part_blocks)
-        ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
     pkv.check(pkv.pkv_decode_step_fp8(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
                                       d["k_scale"], d["v_scale"], d["block_tables"], d["context_lens"],
                                       w.scale, out, lse, slots, part_blocks, P, ws, err))

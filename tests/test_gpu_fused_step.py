@@ -33,7 +33,7 @@ def _separate(pkv, w, part_blocks):
     lse = torch.empty(w.B, w.N, dtype=torch.float32, device="cuda")
     if part_blocks:
         P = pkv.max_partitions_for(w.max_blocks, part_blocks)
-        ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
         pkv.check(pkv.pkv_decode_attn_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
                                              d["context_lens"], w.scale, out, part_blocks, P, ws, lse))
     else:
@@ -50,7 +50,7 @@ def _fused(pkv, w, part_blocks, err=None):
     P, ws = 0, None
     if part_blocks:
         P = pkv.max_partitions_for(w.max_blocks, part_blocks)
-        ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
     pkv.check(pkv.pkv_decode_step(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
                                   d["block_tables"], d["context_lens"], w.scale, out, lse, slots,
                                   part_blocks, P, ws, err))

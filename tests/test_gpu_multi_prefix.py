@@ -53,7 +53,7 @@ def run_multi(pkv, c: MultiCase, kc, vc, part_blocks, err=None):
     P, ws = 0, None
     if part_blocks:
         P = pkv.max_partitions_for(w.max_blocks, part_blocks)
-        ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B * c.T, w.N, w.H, P), dtype=torch.uint8,
+        ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B * c.T, w.N, w.H, P), dtype=torch.uint8,
                          device="cuda")
     pkv.check(pkv.pkv_decode_attn_multi(q, kc, vc, i32_dev(w.block_tables), i32_dev(w.context_lens),
                                         w.scale, out, lse, part_blocks, P, ws, err))
@@ -115,7 +115,7 @@ def test_multi_with_one_token_is_the_decode_kernel(pkv, oracle, part_blocks):
     lse2 = torch.empty(w.B, 1, w.N, dtype=torch.float32, device="cuda")
     if part_blocks:
         P = pkv.max_partitions_for(w.max_blocks, part_blocks)
-        ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
         pkv.check(pkv.pkv_decode_attn_splitk(q, dk, dv, bt, cl, w.scale, out1, part_blocks, P, ws, lse1))
         ws2 = torch.empty_like(ws)
         pkv.check(pkv.pkv_decode_attn_multi(q.view(w.B, 1, w.N, w.H), dk, dv, bt, cl, w.scale, out2, lse2,

@@ -69,7 +69,7 @@ def _balanced(pkv, w, d, err=None):
 
 def _splitk(pkv, w, d, part_blocks, err=None):
     P = pkv.max_partitions_for(w.max_blocks, part_blocks)
-    ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
     out = torch.empty_like(d["q"])
     lse = torch.empty(w.B, w.N, dtype=torch.float32, device="cuda")
     pkv.check(pkv.pkv_decode_attn_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],

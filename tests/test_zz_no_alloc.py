@@ -42,7 +42,7 @@ def _both(pkv, w, part_blocks):
     pkv.check(pkv.pkv_decode_attn_splitk_noalloc(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
                                                  d["context_lens"], w.scale, out_na, part_blocks, P,
                                                  lse_na, err))
-    ws = torch.empty(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
     out_ws = torch.empty_like(d["q"])
     lse_ws = torch.empty(w.B, w.N, dtype=torch.float32, device="cuda")
     pkv.check(pkv.pkv_decode_attn_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
