@@ -43,6 +43,21 @@ def _dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of per-rank timings: the slowest replica sets the job's step time."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_gbs(world_size: int, bytes_per_step_per_rank: int, ms_per_step: float) -> float:
+    """Weak scaling: every rank moves the same bytes per step; the job's time is the max."""
+    return world_size * bytes_per_step_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def load_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -394,10 +409,7 @@ def run_ours(args):
     attn_ms = step_ms if step.fused else [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     mean_step = sum(step_ms) / len(step_ms)
     mean_attn = sum(attn_ms) / len(attn_ms)
-    if dist is not None:
-        t = torch.tensor([mean_step, mean_attn], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_step, mean_attn = t.tolist()
+    mean_step, mean_attn = max_over_ranks([mean_step, mean_attn], dist, dev)
 
     st, flag = pkv.pkv_read_err_flag(err, stream)
     if st != pkv.PKV_OK:
@@ -419,10 +431,7 @@ def run_ours(args):
                 g_ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     graph_ms = sum(e[0].elapsed_time(e[1]) for e in g_ev) / args.steps
-    if dist is not None:
-        t = torch.tensor([graph_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        graph_ms = t.item()
+    graph_ms, = max_over_ranks([graph_ms], dist, dev)
     st, flag = pkv.pkv_read_err_flag(err, stream)
     if st != pkv.PKV_OK:
         raise RuntimeError(f"device error flag {flag:#x} during the graph replays")
@@ -448,15 +457,12 @@ def run_ours(args):
                 e2e_ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / args.steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = t.item()
+    e2e_ms, = max_over_ranks([e2e_ms], dist, dev)
 
     peak, peak_kind = load_peak()
     attn_bytes = nbytes["attn_unique"] if w.unique_tokens is not None else nbytes["attn"]
     achieved = attn_bytes / (mean_attn * 1e-3) / 1e9
-    value = ws * nbytes["step"] / (mean_step * 1e-3) / 1e9
+    value = whole_job_gbs(ws, nbytes["step"], mean_step)
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
@@ -476,10 +482,10 @@ def run_ours(args):
                                + (" (append fused)" if step.fused else ""),
                      "bytes_per_launch": attn_bytes,
                      "traffic": recorded_traffic(args.config + ("" if args.kv == "bf16" else "+fp8"))},
-        "e2e": {"value": ws * nbytes["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": whole_job_gbs(ws, nbytes["step"], e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "graph": {"us_per_step": graph_ms * 1e3,
-                  "value": ws * nbytes["step"] / (graph_ms * 1e-3) / 1e9,
+                  "value": whole_job_gbs(ws, nbytes["step"], graph_ms),
                   "note": "the same step captured once in a CUDA graph and replayed per step"},
         "step_launches": step.launches_per_step(),
         "gpu_launches": args.steps * step.launches_per_step(),
