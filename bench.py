@@ -256,6 +256,25 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def traffic_key(args) -> str:
+    """Workload key of profiles/ncu_traffic.txt: the config plus every option that changes the
+    timed kernel (a recorded figure is reported only for exactly that kernel and workload)."""
+    key = args.config
+    if args.kv != "bf16":
+        key += "+" + args.kv
+    if args.tokens > 1:
+        key += f"+T{args.tokens}"
+    if args.attn != "auto":
+        key += "+" + args.attn
+    if args.unfused:
+        key += "+unfused"
+    if args.partition_blocks is not None:
+        key += f"+pb{args.partition_blocks}"
+    if args.mode is not None:
+        key += "+" + args.mode
+    return key
+
+
 def kernel_label(args, plan, step) -> str:
     if args.tokens > 1:
         return "attn_cols_kernel<128>" + (" + lse_merge_kernel" if plan.mode == "split" else "")
@@ -481,7 +500,7 @@ def run_ours(args):
                      "kernel": kernel_label(args, plan, step)
                                + (" (append fused)" if step.fused else ""),
                      "bytes_per_launch": attn_bytes,
-                     "traffic": recorded_traffic(args.config + ("" if args.kv == "bf16" else "+fp8"))},
+                     "traffic": recorded_traffic(traffic_key(args))},
         "e2e": {"value": whole_job_gbs(ws, nbytes["step"], e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "graph": {"us_per_step": graph_ms * 1e3,

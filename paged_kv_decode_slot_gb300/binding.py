@@ -193,6 +193,17 @@ def pkv_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale: floa
                                 _stream(stream))
 
 
+# The partitioned attention entry points merge inside their one launch when the G x max_partitions
+# log-sum-exp weights of a unit fit the kernel's drained ring, else in a pkv_lse_merge launch.
+IN_KERNEL_MERGE_WEIGHTS = 8192
+
+
+def split_attention_launches(num_q_heads: int, num_kv_heads: int, max_partitions: int) -> int:
+    """Kernel launches of one partitioned attention call (pkv_decode_attn_splitk, pkv_decode_step,
+    and the e4m3 forms)."""
+    return 1 if (num_q_heads // num_kv_heads) * max_partitions <= IN_KERNEL_MERGE_WEIGHTS else 2
+
+
 def pkv_splitk_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_partitions: int) -> int:
     return int(_lib.pkv_splitk_workspace_bytes(num_seqs, num_q_heads, head_dim, max_partitions))
 

@@ -150,7 +150,10 @@ class DecodeStep:
         self.attention(stream)
 
     def launches_per_step(self) -> int:
-        attn = 2 if self.plan.split else 1
+        if self.plan.mode == "split":
+            attn = B.split_attention_launches(self.q.shape[1], self.k_cache.shape[2], self.plan.max_partitions)
+        else:
+            attn = 2 if self.plan.mode == "balanced" else 1
         return attn if self.fused else 2 + attn
 
     def inputs(self):
@@ -195,7 +198,9 @@ class DecodeStepFp8:
                                       self.err_flag, stream))
 
     def launches_per_step(self) -> int:
-        return 2 if self.plan.mode == "split" else 1
+        if self.plan.mode == "split":
+            return B.split_attention_launches(self.q.shape[1], self.k_cache.shape[2], self.plan.max_partitions)
+        return 1
 
     def inputs(self):
         return [self.q, self.k_new, self.v_new, self.block_tables, self.context_lens]
