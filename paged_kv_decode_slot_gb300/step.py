@@ -41,6 +41,47 @@ class AttentionPlan:
         return "single-pass"
 
 
+class PackedInputs:
+    """One host->device copy per step for a step's inputs.
+
+    The given device tensors (a step's ``inputs()``) are moved into one device buffer (each
+    segment 256-byte aligned, contents kept) and the step's attributes are re-pointed at those
+    views; a pinned host buffer mirrors the layout.  Per step the caller writes the new inputs
+    into ``host`` (views with the same shapes and dtypes) and calls ``upload(stream)``: a single
+    cudaMemcpyAsync instead of one per tensor.
+    """
+
+    ALIGN = 256
+
+    def __init__(self, step, names=("q", "k_new", "v_new", "block_tables", "context_lens")):
+        tensors = [getattr(step, n) for n in names]
+        dev = tensors[0].device
+        offsets, off = [], 0
+        for t in tensors:
+            offsets.append(off)
+            off += -(-t.numel() * t.element_size() // self.ALIGN) * self.ALIGN
+        self.nbytes = off
+        self.device_buf = torch.empty(off, dtype=torch.uint8, device=dev)
+        self.host_buf = torch.empty(off, dtype=torch.uint8).pin_memory()
+        self.host = {}
+        for n, t, o in zip(names, tensors, offsets):
+            size = t.numel() * t.element_size()
+            dview = self.device_buf[o:o + size].view(t.dtype).view(t.shape)
+            dview.copy_(t)
+            hview = self.host_buf[o:o + size].view(t.dtype).view(t.shape)
+            hview.copy_(t.cpu())
+            setattr(step, n, dview)
+            self.host[n] = hview
+
+    def upload(self, stream=None) -> None:
+        stream = stream or torch.cuda.current_stream(self.device_buf.device)
+        with torch.cuda.stream(stream):
+            self.device_buf.copy_(self.host_buf, non_blocking=True)
+
+    def bytes_per_step(self) -> int:
+        return sum(v.numel() * v.element_size() for v in self.host.values())
+
+
 LONG_PARTITION_BLOCKS = 128
 
 
@@ -156,9 +197,12 @@ class DecodeStep:
             attn = 2 if self.plan.mode == "balanced" else 1
         return attn if self.fused else 2 + attn
 
-    def inputs(self):
+    def input_names(self):
         """The tensors a caller refreshes every step (the pools are state)."""
-        return [self.q, self.k_new, self.v_new, self.block_tables, self.context_lens]
+        return ("q", "k_new", "v_new", "block_tables", "context_lens")
+
+    def inputs(self):
+        return [getattr(self, n) for n in self.input_names()]
 
 
 class DecodeStepFp8:
@@ -202,8 +246,11 @@ class DecodeStepFp8:
             return B.split_attention_launches(self.q.shape[1], self.k_cache.shape[2], self.plan.max_partitions)
         return 1
 
+    def input_names(self):
+        return ("q", "k_new", "v_new", "block_tables", "context_lens")
+
     def inputs(self):
-        return [self.q, self.k_new, self.v_new, self.block_tables, self.context_lens]
+        return [getattr(self, n) for n in self.input_names()]
 
 
 class MultiTokenStep:
@@ -265,8 +312,11 @@ class MultiTokenStep:
     def launches_per_step(self) -> int:
         return 3 + (1 if self.plan.mode == "split" else 0)
 
+    def input_names(self):
+        return ("q", "k_new", "v_new", "block_tables", "context_lens")
+
     def inputs(self):
-        return [self.q, self.k_new, self.v_new, self.block_tables, self.context_lens]
+        return [getattr(self, n) for n in self.input_names()]
 
 
 class PrefixDecodeStep:
@@ -322,6 +372,8 @@ class PrefixDecodeStep:
     def launches_per_step(self) -> int:
         return 4
 
+    def input_names(self):
+        return ("q", "k_new", "v_new", "block_tables", "context_lens", "group_starts", "prefix_blocks")
+
     def inputs(self):
-        return [self.q, self.k_new, self.v_new, self.block_tables, self.context_lens,
-                self.group_starts, self.prefix_blocks]
+        return [getattr(self, n) for n in self.input_names()]

@@ -117,3 +117,28 @@ def test_fused_step_empty_sequence_and_bad_last_block(pkv):
     after = bf16_host(d["k_cache"])
     changed = np.argwhere(np.any(after != before, axis=(2, 3)))
     assert [tuple(x) for x in changed] == [(int(w.block_tables[1, 1]), 3)]   # only sequence 1's slot
+
+
+def test_packed_inputs_one_copy_per_step(pkv, oracle):
+    """A step whose inputs live in one pinned staging buffer (one host->device copy per step)
+    gives the same results as the step fed tensor by tensor."""
+    from paged_kv_decode_slot_gb300.step import DecodeStep, PackedInputs
+    w = gen.make_workload("f_packed", 77, 16, 4, 128, [30, 300, 17, 64, 900])
+    d = upload(w)
+    step = DecodeStep(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["block_tables"],
+                      d["context_lens"], w.scale)
+    packed = PackedInputs(step, step.input_names())
+    assert packed.bytes_per_step() == sum(t.numel() * t.element_size() for t in step.inputs())
+    q2 = gen.normal_bf16(78, 1, (w.B, w.N, w.H))
+    packed.host["q"].copy_(torch.from_numpy(q2.view(np.int16)).view(torch.bfloat16))
+    packed.upload()
+    step.run()
+    torch.cuda.synchronize()
+    ref = upload(w)
+    ref_step = DecodeStep(torch.from_numpy(q2.view(np.int16)).cuda().view(torch.bfloat16), ref["k_new"],
+                          ref["v_new"], ref["k_cache"], ref["v_cache"], ref["block_tables"],
+                          ref["context_lens"], w.scale)
+    ref_step.run()
+    torch.cuda.synchronize()
+    assert torch.equal(step.out.view(torch.int16), ref_step.out.view(torch.int16))
+    assert torch.equal(step.k_cache.view(torch.int16), ref_step.k_cache.view(torch.int16))
