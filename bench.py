@@ -281,8 +281,11 @@ def kernel_label(args, plan, step) -> str:
     if args.attn == "prefix":
         return "attn_cols_kernel<128> (prefix + suffix passes) + cascade_merge_kernel"
     fp8 = "1" if args.kv == "fp8" else "0"
+    if plan.mode == "split":
+        if step.launches_per_step() - (0 if step.fused else 2) == 1:
+            return f"attn_kernel<128,1,{fp8}> (partitions merged in the same launch)"
+        return f"attn_kernel<128,1,{fp8}> + lse_merge_kernel"
     return {"single": f"attn_kernel<128,0,{fp8}>",
-            "split": f"attn_kernel<128,1,{fp8}> + lse_merge_kernel",
             "balanced": "attn_balanced_kernel + balanced_merge_kernel"}[plan.mode]
 
 
