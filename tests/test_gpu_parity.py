@@ -335,3 +335,58 @@ def test_full_size_sampled(pkv, oracle, name):
     got = out_f64(step.out)[rows]
     assert_close(got, ref, f"{name} ({step.plan.describe()}) rows {rows}")
     assert_lse_close(step.lse.cpu().numpy()[rows], ref_lse, name)
+
+
+# --------------------------- partition merge paths and large shapes ---------------------------
+@pytest.mark.parametrize("part_blocks", [1, 2, 7])
+def test_split_merge_in_kernel_and_separate(pkv, oracle, part_blocks):
+    """1-block partitions of a 20K-token sequence make 1,250 partitions: G x 1,250 weights exceed
+    the attention kernel's ring, so the merge runs as a second launch; 2-block partitions (625)
+    merge inside the launch.  Both, and the fused step, match the oracle; a second call on the
+    same workspace (its counters back at zero) repeats the first bit for bit."""
+    w = gen.make_workload("merge_paths", 151, 16, 2, 128, [20000, 3000, 1, 17])
+    d = _post_append_device(pkv, oracle, w)
+    out, lse = _splitk(pkv, w, d, part_blocks)
+    kc, vc = appended_host_cache(oracle, w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    assert_close(out_f64(out), ref, f"split pb={part_blocks}")
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), ref_lse, f"split pb={part_blocks}")
+    P = pkv.max_partitions_for(w.max_blocks, part_blocks)
+    ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        o = torch.empty_like(d["q"])
+        pkv.check(pkv.pkv_decode_attn_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                             d["context_lens"], w.scale, o, part_blocks, P, ws))
+        outs.append(o)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.equal(outs[0].view(torch.int16), out.view(torch.int16))
+    # the workspace counters are zero again after every call
+    torch.cuda.synchronize()
+    cnt_off = ws.numel() - w.B * w.N * 4
+    assert int(ws[cnt_off:].view(torch.int32).abs().sum()) == 0
+
+
+def test_many_short_sequences(pkv, oracle):
+    """2,048 sequences of 1..64 tokens (a grid 2,048 sequences deep), every element."""
+    ctx = gen.uniform_int(161, 9, 2048, 1, 64)
+    w = gen.make_workload("many_short", 161, 32, 8, 128, ctx)
+    d = _post_append_device(pkv, oracle, w)
+    out, lse = _single(pkv, w, d)
+    kc, vc = appended_host_cache(oracle, w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    assert_close(out_f64(out), ref, "2048 short sequences")
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), ref_lse, "2048 short sequences")
+
+
+@pytest.mark.parametrize("part_blocks", [0, 4, 3])
+def test_context_fills_the_table(pkv, oracle, part_blocks):
+    """Every sequence as long as its table allows (ctx = max_blocks * 16): the last block is
+    full and the last partition ends at the table's end (or inside it)."""
+    w = gen.make_workload("full_table", 171, 16, 4, 64, [320, 320, 320], pool_factor=1.0)
+    assert w.max_blocks * 16 == 320
+    d = _post_append_device(pkv, oracle, w)
+    out, _ = _splitk(pkv, w, d, part_blocks) if part_blocks else _single(pkv, w, d)
+    kc, vc = appended_host_cache(oracle, w)
+    ref, _ = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    assert_close(out_f64(out), ref, f"full tables pb={part_blocks}")
