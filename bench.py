@@ -271,7 +271,7 @@ def traffic_key(args) -> str:
     if args.tokens > 1:
         key += f"+T{args.tokens}"
     if args.attn != "auto":
-        key += "+" + args.attn
+        key += "+" + args.attn + (f"{args.prefix_partition_blocks}" if args.attn == "prefix" else "")
     if args.unfused:
         key += "+unfused"
     if args.partition_blocks is not None:
@@ -357,7 +357,8 @@ def run_ours(args):
         gs, pb = groups
         step = PrefixDecodeStep(q, kn, vn, kc, vc, bt, cl, w.scale, d32(gs), d32(pb),
                                 int(np.max(np.diff(gs))), int(pb.max()),
-                                partition_blocks=args.partition_blocks or 16, err_flag=err)
+                                partition_blocks=args.partition_blocks or 16,
+                                prefix_partition_blocks=args.prefix_partition_blocks, err_flag=err)
         plan = step.plan
     elif args.kv == "fp8":
         if args.unfused or plan.mode == "balanced":
@@ -557,6 +558,8 @@ def main():
                     help="new tokens per sequence (> 1: speculative verification of that many)")
     ap.add_argument("--attn", choices=("auto", "prefix"), default="auto",
                     help="prefix: shared-prefix decode on a workload whose sequences share blocks")
+    ap.add_argument("--prefix-partition-blocks", type=int, default=0,
+                    help="with --attn prefix: blocks per partition of the shared-prefix pass")
     ap.add_argument("--unfused", action="store_true",
                     help="separate slot-mapping, append and attention launches")
     args = ap.parse_args()

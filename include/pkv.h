@@ -365,7 +365,7 @@ int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_dst, int32_
 /* Workspace bytes of pkv_decode_attn_prefix. */
 size_t pkv_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                   int32_t max_blocks_per_seq, int32_t max_prefix_blocks,
-                                  int32_t partition_blocks);
+                                  int32_t partition_blocks, int32_t prefix_partition_blocks);
 
 /* Decode attention (one token per sequence, the result of pkv_decode_attn) for a batch whose
    sequences form groups that share their leading blocks.  group_starts int32 [num_groups + 1]
@@ -374,8 +374,9 @@ size_t pkv_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
    blocks that every member's table shares with the group's first member (full blocks: a partly
    filled prefix block is copied on write and belongs to each member).  Sequences outside every
    group have no shared prefix.  The shared blocks are attended once per KV head for all the
-   group's queries (up to 32 query rows per loaded tile), each sequence's own blocks separately
-   in partitions of partition_blocks, and the partials are merged by their log-sum-exp.
+   group's queries (up to 32 query rows per loaded tile) in partitions of prefix_partition_blocks
+   (0: partition_blocks), each sequence's own blocks separately in partitions of
+   partition_blocks, and the partials are merged by their log-sum-exp.
    Host-side bounds: every group has at most max_group_size members and at most
    max_prefix_blocks (<= max_blocks_per_seq) shared blocks; a group beyond them, or a member
    shorter than its prefix, sets PKV_FLAG_GROUP_RANGE (that member's result is then void).  The
@@ -388,8 +389,8 @@ int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
                            float scale, const int32_t *group_starts, const int32_t *prefix_blocks,
                            int32_t num_groups, int32_t max_group_size, int32_t max_prefix_blocks,
                            pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
-                           int32_t partition_blocks, void *workspace, size_t workspace_bytes,
-                           int32_t *err_flag, pkv_stream_t stream);
+                           int32_t partition_blocks, int32_t prefix_partition_blocks, void *workspace,
+                           size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream);
 
 /* Synchronise the stream, copy *err_flag to *host_value; PKV_ERR_RANGE if it is non-zero. */
 int pkv_read_err_flag(const int32_t *err_flag, int32_t *host_value, pkv_stream_t stream);

@@ -406,11 +406,11 @@ _lib.pkv_slot_mapping_multi.argtypes = [_P, _I32, _P, _I32, _I32, _I32, _P, _P, 
 _lib.pkv_decode_attn_multi.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, ctypes.c_float, _P,
                                        _P, CacheDesc, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
 _lib.pkv_copy_blocks.argtypes = [_P, _P, _P, _I32, CacheDesc, _I32, _P, _P]
-_lib.pkv_prefix_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32]
+_lib.pkv_prefix_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32, _I32]
 _lib.pkv_prefix_workspace_bytes.restype = ctypes.c_size_t
 _lib.pkv_decode_attn_prefix.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P, _P,
-                                        _I32, _I32, _I32, _P, _P, CacheDesc, _I32, _P, ctypes.c_size_t,
-                                        _P, _P]
+                                        _I32, _I32, _I32, _P, _P, CacheDesc, _I32, _I32, _P,
+                                        ctypes.c_size_t, _P, _P]
 
 
 def pkv_slot_mapping_multi(block_tables, context_lens, num_blocks: int, slot_mapping, err_flag=None,
@@ -463,14 +463,16 @@ def pkv_copy_blocks(k_cache, v_cache, src_dst, err_flag=None, stream=None) -> in
 
 
 def pkv_prefix_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_blocks_per_seq: int,
-                               max_prefix_blocks: int, partition_blocks: int) -> int:
+                               max_prefix_blocks: int, partition_blocks: int,
+                               prefix_partition_blocks: int = 0) -> int:
     return int(_lib.pkv_prefix_workspace_bytes(num_seqs, num_q_heads, head_dim, max_blocks_per_seq,
-                                               max_prefix_blocks, partition_blocks))
+                                               max_prefix_blocks, partition_blocks, prefix_partition_blocks))
 
 
 def pkv_decode_attn_prefix(q, k_cache, v_cache, block_tables, context_lens, scale: float, group_starts,
                            prefix_blocks, max_group_size: int, max_prefix_blocks: int, out, lse_out=None,
-                           partition_blocks: int = 16, workspace=None, err_flag=None, stream=None) -> int:
+                           partition_blocks: int = 16, workspace=None, err_flag=None, stream=None,
+                           prefix_partition_blocks: int = 0) -> int:
     """Decode attention with each group's shared leading blocks attended once per KV head."""
     _need(q, torch.bfloat16, 3, "q")
     _need(k_cache, torch.bfloat16, 4, "k_cache")
@@ -490,9 +492,9 @@ def pkv_decode_attn_prefix(q, k_cache, v_cache, block_tables, context_lens, scal
                                        block_tables.shape[1], _ptr(context_lens), B, N, float(scale),
                                        _ptr(group_starts), _ptr(prefix_blocks), prefix_blocks.numel(),
                                        max_group_size, max_prefix_blocks, _ptr(out), _ptr(lse_out),
-                                       cache_desc(k_cache), partition_blocks, _ptr(workspace),
-                                       0 if workspace is None else workspace.numel(), _ptr(err_flag),
-                                       _stream(stream))
+                                       cache_desc(k_cache), partition_blocks, prefix_partition_blocks,
+                                       _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                                       _ptr(err_flag), _stream(stream))
 
 
 def pkv_gather(k_cache, v_cache, block_tables, context_lens, cu_seqlens, k_out, v_out, err_flag=None,

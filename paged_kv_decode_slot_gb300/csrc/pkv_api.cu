@@ -952,12 +952,13 @@ PKV_EXPORT int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache,
 
 PKV_EXPORT size_t pkv_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                              int32_t max_blocks_per_seq, int32_t max_prefix_blocks,
-                                             int32_t partition_blocks)
+                                             int32_t partition_blocks, int32_t prefix_partition_blocks)
 {
+    if (prefix_partition_blocks == 0) prefix_partition_blocks = partition_blocks;
     if (num_seqs < 0 || num_q_heads < 0 || head_dim < 0 || max_blocks_per_seq <= 0 ||
-        max_prefix_blocks < 0 || partition_blocks <= 0)
+        max_prefix_blocks < 0 || partition_blocks <= 0 || prefix_partition_blocks <= 0)
         return 0;
-    const int32_t parts = prefix_parts_for(max_prefix_blocks, partition_blocks) +
+    const int32_t parts = prefix_parts_for(max_prefix_blocks, prefix_partition_blocks) +
                           (max_blocks_per_seq + partition_blocks - 1) / partition_blocks;
     return pkv_splitk_workspace_bytes(num_seqs, num_q_heads, head_dim, parts);
 }
@@ -969,15 +970,16 @@ PKV_EXPORT int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache
                                       const int32_t *prefix_blocks, int32_t num_groups,
                                       int32_t max_group_size, int32_t max_prefix_blocks, pkv_bf16 *out,
                                       float *lse_out, pkv_cache_desc cache, int32_t partition_blocks,
-                                      void *workspace, size_t workspace_bytes, int32_t *err_flag,
-                                      pkv_stream_t stream)
+                                      int32_t prefix_partition_blocks, void *workspace,
+                                      size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream)
 {
+    if (prefix_partition_blocks == 0) prefix_partition_blocks = partition_blocks;
     AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                num_q_heads, scale, cache, err_flag};
     int st = validate_attn(a);
     if (st != PKV_OK) return st;
     if (!out || !workspace) return PKV_ERR_NULL;
-    if (num_groups < 0 || partition_blocks <= 0 || max_prefix_blocks < 0 ||
+    if (num_groups < 0 || partition_blocks <= 0 || prefix_partition_blocks <= 0 || max_prefix_blocks < 0 ||
         max_prefix_blocks > max_blocks_per_seq)
         return PKV_ERR_SHAPE;
     if (num_groups > 0 && (!group_starts || !prefix_blocks)) return PKV_ERR_NULL;
@@ -985,12 +987,13 @@ PKV_EXPORT int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache
     if (!aligned(out, 4) || !aligned(lse_out, 4) || !aligned(workspace, 256)) return PKV_ERR_ALIGN;
     if (workspace_bytes < pkv_prefix_workspace_bytes(num_seqs, num_q_heads, cache.head_dim,
                                                      max_blocks_per_seq, max_prefix_blocks,
-                                                     partition_blocks))
+                                                     partition_blocks, prefix_partition_blocks))
         return PKV_ERR_WORKSPACE;
     const int32_t G = num_q_heads / cache.num_kv_heads;
-    const int32_t prefix_parts = prefix_parts_for(max_prefix_blocks, partition_blocks);
+    const int32_t prefix_parts = prefix_parts_for(max_prefix_blocks, prefix_partition_blocks);
     const int32_t suffix_parts = (max_blocks_per_seq + partition_blocks - 1) / partition_blocks;
     const int32_t max_parts = prefix_parts + suffix_parts;
+    if (max_parts > kMaxMergeParts) return PKV_ERR_UNSUPPORTED;
     const int32_t chunks = num_groups > 0 ? (max_group_size * G + kColsPerCta - 1) / kColsPerCta : 1;
     const int64_t prefix_ctas = (int64_t)cache.num_kv_heads * num_groups * chunks * prefix_parts;
     const int64_t grid = prefix_ctas + (int64_t)cache.num_kv_heads * num_seqs * suffix_parts;
@@ -1002,6 +1005,7 @@ PKV_EXPORT int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache
     if (st != PKV_OK) return st;
     pkv::ColsParams p = cols_params_of(a, tok_major);
     p.part_blocks = partition_blocks;
+    p.prefix_part_blocks = prefix_partition_blocks;
     p.parts = max_parts;
     p.split = 1;
     p.max_parts = max_parts;

@@ -43,6 +43,12 @@ struct ColsWork {
     int slot;       // partition slot of the outputs, -1: final outputs (multi, one pass)
 };
 
+// Shared leading blocks of group g, clamped to what the prefix pass covers and the table holds.
+__device__ __forceinline__ int prefix_blocks_of(const ColsParams &p, int g)
+{
+    return max(0, min(p.prefix_blocks[g], min(p.prefix_parts * p.prefix_part_blocks, p.max_nb)));
+}
+
 // Group of sequence b: the largest g with group_starts[g] <= b (b outside every group: -1).
 __device__ __forceinline__ int group_of(const ColsParams &p, int b)
 {
@@ -97,25 +103,25 @@ __device__ __forceinline__ bool cols_work(const ColsParams &p, int64_t c, ColsWo
         const int cols = (ge - gs) * p.G;
         int pnb = p.prefix_blocks[g];
         if (first_thread && w.kvh == 0 && ppart == 0 && chunk == p.chunks - 1 &&
-            (ge - gs > p.max_group || pnb > p.prefix_parts * p.part_blocks || pnb < 0 ||
+            (ge - gs > p.max_group || pnb > p.prefix_parts * p.prefix_part_blocks || pnb < 0 ||
              gs != gs_raw || ge != ge_raw))
             set_flag(p.err_flag, PKV_FLAG_GROUP_RANGE);
-        pnb = max(0, min(pnb, min(p.prefix_parts * p.part_blocks, p.max_nb)));
+        pnb = prefix_blocks_of(p, g);
         w.mode = kModePrefix;
         w.b = gs;
         w.vis = pnb * kBlockSize;
         w.col_base = chunk * kColsPerCta;
         w.ncols = min(kColsPerCta, cols - w.col_base);
         w.table_row = gs;
-        w.blk_begin = ppart * p.part_blocks;
-        w.blk_end = min(pnb, w.blk_begin + p.part_blocks);
+        w.blk_begin = ppart * p.prefix_part_blocks;
+        w.blk_end = min(pnb, w.blk_begin + p.prefix_part_blocks);
         w.data_end = w.vis;
         w.slot = ppart;
         return w.ncols > 0 && w.blk_begin < w.blk_end;
     }
     // suffix pass: (sequence, suffix partition)
     c -= p.prefix_ctas / p.K;
-    const int sparts = p.max_parts - p.prefix_parts;
+    const int sparts = (p.max_nb + p.part_blocks - 1) / p.part_blocks;
     const int spart = (int)(c % sparts);
     w.mode = kModeSuffix;
     w.b = (int)(c / sparts);
@@ -125,7 +131,7 @@ __device__ __forceinline__ bool cols_work(const ColsParams &p, int64_t c, ColsWo
         return false;
     }
     const int g = group_of(p, w.b);
-    const int pnb = g >= 0 ? max(0, min(p.prefix_blocks[g], min(p.prefix_parts * p.part_blocks, p.max_nb))) : 0;
+    const int pnb = g >= 0 ? prefix_blocks_of(p, g) : 0;
     if (pnb * kBlockSize > ctx) {
         if (first_thread && w.kvh == 0 && spart == 0) set_flag(p.err_flag, PKV_FLAG_GROUP_RANGE);
         return false;
@@ -138,7 +144,8 @@ __device__ __forceinline__ bool cols_work(const ColsParams &p, int64_t c, ColsWo
     w.blk_begin = pnb + spart * p.part_blocks;
     w.blk_end = min(nb, w.blk_begin + p.part_blocks);
     w.data_end = ctx;
-    w.slot = p.prefix_parts + spart;
+    // a row's partials are contiguous: its prefix partitions, then its suffix partitions
+    w.slot = (pnb + p.prefix_part_blocks - 1) / p.prefix_part_blocks + spart;
     return w.blk_begin < w.blk_end;
 }
 
@@ -407,36 +414,31 @@ attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 }
 
 // Merge of the prefix pass and the suffix pass of one (sequence, query head): slots
-// [0, ceil(pnb / PB)) hold the shared prefix, [prefix_parts, prefix_parts + ceil((nb - pnb) / PB))
-// the sequence's own blocks.
+// [0, ceil(pnb / prefix PB)) hold the shared prefix, the next ceil((nb - pnb) / PB) the
+// sequence's own blocks; one warp computes the log-sum-exp weights, every thread one element.
 __global__ void cascade_merge_kernel(const ColsParams p, __nv_bfloat16 *__restrict__ out,
                                      float *__restrict__ lse_out)
 {
+    extern __shared__ float wts[];  // [max_parts]
+    __shared__ float row_lse;
     const int n = blockIdx.x, b = blockIdx.y, h = threadIdx.x;
     const int H = blockDim.x;
     const int64_t row = (int64_t)b * p.N + n;
     const int ctx = p.context_lens[b];
     const int g = group_of(p, b);
-    const int pnb = g >= 0 ? max(0, min(p.prefix_blocks[g], min(p.prefix_parts * p.part_blocks, p.max_nb))) : 0;
+    const int pnb = g >= 0 ? prefix_blocks_of(p, g) : 0;
     const bool ok = ctx >= 0 && ctx <= p.max_nb * kBlockSize && pnb * kBlockSize <= ctx;
     const int nb = ok ? (ctx + kBlockSize - 1) / kBlockSize : 0;
-    const int np_pre = ok ? (pnb + p.part_blocks - 1) / p.part_blocks : 0;
-    const int np_suf = ok ? (nb - pnb + p.part_blocks - 1) / p.part_blocks : 0;
-    const float *lp = p.part_lse + row * p.max_parts;
-    const float *po = p.part_out + row * p.max_parts * H + h;
-    auto slot = [&](int q) { return q < np_pre ? q : p.prefix_parts + (q - np_pre); };
-    const int np = np_pre + np_suf;
-    float M = -INFINITY;
-    for (int q = 0; q < np; ++q) M = fmaxf(M, lp[slot(q)]);
-    float total = -INFINITY, val = 0.f;
-    if (M != -INFINITY) {
-        float sum = 0.f;
-        for (int q = 0; q < np; ++q) sum += expf(lp[slot(q)] - M);
-        total = M + logf(sum);
-        for (int q = 0; q < np; ++q) val += expf(lp[slot(q)] - total) * po[(int64_t)slot(q) * H];
+    const int np = ok ? (pnb + p.prefix_part_blocks - 1) / p.prefix_part_blocks +
+                            (nb - pnb + p.part_blocks - 1) / p.part_blocks
+                      : 0;
+    if (h < 32) {
+        const float L = lse_merge_weights(p.part_lse + row * p.max_parts, np, wts, h);
+        if (h == 0) row_lse = L;
     }
-    out[row * H + h] = __float2bfloat16_rn(val);
-    if (h == 0 && lse_out) lse_out[row] = total;
+    __syncthreads();
+    out[row * H + h] = __float2bfloat16_rn(lse_merge_value(wts, p.part_out + row * p.max_parts * H + h, np, H));
+    if (h == 0 && lse_out) lse_out[row] = row_lse;
 }
 
 template <typename Kern>
@@ -476,7 +478,7 @@ cudaError_t launch_cascade_merge(const ColsParams &p, int H, __nv_bfloat16 *out,
                                  cudaStream_t stream)
 {
     if (p.B <= 0) return cudaSuccess;
-    cascade_merge_kernel<<<dim3(p.N, p.B), H, 0, stream>>>(p, out, lse_out);
+    cascade_merge_kernel<<<dim3(p.N, p.B), H, (size_t)p.max_parts * sizeof(float), stream>>>(p, out, lse_out);
     return cudaGetLastError();
 }
 

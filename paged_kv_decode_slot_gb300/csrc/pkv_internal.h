@@ -78,7 +78,8 @@ struct ColsParams {
     const int32_t *prefix_blocks;  // prefix mode: [num_groups] shared leading blocks per group
     int32_t num_groups;
     int32_t max_group;             // prefix mode: declared bound on the members of a group
-    int32_t prefix_parts;          // prefix mode: partition slots of the prefix pass
+    int32_t prefix_part_blocks;    // prefix mode: blocks per prefix-pass partition
+    int32_t prefix_parts;          // prefix mode: partitions of the prefix pass (grid)
     int32_t prefix_ctas;           // prefix mode: CTAs of the prefix pass
     int32_t *err_flag;
 };

@@ -322,8 +322,12 @@ class MultiTokenStep:
 class PrefixDecodeStep:
     """A decode step of a batch whose sequences share leading blocks (copy-on-write prefix
     sharing): slot mapping and append of the new token, then ``pkv_decode_attn_prefix`` -- each
-    group's shared blocks attended once per KV head for all its members, each sequence's own
-    blocks in partitions of ``partition_blocks``, merged by log-sum-exp.
+    group's shared blocks attended once per KV head for all its members in partitions of
+    ``prefix_partition_blocks`` (0: ``partition_blocks``), each sequence's own blocks in partitions
+    of ``partition_blocks``, merged by log-sum-exp.  Every partition leaves fp32 partials for 32
+    query rows, so small prefix partitions cost more in partial traffic and merging than they
+    gain in parallelism (measured on the 1000-token shared prompt: 1-block prefix partitions
+    126 us per step, 16-block 42 us).
 
     group_starts int32 [G+1] and prefix_blocks int32 [G] on the device; max_group_size and
     max_prefix_blocks are host-side bounds on them.
@@ -331,13 +335,14 @@ class PrefixDecodeStep:
 
     def __init__(self, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
                  group_starts, prefix_blocks, max_group_size: int, max_prefix_blocks: int,
-                 partition_blocks: int = 16, err_flag=None):
+                 partition_blocks: int = 16, prefix_partition_blocks: int = 0, err_flag=None):
         self.q, self.k_new, self.v_new = q, k_new, v_new
         self.k_cache, self.v_cache = k_cache, v_cache
         self.block_tables, self.context_lens = block_tables, context_lens
         self.group_starts, self.prefix_blocks = group_starts, prefix_blocks
         self.max_group_size, self.max_prefix_blocks = int(max_group_size), int(max_prefix_blocks)
         self.partition_blocks = int(partition_blocks)
+        self.prefix_partition_blocks = int(prefix_partition_blocks)
         self.scale = float(scale)
         dev = q.device
         nseq, N, H = q.shape
@@ -349,7 +354,7 @@ class PrefixDecodeStep:
         self.lse = torch.empty(nseq, N, dtype=torch.float32, device=dev)
         self.err_flag = err_flag
         nbytes = B.pkv_prefix_workspace_bytes(nseq, N, H, block_tables.shape[1], self.max_prefix_blocks,
-                                              self.partition_blocks)
+                                              self.partition_blocks, self.prefix_partition_blocks)
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def slot_and_append(self, stream=None) -> None:
@@ -363,7 +368,8 @@ class PrefixDecodeStep:
                                          self.context_lens, self.scale, self.group_starts,
                                          self.prefix_blocks, self.max_group_size,
                                          self.max_prefix_blocks, self.out, self.lse,
-                                         self.partition_blocks, self.workspace, self.err_flag, stream))
+                                         self.partition_blocks, self.workspace, self.err_flag, stream,
+                                         prefix_partition_blocks=self.prefix_partition_blocks))
 
     def run(self, stream=None) -> None:
         self.slot_and_append(stream)

@@ -221,28 +221,30 @@ def share_prefixes(w: gen.Workload, groups):
 
 
 def run_prefix(pkv, w, kc, vc, tables, starts, pblocks, part_blocks, max_group=None, max_prefix=None,
-               err=None):
+               err=None, prefix_part_blocks=0):
     q = bf16_dev(w.q)
     out = torch.empty_like(q)
     lse = torch.empty(w.B, w.N, dtype=torch.float32, device="cuda")
     max_group = max_group or int(np.max(np.diff(starts)))
     max_prefix = int(pblocks.max()) if max_prefix is None else max_prefix
-    ws = torch.empty(pkv.pkv_prefix_workspace_bytes(w.B, w.N, w.H, tables.shape[1], max_prefix, part_blocks),
+    ws = torch.empty(pkv.pkv_prefix_workspace_bytes(w.B, w.N, w.H, tables.shape[1], max_prefix, part_blocks,
+                                                    prefix_part_blocks),
                      dtype=torch.uint8, device="cuda")
     pkv.check(pkv.pkv_decode_attn_prefix(q, kc, vc, i32_dev(tables), i32_dev(w.context_lens), w.scale,
                                          i32_dev(starts), i32_dev(pblocks), max_group, max_prefix, out, lse,
-                                         part_blocks, ws, err))
+                                         part_blocks, ws, err, prefix_partition_blocks=prefix_part_blocks))
     return out, lse
 
 
-@pytest.mark.parametrize("part_blocks", [4, 8, 16, 64])
-def test_prefix_workload_matches_oracle(pkv, oracle, part_blocks):
+@pytest.mark.parametrize("part_blocks,prefix_part_blocks", [(4, 0), (8, 0), (16, 0), (64, 0), (16, 4), (8, 2),
+                                                           (16, 7)])
+def test_prefix_workload_matches_oracle(pkv, oracle, part_blocks, prefix_part_blocks):
     w = gen.make_config("prefix_l3_70b")
     starts, pblocks = w.prefix_groups()
     kc, vc = appended_host_cache(oracle, w)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, lse = run_prefix(pkv, w, bf16_dev(kc), bf16_dev(vc), w.block_tables, starts, pblocks, part_blocks,
-                          err=err)
+                          err=err, prefix_part_blocks=prefix_part_blocks)
     assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
     ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
     assert_close(out_f64(out), ref, f"prefix pb={part_blocks}")
@@ -259,16 +261,17 @@ PREFIX_CASES = [
 ]
 
 
-@pytest.mark.parametrize("part_blocks", [2, 5, 16])
+@pytest.mark.parametrize("part_blocks,prefix_part_blocks", [(2, 0), (5, 0), (16, 0), (16, 3)])
 @pytest.mark.parametrize("name,N,K,H,ctx,groups", PREFIX_CASES, ids=[c[0] for c in PREFIX_CASES])
-def test_prefix_groups_match_oracle(pkv, oracle, name, N, K, H, ctx, groups, part_blocks):
+def test_prefix_groups_match_oracle(pkv, oracle, name, N, K, H, ctx, groups, part_blocks, prefix_part_blocks):
     w = gen.make_workload(f"p_{name}", 131, N, K, H, ctx)
     tables, starts, pblocks = share_prefixes(w, groups)
     kc, vc = w.k_cache.copy(), w.v_cache.copy()
     slots = oracle.slot_mapping(tables, w.context_lens)
     oracle.append(w.k_new, w.v_new, slots, kc, vc)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out, lse = run_prefix(pkv, w, bf16_dev(kc), bf16_dev(vc), tables, starts, pblocks, part_blocks, err=err)
+    out, lse = run_prefix(pkv, w, bf16_dev(kc), bf16_dev(vc), tables, starts, pblocks, part_blocks, err=err,
+                          prefix_part_blocks=prefix_part_blocks)
     assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
     ref, ref_lse = oracle.decode(w.q, kc, vc, tables, w.context_lens, w.scale)
     assert_close(out_f64(out), ref, f"prefix {name} pb={part_blocks}")
