@@ -42,6 +42,22 @@ int check_copy_desc(const pkv_cache_desc &d)
     return PKV_OK;
 }
 
+// SM count of the current device (cached per device).
+int sm_count(int *sms)
+{
+    static int cache[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return PKV_ERR_UNSUPPORTED;
+    if (!cache[dev]) {
+        e = cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    }
+    *sms = cache[dev];
+    return PKV_OK;
+}
+
 // ---- TMA descriptors for the K and V pools -----------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
@@ -512,7 +528,11 @@ int fp8_attention(const AttnArgs &a, const pkv_bf16 *k_new, const pkv_bf16 *v_ne
         p.part_lse = sw.part_lse;
         p.counters = merge_in_kernel(a.N, a.d.num_kv_heads, max_partitions) ? sw.counters : nullptr;
     }
-    cudaError_t e = pkv::launch_attn(a.d.head_dim, split, tk, tv, p, stream, true);
+    int sms = 0;
+    st = sm_count(&sms);
+    if (st != PKV_OK) return st;
+    const bool pairs = (int64_t)a.B * a.d.num_kv_heads < sms;
+    cudaError_t e = pkv::launch_attn(a.d.head_dim, split, tk, tv, p, stream, true, pairs);
     if (e != cudaSuccess) return cuda_fail(e, "e4m3 attention launch");
     if (!split || p.counters) return PKV_OK;
     return pkv_lse_merge(sw.part_out, sw.part_lse, a.context_lens, a.B, a.N, a.d.head_dim, max_partitions,
@@ -589,20 +609,6 @@ PKV_EXPORT int pkv_decode_step_fp8(const pkv_bf16 *q, const pkv_bf16 *k_new, con
 // ---- balanced split (persistent grid, equal tile shares) -----------------------------------
 namespace {
 
-int sm_count(int *sms)
-{
-    static int cache[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= 64) return PKV_ERR_UNSUPPORTED;
-    if (!cache[dev]) {
-        e = cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    }
-    *sms = cache[dev];
-    return PKV_OK;
-}
 
 // The balanced kernel's CTAs per SM times the SM count, rounded down to a multiple of the KV
 // head count: CTA c = share * K + head.  The merge holds at most 512 pieces of one unit.

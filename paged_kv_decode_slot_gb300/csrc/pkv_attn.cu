@@ -95,7 +95,7 @@ __device__ __forceinline__ void append_new_token_fp8(const AttnParams &p, int b,
 // ------------------------ single pass and fixed partitions --------------------------------
 // kFp8: the pools hold e4m3 codes with per-KV-head scales (H = 128); the K scale is folded into
 // the logit multiplier, the V scale into the final normalisation.
-template <int H, bool kSplit, bool kFp8 = false>
+template <int H, bool kSplit, bool kFp8 = false, bool kPairs = false>
 __global__ void __launch_bounds__(kAttnThreads, PKV_CTAS_PER_SM)
 attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
             const AttnParams p)
@@ -194,6 +194,51 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
             const size_t row = ((size_t)b * p.K + kvh) * H;
             prefetch_l2((lane ? p.v_new : p.k_new) + row);
         }
+        if constexpr (kPairs) {
+            // e4m3, few CTAs per SM: each warp takes its next two tiles (i and i + W) in one step
+            // (two independent chains in flight); the ring holds S >= 2W stages, so the producer
+            // can always fill the second one.
+            static_assert(S >= 2 * kConsumerWarps, "pairs of tiles need two stages per warp");
+            for (int i = warp; i < nblk; i += 2 * kConsumerWarps) {
+                const int i2 = i + kConsumerWarps;
+                const bool has2 = i2 < nblk;
+                const int s1 = i % S, s2 = i2 % S;
+                bool ok = mbar_wait_bounded(bar_full + 8 * s1, (i / S) & 1, abort_flag, kWaitLimitNs);
+                if (ok && has2) ok = mbar_wait_bounded(bar_full + 8 * s2, (i2 / S) & 1, abort_flag, kWaitLimitNs);
+                if (!ok) {
+                    if (!*abort_flag) set_flag(p.err_flag, PKV_FLAG_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                uint32_t kts[2], vts[2];
+                int valid[2];
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const int it = t ? i2 : i, st = t ? s2 : s1;
+                    const bool here = t == 0 || has2;
+                    kts[t] = base_u32 + (here ? st : s1) * L::kStageBytes;
+                    vts[t] = kts[t] + L::kTileBytes;
+                    valid[t] = here && slot_ok[st] ? min(kBlockSize, ctx - (blk_begin + it) * kBlockSize) : 0;
+                    // fused append: the tile of the sequence's last block holds the new token
+                    const bool newest = here && p.k_new && blk_begin + it == nb - 1;
+                    if (newest) {
+                        const int last_bid = __ldg(p.block_tables + (size_t)b * p.max_nb + nb - 1);
+                        if (slot_ok[st]) {
+                            append_new_token_fp8<H>(p, b, kvh, ctx, last_bid, kts[t], vts[t], lane);
+                            __syncwarp();
+                        }
+                        if (p.slot_out && kvh == 0 && lane == 0)
+                            p.slot_out[b] = slot_ok[st] ? (int64_t)last_bid * kBlockSize + (ctx - 1) % kBlockSize : -1;
+                    }
+                }
+                if (valid[0] > 0 || valid[1] > 0) tile_update_fp8_n<H, 2>(acc, qf, kts, vts, valid, sl2, lane);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar_empty + 8 * s1);
+                    if (has2) mbar_arrive(bar_empty + 8 * s2);
+                }
+            }
+        } else
         for (int i = warp; i < nblk; i += kConsumerWarps) {
             const int s = i % S;
             if (!mbar_wait_bounded(bar_full + 8 * s, (i / S) & 1, abort_flag, kWaitLimitNs)) {
@@ -599,26 +644,30 @@ static cudaError_t ensure_smem(Kern kern, int smem, int *cached)
     return e;
 }
 
-template <int H, bool kSplit, bool kFp8>
+template <int H, bool kSplit, bool kFp8, bool kPairs = false>
 static cudaError_t launch_attn_t(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
                                  dim3 grid, cudaStream_t stream)
 {
     constexpr int smem = AttnLayout<H, kFp8 ? kStagesFp8 : kStages, kConsumerWarps, kProducers,
                                     kFp8 ? 1 : 2>::kAlloc;
     static int cached[64] = {};
-    cudaError_t e = ensure_smem(attn_kernel<H, kSplit, kFp8>, smem, cached);
+    cudaError_t e = ensure_smem(attn_kernel<H, kSplit, kFp8, kPairs>, smem, cached);
     if (e != cudaSuccess) return e;
-    attn_kernel<H, kSplit, kFp8><<<grid, kAttnThreads, smem, stream>>>(tk, tv, p);
+    attn_kernel<H, kSplit, kFp8, kPairs><<<grid, kAttnThreads, smem, stream>>>(tk, tv, p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const AttnParams &p, cudaStream_t stream, bool fp8)
+                        const AttnParams &p, cudaStream_t stream, bool fp8, bool pairs)
 {
     dim3 grid = split ? dim3(p.K, p.B, p.max_parts) : dim3(p.K, p.B, 1);
-    if (fp8)  // e4m3 pools: H = 128 only
+    if (fp8) {  // e4m3 pools: H = 128 only; tile pairs for grids with few CTAs per SM
+        if (pairs)
+            return split ? launch_attn_t<128, true, true, true>(tk, tv, p, grid, stream)
+                         : launch_attn_t<128, false, true, true>(tk, tv, p, grid, stream);
         return split ? launch_attn_t<128, true, true>(tk, tv, p, grid, stream)
                      : launch_attn_t<128, false, true>(tk, tv, p, grid, stream);
+    }
     if (H == 128)
         return split ? launch_attn_t<128, true, false>(tk, tv, p, grid, stream)
                      : launch_attn_t<128, false, false>(tk, tv, p, grid, stream);

@@ -345,6 +345,123 @@ __device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&
     }
 }
 
+// NT e4m3 tiles (each 16 tokens, the first valid[t] of them count) folded into a warp's state in
+// one step: the NT QK^T chains are independent, one max / rescale covers all 16 NT tokens, then
+// the NT PV products accumulate.  A warp that takes two of its tiles at once has two
+// independent dependency chains in flight where one tile's chain would leave it waiting.  A
+// column that has seen no key keeps m = -inf and gets zero weights.  The caller skips a step in
+// which no tile has a valid token.
+template <int H, int NT>
+__device__ __forceinline__ void tile_update_fp8_n(WarpAcc<H> &a, const uint32_t (&qf)[H / 16][2],
+                                                  const uint32_t (&kt)[NT], const uint32_t (&vt)[NT],
+                                                  const int (&valid)[NT], float sl2, int lane)
+{
+    constexpr int kKSteps = H / 16;
+    const int mi = lane >> 3, ri = lane & 7;
+    const int tok = ri + 8 * (mi & 1), coff = mi >> 1;
+    const int t0 = lane >> 2, t1 = t0 + 8;
+
+    // S^T = K . Q^T for each tile
+    float x[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < kKSteps; kk += 2) {
+            uint32_t r[4];
+            ldsm_x4(r, kt[t] + fp8_chunk_offset(tok, kk + coff));
+            uint32_t a0[4], a1[4];
+            a0[0] = e4m3x2_to_f16x2((uint16_t)(r[0] & 0xFFFFu));
+            a0[1] = e4m3x2_to_f16x2((uint16_t)(r[1] & 0xFFFFu));
+            a0[2] = e4m3x2_to_f16x2((uint16_t)(r[0] >> 16));
+            a0[3] = e4m3x2_to_f16x2((uint16_t)(r[1] >> 16));
+            a1[0] = e4m3x2_to_f16x2((uint16_t)(r[2] & 0xFFFFu));
+            a1[1] = e4m3x2_to_f16x2((uint16_t)(r[3] & 0xFFFFu));
+            a1[2] = e4m3x2_to_f16x2((uint16_t)(r[2] >> 16));
+            a1[3] = e4m3x2_to_f16x2((uint16_t)(r[3] >> 16));
+            mma_f16_16816(sa, a0, qf[kk][0], qf[kk][1]);
+            mma_f16_16816(sb, a1, qf[kk + 1][0], qf[kk + 1][1]);
+        }
+        x[t][0] = t0 < valid[t] ? (sa[0] + sb[0]) * sl2 : -INFINITY;
+        x[t][1] = t0 < valid[t] ? (sa[1] + sb[1]) * sl2 : -INFINITY;
+        x[t][2] = t1 < valid[t] ? (sa[2] + sb[2]) * sl2 : -INFINITY;
+        x[t][3] = t1 < valid[t] ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+    }
+    float mA = -INFINITY, mB = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        mA = fmaxf(mA, fmaxf(x[t][0], x[t][2]));
+        mB = fmaxf(mB, fmaxf(x[t][1], x[t][3]));
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mA = fmaxf(mA, __shfl_xor_sync(0xFFFFFFFFu, mA, off));
+        mB = fmaxf(mB, __shfl_xor_sync(0xFFFFFFFFu, mB, off));
+    }
+    const bool needA = mA > a.m[0] + kRescaleThreshold;
+    const bool needB = mB > a.m[1] + kRescaleThreshold;
+    if (__any_sync(0xFFFFFFFFu, needA || needB)) {
+        const float alphaA = needA ? exp2f(a.m[0] - mA) : 1.f;
+        const float alphaB = needB ? exp2f(a.m[1] - mB) : 1.f;
+        if (needA) a.m[0] = mA;
+        if (needB) a.m[1] = mB;
+        a.l[0] *= alphaA;
+        a.l[1] *= alphaB;
+#pragma unroll
+        for (int mt = 0; mt < kKSteps; ++mt) {
+            a.o[mt][0] *= alphaA;
+            a.o[mt][1] *= alphaB;
+            a.o[mt][2] *= alphaA;
+            a.o[mt][3] *= alphaB;
+        }
+    }
+    const float baseA = a.m[0] == -INFINITY ? 0.f : a.m[0];
+    const float baseB = a.m[1] == -INFINITY ? 0.f : a.m[1];
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const uint32_t p01 = pack_f16x2(exp2f(x[t][0] - baseA), exp2f(x[t][1] - baseB));
+        const uint32_t p23 = pack_f16x2(exp2f(x[t][2] - baseA), exp2f(x[t][3] - baseB));
+        a.l[0] += f16x2_lo(p01) + f16x2_lo(p23);
+        a.l[1] += f16x2_hi(p01) + f16x2_hi(p23);
+        pb[t][0] = movmatrix_trans(p01);
+        pb[t][1] = movmatrix_trans(p23);
+    }
+
+    // O^T += V^T . P^T for each tile (see tile_update_fp8 for the byte regrouping)
+    const int tc = (lane & 3) * 2;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const bool partial = valid[t] < kBlockSize;
+#pragma unroll
+        for (int mt = 0; mt < kKSteps; mt += 2) {
+            uint32_t r[4];
+            ldsm_x4_trans(r, vt[t] + fp8_chunk_offset(tok, mt + coff));
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const uint32_t lo = byte_perm(r[2 * hf], 0u, 0x3120u);
+                const uint32_t hi = byte_perm(r[2 * hf + 1], 0u, 0x3120u);
+                uint32_t av[4];
+                av[0] = e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu));
+                av[1] = e4m3x2_to_f16x2((uint16_t)(lo >> 16));
+                av[2] = e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu));
+                av[3] = e4m3x2_to_f16x2((uint16_t)(hi >> 16));
+                if (partial) {
+                    const uint32_t lo0 = tc < valid[t] ? 0x0000FFFFu : 0u;
+                    const uint32_t hi0 = tc + 1 < valid[t] ? 0xFFFF0000u : 0u;
+                    const uint32_t lo1 = tc + 8 < valid[t] ? 0x0000FFFFu : 0u;
+                    const uint32_t hi1 = tc + 9 < valid[t] ? 0xFFFF0000u : 0u;
+                    av[0] &= lo0 | hi0;
+                    av[1] &= lo0 | hi0;
+                    av[2] &= lo1 | hi1;
+                    av[3] &= lo1 | hi1;
+                }
+                mma_f16_16816(a.o[mt + hf], av, pb[t][0], pb[t][1]);
+            }
+        }
+    }
+}
+
 // Finish a warp's sums (across the lanes that share a column) and store its state in the
 // merge area: mo[W][8][H], mm[W][8] (running max), ml[W][8] (running sum).
 template <int H, bool kFp8 = false>

@@ -43,8 +43,10 @@ struct AttnParams {
     int32_t *err_flag;             // nullable
 };
 
+// fp8: e4m3 pools (H = 128); pairs: e4m3 consumers take two tiles per step (for grids with
+// fewer (sequence, KV head) units than SMs, where each CTA's dependency chains set the pace).
 cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const AttnParams &p, cudaStream_t stream, bool fp8 = false);
+                        const AttnParams &p, cudaStream_t stream, bool fp8 = false, bool pairs = false);
 
 // Column-parallel attention (pkv_attn_cols.cu): a CTA serves up to 32 query rows ("columns")
 // of one KV head over one list of logical blocks; each consumer warp owns 8 columns, and every
