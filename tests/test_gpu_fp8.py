@@ -237,3 +237,26 @@ def test_fp8_full_size_sampled(pkv, oracle):
     ref, _ = oracle.decode_fp8(w.q[sample], c.kc8_app, c.vc8_app, c.ks, c.vs, bt, cl, w.scale)
     assert_close(out_f64(out[sample]), ref, "fp8 l3_8b_b64 single")
     assert_close(out_f64(out_s[sample]), ref, "fp8 l3_8b_b64 split")
+
+
+@pytest.mark.parametrize("name", ["l3_8b_b64", "l2_13b_mha_b128", "long_splitk", "l3_8b_b16"])
+def test_fp8_step_full_size_in_bench_plan(pkv, oracle, name):
+    """The e4m3 decode step as the benchmark times it (DecodeStepFp8 with the planner's plan: one
+    tile per step on wide grids, two on grids with fewer units than SMs), sampled sequences."""
+    from paged_kv_decode_slot_gb300.step import DecodeStepFp8
+    w = gen.make_config(name)
+    c = Fp8Case(oracle, w)
+    d = c.device(appended=False)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    step = DecodeStepFp8(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["k_scale"],
+                         d["v_scale"], d["block_tables"], d["context_lens"], w.scale, err_flag=err)
+    step.run()
+    assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
+    assert codes_equal(d["k_cache"].cpu().numpy(), c.kc8_app)
+    rng = np.random.default_rng(w.seed)
+    rows = sorted({0, w.B - 1, int(np.argmax(w.context_lens))} | set(rng.integers(0, w.B, size=3).tolist()))
+    bt = np.ascontiguousarray(w.block_tables[rows])
+    cl = np.ascontiguousarray(w.context_lens[rows])
+    ref, ref_lse = oracle.decode_fp8(w.q[rows], c.kc8_app, c.vc8_app, c.ks, c.vs, bt, cl, w.scale)
+    assert_close(out_f64(step.out)[rows], ref, f"fp8 {name} ({step.plan.describe()})")
+    assert_lse_close(step.lse.cpu().numpy().astype(np.float64)[rows], ref_lse, f"fp8 {name}")
