@@ -337,7 +337,10 @@ int pkv_slot_mapping_multi(const int32_t *block_tables, int32_t max_blocks_per_s
    partitions of that many blocks and a log-sum-exp merge, with max_partitions as for
    pkv_decode_attn_splitk and a workspace of pkv_splitk_workspace_bytes(num_seqs * T, N, H,
    max_partitions) bytes (256-byte aligned).  Each CTA loads a K/V tile once for up to 32 of a
-   sequence's (token, head) rows of one KV head.  H in {64, 128}; G in {1, 2, 4, 8}. */
+   sequence's (token, head) rows of one KV head.  H in {64, 128}; G in {1, 2, 4, 8}.  With more
+   than 16 rows per CTA (min(T * G, 32) > 16) and H = 128 the contraction runs on the tcgen05
+   tensor cores (accumulators in tensor memory), otherwise on warp-level mma.sync; both compute
+   the same definition (results agree within rounding, not bit for bit). */
 int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
                           const int32_t *block_tables, int32_t max_blocks_per_seq,
                           const int32_t *context_lens, int32_t num_seqs, int32_t num_new,
@@ -345,6 +348,11 @@ int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_
                           pkv_cache_desc cache, int32_t partition_blocks, int32_t max_partitions,
                           void *workspace, size_t workspace_bytes, int32_t *err_flag,
                           pkv_stream_t stream);
+
+/* 1 if pkv_decode_attn_multi with these sizes runs its tcgen05 column kernel, 0 if the mma.sync
+   one (no GPU work; the answer assumes the half-major tensor-map layout, which the driver
+   accepted on every GB300 here -- if it were refused the call would fall back to mma.sync). */
+int pkv_multi_uses_tcgen05(int32_t num_new, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim);
 
 /*
  * ---- shared prefixes and copy-on-write ------------------------------------------------------

@@ -405,6 +405,7 @@ def pkv_lse_merge(part_out, part_lse, context_lens, partition_blocks: int, out, 
 _lib.pkv_slot_mapping_multi.argtypes = [_P, _I32, _P, _I32, _I32, _I32, _P, _P, _P]
 _lib.pkv_decode_attn_multi.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, ctypes.c_float, _P,
                                        _P, CacheDesc, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
+_lib.pkv_multi_uses_tcgen05.argtypes = [_I32, _I32, _I32, _I32]
 _lib.pkv_copy_blocks.argtypes = [_P, _P, _P, _I32, CacheDesc, _I32, _P, _P]
 _lib.pkv_prefix_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32, _I32]
 _lib.pkv_prefix_workspace_bytes.restype = ctypes.c_size_t
@@ -445,6 +446,11 @@ def pkv_decode_attn_multi(q, k_cache, v_cache, block_tables, context_lens, scale
                                       max_partitions, _ptr(workspace),
                                       0 if workspace is None else workspace.numel(), _ptr(err_flag),
                                       _stream(stream))
+
+
+def pkv_multi_uses_tcgen05(num_new: int, num_q_heads: int, num_kv_heads: int, head_dim: int) -> bool:
+    """Whether pkv_decode_attn_multi runs its tcgen05 column kernel for these sizes."""
+    return bool(_lib.pkv_multi_uses_tcgen05(num_new, num_q_heads, num_kv_heads, head_dim))
 
 
 def pkv_copy_blocks(k_cache, v_cache, src_dst, err_flag=None, stream=None) -> int:

@@ -12,8 +12,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libpagedkv.so")
-SOURCES = ["pkv_api.cu", "pkv_attn.cu", "pkv_attn_cols.cu", "pkv_cache_ops.cu"]
-HEADERS = ["pkv_device.cuh", "pkv_internal.h", "pkv_attn_common.cuh"]
+SOURCES = ["pkv_api.cu", "pkv_attn.cu", "pkv_attn_cols.cu", "pkv_attn_tc.cu", "pkv_cache_ops.cu"]
+HEADERS = ["pkv_device.cuh", "pkv_internal.h", "pkv_attn_common.cuh", "pkv_cols.cuh", "pkv_tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,6 +1,7 @@
 // pkv_api.cu - the C ABI of libpagedkv: host-side validation, TMA descriptor encoding and
 // kernel launches.  Every entry point validates its arguments before launching anything and
 // returns a pkv_status; device-detected errors go to the caller's err_flag.
+#include <algorithm>
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -78,8 +79,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 // 64-element (128-byte) rows so the 128-byte swizzle applies.  Half-major order
 // (dims h_lo, token, half, head, block) lands in shared memory as [half][token][64], which
 // makes the MMA fragment loads bank-conflict free; token-major order (h_lo, half, head,
-// token, block) is the fallback with monotone strides.
-CUresult encode_kv_map(CUtensorMap *map, const void *base, const pkv_cache_desc &d, int tok_major)
+// token, block) is the fallback with monotone strides.  With half_box the half-major box is one
+// 64-element half (16 x 128 bytes): the tcgen05 column kernel lands the two halves of a K tile in
+// separate regions, so consecutive tiles form one operand of uniform row stride.
+CUresult encode_kv_map(CUtensorMap *map, const void *base, const pkv_cache_desc &d, int tok_major,
+                       int half_box = 0)
 {
     const cuuint64_t H = (cuuint64_t)d.head_dim, K = (cuuint64_t)d.num_kv_heads;
     const cuuint64_t halves = H / 64;
@@ -91,7 +95,7 @@ CUresult encode_kv_map(CUtensorMap *map, const void *base, const pkv_cache_desc 
     if (!tok_major) {
         const cuuint64_t d5[5] = {64, 16, halves, K, (cuuint64_t)d.num_blocks};
         const cuuint64_t s4[4] = {tok_stride, half_stride, head_stride, blk_stride};
-        const cuuint32_t b5[5] = {64, 16, (cuuint32_t)halves, 1, 1};
+        const cuuint32_t b5[5] = {64, 16, half_box ? 1u : (cuuint32_t)halves, 1, 1};
         for (int i = 0; i < 5; ++i) dims[i] = d5[i], box[i] = b5[i];
         for (int i = 0; i < 4; ++i) strides[i] = s4[i];
     } else {
@@ -849,6 +853,15 @@ pkv::ColsParams cols_params_of(const AttnArgs &a, int tok_major)
 }
 
 constexpr int kColsPerCta = 32;  // query rows per CTA of the column-parallel kernel
+// Query rows per CTA from which the tcgen05 column kernel does the work.  Its time per 64-token
+// group is set by its MMA instructions (8 QK^T + 4 PV whatever the row count), the mma.sync
+// kernel's by its per-warp tile updates (one per 8 rows): with 32 rows the tensor cores are 1.5x
+// faster (Llama-3-8B batch of 64, 8 new tokens: 252 vs 377 us per step), with 16 rows the warps
+// are (222 vs 238 us).
+#ifndef PKV_COLS_TC_MIN_ROWS
+#define PKV_COLS_TC_MIN_ROWS 17
+#endif
+constexpr int kColsTcMinRows = PKV_COLS_TC_MIN_ROWS;
 
 int32_t prefix_parts_for(int32_t max_prefix_blocks, int32_t partition_blocks)
 {
@@ -948,12 +961,27 @@ PKV_EXPORT int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache,
     p.lse_out = lse_out;
     p.part_out = part_out;
     p.part_lse = part_lse;
-    cudaError_t e = pkv::launch_attn_cols(cache.head_dim, tk, tv, p, grid, stream);
+    // With more than 16 query rows per CTA the tensor-core (tcgen05) form of the column kernel does
+    // the contraction.
+    bool tc = std::min(num_new * G, kColsPerCta) >= kColsTcMinRows &&
+              pkv::cols_tc_supported(cache.head_dim, tok_major);
+    CUtensorMap tk_half;
+    if (tc) tc = encode_kv_map(&tk_half, k_cache, cache, 0, 1) == CUDA_SUCCESS;
+    cudaError_t e = tc ? pkv::launch_attn_cols_tc(cache.head_dim, tk_half, tv, p, grid, stream)
+                       : pkv::launch_attn_cols(cache.head_dim, tk, tv, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "multi-token attention launch");
     if (!split) return PKV_OK;
     // rows of one sequence: its T tokens x N heads, all with the sequence's context length
     return pkv_lse_merge(part_out, part_lse, context_lens, num_seqs, num_new * num_q_heads,
                          cache.head_dim, max_partitions, partition_blocks, out, lse_out, stream);
+}
+
+PKV_EXPORT int pkv_multi_uses_tcgen05(int32_t num_new, int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim)
+{
+    if (num_new <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
+    const int32_t G = num_q_heads / num_kv_heads;
+    return std::min(num_new * G, kColsPerCta) >= kColsTcMinRows && pkv::cols_tc_supported(head_dim, 0) ? 1 : 0;
 }
 
 PKV_EXPORT size_t pkv_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,

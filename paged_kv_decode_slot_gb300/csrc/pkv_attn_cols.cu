@@ -18,155 +18,9 @@
 // w % ng and reads the tiles i = w / ng (mod 4 / ng), so each stage is consumed by ng warps and its
 // empty barrier counts ng arrivals.  With ng < 4 the warps of one group split the tiles and their
 // states are merged in shared memory, as in attn_kernel.
-#include "pkv_attn_common.cuh"
+#include "pkv_cols.cuh"
 
 namespace pkv {
-
-constexpr int kColsPerWarp = 8;
-constexpr int kColsPerCta = 32;  // at most 4 groups of 8 rows; the API sizes its chunks by this
-static_assert(kConsumerWarps % 4 == 0, "column groups of a CTA must divide its consumer warps");
-
-enum ColsMode { kModeMulti = 0, kModePrefix = 1, kModeSuffix = 2 };
-
-// The work of one CTA (identical in every thread).
-struct ColsWork {
-    int mode;
-    int kvh;
-    int b;          // multi / suffix: the sequence; prefix: the group's first member
-    int ctx;        // multi: the sequence's context length
-    int vis;        // prefix / suffix: tokens every column sees
-    int col_base;   // first column of this CTA's chunk
-    int ncols;      // columns of this CTA (1..32)
-    int table_row;  // block-table row the blocks come from
-    int blk_begin, blk_end;
-    int data_end;   // tokens [0, data_end) of the block list hold data; later slots may be poison
-    int slot;       // partition slot of the outputs, -1: final outputs (multi, one pass)
-};
-
-// Shared leading blocks of group g, clamped to what the prefix pass covers and the table holds.
-__device__ __forceinline__ int prefix_blocks_of(const ColsParams &p, int g)
-{
-    return max(0, min(p.prefix_blocks[g], min(p.prefix_parts * p.prefix_part_blocks, p.max_nb)));
-}
-
-// Group of sequence b: the largest g with group_starts[g] <= b (b outside every group: -1).
-__device__ __forceinline__ int group_of(const ColsParams &p, int b)
-{
-    if (p.num_groups <= 0 || b < p.group_starts[0] || b >= p.group_starts[p.num_groups]) return -1;
-    int lo = 0, hi = p.num_groups - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.group_starts[mid] <= b) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
-
-// Decode CTA c of the grid into its work.  Returns false when the CTA has nothing to do.
-__device__ __forceinline__ bool cols_work(const ColsParams &p, int64_t c, ColsWork &w)
-{
-    const bool first_thread = threadIdx.x == 0;
-    w.kvh = (int)(c % p.K);
-    c /= p.K;
-    if (!p.group_starts) {
-        // several new tokens: partitions slowest, highest first (the longest work starts first)
-        const int64_t per_part = (int64_t)p.B * p.chunks;
-        const int part = p.parts - 1 - (int)(c / per_part);
-        c %= per_part;
-        const int chunk = (int)(c % p.chunks);
-        w.mode = kModeMulti;
-        w.b = (int)(c / p.chunks);
-        int ctx = p.context_lens[w.b];
-        if (ctx < 0 || ctx > p.max_nb * kBlockSize) {
-            if (first_thread && w.kvh == 0 && part == 0 && chunk == 0) set_flag(p.err_flag, PKV_FLAG_CTX_RANGE);
-            ctx = 0;
-        }
-        w.ctx = ctx;
-        w.vis = ctx;
-        w.col_base = chunk * kColsPerCta;
-        w.ncols = min(kColsPerCta, p.T * p.G - w.col_base);
-        w.table_row = w.b;
-        const int nb = (ctx + kBlockSize - 1) / kBlockSize;
-        w.blk_begin = part * p.part_blocks;
-        w.blk_end = min(nb, w.blk_begin + p.part_blocks);
-        w.data_end = ctx;
-        w.slot = p.split ? part : -1;
-        return w.ncols > 0;
-    }
-    if (c < p.prefix_ctas / p.K) {
-        // prefix pass: (group, chunk, prefix partition)
-        const int ppart = (int)(c % p.prefix_parts);
-        c /= p.prefix_parts;
-        const int chunk = (int)(c % p.chunks);
-        const int g = (int)(c / p.chunks);
-        const int gs_raw = p.group_starts[g], ge_raw = p.group_starts[g + 1];
-        const int gs = max(0, min(gs_raw, p.B)), ge = max(gs, min(ge_raw, p.B));
-        const int cols = (ge - gs) * p.G;
-        int pnb = p.prefix_blocks[g];
-        if (first_thread && w.kvh == 0 && ppart == 0 && chunk == p.chunks - 1 &&
-            (ge - gs > p.max_group || pnb > p.prefix_parts * p.prefix_part_blocks || pnb < 0 ||
-             gs != gs_raw || ge != ge_raw))
-            set_flag(p.err_flag, PKV_FLAG_GROUP_RANGE);
-        pnb = prefix_blocks_of(p, g);
-        w.mode = kModePrefix;
-        w.b = gs;
-        w.vis = pnb * kBlockSize;
-        w.col_base = chunk * kColsPerCta;
-        w.ncols = min(kColsPerCta, cols - w.col_base);
-        w.table_row = gs;
-        w.blk_begin = ppart * p.prefix_part_blocks;
-        w.blk_end = min(pnb, w.blk_begin + p.prefix_part_blocks);
-        w.data_end = w.vis;
-        w.slot = ppart;
-        return w.ncols > 0 && w.blk_begin < w.blk_end;
-    }
-    // suffix pass: (sequence, suffix partition)
-    c -= p.prefix_ctas / p.K;
-    const int sparts = (p.max_nb + p.part_blocks - 1) / p.part_blocks;
-    const int spart = (int)(c % sparts);
-    w.mode = kModeSuffix;
-    w.b = (int)(c / sparts);
-    int ctx = p.context_lens[w.b];
-    if (ctx < 0 || ctx > p.max_nb * kBlockSize) {
-        if (first_thread && w.kvh == 0 && spart == 0) set_flag(p.err_flag, PKV_FLAG_CTX_RANGE);
-        return false;
-    }
-    const int g = group_of(p, w.b);
-    const int pnb = g >= 0 ? prefix_blocks_of(p, g) : 0;
-    if (pnb * kBlockSize > ctx) {
-        if (first_thread && w.kvh == 0 && spart == 0) set_flag(p.err_flag, PKV_FLAG_GROUP_RANGE);
-        return false;
-    }
-    const int nb = (ctx + kBlockSize - 1) / kBlockSize;
-    w.vis = ctx;
-    w.col_base = 0;
-    w.ncols = p.G;
-    w.table_row = w.b;
-    w.blk_begin = pnb + spart * p.part_blocks;
-    w.blk_end = min(nb, w.blk_begin + p.part_blocks);
-    w.data_end = ctx;
-    // a row's partials are contiguous: its prefix partitions, then its suffix partitions
-    w.slot = (pnb + p.prefix_part_blocks - 1) / p.prefix_part_blocks + spart;
-    return w.blk_begin < w.blk_end;
-}
-
-// Row (of q, out and the partials) and visible-token limit of column j of the CTA.
-__device__ __forceinline__ void col_of(const ColsParams &p, const ColsWork &w, int j, int64_t &row,
-                                       int &vis)
-{
-    const int cj = w.col_base + j;
-    if (w.mode == kModeMulti) {
-        const int t = cj / p.G, g = cj - t * p.G;
-        row = ((int64_t)w.b * p.T + t) * p.N + (int64_t)w.kvh * p.G + g;
-        vis = w.ctx - p.T + t + 1;
-    } else if (w.mode == kModePrefix) {
-        const int m = cj / p.G, g = cj - m * p.G;
-        row = (int64_t)(w.b + m) * p.N + (int64_t)w.kvh * p.G + g;
-        vis = w.vis;
-    } else {
-        row = (int64_t)w.b * p.N + (int64_t)w.kvh * p.G + cj;
-        vis = w.vis;
-    }
-}
 
 // Q^T as the B operand for the warp's 8 columns: lane l holds row l/4 (qrow, or zeros).
 template <int H>

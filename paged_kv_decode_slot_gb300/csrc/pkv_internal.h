@@ -88,6 +88,11 @@ struct ColsParams {
 
 cudaError_t launch_attn_cols(int H, const CUtensorMap &tk, const CUtensorMap &tv, const ColsParams &p,
                              int64_t grid, cudaStream_t stream);
+// tcgen05 form of the same column kernel (H = 128, half-major tensor maps only; the K map's box
+// is one 64-element half of a tile, the V map's the whole tile).
+bool cols_tc_supported(int H, int tok_major);
+cudaError_t launch_attn_cols_tc(int H, const CUtensorMap &tk, const CUtensorMap &tv, const ColsParams &p,
+                                int64_t grid, cudaStream_t stream);
 cudaError_t launch_cascade_merge(const ColsParams &p, int H, __nv_bfloat16 *out, float *lse_out,
                                  cudaStream_t stream);
 cudaError_t launch_slot_mapping_multi(const int32_t *block_tables, int max_nb,

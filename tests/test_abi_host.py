@@ -184,3 +184,17 @@ def test_decode_step_host_validation(lib):
     assert f(*args(pb=2, P_=1)) == -2                   # 1 partition of 2 blocks < 4 blocks
     assert f(*args(pb=2, P_=2)) == -7                   # partitions need the workspace
     assert f(*args(B=0)) == 0
+
+
+def test_multi_kernel_choice():
+    """pkv_decode_attn_multi runs the tcgen05 column kernel from 17 query rows per CTA at H = 128
+    (rows = min(T * G, 32)), the mma.sync one below that and at H = 64; no GPU work."""
+    from paged_kv_decode_slot_gb300 import binding as B
+    assert B.pkv_multi_uses_tcgen05(8, 32, 8, 128)        # 32 rows
+    assert not B.pkv_multi_uses_tcgen05(4, 32, 8, 128)    # 16 rows
+    assert B.pkv_multi_uses_tcgen05(5, 32, 8, 128)        # 20 rows
+    assert B.pkv_multi_uses_tcgen05(3, 16, 2, 128)        # G = 8: 24 rows
+    assert B.pkv_multi_uses_tcgen05(64, 32, 8, 128)       # chunks of 32 rows
+    assert not B.pkv_multi_uses_tcgen05(8, 32, 8, 64)     # H = 64
+    assert not B.pkv_multi_uses_tcgen05(1, 64, 8, 128)    # one token, G = 8: 8 rows
+    assert not B.pkv_multi_uses_tcgen05(0, 32, 8, 128)

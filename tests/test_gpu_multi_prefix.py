@@ -1,7 +1,10 @@
 """Several new tokens per sequence, shared-prefix decode and copy-on-write, on the GPU.
 
 Multi-token decode (speculative verification): slots bit-exact, attention within the bf16
-tolerance of the oracle's masked attention, T = 1 bit-identical to the one-token kernel.
+tolerance of the oracle's masked attention, T = 1 bit-identical to the one-token kernel.  With
+more than 16 query rows per CTA (T * G, in chunks of 32) at H = 128 the tcgen05 column kernel runs:
+T = 8, 9 at G = 4 and T = 3 and up at G = 8 (rows 24 .. 72, partial chunks); fewer rows and H = 64
+run the mma.sync column kernel.
 Shared-prefix decode: within tolerance of the oracle's plain decode (the prefix pass plus suffix
 pass plus merge reach the same definition).  Block copies: bit-exact.
 """
@@ -81,7 +84,7 @@ def test_slot_mapping_multi_matches_oracle(pkv, oracle, T):
 
 
 @pytest.mark.parametrize("part_blocks", [0, 2, 5])
-@pytest.mark.parametrize("T", [1, 2, 4, 8])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 8, 9])
 @pytest.mark.parametrize("name,N,K,H,ctx", MULTI_CASES, ids=[c[0] for c in MULTI_CASES])
 def test_decode_attn_multi_matches_oracle(pkv, oracle, name, N, K, H, ctx, T, part_blocks):
     w = gen.make_workload(f"m_{name}", 80 + T, N, K, H, ctx)
@@ -296,3 +299,48 @@ def test_prefix_bounds_are_flagged(pkv, oracle):
     st, flag = pkv.pkv_read_err_flag(err)
     assert st == pkv.PKV_ERR_RANGE and flag & pkv.PKV_FLAG_GROUP_RANGE
     assert torch.all(out[0].float() == 0)
+
+
+@pytest.mark.parametrize("T", [8, 4])
+def test_multi_step_full_size_in_bench_plan(pkv, oracle, T):
+    """The multi-token step as the benchmark times it (MultiTokenStep with its default plan) on the
+    Llama-3-8B-shaped batch of 64: T = 8 and T = 4 new tokens (32 query rows per CTA: the tcgen05
+    column kernel; 16: the mma.sync one), sampled sequences against the oracle."""
+    from paged_kv_decode_slot_gb300.step import MultiTokenStep
+    w = gen.make_config("l3_8b_b64")
+    c = MultiCase(oracle, w, T, 200 + T)
+    kc, vc = bf16_dev(w.k_cache), bf16_dev(w.v_cache)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    step = MultiTokenStep(bf16_dev(c.q), bf16_dev(c.k_new), bf16_dev(c.v_new), kc, vc, i32_dev(w.block_tables),
+                          i32_dev(w.context_lens), w.scale, err_flag=err)
+    step.run()
+    assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
+    rng = np.random.default_rng(T)
+    sample = sorted({0, w.B - 1, int(np.argmax(w.context_lens))} | set(rng.integers(0, w.B, size=3).tolist()))
+    bt = np.ascontiguousarray(w.block_tables[sample])
+    cl = np.ascontiguousarray(w.context_lens[sample])
+    ref, ref_lse = oracle.decode_multi(c.q[sample], c.kc, c.vc, bt, cl, w.scale)
+    assert_close(out_f64(step.out[sample]), ref, f"multi step T={T} ({step.plan.describe()})")
+    assert_lse_close(step.lse[sample].cpu().numpy().astype(np.float64), ref_lse, f"multi step T={T}")
+
+
+def test_multi_skipped_block_is_flagged_and_masked(pkv, oracle):
+    """An out-of-range block id in one sequence's table (tcgen05 path, T = 8, G = 4): the range
+    flag is raised, the tile is skipped, and every other sequence still matches the oracle."""
+    w = gen.make_workload("m_badblk", 131, 16, 4, 128, [40, 90, 300, 17])
+    T = 8
+    c = MultiCase(oracle, w, T, 132)
+    bt = w.block_tables.copy()
+    bt[2, 3] = w.num_blocks + 5
+    out, lse = None, None
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q = bf16_dev(c.q)
+    out = torch.empty_like(q)
+    lse = torch.empty(w.B, T, w.N, dtype=torch.float32, device="cuda")
+    pkv.check(pkv.pkv_decode_attn_multi(q, bf16_dev(c.kc), bf16_dev(c.vc), i32_dev(bt), i32_dev(w.context_lens),
+                                        w.scale, out, lse, 0, 0, None, err))
+    code, flags = pkv.pkv_read_err_flag(err)
+    assert flags & pkv.PKV_FLAG_BLOCK_RANGE
+    ref, _ = c.reference(oracle)
+    keep = [0, 1, 3]
+    assert_close(out_f64(out)[keep], ref[keep], "multi with a skipped block, other sequences")
