@@ -71,9 +71,9 @@ class Oracle:
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_decode.restype = _D
-        lib.oracle_quantize_fp8.argtypes = [_P, _I64, _I32, _I32, _P, _P]
-        lib.oracle_append_fp8.argtypes = [_P, _P, _P, _P, _P, _I32, _P, _P, _I32, _I32]
-        lib.oracle_decode_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, _I32,
+        lib.oracle_quantize_fp8.argtypes = [_P, _I64, _I32, _I32, _P, _I32, _I32, _P]
+        lib.oracle_append_fp8.argtypes = [_P, _P, _P, _P, _I32, _I32, _P, _I32, _P, _P, _I32, _I32]
+        lib.oracle_decode_fp8.argtypes = [_P, _P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                           _I32, _D, _P, _P, ctypes.c_int]
         self.lib = lib
 
@@ -198,17 +198,21 @@ class Oracle:
     def e4m3_decode_table(self) -> np.ndarray:
         return np.array([self.lib.oracle_e4m3_decode(c) for c in range(256)], dtype=np.float64)
 
-    def quantize_fp8(self, src, scale) -> np.ndarray:
-        """e4m3 codes of a bf16 array [..., K, H] with per-KV-head scales [K]."""
+    def quantize_fp8(self, src, scale, bs=16) -> np.ndarray:
+        """e4m3 codes of a bf16 array [..., K, H] with per-KV-head scales [K], or of a pool
+        [num_blocks, bs, K, H] with per-(block, head) scales [num_blocks, K]."""
         x = np.ascontiguousarray(src, dtype=np.uint16)
         sc = np.ascontiguousarray(scale, dtype=np.float32)
         K, H = x.shape[-2], x.shape[-1]
         rows = x.size // (K * H)
+        stride = _scale_stride(sc, K)
+        if stride:
+            assert rows == sc.shape[0] * bs, "per-block scales need the whole pool"
         out = np.empty(x.shape, dtype=np.uint8)
-        self.lib.oracle_quantize_fp8(_ptr(x), rows, K, H, _ptr(sc), _ptr(out))
+        self.lib.oracle_quantize_fp8(_ptr(x), rows, K, H, _ptr(sc), stride, bs, _ptr(out))
         return out
 
-    def append_fp8(self, k_new, v_new, k_scale, v_scale, slots, k_cache8, v_cache8):
+    def append_fp8(self, k_new, v_new, k_scale, v_scale, slots, k_cache8, v_cache8, bs=16):
         assert k_cache8.flags.c_contiguous and v_cache8.flags.c_contiguous
         kn = np.ascontiguousarray(k_new, dtype=np.uint16)
         vn = np.ascontiguousarray(v_new, dtype=np.uint16)
@@ -216,7 +220,9 @@ class Oracle:
         vs = np.ascontiguousarray(v_scale, dtype=np.float32)
         sl = np.ascontiguousarray(slots, dtype=np.int64)
         K, H = kn.shape[1], kn.shape[2]
-        self.lib.oracle_append_fp8(_ptr(kn), _ptr(vn), _ptr(ks), _ptr(vs), _ptr(sl), sl.shape[0],
+        stride = _scale_stride(ks, K)
+        assert _scale_stride(vs, K) == stride
+        self.lib.oracle_append_fp8(_ptr(kn), _ptr(vn), _ptr(ks), _ptr(vs), stride, bs, _ptr(sl), sl.shape[0],
                                    _ptr(k_cache8), _ptr(v_cache8), K, H)
         return k_cache8, v_cache8
 
@@ -231,12 +237,23 @@ class Oracle:
         cl = np.ascontiguousarray(context_lens, dtype=np.int32)
         B, N, H = q.shape
         K = kc.shape[2]
+        stride = _scale_stride(ks, K)
+        assert _scale_stride(vs, K) == stride
         out = np.empty((B, N, H), dtype=np.float64)
         lse = np.empty((B, N), dtype=np.float64)
-        self.lib.oracle_decode_fp8(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
+        self.lib.oracle_decode_fp8(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), stride, _ptr(bt),
                                    bt.shape[1], _ptr(cl), B, N, K, H, bs, float(scale), _ptr(out),
                                    _ptr(lse), threads)
         return out, lse
+
+
+def _scale_stride(scale: np.ndarray, K: int) -> int:
+    """0 for per-KV-head scales [K]; K for per-(block, head) scales [num_blocks, K]."""
+    if scale.ndim == 1:
+        assert scale.shape[0] == K
+        return 0
+    assert scale.ndim == 2 and scale.shape[1] == K
+    return K
 
 
 _default = None

@@ -145,6 +145,7 @@ typedef struct {
     double *out, *lse;
     int nthreads, tid;
     int32_t T; /* query tokens per sequence (0 means 1) */
+    int32_t scale_block_stride; /* e4m3: 0 = one scale per KV head, else per (block, head) */
 } decode_job;
 
 /* One (sequence, KV head) unit: gather its K/V rows through the block table into
@@ -164,9 +165,10 @@ static void decode_unit(const decode_job *j, int32_t b, int32_t kvh)
         int64_t slot = physical_slot(j->block_tables, j->max_nb, b, t, j->bs);
         const size_t row = ((size_t)slot * j->K + kvh) * H;
         for (int32_t h = 0; h < H; ++h) {
-            if (j->k8) { /* dequantize: decode(code) * per-head scale */
-                keys[t * H + h] = oracle_e4m3_decode(j->k8[row + h]) * (double)j->k_scale[kvh];
-                values[t * H + h] = oracle_e4m3_decode(j->v8[row + h]) * (double)j->v_scale[kvh];
+            if (j->k8) { /* dequantize: decode(code) * the scale of (physical block, head) */
+                const size_t si = (j->scale_block_stride ? (size_t)(slot / j->bs) * (size_t)j->scale_block_stride : 0) + kvh;
+                keys[t * H + h] = oracle_e4m3_decode(j->k8[row + h]) * (double)j->k_scale[si];
+                values[t * H + h] = oracle_e4m3_decode(j->v8[row + h]) * (double)j->v_scale[si];
             } else {
                 keys[t * H + h] = bf16_to_double(j->k_cache[row + h]);
                 values[t * H + h] = bf16_to_double(j->v_cache[row + h]);
@@ -358,35 +360,43 @@ uint8_t oracle_e4m3_encode(float x)
 }
 
 void oracle_quantize_fp8(const uint16_t *src, int64_t rows, int32_t K, int32_t H,
-                         const float *scale, uint8_t *dst)
+                         const float *scale, int32_t scale_block_stride, int32_t bs, uint8_t *dst)
 {
-    for (int64_t r = 0; r < rows; ++r)
+    for (int64_t r = 0; r < rows; ++r) {
+        /* row r of a pool belongs to physical block r / bs */
+        const float *sc = scale + (scale_block_stride ? (size_t)(r / bs) * (size_t)scale_block_stride : 0);
         for (int32_t kvh = 0; kvh < K; ++kvh)
             for (int32_t h = 0; h < H; ++h) {
                 size_t i = ((size_t)r * K + kvh) * H + h;
                 float x = (float)bf16_to_double(src[i]);
-                dst[i] = oracle_e4m3_encode(x / scale[kvh]);
+                dst[i] = oracle_e4m3_encode(x / sc[kvh]);
             }
+    }
 }
 
 void oracle_append_fp8(const uint16_t *k_new, const uint16_t *v_new, const float *k_scale,
-                       const float *v_scale, const int64_t *slots, int32_t T, uint8_t *k_cache,
-                       uint8_t *v_cache, int32_t K, int32_t H)
+                       const float *v_scale, int32_t scale_block_stride, int32_t bs,
+                       const int64_t *slots, int32_t T, uint8_t *k_cache, uint8_t *v_cache, int32_t K,
+                       int32_t H)
 {
     size_t row = (size_t)K * (size_t)H;
     for (int32_t i = 0; i < T; ++i) {
         if (slots[i] < 0) continue;
-        oracle_quantize_fp8(k_new + (size_t)i * row, 1, K, H, k_scale, k_cache + (size_t)slots[i] * row);
-        oracle_quantize_fp8(v_new + (size_t)i * row, 1, K, H, v_scale, v_cache + (size_t)slots[i] * row);
+        /* the scales of the physical block the slot lies in */
+        const size_t off = scale_block_stride ? (size_t)(slots[i] / bs) * (size_t)scale_block_stride : 0;
+        oracle_quantize_fp8(k_new + (size_t)i * row, 1, K, H, k_scale + off, 0, 1, k_cache + (size_t)slots[i] * row);
+        oracle_quantize_fp8(v_new + (size_t)i * row, 1, K, H, v_scale + off, 0, 1, v_cache + (size_t)slots[i] * row);
     }
 }
 
 void oracle_decode_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
-                       const float *k_scale, const float *v_scale, const int32_t *block_tables,
-                       int32_t max_nb, const int32_t *context_lens, int32_t B, int32_t N, int32_t K,
-                       int32_t H, int32_t bs, double scale, double *out, double *lse, int nthreads)
+                       const float *k_scale, const float *v_scale, int32_t scale_block_stride,
+                       const int32_t *block_tables, int32_t max_nb, const int32_t *context_lens,
+                       int32_t B, int32_t N, int32_t K, int32_t H, int32_t bs, double scale, double *out,
+                       double *lse, int nthreads)
 {
     decode_job j = {q, 0, 0, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, max_nb,
                     B, N, K, H, bs, scale, 0, 1, out, lse, nthreads, 0};
+    j.scale_block_stride = scale_block_stride;
     run_decode(j);
 }

@@ -82,25 +82,31 @@ void oracle_copy_blocks(uint8_t *k_cache, uint8_t *v_cache, const int32_t *src_d
    subnormals m * 2^-9; S.1111.111 is NaN; no infinities; largest finite 448.
    Quantization of a value x of KV head kvh: code = e4m3(x / scale[kvh]) with the division
    in float (round to nearest) and round-to-nearest-even onto the e4m3 grid, saturating at
-   +-448; dequantization: decode(code) * scale[kvh]. */
+   +-448; dequantization: decode(code) * scale[kvh].  With scale_block_stride > 0 the scales
+   are per (physical block, KV head): value x of a row in block blk uses
+   scale[blk * scale_block_stride + kvh] instead (scale_block_stride = K for [num_blocks][K]). */
 uint8_t oracle_e4m3_encode(float x);
 double oracle_e4m3_decode(uint8_t code);
 
-/* dst[r][kvh][h] = e4m3(src[r][kvh][h] / scale[kvh]) for rows [rows][K][H] (bf16 in). */
+/* dst[r][kvh][h] = e4m3(src[r][kvh][h] / scale[kvh]) for rows [rows][K][H] (bf16 in); with
+   scale_block_stride > 0, row r lies in block r / bs and uses that block's scales. */
 void oracle_quantize_fp8(const uint16_t *src, int64_t rows, int32_t K, int32_t H,
-                         const float *scale, uint8_t *dst);
+                         const float *scale, int32_t scale_block_stride, int32_t bs, uint8_t *dst);
 
-/* append: quantize k_new/v_new rows [T][K][H] into their slots; negative slots skipped. */
+/* append: quantize k_new/v_new rows [T][K][H] into their slots (with the scales of the block
+   a slot lies in, slot / bs); negative slots skipped. */
 void oracle_append_fp8(const uint16_t *k_new, const uint16_t *v_new, const float *k_scale,
-                       const float *v_scale, const int64_t *slots, int32_t T, uint8_t *k_cache,
-                       uint8_t *v_cache, int32_t K, int32_t H);
+                       const float *v_scale, int32_t scale_block_stride, int32_t bs,
+                       const int64_t *slots, int32_t T, uint8_t *k_cache, uint8_t *v_cache, int32_t K,
+                       int32_t H);
 
 /* decode attention over an e4m3 cache [num_blocks][bs][K][H] dequantized with the per-head
-   scales; same outputs as oracle_decode. */
+   (or per (block, head)) scales; same outputs as oracle_decode. */
 void oracle_decode_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
-                       const float *k_scale, const float *v_scale, const int32_t *block_tables,
-                       int32_t max_nb, const int32_t *context_lens, int32_t B, int32_t N, int32_t K,
-                       int32_t H, int32_t bs, double scale, double *out, double *lse, int nthreads);
+                       const float *k_scale, const float *v_scale, int32_t scale_block_stride,
+                       const int32_t *block_tables, int32_t max_nb, const int32_t *context_lens,
+                       int32_t B, int32_t N, int32_t K, int32_t H, int32_t bs, double scale, double *out,
+                       double *lse, int nthreads);
 
 #ifdef __cplusplus
 }

@@ -332,6 +332,47 @@ def check_fp8_attention_is_dequantized_attention(orc):
         assert np.all(np.abs(out[0, n] - v0[kvh]) <= bound)
 
 
+def check_fp8_block_scales(orc):
+    """Per-(physical block, KV head) scales [num_blocks, K]: (1) quantizing a pool equals
+    quantizing each block with the per-head scales of that block; (2) attention equals SDPA on
+    the values dequantized with the scales of each token's physical block (the tables are
+    permuted, so a logical block index would pick other scales); (3) an append quantizes the new
+    row with the scales of the block its slot lies in."""
+    q, ks, vs = random_case(97, 8, 2, 128, [5, 17, 70])
+    kc, vc, tables, ctx = paged_from_contiguous(ks, vs, 12)
+    nblk = kc.shape[0]
+    rng = np.random.default_rng(97)
+    k_sc = rng.uniform(0.004, 0.02, size=(nblk, 2)).astype(np.float32)
+    v_sc = rng.uniform(0.004, 0.02, size=(nblk, 2)).astype(np.float32)
+    kc8 = orc.quantize_fp8(kc, k_sc)
+    vc8 = orc.quantize_fp8(vc, v_sc)
+    for blk in range(nblk):
+        assert np.array_equal(kc8[blk], orc.quantize_fp8(kc[blk], k_sc[blk]))
+        assert np.array_equal(vc8[blk], orc.quantize_fp8(vc[blk], v_sc[blk]))
+    out, lse = orc.decode_fp8(q, kc8, vc8, k_sc, v_sc, tables, ctx, 1 / math.sqrt(128))
+    t = orc.e4m3_decode_table()
+    import torch
+    for b in range(3):
+        n = int(ctx[b])
+        blocks = tables[b, np.arange(n) // BS]
+        offs = np.arange(n) % BS
+        kd = t[kc8[blocks, offs]] * k_sc[blocks][:, :, None].astype(np.float64)   # [n, K, H]
+        vd = t[vc8[blocks, offs]] * v_sc[blocks][:, :, None].astype(np.float64)
+        qt = torch.from_numpy(to_f64(q[b])).reshape(1, 8, 1, 128)
+        kt = torch.from_numpy(kd).permute(1, 0, 2).unsqueeze(0).repeat_interleave(4, dim=1)
+        vt = torch.from_numpy(vd).permute(1, 0, 2).unsqueeze(0).repeat_interleave(4, dim=1)
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=1 / math.sqrt(128))
+        assert np.max(np.abs(out[b] - ref.reshape(8, 128).numpy())) < 1e-12
+    kn = gen.normal_bf16(97, 400, (3, 2, 128))
+    vn = gen.normal_bf16(97, 401, (3, 2, 128))
+    slots = np.array([tables[0, 0] * BS + 5, tables[2, 4] * BS + 15, tables[1, 1] * BS + 2], dtype=np.int64)
+    orc.append_fp8(kn, vn, k_sc, v_sc, slots, kc8, vc8)
+    for i, s_ in enumerate(slots.tolist()):
+        blk = s_ // BS
+        assert np.array_equal(kc8[blk, s_ % BS], orc.quantize_fp8(kn[i:i + 1], k_sc[blk])[0])
+        assert np.array_equal(vc8[blk, s_ % BS], orc.quantize_fp8(vn[i:i + 1], v_sc[blk])[0])
+
+
 def check_fp8_append_roundtrip(orc):
     w = gen.make_config("tiny")
     k_scale = np.array([0.01, 0.02], dtype=np.float32)
@@ -440,6 +481,6 @@ ALL_CHECKS = [check_kv_bytes_golden, check_paged_equals_contiguous,
               check_partitions_merge_to_unsplit, check_ctx0, check_slot_mapping,
               check_append_gather_roundtrip, check_gather_inverts_scatter,
               check_e4m3_decode_table, check_e4m3_encode_nearest_even,
-              check_fp8_attention_is_dequantized_attention, check_fp8_append_roundtrip,
+              check_fp8_attention_is_dequantized_attention, check_fp8_block_scales, check_fp8_append_roundtrip,
               check_multi_query_equals_masked_sdpa, check_multi_query_is_a_sequence_of_decode_steps,
               check_slot_mapping_multi, check_copy_blocks]

@@ -41,9 +41,15 @@ MUTANTS = {
     "e4m3_round_half_up": [("double r = nearbyint(a / quantum);", "double r = floor(a / quantum + 0.5);")],
     "e4m3_no_saturation": [("if (a >= 448.0) return (uint8_t)(sign | 0x7E);", "if (a >= 480.0) return (uint8_t)(sign | 0x7E);")],
     "e4m3_subnormal_quantum": [("const double quantum = ldexp(1.0, e - 3);", "const double quantum = ldexp(1.0, e - 3 + (e == -6));")],
-    "fp8_scale_multiplies": [("dst[i] = oracle_e4m3_encode(x / scale[kvh]);", "dst[i] = oracle_e4m3_encode(x * scale[kvh]);")],
-    "fp8_v_scale_for_k": [("keys[t * H + h] = oracle_e4m3_decode(j->k8[row + h]) * (double)j->k_scale[kvh];",
-                           "keys[t * H + h] = oracle_e4m3_decode(j->k8[row + h]) * (double)j->v_scale[kvh];")],
+    "fp8_scale_multiplies": [("dst[i] = oracle_e4m3_encode(x / sc[kvh]);", "dst[i] = oracle_e4m3_encode(x * sc[kvh]);")],
+    "fp8_v_scale_for_k": [("keys[t * H + h] = oracle_e4m3_decode(j->k8[row + h]) * (double)j->k_scale[si];",
+                           "keys[t * H + h] = oracle_e4m3_decode(j->k8[row + h]) * (double)j->v_scale[si];")],
+    "fp8_block_scale_of_logical_block": [("(size_t)(slot / j->bs) * (size_t)j->scale_block_stride",
+                                          "(size_t)(t / j->bs) * (size_t)j->scale_block_stride")],
+    "fp8_quantize_ignores_block": [("scale + (scale_block_stride ? (size_t)(r / bs) * (size_t)scale_block_stride : 0)",
+                                    "scale")],
+    "fp8_append_scale_of_wrong_block": [("(size_t)(slots[i] / bs) * (size_t)scale_block_stride",
+                                         "(size_t)(slots[i] % bs) * (size_t)scale_block_stride")],
     "multi_mask_top_left": [("int64_t visible = ctx - T + t + 1;", "int64_t visible = t + 1;")],
     "multi_mask_off_by_one": [("int64_t visible = ctx - T + t + 1;", "int64_t visible = ctx - T + t;")],
     "multi_query_row": [("const uint16_t *qrow = j->q + bn * H;",
