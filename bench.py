@@ -89,17 +89,19 @@ def recorded_traffic(config: str):
     return None
 
 
-def step_bytes(w, kv: str = "bf16", tokens: int = 1) -> dict:
+def step_bytes(w, kv: str = "bf16", tokens: int = 1, fp8_scales: str = "head") -> dict:
     """Algorithmic bytes of one step (what the method must move, padding not counted).
 
     With an e4m3 cache the K/V history is one byte per element (half the bf16 bytes), the
     append reads the new bf16 rows and writes one-byte codes, and attention also reads the
-    2 x K per-head scales.  With T new tokens per sequence (verification) q, out and the
-    append are T times larger and the block tables are read once per 32-row chunk."""
-    tables = int(sum(-(-int(c) // 16) for c in w.context_lens)) * 4
+    scales: 2 x K per-head ones, or with per-(block, head) scales the K and V scale of every
+    (block, KV head) tile it reads.  With T new tokens per sequence (verification) q, out and
+    the append are T times larger and the block tables are read once per 32-row chunk."""
+    blocks = int(sum(-(-int(c) // 16) for c in w.context_lens))
+    tables = blocks * 4
     meta = w.B * 4 + tables + w.B * 8 * 2          # context lens, table entries, slots (write+read)
     if kv == "fp8":
-        scales = 2 * w.K * 4
+        scales = 2 * w.K * 4 if fp8_scales == "head" else blocks * w.K * 2 * 4
         attn = w.kv_bytes() // 2 + w.qo_bytes() + scales
         attn_unique = w.unique_kv_bytes() // 2 + w.qo_bytes() + scales
         append = w.append_bytes() * 3 // 4
@@ -267,7 +269,7 @@ def traffic_key(args) -> str:
     timed kernel (a recorded figure is reported only for exactly that kernel and workload)."""
     key = args.config
     if args.kv != "bf16":
-        key += "+" + args.kv
+        key += "+" + args.kv + ("+bscale" if args.fp8_scales == "block" else "")
     if args.tokens > 1:
         key += f"+T{args.tokens}"
     if args.attn != "auto":
@@ -367,9 +369,11 @@ def run_ours(args):
     elif args.kv == "fp8":
         if args.unfused or plan.mode == "balanced":
             raise SystemExit("--kv fp8 runs the fused single-pass or split step only")
-        # per-KV-head scales from the cache's own absolute maxima (NaN tail poison ignored)
+        # scales from the cache's own absolute maxima (NaN tail poison ignored): per KV head, or
+        # per (physical block, KV head)
         def head_scale(c):
-            amax = torch.nan_to_num(c.float(), nan=0.0).abs().amax(dim=(0, 1, 3))
+            dims = (0, 1, 3) if args.fp8_scales == "head" else (1, 3)
+            amax = torch.nan_to_num(c.float(), nan=0.0).abs().amax(dim=dims)
             return (torch.where(amax > 0, amax, torch.ones_like(amax)) / 448.0).contiguous()
         ks, vs = head_scale(kc), head_scale(vc)
         kc8 = torch.empty(kc.shape, dtype=torch.uint8, device=dev)
@@ -395,7 +399,7 @@ def run_ours(args):
         # timed step starts with an L2 that holds neither its inputs nor write-back debt.
         flush_w.add_(1.0)
         torch.sum(flush_r, dim=0, keepdim=True, out=flush_sink)
-    nbytes = step_bytes(w, args.kv, args.tokens)
+    nbytes = step_bytes(w, args.kv, args.tokens, args.fp8_scales)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -532,7 +536,8 @@ def run_ours(args):
     if args.attn == "prefix":
         line["config"]["prefix_groups"] = "one group of the whole batch sharing its full prefix blocks"
     if args.kv == "fp8":
-        line["config"]["kv_cache"] = "e4m3, per-KV-head scales (amax / 448)"
+        line["config"]["kv_cache"] = ("e4m3, per-KV-head scales (amax / 448)" if args.fp8_scales == "head"
+                                      else "e4m3, per-(block, KV head) scales (amax / 448)")
         line["kv_gbs"] = w.kv_bytes() / 2 / (mean_attn * 1e-3) / 1e9
         line["kv_gbs_bf16_equivalent"] = w.kv_bytes() / (mean_attn * 1e-3) / 1e9
     if w.unique_tokens is not None:
@@ -558,6 +563,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv", choices=("bf16", "fp8"), default="bf16",
                     help="KV cache element type (fp8 = e4m3 codes with per-KV-head scales)")
+    ap.add_argument("--fp8-scales", choices=("head", "block"), default="head",
+                    help="with --kv fp8: one scale per KV head, or one per (physical block, KV head)")
     ap.add_argument("--tokens", type=int, default=1,
                     help="new tokens per sequence (> 1: speculative verification of that many)")
     ap.add_argument("--attn", choices=("auto", "prefix"), default="auto",

@@ -182,29 +182,39 @@ int pkv_decode_step(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_
  * Cache quantization halves the bytes a decode step reads ("Week 11. Inference", Step 2:
  * storing K and V in 8 bits instead of 16; "Optimización de la inferencia", exercise on KV
  * cache quantization).  Pools hold e4m3 codes [num_blocks][16][K][H] (1 byte each; H = 128);
- * each KV head has one scale for K and one for V (float arrays [K], set when the cache is
- * calibrated), value = decode(code) * scale.  Quantizing x: code = e4m3(x / scale) with the
- * division rounded to nearest in fp32 and round-to-nearest-even onto the e4m3 grid,
- * saturating at +-448 (e4m3: 4 exponent bits with bias 7, 3 mantissa bits, no infinities).
- * Attention reads the codes, widens them exactly to f16 for the tensor-core contractions and
- * applies the scales (K's to the logits, V's to the output); results otherwise as pkv_decode_attn.
+ * value = decode(code) * scale.  Scales (positive, finite floats; one array for K, one for V)
+ * come in one of two granularities, chosen by scale_block_stride:
+ *   0  one scale per KV head, float [K] (calibrated once for the whole pool);
+ *   K  one scale per (physical block, KV head), float [num_blocks][K]: element (blk, kvh) scales
+ *      every value of that head in that block (the block's 16 tokens).
+ * Quantizing x: code = e4m3(x / scale) with the division rounded to nearest in fp32 and
+ * round-to-nearest-even onto the e4m3 grid, saturating at +-448 (e4m3: 4 exponent bits with
+ * bias 7, 3 mantissa bits, no infinities).  Attention reads the codes, widens them exactly to f16
+ * for the tensor-core contractions and applies the scales (K's to the logits, V's to the weights
+ * of each block relative to one V scale per partition, which multiplies the output); results
+ * otherwise as pkv_decode_attn.  The per-block scales of the blocks a step writes into must be
+ * set before the step (an append quantizes with them).
  */
 
-/* dst[r][kvh][h] = e4m3(src[r][kvh][h] / scale[kvh]) for src bf16 [rows][K][H] (16-byte aligned). */
+/* dst[r][kvh][h] = e4m3(src[r][kvh][h] / scale[kvh]) for src bf16 [rows][K][H] (16-byte aligned);
+   with scale_block_stride = K, src is a pool (rows a multiple of 16, row r in block r / 16) and
+   the scale is scale[(r / 16) * K + kvh]. */
 int pkv_quantize_fp8(const pkv_bf16 *src, int64_t rows, int32_t num_kv_heads, int32_t head_dim,
-                     const float *scale, uint8_t *dst, pkv_stream_t stream);
+                     const float *scale, int32_t scale_block_stride, uint8_t *dst, pkv_stream_t stream);
 
-/* pkv_append for an e4m3 pool: each token's K/V row quantized into its slot. */
+/* pkv_append for an e4m3 pool: each token's K/V row quantized into its slot (with the scales of
+   the slot's block, slot / 16, when scale_block_stride = K). */
 int pkv_append_fp8(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const float *k_scale,
-                   const float *v_scale, const int64_t *slot_mapping, int32_t num_tokens,
-                   uint8_t *k_cache, uint8_t *v_cache, pkv_cache_desc cache, int32_t *err_flag,
-                   pkv_stream_t stream);
+                   const float *v_scale, int32_t scale_block_stride, const int64_t *slot_mapping,
+                   int32_t num_tokens, uint8_t *k_cache, uint8_t *v_cache, pkv_cache_desc cache,
+                   int32_t *err_flag, pkv_stream_t stream);
 
 /* Decode attention over e4m3 pools: partition_blocks 0 = single pass (workspace unused),
    > 0 = fixed partitions + log-sum-exp merge with the workspace of pkv_decode_attn_splitk.
    q 8-byte aligned. */
 int pkv_decode_attn_fp8(const pkv_bf16 *q, const uint8_t *k_cache, const uint8_t *v_cache,
-                        const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                        const float *k_scale, const float *v_scale, int32_t scale_block_stride,
+                        const int32_t *block_tables,
                         int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
                         int32_t num_q_heads, float scale, pkv_bf16 *out, float *lse_out,
                         pkv_cache_desc cache, int32_t partition_blocks, int32_t max_partitions,
@@ -215,7 +225,7 @@ int pkv_decode_attn_fp8(const pkv_bf16 *q, const uint8_t *k_cache, const uint8_t
    the same launch; bit-identical to pkv_append_fp8 followed by pkv_decode_attn_fp8. */
 int pkv_decode_step_fp8(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
                         uint8_t *k_cache, uint8_t *v_cache, const float *k_scale,
-                        const float *v_scale, const int32_t *block_tables,
+                        const float *v_scale, int32_t scale_block_stride, const int32_t *block_tables,
                         int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
                         int32_t num_q_heads, float scale, pkv_bf16 *out, float *lse_out,
                         int64_t *slot_mapping_out, pkv_cache_desc cache, int32_t partition_blocks,

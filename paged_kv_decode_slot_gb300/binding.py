@@ -279,11 +279,11 @@ def pkv_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_len
                                 _stream(stream))
 
 
-_lib.pkv_quantize_fp8.argtypes = [_P, _I64, _I32, _I32, _P, _P, _P]
-_lib.pkv_append_fp8.argtypes = [_P, _P, _P, _P, _P, _I32, _P, _P, CacheDesc, _P, _P]
-_lib.pkv_decode_attn_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P,
+_lib.pkv_quantize_fp8.argtypes = [_P, _I64, _I32, _I32, _P, _I32, _P, _P]
+_lib.pkv_append_fp8.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _P, _P, CacheDesc, _P, _P]
+_lib.pkv_decode_attn_fp8.argtypes = [_P, _P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P,
                                      _P, CacheDesc, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
-_lib.pkv_decode_step_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
+_lib.pkv_decode_step_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32, _P, _I32, _I32,
                                      ctypes.c_float, _P, _P, _P, CacheDesc, _I32, _I32, _P,
                                      ctypes.c_size_t, _P, _P]
 
@@ -292,8 +292,23 @@ def _need_fp8_pool(t, name):
     _need(t, torch.uint8, 4, name)
 
 
+def scale_block_stride(k_scale, v_scale, num_kv_heads: int) -> int:
+    """0 for per-KV-head scales [K]; K for per-(physical block, KV head) scales [num_blocks, K]."""
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous float32 CUDA tensor")
+    if k_scale.shape != v_scale.shape:
+        raise ValueError("k_scale and v_scale shapes differ")
+    if k_scale.dim() == 1 and k_scale.shape[0] == num_kv_heads:
+        return 0
+    if k_scale.dim() == 2 and k_scale.shape[1] == num_kv_heads:
+        return num_kv_heads
+    raise ValueError("scales must be [K] (per KV head) or [num_blocks, K] (per block and KV head)")
+
+
 def pkv_quantize_fp8(src, scale, dst, stream=None) -> int:
-    """e4m3 codes of a bf16 tensor [..., K, H] with per-KV-head scales [K] into dst (uint8)."""
+    """e4m3 codes of a bf16 tensor [..., K, H] into dst (uint8) with per-KV-head scales [K], or of
+    a pool [num_blocks, 16, K, H] with per-(block, head) scales [num_blocks, K]."""
     if src.dtype != torch.bfloat16 or dst.dtype != torch.uint8 or scale.dtype != torch.float32:
         raise TypeError("src bf16, scale float32, dst uint8")
     for t, n in ((src, "src"), (scale, "scale"), (dst, "dst")):
@@ -302,7 +317,10 @@ def pkv_quantize_fp8(src, scale, dst, stream=None) -> int:
     if src.shape != dst.shape:
         raise ValueError("src and dst shapes differ")
     K, H = src.shape[-2], src.shape[-1]
-    return _lib.pkv_quantize_fp8(_ptr(src), src.numel() // (K * H), K, H, _ptr(scale), _ptr(dst),
+    stride = scale_block_stride(scale, scale, K)
+    if stride and (src.dim() != 4 or src.shape[0] != scale.shape[0]):
+        raise ValueError("per-block scales quantize a whole pool [num_blocks, 16, K, H]")
+    return _lib.pkv_quantize_fp8(_ptr(src), src.numel() // (K * H), K, H, _ptr(scale), stride, _ptr(dst),
                                  _stream(stream))
 
 
@@ -310,40 +328,38 @@ def pkv_append_fp8(k_new, v_new, k_scale, v_scale, slot_mapping, k_cache, v_cach
                    stream=None) -> int:
     _need(k_new, torch.bfloat16, 3, "k_new")
     _need(v_new, torch.bfloat16, 3, "v_new")
-    _need(k_scale, torch.float32, 1, "k_scale")
-    _need(v_scale, torch.float32, 1, "v_scale")
     _need(slot_mapping, torch.int64, 1, "slot_mapping")
     _need_fp8_pool(k_cache, "k_cache")
     _need_fp8_pool(v_cache, "v_cache")
     _opt(err_flag, torch.int32, 1, "err_flag")
-    return _lib.pkv_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping),
-                               k_new.shape[0], _ptr(k_cache), _ptr(v_cache), cache_desc(k_cache),
-                               _ptr(err_flag), _stream(stream))
+    stride = scale_block_stride(k_scale, v_scale, k_cache.shape[2])
+    return _lib.pkv_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_scale), _ptr(v_scale), stride,
+                               _ptr(slot_mapping), k_new.shape[0], _ptr(k_cache), _ptr(v_cache),
+                               cache_desc(k_cache), _ptr(err_flag), _stream(stream))
 
 
 def _fp8_common(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens):
     _need(q, torch.bfloat16, 3, "q")
     _need_fp8_pool(k_cache, "k_cache")
     _need_fp8_pool(v_cache, "v_cache")
-    _need(k_scale, torch.float32, 1, "k_scale")
-    _need(v_scale, torch.float32, 1, "v_scale")
     _need(block_tables, torch.int32, 2, "block_tables")
     _need(context_lens, torch.int32, 1, "context_lens")
     if v_cache.shape != k_cache.shape or q.shape[2] != k_cache.shape[3]:
         raise ValueError("pool shapes / head_dim differ")
+    return scale_block_stride(k_scale, v_scale, k_cache.shape[2])
 
 
 def pkv_decode_attn_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale: float,
                         out, lse_out=None, partition_blocks: int = 0, max_partitions: int = 0,
                         workspace=None, err_flag=None, stream=None) -> int:
-    _fp8_common(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens)
+    stride = _fp8_common(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens)
     _need(out, torch.bfloat16, 3, "out")
     _opt(lse_out, torch.float32, 2, "lse_out")
     _opt(workspace, torch.uint8, 1, "workspace")
     _opt(err_flag, torch.int32, 1, "err_flag")
     B, N, _ = q.shape
     return _lib.pkv_decode_attn_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                                    _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, N,
+                                    stride, _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, N,
                                     float(scale), _ptr(out), _ptr(lse_out), cache_desc(k_cache),
                                     partition_blocks, max_partitions, _ptr(workspace),
                                     0 if workspace is None else workspace.numel(), _ptr(err_flag),
@@ -353,7 +369,7 @@ def pkv_decode_attn_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, con
 def pkv_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
                         scale: float, out, lse_out=None, slot_mapping_out=None, partition_blocks: int = 0,
                         max_partitions: int = 0, workspace=None, err_flag=None, stream=None) -> int:
-    _fp8_common(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens)
+    stride = _fp8_common(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens)
     _need(k_new, torch.bfloat16, 3, "k_new")
     _need(v_new, torch.bfloat16, 3, "v_new")
     _need(out, torch.bfloat16, 3, "out")
@@ -363,7 +379,7 @@ def pkv_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, blo
     _opt(err_flag, torch.int32, 1, "err_flag")
     B, N, _ = q.shape
     return _lib.pkv_decode_step_fp8(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-                                    _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
+                                    _ptr(k_scale), _ptr(v_scale), stride, _ptr(block_tables), block_tables.shape[1],
                                     _ptr(context_lens), B, N, float(scale), _ptr(out), _ptr(lse_out),
                                     _ptr(slot_mapping_out), cache_desc(k_cache), partition_blocks,
                                     max_partitions, _ptr(workspace),

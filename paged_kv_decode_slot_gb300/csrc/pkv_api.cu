@@ -480,7 +480,8 @@ int check_fp8_desc(const pkv_cache_desc &d)
 }
 
 int fp8_attention(const AttnArgs &a, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
-                  const float *k_scale, const float *v_scale, pkv_bf16 *out, float *lse_out,
+                  const float *k_scale, const float *v_scale, int32_t scale_block_stride,
+                  pkv_bf16 *out, float *lse_out,
                   int64_t *slot_out, int32_t partition_blocks, int32_t max_partitions,
                   void *workspace, size_t workspace_bytes, cudaStream_t stream)
 {
@@ -489,6 +490,7 @@ int fp8_attention(const AttnArgs &a, const pkv_bf16 *k_new, const pkv_bf16 *v_ne
     if (a.B < 0 || a.max_nb <= 0 || a.N <= 0) return PKV_ERR_SHAPE;
     int st = check_fp8_desc(a.d);
     if (st != PKV_OK) return st;
+    if (scale_block_stride != 0 && scale_block_stride != a.d.num_kv_heads) return PKV_ERR_SHAPE;
     if (a.N % a.d.num_kv_heads != 0) return PKV_ERR_SHAPE;
     const int G = a.N / a.d.num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
@@ -520,6 +522,7 @@ int fp8_attention(const AttnArgs &a, const pkv_bf16 *k_new, const pkv_bf16 *v_ne
     p.lse_out = lse_out;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    p.scale_stride = scale_block_stride;
     p.k_new = k_new;
     p.v_new = v_new;
     p.k_cache_w = const_cast<pkv_bf16 *>(a.k_cache);
@@ -546,21 +549,23 @@ int fp8_attention(const AttnArgs &a, const pkv_bf16 *k_new, const pkv_bf16 *v_ne
 }  // namespace
 
 PKV_EXPORT int pkv_quantize_fp8(const pkv_bf16 *src, int64_t rows, int32_t num_kv_heads,
-                                int32_t head_dim, const float *scale, uint8_t *dst,
-                                pkv_stream_t stream)
+                                int32_t head_dim, const float *scale, int32_t scale_block_stride,
+                                uint8_t *dst, pkv_stream_t stream)
 {
     if (!src || !scale || !dst) return PKV_ERR_NULL;
     if (rows < 0 || num_kv_heads <= 0 || head_dim <= 0) return PKV_ERR_SHAPE;
+    if (scale_block_stride != 0 && (scale_block_stride != num_kv_heads || rows % 16 != 0)) return PKV_ERR_SHAPE;
     if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
     if (!aligned(src, 16) || !aligned(dst, 8) || !aligned(scale, 4)) return PKV_ERR_ALIGN;
     if (rows == 0) return PKV_OK;
-    cudaError_t e = pkv::launch_quantize_fp8(src, rows, num_kv_heads, head_dim, scale, dst, stream);
+    cudaError_t e = pkv::launch_quantize_fp8(src, rows, num_kv_heads, head_dim, scale, scale_block_stride, dst,
+                                             stream);
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "e4m3 quantize launch");
 }
 
 PKV_EXPORT int pkv_append_fp8(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const float *k_scale,
-                              const float *v_scale, const int64_t *slot_mapping, int32_t num_tokens,
-                              uint8_t *k_cache, uint8_t *v_cache, pkv_cache_desc cache,
+                              const float *v_scale, int32_t scale_block_stride, const int64_t *slot_mapping,
+                              int32_t num_tokens, uint8_t *k_cache, uint8_t *v_cache, pkv_cache_desc cache,
                               int32_t *err_flag, pkv_stream_t stream)
 {
     if (!k_new || !v_new || !k_scale || !v_scale || !slot_mapping || !k_cache || !v_cache)
@@ -568,17 +573,19 @@ PKV_EXPORT int pkv_append_fp8(const pkv_bf16 *k_new, const pkv_bf16 *v_new, cons
     if (num_tokens < 0) return PKV_ERR_SHAPE;
     int st = check_copy_desc(cache);
     if (st != PKV_OK) return st;
+    if (scale_block_stride != 0 && scale_block_stride != cache.num_kv_heads) return PKV_ERR_SHAPE;
     if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 8) || !aligned(v_cache, 8))
         return PKV_ERR_ALIGN;
     if (num_tokens == 0) return PKV_OK;
-    cudaError_t e = pkv::launch_append_fp8(k_new, v_new, k_scale, v_scale, slot_mapping, num_tokens,
+    cudaError_t e = pkv::launch_append_fp8(k_new, v_new, k_scale, v_scale, scale_block_stride, slot_mapping,
+                                           num_tokens,
                                            k_cache, v_cache, cache.num_blocks, cache.num_kv_heads,
                                            cache.head_dim, err_flag, stream);
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "e4m3 append launch");
 }
 
 PKV_EXPORT int pkv_decode_attn_fp8(const pkv_bf16 *q, const uint8_t *k_cache, const uint8_t *v_cache,
-                                   const float *k_scale, const float *v_scale,
+                                   const float *k_scale, const float *v_scale, int32_t scale_block_stride,
                                    const int32_t *block_tables, int32_t max_blocks_per_seq,
                                    const int32_t *context_lens, int32_t num_seqs,
                                    int32_t num_q_heads, float scale, pkv_bf16 *out, float *lse_out,
@@ -589,13 +596,13 @@ PKV_EXPORT int pkv_decode_attn_fp8(const pkv_bf16 *q, const uint8_t *k_cache, co
     AttnArgs a{q, reinterpret_cast<const pkv_bf16 *>(k_cache), reinterpret_cast<const pkv_bf16 *>(v_cache),
                block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale, cache,
                err_flag};
-    return fp8_attention(a, nullptr, nullptr, k_scale, v_scale, out, lse_out, nullptr,
+    return fp8_attention(a, nullptr, nullptr, k_scale, v_scale, scale_block_stride, out, lse_out, nullptr,
                          partition_blocks, max_partitions, workspace, workspace_bytes, stream);
 }
 
 PKV_EXPORT int pkv_decode_step_fp8(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
                                    uint8_t *k_cache, uint8_t *v_cache, const float *k_scale,
-                                   const float *v_scale, const int32_t *block_tables,
+                                   const float *v_scale, int32_t scale_block_stride, const int32_t *block_tables,
                                    int32_t max_blocks_per_seq, const int32_t *context_lens,
                                    int32_t num_seqs, int32_t num_q_heads, float scale, pkv_bf16 *out,
                                    float *lse_out, int64_t *slot_mapping_out, pkv_cache_desc cache,
@@ -606,7 +613,7 @@ PKV_EXPORT int pkv_decode_step_fp8(const pkv_bf16 *q, const pkv_bf16 *k_new, con
     AttnArgs a{q, reinterpret_cast<const pkv_bf16 *>(k_cache), reinterpret_cast<const pkv_bf16 *>(v_cache),
                block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads, scale, cache,
                err_flag};
-    return fp8_attention(a, k_new, v_new, k_scale, v_scale, out, lse_out, slot_mapping_out,
+    return fp8_attention(a, k_new, v_new, k_scale, v_scale, scale_block_stride, out, lse_out, slot_mapping_out,
                          partition_blocks, max_partitions, workspace, workspace_bytes, stream);
 }
 

@@ -65,14 +65,15 @@ __device__ __forceinline__ void append_new_token(const AttnParams &p, int b, int
 // [0, H/16) handle the K row, [H/16, H/8) the V row, 16 codes each.
 template <int H>
 __device__ __forceinline__ void append_new_token_fp8(const AttnParams &p, int b, int kvh, int ctx,
-                                                     int bid, uint32_t kt, uint32_t vt, int lane)
+                                                     int bid, uint32_t kt, uint32_t vt, float k_sc,
+                                                     float v_sc, int lane)
 {
     constexpr int kChunks = H / 16;
     if (lane >= 2 * kChunks) return;
     const int tok = (ctx - 1) % kBlockSize;
     const bool is_v = lane >= kChunks;
     const int c = is_v ? lane - kChunks : lane;
-    const float sc = (is_v ? p.v_scale : p.k_scale)[kvh];
+    const float sc = is_v ? v_sc : k_sc;  // the scales of the block being written
     const uint4 *src = reinterpret_cast<const uint4 *>((is_v ? p.v_new : p.k_new) +
                                                         ((size_t)b * p.K + kvh) * H + 16 * c);
     const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
@@ -95,7 +96,7 @@ __device__ __forceinline__ void append_new_token_fp8(const AttnParams &p, int b,
 // ------------------------ single pass and fixed partitions --------------------------------
 // kFp8: the pools hold e4m3 codes with per-KV-head scales (H = 128); the K scale is folded into
 // the logit multiplier, the V scale into the final normalisation.
-template <int H, bool kSplit, bool kFp8 = false, bool kPairs = false>
+template <int H, bool kSplit, bool kFp8 = false, bool kPairs = false, bool kBScale = false>
 __global__ void __launch_bounds__(kAttnThreads, PKV_CTAS_PER_SM)
 attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
             const AttnParams p)
@@ -154,6 +155,17 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     volatile int *slot_ok = reinterpret_cast<volatile int *>(base + L::kMiscOffset);
     volatile int *abort_flag = slot_ok + S;
     volatile int *issued_count = abort_flag + 1;  // [kProducers]
+    // e4m3 with per-(block, head) scales: the producers store each stage's (K, V) scales; the
+    // weights of a tile are taken relative to vref (the V scale of the CTA's first block), which
+    // multiplies the output at the end; with per-head scales vref is the head's V scale.
+    volatile float2 *stage_sc = reinterpret_cast<volatile float2 *>(base + L::kScaleOffset);
+    constexpr bool bscale = kFp8 && kBScale;
+    float vref = 1.f, inv_vref = 1.f;  // per-head scales: the head's V scale, read at the end
+    if constexpr (bscale) {
+        const int bid0 = __ldg(p.block_tables + (size_t)b * p.max_nb + blk_begin);
+        vref = bid0 >= 0 && bid0 < p.num_blocks ? __ldg(p.v_scale + (size_t)bid0 * p.scale_stride + kvh) : 1.f;
+        inv_vref = 1.f / vref;
+    }
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -172,12 +184,17 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
             prefetch_tensormap(&tm_v);
         }
         const int32_t *tbl = p.block_tables + (size_t)b * p.max_nb + blk_begin;
-        const int64_t issued = run_producer<kProducers>(
+        const int64_t issued = run_producer<kProducers, bscale>(
             pw, lane, nblk, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, p.err_flag,
-            [&](int64_t i, int bid, bool ok) {
+            [&](int64_t i, int bid, bool ok, float2 sc) {
                 return produce_tile<H, S, kFp8>(i, kvh, bid, ok, base_u32, bar_full, bar_empty,
                                                 slot_ok, abort_flag, &tm_k, &tm_v, p.tok_major,
-                                                p.err_flag);
+                                                p.err_flag, bscale ? stage_sc : nullptr, sc);
+            },
+            [&](int bid) {
+                if (!bscale) return make_float2(0.f, 0.f);
+                const size_t si = (size_t)bid * p.scale_stride + kvh;
+                return make_float2(__ldg(p.k_scale + si), __ldg(p.v_scale + si));
             });
         if (lane == 0) issued_count[pw] = (int)issued;
     } else {
@@ -212,6 +229,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
                 }
                 uint32_t kts[2], vts[2];
                 int valid[2];
+                float sl2s[2] = {sl2, sl2}, vsrs[2] = {1.f, 1.f}, ivss[2] = {1.f, 1.f};
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     const int it = t ? i2 : i, st = t ? s2 : s1;
@@ -219,19 +237,27 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
                     kts[t] = base_u32 + (here ? st : s1) * L::kStageBytes;
                     vts[t] = kts[t] + L::kTileBytes;
                     valid[t] = here && slot_ok[st] ? min(kBlockSize, ctx - (blk_begin + it) * kBlockSize) : 0;
+                    if (bscale && valid[t] > 0) {
+                        const float ks_t = stage_sc[st].x, vs_t = stage_sc[st].y;
+                        sl2s[t] = p.scale_log2 * ks_t;
+                        vsrs[t] = vs_t * inv_vref;
+                        ivss[t] = __fdividef(vref, vs_t);
+                    }
                     // fused append: the tile of the sequence's last block holds the new token
                     const bool newest = here && p.k_new && blk_begin + it == nb - 1;
                     if (newest) {
                         const int last_bid = __ldg(p.block_tables + (size_t)b * p.max_nb + nb - 1);
                         if (slot_ok[st]) {
-                            append_new_token_fp8<H>(p, b, kvh, ctx, last_bid, kts[t], vts[t], lane);
+                            append_new_token_fp8<H>(p, b, kvh, ctx, last_bid, kts[t], vts[t],
+                                                    bscale ? stage_sc[st].x : p.k_scale[kvh],
+                                                    bscale ? stage_sc[st].y : p.v_scale[kvh], lane);
                             __syncwarp();
                         }
                         if (p.slot_out && kvh == 0 && lane == 0)
                             p.slot_out[b] = slot_ok[st] ? (int64_t)last_bid * kBlockSize + (ctx - 1) % kBlockSize : -1;
                     }
                 }
-                if (valid[0] > 0 || valid[1] > 0) tile_update_fp8_n<H, 2>(acc, qf, kts, vts, valid, sl2, lane);
+                if (valid[0] > 0 || valid[1] > 0) tile_update_fp8_n<H, 2, bscale>(acc, qf, kts, vts, valid, sl2s, vsrs, ivss, lane);
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(bar_empty + 8 * s1);
@@ -252,15 +278,24 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
             if (slot_ok[s]) {
                 const int valid = min(kBlockSize, ctx - (blk_begin + i) * kBlockSize);
                 const uint32_t kt = base_u32 + s * L::kStageBytes;
+                float sl2_t = sl2, vsr = 1.f, ivs = 1.f;  // this tile's logit multiplier, V-scale ratio
+                if constexpr (bscale) {
+                    const float ks_t = stage_sc[s].x, vs_t = stage_sc[s].y;
+                    sl2_t = p.scale_log2 * ks_t;
+                    vsr = vs_t * inv_vref;
+                    ivs = __fdividef(vref, vs_t);
+                }
                 if (newest) {
                     if constexpr (kFp8)
-                        append_new_token_fp8<H>(p, b, kvh, ctx, last_bid, kt, kt + L::kTileBytes, lane);
+                        append_new_token_fp8<H>(p, b, kvh, ctx, last_bid, kt, kt + L::kTileBytes,
+                                                bscale ? stage_sc[s].x : p.k_scale[kvh],
+                                                bscale ? stage_sc[s].y : p.v_scale[kvh], lane);
                     else
                         append_new_token<H>(p, b, kvh, ctx, last_bid, kt, kt + L::kTileBytes, lane);
                     __syncwarp();
                 }
                 if constexpr (kFp8)
-                    tile_update_fp8<H>(acc, qf, kt, kt + L::kTileBytes, valid, sl2, lane);
+                    tile_update_fp8<H>(acc, qf, kt, kt + L::kTileBytes, valid, sl2_t, vsr, ivs, lane);
                 else
                     tile_update<H>(acc, qf, kt, kt + L::kTileBytes, valid, sl2, p.tok_major, lane);
             }
@@ -290,7 +325,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
         if (warp < kConsumerWarps) deposit<H, kFp8>(acc, mo, mm, ml, warp, lane);
         __syncthreads();
     }
-    const float vscale = kFp8 ? p.v_scale[kvh] : 1.f;
+    const float vscale = kFp8 ? (bscale ? vref : p.v_scale[kvh]) : 1.f;
     for (int idx = threadIdx.x; idx < G * H; idx += kAttnThreads) {
         const int g = idx / H, h = idx - g * H;
         float val = __int_as_float(0x7FC00000), lse = __int_as_float(0x7FC00000);  // NaN: void
@@ -451,7 +486,7 @@ attn_balanced_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             return __ldg(p.block_tables + (size_t)tl.b * p.max_nb + tl.j);
         };
         const int64_t issued = run_producer<P>(
-            pw, lane, n, lookup, p.num_blocks, p.err_flag, [&](int64_t i, int bid, bool ok) {
+            pw, lane, n, lookup, p.num_blocks, p.err_flag, [&](int64_t i, int bid, bool ok, float2) {
                 return produce_tile<H, S>(i, kvh, bid, ok, base_u32, bar_full, bar_empty, slot_ok,
                                           abort_flag, &tm_k, &tm_v, p.tok_major, p.err_flag);
             });
@@ -644,16 +679,16 @@ static cudaError_t ensure_smem(Kern kern, int smem, int *cached)
     return e;
 }
 
-template <int H, bool kSplit, bool kFp8, bool kPairs = false>
+template <int H, bool kSplit, bool kFp8, bool kPairs = false, bool kBScale = false>
 static cudaError_t launch_attn_t(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
                                  dim3 grid, cudaStream_t stream)
 {
     constexpr int smem = AttnLayout<H, kFp8 ? kStagesFp8 : kStages, kConsumerWarps, kProducers,
                                     kFp8 ? 1 : 2>::kAlloc;
     static int cached[64] = {};
-    cudaError_t e = ensure_smem(attn_kernel<H, kSplit, kFp8, kPairs>, smem, cached);
+    cudaError_t e = ensure_smem(attn_kernel<H, kSplit, kFp8, kPairs, kBScale>, smem, cached);
     if (e != cudaSuccess) return e;
-    attn_kernel<H, kSplit, kFp8, kPairs><<<grid, kAttnThreads, smem, stream>>>(tk, tv, p);
+    attn_kernel<H, kSplit, kFp8, kPairs, kBScale><<<grid, kAttnThreads, smem, stream>>>(tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -662,6 +697,13 @@ cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensor
 {
     dim3 grid = split ? dim3(p.K, p.B, p.max_parts) : dim3(p.K, p.B, 1);
     if (fp8) {  // e4m3 pools: H = 128 only; tile pairs for grids with few CTAs per SM
+        if (p.scale_stride) {  // per-(block, head) scales
+            if (pairs)
+                return split ? launch_attn_t<128, true, true, true, true>(tk, tv, p, grid, stream)
+                             : launch_attn_t<128, false, true, true, true>(tk, tv, p, grid, stream);
+            return split ? launch_attn_t<128, true, true, false, true>(tk, tv, p, grid, stream)
+                         : launch_attn_t<128, false, true, false, true>(tk, tv, p, grid, stream);
+        }
         if (pairs)
             return split ? launch_attn_t<128, true, true, true>(tk, tv, p, grid, stream)
                          : launch_attn_t<128, false, true, true>(tk, tv, p, grid, stream);

@@ -79,7 +79,9 @@ struct AttnLayout {
     static constexpr int kDataBytes = kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes;
     static constexpr int kBarOffset = kDataBytes;           // full[S], empty[S]
     static constexpr int kMiscOffset = kBarOffset + 2 * S * 8;  // slot_ok[S], abort, issued[P]
-    static constexpr int kBytes = kMiscOffset + (S + 1 + P) * 4;
+    // e4m3 with per-(block, head) scales: the (K, V) scales of each stage's tile, float2[S]
+    static constexpr int kScaleOffset = (kMiscOffset + (S + 1 + P) * 4 + 7) / 8 * 8;
+    static constexpr int kBytes = kScaleOffset + S * 8;
     static constexpr int kAlloc = kBytes + 1024;             // slack for 1024-byte alignment
     // balanced kernel: pipeline, its own merge area, barriers, misc, then the block prefix
     static constexpr int kBalMergeOffset = kPipeBytes;
@@ -250,11 +252,14 @@ __device__ __forceinline__ void load_q_frags_fp8(uint32_t (&qf)[H / 16][2], cons
     }
 }
 
-// One 16-token e4m3 tile folded into a warp's state (the codes only; the per-head scales are
-// folded into sl2 and into the final normalisation).
+// One 16-token e4m3 tile folded into a warp's state (the codes only: the tile's K scale is
+// folded into sl2; its weights enter P.V multiplied by vsr, the tile's V scale relative to the
+// one the caller multiplies the output by, and the running sum as the P.V weights times
+// ivs = 1 / vsr -- both 1 with one scale per head).
 template <int H>
 __device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&qf)[H / 16][2],
-                                                uint32_t kt, uint32_t vt, int valid, float sl2, int lane)
+                                                uint32_t kt, uint32_t vt, int valid, float sl2, float vsr,
+                                                float ivs, int lane)
 {
     constexpr int kKSteps = H / 16;
     const int mi = lane >> 3, ri = lane & 7;
@@ -306,10 +311,10 @@ __device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&
             a.o[mt][3] *= alphaB;
         }
     }
-    const uint32_t p01 = pack_f16x2(exp2f(x0 - a.m[0]), exp2f(x1 - a.m[1]));
-    const uint32_t p23 = pack_f16x2(exp2f(x2 - a.m[0]), exp2f(x3 - a.m[1]));
-    a.l[0] += f16x2_lo(p01) + f16x2_lo(p23);
-    a.l[1] += f16x2_hi(p01) + f16x2_hi(p23);
+    const uint32_t p01 = pack_f16x2(exp2f(x0 - a.m[0]) * vsr, exp2f(x1 - a.m[1]) * vsr);
+    const uint32_t p23 = pack_f16x2(exp2f(x2 - a.m[0]) * vsr, exp2f(x3 - a.m[1]) * vsr);
+    a.l[0] += (f16x2_lo(p01) + f16x2_lo(p23)) * ivs;
+    a.l[1] += (f16x2_hi(p01) + f16x2_hi(p23)) * ivs;
     const uint32_t pb0 = movmatrix_trans(p01);
     const uint32_t pb1 = movmatrix_trans(p23);
 
@@ -351,10 +356,13 @@ __device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&
 // independent dependency chains in flight where one tile's chain would leave it waiting.  A
 // column that has seen no key keeps m = -inf and gets zero weights.  The caller skips a step in
 // which no tile has a valid token.
-template <int H, int NT>
+// kBS: per-tile scales (sl2[t], vsr[t], ivs[t] as in tile_update_fp8); otherwise sl2[0] for every
+// tile and no V-scale ratios.
+template <int H, int NT, bool kBS = false>
 __device__ __forceinline__ void tile_update_fp8_n(WarpAcc<H> &a, const uint32_t (&qf)[H / 16][2],
                                                   const uint32_t (&kt)[NT], const uint32_t (&vt)[NT],
-                                                  const int (&valid)[NT], float sl2, int lane)
+                                                  const int (&valid)[NT], const float (&sl2)[NT],
+                                                  const float (&vsr)[NT], const float (&ivs)[NT], int lane)
 {
     constexpr int kKSteps = H / 16;
     const int mi = lane >> 3, ri = lane & 7;
@@ -382,10 +390,11 @@ __device__ __forceinline__ void tile_update_fp8_n(WarpAcc<H> &a, const uint32_t 
             mma_f16_16816(sa, a0, qf[kk][0], qf[kk][1]);
             mma_f16_16816(sb, a1, qf[kk + 1][0], qf[kk + 1][1]);
         }
-        x[t][0] = t0 < valid[t] ? (sa[0] + sb[0]) * sl2 : -INFINITY;
-        x[t][1] = t0 < valid[t] ? (sa[1] + sb[1]) * sl2 : -INFINITY;
-        x[t][2] = t1 < valid[t] ? (sa[2] + sb[2]) * sl2 : -INFINITY;
-        x[t][3] = t1 < valid[t] ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+        const float m_t = sl2[kBS ? t : 0];
+        x[t][0] = t0 < valid[t] ? (sa[0] + sb[0]) * m_t : -INFINITY;
+        x[t][1] = t0 < valid[t] ? (sa[1] + sb[1]) * m_t : -INFINITY;
+        x[t][2] = t1 < valid[t] ? (sa[2] + sb[2]) * m_t : -INFINITY;
+        x[t][3] = t1 < valid[t] ? (sa[3] + sb[3]) * m_t : -INFINITY;
     }
     float mA = -INFINITY, mB = -INFINITY;
 #pragma unroll
@@ -420,10 +429,11 @@ __device__ __forceinline__ void tile_update_fp8_n(WarpAcc<H> &a, const uint32_t 
     uint32_t pb[NT][2];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        const uint32_t p01 = pack_f16x2(exp2f(x[t][0] - baseA), exp2f(x[t][1] - baseB));
-        const uint32_t p23 = pack_f16x2(exp2f(x[t][2] - baseA), exp2f(x[t][3] - baseB));
-        a.l[0] += f16x2_lo(p01) + f16x2_lo(p23);
-        a.l[1] += f16x2_hi(p01) + f16x2_hi(p23);
+        const float r_t = kBS ? vsr[t] : 1.f, ir_t = kBS ? ivs[t] : 1.f;
+        const uint32_t p01 = pack_f16x2(exp2f(x[t][0] - baseA) * r_t, exp2f(x[t][1] - baseB) * r_t);
+        const uint32_t p23 = pack_f16x2(exp2f(x[t][2] - baseA) * r_t, exp2f(x[t][3] - baseB) * r_t);
+        a.l[0] += (f16x2_lo(p01) + f16x2_lo(p23)) * ir_t;
+        a.l[1] += (f16x2_hi(p01) + f16x2_hi(p23)) * ir_t;
         pb[t][0] = movmatrix_trans(p01);
         pb[t][1] = movmatrix_trans(p23);
     }
@@ -565,7 +575,8 @@ __device__ __forceinline__ bool produce_tile(int64_t i, int kvh, int bid, bool o
                                              uint32_t bar_full, uint32_t bar_empty,
                                              volatile int *slot_ok, volatile int *abort_flag,
                                              const CUtensorMap *tm_k, const CUtensorMap *tm_v,
-                                             int tok_major, int32_t *err_flag)
+                                             int tok_major, int32_t *err_flag,
+                                             volatile float2 *stage_scale = nullptr, float2 scales = {})
 {
     using L = AttnLayout<H, S, kConsumerWarps, kProducers, kFp8 ? 1 : 2>;
     const int s = (int)(i % S);
@@ -575,6 +586,11 @@ __device__ __forceinline__ bool produce_tile(int64_t i, int kvh, int bid, bool o
         if (!*abort_flag) set_flag(err_flag, PKV_FLAG_TIMEOUT);
         *abort_flag = 1;
         return false;
+    }
+    // the tile's scales, once the stage is free and before its barrier can complete
+    if (stage_scale) {
+        stage_scale[s].x = scales.x;
+        stage_scale[s].y = scales.y;
     }
     if (ok) {
         slot_ok[s] = 1;
@@ -600,27 +616,42 @@ __device__ __forceinline__ bool produce_tile(int64_t i, int kvh, int bid, bool o
 
 // Producer warp p of P issues the CTA's tiles i = p, p + P, p + 2P, ... in order: `lookup(i)`
 // gives tile i's physical block id (lanes look up 32 tiles at a time, the next 32 while the
-// current ones are issued) and `issue(i, bid, ok)` waits for the stage and loads it, returning
-// false when its wait expired.  Returns the number of tiles this producer issued (on lane 0).
-template <int P, typename Lookup, typename Issue>
+// current ones are issued), `aux(bid)` a per-block value fetched along with it (in-range ids
+// only; e.g. the block's e4m3 scales), and `issue(i, bid, ok, aux)` waits for the stage and
+// loads it, returning false when its wait expired.  Returns the number of tiles this producer
+// issued (on lane 0).
+struct NoAux {
+    __device__ __forceinline__ float2 operator()(int) const { return make_float2(0.f, 0.f); }
+};
+
+template <int P, bool kAux = false, typename Lookup, typename Issue, typename Aux = NoAux>
 __device__ __forceinline__ int64_t run_producer(int pw, int lane, int64_t n, Lookup lookup,
-                                                int num_blocks, int32_t *err_flag, Issue issue)
+                                                int num_blocks, int32_t *err_flag, Issue issue, Aux aux = Aux())
 {
     const int64_t mine = n > pw ? (n - pw + P - 1) / P : 0;
+    auto fetch = [&](int bid) {
+        if constexpr (kAux) return bid >= 0 && bid < num_blocks ? aux(bid) : make_float2(0.f, 0.f);
+        return make_float2(0.f, 0.f);
+    };
     int cur = lane < mine ? lookup(pw + (int64_t)P * lane) : 0;
+    float2 cur_aux = lane < mine ? fetch(cur) : make_float2(0.f, 0.f);
     int64_t issued = 0;
     bool aborted = false;
     for (int64_t k0 = 0; k0 < mine && !aborted; k0 += 32) {
-        const int nxt = (k0 + 32 + lane < mine) ? lookup(pw + (int64_t)P * (k0 + 32 + lane)) : 0;
+        const bool more = k0 + 32 + lane < mine;
+        const int nxt = more ? lookup(pw + (int64_t)P * (k0 + 32 + lane)) : 0;
+        const float2 nxt_aux = more ? fetch(nxt) : make_float2(0.f, 0.f);
         const int cnt = (int)min((int64_t)32, mine - k0);
         const bool bad = lane < cnt && (cur < 0 || cur >= num_blocks);
         const unsigned badmask = __ballot_sync(0xFFFFFFFFu, bad);
         if (badmask && lane == 0) set_flag(err_flag, PKV_FLAG_BLOCK_RANGE);
         for (int k = 0; k < cnt; ++k) {
             const int bid = __shfl_sync(0xFFFFFFFFu, cur, k);
+            float2 a = make_float2(0.f, 0.f);
+            if constexpr (kAux) a = make_float2(__shfl_sync(0xFFFFFFFFu, cur_aux.x, k), __shfl_sync(0xFFFFFFFFu, cur_aux.y, k));
             int lane0_abort = 0;
             if (lane == 0) {
-                if (issue(pw + (int64_t)P * (k0 + k), bid, !((badmask >> k) & 1u)))
+                if (issue(pw + (int64_t)P * (k0 + k), bid, !((badmask >> k) & 1u), a))
                     ++issued;
                 else
                     lane0_abort = 1;
@@ -629,6 +660,7 @@ __device__ __forceinline__ int64_t run_producer(int pw, int lane, int64_t n, Loo
             if (aborted) break;
         }
         cur = nxt;
+        cur_aux = nxt_aux;
     }
     return issued;
 }

@@ -206,6 +206,8 @@ cudaError_t launch_gather(const uint16_t *k_cache, const uint16_t *v_cache,
 // ---------------------------------- FP8 (e4m3) cache ----------------------------------------
 // code = e4m3(x / scale[kvh]): the division rounded to nearest in fp32, then round-to-nearest-
 // even onto the e4m3 grid with saturation at +-448 (cvt.rn.satfinite).  One thread per 8 values.
+// With scale_stride > 0 the scales are per (physical block, KV head): a value in block blk uses
+// scale[blk * scale_stride + kvh].
 namespace pkv {
 
 __device__ __forceinline__ uint2 quantize8(const uint4 x, float sc)
@@ -218,17 +220,21 @@ __device__ __forceinline__ uint2 quantize8(const uint4 x, float sc)
 }
 
 __global__ void quantize_fp8_kernel(const uint4 *__restrict__ src, int64_t n8, int K, int H,
-                                    const float *__restrict__ scale, uint2 *__restrict__ dst)
+                                    const float *__restrict__ scale, int scale_stride,
+                                    uint2 *__restrict__ dst)
 {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n8) return;
-    const int kvh = (int)(((i * 8) / H) % K);
-    dst[i] = quantize8(__ldg(src + i), __ldg(scale + kvh));
+    const int64_t row = (i * 8) / H;  // [rows][K] of H-element head rows
+    const int kvh = (int)(row % K);
+    const int64_t blk = row / ((int64_t)K * kBlockSize);
+    dst[i] = quantize8(__ldg(src + i), __ldg(scale + blk * scale_stride + kvh));
 }
 
 __global__ void append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                                   const float *__restrict__ k_scale, const float *__restrict__ v_scale,
-                                  const int64_t *__restrict__ slots, int T, uint2 *__restrict__ k_cache,
+                                  int scale_stride, const int64_t *__restrict__ slots, int T,
+                                  uint2 *__restrict__ k_cache,
                                   uint2 *__restrict__ v_cache, int64_t capacity, int K, int H,
                                   int32_t *err_flag)
 {
@@ -245,22 +251,24 @@ __global__ void append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *
     }
     const int kvh = r * 8 / H;
     const int64_t src = (int64_t)i * vec_per_row + r, dst = slot * vec_per_row + r;
-    k_cache[dst] = quantize8(__ldg(k_new + src), __ldg(k_scale + kvh));
-    v_cache[dst] = quantize8(__ldg(v_new + src), __ldg(v_scale + kvh));
+    const int64_t si = (slot / kBlockSize) * scale_stride + kvh;  // scales of the slot's block
+    k_cache[dst] = quantize8(__ldg(k_new + src), __ldg(k_scale + si));
+    v_cache[dst] = quantize8(__ldg(v_new + src), __ldg(v_scale + si));
 }
 
 cudaError_t launch_quantize_fp8(const uint16_t *src, int64_t rows, int K, int H, const float *scale,
-                                uint8_t *dst, cudaStream_t stream)
+                                int scale_stride, uint8_t *dst, cudaStream_t stream)
 {
     const int64_t n8 = rows * K * H / 8;
     const int threads = 256;
     quantize_fp8_kernel<<<(unsigned)((n8 + threads - 1) / threads), threads, 0, stream>>>(
-        reinterpret_cast<const uint4 *>(src), n8, K, H, scale, reinterpret_cast<uint2 *>(dst));
+        reinterpret_cast<const uint4 *>(src), n8, K, H, scale, scale_stride, reinterpret_cast<uint2 *>(dst));
     return cudaGetLastError();
 }
 
 cudaError_t launch_append_fp8(const uint16_t *k_new, const uint16_t *v_new, const float *k_scale,
-                              const float *v_scale, const int64_t *slots, int T, uint8_t *k_cache,
+                              const float *v_scale, int scale_stride, const int64_t *slots, int T,
+                              uint8_t *k_cache,
                               uint8_t *v_cache, int num_blocks, int K, int H, int32_t *err_flag,
                               cudaStream_t stream)
 {
@@ -268,7 +276,7 @@ cudaError_t launch_append_fp8(const uint16_t *k_new, const uint16_t *v_new, cons
     const int threads = 256;
     append_fp8_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, stream>>>(
         reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), k_scale,
-        v_scale, slots, T, reinterpret_cast<uint2 *>(k_cache), reinterpret_cast<uint2 *>(v_cache),
+        v_scale, scale_stride, slots, T, reinterpret_cast<uint2 *>(k_cache), reinterpret_cast<uint2 *>(v_cache),
         (int64_t)num_blocks * kBlockSize, K, H, err_flag);
     return cudaGetLastError();
 }

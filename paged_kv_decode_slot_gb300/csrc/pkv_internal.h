@@ -35,8 +35,9 @@ struct AttnParams {
     const uint16_t *v_new;
     void *k_cache_w;               // the pools (bf16 or e4m3), written at the newest slot
     void *v_cache_w;
-    const float *k_scale;          // e4m3 pools: per-KV-head scales [K] (value = code * scale)
+    const float *k_scale;          // e4m3 pools: scales (value = code * scale), [K] or [num_blocks][K]
     const float *v_scale;
+    int32_t scale_stride;          // e4m3: 0 = one scale per KV head; K = per (physical block, KV head)
     int64_t *slot_out;             // [B] slot of the newest token (-1 none), nullable
     int32_t *counters;             // split-KV with the merge in the kernel: [B][K], zero between
                                    // calls (nullptr: write every partial, merge separately)
@@ -103,10 +104,11 @@ cudaError_t launch_copy_blocks(uint8_t *k_cache, uint8_t *v_cache, const int32_t
                                cudaStream_t stream);
 
 cudaError_t launch_quantize_fp8(const uint16_t *src, int64_t rows, int K, int H, const float *scale,
-                                uint8_t *dst, cudaStream_t stream);
+                                int scale_stride, uint8_t *dst, cudaStream_t stream);
 
 cudaError_t launch_append_fp8(const uint16_t *k_new, const uint16_t *v_new, const float *k_scale,
-                              const float *v_scale, const int64_t *slots, int T, uint8_t *k_cache,
+                              const float *v_scale, int scale_stride, const int64_t *slots, int T,
+                              uint8_t *k_cache,
                               uint8_t *v_cache, int num_blocks, int K, int H, int32_t *err_flag,
                               cudaStream_t stream);
 

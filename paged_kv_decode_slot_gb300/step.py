@@ -206,8 +206,9 @@ class DecodeStep:
 
 
 class DecodeStepFp8:
-    """A decode step over e4m3 pools with per-KV-head scales: one ``pkv_decode_step_fp8`` call
-    (single pass or fixed partitions, as ``plan_attention`` picks; never the balanced path)."""
+    """A decode step over e4m3 pools with per-KV-head scales [K] or per-(physical block, KV head)
+    scales [num_blocks, K]: one ``pkv_decode_step_fp8`` call (single pass or fixed partitions, as
+    ``plan_attention`` picks; never the balanced path)."""
 
     def __init__(self, q, k_new, v_new, k_cache8, v_cache8, k_scale, v_scale, block_tables,
                  context_lens, scale, plan: AttentionPlan | None = None, err_flag=None):

@@ -3,7 +3,9 @@
 Quantization and append are byte work: the codes must equal the oracle's bit for bit (NaN
 inputs must give a NaN code; its sign bit is not compared).  Attention over e4m3 pools is
 compared with the oracle's float64 attention over the dequantized pools, at the bf16 path's
-tolerance; the fused fp8 step must equal the separate fp8 calls bit for bit.
+tolerance; the fused fp8 step must equal the separate fp8 calls bit for bit.  Both scale
+granularities run: one scale per KV head ([K]) and one per (physical block, KV head)
+([num_blocks, K]).
 """
 from __future__ import annotations
 
@@ -37,6 +39,19 @@ def head_scales(cache_bits: np.ndarray, spread: bool = True) -> np.ndarray:
     return (amax / 448.0 * mult).astype(np.float32)
 
 
+def block_scales(cache_bits: np.ndarray) -> np.ndarray:
+    """Per-(block, KV head) scale = that block's amax / 448 over its finite values (1 where it has
+    none), times (1 + kvh) so that a wrong head's scale is visibly wrong; blocks differ by their
+    own maxima, so a wrong block's scale is too."""
+    x = gen.bf16_bits_to_f32(cache_bits)                                   # [nb, 16, K, H]
+    amax = np.nanmax(np.abs(np.where(np.isfinite(x), x, np.nan)), axis=(1, 3))  # [nb, K]
+    amax = np.where(np.isfinite(amax) & (amax > 0), amax, 1.0)
+    return (amax / 448.0 * (1.0 + np.arange(amax.shape[1]))[None, :]).astype(np.float32)
+
+
+GRANULARITIES = ["head", "block"]
+
+
 def codes_equal(got: np.ndarray, ref: np.ndarray) -> bool:
     nan_ref = (ref & 0x7F) == 0x7F
     nan_got = (got & 0x7F) == 0x7F
@@ -52,12 +67,14 @@ def f32_dev(a: np.ndarray) -> torch.Tensor:
 
 
 class Fp8Case:
-    """A workload with its e4m3 pools (oracle-quantized) before and after the append."""
+    """A workload with its e4m3 pools (oracle-quantized) before and after the append, with one
+    scale per KV head or one per (physical block, KV head)."""
 
-    def __init__(self, oracle, w: gen.Workload):
+    def __init__(self, oracle, w: gen.Workload, granularity: str = "head"):
         self.w = w
-        self.ks = head_scales(w.k_cache)
-        self.vs = head_scales(w.v_cache)
+        scales = block_scales if granularity == "block" else head_scales
+        self.ks = scales(w.k_cache)
+        self.vs = scales(w.v_cache)
         self.kc8 = oracle.quantize_fp8(w.k_cache, self.ks)
         self.vc8 = oracle.quantize_fp8(w.v_cache, self.vs)
         self.slots = oracle.slot_mapping(w.block_tables, w.context_lens)
@@ -124,6 +141,17 @@ def test_quantize_matches_oracle_codes(pkv, oracle):
     assert codes_equal(got, ref), f"{int(np.sum(got != ref))} codes differ"
 
 
+def test_quantize_block_scales_matches_oracle(pkv, oracle):
+    """A whole pool quantized with per-(block, head) scales: codes equal the oracle's."""
+    w = gen.make_workload("p8_qblk", 86, 16, 4, 128, [33, 170, 300, 9])
+    for cache in (w.k_cache, w.v_cache):
+        sc = block_scales(cache)
+        ref = oracle.quantize_fp8(cache, sc)
+        dst = torch.empty(cache.shape, dtype=torch.uint8, device="cuda")
+        pkv.check(pkv.pkv_quantize_fp8(bf16_dev(cache), f32_dev(sc), dst))
+        assert codes_equal(dst.cpu().numpy(), ref)
+
+
 def test_quantize_every_bf16_bit_pattern(pkv, oracle):
     """All 65536 bf16 patterns (NaNs and infinities included) at two scales."""
     bits = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(512, 1, 128)
@@ -144,8 +172,9 @@ CASES = [
 ]
 
 
-def test_append_fp8_matches_oracle(pkv, oracle):
-    c = Fp8Case(oracle, CASES[1][1]())
+@pytest.mark.parametrize("gran", GRANULARITIES)
+def test_append_fp8_matches_oracle(pkv, oracle, gran):
+    c = Fp8Case(oracle, CASES[1][1](), gran)
     d = c.device(appended=False)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     pkv.check(pkv.pkv_append_fp8(d["k_new"], d["v_new"], d["k_scale"], d["v_scale"],
@@ -155,22 +184,24 @@ def test_append_fp8_matches_oracle(pkv, oracle):
     assert codes_equal(d["v_cache"].cpu().numpy(), c.vc8_app)
 
 
+@pytest.mark.parametrize("gran", GRANULARITIES)
 @pytest.mark.parametrize("part_blocks", [0, 2, 7])
 @pytest.mark.parametrize("name,make", CASES, ids=[c[0] for c in CASES])
-def test_decode_attn_fp8_matches_oracle(pkv, oracle, name, make, part_blocks):
-    c = Fp8Case(oracle, make())
+def test_decode_attn_fp8_matches_oracle(pkv, oracle, name, make, part_blocks, gran):
+    c = Fp8Case(oracle, make(), gran)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out, lse = _attn(pkv, c, c.device(appended=True), part_blocks, err)
     assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
     ref, ref_lse = c.reference(oracle)
-    assert_close(out_f64(out), ref, f"fp8 {name} pb={part_blocks}")
-    assert_lse_close(lse.cpu().numpy().astype(np.float64), ref_lse, f"fp8 {name} pb={part_blocks}")
+    assert_close(out_f64(out), ref, f"fp8 {name} pb={part_blocks} {gran}")
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), ref_lse, f"fp8 {name} pb={part_blocks} {gran}")
 
 
+@pytest.mark.parametrize("gran", GRANULARITIES)
 @pytest.mark.parametrize("part_blocks", [0, 3])
 @pytest.mark.parametrize("name,make", CASES, ids=[c[0] for c in CASES])
-def test_decode_step_fp8_equals_separate_calls(pkv, oracle, name, make, part_blocks):
-    c = Fp8Case(oracle, make())
+def test_decode_step_fp8_equals_separate_calls(pkv, oracle, name, make, part_blocks, gran):
+    c = Fp8Case(oracle, make(), gran)
     # separate: append then attention
     d1 = c.device(appended=False)
     slots1 = torch.empty(c.w.B, dtype=torch.int64, device="cuda")
@@ -193,10 +224,11 @@ def test_decode_step_fp8_equals_separate_calls(pkv, oracle, name, make, part_blo
     assert_close(out_f64(out2), ref, f"fp8 step {name} pb={part_blocks}")
 
 
+@pytest.mark.parametrize("gran", GRANULARITIES)
 @pytest.mark.parametrize("G", [1, 4, 8])
-def test_fp8_every_tail(pkv, oracle, G):
+def test_fp8_every_tail(pkv, oracle, G, gran):
     """Context lengths 1..49 (every in-block position of the new token) for group sizes 1/4/8."""
-    c = Fp8Case(oracle, gen.make_workload(f"p8_tail{G}", 90 + G, 2 * G, 2, 128, list(range(1, 50))))
+    c = Fp8Case(oracle, gen.make_workload(f"p8_tail{G}", 90 + G, 2 * G, 2, 128, list(range(1, 50))), gran)
     out, lse = _attn(pkv, c, c.device(appended=True), 0)
     ref, ref_lse = c.reference(oracle)
     assert_close(out_f64(out), ref, f"fp8 tails G={G}")
@@ -239,13 +271,15 @@ def test_fp8_full_size_sampled(pkv, oracle):
     assert_close(out_f64(out_s[sample]), ref, "fp8 l3_8b_b64 split")
 
 
-@pytest.mark.parametrize("name", ["l3_8b_b64", "l2_13b_mha_b128", "long_splitk", "l3_8b_b16"])
-def test_fp8_step_full_size_in_bench_plan(pkv, oracle, name):
+@pytest.mark.parametrize("name,gran", [("l3_8b_b64", "head"), ("l2_13b_mha_b128", "head"),
+                                       ("long_splitk", "head"), ("l3_8b_b16", "head"),
+                                       ("l3_8b_b64", "block"), ("l3_8b_b16", "block")])
+def test_fp8_step_full_size_in_bench_plan(pkv, oracle, name, gran):
     """The e4m3 decode step as the benchmark times it (DecodeStepFp8 with the planner's plan: one
     tile per step on wide grids, two on grids with fewer units than SMs), sampled sequences."""
     from paged_kv_decode_slot_gb300.step import DecodeStepFp8
     w = gen.make_config(name)
-    c = Fp8Case(oracle, w)
+    c = Fp8Case(oracle, w, gran)
     d = c.device(appended=False)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     step = DecodeStepFp8(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["k_scale"],
