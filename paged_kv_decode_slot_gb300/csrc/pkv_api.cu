@@ -200,7 +200,7 @@ struct SplitWs {
 
 // The in-kernel merge keeps G x max_parts weights in the attention kernel's drained ring (32 KiB
 // at least); larger splits merge in pkv_lse_merge.  pkv_lse_merge keeps max_parts weights.
-constexpr int64_t kInKernelMergeWeights = 8192;
+constexpr int64_t kInKernelMergeWeights = pkv::kInKernelMergeWeights;
 constexpr int32_t kMaxMergeParts = 12288;
 
 bool merge_in_kernel(int32_t N, int32_t K, int32_t max_parts)

@@ -353,19 +353,17 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     if (threadIdx.x == 0) last_one = atomic_add_acq_rel_gpu(count, 1) == nparts - 1;
     __syncthreads();
     if (!last_one) return;
-    float *wts = reinterpret_cast<float *>(base);  // [G][nparts]
+    float *wts = reinterpret_cast<float *>(base);                          // [G][nparts]
+    float *red = reinterpret_cast<float *>(base) + kInKernelMergeWeights;  // [kMergeWarps][8][H]
     for (int g = warp; g < G; g += kAttnThreads / 32) {
         const size_t bn = (size_t)b * p.N + (size_t)kvh * G + g;
         const float L = lse_merge_weights(p.part_lse + bn * p.max_parts, nparts, wts + g * nparts, lane);
         if (lane == 0 && p.lse_out) p.lse_out[bn] = L;
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < G * H; idx += kAttnThreads) {
-        const int g = idx / H, h = idx - g * H;
-        const size_t bn = (size_t)b * p.N + (size_t)kvh * G + g;
-        const float val = lse_merge_value(wts + g * nparts, p.part_out + bn * p.max_parts * H + h, nparts, H);
-        p.out[bn * H + h] = __float2bfloat16_rn(val);
-    }
+    const size_t bn0 = (size_t)b * p.N + (size_t)kvh * G;
+    merge_rows<H, 8>(wts, nparts, G, p.part_out + bn0 * p.max_parts * H, (size_t)p.max_parts * H, red, p.out + bn0 * H,
+                     H, threadIdx.x, kAttnThreads);
     if (threadIdx.x == 0) *count = 0;  // ready for the next call
 }
 
@@ -645,25 +643,31 @@ balanced_merge_kernel(const float *__restrict__ part_out, const float *__restric
 
 // ---------------------------------- LSE merge ----------------------------------------------
 // One CTA per (query head n, sequence b), one thread per output element h.
-__global__ void lse_merge_kernel(const float *__restrict__ part_out, const float *__restrict__ part_lse,
-                                 const int32_t *__restrict__ context_lens, int N, int H, int max_parts,
-                                 int part_blocks, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out)
+// One CTA merges R consecutive rows (query heads) of one sequence: R = 8 when their weights fit in
+// shared memory, else 1.  Each row's bits do not depend on R (merge_rows).
+template <int H, int R>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+lse_merge_kernel(const float *__restrict__ part_out, const float *__restrict__ part_lse,
+                 const int32_t *__restrict__ context_lens, int N, int max_parts, int part_blocks,
+                 __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out)
 {
-    extern __shared__ float wts[];  // [max_parts]
-    __shared__ float row_lse;
-    const int n = blockIdx.x, b = blockIdx.y, h = threadIdx.x;
-    const size_t bn = (size_t)b * N + n;
+    extern __shared__ float smem_f[];  // weights [R][np], then the warps' sums [kMergeWarps][R][H]
+    const int n0 = blockIdx.x * R, b = blockIdx.y, t = threadIdx.x;
+    const int nrows = min(R, N - n0);
+    const size_t bn0 = (size_t)b * N + n0;
     int ctx = context_lens[b];
     const int nb = ctx > 0 ? (ctx + kBlockSize - 1) / kBlockSize : 0;
     int np = (nb + part_blocks - 1) / part_blocks;
     if (np > max_parts) np = max_parts;
-    if (h < 32) {
-        const float L = lse_merge_weights(part_lse + bn * max_parts, np, wts, h);
-        if (h == 0) row_lse = L;
+    float *wts = smem_f;
+    float *red = smem_f + ((size_t)R * max_parts + 3) / 4 * 4;
+    for (int g = t >> 5; g < nrows; g += kMergeWarps) {
+        const float L = lse_merge_weights(part_lse + (bn0 + g) * max_parts, np, wts + g * np, t & 31);
+        if ((t & 31) == 0 && lse_out) lse_out[bn0 + g] = L;
     }
     __syncthreads();
-    if (h < H) out[bn * H + h] = __float2bfloat16_rn(lse_merge_value(wts, part_out + bn * max_parts * H + h, np, H));
-    if (h == 0 && lse_out) lse_out[bn] = row_lse;
+    merge_rows<H, R>(wts, np, nrows, part_out + bn0 * max_parts * H, (size_t)max_parts * H, red, out + bn0 * H, H, t,
+                     blockDim.x);
 }
 
 // ---------------------------------- launchers ----------------------------------------------
@@ -746,15 +750,33 @@ cudaError_t launch_balanced_merge(const float *part_out, const float *part_lse, 
     return cudaGetLastError();
 }
 
+template <int H, int R>
+static cudaError_t launch_lse_merge_t(const float *part_out, const float *part_lse, const int32_t *context_lens,
+                                      int B, int N, int max_parts, int part_blocks, uint16_t *out, float *lse_out,
+                                      cudaStream_t stream)
+{
+    const size_t smem = (((size_t)R * max_parts + 3) / 4 * 4 + (size_t)kMergeWarps * R * H) * sizeof(float);
+    static int cached[64] = {};
+    cudaError_t e = ensure_smem(lse_merge_kernel<H, R>, (int)smem, cached);
+    if (e != cudaSuccess) return e;
+    lse_merge_kernel<H, R><<<dim3((N + R - 1) / R, B), kMergeWarps * 32, smem, stream>>>(
+        part_out, part_lse, context_lens, N, max_parts, part_blocks, reinterpret_cast<__nv_bfloat16 *>(out), lse_out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_lse_merge(const float *part_out, const float *part_lse, const int32_t *context_lens,
                              int B, int N, int H, int max_parts, int part_blocks, uint16_t *out,
                              float *lse_out, cudaStream_t stream)
 {
-    const int threads = H < 32 ? 32 : H;
-    lse_merge_kernel<<<dim3(N, B), threads, (size_t)max_parts * sizeof(float), stream>>>(
-        part_out, part_lse, context_lens, N, H, max_parts, part_blocks,
-        reinterpret_cast<__nv_bfloat16 *>(out), lse_out);
-    return cudaGetLastError();
+    // eight rows per CTA while their weights stay within 32 KB
+    const bool eight = (int64_t)8 * max_parts <= 8192;
+    if (H == 128)
+        return eight ? launch_lse_merge_t<128, 8>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, out, lse_out, stream)
+                     : launch_lse_merge_t<128, 1>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, out, lse_out, stream);
+    if (H == 64)
+        return eight ? launch_lse_merge_t<64, 8>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, out, lse_out, stream)
+                     : launch_lse_merge_t<64, 1>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, out, lse_out, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv

@@ -75,8 +75,11 @@ struct AttnLayout {
     static constexpr int kStageBytes = 2 * kTileBytes;      // K tile then V tile
     static constexpr int kPipeBytes = S * kStageBytes;
     static constexpr int kMergeBytes = W * 8 * (H + 2) * 4;
-    // single-pass / partition kernel: the merge area reuses the drained pipeline
-    static constexpr int kDataBytes = kPipeBytes > kMergeBytes ? kPipeBytes : kMergeBytes;
+    // in-kernel partition merge: weights [G][parts] then the warps' sums [kMergeWarps][8][H]
+    static constexpr int kLseMergeBytes = kInKernelMergeWeights * 4 + kMergeWarps * 8 * H * 4;
+    // single-pass / partition kernel: the merge areas reuse the drained pipeline
+    static constexpr int kMergeMax = kMergeBytes > kLseMergeBytes ? kMergeBytes : kLseMergeBytes;
+    static constexpr int kDataBytes = kPipeBytes > kMergeMax ? kPipeBytes : kMergeMax;
     static constexpr int kBarOffset = kDataBytes;           // full[S], empty[S]
     static constexpr int kMiscOffset = kBarOffset + 2 * S * 8;  // slot_ok[S], abort, issued[P]
     // e4m3 with per-(block, head) scales: the (K, V) scales of each stage's tile, float2[S]
@@ -555,6 +558,63 @@ __device__ __forceinline__ float lse_merge_value(const float *w, const float *po
 #pragma unroll 4
     for (int q = 0; q < n; ++q) val += w[q] * __ldcg(po + (size_t)q * stride);
     return val;
+}
+
+// out[g][h] = sum_q w[g * n + q] * po[g * po_row + q * H + h] for nrows <= kMaxRows rows, in an
+// order that depends on nothing but n: warp w (< kMergeWarps) adds the partitions q = w,
+// w + kMergeWarps, ... in increasing q with fused multiply-adds, lane l holding the row's elements
+// [l * H / 32, (l + 1) * H / 32) from one vector load per partition (all of a warp's loads are
+// independent, so they are in flight together); the warps' sums, staged in red
+// [kMergeWarps][kMaxRows][H], are then added in warp order.  A CTA merging one row and one merging
+// eight give the same bits.  Needs kMergeWarps warps among the nthreads; ends with the rows written
+// (bf16) and a __syncthreads between the two phases.
+template <int H, int kMaxRows>
+__device__ __forceinline__ void merge_rows(const float *w, int n, int nrows, const float *po, size_t po_row,
+                                           float *red, __nv_bfloat16 *out, size_t out_row, int tid, int nthreads)
+{
+    constexpr int E = H / 32;
+    static_assert(E == 2 || E == 4, "H = 64 or 128");
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp < kMergeWarps) {
+        float acc[kMaxRows][E];
+#pragma unroll
+        for (int g = 0; g < kMaxRows; ++g)
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
+        for (int q = warp; q < n; q += kMergeWarps) {
+#pragma unroll
+            for (int g = 0; g < kMaxRows; ++g) {
+                if (g < nrows) {
+                    const float wq = w[g * n + q];
+                    const float *src = po + g * po_row + (size_t)q * H + lane * E;
+                    if constexpr (E == 4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                        acc[g][0] = __fmaf_rn(wq, v.x, acc[g][0]);
+                        acc[g][1] = __fmaf_rn(wq, v.y, acc[g][1]);
+                        acc[g][2] = __fmaf_rn(wq, v.z, acc[g][2]);
+                        acc[g][3] = __fmaf_rn(wq, v.w, acc[g][3]);
+                    } else {
+                        const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                        acc[g][0] = __fmaf_rn(wq, v.x, acc[g][0]);
+                        acc[g][1] = __fmaf_rn(wq, v.y, acc[g][1]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < kMaxRows; ++g)
+            if (g < nrows)
+#pragma unroll
+                for (int e = 0; e < E; ++e) red[(warp * kMaxRows + g) * H + lane * E + e] = acc[g][e];
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nrows * H; idx += nthreads) {
+        const int g = idx / H, h = idx - g * H;
+        float v = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < kMergeWarps; ++ww) v += red[(ww * kMaxRows + g) * H + h];
+        out[g * out_row + h] = __float2bfloat16_rn(v);
+    }
 }
 
 template <int S>

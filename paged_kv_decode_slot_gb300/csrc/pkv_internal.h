@@ -13,6 +13,12 @@ namespace pkv {
 // sequences per call.
 constexpr int kMaxBalancedSeqs = 1024;
 
+// The log-sum-exp merge of a row's partitions (merge_rows): kMergeWarps warps split the
+// partitions; the last partition CTA of a split runs it inside the attention kernel when the
+// G * parts weights fit in kInKernelMergeWeights floats, otherwise lse_merge_kernel does.
+constexpr int kMergeWarps = 6;
+constexpr int kInKernelMergeWeights = 8192;
+
 struct AttnParams {
     const uint16_t *q;             // [B][N][H] bf16
     const int32_t *block_tables;   // [B][max_nb]

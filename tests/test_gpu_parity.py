@@ -390,3 +390,24 @@ def test_context_fills_the_table(pkv, oracle, part_blocks):
     kc, vc = appended_host_cache(oracle, w)
     ref, _ = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
     assert_close(out_f64(out), ref, f"full tables pb={part_blocks}")
+
+
+@pytest.mark.parametrize("part_blocks,H", [(3, 128), (1, 128), (2, 64), (5, 64)])
+def test_in_kernel_merge_equals_separate_merge(pkv, oracle, part_blocks, H):
+    """The last partition CTA's merge (inside the split launch) and lse_merge_kernel (the partials
+    export followed by pkv_lse_merge) give the same bits: one merge order per row, whichever
+    kernel runs it and however many rows that kernel merges at once."""
+    w = gen.make_workload(f"merge_same_{H}", 152, 16, 4, H, [1, 16, 17, 300, 1000, 4000])
+    d = _post_append_device(pkv, oracle, w)
+    out_k, lse_k = _splitk(pkv, w, d, part_blocks)
+    P = pkv.max_partitions_for(w.max_blocks, part_blocks)
+    part_out = torch.empty(w.B, w.N, P, w.H, dtype=torch.float32, device="cuda")
+    part_lse = torch.empty(w.B, w.N, P, dtype=torch.float32, device="cuda")
+    pkv.check(pkv.pkv_decode_attn_partitions(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                             d["context_lens"], w.scale, part_blocks, part_out, part_lse))
+    out_m = torch.empty_like(d["q"])
+    lse_m = torch.empty(w.B, w.N, dtype=torch.float32, device="cuda")
+    pkv.check(pkv.pkv_lse_merge(part_out, part_lse, d["context_lens"], part_blocks, out_m, lse_m))
+    torch.cuda.synchronize()
+    assert torch.equal(out_k.view(torch.int16), out_m.view(torch.int16))
+    assert torch.equal(lse_k, lse_m)
