@@ -33,7 +33,8 @@ FALLBACK_HBM_GBS = 6800.0     # copy bandwidth of an earlier GB300 measurement
 DEFAULT_CONFIG = "l3_8b_b64"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 ATTN_SOURCES = [os.path.join(ROOT, "paged_kv_decode_slot_gb300", "csrc", f)
-                for f in ("pkv_attn.cu", "pkv_attn_common.cuh", "pkv_device.cuh", "pkv_internal.h")]
+                for f in ("pkv_attn.cu", "pkv_attn_common.cuh", "pkv_device.cuh", "pkv_internal.h",
+                          "pkv_attn_cols.cu", "pkv_cols.cuh", "pkv_attn_tc.cu", "pkv_tcgen05.cuh")]
 
 
 def _dist_env():
