@@ -153,21 +153,6 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     volatile int *issued_count = abort_flag + 1;  // [kTcProducers]
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(issued_count + kTcProducers);
 
-    // The CTA's q rows into the K-major, 128B-swizzled A operand (rows past ncols are zero).
-    for (int idx = threadIdx.x; idx < kColsPerCta * (H / 8); idx += kTcThreads) {
-        const int r = idx / (H / 8), u = idx - r * (H / 8);  // row, 16-byte unit of the row
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (r < wk.ncols) {
-            int64_t row;
-            int vis;
-            col_of(p, wk, r, row, vis);
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(p.q + row * H + 8 * u);
-            v = make_uint4(__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3));
-        }
-        const int half = u >> 3, cu = u & 7;
-        st_shared_v4(q_u32 + half * L::kQHalfBytes + (r >> 3) * 1024 + (r & 7) * 128 + ((cu ^ (r & 7)) << 4), v);
-    }
-    fence_proxy_async_shared();
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int q = 0; q < kTcProducers; ++q) issued_count[q] = 0;
@@ -181,15 +166,49 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         mbar_init(bar_fin, 2);  // one commit from each MMA-issuing warp
         fence_barrier_init();
     }
-    if (warp == 1) {
-        tmem_alloc(smem_u32((const void *)tmem_slot), kTcCols);
-        tmem_relinquish();
+    __syncthreads();  // the barriers are ready: the producers start loading at once
+
+    // Meanwhile warps 0-2 put the CTA's q rows into the K-major, 128B-swizzled A operand (rows
+    // past ncols are zero) and warp 1 allocates the tensor memory; they meet at a named barrier.
+    uint32_t tm_o = 0, tm_s = 0;  // O at tm_o (lane 0, first allocated column), S/P at tm_s, tm_s + 64
+    if (warp < 3) {
+        // all of a thread's loads first (one round trip), then the stores
+        constexpr int kUnits = kColsPerCta * (H / 8), kPer = (kUnits + 95) / 96;
+        uint4 v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int idx = threadIdx.x + 96 * k;
+            const int r = idx / (H / 8), u = idx - r * (H / 8);  // row, 16-byte unit of the row
+            v[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (idx < kUnits && r < wk.ncols) {
+                int64_t row;
+                int vis;
+                col_of(p, wk, r, row, vis);
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(p.q + row * H + 8 * u);
+                v[k] = make_uint4(__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3));
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int idx = threadIdx.x + 96 * k;
+            if (idx < kUnits) {
+                const int r = idx / (H / 8), u = idx - r * (H / 8);
+                const int half = u >> 3, cu = u & 7;
+                st_shared_v4(q_u32 + half * L::kQHalfBytes + (r >> 3) * 1024 + (r & 7) * 128 + ((cu ^ (r & 7)) << 4),
+                             v[k]);
+            }
+        }
+        fence_proxy_async_shared();
+        if (warp == 1) {
+            tmem_alloc(smem_u32((const void *)tmem_slot), kTcCols);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        asm volatile("bar.sync 1, 96;" ::: "memory");  // warps 0-2
+        tc_fence_after();
+        tm_o = *tmem_slot;
+        tm_s = tm_o + H;
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tm_o = *tmem_slot;  // lane 0, first allocated column
-    const uint32_t tm_s = tm_o + H;    // S/P buffers: tm_s and tm_s + 64
 
     if (warp >= 3) {
         // ------------------------------ producer warps ------------------------------
