@@ -33,8 +33,10 @@ FALLBACK_HBM_GBS = 6800.0     # copy bandwidth of an earlier GB300 measurement
 DEFAULT_CONFIG = "l3_8b_b64"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 ATTN_SOURCES = [os.path.join(ROOT, "paged_kv_decode_slot_gb300", "csrc", f)
-                for f in ("pkv_attn.cu", "pkv_attn_common.cuh", "pkv_device.cuh", "pkv_internal.h",
-                          "pkv_attn_cols.cu", "pkv_cols.cuh", "pkv_attn_tc.cu", "pkv_tcgen05.cuh")]
+                for f in ("pkv_attn.cu", "pkv_attn_common.cuh", "pkv_device.cuh", "pkv_internal.h")]
+# the column kernels (several new tokens, shared prefixes) build on the same headers
+COLS_SOURCES = ATTN_SOURCES + [os.path.join(ROOT, "paged_kv_decode_slot_gb300", "csrc", f)
+                               for f in ("pkv_attn_cols.cu", "pkv_cols.cuh", "pkv_attn_tc.cu", "pkv_tcgen05.cuh")]
 
 
 def _dist_env():
@@ -69,9 +71,11 @@ def load_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def attn_source_hash() -> str:
+def attn_source_hash(files=None) -> str:
+    """Hash of the sources of the timed attention kernel (the column kernels' for workload keys
+    with several new tokens or the shared-prefix cascade)."""
     h = hashlib.sha256()
-    for p in ATTN_SOURCES:
+    for p in files or ATTN_SOURCES:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -81,7 +85,8 @@ def recorded_traffic(config: str):
     """dram bytes per attention launch from an ncu capture of the current kernel source, else None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    want = attn_source_hash()
+    cols = "+T" in config or "+prefix" in config
+    want = attn_source_hash(COLS_SOURCES if cols else None)
     with open(TRAFFIC_FILE, encoding="utf-8") as f:
         for line in f:
             parts = line.split()
@@ -554,8 +559,8 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--partition-blocks", type=int, default=None)
