@@ -393,6 +393,23 @@ def run_ours(args):
     else:
         step = DecodeStep(q, kn, vn, kc, vc, bt, cl, w.scale, plan=plan, err_flag=err,
                           fused=not args.unfused)
+    if args.layers > 1:
+        # a multi-layer step: every layer its own copy of the pools and of q / k_new / v_new,
+        # the same block tables and context lengths (the same sequences)
+        if args.tokens > 1 or args.attn != "auto" or args.unfused:
+            raise SystemExit("--layers runs the fused one-token step (bf16 or e4m3)")
+        from paged_kv_decode_slot_gb300.step import LayerStack
+        layers = [step]
+        for _ in range(args.layers - 1):
+            if args.kv == "fp8":
+                layers.append(DecodeStepFp8(step.q.clone(), step.k_new.clone(), step.v_new.clone(),
+                                            step.k_cache.clone(), step.v_cache.clone(), step.k_scale,
+                                            step.v_scale, bt, cl, w.scale, plan=plan, err_flag=err))
+            else:
+                layers.append(DecodeStep(step.q.clone(), step.k_new.clone(), step.v_new.clone(),
+                                         step.k_cache.clone(), step.v_cache.clone(), bt, cl, w.scale,
+                                         plan=plan, err_flag=err))
+        step = LayerStack(layers)
     stream = torch.cuda.Stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.zeros(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
@@ -405,7 +422,7 @@ def run_ours(args):
         # timed step starts with an L2 that holds neither its inputs nor write-back debt.
         flush_w.add_(1.0)
         torch.sum(flush_r, dim=0, keepdim=True, out=flush_sink)
-    nbytes = step_bytes(w, args.kv, args.tokens, args.fp8_scales)
+    nbytes = {k: v * args.layers for k, v in step_bytes(w, args.kv, args.tokens, args.fp8_scales).items()}
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -517,14 +534,14 @@ def run_ours(args):
         "us_per_step_median": statistics.median(step_ms) * 1e3,
         "us_per_step_best": min(step_ms) * 1e3,
         "attn_us": mean_attn * 1e3,
-        "attn_calls_per_s": 1e3 / mean_attn,
-        "kv_gbs": w.kv_bytes() / (mean_attn * 1e-3) / 1e9,
+        "attn_calls_per_s": args.layers * 1e3 / mean_attn,
+        "kv_gbs": args.layers * w.kv_bytes() / (mean_attn * 1e-3) / 1e9,
         "frac_of_8tbs": achieved / (TARGET_HBM_TBS * 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "kernel": kernel_label(args, plan, step)
+                     "kernel": kernel_label(args, plan, getattr(step, "layers", [step])[0])
                                + (" (append fused)" if step.fused else ""),
-                     "bytes_per_launch": attn_bytes,
+                     "bytes_per_launch": attn_bytes // args.layers,
                      "traffic": recorded_traffic(traffic_key(args))},
         "e2e": {"value": whole_job_gbs(ws, nbytes["step"], e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -539,15 +556,19 @@ def run_ours(args):
     }
     if args.tokens > 1:
         line["config"]["new_tokens_per_seq"] = args.tokens
+    if args.layers > 1:
+        line["config"]["layers"] = args.layers
+        line["us_per_layer"] = mean_step * 1e3 / args.layers
+        line["graph"]["us_per_layer"] = line["graph"]["us_per_step"] / args.layers
     if args.attn == "prefix":
         line["config"]["prefix_groups"] = "one group of the whole batch sharing its full prefix blocks"
     if args.kv == "fp8":
         line["config"]["kv_cache"] = ("e4m3, per-KV-head scales (amax / 448)" if args.fp8_scales == "head"
                                       else "e4m3, per-(block, KV head) scales (amax / 448)")
-        line["kv_gbs"] = w.kv_bytes() / 2 / (mean_attn * 1e-3) / 1e9
-        line["kv_gbs_bf16_equivalent"] = w.kv_bytes() / (mean_attn * 1e-3) / 1e9
+        line["kv_gbs"] = args.layers * w.kv_bytes() / 2 / (mean_attn * 1e-3) / 1e9
+        line["kv_gbs_bf16_equivalent"] = args.layers * w.kv_bytes() / (mean_attn * 1e-3) / 1e9
     if w.unique_tokens is not None:
-        line["kv_gbs_logical"] = w.kv_bytes() / (mean_attn * 1e-3) / 1e9
+        line["kv_gbs_logical"] = args.layers * w.kv_bytes() / (mean_attn * 1e-3) / 1e9
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = run_cpu_baseline(w)
     if rank == 0:
@@ -569,6 +590,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv", choices=("bf16", "fp8"), default="bf16",
                     help="KV cache element type (fp8 = e4m3 codes with per-KV-head scales)")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="attention layers per step (each its own pools; the same sequences)")
     ap.add_argument("--fp8-scales", choices=("head", "block"), default="head",
                     help="with --kv fp8: one scale per KV head, or one per (physical block, KV head)")
     ap.add_argument("--tokens", type=int, default=1,

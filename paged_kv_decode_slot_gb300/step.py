@@ -384,3 +384,78 @@ class PrefixDecodeStep:
 
     def inputs(self):
         return [getattr(self, n) for n in self.input_names()]
+
+
+class LayerStack:
+    """One decode step of a model with several attention layers: the same sequences (block tables
+    and context lengths) in every layer, each layer with its own pools and its own q, k_new and
+    v_new.  ``run`` launches the layers' fused steps in order (one launch each, two with a
+    separate merge); captured in a CUDA graph (``StepGraph``) the whole multi-layer step replays
+    as one graph launch.  Attribute names ``"<name>.<layer>"`` (``"q.3"``) reach one layer's
+    inputs, ``block_tables`` / ``context_lens`` are shared, ``out`` / ``lse`` are the last
+    layer's; so ``PackedInputs(stack, stack.input_names())`` packs every layer's inputs into one
+    host-to-device copy per step."""
+
+    _SHARED = ("block_tables", "context_lens")
+
+    def __init__(self, layers):
+        layers = list(layers)
+        if not layers or not all(getattr(l, "fused", False) for l in layers):
+            raise ValueError("a layer stack needs fused decode steps")
+        object.__setattr__(self, "layers", layers)
+        object.__setattr__(self, "plan", layers[0].plan)
+        object.__setattr__(self, "fused", True)
+
+    def __getattr__(self, name):
+        if "." in name:
+            attr, idx = name.rsplit(".", 1)
+            return getattr(self.layers[int(idx)], attr)
+        if name in self._SHARED:
+            return getattr(self.layers[0], name)
+        if name in ("out", "lse", "slot_mapping"):
+            return getattr(self.layers[-1], name)
+        raise AttributeError(name)
+
+    def __setattr__(self, name, value):
+        if "." in name:
+            attr, idx = name.rsplit(".", 1)
+            setattr(self.layers[int(idx)], attr, value)
+        elif name in self._SHARED:
+            for layer in self.layers:
+                setattr(layer, name, value)
+        else:
+            object.__setattr__(self, name, value)
+
+    def run(self, stream=None) -> None:
+        for layer in self.layers:
+            layer.run(stream)
+
+    def launches_per_step(self) -> int:
+        return sum(layer.launches_per_step() for layer in self.layers)
+
+    def input_names(self):
+        return self._SHARED + tuple(f"{n}.{i}" for i in range(len(self.layers)) for n in ("q", "k_new", "v_new"))
+
+    def inputs(self):
+        return [getattr(self, n) for n in self.input_names()]
+
+
+class StepGraph:
+    """A step (or a LayerStack) captured once into a CUDA graph and replayed: the launches of all
+    its kernels cost one graph launch.  The step is run once eagerly first (kernel attributes are
+    set on first use, outside the capture); a decode step is idempotent for fixed inputs (the same
+    rows land in the same slots), so that run changes nothing the replay would not."""
+
+    def __init__(self, step, stream=None):
+        dev = step.out.device
+        self.step = step
+        self.stream = stream or torch.cuda.Stream(dev)
+        with torch.cuda.stream(self.stream):
+            step.run(self.stream)
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            step.run(self.stream)
+
+    def replay(self) -> None:
+        self.graph.replay()
