@@ -28,11 +28,14 @@
  *                     slot = block * 16 + offset, negative = skip the token
  * Supported shapes: block_size 16, H in {64, 128}, G = N/K in {1, 2, 4, 8}.
  *
- * Ownership: every pointer is caller-owned device memory (k_new/v_new/q etc.
- * must be in the same device's global memory); the library allocates nothing
- * and keeps no state between calls besides cached device attributes (and the
- * static scratch of pkv_decode_attn_splitk_noalloc, described there).  Calls
- * are asynchronous on the given stream (0 = the legacy default stream).
+ * Ownership: every pointer is caller-owned memory the current device can address: the KV
+ * pools (read by TMA) and the workspaces must be device memory; every other buffer (q, out,
+ * lse, k_new, v_new, block tables, context lengths, slot mappings) may also be pinned
+ * (page-locked) host memory, which the kernels read and write in place -- on a GB300 over
+ * NVLink-C2C, so a step's inputs and outputs need no separate copies.  The library allocates
+ * nothing and keeps no state between calls besides cached device attributes (and the static
+ * scratch of pkv_decode_attn_splitk_noalloc, described there).  Calls are asynchronous on the
+ * given stream (0 = the legacy default stream).
  *
  * Errors: each call returns a pkv_status.  Host-side validation happens
  * before anything is launched.  Bad values that only the device sees (a

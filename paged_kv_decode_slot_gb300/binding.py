@@ -106,6 +106,12 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+# The pools and the workspaces must be device memory (the pools are read by TMA).  Every other
+# argument may also be pinned (page-locked) host memory, which the kernels read and write in place
+# (on a GB300 over NVLink-C2C) -- a step's inputs and outputs need no copies then.
+_DEVICE_ONLY = ("k_cache", "v_cache", "workspace", "part_out", "part_lse")
+
+
 def _need(t, dtype, ndim, name):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -113,8 +119,8 @@ def _need(t, dtype, ndim, name):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_cuda and (name in _DEVICE_ONLY or not t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" + ("" if name in _DEVICE_ONLY else " or pinned host memory"))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
 

@@ -122,7 +122,10 @@ def plan_attention(num_seqs: int, num_kv_heads: int, max_blocks_per_seq: int, nu
 
 
 class DecodeStep:
-    """Device-resident state of one decode step over a paged cache (all torch CUDA tensors).
+    """State of one decode step over a paged cache: the pools and workspace on the GPU; q,
+    k_new, v_new, block tables and context lengths on the GPU or in pinned host memory (then
+    read in place by the kernel); out / lse / slot_mapping are allocated on the GPU and may be
+    replaced by pinned host tensors.
 
     q [B, N, H] bf16; k_new/v_new [B, K, H] bf16; k_cache/v_cache [nb, 16, K, H] bf16;
     block_tables [B, max_blocks] int32; context_lens [B] int32 (including the new token).
@@ -134,7 +137,7 @@ class DecodeStep:
         self.k_cache, self.v_cache = k_cache, v_cache
         self.block_tables, self.context_lens = block_tables, context_lens
         self.scale = float(scale)
-        dev = q.device
+        dev = k_cache.device  # the pools' GPU (q and the other inputs may be pinned host memory)
         nseq = q.shape[0]
         self.num_blocks = k_cache.shape[0]
         if plan is None:
@@ -142,7 +145,7 @@ class DecodeStep:
             plan = plan_attention(nseq, k_cache.shape[2], block_tables.shape[1], sms)
         self.plan = plan
         self.slot_mapping = torch.empty(nseq, dtype=torch.int64, device=dev)
-        self.out = torch.empty_like(q)
+        self.out = torch.empty(tuple(q.shape), dtype=q.dtype, device=dev)
         self.lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev)
         self.err_flag = err_flag
         # fused: one pkv_decode_step call (single pass or fixed partitions) does it all
@@ -217,7 +220,7 @@ class DecodeStepFp8:
         self.k_scale, self.v_scale = k_scale, v_scale
         self.block_tables, self.context_lens = block_tables, context_lens
         self.scale = float(scale)
-        dev = q.device
+        dev = k_cache8.device  # the pools' GPU (q and the other inputs may be pinned host memory)
         nseq = q.shape[0]
         if plan is None or plan.mode == "balanced":
             sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -225,7 +228,7 @@ class DecodeStepFp8:
         self.plan = plan
         self.fused = True
         self.slot_mapping = torch.empty(nseq, dtype=torch.int64, device=dev)
-        self.out = torch.empty_like(q)
+        self.out = torch.empty(tuple(q.shape), dtype=q.dtype, device=dev)
         self.lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev)
         self.err_flag = err_flag
         self.workspace = None
@@ -270,7 +273,7 @@ class MultiTokenStep:
         self.k_cache, self.v_cache = k_cache, v_cache
         self.block_tables, self.context_lens = block_tables, context_lens
         self.scale = float(scale)
-        dev = q.device
+        dev = k_cache.device  # the pools' GPU (q and the other inputs may be pinned host memory)
         nseq, T, N, H = q.shape
         K = k_cache.shape[2]
         self.T = T
@@ -281,7 +284,7 @@ class MultiTokenStep:
                                    partition_blocks=partition_blocks)
         self.fused = False
         self.slot_mapping = torch.empty(nseq, T, dtype=torch.int64, device=dev)
-        self.out = torch.empty_like(q)
+        self.out = torch.empty(tuple(q.shape), dtype=q.dtype, device=dev)
         self.lse = torch.empty(nseq, T, N, dtype=torch.float32, device=dev)
         self.err_flag = err_flag
         self.workspace = None
@@ -345,13 +348,13 @@ class PrefixDecodeStep:
         self.partition_blocks = int(partition_blocks)
         self.prefix_partition_blocks = int(prefix_partition_blocks)
         self.scale = float(scale)
-        dev = q.device
+        dev = k_cache.device  # the pools' GPU (q and the other inputs may be pinned host memory)
         nseq, N, H = q.shape
         self.num_blocks = k_cache.shape[0]
         self.plan = AttentionPlan("prefix", self.partition_blocks, 0)
         self.fused = False
         self.slot_mapping = torch.empty(nseq, dtype=torch.int64, device=dev)
-        self.out = torch.empty_like(q)
+        self.out = torch.empty(tuple(q.shape), dtype=q.dtype, device=dev)
         self.lse = torch.empty(nseq, N, dtype=torch.float32, device=dev)
         self.err_flag = err_flag
         nbytes = B.pkv_prefix_workspace_bytes(nseq, N, H, block_tables.shape[1], self.max_prefix_blocks,

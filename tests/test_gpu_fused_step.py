@@ -185,3 +185,36 @@ def test_layer_stack_graph_replay_equals_eager(pkv, oracle):
         oracle.append(kn, vn, slots, kc2, vc2)
         ref, _ = oracle.decode(q, kc2, vc2, base.block_tables, base.context_lens, base.scale)
         assert_close(out_f64(b.out), ref, f"layer {l}")
+
+
+@pytest.mark.parametrize("part_blocks", [0, 32])
+def test_step_with_host_resident_inputs_and_outputs(pkv, oracle, part_blocks):
+    """q, k_new, v_new, block tables, context lengths, out, lse and the slot mapping in pinned host
+    memory (read and written by the kernel in place), the pools in HBM: the same bits as with
+    every buffer on the device."""
+    from paged_kv_decode_slot_gb300.step import AttentionPlan, DecodeStep
+    w = gen.make_workload("hostio", 181, 32, 8, 128, [1, 17, 300, 2000, 64, 900])
+    P = pkv.max_partitions_for(w.max_blocks, part_blocks) if part_blocks else 1
+    plan = AttentionPlan("split", part_blocks, P) if part_blocks else AttentionPlan("single")
+
+    def pinned(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a).view(dt)).pin_memory()
+
+    d = upload(w)
+    dev_step = DecodeStep(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["block_tables"],
+                          d["context_lens"], w.scale, plan=plan)
+    dev_step.run()
+    h = upload(w)
+    host_step = DecodeStep(pinned(w.q, np.int16).view(torch.bfloat16), pinned(w.k_new, np.int16).view(torch.bfloat16),
+                           pinned(w.v_new, np.int16).view(torch.bfloat16), h["k_cache"], h["v_cache"],
+                           pinned(w.block_tables, np.int32), pinned(w.context_lens, np.int32), w.scale, plan=plan)
+    host_step.out = torch.empty(tuple(dev_step.out.shape), dtype=torch.bfloat16).pin_memory()
+    host_step.lse = torch.empty(tuple(dev_step.lse.shape), dtype=torch.float32).pin_memory()
+    host_step.slot_mapping = torch.empty(tuple(dev_step.slot_mapping.shape), dtype=torch.int64).pin_memory()
+    host_step.run()
+    torch.cuda.synchronize()
+    assert torch.equal(dev_step.out.cpu().view(torch.int16), host_step.out.view(torch.int16))
+    assert torch.equal(dev_step.lse.cpu(), host_step.lse)
+    assert torch.equal(dev_step.slot_mapping.cpu(), host_step.slot_mapping)
+    assert torch.equal(d["k_cache"].view(torch.int16), h["k_cache"].view(torch.int16))  # NaN-poisoned pools:
+    assert torch.equal(d["v_cache"].view(torch.int16), h["v_cache"].view(torch.int16))  # compare the bits
