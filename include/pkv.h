@@ -362,6 +362,18 @@ int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_
                           void *workspace, size_t workspace_bytes, int32_t *err_flag,
                           pkv_stream_t stream);
 
+/* Limit (ns, default 2e9) of every bounded wait inside the attention kernels, for the calls
+   launched after it is set (process-wide); returns the previous limit (0 sets 1 ns).  An
+   expired wait sets PKV_FLAG_TIMEOUT and voids the unit's result: the kernel stops issuing,
+   drains the copies it started, releases what it holds and returns, and a later call with the
+   default limit runs normally.  Lowering it is a way to exercise those paths. */
+uint64_t pkv_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Self-test of the bounded waits: one warp waits, with the attention kernels' bounded wait, on
+   an mbarrier that nothing ever completes; after the current wait limit it gives up and sets
+   PKV_FLAG_TIMEOUT in err_flag (device or pinned host int32, required).  No fault, no hang. */
+int pkv_check_wait_expiry(int32_t *err_flag, pkv_stream_t stream);
+
 /* 1 if pkv_decode_attn_multi with these sizes runs its tcgen05 column kernel, 0 if the mma.sync
    one (no GPU work; the answer assumes the half-major tensor-map layout, which the driver
    accepted on every GB300 here -- if it were refused the call would fall back to mma.sync). */

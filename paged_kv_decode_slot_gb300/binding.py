@@ -428,6 +428,22 @@ _lib.pkv_slot_mapping_multi.argtypes = [_P, _I32, _P, _I32, _I32, _I32, _P, _P, 
 _lib.pkv_decode_attn_multi.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, ctypes.c_float, _P,
                                        _P, CacheDesc, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
 _lib.pkv_multi_uses_tcgen05.argtypes = [_I32, _I32, _I32, _I32]
+_lib.pkv_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+_lib.pkv_set_wait_limit_ns.restype = ctypes.c_uint64
+
+
+_lib.pkv_check_wait_expiry.argtypes = [_P, _P]
+
+
+def pkv_check_wait_expiry(err_flag, stream=None) -> int:
+    """One bounded wait that cannot complete: sets PKV_FLAG_TIMEOUT after the current limit."""
+    _need(err_flag, torch.int32, 1, "err_flag")
+    return _lib.pkv_check_wait_expiry(_ptr(err_flag), _stream(stream))
+
+
+def pkv_set_wait_limit_ns(limit_ns: int) -> int:
+    """Limit of every bounded in-kernel wait for later calls (default 2 s); returns the previous."""
+    return int(_lib.pkv_set_wait_limit_ns(int(limit_ns)))
 _lib.pkv_copy_blocks.argtypes = [_P, _P, _P, _I32, CacheDesc, _I32, _P, _P]
 _lib.pkv_prefix_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32, _I32]
 _lib.pkv_prefix_workspace_bytes.restype = ctypes.c_size_t

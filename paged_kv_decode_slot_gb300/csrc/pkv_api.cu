@@ -2,6 +2,7 @@
 // kernel launches.  Every entry point validates its arguments before launching anything and
 // returns a pkv_status; device-detected errors go to the caller's err_flag.
 #include <algorithm>
+#include <atomic>
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -112,6 +113,8 @@ CUresult encode_kv_map(CUtensorMap *map, const void *base, const pkv_cache_desc 
 
 int g_tok_major = -1;  // layout the driver accepted first (-1: not yet known)
 std::mutex g_layout_mu;
+// limit of every bounded wait inside the attention kernels (pkv_set_wait_limit_ns)
+std::atomic<uint64_t> g_wait_ns{pkv::kWaitLimitNs};
 
 int make_kv_maps(CUtensorMap *tk, CUtensorMap *tv, const void *k, const void *v,
                  const pkv_cache_desc &d, int *tok_major)
@@ -176,6 +179,7 @@ pkv::AttnParams params_of(const AttnArgs &a, int tok_major)
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.tok_major = tok_major;
     p.err_flag = a.err_flag;
+    p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     return p;
 }
 
@@ -856,6 +860,7 @@ pkv::ColsParams cols_params_of(const AttnArgs &a, int tok_major)
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.tok_major = tok_major;
     p.err_flag = a.err_flag;
+    p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     return p;
 }
 
@@ -981,6 +986,18 @@ PKV_EXPORT int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache,
     // rows of one sequence: its T tokens x N heads, all with the sequence's context length
     return pkv_lse_merge(part_out, part_lse, context_lens, num_seqs, num_new * num_q_heads,
                          cache.head_dim, max_partitions, partition_blocks, out, lse_out, stream);
+}
+
+PKV_EXPORT uint64_t pkv_set_wait_limit_ns(uint64_t limit_ns)
+{
+    return g_wait_ns.exchange(limit_ns == 0 ? 1 : limit_ns);
+}
+
+PKV_EXPORT int pkv_check_wait_expiry(int32_t *err_flag, pkv_stream_t stream)
+{
+    if (!err_flag) return PKV_ERR_NULL;
+    cudaError_t e = pkv::launch_wait_expiry(g_wait_ns.load(std::memory_order_relaxed), err_flag, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "wait-expiry self-test launch");
 }
 
 PKV_EXPORT int pkv_multi_uses_tcgen05(int32_t num_new, int32_t num_q_heads, int32_t num_kv_heads,

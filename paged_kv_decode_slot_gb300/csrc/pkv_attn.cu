@@ -189,7 +189,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
             [&](int64_t i, int bid, bool ok, float2 sc) {
                 return produce_tile<H, S, kFp8>(i, kvh, bid, ok, base_u32, bar_full, bar_empty,
                                                 slot_ok, abort_flag, &tm_k, &tm_v, p.tok_major,
-                                                p.err_flag, bscale ? stage_sc : nullptr, sc);
+                                                p.err_flag, p.wait_ns, bscale ? stage_sc : nullptr, sc);
             },
             [&](int bid) {
                 if (!bscale) return make_float2(0.f, 0.f);
@@ -220,8 +220,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
                 const int i2 = i + kConsumerWarps;
                 const bool has2 = i2 < nblk;
                 const int s1 = i % S, s2 = i2 % S;
-                bool ok = mbar_wait_bounded(bar_full + 8 * s1, (i / S) & 1, abort_flag, kWaitLimitNs);
-                if (ok && has2) ok = mbar_wait_bounded(bar_full + 8 * s2, (i2 / S) & 1, abort_flag, kWaitLimitNs);
+                bool ok = mbar_wait_bounded(bar_full + 8 * s1, (i / S) & 1, abort_flag, p.wait_ns);
+                if (ok && has2) ok = mbar_wait_bounded(bar_full + 8 * s2, (i2 / S) & 1, abort_flag, p.wait_ns);
+                ok = __all_sync(0xFFFFFFFFu, ok);  // lanes may differ at the deadline: the warp agrees
                 if (!ok) {
                     if (!*abort_flag) set_flag(p.err_flag, PKV_FLAG_TIMEOUT);
                     *abort_flag = 1;
@@ -267,7 +268,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
         } else
         for (int i = warp; i < nblk; i += kConsumerWarps) {
             const int s = i % S;
-            if (!mbar_wait_bounded(bar_full + 8 * s, (i / S) & 1, abort_flag, kWaitLimitNs)) {
+            // lanes may differ at the deadline: the warp agrees before its collective MMA work
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_full + 8 * s, (i / S) & 1, abort_flag, p.wait_ns))) {
                 if (!*abort_flag) set_flag(p.err_flag, PKV_FLAG_TIMEOUT);
                 *abort_flag = 1;
                 break;
@@ -486,7 +488,7 @@ attn_balanced_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         const int64_t issued = run_producer<P>(
             pw, lane, n, lookup, p.num_blocks, p.err_flag, [&](int64_t i, int bid, bool ok, float2) {
                 return produce_tile<H, S>(i, kvh, bid, ok, base_u32, bar_full, bar_empty, slot_ok,
-                                          abort_flag, &tm_k, &tm_v, p.tok_major, p.err_flag);
+                                          abort_flag, &tm_k, &tm_v, p.tok_major, p.err_flag, p.wait_ns);
             });
         if (lane == 0) issued_count[pw] = issued;
     } else {
@@ -509,8 +511,8 @@ attn_balanced_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             int64_t i = ibeg + (int64_t)((warp - (int)(ibeg % W) + W) % W);
             for (; i < iend && !aborted; i += W) {
                 const int s = (int)(i % S);
-                if (!mbar_wait_bounded(bar_full + 8 * s, (uint32_t)((i / S) & 1), abort_flag,
-                                       kWaitLimitNs)) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_full + 8 * s, (uint32_t)((i / S) & 1),
+                                                               abort_flag, p.wait_ns))) {
                     if (!*abort_flag) set_flag(p.err_flag, PKV_FLAG_TIMEOUT);
                     *abort_flag = 1;
                     aborted = true;

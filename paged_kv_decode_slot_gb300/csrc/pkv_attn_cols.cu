@@ -177,7 +177,7 @@ attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             pw, lane, nblk, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, p.err_flag,
             [&](int64_t i, int bid, bool ok, float2) {
                 return produce_tile<H, S>(i, wk.kvh, bid, ok, base_u32, bar_full, bar_empty, slot_ok,
-                                          abort_flag, &tm_k, &tm_v, p.tok_major, p.err_flag);
+                                          abort_flag, &tm_k, &tm_v, p.tok_major, p.err_flag, p.wait_ns);
             });
         if (lane == 0) issued_count[pw] = (int)issued;
     } else {
@@ -204,7 +204,8 @@ attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         acc_reset<H>(acc);
         for (int i = r; i < nblk; i += R) {
             const int s = i % S;
-            if (!mbar_wait_bounded(bar_full + 8 * s, (i / S) & 1, abort_flag, kWaitLimitNs)) {
+            // lanes may differ at the deadline: the warp agrees before its collective MMA work
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_full + 8 * s, (i / S) & 1, abort_flag, p.wait_ns))) {
                 if (!*abort_flag) set_flag(p.err_flag, PKV_FLAG_TIMEOUT);
                 *abort_flag = 1;
                 break;

@@ -635,14 +635,13 @@ __device__ __forceinline__ bool produce_tile(int64_t i, int kvh, int bid, bool o
                                              uint32_t bar_full, uint32_t bar_empty,
                                              volatile int *slot_ok, volatile int *abort_flag,
                                              const CUtensorMap *tm_k, const CUtensorMap *tm_v,
-                                             int tok_major, int32_t *err_flag,
+                                             int tok_major, int32_t *err_flag, uint64_t wait_ns,
                                              volatile float2 *stage_scale = nullptr, float2 scales = {})
 {
     using L = AttnLayout<H, S, kConsumerWarps, kProducers, kFp8 ? 1 : 2>;
     const int s = (int)(i % S);
     if (i >= S &&
-        !mbar_wait_bounded(bar_empty + 8 * s, (uint32_t)(((i / S) & 1) ^ 1), abort_flag,
-                           kWaitLimitNs)) {
+        !mbar_wait_bounded(bar_empty + 8 * s, (uint32_t)(((i / S) & 1) ^ 1), abort_flag, wait_ns)) {
         if (!*abort_flag) set_flag(err_flag, PKV_FLAG_TIMEOUT);
         *abort_flag = 1;
         return false;

@@ -80,13 +80,13 @@ template <int H>
 __device__ __forceinline__ bool produce_tile_tc(int64_t i, int kvh, int bid, bool ok, uint32_t kreg, uint32_t vreg,
                                                 uint32_t bar_full, uint32_t bar_free, volatile int *slot_ok,
                                                 volatile int *abort_flag, const CUtensorMap *tm_kh,
-                                                const CUtensorMap *tm_v, int32_t *err_flag)
+                                                const CUtensorMap *tm_v, int32_t *err_flag, uint64_t wait_ns)
 {
     using L = TcLayout<H>;
     const int s = (int)(i % kTcStages);
     const int slot = (int)((i / kTcGroupTiles) % L::kGroupSlots);
     if (i >= kTcStages &&
-        !mbar_wait_bounded(bar_free + 8 * slot, (uint32_t)(((i / kTcStages) & 1) ^ 1), abort_flag, kWaitLimitNs)) {
+        !mbar_wait_bounded(bar_free + 8 * slot, (uint32_t)(((i / kTcStages) & 1) ^ 1), abort_flag, wait_ns)) {
         if (!*abort_flag) set_flag(err_flag, PKV_FLAG_TIMEOUT);
         *abort_flag = 1;
         return false;
@@ -222,7 +222,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             pw, lane, nblk, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, p.err_flag,
             [&](int64_t i, int bid, bool ok, float2) {
                 return produce_tile_tc<H>(i, wk.kvh, bid, ok, kreg, vreg, bar_full, bar_free, slot_ok, abort_flag,
-                                          &tm_k, &tm_v, p.err_flag);
+                                          &tm_k, &tm_v, p.err_flag, p.wait_ns);
             });
         if (lane == 0) issued_count[pw] = (int)issued;
     } else if (warp == 1) {
@@ -233,14 +233,14 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             for (int j = 0; j < gt && ok; ++j) {
                 const int i = i0 + j;
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_full + 8 * (i % S), (uint32_t)((i / S) & 1),
-                                                               abort_flag, kWaitLimitNs));
+                                                               abort_flag, p.wait_ns));
             }
             // S buffer g % 2 holds P(g - 2) until PV(g - 2) has read it (the release of its slot)
             if (ok && g >= 2) {
                 const int gq = g - 2;
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_free + 8 * (gq % L::kGroupSlots),
                                                                (uint32_t)((gq / L::kGroupSlots) & 1), abort_flag,
-                                                               kWaitLimitNs));
+                                                               p.wait_ns));
             }
             if (!ok) break;
             tc_fence_after();
@@ -276,7 +276,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         for (int g = 0; g < ngroups && ok; ++g) {
             const int i0 = g * GT, gt = min(GT, nblk - i0);
             ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_pready + 8 * (g & 1), (uint32_t)((g >> 1) & 1),
-                                                           abort_flag, kWaitLimitNs));
+                                                           abort_flag, p.wait_ns));
             if (!ok) break;
             if (tail_tile >= i0 && tail_tile < i0 + gt && slot_ok[tail_tile % S]) {
                 const uint32_t vt = vreg + (tail_tile % S) * L::kVTile;
@@ -325,11 +325,11 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             for (int j = 0; j < gt && ok; ++j) {
                 const int i = i0 + j;
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_full + 8 * (i % S), (uint32_t)((i / S) & 1),
-                                                               abort_flag, kWaitLimitNs));
+                                                               abort_flag, p.wait_ns));
             }
             if (ok)
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_sfull + 8 * (g & 1), (uint32_t)((g >> 1) & 1),
-                                                               abort_flag, kWaitLimitNs));
+                                                               abort_flag, p.wait_ns));
             if (!ok) break;
             tc_fence_after();
             const uint32_t sb = tm_s + 64 * (g & 1);
@@ -361,7 +361,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     const int gq = g - 1;
                     ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_free + 8 * (gq % L::kGroupSlots),
                                                                    (uint32_t)((gq / L::kGroupSlots) & 1), abort_flag,
-                                                                   kWaitLimitNs));
+                                                                   p.wait_ns));
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll 1
@@ -392,7 +392,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_pready + 8 * (g & 1));
         }
-        if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_odone, 0u, abort_flag, kWaitLimitNs));
+        if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_odone, 0u, abort_flag, p.wait_ns));
         if (!ok) {
             if (lane == 0 && !*abort_flag) set_flag(p.err_flag, PKV_FLAG_TIMEOUT);
             *abort_flag = 1;

@@ -203,6 +203,32 @@ cudaError_t launch_gather(const uint16_t *k_cache, const uint16_t *v_cache,
 
 }  // namespace pkv
 
+// ------------------------------ bounded-wait self-test ------------------------------------
+// One warp waits, with the same bounded wait the attention kernels use, on an mbarrier that no
+// thread ever arrives at: the wait expires after limit_ns and the kernel sets PKV_FLAG_TIMEOUT.
+namespace pkv {
+
+__global__ void wait_expiry_kernel(uint64_t limit_ns, int32_t *err_flag)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    const bool ok = mbar_wait_bounded(b, 0u, nullptr, limit_ns);
+    if (!ok && threadIdx.x == 0) set_flag(err_flag, PKV_FLAG_TIMEOUT);
+}
+
+cudaError_t launch_wait_expiry(uint64_t limit_ns, int32_t *err_flag, cudaStream_t stream)
+{
+    wait_expiry_kernel<<<1, 32, 0, stream>>>(limit_ns, err_flag);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv
+
 // ---------------------------------- FP8 (e4m3) cache ----------------------------------------
 // code = e4m3(x / scale[kvh]): the division rounded to nearest in fp32, then round-to-nearest-
 // even onto the e4m3 grid with saturation at +-448 (cvt.rn.satfinite).  One thread per 8 values.

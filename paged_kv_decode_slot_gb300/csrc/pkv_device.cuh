@@ -14,9 +14,8 @@ namespace pkv {
 
 constexpr int kBlockSize = 16;  // tokens per KV block
 
-// Upper bound on any in-kernel wait; expiry sets PKV_FLAG_TIMEOUT and the kernel returns.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-// Second, shorter bound used while draining copies after an expired wait.
+// Second, shorter bound used while draining copies after an expired wait (the first bound, on
+// every other wait, is a kernel parameter: kWaitLimitNs by default, pkv_internal.h).
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)

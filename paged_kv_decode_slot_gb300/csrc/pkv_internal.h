@@ -17,6 +17,8 @@ constexpr int kMaxBalancedSeqs = 1024;
 // partitions; the last partition CTA of a split runs it inside the attention kernel when the
 // G * parts weights fit in kInKernelMergeWeights floats, otherwise lse_merge_kernel does.
 constexpr int kMergeWarps = 6;
+// Default bound on the in-kernel waits; expiry sets PKV_FLAG_TIMEOUT and the kernel returns.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kInKernelMergeWeights = 8192;
 
 struct AttnParams {
@@ -48,6 +50,7 @@ struct AttnParams {
     int32_t *counters;             // split-KV with the merge in the kernel: [B][K], zero between
                                    // calls (nullptr: write every partial, merge separately)
     int32_t *err_flag;             // nullable
+    uint64_t wait_ns;              // limit of every in-kernel wait (pkv_set_wait_limit_ns)
 };
 
 // fp8: e4m3 pools (H = 128); pairs: e4m3 consumers take two tiles per step (for grids with
@@ -91,6 +94,7 @@ struct ColsParams {
     int32_t prefix_parts;          // prefix mode: partitions of the prefix pass (grid)
     int32_t prefix_ctas;           // prefix mode: CTAs of the prefix pass
     int32_t *err_flag;
+    uint64_t wait_ns;              // limit of every in-kernel wait (pkv_set_wait_limit_ns)
 };
 
 cudaError_t launch_attn_cols(int H, const CUtensorMap &tk, const CUtensorMap &tv, const ColsParams &p,
@@ -108,6 +112,8 @@ cudaError_t launch_slot_mapping_multi(const int32_t *block_tables, int max_nb,
 cudaError_t launch_copy_blocks(uint8_t *k_cache, uint8_t *v_cache, const int32_t *src_dst, int n,
                                int num_blocks, int64_t block_bytes, int32_t *err_flag,
                                cudaStream_t stream);
+
+cudaError_t launch_wait_expiry(uint64_t limit_ns, int32_t *err_flag, cudaStream_t stream);
 
 cudaError_t launch_quantize_fp8(const uint16_t *src, int64_t rows, int K, int H, const float *scale,
                                 int scale_stride, uint8_t *dst, cudaStream_t stream);
