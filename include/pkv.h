@@ -369,6 +369,13 @@ int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_
    default limit runs normally.  Lowering it is a way to exercise those paths. */
 uint64_t pkv_set_wait_limit_ns(uint64_t limit_ns);
 
+/* Test hook for the expiry paths: in the attention launches that follow (process-wide), every
+   CTA's producer skips its tile `tile` (0-based within the CTA's block list): it neither loads
+   it nor signals it, so the consumer's bounded wait on it expires (PKV_FLAG_TIMEOUT) and the
+   CTA takes its abort path -- drain, void result, release, return -- with no fault and no hang.
+   -1 switches it off (the default); returns the previous value.  Results are void while set. */
+int64_t pkv_debug_withhold_tile(int64_t tile);
+
 /* Self-test of the bounded waits: one warp waits, with the attention kernels' bounded wait, on
    an mbarrier that nothing ever completes; after the current wait limit it gives up and sets
    PKV_FLAG_TIMEOUT in err_flag (device or pinned host int32, required).  No fault, no hang. */

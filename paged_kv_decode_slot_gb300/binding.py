@@ -433,6 +433,13 @@ _lib.pkv_set_wait_limit_ns.restype = ctypes.c_uint64
 
 
 _lib.pkv_check_wait_expiry.argtypes = [_P, _P]
+_lib.pkv_debug_withhold_tile.argtypes = [ctypes.c_int64]
+_lib.pkv_debug_withhold_tile.restype = ctypes.c_int64
+
+
+def pkv_debug_withhold_tile(tile: int) -> int:
+    """Test hook: the attention producers skip this tile of every CTA (-1: off); returns the previous."""
+    return int(_lib.pkv_debug_withhold_tile(int(tile)))
 
 
 def pkv_check_wait_expiry(err_flag, stream=None) -> int:

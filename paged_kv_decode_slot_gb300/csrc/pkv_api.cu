@@ -115,6 +115,8 @@ int g_tok_major = -1;  // layout the driver accepted first (-1: not yet known)
 std::mutex g_layout_mu;
 // limit of every bounded wait inside the attention kernels (pkv_set_wait_limit_ns)
 std::atomic<uint64_t> g_wait_ns{pkv::kWaitLimitNs};
+// test hook: a tile index that the attention kernels' producers skip (-1: none)
+std::atomic<int64_t> g_withhold_tile{-1};
 
 int make_kv_maps(CUtensorMap *tk, CUtensorMap *tv, const void *k, const void *v,
                  const pkv_cache_desc &d, int *tok_major)
@@ -180,6 +182,7 @@ pkv::AttnParams params_of(const AttnArgs &a, int tok_major)
     p.tok_major = tok_major;
     p.err_flag = a.err_flag;
     p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    p.withhold_tile = g_withhold_tile.load(std::memory_order_relaxed);
     return p;
 }
 
@@ -861,6 +864,7 @@ pkv::ColsParams cols_params_of(const AttnArgs &a, int tok_major)
     p.tok_major = tok_major;
     p.err_flag = a.err_flag;
     p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    p.withhold_tile = g_withhold_tile.load(std::memory_order_relaxed);
     return p;
 }
 
@@ -991,6 +995,11 @@ PKV_EXPORT int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache,
 PKV_EXPORT uint64_t pkv_set_wait_limit_ns(uint64_t limit_ns)
 {
     return g_wait_ns.exchange(limit_ns == 0 ? 1 : limit_ns);
+}
+
+PKV_EXPORT int64_t pkv_debug_withhold_tile(int64_t tile)
+{
+    return g_withhold_tile.exchange(tile < 0 ? -1 : tile);
 }
 
 PKV_EXPORT int pkv_check_wait_expiry(int32_t *err_flag, pkv_stream_t stream)

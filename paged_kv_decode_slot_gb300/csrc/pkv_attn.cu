@@ -187,6 +187,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
         const int64_t issued = run_producer<kProducers, bscale>(
             pw, lane, nblk, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, p.err_flag,
             [&](int64_t i, int bid, bool ok, float2 sc) {
+                if (i == p.withhold_tile) return true;  // test hook: never loaded, never signalled
                 return produce_tile<H, S, kFp8>(i, kvh, bid, ok, base_u32, bar_full, bar_empty,
                                                 slot_ok, abort_flag, &tm_k, &tm_v, p.tok_major,
                                                 p.err_flag, p.wait_ns, bscale ? stage_sc : nullptr, sc);

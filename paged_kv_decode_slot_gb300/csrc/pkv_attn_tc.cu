@@ -221,6 +221,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         const int64_t issued = run_producer<kTcProducers>(
             pw, lane, nblk, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, p.err_flag,
             [&](int64_t i, int bid, bool ok, float2) {
+                if (i == p.withhold_tile) return true;  // test hook: never loaded, never signalled
                 return produce_tile_tc<H>(i, wk.kvh, bid, ok, kreg, vreg, bar_full, bar_free, slot_ok, abort_flag,
                                           &tm_k, &tm_v, p.err_flag, p.wait_ns);
             });

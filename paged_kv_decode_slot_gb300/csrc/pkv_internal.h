@@ -51,6 +51,7 @@ struct AttnParams {
                                    // calls (nullptr: write every partial, merge separately)
     int32_t *err_flag;             // nullable
     uint64_t wait_ns;              // limit of every in-kernel wait (pkv_set_wait_limit_ns)
+    int64_t withhold_tile;         // test hook (pkv_debug_withhold_tile): -1, or a tile no CTA loads
 };
 
 // fp8: e4m3 pools (H = 128); pairs: e4m3 consumers take two tiles per step (for grids with
@@ -95,6 +96,7 @@ struct ColsParams {
     int32_t prefix_ctas;           // prefix mode: CTAs of the prefix pass
     int32_t *err_flag;
     uint64_t wait_ns;              // limit of every in-kernel wait (pkv_set_wait_limit_ns)
+    int64_t withhold_tile;         // test hook (pkv_debug_withhold_tile): -1, or a tile no CTA loads
 };
 
 cudaError_t launch_attn_cols(int H, const CUtensorMap &tk, const CUtensorMap &tv, const ColsParams &p,

@@ -5,11 +5,13 @@ sets PKV_FLAG_TIMEOUT; the kernel stops issuing, drains the copies it started, r
 holds (tensor memory included) and returns, and the unit's result is void.
   * pkv_check_wait_expiry waits, with the same bounded wait, on an mbarrier nothing completes:
     the expiry is certain and flagged.
-  * The attention kernels run at a 1 ns limit: every wait that is not satisfied at once may
-    expire (whether one does depends on timing), and any expiry must be flagged, not fault.
-    The same steps then run again with the default limit and must match the oracle -- the
-    context works, the fused append lands, and the split workspace's merge counters are back
-    at zero.
+  * Every attention path runs with pkv_debug_withhold_tile(3) and a 1 ms limit: each CTA's
+    producer skips its fourth tile (no load, no barrier arrival -- a flag nothing sets), so the
+    consumer's wait on it expires and every CTA with four or more tiles takes its abort path
+    (stop issuing, drain the copies it started, let its MMAs finish, release its tensor memory,
+    count toward the merge, return).  Only PKV_FLAG_TIMEOUT may be flagged, and it must be.
+    The same step then runs again with the defaults and must match the oracle: the context
+    works, the fused append lands, and the split workspace's merge counters are back at zero.
 """
 from __future__ import annotations
 
@@ -47,18 +49,20 @@ def test_wait_that_never_completes_expires_and_is_flagged(pkv):
     assert float(x.sum()) == 1023 * 1024 / 2
 
 
-def _flags_at_tiny_limit(pkv, run):
-    """Run `run(err)` with every in-kernel wait limited to 1 ns; return the device flags."""
-    prev = pkv.pkv_set_wait_limit_ns(1)
+def _flags_with_withheld_tile(pkv, run):
+    """Run `run(err)` with tile 3 of every CTA withheld and a 1 ms wait limit; return the flags."""
+    prev = pkv.pkv_set_wait_limit_ns(1_000_000)
+    prev_w = pkv.pkv_debug_withhold_tile(3)
     try:
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         run(err)
         torch.cuda.synchronize()
     finally:
+        pkv.pkv_debug_withhold_tile(prev_w)
         pkv.pkv_set_wait_limit_ns(prev)
-    assert prev == 2_000_000_000 or prev > 1
+    assert prev_w == -1
     _, flag = pkv.pkv_read_err_flag(err)
-    assert flag & ~pkv.PKV_FLAG_TIMEOUT == 0, f"only timeouts may be flagged, got {flag:#x}"
+    assert flag == pkv.PKV_FLAG_TIMEOUT, f"expected exactly the timeout flag, got {flag:#x}"
     return flag
 
 
@@ -125,7 +129,7 @@ def test_kernels_survive_expired_waits_and_recover(pkv, oracle, kind):
 
     err0 = torch.zeros(1, dtype=torch.int32, device="cuda")
     step = make(err0)
-    _flags_at_tiny_limit(pkv, lambda err: (setattr(step, "err_flag", err), step.run()))
+    _flags_with_withheld_tile(pkv, lambda err: (setattr(step, "err_flag", err), step.run()))
     # the same step object (its workspace and counters included) with the default limit
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     step.err_flag = err
