@@ -294,8 +294,12 @@ def kernel_label(args, plan, step) -> str:
         from paged_kv_decode_slot_gb300 import binding
         w = step.q.shape  # [B, T, N, H]
         tc = binding.pkv_multi_uses_tcgen05(args.tokens, w[2], step.k_cache.shape[2], w[3])
-        return ("attn_cols_tc_kernel<128>" if tc else "attn_cols_kernel<128>") + (
-            " + lse_merge_kernel" if plan.mode == "split" else "")
+        name = "attn_cols_tc_kernel<128>" if tc else "attn_cols_kernel<128>"
+        if plan.mode != "split":
+            return name
+        if binding.multi_attention_launches(plan.max_partitions, bool(tc)) == 1:
+            return name + " (partitions merged in the same launch)"
+        return name + " + lse_merge_kernel"
     if args.attn == "prefix":
         return "attn_cols_kernel<128> (prefix + suffix passes) + cascade_merge_kernel"
     fp8 = "1" if args.kv == "fp8" else "0"

@@ -349,7 +349,14 @@ int pkv_slot_mapping_multi(const int32_t *block_tables, int32_t max_blocks_per_s
    [num_seqs][T][N] (nullable).  partition_blocks 0: one pass (no workspace); > 0: fixed
    partitions of that many blocks and a log-sum-exp merge, with max_partitions as for
    pkv_decode_attn_splitk and a workspace of pkv_splitk_workspace_bytes(num_seqs * T, N, H,
-   max_partitions) bytes (256-byte aligned).  Each CTA loads a K/V tile once for up to 32 of a
+   max_partitions) bytes, 256-byte aligned and ZEROED BEFORE ITS FIRST USE.  On the mma.sync
+   column kernel with 32 * max_partitions <= 8192 the merge runs in the same launch: a sequence
+   held by one partition is written out directly, and the last CTA of each (sequence, KV head,
+   chunk of 32 rows) to finish merges the chunk's partials (the arithmetic of pkv_lse_merge, bit
+   for bit) and leaves its counter (in the workspace's counter area) at zero again, so the
+   workspace can be reused and captured in a CUDA graph.  The tcgen05 kernel and larger splits
+   merge in a second launch (pkv_lse_merge).  Calls that share a workspace must not overlap on
+   the GPU.  Each CTA loads a K/V tile once for up to 32 of a
    sequence's (token, head) rows of one KV head.  H in {64, 128}; G in {1, 2, 4, 8}.  With more
    than 16 rows per CTA (min(T * G, 32) > 16) and H = 128 the contraction runs on the tcgen05
    tensor cores (accumulators in tensor memory), otherwise on warp-level mma.sync; both compute

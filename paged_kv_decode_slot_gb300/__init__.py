@@ -13,7 +13,8 @@ ImportError (there is no fallback path).
 
 def __getattr__(name):
     if name.startswith(("pkv_", "PKV_")) or name in ("BLOCK_SIZE", "CacheDesc", "PkvError", "cache_desc",
-                                                    "check", "library", "max_partitions_for"):
+                                                    "check", "library", "max_partitions_for", "IN_KERNEL_MERGE_WEIGHTS",
+                                                    "split_attention_launches", "multi_attention_launches"):
         from . import binding
         return getattr(binding, name)
     raise AttributeError(f"module {__name__!r} has no attribute {name!r}")

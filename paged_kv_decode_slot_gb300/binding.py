@@ -210,6 +210,14 @@ def split_attention_launches(num_q_heads: int, num_kv_heads: int, max_partitions
     return 1 if (num_q_heads // num_kv_heads) * max_partitions <= IN_KERNEL_MERGE_WEIGHTS else 2
 
 
+def multi_attention_launches(max_partitions: int, tcgen05: bool) -> int:
+    """Kernel launches of one partitioned pkv_decode_attn_multi call: the mma.sync column kernel's
+    last CTA of each (sequence, KV head, chunk of 32 rows) merges the chunk when its
+    32 x max_partitions weights fit; otherwise, and always after the tcgen05 kernel, a
+    pkv_lse_merge launch follows."""
+    return 1 if not tcgen05 and 32 * max_partitions <= IN_KERNEL_MERGE_WEIGHTS else 2
+
+
 def pkv_splitk_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_partitions: int) -> int:
     return int(_lib.pkv_splitk_workspace_bytes(num_seqs, num_q_heads, head_dim, max_partitions))
 

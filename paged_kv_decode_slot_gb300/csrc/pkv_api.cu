@@ -983,10 +983,18 @@ PKV_EXPORT int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache,
               pkv::cols_tc_supported(cache.head_dim, tok_major);
     CUtensorMap tk_half;
     if (tc) tc = encode_kv_map(&tk_half, k_cache, cache, 0, 1) == CUDA_SUCCESS;
+    // The mma.sync kernel's last CTA of each (sequence, KV head, chunk of 32 rows) merges the chunk
+    // in the same launch when the chunk's weights (32 x max_partitions) fit in its drained ring.
+    // The tcgen05 kernel's partials go to pkv_lse_merge: its merging CTAs (the partition-0 CTAs,
+    // which start last) would merge 32 rows with five warps at the end of the grid, measured
+    // slower than the separate launch (Llama-3-8B batch of 64, 8 new tokens: 280 vs 262 us).
+    if (split && !tc && (int64_t)kColsPerCta * max_partitions <= kInKernelMergeWeights)
+        p.counters = split_ws(workspace, (int32_t)(num_seqs * (int64_t)num_new), num_q_heads, cache.head_dim,
+                              max_partitions).counters;
     cudaError_t e = tc ? pkv::launch_attn_cols_tc(cache.head_dim, tk_half, tv, p, grid, stream)
                        : pkv::launch_attn_cols(cache.head_dim, tk, tv, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "multi-token attention launch");
-    if (!split) return PKV_OK;
+    if (!split || p.counters) return PKV_OK;
     // rows of one sequence: its T tokens x N heads, all with the sequence's context length
     return pkv_lse_merge(part_out, part_lse, context_lens, num_seqs, num_new * num_q_heads,
                          cache.head_dim, max_partitions, partition_blocks, out, lse_out, stream);

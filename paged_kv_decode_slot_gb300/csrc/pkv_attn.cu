@@ -358,13 +358,19 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     if (!last_one) return;
     float *wts = reinterpret_cast<float *>(base);                          // [G][nparts]
     float *red = reinterpret_cast<float *>(base) + kInKernelMergeWeights;  // [kMergeWarps][8][H]
-    for (int g = warp; g < G; g += kAttnThreads / 32) {
-        const size_t bn = (size_t)b * p.N + (size_t)kvh * G + g;
-        const float L = lse_merge_weights(p.part_lse + bn * p.max_parts, nparts, wts + g * nparts, lane);
-        if (lane == 0 && p.lse_out) p.lse_out[bn] = L;
+    const size_t bn0 = (size_t)b * p.N + (size_t)kvh * G;
+    // the rows' partial lse first, all loads independent (one round trip), then each row's weights
+    // from that copy, in place
+    for (int idx = threadIdx.x; idx < G * nparts; idx += kAttnThreads) {
+        const int g = idx / nparts, q = idx - g * nparts;
+        wts[idx] = __ldcg(p.part_lse + (bn0 + g) * p.max_parts + q);
     }
     __syncthreads();
-    const size_t bn0 = (size_t)b * p.N + (size_t)kvh * G;
+    for (int g = warp; g < G; g += kAttnThreads / 32) {
+        const float L = lse_merge_weights<true>(wts + g * nparts, nparts, wts + g * nparts, lane);
+        if (lane == 0 && p.lse_out) p.lse_out[bn0 + g] = L;
+    }
+    __syncthreads();
     merge_rows<H, 8>(wts, nparts, G, p.part_out + bn0 * p.max_parts * H, (size_t)p.max_parts * H, red, p.out + bn0 * H,
                      H, threadIdx.x, kAttnThreads);
     if (threadIdx.x == 0) *count = 0;  // ready for the next call
@@ -664,8 +670,15 @@ lse_merge_kernel(const float *__restrict__ part_out, const float *__restrict__ p
     if (np > max_parts) np = max_parts;
     float *wts = smem_f;
     float *red = smem_f + ((size_t)R * max_parts + 3) / 4 * 4;
+    // the rows' partial lse first, all loads independent (one round trip), then each row's weights
+    // from that copy, in place
+    for (int idx = t; idx < nrows * np; idx += blockDim.x) {
+        const int g = idx / np, q = idx - g * np;
+        wts[g * np + q] = __ldcg(part_lse + (bn0 + g) * max_parts + q);
+    }
+    __syncthreads();
     for (int g = t >> 5; g < nrows; g += kMergeWarps) {
-        const float L = lse_merge_weights(part_lse + (bn0 + g) * max_parts, np, wts + g * np, t & 31);
+        const float L = lse_merge_weights<true>(wts + g * np, np, wts + g * np, t & 31);
         if ((t & 31) == 0 && lse_out) lse_out[bn0 + g] = L;
     }
     __syncthreads();

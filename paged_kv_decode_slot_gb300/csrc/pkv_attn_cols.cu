@@ -131,9 +131,14 @@ attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     ColsWork wk;
     if (!cols_work(p, blockIdx.x, wk)) return;
     const int nblk = wk.blk_end - wk.blk_begin;
+    // Split multi-token units merged in this launch: a sequence held by one partition is written
+    // out directly, one held by several leaves partials for the last of its CTAs to merge.
+    const bool merge_multi = p.counters != nullptr && wk.mode == kModeMulti && wk.slot >= 0;
+    const int nparts = merge_multi ? cols_nparts(p, wk) : 0;
+    const bool direct = wk.slot < 0 || (merge_multi && nparts <= 1);
     if (nblk <= 0) {
-        // several new tokens, one pass, empty sequence: 0 and -inf
-        if (wk.slot < 0) {
+        // several new tokens, empty sequence (one pass, or partition 0 when merged here): 0, -inf
+        if (wk.slot < 0 || (merge_multi && wk.slot == 0 && nparts == 0)) {
             for (int idx = threadIdx.x; idx < wk.ncols * H; idx += kAttnThreads) {
                 const int j = idx / H, h = idx - j * H;
                 int64_t row;
@@ -226,39 +231,47 @@ attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
 
     __syncthreads();
-    if (*abort_flag) {
+    const bool aborted = *abort_flag != 0;
+    const bool merge_here = merge_multi && nparts > 1;
+    if (aborted) {
         if (warp >= kConsumerWarps && lane == 0)
             drain_ring<S, kProducers>(bar_full, warp - kConsumerWarps, issued_count[warp - kConsumerWarps]);
         __syncthreads();
-        return;
+        // the sequence's other partitions still count on this one: it leaves a void partial
+        if (!merge_here) return;
     }
 
     // merge: column j (group j / 8, row j % 8) was seen by warps j/8 + ng * r, r < R
     float *mo = reinterpret_cast<float *>(base);
     float *mm = mo + kConsumerWarps * 8 * H;
     float *ml = mm + kConsumerWarps * 8;
-    if (warp < kConsumerWarps) deposit<H>(acc, mo, mm, ml, warp, lane);
-    __syncthreads();
+    if (!aborted) {
+        if (warp < kConsumerWarps) deposit<H>(acc, mo, mm, ml, warp, lane);
+        __syncthreads();
+    }
     for (int idx = threadIdx.x; idx < wk.ncols * H; idx += kAttnThreads) {
         const int j = idx / H, h = idx - j * H;
-        const int cg = j / kColsPerWarp, g8 = j - cg * kColsPerWarp;
-        float M = -INFINITY;
-        for (int rr = 0; rr < R; ++rr) M = fmaxf(M, mm[(cg + ng * rr) * 8 + g8]);
-        float accv = 0.f, lsum = 0.f;
-        if (M != -INFINITY) {
-            for (int rr = 0; rr < R; ++rr) {
-                const int w = cg + ng * rr;
-                const float sc = exp2f(mm[w * 8 + g8] - M);
-                lsum += sc * ml[w * 8 + g8];
-                accv += sc * mo[(w * 8 + g8) * H + h];
+        float val = __int_as_float(0x7FC00000), lse = __int_as_float(0x7FC00000);  // NaN: void
+        if (!aborted) {
+            const int cg = j / kColsPerWarp, g8 = j - cg * kColsPerWarp;
+            float M = -INFINITY;
+            for (int rr = 0; rr < R; ++rr) M = fmaxf(M, mm[(cg + ng * rr) * 8 + g8]);
+            float accv = 0.f, lsum = 0.f;
+            if (M != -INFINITY) {
+                for (int rr = 0; rr < R; ++rr) {
+                    const int w = cg + ng * rr;
+                    const float sc = exp2f(mm[w * 8 + g8] - M);
+                    lsum += sc * ml[w * 8 + g8];
+                    accv += sc * mo[(w * 8 + g8) * H + h];
+                }
             }
+            val = M != -INFINITY ? accv / lsum : 0.f;
+            lse = M != -INFINITY ? (M + log2f(lsum)) * kLn2 : -INFINITY;
         }
-        const float val = M != -INFINITY ? accv / lsum : 0.f;
-        const float lse = M != -INFINITY ? (M + log2f(lsum)) * kLn2 : -INFINITY;
         int64_t row;
         int vis;
         col_of(p, wk, j, row, vis);
-        if (wk.slot < 0) {
+        if (direct) {
             p.out[row * H + h] = __float2bfloat16_rn(val);
             if (h == 0 && p.lse_out) p.lse_out[row] = lse;
         } else {
@@ -267,6 +280,7 @@ attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             if (h == 0) p.part_lse[rp] = lse;
         }
     }
+    if (merge_here) cols_merge_chunk<H>(p, wk, nparts, reinterpret_cast<float *>(base), kAttnThreads);
 }
 
 // Merge of the prefix pass and the suffix pass of one (sequence, query head): slots
@@ -288,8 +302,11 @@ __global__ void cascade_merge_kernel(const ColsParams p, __nv_bfloat16 *__restri
     const int np = ok ? (pnb + p.prefix_part_blocks - 1) / p.prefix_part_blocks +
                             (nb - pnb + p.part_blocks - 1) / p.part_blocks
                       : 0;
+    // the row's partial lse first (one round trip), then its weights from that copy, in place
+    for (int q = h; q < np; q += H) wts[q] = __ldcg(p.part_lse + row * p.max_parts + q);
+    __syncthreads();
     if (h < 32) {
-        const float L = lse_merge_weights(p.part_lse + row * p.max_parts, np, wts, h);
+        const float L = lse_merge_weights<true>(wts, np, wts, h);
         if (h == 0) row_lse = L;
     }
     __syncthreads();

@@ -532,21 +532,25 @@ __device__ __forceinline__ void combine(const float *mo, const float *mm, const 
 // without keys): M = max_q lse_q, L = M + ln sum_q exp(lse_q - M), w_q = exp(lse_q - L), all
 // zero and L = -inf when M = -inf.  Called by one whole warp (lanes stride the parts, shuffles
 // reduce); writes w[0..n) and returns L on every lane.  The merged output is sum_q w_q o_q.
+// kShared: lp is a copy in shared memory (plain loads; the arithmetic, hence the bits, are the
+// same), and w may be lp itself (each lane reads its q's last before it writes them).
+template <bool kShared = false>
 __device__ __forceinline__ float lse_merge_weights(const float *lp, int n, float *w, int lane)
 {
+    auto ld = [&](int q) { return kShared ? lp[q] : __ldcg(lp + q); };
     float M = -INFINITY;
-    for (int q = lane; q < n; q += 32) M = fmaxf(M, __ldcg(lp + q));
+    for (int q = lane; q < n; q += 32) M = fmaxf(M, ld(q));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
     float L = -INFINITY;
     if (M != -INFINITY) {
         float sum = 0.f;
-        for (int q = lane; q < n; q += 32) sum += expf(__ldcg(lp + q) - M);
+        for (int q = lane; q < n; q += 32) sum += expf(ld(q) - M);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
         L = M + logf(sum);
     }
-    for (int q = lane; q < n; q += 32) w[q] = L == -INFINITY ? 0.f : expf(__ldcg(lp + q) - L);
+    for (int q = lane; q < n; q += 32) w[q] = L == -INFINITY ? 0.f : expf(ld(q) - L);
     __syncwarp();
     return L;
 }
@@ -561,27 +565,28 @@ __device__ __forceinline__ float lse_merge_value(const float *w, const float *po
 }
 
 // out[g][h] = sum_q w[g * n + q] * po[g * po_row + q * H + h] for nrows <= kMaxRows rows, in an
-// order that depends on nothing but n: warp w (< kMergeWarps) adds the partitions q = w,
+// order that depends on nothing but n: merge slot w (< kMergeWarps) adds the partitions q = w,
 // w + kMergeWarps, ... in increasing q with fused multiply-adds, lane l holding the row's elements
-// [l * H / 32, (l + 1) * H / 32) from one vector load per partition (all of a warp's loads are
-// independent, so they are in flight together); the warps' sums, staged in red
-// [kMergeWarps][kMaxRows][H], are then added in warp order.  A CTA merging one row and one merging
-// eight give the same bits.  Needs kMergeWarps warps among the nthreads; ends with the rows written
-// (bf16) and a __syncthreads between the two phases.
+// [l * H / 32, (l + 1) * H / 32) from one vector load per partition (all of a slot's loads are
+// independent, so they are in flight together); the slots' sums, staged in red
+// [kMergeWarps][kMaxRows][H], are then added in slot order.  Warp w takes the slots w, w + W, ...
+// of the CTA's W warps, so a CTA merging one row and one merging eight, with five warps or six,
+// give the same bits.  Ends with the rows written (bf16) and a __syncthreads between the two
+// phases.
 template <int H, int kMaxRows>
 __device__ __forceinline__ void merge_rows(const float *w, int n, int nrows, const float *po, size_t po_row,
                                            float *red, __nv_bfloat16 *out, size_t out_row, int tid, int nthreads)
 {
     constexpr int E = H / 32;
     static_assert(E == 2 || E == 4, "H = 64 or 128");
-    const int warp = tid >> 5, lane = tid & 31;
-    if (warp < kMergeWarps) {
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
+    for (int slot = warp; slot < kMergeWarps; slot += nwarps) {
         float acc[kMaxRows][E];
 #pragma unroll
         for (int g = 0; g < kMaxRows; ++g)
 #pragma unroll
             for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
-        for (int q = warp; q < n; q += kMergeWarps) {
+        for (int q = slot; q < n; q += kMergeWarps) {
 #pragma unroll
             for (int g = 0; g < kMaxRows; ++g) {
                 if (g < nrows) {
@@ -605,7 +610,7 @@ __device__ __forceinline__ void merge_rows(const float *w, int n, int nrows, con
         for (int g = 0; g < kMaxRows; ++g)
             if (g < nrows)
 #pragma unroll
-                for (int e = 0; e < E; ++e) red[(warp * kMaxRows + g) * H + lane * E + e] = acc[g][e];
+                for (int e = 0; e < E; ++e) red[(slot * kMaxRows + g) * H + lane * E + e] = acc[g][e];
     }
     __syncthreads();
     for (int idx = tid; idx < nrows * H; idx += nthreads) {

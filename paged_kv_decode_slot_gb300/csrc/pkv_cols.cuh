@@ -154,4 +154,67 @@ __device__ __forceinline__ void col_of(const ColsParams &p, const ColsWork &w, i
     }
 }
 
+// Partitions of a multi-token unit's sequence that hold blocks (the CTAs its merge waits for).
+__device__ __forceinline__ int cols_nparts(const ColsParams &p, const ColsWork &w)
+{
+    const int nb = (w.ctx + kBlockSize - 1) / kBlockSize;
+    return (nb + p.part_blocks - 1) / p.part_blocks;
+}
+
+// In-kernel log-sum-exp merge of one chunk of a split multi-token unit.  Every CTA of the unit
+// calls it once its partials are written (void NaN partials after an expired wait, so the count
+// still completes); the last of the nparts CTAs of (sequence, KV head, chunk) to arrive merges the
+// chunk's rows with the arithmetic of the separate merge (lse_merge_weights, merge_rows: the same
+// bits) and resets the count to zero for the next call.  `smem` is kLseMergeBytes of the CTA's
+// shared memory that nothing uses any more.  Rows of one head g are N rows apart from token to
+// token, so each merge_rows call takes up to eight tokens of one head.
+template <int H>
+__device__ void cols_merge_chunk(const ColsParams &p, const ColsWork &wk, int nparts, float *smem, int nthreads)
+{
+    __shared__ int last_one;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
+    __syncthreads();  // every partial of this CTA is written
+    int32_t *count = p.counters + ((int64_t)wk.b * p.K + wk.kvh) * p.chunks + wk.col_base / kColsPerCta;
+    if (tid == 0) last_one = atomic_add_acq_rel_gpu(count, 1) == nparts - 1;
+    __syncthreads();
+    if (!last_one) return;
+    const int G = p.G;
+    const int tcount = wk.ncols / G;            // tokens of the chunk (a chunk holds whole tokens)
+    float *wts = smem;                          // [G][tcount][nparts]
+    float *red = smem + kInKernelMergeWeights;  // [kMergeWarps][8][H]
+    // the chunk's partial lse first, all loads independent (one round trip), then each row's
+    // weights from that copy, in place
+    for (int idx = tid; idx < wk.ncols * nparts; idx += nthreads) {
+        const int j = idx / nparts, q = idx - j * nparts;
+        int64_t row;
+        int vis;
+        col_of(p, wk, j, row, vis);
+        const int tl = j / G, g = j - tl * G;
+        wts[((size_t)g * tcount + tl) * nparts + q] = __ldcg(p.part_lse + row * p.max_parts + q);
+    }
+    __syncthreads();
+    for (int j = warp; j < wk.ncols; j += nwarps) {
+        int64_t row;
+        int vis;
+        col_of(p, wk, j, row, vis);
+        const int tl = j / G, g = j - tl * G;
+        float *wr = wts + ((size_t)g * tcount + tl) * nparts;
+        const float L = lse_merge_weights<true>(wr, nparts, wr, lane);
+        if (lane == 0 && p.lse_out) p.lse_out[row] = L;
+    }
+    __syncthreads();
+    for (int g = 0; g < G; ++g) {
+        for (int t0 = 0; t0 < tcount; t0 += 8) {
+            int64_t row;
+            int vis;
+            col_of(p, wk, t0 * G + g, row, vis);
+            merge_rows<H, 8>(wts + ((size_t)g * tcount + t0) * nparts, nparts, min(8, tcount - t0),
+                             p.part_out + row * p.max_parts * H, (size_t)p.N * p.max_parts * H, red,
+                             p.out + row * H, (size_t)p.N * H, tid, nthreads);
+            __syncthreads();  // red is reused by the next rows
+        }
+    }
+    if (tid == 0) *count = 0;  // ready for the next call
+}
+
 }  // namespace pkv

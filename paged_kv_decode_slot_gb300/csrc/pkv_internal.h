@@ -87,6 +87,8 @@ struct ColsParams {
     float *lse_out;                // nullable
     float *part_out;               // [rows][max_parts][H]
     float *part_lse;               // [rows][max_parts]
+    int32_t *counters;             // multi, split: [B][K][chunks] merge counts (zero between
+                                   // calls; nullptr: the partials are merged by a separate launch)
     const int32_t *group_starts;   // prefix mode: [num_groups + 1]
     const int32_t *prefix_blocks;  // prefix mode: [num_groups] shared leading blocks per group
     int32_t num_groups;

@@ -261,7 +261,9 @@ class MultiTokenStep:
     """Verification of T new tokens per sequence (speculative decoding): the slots of the last T
     positions (``pkv_slot_mapping_multi``), the append of the B*T new K/V rows (``pkv_append``),
     then ``pkv_decode_attn_multi`` -- one pass when the (sequence, KV head, 32-row chunk) units
-    cover the SMs, else fixed partitions sized like ``plan_attention``'s.
+    cover the SMs, else fixed partitions sized like ``plan_attention``'s and a log-sum-exp merge
+    (in the same launch for the mma.sync column kernel, a second one after the tcgen05 kernel).
+    The workspace is zeroed once here; each call leaves its merge counters at zero.
 
     q [B, T, N, H] bf16; k_new/v_new [B, T, K, H]; pools, tables and lengths as ``DecodeStep``
     (context_lens counts the T new tokens).
@@ -314,7 +316,11 @@ class MultiTokenStep:
         self.attention(stream)
 
     def launches_per_step(self) -> int:
-        return 3 + (1 if self.plan.mode == "split" else 0)
+        if self.plan.mode != "split":
+            return 3
+        _, T, N, H = self.q.shape
+        tc = bool(B.pkv_multi_uses_tcgen05(T, N, self.k_cache.shape[2], H))
+        return 2 + B.multi_attention_launches(self.plan.max_partitions, tc)
 
     def input_names(self):
         return ("q", "k_new", "v_new", "block_tables", "context_lens")

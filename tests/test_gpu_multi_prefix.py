@@ -104,6 +104,41 @@ def test_decode_attn_multi_matches_oracle(pkv, oracle, name, N, K, H, ctx, T, pa
     assert_lse_close(lse.cpu().numpy().astype(np.float64), ref_lse, f"multi {name} T={T} pb={part_blocks}")
 
 
+@pytest.mark.parametrize("T,N,K,H", [(8, 16, 4, 128), (9, 16, 4, 128), (2, 16, 4, 128), (4, 4, 4, 64)],
+                         ids=["tcgen05_T8", "tcgen05_T9_two_chunks", "mma_T2", "mma_mha_h64_T4"])
+def test_multi_in_kernel_merge_equals_separate_merge(pkv, oracle, T, N, K, H):
+    """Partitioned multi-token attention with the merge its kernel picks (mma.sync: by the last CTA
+    of each (sequence, KV head, chunk) in the same launch; tcgen05: pkv_lse_merge) equals the same
+    partials merged by pkv_lse_merge (forced by a max_partitions whose 32 x max_partitions weights
+    exceed the in-kernel budget), bit for bit -- with an empty sequence, sequences shorter than T,
+    single-partition sequences written out directly, and a second call on the same workspace (the
+    counters were left at zero)."""
+    w = gen.make_workload(f"m_merge_{T}", 300 + T, N, K, H, [0, 1, T - 1, 16, 17, 40, 333, 700, 1000])
+    c = MultiCase(oracle, w, T, 310 + T)
+    kc, vc = bf16_dev(c.kc), bf16_dev(c.vc)
+    pb = 8
+    P = pkv.max_partitions_for(w.max_blocks, pb)
+    assert 32 * P <= pkv.IN_KERNEL_MERGE_WEIGHTS < 32 * 300
+    q = bf16_dev(c.q)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for parts, calls in ((P, 2), (300, 1)):
+        ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B * T, N, H, parts), dtype=torch.uint8, device="cuda")
+        for _ in range(calls):
+            out = torch.full_like(q, float("nan"))
+            lse = torch.full((w.B, T, N), float("nan"), dtype=torch.float32, device="cuda")
+            pkv.check(pkv.pkv_decode_attn_multi(q, kc, vc, i32_dev(w.block_tables), i32_dev(w.context_lens),
+                                                w.scale, out, lse, pb, parts, ws, err))
+            outs.append((out, lse))
+    assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
+    (o1, l1), (o2, l2), (o3, l3) = outs
+    assert torch.equal(o1, o3) and torch.equal(l1, l3), "in-kernel merge differs from pkv_lse_merge"
+    assert torch.equal(o1, o2) and torch.equal(l1, l2), "second call on the same workspace differs"
+    ref, ref_lse = c.reference(oracle)
+    assert_close(out_f64(o1), ref, f"multi in-kernel merge T={T}")
+    assert_lse_close(l1.cpu().numpy().astype(np.float64), ref_lse, f"multi in-kernel merge T={T}")
+
+
 @pytest.mark.parametrize("part_blocks", [0, 3])
 def test_multi_with_one_token_is_the_decode_kernel(pkv, oracle, part_blocks):
     """T = 1 through the column-parallel kernel equals pkv_decode_attn / _splitk bit for bit."""
@@ -120,7 +155,7 @@ def test_multi_with_one_token_is_the_decode_kernel(pkv, oracle, part_blocks):
         P = pkv.max_partitions_for(w.max_blocks, part_blocks)
         ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
         pkv.check(pkv.pkv_decode_attn_splitk(q, dk, dv, bt, cl, w.scale, out1, part_blocks, P, ws, lse1))
-        ws2 = torch.empty_like(ws)
+        ws2 = torch.zeros_like(ws)  # zeroed before its first use, like every split workspace
         pkv.check(pkv.pkv_decode_attn_multi(q.view(w.B, 1, w.N, w.H), dk, dv, bt, cl, w.scale, out2, lse2,
                                             part_blocks, P, ws2))
     else:
