@@ -141,9 +141,15 @@ size_t pkv_splitk_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
 
 /*
  * Split-KV decode attention (FlashDecoding, named in CS336 Lecture 10 notes,
- * "其他优化"): partition p of sequence b covers logical blocks
- * [p * partition_blocks, (p+1) * partition_blocks) of its table.  One CTA per
- * (partition, KV head, sequence), highest partition first, in one launch: a
+ * "其他优化"): sequence b's table is cut into partitions of partition_blocks
+ * blocks, partition p covering blocks [p * partition_blocks, (p+1) *
+ * partition_blocks).  When num_seqs * num_kv_heads >= the device's SM count
+ * (the grid runs in several waves) and max_partitions >= 1 + ceil((max_nb -
+ * partition_blocks / 2) / partition_blocks) (partition_blocks >= 2), the
+ * partitions taper instead: partition 0, launched last, covers the first
+ * partition_blocks / 2 blocks and partition p >= 1 the partition_blocks blocks
+ * after them, so that the grid's final wave is made of half-length CTAs.  The
+ * partials are internal; the result is the same up to rounding.  One CTA per (partition, KV head, sequence), highest partition first, in one launch: a
  * sequence that fits in one partition is written to out directly; the others
  * leave normalised partial outputs and lse in the workspace, and the last CTA of
  * each (sequence, KV head) to finish merges them by log-sum-exp (the same
@@ -295,6 +301,8 @@ int pkv_decode_attn_splitk_noalloc(const pkv_bf16 *q, const pkv_bf16 *k_cache,
  * The partition step alone: writes part_out [num_seqs][N][max_partitions][H] and
  * part_lse [num_seqs][N][max_partitions] (float, natural log) for the partitions
  * that hold tokens; partitions past a sequence's last block are not written.
+ * Partition p always covers blocks [p * partition_blocks, (p+1) *
+ * partition_blocks) here (never the tapered layout: the partials are the caller's).
  */
 int pkv_decode_attn_partitions(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                                const pkv_bf16 *v_cache, const int32_t *block_tables,

@@ -13,7 +13,7 @@ ImportError (there is no fallback path).
 
 def __getattr__(name):
     if name.startswith(("pkv_", "PKV_")) or name in ("BLOCK_SIZE", "CacheDesc", "PkvError", "cache_desc",
-                                                    "check", "library", "max_partitions_for", "IN_KERNEL_MERGE_WEIGHTS",
+                                                    "check", "library", "max_partitions_for", "tapered_partitions_for", "IN_KERNEL_MERGE_WEIGHTS",
                                                     "split_attention_launches", "multi_attention_launches"):
         from . import binding
         return getattr(binding, name)

@@ -226,6 +226,16 @@ def max_partitions_for(max_blocks_per_seq: int, partition_blocks: int) -> int:
     return max(1, -(-max_blocks_per_seq // partition_blocks))
 
 
+def tapered_partitions_for(max_blocks_per_seq: int, partition_blocks: int) -> int:
+    """Partitions the tapered layout needs (partition 0 of partition_blocks // 2 blocks, the others
+    of partition_blocks): the split entry points taper when max_partitions is at least this and
+    num_seqs x num_kv_heads >= the SM count."""
+    h = partition_blocks // 2
+    if partition_blocks < 2 or max_blocks_per_seq <= h:
+        return max_partitions_for(max_blocks_per_seq, partition_blocks)
+    return 1 + -(-(max_blocks_per_seq - h) // partition_blocks)
+
+
 def pkv_decode_attn_splitk(q, k_cache, v_cache, block_tables, context_lens, scale: float, out,
                            partition_blocks: int, max_partitions: int, workspace, lse_out=None,
                            err_flag=None, stream=None) -> int:

@@ -124,13 +124,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
         ctx = 0;
     }
     const int nb = (ctx + kBlockSize - 1) / kBlockSize;
-    const int blk_begin = kSplit ? part * p.part_blocks : 0;
-    const int blk_end = kSplit ? min(nb, blk_begin + p.part_blocks) : nb;
+    const int nparts = kSplit ? partition_count(nb, p.part_blocks, p.taper != 0) : 1;
+    int blk_begin = 0, blk_end = nb;
+    if (kSplit) partition_range(part, nparts, nb, p.part_blocks, p.taper != 0, blk_begin, blk_end);
     const int nblk = blk_end - blk_begin;
     // In-kernel merge (split with counters): a sequence held by one partition is written out
     // directly; one held by several leaves partials, and the last of its CTAs to finish (per KV
     // head, counted in p.counters) merges them and resets the count to zero.
-    const int nparts = kSplit ? (nb + p.part_blocks - 1) / p.part_blocks : 1;
     const bool merge_here = kSplit && p.counters != nullptr;
     const bool direct = !kSplit || (merge_here && nparts <= 1);
 
@@ -657,7 +657,7 @@ balanced_merge_kernel(const float *__restrict__ part_out, const float *__restric
 template <int H, int R>
 __global__ void __launch_bounds__(kMergeWarps * 32)
 lse_merge_kernel(const float *__restrict__ part_out, const float *__restrict__ part_lse,
-                 const int32_t *__restrict__ context_lens, int N, int max_parts, int part_blocks,
+                 const int32_t *__restrict__ context_lens, int N, int max_parts, int part_blocks, int taper,
                  __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out)
 {
     extern __shared__ float smem_f[];  // weights [R][np], then the warps' sums [kMergeWarps][R][H]
@@ -666,7 +666,7 @@ lse_merge_kernel(const float *__restrict__ part_out, const float *__restrict__ p
     const size_t bn0 = (size_t)b * N + n0;
     int ctx = context_lens[b];
     const int nb = ctx > 0 ? (ctx + kBlockSize - 1) / kBlockSize : 0;
-    int np = (nb + part_blocks - 1) / part_blocks;
+    int np = partition_count(nb, part_blocks, taper != 0);
     if (np > max_parts) np = max_parts;
     float *wts = smem_f;
     float *red = smem_f + ((size_t)R * max_parts + 3) / 4 * 4;
@@ -768,30 +768,32 @@ cudaError_t launch_balanced_merge(const float *part_out, const float *part_lse, 
 
 template <int H, int R>
 static cudaError_t launch_lse_merge_t(const float *part_out, const float *part_lse, const int32_t *context_lens,
-                                      int B, int N, int max_parts, int part_blocks, uint16_t *out, float *lse_out,
-                                      cudaStream_t stream)
+                                      int B, int N, int max_parts, int part_blocks, int taper, uint16_t *out,
+                                      float *lse_out, cudaStream_t stream)
 {
     const size_t smem = (((size_t)R * max_parts + 3) / 4 * 4 + (size_t)kMergeWarps * R * H) * sizeof(float);
     static int cached[64] = {};
     cudaError_t e = ensure_smem(lse_merge_kernel<H, R>, (int)smem, cached);
     if (e != cudaSuccess) return e;
     lse_merge_kernel<H, R><<<dim3((N + R - 1) / R, B), kMergeWarps * 32, smem, stream>>>(
-        part_out, part_lse, context_lens, N, max_parts, part_blocks, reinterpret_cast<__nv_bfloat16 *>(out), lse_out);
+        part_out, part_lse, context_lens, N, max_parts, part_blocks, taper, reinterpret_cast<__nv_bfloat16 *>(out),
+        lse_out);
     return cudaGetLastError();
 }
 
 cudaError_t launch_lse_merge(const float *part_out, const float *part_lse, const int32_t *context_lens,
-                             int B, int N, int H, int max_parts, int part_blocks, uint16_t *out,
+                             int B, int N, int H, int max_parts, int part_blocks, bool taper, uint16_t *out,
                              float *lse_out, cudaStream_t stream)
 {
+    const int tp = taper ? 1 : 0;
     // eight rows per CTA while their weights stay within 32 KB
     const bool eight = (int64_t)8 * max_parts <= 8192;
     if (H == 128)
-        return eight ? launch_lse_merge_t<128, 8>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, out, lse_out, stream)
-                     : launch_lse_merge_t<128, 1>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, out, lse_out, stream);
+        return eight ? launch_lse_merge_t<128, 8>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, tp, out, lse_out, stream)
+                     : launch_lse_merge_t<128, 1>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, tp, out, lse_out, stream);
     if (H == 64)
-        return eight ? launch_lse_merge_t<64, 8>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, out, lse_out, stream)
-                     : launch_lse_merge_t<64, 1>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, out, lse_out, stream);
+        return eight ? launch_lse_merge_t<64, 8>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, tp, out, lse_out, stream)
+                     : launch_lse_merge_t<64, 1>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, tp, out, lse_out, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -564,6 +564,31 @@ __device__ __forceinline__ float lse_merge_value(const float *w, const float *po
     return val;
 }
 
+// Partitions of a sequence of nb blocks, and the blocks [begin, end) of partition `part`.
+// Uniform: ceil(nb / pb) partitions, partition p covering [p * pb, (p + 1) * pb) clipped to nb.
+// Tapered (pb >= 2): partition 0, which the split grid launches last, covers [0, pb / 2) and
+// partition p >= 1 covers [pb / 2 + (p - 1) * pb, pb / 2 + p * pb), clipped to nb -- one
+// partition more than uniform at most, and the grid's final wave is made of half-length CTAs.
+// Partitions at or past the count are empty.
+__device__ __forceinline__ int partition_count(int nb, int pb, bool taper)
+{
+    if (nb <= 0) return 0;
+    const int h = pb / 2;
+    return !taper ? (nb + pb - 1) / pb : (nb <= h ? 1 : 1 + (nb - h + pb - 1) / pb);
+}
+
+__device__ __forceinline__ void partition_range(int part, int nparts, int nb, int pb, bool taper, int &begin,
+                                                int &end)
+{
+    if (part >= nparts) {
+        begin = end = nb;
+        return;
+    }
+    const int h = pb / 2;
+    begin = !taper ? part * pb : (part == 0 ? 0 : h + (part - 1) * pb);
+    end = min(nb, !taper ? begin + pb : (part == 0 ? h : begin + pb));
+}
+
 // out[g][h] = sum_q w[g * n + q] * po[g * po_row + q * H + h] for nrows <= kMaxRows rows, in an
 // order that depends on nothing but n: merge slot w (< kMergeWarps) adds the partitions q = w,
 // w + kMergeWarps, ... in increasing q with fused multiply-adds, lane l holding the row's elements

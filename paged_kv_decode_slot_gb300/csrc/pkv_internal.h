@@ -31,6 +31,7 @@ struct AttnParams {
     float scale_log2;              // scale * log2(e)
     int32_t tok_major;             // smem tile layout chosen by the tensor map (see pkv_attn.cu)
     int32_t part_blocks;           // split-KV: blocks per partition
+    int32_t taper;                 // split-KV: tapered partitions (partition_range), else uniform
     int32_t max_parts;             // split-KV: partition stride of part_out / part_lse
     __nv_bfloat16 *out;            // single pass: [B][N][H]
     float *lse_out;                // single pass: [B][N] (nullable)
@@ -140,9 +141,10 @@ cudaError_t launch_balanced_merge(const float *part_out, const float *part_lse, 
                                   int B, int N, int K, int H, int grid, int KG, uint16_t *out,
                                   float *lse_out, cudaStream_t stream);
 
+// taper: the partials come from partition_range's tapered layout (partition_count partitions).
 cudaError_t launch_lse_merge(const float *part_out, const float *part_lse,
                              const int32_t *context_lens, int B, int N, int H, int max_parts,
-                             int part_blocks, uint16_t *out, float *lse_out, cudaStream_t stream);
+                             int part_blocks, bool taper, uint16_t *out, float *lse_out, cudaStream_t stream);
 
 cudaError_t launch_slot_mapping(const int32_t *block_tables, int max_nb, const int32_t *context_lens,
                                 int B, int num_blocks, int64_t *slots, int32_t *err_flag,

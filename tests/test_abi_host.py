@@ -141,7 +141,9 @@ def test_library_kv_bytes_matches_pages(lib):
 def test_attention_plan():
     from paged_kv_decode_slot_gb300.step import plan_attention
     p = plan_attention(64, 8, 512, 152)                                 # 512 units cover 152 SMs,
-    assert (p.mode, p.partition_blocks, p.max_partitions) == ("split", 128, 4)   # long tables split
+    assert (p.mode, p.partition_blocks, p.max_partitions) == ("split", 128, 5)   # long tables split,
+    p = plan_attention(64, 8, 512, 152, taper=False)                    # one more partition: taper
+    assert (p.mode, p.partition_blocks, p.max_partitions) == ("split", 128, 4)
     assert plan_attention(20, 8, 95, 152).mode == "single"
     assert plan_attention(128, 40, 64, 152).mode == "single"
     p = plan_attention(2, 8, 8192, 152)                                 # long context: 256 blocks
@@ -153,6 +155,20 @@ def test_attention_plan():
     assert plan_attention(64, 8, 512, 152, mode="balanced").mode == "balanced"
     p = plan_attention(64, 8, 512, 152, partition_blocks=64)
     assert p.mode == "split" and p.max_partitions == 8
+
+
+def test_tapered_partition_count():
+    """Partition 0 of half a partition, then whole ones: one more partition than the uniform
+    layout needs unless the table ends within the first half partition."""
+    import paged_kv_decode_slot_gb300 as pkv
+    for pb in (2, 3, 4, 7, 128, 256):
+        h = pb // 2
+        for nb in range(1, 3 * pb + 3):
+            n = pkv.tapered_partitions_for(nb, pb)
+            covered = h + (n - 1) * pb             # blocks the n tapered partitions cover
+            assert covered >= nb and (n == 1 or h + (n - 2) * pb < nb), (pb, nb, n)
+            assert n <= pkv.max_partitions_for(nb, pb) + 1
+    assert pkv.tapered_partitions_for(5, 1) == 5   # no taper below two blocks a partition
 
 
 def test_balanced_host_validation(lib):

@@ -306,6 +306,43 @@ def test_bad_slot_and_ctx_set_flags(pkv, oracle):
     assert torch.all(out[2].float() == 0)
 
 
+def test_tapered_partitions_merge_in_kernel_and_separate(pkv, oracle):
+    """With at least one (sequence, KV head) unit per SM and room for one more partition, the merged
+    split entry points taper their partitions (partition 0, launched last, covers half a
+    partition).  Every row matches the oracle -- no block missed or counted twice for sequences
+    with 0, 1, 2, 3 and many partitions, lengths on and off the half-partition edge -- and the
+    in-kernel merge equals the separate merge of the same tapered partials (forced by
+    max_partitions > 8192 / G) bit for bit."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    K, G = 4, 4
+    B = -(-sms // K) + 2
+    lens = [0, 1, 16, 17, 31, 32, 33, 48, 64, 65, 80, 96, 97, 127, 128, 129, 200, 333, 700, 1000]
+    w = gen.make_workload("tapered", 153, K * G, K, 128, [lens[i % len(lens)] for i in range(B)])
+    assert w.B * w.K >= sms
+    d = _post_append_device(pkv, oracle, w)
+    pb = 4  # 64 tokens: tapered partition 0 holds 2 blocks, the others 4
+    P = pkv.tapered_partitions_for(w.max_blocks, pb)
+    assert P == pkv.max_partitions_for(w.max_blocks, pb) + 1
+    ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+    out_k = torch.empty_like(d["q"])
+    lse_k = torch.empty(w.B, w.N, dtype=torch.float32, device="cuda")
+    pkv.check(pkv.pkv_decode_attn_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                         d["context_lens"], w.scale, out_k, pb, P, ws, lse_k))
+    kc, vc = appended_host_cache(oracle, w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    assert_close(out_f64(out_k), ref, "tapered split, in-kernel merge")
+    assert_lse_close(lse_k.cpu().numpy().astype(np.float64), ref_lse, "tapered split, in-kernel merge")
+    P = pkv.IN_KERNEL_MERGE_WEIGHTS // G + 1
+    ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B, w.N, w.H, P), dtype=torch.uint8, device="cuda")
+    out_m = torch.empty_like(d["q"])
+    lse_m = torch.empty(w.B, w.N, dtype=torch.float32, device="cuda")
+    pkv.check(pkv.pkv_decode_attn_splitk(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                         d["context_lens"], w.scale, out_m, pb, P, ws, lse_m))
+    torch.cuda.synchronize()
+    assert torch.equal(out_k.view(torch.int16), out_m.view(torch.int16))
+    assert torch.equal(lse_k, lse_m)
+
+
 # ------------------------------------ full-size workloads, sampled -------------------------
 FULL = ["l3_8b_b64", "l2_13b_mha_b1", "l2_13b_mha_b8", "l2_13b_mha_b64", "l2_13b_mha_b128",
         "prefix_l3_70b", "long_splitk"]
