@@ -116,14 +116,13 @@ def plan_attention(num_seqs: int, num_kv_heads: int, max_blocks_per_seq: int, nu
             if max_blocks_per_seq <= LONG_PARTITION_BLOCKS:
                 return AttentionPlan("single", max_blocks_per_seq, 1)
             partition_blocks = LONG_PARTITION_BLOCKS
-            count = B.tapered_partitions_for if taper else B.max_partitions_for
-            return AttentionPlan("split", partition_blocks, count(max_blocks_per_seq, partition_blocks))
-        want = -(-max_blocks_per_seq * units // 512)
-        partition_blocks = 8
-        while partition_blocks < want:
-            partition_blocks *= 2
-    return AttentionPlan("split", partition_blocks,
-                         B.max_partitions_for(max_blocks_per_seq, partition_blocks))
+        else:
+            want = -(-max_blocks_per_seq * units // 512)
+            partition_blocks = 8
+            while partition_blocks < want:
+                partition_blocks *= 2
+    count = B.tapered_partitions_for if taper and units >= num_sms else B.max_partitions_for
+    return AttentionPlan("split", partition_blocks, count(max_blocks_per_seq, partition_blocks))
 
 
 class DecodeStep:

@@ -153,7 +153,9 @@ def test_attention_plan():
     p = plan_attention(1, 40, 64, 152)                                  # at least 8 blocks
     assert p.mode == "split" and p.partition_blocks == 8
     assert plan_attention(64, 8, 512, 152, mode="balanced").mode == "balanced"
-    p = plan_attention(64, 8, 512, 152, partition_blocks=64)
+    p = plan_attention(64, 8, 512, 152, partition_blocks=64)            # several waves: tapered
+    assert p.mode == "split" and p.max_partitions == 9
+    p = plan_attention(16, 8, 512, 152, partition_blocks=64)            # one wave: uniform
     assert p.mode == "split" and p.max_partitions == 8
 
 
