@@ -358,7 +358,9 @@ int pkv_slot_mapping_multi(const int32_t *block_tables, int32_t max_blocks_per_s
    partitions of that many blocks and a log-sum-exp merge, with max_partitions as for
    pkv_decode_attn_splitk and a workspace of pkv_splitk_workspace_bytes(num_seqs * T, N, H,
    max_partitions) bytes, 256-byte aligned and ZEROED BEFORE ITS FIRST USE.  On the mma.sync
-   column kernel with 32 * max_partitions <= 8192 the merge runs in the same launch: a sequence
+   column kernel the partitions taper as in pkv_decode_attn_splitk, with num_seqs * chunks of
+   32 rows * num_kv_heads in place of num_seqs * num_kv_heads; the tcgen05 kernel keeps them
+   uniform.  On the mma.sync column kernel with 32 * max_partitions <= 8192 the merge runs in the same launch: a sequence
    held by one partition is written out directly, and the last CTA of each (sequence, KV head,
    chunk of 32 rows) to finish merges the chunk's partials (the arithmetic of pkv_lse_merge, bit
    for bit) and leaves its counter (in the workspace's counter area) at zero again, so the

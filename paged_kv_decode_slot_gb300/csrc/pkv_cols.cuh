@@ -72,8 +72,8 @@ __device__ __forceinline__ bool cols_work(const ColsParams &p, int64_t c, ColsWo
         w.ncols = min(kColsPerCta, p.T * p.G - w.col_base);
         w.table_row = w.b;
         const int nb = (ctx + kBlockSize - 1) / kBlockSize;
-        w.blk_begin = part * p.part_blocks;
-        w.blk_end = min(nb, w.blk_begin + p.part_blocks);
+        partition_range(part, partition_count(nb, p.part_blocks, p.taper != 0), nb, p.part_blocks, p.taper != 0,
+                        w.blk_begin, w.blk_end);
         w.data_end = ctx;
         w.slot = p.split ? part : -1;
         return w.ncols > 0;
@@ -158,7 +158,7 @@ __device__ __forceinline__ void col_of(const ColsParams &p, const ColsWork &w, i
 __device__ __forceinline__ int cols_nparts(const ColsParams &p, const ColsWork &w)
 {
     const int nb = (w.ctx + kBlockSize - 1) / kBlockSize;
-    return (nb + p.part_blocks - 1) / p.part_blocks;
+    return partition_count(nb, p.part_blocks, p.taper != 0);
 }
 
 // In-kernel log-sum-exp merge of one chunk of a split multi-token unit.  Every CTA of the unit

@@ -80,6 +80,7 @@ struct ColsParams {
     float scale_log2;
     int32_t tok_major;
     int32_t part_blocks;           // blocks per partition
+    int32_t taper;                 // multi: tapered partitions (partition_range), else uniform
     int32_t parts;                 // multi: partitions per sequence
     int32_t split;                 // multi: write partials (1) or final outputs (0, parts == 1)
     int32_t max_parts;             // partition stride of part_out / part_lse

@@ -104,7 +104,8 @@ def plan_attention(num_seqs: int, num_kv_heads: int, max_blocks_per_seq: int, nu
     With at least one unit per SM the grid runs in several waves; ``taper`` then leaves room for
     one more partition, so the split entry points taper (partition 0, launched last, covers half a
     partition and the final wave is short: bf16 180.2 -> 178.1 us, e4m3 118.8 -> 114.7 on the
-    batch of 64).  The column kernels of several new tokens do not taper (``taper=False``).
+    batch of 64).  The tcgen05 column kernel of several new tokens does not taper
+    (``taper=False``); the mma.sync one does.
     """
     if mode == "balanced":
         return AttentionPlan("balanced")
@@ -286,8 +287,11 @@ class MultiTokenStep:
         self.num_blocks = k_cache.shape[0]
         chunks = -(-T * (N // K) // 32)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        # the mma.sync column kernel tapers its partitions like the one-token kernel; the tcgen05
+        # one keeps them uniform
+        tc = bool(B.pkv_multi_uses_tcgen05(T, N, K, H))
         self.plan = plan_attention(nseq * chunks, K, block_tables.shape[1], sms,
-                                   partition_blocks=partition_blocks, taper=False)
+                                   partition_blocks=partition_blocks, taper=not tc)
         self.fused = False
         self.slot_mapping = torch.empty(nseq, T, dtype=torch.int64, device=dev)
         self.out = torch.empty(tuple(q.shape), dtype=q.dtype, device=dev)

@@ -139,6 +139,42 @@ def test_multi_in_kernel_merge_equals_separate_merge(pkv, oracle, T, N, K, H):
     assert_lse_close(l1.cpu().numpy().astype(np.float64), ref_lse, f"multi in-kernel merge T={T}")
 
 
+@pytest.mark.parametrize("T", [2, 4])
+def test_multi_tapered_partitions(pkv, oracle, T):
+    """With at least one (sequence, chunk, KV head) unit per SM and room for one more partition the
+    mma.sync column kernel tapers its partitions (partition 0, launched last, covers half a
+    partition).  Every row matches the oracle -- 0, 1, 2, 3 and many partitions, lengths on and
+    off the half-partition edge, lengths below T -- and the in-kernel merge equals pkv_lse_merge of
+    the same tapered partials (forced by 32 x max_partitions > 8192) bit for bit."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    K, G = 4, 4
+    B = -(-sms // K) + 2
+    lens = [0, 1, T - 1, 16, 17, 31, 32, 33, 48, 64, 65, 96, 97, 127, 128, 129, 200, 333, 700, 1000]
+    w = gen.make_workload(f"m_taper_{T}", 320 + T, K * G, K, 128, [lens[i % len(lens)] for i in range(B)])
+    assert w.B * w.K >= sms and not pkv.pkv_multi_uses_tcgen05(T, w.N, w.K, w.H)
+    c = MultiCase(oracle, w, T, 330 + T)
+    kc, vc = bf16_dev(c.kc), bf16_dev(c.vc)
+    q = bf16_dev(c.q)
+    pb = 4
+    P = pkv.tapered_partitions_for(w.max_blocks, pb)
+    assert P == pkv.max_partitions_for(w.max_blocks, pb) + 1
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for parts in (P, 300):
+        ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B * T, w.N, w.H, parts), dtype=torch.uint8, device="cuda")
+        out = torch.full_like(q, float("nan"))
+        lse = torch.full((w.B, T, w.N), float("nan"), dtype=torch.float32, device="cuda")
+        pkv.check(pkv.pkv_decode_attn_multi(q, kc, vc, i32_dev(w.block_tables), i32_dev(w.context_lens),
+                                            w.scale, out, lse, pb, parts, ws, err))
+        outs.append((out, lse))
+    assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
+    (o1, l1), (o2, l2) = outs
+    assert torch.equal(o1, o2) and torch.equal(l1, l2), "in-kernel merge differs from pkv_lse_merge"
+    ref, ref_lse = c.reference(oracle)
+    assert_close(out_f64(o1), ref, f"multi tapered T={T}")
+    assert_lse_close(l1.cpu().numpy().astype(np.float64), ref_lse, f"multi tapered T={T}")
+
+
 @pytest.mark.parametrize("part_blocks", [0, 3])
 def test_multi_with_one_token_is_the_decode_kernel(pkv, oracle, part_blocks):
     """T = 1 through the column-parallel kernel equals pkv_decode_attn / _splitk bit for bit."""
@@ -174,12 +210,20 @@ def test_multi_full_size_sampled(pkv, oracle):
     kc, vc = bf16_dev(c.kc), bf16_dev(c.vc)
     out, _ = run_multi(pkv, c, kc, vc, 0)
     out_s, _ = run_multi(pkv, c, kc, vc, 64)
+    # the multi-token step's own plan: 128-block partitions, tapered (512 units cover the SMs)
+    from paged_kv_decode_slot_gb300.step import MultiTokenStep
+    step = MultiTokenStep(bf16_dev(c.q), bf16_dev(c.k_new), bf16_dev(c.v_new), kc, vc, i32_dev(w.block_tables),
+                          i32_dev(w.context_lens), w.scale)
+    assert step.plan.mode == "split"
+    assert step.plan.max_partitions == pkv.tapered_partitions_for(w.max_blocks, step.plan.partition_blocks)
+    step.attention()
     sample = [0, 5, 31, 62]
     bt = np.ascontiguousarray(w.block_tables[sample])
     cl = np.ascontiguousarray(w.context_lens[sample])
     ref, _ = oracle.decode_multi(c.q[sample], c.kc, c.vc, bt, cl, w.scale)
     assert_close(out_f64(out[sample]), ref, "multi l3_8b_b64 one pass")
     assert_close(out_f64(out_s[sample]), ref, "multi l3_8b_b64 partitions")
+    assert_close(out_f64(step.out[sample]), ref, "multi l3_8b_b64 step plan (tapered)")
 
 
 # ------------------------------------ copy-on-write ----------------------------------------
