@@ -118,6 +118,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     const int lane = threadIdx.x & 31;
     const int G = p.G;
 
+    // The producers' first block-table entries do not depend on the context length: loaded
+    // before it (within the table row), their round trip overlaps its round trip.
+    const int first_blk = kSplit ? partition_first_block(part, p.part_blocks, p.taper != 0) : 0;
+    int tbl_first = 0;
+    if (warp >= kConsumerWarps) {
+        const int64_t j = first_blk + (warp - kConsumerWarps) + (int64_t)kProducers * lane;
+        if (j < p.max_nb) tbl_first = __ldg(p.block_tables + (size_t)b * p.max_nb + j);
+    }
     int ctx = p.context_lens[b];
     if (ctx < 0 || ctx > p.max_nb * kBlockSize) {
         if (threadIdx.x == 0 && kvh == 0 && part == 0) set_flag(p.err_flag, PKV_FLAG_CTX_RANGE);
@@ -196,7 +204,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
                 if (!bscale) return make_float2(0.f, 0.f);
                 const size_t si = (size_t)bid * p.scale_stride + kvh;
                 return make_float2(__ldg(p.k_scale + si), __ldg(p.v_scale + si));
-            });
+            },
+            true, tbl_first);
         if (lane == 0) issued_count[pw] = (int)issued;
     } else {
         // ------------------------------ consumer warps ------------------------------

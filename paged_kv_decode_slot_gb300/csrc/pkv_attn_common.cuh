@@ -577,6 +577,13 @@ __device__ __forceinline__ int partition_count(int nb, int pb, bool taper)
     return !taper ? (nb + pb - 1) / pb : (nb <= h ? 1 : 1 + (nb - h + pb - 1) / pb);
 }
 
+// First block of partition `part` whatever the sequence's length (partition_range's begin for a
+// partition that holds blocks).
+__device__ __forceinline__ int partition_first_block(int part, int pb, bool taper)
+{
+    return !taper ? part * pb : (part == 0 ? 0 : pb / 2 + (part - 1) * pb);
+}
+
 __device__ __forceinline__ void partition_range(int part, int nparts, int nb, int pb, bool taper, int &begin,
                                                 int &end)
 {
@@ -713,16 +720,20 @@ struct NoAux {
     __device__ __forceinline__ float2 operator()(int) const { return make_float2(0.f, 0.f); }
 };
 
+// `first` (have_first): lookup(pw + P * lane) already loaded by the caller -- a caller that knows
+// its table row before its tile count issues these loads early, overlapping their round trip with
+// whatever the count waits for.
 template <int P, bool kAux = false, typename Lookup, typename Issue, typename Aux = NoAux>
 __device__ __forceinline__ int64_t run_producer(int pw, int lane, int64_t n, Lookup lookup,
-                                                int num_blocks, int32_t *err_flag, Issue issue, Aux aux = Aux())
+                                                int num_blocks, int32_t *err_flag, Issue issue, Aux aux = Aux(),
+                                                bool have_first = false, int first = 0)
 {
     const int64_t mine = n > pw ? (n - pw + P - 1) / P : 0;
     auto fetch = [&](int bid) {
         if constexpr (kAux) return bid >= 0 && bid < num_blocks ? aux(bid) : make_float2(0.f, 0.f);
         return make_float2(0.f, 0.f);
     };
-    int cur = lane < mine ? lookup(pw + (int64_t)P * lane) : 0;
+    int cur = lane < mine ? (have_first ? first : lookup(pw + (int64_t)P * lane)) : 0;
     float2 cur_aux = lane < mine ? fetch(cur) : make_float2(0.f, 0.f);
     int64_t issued = 0;
     bool aborted = false;
