@@ -159,6 +159,17 @@ def test_attention_plan():
     assert p.mode == "split" and p.max_partitions == 8
 
 
+def test_launch_counts():
+    """Launches per partitioned call, as the entry points decide them: the one-token split merges
+    in its launch while G x max_partitions weights fit in 8192; the mma.sync column kernel while
+    32 x max_partitions do; the tcgen05 column kernel always merges in a second launch."""
+    import paged_kv_decode_slot_gb300 as pkv
+    assert pkv.IN_KERNEL_MERGE_WEIGHTS == 8192
+    assert pkv.split_attention_launches(32, 8, 2048) == 1 and pkv.split_attention_launches(32, 8, 2049) == 2
+    assert pkv.multi_attention_launches(256, False) == 1 and pkv.multi_attention_launches(257, False) == 2
+    assert pkv.multi_attention_launches(4, True) == 2
+
+
 def test_tapered_partition_count():
     """Partition 0 of half a partition, then whole ones: one more partition than the uniform
     layout needs unless the table ends within the first half partition."""
