@@ -139,8 +139,8 @@ def test_multi_in_kernel_merge_equals_separate_merge(pkv, oracle, T, N, K, H):
     assert_lse_close(l1.cpu().numpy().astype(np.float64), ref_lse, f"multi in-kernel merge T={T}")
 
 
-@pytest.mark.parametrize("T", [2, 4])
-def test_multi_tapered_partitions(pkv, oracle, T):
+@pytest.mark.parametrize("T,pb", [(2, 4), (4, 4), (4, 3)])
+def test_multi_tapered_partitions(pkv, oracle, T, pb):
     """With at least one (sequence, chunk, KV head) unit per SM and room for one more partition the
     mma.sync column kernel tapers its partitions (partition 0, launched last, covers half a
     partition).  Every row matches the oracle -- 0, 1, 2, 3 and many partitions, lengths on and
@@ -155,9 +155,8 @@ def test_multi_tapered_partitions(pkv, oracle, T):
     c = MultiCase(oracle, w, T, 330 + T)
     kc, vc = bf16_dev(c.kc), bf16_dev(c.vc)
     q = bf16_dev(c.q)
-    pb = 4
     P = pkv.tapered_partitions_for(w.max_blocks, pb)
-    assert P == pkv.max_partitions_for(w.max_blocks, pb) + 1
+    assert P >= pkv.max_partitions_for(w.max_blocks, pb)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     outs = []
     for parts in (P, 300):
