@@ -70,8 +70,8 @@ __device__ __forceinline__ void tile_update_cols(WarpAcc<H> &a, const uint32_t (
     const bool needA = mA > a.m[0] + kRescaleThreshold;
     const bool needB = mB > a.m[1] + kRescaleThreshold;
     if (__any_sync(0xFFFFFFFFu, needA || needB)) {
-        const float alphaA = needA ? exp2f(a.m[0] - mA) : 1.f;
-        const float alphaB = needB ? exp2f(a.m[1] - mB) : 1.f;
+        const float alphaA = needA ? exp2_sfu(a.m[0] - mA) : 1.f;
+        const float alphaB = needB ? exp2_sfu(a.m[1] - mB) : 1.f;
         if (needA) a.m[0] = mA;
         if (needB) a.m[1] = mB;
         a.l[0] *= alphaA;
@@ -86,8 +86,8 @@ __device__ __forceinline__ void tile_update_cols(WarpAcc<H> &a, const uint32_t (
     }
     const float baseA = a.m[0] == -INFINITY ? 0.f : a.m[0];
     const float baseB = a.m[1] == -INFINITY ? 0.f : a.m[1];
-    const uint32_t p01 = pack_bf16x2(exp2f(x0 - baseA), exp2f(x1 - baseB));
-    const uint32_t p23 = pack_bf16x2(exp2f(x2 - baseA), exp2f(x3 - baseB));
+    const uint32_t p01 = pack_bf16x2(exp2_sfu(x0 - baseA), exp2_sfu(x1 - baseB));
+    const uint32_t p23 = pack_bf16x2(exp2_sfu(x2 - baseA), exp2_sfu(x3 - baseB));
     a.l[0] += bf16x2_lo(p01) + bf16x2_lo(p23);
     a.l[1] += bf16x2_hi(p01) + bf16x2_hi(p23);
     const uint32_t pb0 = movmatrix_trans(p01);
@@ -260,7 +260,7 @@ attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             if (M != -INFINITY) {
                 for (int rr = 0; rr < R; ++rr) {
                     const int w = cg + ng * rr;
-                    const float sc = exp2f(mm[w * 8 + g8] - M);
+                    const float sc = exp2_sfu(mm[w * 8 + g8] - M);
                     lsum += sc * ml[w * 8 + g8];
                     accv += sc * mo[(w * 8 + g8) * H + h];
                 }

@@ -181,8 +181,8 @@ __device__ __forceinline__ void tile_update(WarpAcc<H> &a, const uint32_t (&qf)[
     const bool needA = mA > a.m[0] + kRescaleThreshold;
     const bool needB = mB > a.m[1] + kRescaleThreshold;
     if (__any_sync(0xFFFFFFFFu, needA || needB)) {
-        const float alphaA = needA ? exp2f(a.m[0] - mA) : 1.f;
-        const float alphaB = needB ? exp2f(a.m[1] - mB) : 1.f;
+        const float alphaA = needA ? exp2_sfu(a.m[0] - mA) : 1.f;
+        const float alphaB = needB ? exp2_sfu(a.m[1] - mB) : 1.f;
         if (needA) a.m[0] = mA;
         if (needB) a.m[1] = mB;
         a.l[0] *= alphaA;
@@ -195,8 +195,8 @@ __device__ __forceinline__ void tile_update(WarpAcc<H> &a, const uint32_t (&qf)[
             a.o[mt][3] *= alphaB;
         }
     }
-    const uint32_t p01 = pack_bf16x2(exp2f(x0 - a.m[0]), exp2f(x1 - a.m[1]));
-    const uint32_t p23 = pack_bf16x2(exp2f(x2 - a.m[0]), exp2f(x3 - a.m[1]));
+    const uint32_t p01 = pack_bf16x2(exp2_sfu(x0 - a.m[0]), exp2_sfu(x1 - a.m[1]));
+    const uint32_t p23 = pack_bf16x2(exp2_sfu(x2 - a.m[0]), exp2_sfu(x3 - a.m[1]));
     a.l[0] += bf16x2_lo(p01) + bf16x2_lo(p23);  // sums of the rounded weights
     a.l[1] += bf16x2_hi(p01) + bf16x2_hi(p23);
     const uint32_t pb0 = movmatrix_trans(p01);    // P^T rows tok 0-7 -> B fragment
@@ -300,8 +300,8 @@ __device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&
     const bool needA = mA > a.m[0] + kRescaleThreshold;
     const bool needB = mB > a.m[1] + kRescaleThreshold;
     if (__any_sync(0xFFFFFFFFu, needA || needB)) {
-        const float alphaA = needA ? exp2f(a.m[0] - mA) : 1.f;
-        const float alphaB = needB ? exp2f(a.m[1] - mB) : 1.f;
+        const float alphaA = needA ? exp2_sfu(a.m[0] - mA) : 1.f;
+        const float alphaB = needB ? exp2_sfu(a.m[1] - mB) : 1.f;
         if (needA) a.m[0] = mA;
         if (needB) a.m[1] = mB;
         a.l[0] *= alphaA;
@@ -314,8 +314,8 @@ __device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&
             a.o[mt][3] *= alphaB;
         }
     }
-    const uint32_t p01 = pack_f16x2(exp2f(x0 - a.m[0]) * vsr, exp2f(x1 - a.m[1]) * vsr);
-    const uint32_t p23 = pack_f16x2(exp2f(x2 - a.m[0]) * vsr, exp2f(x3 - a.m[1]) * vsr);
+    const uint32_t p01 = pack_f16x2(exp2_sfu(x0 - a.m[0]) * vsr, exp2_sfu(x1 - a.m[1]) * vsr);
+    const uint32_t p23 = pack_f16x2(exp2_sfu(x2 - a.m[0]) * vsr, exp2_sfu(x3 - a.m[1]) * vsr);
     a.l[0] += (f16x2_lo(p01) + f16x2_lo(p23)) * ivs;
     a.l[1] += (f16x2_hi(p01) + f16x2_hi(p23)) * ivs;
     const uint32_t pb0 = movmatrix_trans(p01);
@@ -413,8 +413,8 @@ __device__ __forceinline__ void tile_update_fp8_n(WarpAcc<H> &a, const uint32_t 
     const bool needA = mA > a.m[0] + kRescaleThreshold;
     const bool needB = mB > a.m[1] + kRescaleThreshold;
     if (__any_sync(0xFFFFFFFFu, needA || needB)) {
-        const float alphaA = needA ? exp2f(a.m[0] - mA) : 1.f;
-        const float alphaB = needB ? exp2f(a.m[1] - mB) : 1.f;
+        const float alphaA = needA ? exp2_sfu(a.m[0] - mA) : 1.f;
+        const float alphaB = needB ? exp2_sfu(a.m[1] - mB) : 1.f;
         if (needA) a.m[0] = mA;
         if (needB) a.m[1] = mB;
         a.l[0] *= alphaA;
@@ -433,8 +433,8 @@ __device__ __forceinline__ void tile_update_fp8_n(WarpAcc<H> &a, const uint32_t 
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         const float r_t = kBS ? vsr[t] : 1.f, ir_t = kBS ? ivs[t] : 1.f;
-        const uint32_t p01 = pack_f16x2(exp2f(x[t][0] - baseA) * r_t, exp2f(x[t][1] - baseB) * r_t);
-        const uint32_t p23 = pack_f16x2(exp2f(x[t][2] - baseA) * r_t, exp2f(x[t][3] - baseB) * r_t);
+        const uint32_t p01 = pack_f16x2(exp2_sfu(x[t][0] - baseA) * r_t, exp2_sfu(x[t][1] - baseB) * r_t);
+        const uint32_t p23 = pack_f16x2(exp2_sfu(x[t][2] - baseA) * r_t, exp2_sfu(x[t][3] - baseB) * r_t);
         a.l[0] += (f16x2_lo(p01) + f16x2_lo(p23)) * ir_t;
         a.l[1] += (f16x2_hi(p01) + f16x2_hi(p23)) * ir_t;
         pb[t][0] = movmatrix_trans(p01);
@@ -518,7 +518,7 @@ __device__ __forceinline__ void combine(const float *mo, const float *mm, const 
     if (M != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < W; ++w) {
-            const float sc = exp2f(mm[w * 8 + g] - M);
+            const float sc = exp2_sfu(mm[w * 8 + g] - M);
             lsum += sc * ml[w * 8 + g];
             acc += sc * mo[(w * 8 + g) * H + h];
         }

@@ -353,7 +353,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             }
             const bool need = mx > m + kRescaleThreshold;
             if (__any_sync(0xFFFFFFFFu, need)) {
-                const float alpha = need ? exp2f(m - mx) : 1.f;
+                const float alpha = need ? exp2_sfu(m - mx) : 1.f;
                 if (need) m = mx;
                 l *= alpha;
                 if (g > 0) {
@@ -382,7 +382,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             uint32_t pk[2][16];
 #pragma unroll
             for (int c = 0; c < GT * 8; ++c) {
-                const uint32_t v = pack_bf16x2(exp2f(x[2 * c] - bm), exp2f(x[2 * c + 1] - bm));
+                const uint32_t v = pack_bf16x2(exp2_sfu(x[2 * c] - bm), exp2_sfu(x[2 * c + 1] - bm));
                 pk[c >> 4][c & 15] = v;
                 l += bf16x2_lo(v) + bf16x2_hi(v);  // the sum of the weights PV uses
             }

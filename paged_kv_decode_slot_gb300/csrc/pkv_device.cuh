@@ -200,6 +200,16 @@ __device__ __forceinline__ float f16x2_hi(uint32_t v)
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32): one instruction; results below
+// 2^-126 flush to zero -- softmax weights that small vanish next to the row's largest, 1 -- and
+// 2^-inf = +0, so masked logits get zero weight.
+__device__ __forceinline__ float exp2_sfu(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- warp-level bf16 MMA (m16n8k16, fp32 accumulate) -----------------------------------
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
 {
