@@ -174,9 +174,10 @@ int pkv_decode_attn_splitk(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
  * block's row ctx-1 with the new K/V on chip and writes it to the pools, so no separate append
  * pass runs ("Optimización de la inferencia", "Cache de KV": only the new token's K/V is
  * computed and joined to the cache; CUDA graphs / fused kernels: CS336 Lecture 10 notes,
- * "其他优化").  partition_blocks 0 = single pass (workspace unused, may be NULL); > 0 = fixed
- * partitions with the workspace of pkv_decode_attn_splitk.  k_new/v_new 16-byte aligned.
- * Results are bit-identical to the three separate calls.
+ * "其他优化").  partition_blocks 0 = single pass (workspace unused, may be NULL); > 0 =
+ * partitions laid out as in pkv_decode_attn_splitk (tapered under the same conditions), with
+ * its workspace.  k_new/v_new 16-byte aligned.  Results are bit-identical to the three separate
+ * calls.
  */
 int pkv_decode_step(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
                     pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *block_tables,
@@ -219,7 +220,8 @@ int pkv_append_fp8(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const float *k_
                    int32_t *err_flag, pkv_stream_t stream);
 
 /* Decode attention over e4m3 pools: partition_blocks 0 = single pass (workspace unused),
-   > 0 = fixed partitions + log-sum-exp merge with the workspace of pkv_decode_attn_splitk.
+   > 0 = partitions as in pkv_decode_attn_splitk (tapered under the same conditions) + log-sum-exp
+   merge, with its workspace.
    q 8-byte aligned. */
 int pkv_decode_attn_fp8(const pkv_bf16 *q, const uint8_t *k_cache, const uint8_t *v_cache,
                         const float *k_scale, const float *v_scale, int32_t scale_block_stride,
