@@ -263,7 +263,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_s * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)",
-            "config": config_dict(w, "none (host run)"),
+            "config": config_dict(w, args),
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -307,17 +307,30 @@ def kernel_label(args, plan, step) -> str:
         if step.launches_per_step() - (0 if step.fused else 2) == 1:
             return f"attn_kernel<128,1,{fp8}> (partitions merged in the same launch)"
         return f"attn_kernel<128,1,{fp8}> + lse_merge_kernel"
-    return {"single": f"attn_kernel<128,0,{fp8}>",
-            "balanced": "attn_balanced_kernel + balanced_merge_kernel"}[plan.mode]
+    return f"attn_kernel<128,0,{fp8}>"
 
 
-def config_dict(w, flush: str, plan=None) -> dict:
+L2_PROTOCOL = ("flushed between GPU steps: write of one 2x-L2 buffer, then read of another, outside "
+               "the timed events")
+
+
+def config_dict(w, args) -> dict:
+    """The workload and the timing protocol: the same dict in both arms of the benchmark (the plan
+    the GPU arm picked is reported beside it, under "attention")."""
     d = {"workload": w.name, "batch": w.B, "q_heads": w.N, "kv_heads": w.K, "head_dim": w.H,
          "block_size": 16, "total_context_tokens": w.total_tokens,
          "max_context": int(w.context_lens.max()), "pool_blocks": w.num_blocks,
-         "l2": flush, "parallelism": "replicas"}
-    if plan is not None:
-        d["attention"] = plan.describe()
+         "l2": L2_PROTOCOL, "parallelism": "replicas"}
+    opt = lambda name, default: getattr(args, name, default)  # noqa: E731
+    if opt("tokens", 1) > 1:
+        d["new_tokens_per_seq"] = args.tokens
+    if opt("layers", 1) > 1:
+        d["layers"] = args.layers
+    if opt("attn", "auto") == "prefix":
+        d["prefix_groups"] = "one group of the whole batch sharing its full prefix blocks"
+    if opt("kv", "bf16") == "fp8":
+        d["kv_cache"] = ("e4m3, per-KV-head scales (amax / 448)" if opt("fp8_scales", "head") == "head"
+                         else "e4m3, per-(block, KV head) scales (amax / 448)")
     return d
 
 
@@ -364,7 +377,7 @@ def run_ours(args):
         knm = d16(gen.normal_bf16(w.seed, 901, (w.B, T, w.K, w.H)))
         vnm = d16(gen.normal_bf16(w.seed, 902, (w.B, T, w.K, w.H)))
         step = MultiTokenStep(qm, knm, vnm, kc, vc, bt, cl, w.scale,
-                              partition_blocks=args.partition_blocks, err_flag=err)
+                              partition_blocks=args.partition_blocks, err_flag=err, fused=not args.unfused)
         plan = step.plan
     elif args.attn == "prefix":
         groups = w.prefix_groups()
@@ -377,7 +390,7 @@ def run_ours(args):
                                 prefix_partition_blocks=args.prefix_partition_blocks, err_flag=err)
         plan = step.plan
     elif args.kv == "fp8":
-        if args.unfused or plan.mode == "balanced":
+        if args.unfused:
             raise SystemExit("--kv fp8 runs the fused single-pass or split step only")
         # scales from the cache's own absolute maxima (NaN tail poison ignored): per KV head, or
         # per (physical block, KV head)
@@ -563,7 +576,8 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if args.kv == "bf16" else "e4m3 KV (f16 mma, fp32 softmax)",
         "data": "synthetic (seeded)",
-        "config": config_dict(w, "flushed between steps: write of one 2x-L2 buffer, then read of another, outside the timed events", plan),
+        "config": config_dict(w, args),
+        "attention": plan.describe(),
         "us_per_step": mean_step * 1e3,
         "us_per_step_median": statistics.median(step_ms) * 1e3,
         "us_per_step_best": min(step_ms) * 1e3,
@@ -589,17 +603,10 @@ def run_ours(args):
         "wall_s_timed_region": t_wall,
         "step_bytes": nbytes["step"],
     }
-    if args.tokens > 1:
-        line["config"]["new_tokens_per_seq"] = args.tokens
     if args.layers > 1:
-        line["config"]["layers"] = args.layers
         line["us_per_layer"] = mean_step * 1e3 / args.layers
         line["graph"]["us_per_layer"] = line["graph"]["us_per_step"] / args.layers
-    if args.attn == "prefix":
-        line["config"]["prefix_groups"] = "one group of the whole batch sharing its full prefix blocks"
     if args.kv == "fp8":
-        line["config"]["kv_cache"] = ("e4m3, per-KV-head scales (amax / 448)" if args.fp8_scales == "head"
-                                      else "e4m3, per-(block, KV head) scales (amax / 448)")
         line["kv_gbs"] = args.layers * w.kv_bytes() / 2 / (mean_attn * 1e-3) / 1e9
         line["kv_gbs_bf16_equivalent"] = args.layers * w.kv_bytes() / (mean_attn * 1e-3) / 1e9
     if w.unique_tokens is not None:
@@ -612,7 +619,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
@@ -620,7 +627,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--partition-blocks", type=int, default=None)
-    ap.add_argument("--mode", choices=("single", "balanced", "split"), default=None,
+    ap.add_argument("--mode", choices=("single", "split"), default=None,
                     help="force an attention mode (split needs --partition-blocks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv", choices=("bf16", "fp8"), default="bf16",
@@ -637,9 +644,14 @@ def main():
                     help="with --attn prefix: blocks per partition of the shared-prefix pass")
     ap.add_argument("--unfused", action="store_true",
                     help="separate slot-mapping, append and attention launches")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    return args
+
+
+def main():
+    args = parse_args()
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -35,7 +35,8 @@
  * NVLink-C2C, so a step's inputs and outputs need no separate copies.  The library allocates
  * nothing and keeps no state between calls besides cached device attributes (and the static
  * scratch of pkv_decode_attn_splitk_noalloc, described there).  Calls are asynchronous on the
- * given stream (0 = the legacy default stream).
+ * given stream (0 = the legacy default stream).  Those caches are per device and live as long as
+ * the process: resetting a device (cudaDeviceReset) while the library is loaded is not supported.
  *
  * Errors: each call returns a pkv_status.  Host-side validation happens
  * before anything is launched.  Bad values that only the device sees (a
@@ -244,32 +245,6 @@ int pkv_decode_step_fp8(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16
                         int32_t *err_flag, pkv_stream_t stream);
 
 /*
- * Workspace for pkv_decode_attn_balanced: two partial-output slots per CTA of the persistent
- * grid (about 2 CTAs per SM of the current device, a multiple of num_kv_heads) and a
- * per-sequence block prefix.  Queries the current device's SM count; returns 0 on error.
- */
-size_t pkv_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim);
-
-/*
- * Split-KV decode attention with balanced partitions (FlashDecoding's split, CS336 Lecture 10
- * notes "其他优化", cut so every SM gets the same work).  For each KV head the (sequence,
- * block) tiles are numbered in order and split into equal shares, one per CTA of a persistent
- * grid (about 2 CTAs per SM; CTA c serves head c % K); a unit (sequence, KV head) that falls
- * inside one share is finished there, one cut by share
- * boundaries is merged from its pieces' (partial output, lse) by a second, stream-ordered
- * launch with the log-sum-exp formula of pkv_lse_merge.  Same arguments and results as
- * pkv_decode_attn plus a caller-owned, 256-byte aligned workspace of at least
- * pkv_balanced_workspace_bytes(num_seqs, H) bytes.  num_seqs <= 1024 (PKV_ERR_UNSUPPORTED
- * otherwise).
- */
-int pkv_decode_attn_balanced(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
-                             const int32_t *block_tables, int32_t max_blocks_per_seq,
-                             const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
-                             float scale, pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
-                             void *workspace, size_t workspace_bytes, int32_t *err_flag,
-                             pkv_stream_t stream);
-
-/*
  * Size of the static scratch used by pkv_decode_attn_splitk_noalloc (8 MiB).
  */
 #define PKV_STATIC_SCRATCH_BYTES (8u << 20)
@@ -284,9 +259,14 @@ int pkv_decode_attn_balanced(const pkv_bf16 *q, const pkv_bf16 *k_cache, const p
  * library holds until the process exits.
  *  - If pkv_splitk_workspace_bytes(num_seqs, N, H, max_partitions) exceeds
  *    PKV_STATIC_SCRATCH_BYTES the call returns PKV_ERR_WORKSPACE (pkv_last_error() says
- *    how much was needed) and launches nothing.
+ *    how much was needed) and launches nothing; so does every other refusal (max_partitions
+ *    beyond 12288: PKV_ERR_UNSUPPORTED; partitions that do not cover the table: PKV_ERR_SHAPE).
  *  - The first call on a device looks up the scratch's device address with that device
- *    current (cudaGetSymbolAddress); make that first call before any stream capture.
+ *    current (cudaGetSymbolAddress); make that first call before any stream capture.  A call
+ *    with num_seqs = 0 (all pointers may then be any non-NULL, suitably aligned values) launches
+ *    nothing but does that lookup, so a caller can prepare each device before its first real
+ *    call.  The address stays valid until the process exits (see the note on device resets
+ *    above).
  *  - All calls share the one array and it keeps the last call's contents; nothing in it has
  *    to start at zero.  Calls that overlap on the GPU (e.g. on two streams) race on it: order
  *    them on one stream or with events.
@@ -381,19 +361,31 @@ int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_
                           void *workspace, size_t workspace_bytes, int32_t *err_flag,
                           pkv_stream_t stream);
 
+/* The whole verification step in one launch (two with the tcgen05 kernel's separate merge):
+   pkv_slot_mapping_multi + pkv_append + pkv_decode_attn_multi fused.  k_new, v_new bf16
+   [num_seqs][T][K][H] (16-byte aligned) are the T new tokens' keys and values; token t goes to the
+   slot of position ctx - T + t (none below position 0) and slot_mapping_out int64 [num_seqs][T]
+   (nullable, 8-byte aligned) receives those slots, -1 below position 0 or for a block id outside
+   the pool (PKV_FLAG_BLOCK_RANGE).  The CTA that loads a block holding new positions first writes
+   those rows into the pools (its KV head's part) and orders the writes before its own tile load,
+   so attention reads them in the same pass ("Week 11. Inference", Step 3: gamma + 1 tokens checked
+   in one pass; CS336 Lecture 10 notes, "其他优化": fused kernels).  Other arguments, the
+   partition layout and the results are those of pkv_decode_attn_multi, bit for bit; the pools
+   afterwards equal what pkv_append leaves. */
+int pkv_decode_step_multi(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                          pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *block_tables,
+                          int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                          int32_t num_new, int32_t num_q_heads, float scale, pkv_bf16 *out,
+                          float *lse_out, int64_t *slot_mapping_out, pkv_cache_desc cache,
+                          int32_t partition_blocks, int32_t max_partitions, void *workspace,
+                          size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream);
+
 /* Limit (ns, default 2e9) of every bounded wait inside the attention kernels, for the calls
    launched after it is set (process-wide); returns the previous limit (0 sets 1 ns).  An
    expired wait sets PKV_FLAG_TIMEOUT and voids the unit's result: the kernel stops issuing,
    drains the copies it started, releases what it holds and returns, and a later call with the
    default limit runs normally.  Lowering it is a way to exercise those paths. */
 uint64_t pkv_set_wait_limit_ns(uint64_t limit_ns);
-
-/* Test hook for the expiry paths: in the attention launches that follow (process-wide), every
-   CTA's producer skips its tile `tile` (0-based within the CTA's block list): it neither loads
-   it nor signals it, so the consumer's bounded wait on it expires (PKV_FLAG_TIMEOUT) and the
-   CTA takes its abort path -- drain, void result, release, return -- with no fault and no hang.
-   -1 switches it off (the default); returns the previous value.  Results are void while set. */
-int64_t pkv_debug_withhold_tile(int64_t tile);
 
 /* Self-test of the bounded waits: one warp waits, with the attention kernels' bounded wait, on
    an mbarrier that nothing ever completes; after the current wait limit it gives up and sets

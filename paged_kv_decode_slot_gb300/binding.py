@@ -252,31 +252,6 @@ def pkv_decode_attn_splitk(q, k_cache, v_cache, block_tables, context_lens, scal
                                        workspace.numel(), _ptr(err_flag), _stream(stream))
 
 
-_lib.pkv_balanced_workspace_bytes.argtypes = [_I32, _I32, _I32]
-_lib.pkv_balanced_workspace_bytes.restype = ctypes.c_size_t
-_lib.pkv_decode_attn_balanced.argtypes = [_P, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P,
-                                          _P, CacheDesc, _P, ctypes.c_size_t, _P, _P]
-MAX_BALANCED_SEQS = 1024
-
-
-def pkv_balanced_workspace_bytes(num_seqs: int, num_kv_heads: int, head_dim: int) -> int:
-    return int(_lib.pkv_balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim))
-
-
-def pkv_decode_attn_balanced(q, k_cache, v_cache, block_tables, context_lens, scale: float, out,
-                             workspace, lse_out=None, err_flag=None, stream=None) -> int:
-    _attn_common(q, k_cache, v_cache, block_tables, context_lens)
-    _need(out, torch.bfloat16, 3, "out")
-    _opt(lse_out, torch.float32, 2, "lse_out")
-    _opt(err_flag, torch.int32, 1, "err_flag")
-    _need(workspace, torch.uint8, 1, "workspace")
-    B, N, _ = q.shape
-    return _lib.pkv_decode_attn_balanced(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                         block_tables.shape[1], _ptr(context_lens), B, N, float(scale),
-                                         _ptr(out), _ptr(lse_out), cache_desc(k_cache), _ptr(workspace),
-                                         workspace.numel(), _ptr(err_flag), _stream(stream))
-
-
 _lib.pkv_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P, _P,
                                  _P, CacheDesc, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
 
@@ -451,12 +426,19 @@ _lib.pkv_set_wait_limit_ns.restype = ctypes.c_uint64
 
 
 _lib.pkv_check_wait_expiry.argtypes = [_P, _P]
-_lib.pkv_debug_withhold_tile.argtypes = [ctypes.c_int64]
-_lib.pkv_debug_withhold_tile.restype = ctypes.c_int64
+# Test builds of the library (-DPKV_TEST_HOOKS, loaded through PKV_LIBRARY) also export
+# pkv_debug_withhold_tile; the product library does not.
+HAS_TEST_HOOKS = hasattr(_lib, "pkv_debug_withhold_tile")
+if HAS_TEST_HOOKS:
+    _lib.pkv_debug_withhold_tile.argtypes = [ctypes.c_int64]
+    _lib.pkv_debug_withhold_tile.restype = ctypes.c_int64
 
 
 def pkv_debug_withhold_tile(tile: int) -> int:
-    """Test hook: the attention producers skip this tile of every CTA (-1: off); returns the previous."""
+    """Test builds only: the attention producers skip this tile of every CTA (-1: off); returns
+    the previous value.  Raises on the product library, which has no such hook."""
+    if not HAS_TEST_HOOKS:
+        raise RuntimeError("pkv_debug_withhold_tile exists only in test builds (-DPKV_TEST_HOOKS)")
     return int(_lib.pkv_debug_withhold_tile(int(tile)))
 
 
@@ -507,6 +489,38 @@ def pkv_decode_attn_multi(q, k_cache, v_cache, block_tables, context_lens, scale
                                       block_tables.shape[1], _ptr(context_lens), B, T, N, float(scale),
                                       _ptr(out), _ptr(lse_out), cache_desc(k_cache), partition_blocks,
                                       max_partitions, _ptr(workspace),
+                                      0 if workspace is None else workspace.numel(), _ptr(err_flag),
+                                      _stream(stream))
+
+
+_lib.pkv_decode_step_multi.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _I32, ctypes.c_float, _P,
+                                       _P, _P, CacheDesc, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
+
+
+def pkv_decode_step_multi(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale: float, out,
+                          lse_out=None, slot_mapping=None, partition_blocks: int = 0, max_partitions: int = 0,
+                          workspace=None, err_flag=None, stream=None) -> int:
+    """q, out bf16 [B, T, N, H]; k_new, v_new bf16 [B, T, K, H]; lse_out float32 [B, T, N];
+    slot_mapping int64 [B, T] (written)."""
+    _need(q, torch.bfloat16, 4, "q")
+    _need(k_new, torch.bfloat16, 4, "k_new")
+    _need(v_new, torch.bfloat16, 4, "v_new")
+    _need(k_cache, torch.bfloat16, 4, "k_cache")
+    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    _need(block_tables, torch.int32, 2, "block_tables")
+    _need(context_lens, torch.int32, 1, "context_lens")
+    _need(out, torch.bfloat16, 4, "out")
+    _opt(lse_out, torch.float32, 3, "lse_out")
+    _opt(slot_mapping, torch.int64, 2, "slot_mapping")
+    _opt(workspace, torch.uint8, 1, "workspace")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    B, T, N, _ = q.shape
+    if tuple(k_new.shape) != (B, T, k_cache.shape[2], k_cache.shape[3]) or k_new.shape != v_new.shape:
+        raise ValueError("k_new / v_new must be [B, T, K, H]")
+    return _lib.pkv_decode_step_multi(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, T, N,
+                                      float(scale), _ptr(out), _ptr(lse_out), _ptr(slot_mapping),
+                                      cache_desc(k_cache), partition_blocks, max_partitions, _ptr(workspace),
                                       0 if workspace is None else workspace.numel(), _ptr(err_flag),
                                       _stream(stream))
 

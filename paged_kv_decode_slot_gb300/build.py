@@ -24,10 +24,10 @@ def nvcc_path() -> str:
     raise RuntimeError("nvcc not found: libpagedkv needs the CUDA toolkit to build")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "pkv.h"),
                                                                   os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)
@@ -37,14 +37,16 @@ def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool =
                   out: str | None = None, defines=(), build_dir: str | None = None) -> str:
     """Compile every .cu to an object in _build/, link libpagedkv.so next to this file.
 
-    ``out``/``defines``/``build_dir`` build a variant elsewhere (e.g. other pipeline depths via
-    -DPKV_STAGES=...); the default build is the in-tree library the package loads.
+    ``out``/``defines``/``build_dir`` build a variant elsewhere (e.g. the test build with
+    -DPKV_TEST_HOOKS, or other pipeline depths via -DPKV_STAGES=...; a variant is rebuilt when any
+    source is newer than it, so give each set of defines its own ``out`` and ``build_dir``); the
+    default build is the in-tree library the package loads.
     """
     variant = out is not None
     out = out or LIB_PATH
     bdir = build_dir or BUILD_DIR
-    if not variant and not force and not _stale():
-        return LIB_PATH
+    if not force and not _stale(out):
+        return out
     nvcc = nvcc_path()
     os.makedirs(bdir, exist_ok=True)
     common = [nvcc, "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",

@@ -115,8 +115,10 @@ int g_tok_major = -1;  // layout the driver accepted first (-1: not yet known)
 std::mutex g_layout_mu;
 // limit of every bounded wait inside the attention kernels (pkv_set_wait_limit_ns)
 std::atomic<uint64_t> g_wait_ns{pkv::kWaitLimitNs};
-// test hook: a tile index that the attention kernels' producers skip (-1: none)
+#ifdef PKV_TEST_HOOKS
+// test builds only: a tile index that the attention kernels' producers skip (-1: none)
 std::atomic<int64_t> g_withhold_tile{-1};
+#endif
 
 int make_kv_maps(CUtensorMap *tk, CUtensorMap *tv, const void *k, const void *v,
                  const pkv_cache_desc &d, int *tok_major)
@@ -182,7 +184,9 @@ pkv::AttnParams params_of(const AttnArgs &a, int tok_major)
     p.tok_major = tok_major;
     p.err_flag = a.err_flag;
     p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+#ifdef PKV_TEST_HOOKS
     p.withhold_tile = g_withhold_tile.load(std::memory_order_relaxed);
+#endif
     return p;
 }
 
@@ -659,92 +663,6 @@ PKV_EXPORT int pkv_decode_step_fp8(const pkv_bf16 *q, const pkv_bf16 *k_new, con
                          partition_blocks, max_partitions, workspace, workspace_bytes, stream);
 }
 
-// ---- balanced split (persistent grid, equal tile shares) -----------------------------------
-namespace {
-
-
-// The balanced kernel's CTAs per SM times the SM count, rounded down to a multiple of the KV
-// head count: CTA c = share * K + head.  The merge holds at most 512 pieces of one unit.
-int balanced_grid(int sms, int32_t K)
-{
-    int shares = pkv::balanced_ctas_per_sm() * sms / K;
-    if (shares < 1) shares = 1;
-    if (shares > 512) shares = 512;
-    return shares * K;
-}
-
-struct BalancedWs {
-    int64_t lse_off, pre_off, bytes;
-};
-
-// part_out [grid][2][8][H] float, part_lse [grid][2][8] float, prefix int64 [B + 1]
-BalancedWs balanced_ws_layout(int grid, int32_t B, int32_t H)
-{
-    auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
-    const int64_t slots = (int64_t)grid * 2 * 8;
-    BalancedWs w;
-    w.lse_off = up(slots * H * 4);
-    w.pre_off = w.lse_off + up(slots * 4);
-    w.bytes = w.pre_off + (int64_t)(B + 1) * 8;
-    return w;
-}
-
-}  // namespace
-
-PKV_EXPORT size_t pkv_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads,
-                                               int32_t head_dim)
-{
-    int sms = 0;
-    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || sm_count(&sms) != PKV_OK) return 0;
-    return (size_t)balanced_ws_layout(balanced_grid(sms, num_kv_heads), num_seqs, head_dim).bytes;
-}
-
-PKV_EXPORT int pkv_decode_attn_balanced(const pkv_bf16 *q, const pkv_bf16 *k_cache,
-                                        const pkv_bf16 *v_cache, const int32_t *block_tables,
-                                        int32_t max_blocks_per_seq, const int32_t *context_lens,
-                                        int32_t num_seqs, int32_t num_q_heads, float scale,
-                                        pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
-                                        void *workspace, size_t workspace_bytes, int32_t *err_flag,
-                                        pkv_stream_t stream)
-{
-    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-               num_q_heads, scale, cache, err_flag};
-    if (!out) return PKV_ERR_NULL;
-    int st = validate_attn(a);
-    if (st != PKV_OK) return st;
-    if (num_seqs > pkv::kMaxBalancedSeqs) return PKV_ERR_UNSUPPORTED;
-    if (!workspace) return PKV_ERR_WORKSPACE;
-    if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
-    if (!aligned(out, 4) || !aligned(lse_out, 4)) return PKV_ERR_ALIGN;
-    if (num_seqs == 0) return PKV_OK;
-    int sms = 0;
-    st = sm_count(&sms);
-    if (st != PKV_OK) return st;
-    if (workspace_bytes < pkv_balanced_workspace_bytes(num_seqs, cache.num_kv_heads, cache.head_dim))
-        return PKV_ERR_WORKSPACE;
-    // tile indices times the share count must stay within int64 inside the kernels
-    const double tiles_max = (double)num_seqs * max_blocks_per_seq;
-    if (tiles_max * 1024.0 > 4.0e18) return PKV_ERR_SHAPE;
-    CUtensorMap tk, tv;
-    int tok_major = 0;
-    st = make_kv_maps(&tk, &tv, k_cache, v_cache, cache, &tok_major);
-    if (st != PKV_OK) return st;
-    const int grid = balanced_grid(sms, cache.num_kv_heads);
-    const BalancedWs lay = balanced_ws_layout(grid, num_seqs, cache.head_dim);
-    char *ws = static_cast<char *>(workspace);
-    pkv::AttnParams p = params_of(a, tok_major);
-    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
-    p.lse_out = lse_out;
-    p.part_out = reinterpret_cast<float *>(ws);
-    p.part_lse = reinterpret_cast<float *>(ws + lay.lse_off);
-    p.prefix_out = reinterpret_cast<int64_t *>(ws + lay.pre_off);
-    cudaError_t e = pkv::launch_attn_balanced(cache.head_dim, tk, tv, p, grid, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "balanced attention launch");
-    e = pkv::launch_balanced_merge(p.part_out, p.part_lse, p.prefix_out, num_seqs, num_q_heads,
-                                   cache.num_kv_heads, cache.head_dim, grid, 1, out, lse_out, stream);
-    return e == cudaSuccess ? PKV_OK : cuda_fail(e, "balanced merge launch");
-}
-
 PKV_EXPORT int pkv_gather(const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
                           const int32_t *block_tables, int32_t max_blocks_per_seq,
                           const int32_t *context_lens, const int64_t *cu_seqlens, int32_t num_seqs,
@@ -853,6 +771,9 @@ PKV_EXPORT int pkv_decode_attn_splitk_noalloc(const pkv_bf16 *q, const pkv_bf16 
     if (st != PKV_OK) return st;
     if (partition_blocks <= 0 || max_partitions <= 0) return PKV_ERR_SHAPE;
     if (!aligned(out, 4) || !aligned(lse_out, 4)) return PKV_ERR_ALIGN;
+    // every refusal comes before anything is launched: the separate merge's own limit included
+    if (max_partitions > kMaxMergeParts) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)max_partitions * partition_blocks < max_blocks_per_seq) return PKV_ERR_SHAPE;
     const size_t need = pkv_splitk_workspace_bytes(num_seqs, num_q_heads, cache.head_dim,
                                                    max_partitions);
     if (need > (size_t)PKV_STATIC_SCRATCH_BYTES) {
@@ -862,10 +783,11 @@ PKV_EXPORT int pkv_decode_attn_splitk_noalloc(const pkv_bf16 *q, const pkv_bf16 
                        " (use pkv_decode_attn_splitk with a workspace, or fewer partitions)";
         return PKV_ERR_WORKSPACE;
     }
-    if (num_seqs == 0) return PKV_OK;
+    // the per-device address lookup comes first: a call with no sequences does it and nothing else
     void *scratch = nullptr;
     st = scratch_address(&scratch);
     if (st != PKV_OK) return st;
+    if (num_seqs == 0) return PKV_OK;
     // Nothing in the scratch has to start at zero: the partition step writes every partial
     // output and lse that the merge then reads, within this call.
     float *part_out = static_cast<float *>(scratch);
@@ -900,7 +822,9 @@ pkv::ColsParams cols_params_of(const AttnArgs &a, int tok_major)
     p.tok_major = tok_major;
     p.err_flag = a.err_flag;
     p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+#ifdef PKV_TEST_HOOKS
     p.withhold_tile = g_withhold_tile.load(std::memory_order_relaxed);
+#endif
     return p;
 }
 
@@ -957,21 +881,24 @@ PKV_EXPORT int pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "copy-blocks launch");
 }
 
-PKV_EXPORT int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
-                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
-                                     const int32_t *context_lens, int32_t num_seqs, int32_t num_new,
-                                     int32_t num_q_heads, float scale, pkv_bf16 *out, float *lse_out,
-                                     pkv_cache_desc cache, int32_t partition_blocks,
-                                     int32_t max_partitions, void *workspace, size_t workspace_bytes,
-                                     int32_t *err_flag, pkv_stream_t stream)
+namespace {
+
+// pkv_decode_attn_multi, and with k_new != nullptr the fused step pkv_decode_step_multi (the
+// producers write the new rows into the pools before loading their blocks).
+int multi_attention(const AttnArgs &a, int32_t num_new, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                    pkv_bf16 *k_cache_w, pkv_bf16 *v_cache_w, int64_t *slot_out, pkv_bf16 *out, float *lse_out,
+                    int32_t partition_blocks, int32_t max_partitions, void *workspace, size_t workspace_bytes,
+                    cudaStream_t stream)
 {
-    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-               num_q_heads, scale, cache, err_flag};
+    const pkv_cache_desc &cache = a.d;
+    const int32_t num_seqs = a.B, num_q_heads = a.N, max_blocks_per_seq = a.max_nb;
     int st = validate_attn(a);
     if (st != PKV_OK) return st;
     if (!out) return PKV_ERR_NULL;
     if (num_new <= 0 || num_new > 64) return PKV_ERR_SHAPE;
     if (!aligned(out, 4) || !aligned(lse_out, 4)) return PKV_ERR_ALIGN;
+    if (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_out, 8))) return PKV_ERR_ALIGN;
+    if ((int64_t)num_seqs * num_new > INT32_MAX) return PKV_ERR_SHAPE;
     const int32_t G = num_q_heads / cache.num_kv_heads;
     const int32_t chunks = (num_new * G + kColsPerCta - 1) / kColsPerCta;
     const bool split = partition_blocks > 0;
@@ -981,7 +908,6 @@ PKV_EXPORT int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache,
         if (max_partitions <= 0 || (int64_t)max_partitions * partition_blocks < max_blocks_per_seq)
             return PKV_ERR_SHAPE;
         const int64_t rows = (int64_t)num_seqs * num_new;
-        if (rows > INT32_MAX) return PKV_ERR_SHAPE;
         if (!workspace || workspace_bytes < pkv_splitk_workspace_bytes((int32_t)rows, num_q_heads,
                                                                        cache.head_dim, max_partitions))
             return PKV_ERR_WORKSPACE;
@@ -1000,7 +926,7 @@ PKV_EXPORT int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache,
     if (num_seqs == 0) return PKV_OK;
     CUtensorMap tk, tv;
     int tok_major = 0;
-    st = make_kv_maps(&tk, &tv, k_cache, v_cache, cache, &tok_major);
+    st = make_kv_maps(&tk, &tv, a.k_cache, a.v_cache, cache, &tok_major);
     if (st != PKV_OK) return st;
     pkv::ColsParams p = cols_params_of(a, tok_major);
     p.T = num_new;
@@ -1013,12 +939,17 @@ PKV_EXPORT int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache,
     p.lse_out = lse_out;
     p.part_out = part_out;
     p.part_lse = part_lse;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache_w = k_cache_w;
+    p.v_cache_w = v_cache_w;
+    p.slot_out = slot_out;
     // With more than 16 query rows per CTA the tensor-core (tcgen05) form of the column kernel does
     // the contraction.
     bool tc = std::min(num_new * G, kColsPerCta) >= kColsTcMinRows &&
               pkv::cols_tc_supported(cache.head_dim, tok_major);
     CUtensorMap tk_half;
-    if (tc) tc = encode_kv_map(&tk_half, k_cache, cache, 0, 1) == CUDA_SUCCESS;
+    if (tc) tc = encode_kv_map(&tk_half, a.k_cache, cache, 0, 1) == CUDA_SUCCESS;
     // The mma.sync kernel tapers its partitions as the one-token kernel does (partition_range) when
     // its grid runs in several waves and max_partitions has room: Llama-3-8B batch of 64, 4 new
     // tokens 222.5 -> 218.1 us, 2 new tokens 198.7 -> 196.8; the tcgen05 kernel gained nothing.
@@ -1040,8 +971,39 @@ PKV_EXPORT int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache,
     if (e != cudaSuccess) return cuda_fail(e, "multi-token attention launch");
     if (!split || p.counters) return PKV_OK;
     // rows of one sequence: its T tokens x N heads, all with the sequence's context length
-    return lse_merge_impl(part_out, part_lse, context_lens, num_seqs, num_new * num_q_heads,
+    return lse_merge_impl(part_out, part_lse, a.context_lens, num_seqs, num_new * num_q_heads,
                           cache.head_dim, max_partitions, partition_blocks, out, lse_out, p.taper != 0, stream);
+}
+
+}  // namespace
+
+PKV_EXPORT int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t *context_lens, int32_t num_seqs, int32_t num_new,
+                                     int32_t num_q_heads, float scale, pkv_bf16 *out, float *lse_out,
+                                     pkv_cache_desc cache, int32_t partition_blocks,
+                                     int32_t max_partitions, void *workspace, size_t workspace_bytes,
+                                     int32_t *err_flag, pkv_stream_t stream)
+{
+    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+               num_q_heads, scale, cache, err_flag};
+    return multi_attention(a, num_new, nullptr, nullptr, nullptr, nullptr, nullptr, out, lse_out, partition_blocks,
+                           max_partitions, workspace, workspace_bytes, stream);
+}
+
+PKV_EXPORT int pkv_decode_step_multi(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                                     pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *block_tables,
+                                     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                                     int32_t num_new, int32_t num_q_heads, float scale, pkv_bf16 *out,
+                                     float *lse_out, int64_t *slot_mapping_out, pkv_cache_desc cache,
+                                     int32_t partition_blocks, int32_t max_partitions, void *workspace,
+                                     size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream)
+{
+    if (!k_new || !v_new) return PKV_ERR_NULL;
+    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+               num_q_heads, scale, cache, err_flag};
+    return multi_attention(a, num_new, k_new, v_new, k_cache, v_cache, slot_mapping_out, out, lse_out,
+                           partition_blocks, max_partitions, workspace, workspace_bytes, stream);
 }
 
 PKV_EXPORT uint64_t pkv_set_wait_limit_ns(uint64_t limit_ns)
@@ -1049,10 +1011,14 @@ PKV_EXPORT uint64_t pkv_set_wait_limit_ns(uint64_t limit_ns)
     return g_wait_ns.exchange(limit_ns == 0 ? 1 : limit_ns);
 }
 
+#ifdef PKV_TEST_HOOKS
+// Test builds only (-DPKV_TEST_HOOKS; declared in tests/pkv_test_hooks.h): every CTA's producer in
+// the attention launches that follow skips its tile `tile`, so the consumers' bounded waits expire.
 PKV_EXPORT int64_t pkv_debug_withhold_tile(int64_t tile)
 {
     return g_withhold_tile.exchange(tile < 0 ? -1 : tile);
 }
+#endif
 
 PKV_EXPORT int pkv_check_wait_expiry(int32_t *err_flag, pkv_stream_t stream)
 {

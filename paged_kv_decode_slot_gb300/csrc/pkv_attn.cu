@@ -12,20 +12,13 @@
 //                                                          movmatrix; V^T via ldmatrix.trans)
 // When a unit (sequence, KV head) ends, the four warps' states are merged in shared memory.
 //
-// Three ways to cut the work:
+// Two ways to cut the work:
 //  * attn_kernel<H, false>: one CTA per (KV head, sequence), whole sequence (single pass).
 //  * attn_kernel<H, true>:  one CTA per (KV head, sequence, partition), partitions of a fixed
 //    number of blocks (FlashDecoding), highest partition first.  A sequence that fits in one
 //    partition is written out directly; the partial results of a longer one are merged by the
 //    last of its CTAs to finish (a per-unit counter that the merger resets), or -- when the caller
 //    asks for the partials themselves -- by lse_merge_kernel.
-//  * attn_balanced_kernel<H>: a persistent grid (about two CTAs per SM, a multiple of K) in which
-//    CTA c serves KV head c % K and takes the (c / K)-th equal share of that head's tiles in
-//    (sequence, block) order, keeping its TMA ring streaming across unit boundaries.  The K CTAs
-//    of one share read the same physical blocks at the same time (one per head), as the K CTAs of
-//    a sequence do in the single pass.  Units that lie inside one share are finished in place;
-//    units cut by a share boundary leave fp32 partials (at most two per CTA) for
-//    balanced_merge_kernel.
 //
 // This fuses the block-table gather with attention ("融合块读取和注意力的内核" and FlashDecoding
 // in CS336 Lecture 10's notes) and computes, for one query token, softmax(q K^T * scale) V with
@@ -34,8 +27,6 @@
 #include "pkv_attn_common.cuh"
 
 namespace pkv {
-
-int balanced_ctas_per_sm() { return PKV_BAL_CTAS_PER_SM; }
 
 // Fused decode step: the consumer warp that holds a sequence's last block writes the new token's
 // K and V (k_new/v_new row of this KV head) into that tile's row ctx-1 in shared memory -- so
@@ -163,17 +154,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     volatile int *slot_ok = reinterpret_cast<volatile int *>(base + L::kMiscOffset);
     volatile int *abort_flag = slot_ok + S;
     volatile int *issued_count = abort_flag + 1;  // [kProducers]
-    // e4m3 with per-(block, head) scales: the producers store each stage's (K, V) scales; the
-    // weights of a tile are taken relative to vref (the V scale of the CTA's first block), which
-    // multiplies the output at the end; with per-head scales vref is the head's V scale.
+    // e4m3 with per-(block, head) scales: the producers store each stage's (K, V) scales; each
+    // consumer warp takes its tiles' weights relative to the largest V scale it has seen so far
+    // (VScaleRef), which multiplies its state before the warps' states are merged.  With per-head
+    // scales the head's V scale multiplies the output at the end.
     volatile float2 *stage_sc = reinterpret_cast<volatile float2 *>(base + L::kScaleOffset);
     constexpr bool bscale = kFp8 && kBScale;
-    float vref = 1.f, inv_vref = 1.f;  // per-head scales: the head's V scale, read at the end
-    if constexpr (bscale) {
-        const int bid0 = __ldg(p.block_tables + (size_t)b * p.max_nb + blk_begin);
-        vref = bid0 >= 0 && bid0 < p.num_blocks ? __ldg(p.v_scale + (size_t)bid0 * p.scale_stride + kvh) : 1.f;
-        inv_vref = 1.f / vref;
-    }
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -183,6 +169,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     __syncthreads();
 
     WarpAcc<H> acc;
+    VScaleRef vr{0.f, 0.f};  // e4m3 with per-(block, head) scales only
 
     if (warp >= kConsumerWarps) {
         // ------------------------------ producer warps ------------------------------
@@ -195,7 +182,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
         const int64_t issued = run_producer<kProducers, bscale>(
             pw, lane, nblk, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, p.err_flag,
             [&](int64_t i, int bid, bool ok, float2 sc) {
-                if (i == p.withhold_tile) return true;  // test hook: never loaded, never signalled
+                if (PKV_TILE_WITHHELD(p, i)) return true;  // test builds: never loaded, never signalled
                 return produce_tile<H, S, kFp8>(i, kvh, bid, ok, base_u32, bar_full, bar_empty,
                                                 slot_ok, abort_flag, &tm_k, &tm_v, p.tok_major,
                                                 p.err_flag, p.wait_ns, bscale ? stage_sc : nullptr, sc);
@@ -240,7 +227,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
                 }
                 uint32_t kts[2], vts[2];
                 int valid[2];
-                float sl2s[2] = {sl2, sl2}, vsrs[2] = {1.f, 1.f}, ivss[2] = {1.f, 1.f};
+                float sl2s[2] = {sl2, sl2}, vss[2] = {0.f, 0.f};
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     const int it = t ? i2 : i, st = t ? s2 : s1;
@@ -249,10 +236,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
                     vts[t] = kts[t] + L::kTileBytes;
                     valid[t] = here && slot_ok[st] ? min(kBlockSize, ctx - (blk_begin + it) * kBlockSize) : 0;
                     if (bscale && valid[t] > 0) {
-                        const float ks_t = stage_sc[st].x, vs_t = stage_sc[st].y;
-                        sl2s[t] = p.scale_log2 * ks_t;
-                        vsrs[t] = vs_t * inv_vref;
-                        ivss[t] = __fdividef(vref, vs_t);
+                        sl2s[t] = p.scale_log2 * stage_sc[st].x;
+                        vss[t] = stage_sc[st].y;
                     }
                     // fused append: the tile of the sequence's last block holds the new token
                     const bool newest = here && p.k_new && blk_begin + it == nb - 1;
@@ -268,7 +253,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
                             p.slot_out[b] = slot_ok[st] ? (int64_t)last_bid * kBlockSize + (ctx - 1) % kBlockSize : -1;
                     }
                 }
-                if (valid[0] > 0 || valid[1] > 0) tile_update_fp8_n<H, 2, bscale>(acc, qf, kts, vts, valid, sl2s, vsrs, ivss, lane);
+                if (valid[0] > 0 || valid[1] > 0) tile_update_fp8_n<H, 2, bscale>(acc, qf, kts, vts, valid, sl2s, vss, vr, lane);
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(bar_empty + 8 * s1);
@@ -290,12 +275,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
             if (slot_ok[s]) {
                 const int valid = min(kBlockSize, ctx - (blk_begin + i) * kBlockSize);
                 const uint32_t kt = base_u32 + s * L::kStageBytes;
-                float sl2_t = sl2, vsr = 1.f, ivs = 1.f;  // this tile's logit multiplier, V-scale ratio
+                float sl2_t = sl2, vs_t = 0.f;  // this tile's logit multiplier and V scale
                 if constexpr (bscale) {
-                    const float ks_t = stage_sc[s].x, vs_t = stage_sc[s].y;
-                    sl2_t = p.scale_log2 * ks_t;
-                    vsr = vs_t * inv_vref;
-                    ivs = __fdividef(vref, vs_t);
+                    sl2_t = p.scale_log2 * stage_sc[s].x;
+                    vs_t = stage_sc[s].y;
                 }
                 if (newest) {
                     if constexpr (kFp8)
@@ -307,7 +290,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
                     __syncwarp();
                 }
                 if constexpr (kFp8)
-                    tile_update_fp8<H>(acc, qf, kt, kt + L::kTileBytes, valid, sl2_t, vsr, ivs, lane);
+                    tile_update_fp8<H, bscale>(acc, qf, kt, kt + L::kTileBytes, valid, sl2_t, vs_t, vr, lane);
                 else
                     tile_update<H>(acc, qf, kt, kt + L::kTileBytes, valid, sl2, p.tok_major, lane);
             }
@@ -334,10 +317,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     float *mm = mo + kConsumerWarps * 8 * H;                 // [W][8]
     float *ml = mm + kConsumerWarps * 8;                     // [W][8]
     if (!aborted) {
-        if (warp < kConsumerWarps) deposit<H, kFp8>(acc, mo, mm, ml, warp, lane);
+        if (warp < kConsumerWarps) {
+            if constexpr (bscale) acc_scale_o<H>(acc, vr.v);  // each warp's O in value units
+            deposit<H, kFp8>(acc, mo, mm, ml, warp, lane);
+        }
         __syncthreads();
     }
-    const float vscale = kFp8 ? (bscale ? vref : p.v_scale[kvh]) : 1.f;
+    const float vscale = kFp8 && !bscale ? p.v_scale[kvh] : 1.f;
     for (int idx = threadIdx.x; idx < G * H; idx += kAttnThreads) {
         const int g = idx / H, h = idx - g * H;
         float val = __int_as_float(0x7FC00000), lse = __int_as_float(0x7FC00000);  // NaN: void
@@ -383,280 +369,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CU
     merge_rows<H, 8>(wts, nparts, G, p.part_out + bn0 * p.max_parts * H, (size_t)p.max_parts * H, red, p.out + bn0 * H,
                      H, threadIdx.x, kAttnThreads);
     if (threadIdx.x == 0) *count = 0;  // ready for the next call
-}
-
-// ------------------------------ balanced (stream-K) split ---------------------------------
-// For each KV head the tiles are numbered in (sequence b, block j) order; sequence b owns
-// tiles [pre[b], pre[b+1]) with pre[b+1] - pre[b] = nb_b.  Of the grid's S = gridDim.x / K
-// shares per head, share s takes tiles [floor(T*s/S), floor(T*(s+1)/S)); CTA c = s*K + kvh.
-struct TileLoc {
-    int b, j, nb;
-    int64_t unit_start;  // first tile of sequence b
-};
-
-__device__ __forceinline__ TileLoc locate_tile(const int64_t *pre, int B, int64_t t)
-{
-    int lo = 0, hi = B - 1;  // largest b with pre[b] <= t (it has tiles since pre[b+1] > t)
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pre[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    TileLoc L;
-    L.b = lo;
-    L.nb = (int)(pre[lo + 1] - pre[lo]);
-    L.j = (int)(t - pre[lo]);
-    L.unit_start = pre[lo];
-    return L;
-}
-
-__device__ __forceinline__ int64_t share_start(int64_t T, int G, int c)
-{
-    return T * c / G;  // the host bounds T * grid below 2^62
-}
-
-template <int W>
-__device__ __forceinline__ void consumer_bar()
-{
-    asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
-}
-
-template <int H>
-__global__ void __launch_bounds__(kBalThreads, PKV_BAL_CTAS_PER_SM)
-attn_balanced_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     const AttnParams p)
-{
-    constexpr int S = kBalStages, W = kBalWarps, P = kBalProducers;
-    using L = AttnLayout<H, S, W, P>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_u32 = smem_u32(smem_raw);
-    const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
-    uint8_t *base = smem_raw + (base_u32 - raw_u32);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int B = p.B, K = p.K, G = p.G;
-    int64_t *pre = reinterpret_cast<int64_t *>(base + L::kBalSeqOffset);   // [B + 1]
-
-    // Per-sequence block counts and their prefix, by warp 0 (B <= 1024: 32 sequences a lane).
-    // An out-of-range context length counts as empty (and is flagged once).
-    auto blocks_of = [&](int s) {
-        const int c = p.context_lens[s];
-        return (c < 0 || c > p.max_nb * kBlockSize) ? 0 : (c + kBlockSize - 1) / kBlockSize;
-    };
-    if (warp == 0) {
-        const int per = (B + 31) / 32;
-        const int s0 = min(B, lane * per), s1 = min(B, s0 + per);
-        int64_t local = 0;
-        for (int s = s0; s < s1; ++s) {
-            const int c = p.context_lens[s];
-            if ((c < 0 || c > p.max_nb * kBlockSize) && blockIdx.x == 0)
-                set_flag(p.err_flag, PKV_FLAG_CTX_RANGE);
-            local += blocks_of(s);
-        }
-        int64_t incl = local;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-            if (lane >= off) incl += v;
-        }
-        int64_t run = incl - local;
-        for (int s = s0; s < s1; ++s) {
-            pre[s] = run;
-            run += blocks_of(s);
-        }
-        if (lane == 31) pre[B] = incl;
-    }
-    __syncthreads();
-    const int64_t T = pre[B];
-    const int c = blockIdx.x, kvh = c % K, shares = gridDim.x / K, sh = c / K;
-    if (c == 0 && p.prefix_out)
-        for (int s = threadIdx.x; s <= B; s += kBalThreads) p.prefix_out[s] = pre[s];
-    const int64_t t0 = share_start(T, shares, sh), t1 = share_start(T, shares, sh + 1);
-    if (t0 >= t1) return;
-    const int64_t n = t1 - t0;
-
-    const uint32_t bar_full = base_u32 + L::kBalBarOffset;
-    const uint32_t bar_empty = bar_full + 8 * S;
-    volatile int64_t *issued_count = reinterpret_cast<volatile int64_t *>(base + L::kBalMiscOffset);  // [P]
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + L::kBalMiscOffset + 8 * P);
-    volatile int *slot_ok = abort_flag + 2;
-    float *mo = reinterpret_cast<float *>(base + L::kBalMergeOffset);
-    float *mm = mo + W * 8 * H;
-    float *ml = mm + W * 8;
-
-    if (threadIdx.x == 0) {
-        *abort_flag = 0;
-        for (int q = 0; q < P; ++q) issued_count[q] = 0;
-        init_ring<S>(bar_full, bar_empty);
-    }
-    __syncthreads();
-
-    if (warp >= W) {
-        // ------------------------------ producer warps ------------------------------
-        const int pw = warp - W;
-        if (lane == 0 && pw == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-        }
-        auto lookup = [&](int64_t i) -> int {
-            const TileLoc tl = locate_tile(pre, B, t0 + i);
-            return __ldg(p.block_tables + (size_t)tl.b * p.max_nb + tl.j);
-        };
-        const int64_t issued = run_producer<P>(
-            pw, lane, n, lookup, p.num_blocks, p.err_flag, [&](int64_t i, int bid, bool ok, float2) {
-                return produce_tile<H, S>(i, kvh, bid, ok, base_u32, bar_full, bar_empty, slot_ok,
-                                          abort_flag, &tm_k, &tm_v, p.tok_major, p.err_flag, p.wait_ns);
-            });
-        if (lane == 0) issued_count[pw] = issued;
-    } else {
-        // ------------------------------ consumer warps ------------------------------
-        // Every consumer warp walks the same units in order and meets the others at two
-        // consumer-only barriers per unit (also after an expired wait, so nobody is stranded).
-        WarpAcc<H> acc;
-        uint32_t qf[H / 16][2];
-        bool aborted = false;
-        bool first_unit = true;
-        int64_t t = t0;
-        while (t < t1) {
-            const TileLoc u = locate_tile(pre, B, t);
-            const int64_t ue = min(t1, u.unit_start + u.nb);   // end of this unit's part here
-            const bool whole = u.unit_start >= t0 && u.unit_start + u.nb <= t1;
-            const int ctx = p.context_lens[u.b];
-            load_q_frags<H>(qf, p.q, p.N, u.b, kvh, G, lane);
-            acc_reset<H>(acc);
-            const int64_t ibeg = t - t0, iend = ue - t0;
-            int64_t i = ibeg + (int64_t)((warp - (int)(ibeg % W) + W) % W);
-            for (; i < iend && !aborted; i += W) {
-                const int s = (int)(i % S);
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(bar_full + 8 * s, (uint32_t)((i / S) & 1),
-                                                               abort_flag, p.wait_ns))) {
-                    if (!*abort_flag) set_flag(p.err_flag, PKV_FLAG_TIMEOUT);
-                    *abort_flag = 1;
-                    aborted = true;
-                    break;
-                }
-                if (slot_ok[s]) {
-                    const int j = u.j + (int)(i - ibeg);
-                    const int valid = min(kBlockSize, ctx - j * kBlockSize);
-                    const uint32_t kt = base_u32 + s * L::kStageBytes;
-                    tile_update<H>(acc, qf, kt, kt + L::kTileBytes, valid, p.scale_log2, p.tok_major, lane);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-            }
-            deposit<H>(acc, mo, mm, ml, warp, lane);
-            consumer_bar<W>();
-            if (!*abort_flag) {
-                const int slot = first_unit ? 0 : 1;
-                for (int idx = threadIdx.x; idx < G * H; idx += W * 32) {
-                    const int g = idx / H, h = idx - g * H;
-                    float val, lse;
-                    combine<H, W>(mo, mm, ml, g, h, val, lse);
-                    if (whole) {
-                        const size_t bn = (size_t)u.b * p.N + (size_t)kvh * G + g;
-                        p.out[bn * H + h] = __float2bfloat16_rn(val);
-                        if (h == 0 && p.lse_out) p.lse_out[bn] = lse;
-                    } else {
-                        const size_t cs = ((size_t)c * 2 + slot) * 8 + g;
-                        p.part_out[cs * H + h] = val;
-                        if (h == 0) p.part_lse[cs] = lse;
-                    }
-                }
-            }
-            consumer_bar<W>();
-            first_unit = false;
-            t = ue;
-        }
-    }
-
-    __syncthreads();
-    if (*abort_flag) {
-        if (warp >= W && lane == 0) drain_ring<S, P>(bar_full, warp - W, issued_count[warp - W]);
-        __syncthreads();
-    }
-}
-
-// Merge of the units the balanced kernel left split: one CTA per (KV head, sequence).  A unit
-// whose tiles all fell into one share is already final.  The pieces' lse are loaded in
-// parallel, their weights e^{lse_q - lse} computed once, then every (g, h) output element
-// sums its pieces.
-constexpr int kMergeThreads = 128;
-constexpr int kMaxPieces = 512;  // pieces of one unit held in shared memory per pass
-
-__global__ void __launch_bounds__(kMergeThreads)
-balanced_merge_kernel(const float *__restrict__ part_out, const float *__restrict__ part_lse,
-                      const int64_t *__restrict__ pre, int B, int N, int K, int H, int grid, int KG,
-                      __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out)
-{
-    __shared__ int piece_cs[kMaxPieces];        // (CTA, slot) index of each non-empty piece
-    __shared__ float wgt[kMaxPieces][8];        // lse of piece q, column g, then its weight
-    __shared__ float tot[8];
-    // Pieces come from CTA c = share * (K / KG) + kvh / KG, slot (first/last unit of its share),
-    // head kvh % KG of its group: entry ((c * 2 + slot) * KG + kvh % KG) * 8 + g.
-    const int kvh = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-    const int G = N / K, groups = K / KG, shares = grid / groups;
-    const int grp = kvh / KG, kh = kvh - grp * KG;
-    const int64_t T = pre[B];
-    const int nb = (int)(pre[b + 1] - pre[b]);
-    if (nb == 0) {  // empty sequence: no CTA touched it
-        for (int idx = tid; idx < G * H; idx += kMergeThreads) {
-            const int g = idx / H, h = idx - g * H;
-            const size_t bn = (size_t)b * N + (size_t)kvh * G + g;
-            out[bn * H + h] = __float2bfloat16_rn(0.f);
-            if (h == 0 && lse_out) lse_out[bn] = -INFINITY;
-        }
-        return;
-    }
-    const int64_t s = pre[b], e = s + nb;
-    auto share_of = [&](int64_t t) {
-        int c = (int)(t * shares / T);
-        while (c + 1 < shares && share_start(T, shares, c + 1) <= t) ++c;
-        while (c > 0 && share_start(T, shares, c) > t) --c;
-        return c;
-    };
-    const int q0 = share_of(s), q1 = share_of(e - 1);
-    if (q0 == q1) return;
-    const int slot0 = share_start(T, shares, q0) == s ? 0 : 1;
-    // Non-empty shares between q0 and q1 hold one piece each (shares with no tiles wrote nothing).
-    int np = 0;
-    if (tid == 0) {
-        for (int q = q0; q <= q1 && np < kMaxPieces; ++q)
-            if (share_start(T, shares, q) != share_start(T, shares, q + 1))
-                piece_cs[np++] = ((q * groups + grp) * 2 + (q == q0 ? slot0 : 0)) * KG + kh;
-        tot[0] = __int_as_float(np);
-    }
-    __syncthreads();
-    np = __float_as_int(tot[0]);
-    __syncthreads();
-    for (int idx = tid; idx < np * G; idx += kMergeThreads) {
-        const int q = idx / G, g = idx - q * G;
-        wgt[q][g] = part_lse[(size_t)piece_cs[q] * 8 + g];
-    }
-    __syncthreads();
-    if (tid < G) {
-        float M = -INFINITY;
-        for (int q = 0; q < np; ++q) M = fmaxf(M, wgt[q][tid]);
-        float total = -INFINITY;
-        if (M != -INFINITY) {
-            float sum = 0.f;
-            for (int q = 0; q < np; ++q) sum += expf(wgt[q][tid] - M);
-            total = M + logf(sum);
-            for (int q = 0; q < np; ++q) wgt[q][tid] = expf(wgt[q][tid] - total);
-        } else {
-            for (int q = 0; q < np; ++q) wgt[q][tid] = 0.f;
-        }
-        tot[tid] = total;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < G * H; idx += kMergeThreads) {
-        const int g = idx / H, h = idx - g * H;
-        float val = 0.f;
-#pragma unroll 4
-        for (int q = 0; q < np; ++q)
-            val += wgt[q][g] * part_out[((size_t)piece_cs[q] * 8 + g) * H + h];
-        const size_t bn = (size_t)b * N + (size_t)kvh * G + g;
-        out[bn * H + h] = __float2bfloat16_rn(val);
-        if (h == 0 && lse_out) lse_out[bn] = tot[g];
-    }
 }
 
 // ---------------------------------- LSE merge ----------------------------------------------
@@ -744,35 +456,6 @@ cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensor
                      : launch_attn_t<128, false, false>(tk, tv, p, grid, stream);
     return split ? launch_attn_t<64, true, false>(tk, tv, p, grid, stream)
                  : launch_attn_t<64, false, false>(tk, tv, p, grid, stream);
-}
-
-template <int H>
-static cudaError_t launch_balanced_t(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
-                                     int grid, cudaStream_t stream)
-{
-    using L = AttnLayout<H, kBalStages, kBalWarps, kBalProducers>;
-    const int smem = L::balanced_alloc(p.B);
-    static int cached[64] = {};
-    cudaError_t e = ensure_smem(attn_balanced_kernel<H>, L::balanced_alloc(kMaxBalancedSeqs), cached);
-    if (e != cudaSuccess) return e;
-    attn_balanced_kernel<H><<<grid, kBalThreads, smem, stream>>>(tk, tv, p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_attn_balanced(int H, const CUtensorMap &tk, const CUtensorMap &tv,
-                                 const AttnParams &p, int grid, cudaStream_t stream)
-{
-    return H == 128 ? launch_balanced_t<128>(tk, tv, p, grid, stream)
-                    : launch_balanced_t<64>(tk, tv, p, grid, stream);
-}
-
-cudaError_t launch_balanced_merge(const float *part_out, const float *part_lse, const int64_t *pre,
-                                  int B, int N, int K, int H, int grid, int KG, uint16_t *out,
-                                  float *lse_out, cudaStream_t stream)
-{
-    balanced_merge_kernel<<<dim3(K, B), kMergeThreads, 0, stream>>>(
-        part_out, part_lse, pre, B, N, K, H, grid, KG, reinterpret_cast<__nv_bfloat16 *>(out), lse_out);
-    return cudaGetLastError();
 }
 
 template <int H, int R>

@@ -136,6 +136,7 @@ attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const bool merge_multi = p.counters != nullptr && wk.mode == kModeMulti && wk.slot >= 0;
     const int nparts = merge_multi ? cols_nparts(p, wk) : 0;
     const bool direct = wk.slot < 0 || (merge_multi && nparts <= 1);
+    multi_slots_below_zero(p, wk);
     if (nblk <= 0) {
         // several new tokens, empty sequence (one pass, or partition 0 when merged here): 0, -inf
         if (wk.slot < 0 || (merge_multi && wk.slot == 0 && nparts == 0)) {
@@ -181,10 +182,11 @@ attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         const int64_t issued = run_producer<kProducers>(
             pw, lane, nblk, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, p.err_flag,
             [&](int64_t i, int bid, bool ok, float2) {
-                if (i == p.withhold_tile) return true;  // test hook: never loaded, never signalled
+                if (PKV_TILE_WITHHELD(p, i)) return true;  // test builds: never loaded, never signalled
                 return produce_tile<H, S>(i, wk.kvh, bid, ok, base_u32, bar_full, bar_empty, slot_ok,
                                           abort_flag, &tm_k, &tm_v, p.tok_major, p.err_flag, p.wait_ns);
-            });
+            },
+            NoAux(), false, 0, [&](int64_t i, int bid, bool ok) { append_multi_rows<H>(p, wk, i, bid, ok, lane); });
         if (lane == 0) issued_count[pw] = (int)issued;
     } else {
         const int cg = warp % ng, r = warp / ng;

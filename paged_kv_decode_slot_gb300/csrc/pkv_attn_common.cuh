@@ -19,21 +19,9 @@ namespace pkv {
 #ifndef PKV_CTAS_PER_SM
 #define PKV_CTAS_PER_SM 3
 #endif
-#ifndef PKV_BAL_STAGES
-#define PKV_BAL_STAGES 8
-#endif
-#ifndef PKV_BAL_WARPS
-#define PKV_BAL_WARPS 4
-#endif
-#ifndef PKV_BAL_CTAS_PER_SM
-#define PKV_BAL_CTAS_PER_SM 2
-#endif
 
 #ifndef PKV_PRODUCERS
 #define PKV_PRODUCERS 2
-#endif
-#ifndef PKV_BAL_PRODUCERS
-#define PKV_BAL_PRODUCERS 2
 #endif
 
 #ifndef PKV_FP8_STAGES
@@ -48,20 +36,14 @@ constexpr int kStages = PKV_STAGES;
 constexpr int kStagesFp8 = PKV_FP8_STAGES;  // e4m3 tiles are half the bytes: twice the depth
 constexpr int kProducers = PKV_PRODUCERS;
 constexpr int kAttnThreads = (kConsumerWarps + kProducers) * 32;
-constexpr int kBalStages = PKV_BAL_STAGES;
-constexpr int kBalWarps = PKV_BAL_WARPS;
-constexpr int kBalProducers = PKV_BAL_PRODUCERS;
-constexpr int kBalThreads = (kBalWarps + kBalProducers) * 32;
 // Stage s is reused by tiles s, s+S, s+2S, ... and tile i goes to consumer warp i % W.  With
 // S a multiple of W every use of a stage belongs to the same warp, so a warp only waits for a
 // stage's next phase after it consumed the previous one and mbarrier parities cannot alias.
 // The same holds for the producer warps (producer p issues tiles i = p mod P).
 static_assert(kStages % kConsumerWarps == 0, "pipeline depth must be a multiple of the consumer warps");
-static_assert(kBalStages % kBalWarps == 0, "pipeline depth must be a multiple of the consumer warps");
 static_assert(kStages % kProducers == 0, "pipeline depth must be a multiple of the producer warps");
 static_assert(kStagesFp8 % kConsumerWarps == 0 && kStagesFp8 % kProducers == 0,
               "pipeline depth must be a multiple of the consumer and producer warps");
-static_assert(kBalStages % kBalProducers == 0, "pipeline depth must be a multiple of the producer warps");
 
 // Lazy rescaling: keep the running maximum until a new logit exceeds it by this much
 // (log2 units), so exponentials stay <= 2^8 and the accumulator is rarely rescaled.
@@ -86,15 +68,7 @@ struct AttnLayout {
     static constexpr int kScaleOffset = (kMiscOffset + (S + 1 + P) * 4 + 7) / 8 * 8;
     static constexpr int kBytes = kScaleOffset + S * 8;
     static constexpr int kAlloc = kBytes + 1024;             // slack for 1024-byte alignment
-    // balanced kernel: pipeline, its own merge area, barriers, misc, then the block prefix
-    static constexpr int kBalMergeOffset = kPipeBytes;
-    static constexpr int kBalBarOffset = kBalMergeOffset + kMergeBytes;
-    static constexpr int kBalMiscOffset = kBalBarOffset + 2 * S * 8;
-    // misc: int64 issued[P], abort flag (padded to 8 bytes), slot_ok[S]
-    static constexpr int kBalSeqOffset = (kBalMiscOffset + 8 * P + 8 + S * 4 + 15) / 16 * 16;
-    static int balanced_alloc(int B) { return kBalSeqOffset + (B + 1) * 8 + 1024; }
-    static_assert(kBalMiscOffset % 8 == 0, "the balanced kernel's int64 counter needs 8-byte alignment");
-    static_assert(kBalSeqOffset % 16 == 0 && kPipeBytes % 1024 == 0, "shared-memory layout alignment");
+    static_assert(kPipeBytes % 1024 == 0, "shared-memory layout alignment");
     static_assert(kTileBytes % 1024 == 0, "TMA destinations with 128B swizzle need 1024-byte alignment");
 };
 
@@ -255,14 +229,25 @@ __device__ __forceinline__ void load_q_frags_fp8(uint32_t (&qf)[H / 16][2], cons
     }
 }
 
-// One 16-token e4m3 tile folded into a warp's state (the codes only: the tile's K scale is
-// folded into sl2; its weights enter P.V multiplied by vsr, the tile's V scale relative to the
-// one the caller multiplies the output by, and the running sum as the P.V weights times
-// ivs = 1 / vsr -- both 1 with one scale per head).
-template <int H>
+// Reference V scale of a warp's e4m3 tiles with one scale per (physical block, KV head).  The
+// warp's O holds sum_t w_t (vs_t / v) code_t, so its output is O * v / l.  v is the largest V scale
+// the warp has seen (0 before its first tile): when a tile's scale exceeds it, O is rescaled by
+// v / vs_t and v moves up, as the running maximum of the logits does.  Every tile's ratio vs_t / v
+// is then at most 1 and its f16 weights at most 2^8, whatever the spread of the caller's scales;
+// the running sum l takes the unscaled fp32 weights, so a tiny ratio (weights that round to f16
+// subnormals or zero) costs at most that tile's tiny V values, never the normaliser.
+struct VScaleRef {
+    float v;    // largest V scale seen so far (0: none yet)
+    float inv;  // 1 / v (0 before the first tile)
+};
+
+// One 16-token e4m3 tile folded into a warp's state (the codes only: the tile's K scale is folded
+// into sl2).  kBS: per-(block, head) scales -- the tile's V scale vs_t enters through vr (above);
+// otherwise the head's V scale multiplies the output at the end and vs_t / vr are unused.
+template <int H, bool kBS = false>
 __device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&qf)[H / 16][2],
-                                                uint32_t kt, uint32_t vt, int valid, float sl2, float vsr,
-                                                float ivs, int lane)
+                                                uint32_t kt, uint32_t vt, int valid, float sl2, float vs_t,
+                                                VScaleRef &vr, int lane)
 {
     constexpr int kKSteps = H / 16;
     const int mi = lane >> 3, ri = lane & 7;
@@ -299,13 +284,21 @@ __device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&
     }
     const bool needA = mA > a.m[0] + kRescaleThreshold;
     const bool needB = mB > a.m[1] + kRescaleThreshold;
-    if (__any_sync(0xFFFFFFFFu, needA || needB)) {
-        const float alphaA = needA ? exp2_sfu(a.m[0] - mA) : 1.f;
-        const float alphaB = needB ? exp2_sfu(a.m[1] - mB) : 1.f;
+    const bool needV = kBS && vs_t > vr.v;  // one value per tile: warp-uniform
+    if (__any_sync(0xFFFFFFFFu, needA || needB) || needV) {
+        float alphaA = needA ? exp2_sfu(a.m[0] - mA) : 1.f;
+        float alphaB = needB ? exp2_sfu(a.m[1] - mB) : 1.f;
         if (needA) a.m[0] = mA;
         if (needB) a.m[1] = mB;
         a.l[0] *= alphaA;
         a.l[1] *= alphaB;
+        if (needV) {  // O moves to the new reference scale; l counts unscaled weights
+            const float f = vr.v / vs_t;
+            alphaA *= f;
+            alphaB *= f;
+            vr.v = vs_t;
+            vr.inv = 1.f / vs_t;
+        }
 #pragma unroll
         for (int mt = 0; mt < kKSteps; ++mt) {
             a.o[mt][0] *= alphaA;
@@ -314,10 +307,18 @@ __device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&
             a.o[mt][3] *= alphaB;
         }
     }
-    const uint32_t p01 = pack_f16x2(exp2_sfu(x0 - a.m[0]) * vsr, exp2_sfu(x1 - a.m[1]) * vsr);
-    const uint32_t p23 = pack_f16x2(exp2_sfu(x2 - a.m[0]) * vsr, exp2_sfu(x3 - a.m[1]) * vsr);
-    a.l[0] += (f16x2_lo(p01) + f16x2_lo(p23)) * ivs;
-    a.l[1] += (f16x2_hi(p01) + f16x2_hi(p23)) * ivs;
+    const float w0 = exp2_sfu(x0 - a.m[0]), w1 = exp2_sfu(x1 - a.m[1]);
+    const float w2 = exp2_sfu(x2 - a.m[0]), w3 = exp2_sfu(x3 - a.m[1]);
+    const float vsr = kBS ? vs_t * vr.inv : 1.f;  // <= 1 (+ rounding)
+    const uint32_t p01 = pack_f16x2(w0 * vsr, w1 * vsr);
+    const uint32_t p23 = pack_f16x2(w2 * vsr, w3 * vsr);
+    if constexpr (kBS) {
+        a.l[0] += w0 + w2;
+        a.l[1] += w1 + w3;
+    } else {  // sums of the rounded weights: the weighted average is exactly normalised
+        a.l[0] += f16x2_lo(p01) + f16x2_lo(p23);
+        a.l[1] += f16x2_hi(p01) + f16x2_hi(p23);
+    }
     const uint32_t pb0 = movmatrix_trans(p01);
     const uint32_t pb1 = movmatrix_trans(p23);
 
@@ -359,13 +360,13 @@ __device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&
 // independent dependency chains in flight where one tile's chain would leave it waiting.  A
 // column that has seen no key keeps m = -inf and gets zero weights.  The caller skips a step in
 // which no tile has a valid token.
-// kBS: per-tile scales (sl2[t], vsr[t], ivs[t] as in tile_update_fp8); otherwise sl2[0] for every
-// tile and no V-scale ratios.
+// kBS: per-tile logit multipliers sl2[t] and V scales vs[t] (0 for a tile without valid tokens),
+// the V scales entering through vr as in tile_update_fp8; otherwise sl2[0] for every tile.
 template <int H, int NT, bool kBS = false>
 __device__ __forceinline__ void tile_update_fp8_n(WarpAcc<H> &a, const uint32_t (&qf)[H / 16][2],
                                                   const uint32_t (&kt)[NT], const uint32_t (&vt)[NT],
                                                   const int (&valid)[NT], const float (&sl2)[NT],
-                                                  const float (&vsr)[NT], const float (&ivs)[NT], int lane)
+                                                  const float (&vs)[NT], VScaleRef &vr, int lane)
 {
     constexpr int kKSteps = H / 16;
     const int mi = lane >> 3, ri = lane & 7;
@@ -410,15 +411,28 @@ __device__ __forceinline__ void tile_update_fp8_n(WarpAcc<H> &a, const uint32_t 
         mA = fmaxf(mA, __shfl_xor_sync(0xFFFFFFFFu, mA, off));
         mB = fmaxf(mB, __shfl_xor_sync(0xFFFFFFFFu, mB, off));
     }
+    float vmax = 0.f;
+    if constexpr (kBS) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) vmax = fmaxf(vmax, vs[t]);
+    }
     const bool needA = mA > a.m[0] + kRescaleThreshold;
     const bool needB = mB > a.m[1] + kRescaleThreshold;
-    if (__any_sync(0xFFFFFFFFu, needA || needB)) {
-        const float alphaA = needA ? exp2_sfu(a.m[0] - mA) : 1.f;
-        const float alphaB = needB ? exp2_sfu(a.m[1] - mB) : 1.f;
+    const bool needV = kBS && vmax > vr.v;  // warp-uniform
+    if (__any_sync(0xFFFFFFFFu, needA || needB) || needV) {
+        float alphaA = needA ? exp2_sfu(a.m[0] - mA) : 1.f;
+        float alphaB = needB ? exp2_sfu(a.m[1] - mB) : 1.f;
         if (needA) a.m[0] = mA;
         if (needB) a.m[1] = mB;
         a.l[0] *= alphaA;
         a.l[1] *= alphaB;
+        if (needV) {
+            const float f = vr.v / vmax;
+            alphaA *= f;
+            alphaB *= f;
+            vr.v = vmax;
+            vr.inv = 1.f / vmax;
+        }
 #pragma unroll
         for (int mt = 0; mt < kKSteps; ++mt) {
             a.o[mt][0] *= alphaA;
@@ -432,11 +446,18 @@ __device__ __forceinline__ void tile_update_fp8_n(WarpAcc<H> &a, const uint32_t 
     uint32_t pb[NT][2];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-        const float r_t = kBS ? vsr[t] : 1.f, ir_t = kBS ? ivs[t] : 1.f;
-        const uint32_t p01 = pack_f16x2(exp2_sfu(x[t][0] - baseA) * r_t, exp2_sfu(x[t][1] - baseB) * r_t);
-        const uint32_t p23 = pack_f16x2(exp2_sfu(x[t][2] - baseA) * r_t, exp2_sfu(x[t][3] - baseB) * r_t);
-        a.l[0] += (f16x2_lo(p01) + f16x2_lo(p23)) * ir_t;
-        a.l[1] += (f16x2_hi(p01) + f16x2_hi(p23)) * ir_t;
+        const float r_t = kBS ? vs[t] * vr.inv : 1.f;
+        const float w0 = exp2_sfu(x[t][0] - baseA), w1 = exp2_sfu(x[t][1] - baseB);
+        const float w2 = exp2_sfu(x[t][2] - baseA), w3 = exp2_sfu(x[t][3] - baseB);
+        const uint32_t p01 = pack_f16x2(w0 * r_t, w1 * r_t);
+        const uint32_t p23 = pack_f16x2(w2 * r_t, w3 * r_t);
+        if constexpr (kBS) {
+            a.l[0] += w0 + w2;
+            a.l[1] += w1 + w3;
+        } else {
+            a.l[0] += f16x2_lo(p01) + f16x2_lo(p23);
+            a.l[1] += f16x2_hi(p01) + f16x2_hi(p23);
+        }
         pb[t][0] = movmatrix_trans(p01);
         pb[t][1] = movmatrix_trans(p23);
     }
@@ -472,6 +493,20 @@ __device__ __forceinline__ void tile_update_fp8_n(WarpAcc<H> &a, const uint32_t 
                 mma_f16_16816(a.o[mt + hf], av, pb[t][0], pb[t][1]);
             }
         }
+    }
+}
+
+// O *= f (a warp's accumulator moved to other units, e.g. by its V-scale reference before the
+// warps' states are merged).
+template <int H>
+__device__ __forceinline__ void acc_scale_o(WarpAcc<H> &a, float f)
+{
+#pragma unroll
+    for (int mt = 0; mt < H / 16; ++mt) {
+        a.o[mt][0] *= f;
+        a.o[mt][1] *= f;
+        a.o[mt][2] *= f;
+        a.o[mt][3] *= f;
     }
 }
 
@@ -720,13 +755,19 @@ struct NoAux {
     __device__ __forceinline__ float2 operator()(int) const { return make_float2(0.f, 0.f); }
 };
 
+struct NoBefore {
+    __device__ __forceinline__ void operator()(int64_t, int, bool) const {}
+};
+
 // `first` (have_first): lookup(pw + P * lane) already loaded by the caller -- a caller that knows
 // its table row before its tile count issues these loads early, overlapping their round trip with
-// whatever the count waits for.
-template <int P, bool kAux = false, typename Lookup, typename Issue, typename Aux = NoAux>
+// whatever the count waits for.  `before(i, bid, ok)` runs on the whole warp right before lane 0
+// issues tile i (e.g. to write new rows into the block that tile i then loads).
+template <int P, bool kAux = false, typename Lookup, typename Issue, typename Aux = NoAux,
+          typename Before = NoBefore>
 __device__ __forceinline__ int64_t run_producer(int pw, int lane, int64_t n, Lookup lookup,
                                                 int num_blocks, int32_t *err_flag, Issue issue, Aux aux = Aux(),
-                                                bool have_first = false, int first = 0)
+                                                bool have_first = false, int first = 0, Before before = Before())
 {
     const int64_t mine = n > pw ? (n - pw + P - 1) / P : 0;
     auto fetch = [&](int bid) {
@@ -750,6 +791,7 @@ __device__ __forceinline__ int64_t run_producer(int pw, int lane, int64_t n, Loo
             float2 a = make_float2(0.f, 0.f);
             if constexpr (kAux) a = make_float2(__shfl_sync(0xFFFFFFFFu, cur_aux.x, k), __shfl_sync(0xFFFFFFFFu, cur_aux.y, k));
             int lane0_abort = 0;
+            before(pw + (int64_t)P * (k0 + k), bid, !((badmask >> k) & 1u));
             if (lane == 0) {
                 if (issue(pw + (int64_t)P * (k0 + k), bid, !((badmask >> k) & 1u), a))
                     ++issued;

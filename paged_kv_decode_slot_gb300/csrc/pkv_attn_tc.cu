@@ -123,6 +123,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     ColsWork wk;
     if (!cols_work(p, blockIdx.x, wk)) return;
     const int nblk = wk.blk_end - wk.blk_begin;
+    multi_slots_below_zero(p, wk);
     if (nblk <= 0) {
         // several new tokens, one pass, empty sequence: 0 and -inf
         if (wk.slot < 0) {
@@ -221,10 +222,11 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         const int64_t issued = run_producer<kTcProducers>(
             pw, lane, nblk, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, p.err_flag,
             [&](int64_t i, int bid, bool ok, float2) {
-                if (i == p.withhold_tile) return true;  // test hook: never loaded, never signalled
+                if (PKV_TILE_WITHHELD(p, i)) return true;  // test builds: never loaded, never signalled
                 return produce_tile_tc<H>(i, wk.kvh, bid, ok, kreg, vreg, bar_full, bar_free, slot_ok, abort_flag,
                                           &tm_k, &tm_v, p.err_flag, p.wait_ns);
-            });
+            },
+            NoAux(), false, 0, [&](int64_t i, int bid, bool ok) { append_multi_rows<H>(p, wk, i, bid, ok, lane); });
         if (lane == 0) issued_count[pw] = (int)issued;
     } else if (warp == 1) {
         // ----------------------- QK^T warp (lane 0 issues) -----------------------

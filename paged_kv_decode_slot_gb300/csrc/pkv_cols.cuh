@@ -154,6 +154,52 @@ __device__ __forceinline__ void col_of(const ColsParams &p, const ColsWork &w, i
     }
 }
 
+// Fused multi-token step: right before the producer warp loads tile i (logical block
+// blk_begin + i) of a multi-token unit, it writes the new tokens whose positions fall in that
+// block -- token t of the last T sits at position ctx - T + t -- from k_new / v_new into their
+// slots (this KV head's H elements of each row), fences those writes against the TMA load that
+// follows, and (KV head 0, first chunk) records their slots.  The CTAs of the unit's other chunks
+// write the same bytes.  A block id outside the pool (flagged by the producer) is not written and
+// its slots are -1.  The same rows land where pkv_slot_mapping_multi + pkv_append put them.
+template <int H>
+__device__ __forceinline__ void append_multi_rows(const ColsParams &p, const ColsWork &wk, int64_t i, int bid,
+                                                  bool ok, int lane)
+{
+    if (!p.k_new || wk.mode != kModeMulti) return;
+    const int j = wk.blk_begin + (int)i;
+    const int first = wk.ctx - p.T;
+    const int lo = max(max(first, 0), j * kBlockSize), hi = min(wk.ctx, (j + 1) * kBlockSize);
+    if (lo >= hi) return;  // the same on every lane
+    if (ok) {
+        constexpr int kVec = H / 8;  // 16-byte vectors per row
+        const int per = (hi - lo) * kVec;
+        for (int idx = lane; idx < 2 * per; idx += 32) {
+            const bool is_v = idx >= per;
+            const int r = is_v ? idx - per : idx;
+            const int pos = lo + r / kVec, c = r % kVec;
+            const size_t src = (((size_t)wk.b * p.T + (pos - first)) * p.K + wk.kvh) * H + 8 * c;
+            const size_t dst = (((size_t)bid * kBlockSize + pos % kBlockSize) * p.K + wk.kvh) * H + 8 * c;
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>((is_v ? p.v_new : p.k_new) + src));
+            *reinterpret_cast<uint4 *>((is_v ? p.v_cache_w : p.k_cache_w) + dst) = v;
+        }
+        fence_proxy_async_global();
+    }
+    if (p.slot_out && wk.kvh == 0 && wk.col_base == 0)
+        for (int pos = lo + lane; pos < hi; pos += 32)
+            p.slot_out[(int64_t)wk.b * p.T + (pos - first)] = ok ? (int64_t)bid * kBlockSize + pos % kBlockSize : -1;
+    __syncwarp();
+}
+
+// Fused multi-token step: slots of new tokens below position 0 (ctx < T) are -1, written by the
+// CTAs of the unit's first partition (KV head 0, first chunk), which exist whatever the length.
+__device__ __forceinline__ void multi_slots_below_zero(const ColsParams &p, const ColsWork &wk)
+{
+    if (!p.slot_out || !p.k_new || wk.mode != kModeMulti || wk.kvh != 0 || wk.col_base != 0 || wk.blk_begin != 0)
+        return;
+    for (int t = threadIdx.x; t < p.T && wk.ctx - p.T + t < 0; t += blockDim.x)
+        p.slot_out[(int64_t)wk.b * p.T + t] = -1;
+}
+
 // Partitions of a multi-token unit's sequence that hold blocks (the CTAs its merge waits for).
 __device__ __forceinline__ int cols_nparts(const ColsParams &p, const ColsWork &w)
 {

@@ -106,6 +106,13 @@ __device__ __forceinline__ void fence_proxy_async_shared()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy global writes before async-proxy accesses (TMA loads) that
+// follow it: a producer that writes rows into the pool fences, syncs its warp, then loads them.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2(const void *ptr)
 {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));

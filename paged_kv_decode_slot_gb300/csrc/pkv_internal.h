@@ -9,10 +9,6 @@
 
 namespace pkv {
 
-// The balanced kernel keeps per-sequence tile prefixes in shared memory: at most this many
-// sequences per call.
-constexpr int kMaxBalancedSeqs = 1024;
-
 // The log-sum-exp merge of a row's partitions (merge_rows): kMergeWarps warps split the
 // partitions; the last partition CTA of a split runs it inside the attention kernel when the
 // G * parts weights fit in kInKernelMergeWeights floats, otherwise lse_merge_kernel does.
@@ -20,6 +16,15 @@ constexpr int kMergeWarps = 6;
 // Default bound on the in-kernel waits; expiry sets PKV_FLAG_TIMEOUT and the kernel returns.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kInKernelMergeWeights = 8192;
+
+// Test builds (-DPKV_TEST_HOOKS) can make every CTA's producer skip one of its tiles -- no load,
+// no barrier arrival -- so that the consumers' bounded waits on it expire; product builds carry
+// neither the parameter nor the check.
+#ifdef PKV_TEST_HOOKS
+#define PKV_TILE_WITHHELD(p, i) ((i) == (p).withhold_tile)
+#else
+#define PKV_TILE_WITHHELD(p, i) false
+#endif
 
 struct AttnParams {
     const uint16_t *q;             // [B][N][H] bf16
@@ -37,8 +42,6 @@ struct AttnParams {
     float *lse_out;                // single pass: [B][N] (nullable)
     float *part_out;               // split-KV: [B][N][max_parts][H]
     float *part_lse;               // split-KV: [B][N][max_parts]
-                                   // balanced: part_out [grid][2][8][H], part_lse [grid][2][8]
-    int64_t *prefix_out;           // balanced: tile prefix per sequence [B + 1], for the merge
     // fused decode step (single pass / partitions): append the new token while attending
     const uint16_t *k_new;         // [B][K][H], nullable: no append
     const uint16_t *v_new;
@@ -52,7 +55,9 @@ struct AttnParams {
                                    // calls (nullptr: write every partial, merge separately)
     int32_t *err_flag;             // nullable
     uint64_t wait_ns;              // limit of every in-kernel wait (pkv_set_wait_limit_ns)
-    int64_t withhold_tile;         // test hook (pkv_debug_withhold_tile): -1, or a tile no CTA loads
+#ifdef PKV_TEST_HOOKS
+    int64_t withhold_tile;         // pkv_debug_withhold_tile: -1, or a tile no CTA loads
+#endif
 };
 
 // fp8: e4m3 pools (H = 128); pairs: e4m3 consumers take two tiles per step (for grids with
@@ -98,9 +103,18 @@ struct ColsParams {
     int32_t prefix_part_blocks;    // prefix mode: blocks per prefix-pass partition
     int32_t prefix_parts;          // prefix mode: partitions of the prefix pass (grid)
     int32_t prefix_ctas;           // prefix mode: CTAs of the prefix pass
+    // multi, fused step: the T new tokens' K/V rows [B][T][K][H] (nullable: no append) are written
+    // into their slots by the producer that loads their block, before it loads it
+    const uint16_t *k_new;
+    const uint16_t *v_new;
+    uint16_t *k_cache_w;           // the pools, written at the new tokens' slots
+    uint16_t *v_cache_w;
+    int64_t *slot_out;             // [B][T] slots of the new tokens (-1 below position 0), nullable
     int32_t *err_flag;
     uint64_t wait_ns;              // limit of every in-kernel wait (pkv_set_wait_limit_ns)
-    int64_t withhold_tile;         // test hook (pkv_debug_withhold_tile): -1, or a tile no CTA loads
+#ifdef PKV_TEST_HOOKS
+    int64_t withhold_tile;         // pkv_debug_withhold_tile: -1, or a tile no CTA loads
+#endif
 };
 
 cudaError_t launch_attn_cols(int H, const CUtensorMap &tk, const CUtensorMap &tv, const ColsParams &p,
@@ -129,18 +143,6 @@ cudaError_t launch_append_fp8(const uint16_t *k_new, const uint16_t *v_new, cons
                               uint8_t *k_cache,
                               uint8_t *v_cache, int num_blocks, int K, int H, int32_t *err_flag,
                               cudaStream_t stream);
-
-// CTAs per SM of the balanced kernel's persistent grid (a compile-time choice).
-int balanced_ctas_per_sm();
-
-cudaError_t launch_attn_balanced(int H, const CUtensorMap &tk, const CUtensorMap &tv,
-                                 const AttnParams &p, int grid, cudaStream_t stream);
-
-// Partials are indexed ((c * 2 + slot) * KG + head-in-group) * 8 + g; attn_balanced_kernel
-// writes them with KG = 1.
-cudaError_t launch_balanced_merge(const float *part_out, const float *part_lse, const int64_t *pre,
-                                  int B, int N, int K, int H, int grid, int KG, uint16_t *out,
-                                  float *lse_out, cudaStream_t stream);
 
 // taper: the partials come from partition_range's tapered layout (partition_count partitions).
 cudaError_t launch_lse_merge(const float *part_out, const float *part_lse,

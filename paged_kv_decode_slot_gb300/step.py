@@ -9,8 +9,7 @@ separate library calls instead:
 2. ``pkv_append``         -- its K/V written into that slot of the paged pools;
 3. attention, in the mode ``plan_attention`` picks:
    ``single``   -- ``pkv_decode_attn`` (one CTA per sequence and KV head, no workspace);
-   ``split``    -- ``pkv_decode_attn_splitk`` (fixed partitions of the block table, merge);
-   ``balanced`` -- ``pkv_decode_attn_balanced`` (persistent grid, equal tile shares, merge).
+   ``split``    -- ``pkv_decode_attn_splitk`` (fixed partitions of the block table, merge).
 """
 from __future__ import annotations
 
@@ -23,7 +22,7 @@ from . import binding as B
 
 @dataclass
 class AttentionPlan:
-    mode: str                      # "balanced" | "single" | "split"
+    mode: str                      # "single" | "split" (| "prefix": PrefixDecodeStep)
     partition_blocks: int = 0      # split only
     max_partitions: int = 1        # split only
 
@@ -36,8 +35,6 @@ class AttentionPlan:
             return f"shared-prefix pass + {self.partition_blocks}-block suffix partitions, merged"
         if self.mode == "split":
             return f"split-KV, {self.partition_blocks}-block partitions (max {self.max_partitions})"
-        if self.mode == "balanced":
-            return "balanced split-KV (persistent grid, equal tile shares)"
         return "single-pass"
 
 
@@ -100,15 +97,12 @@ def plan_attention(num_seqs: int, num_kv_heads: int, max_blocks_per_seq: int, nu
       * with fewer units than SMs, partitions sized so the grid holds about 512 partition CTAs
         when every sequence is as long as the table allows (at least 8 blocks each) are fastest:
         256 blocks for two sequences of 128K/32K tokens, 128 for 16 sequences of up to 7.4K.
-    The persistent balanced split is available with ``mode="balanced"``.
     With at least one unit per SM the grid runs in several waves; ``taper`` then leaves room for
     one more partition, so the split entry points taper (partition 0, launched last, covers half a
     partition and the final wave is short: bf16 180.2 -> 178.1 us, e4m3 118.8 -> 114.7 on the
     batch of 64).  The tcgen05 column kernel of several new tokens does not taper
     (``taper=False``); the mma.sync one does.
     """
-    if mode == "balanced":
-        return AttentionPlan("balanced")
     if mode == "single":
         return AttentionPlan("single", max_blocks_per_seq, 1)
     units = num_seqs * num_kv_heads
@@ -154,14 +148,10 @@ class DecodeStep:
         self.lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev)
         self.err_flag = err_flag
         # fused: one pkv_decode_step call (single pass or fixed partitions) does it all
-        self.fused = fused and plan.mode != "balanced"
+        self.fused = fused
         self.workspace = None
         if plan.mode == "split":
             nbytes = B.pkv_splitk_workspace_bytes(nseq, q.shape[1], q.shape[2], plan.max_partitions)
-            self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
-        elif plan.mode == "balanced":
-            with torch.cuda.device(dev):
-                nbytes = B.pkv_balanced_workspace_bytes(nseq, k_cache.shape[2], q.shape[2])
             self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def slot_and_append(self, stream=None) -> None:
@@ -176,10 +166,6 @@ class DecodeStep:
                                              self.context_lens, self.scale, self.out,
                                              self.plan.partition_blocks, self.plan.max_partitions,
                                              self.workspace, self.lse, self.err_flag, stream))
-        elif self.plan.mode == "balanced":
-            B.check(B.pkv_decode_attn_balanced(self.q, self.k_cache, self.v_cache, self.block_tables,
-                                               self.context_lens, self.scale, self.out, self.workspace,
-                                               self.lse, self.err_flag, stream))
         else:
             B.check(B.pkv_decode_attn(self.q, self.k_cache, self.v_cache, self.block_tables,
                                       self.context_lens, self.scale, self.out, self.lse,
@@ -202,7 +188,7 @@ class DecodeStep:
         if self.plan.mode == "split":
             attn = B.split_attention_launches(self.q.shape[1], self.k_cache.shape[2], self.plan.max_partitions)
         else:
-            attn = 2 if self.plan.mode == "balanced" else 1
+            attn = 1
         return attn if self.fused else 2 + attn
 
     def input_names(self):
@@ -216,7 +202,7 @@ class DecodeStep:
 class DecodeStepFp8:
     """A decode step over e4m3 pools with per-KV-head scales [K] or per-(physical block, KV head)
     scales [num_blocks, K]: one ``pkv_decode_step_fp8`` call (single pass or fixed partitions, as
-    ``plan_attention`` picks; never the balanced path)."""
+    ``plan_attention`` picks)."""
 
     def __init__(self, q, k_new, v_new, k_cache8, v_cache8, k_scale, v_scale, block_tables,
                  context_lens, scale, plan: AttentionPlan | None = None, err_flag=None):
@@ -227,7 +213,7 @@ class DecodeStepFp8:
         self.scale = float(scale)
         dev = k_cache8.device  # the pools' GPU (q and the other inputs may be pinned host memory)
         nseq = q.shape[0]
-        if plan is None or plan.mode == "balanced":
+        if plan is None:
             sms = torch.cuda.get_device_properties(dev).multi_processor_count
             plan = plan_attention(nseq, k_cache8.shape[2], block_tables.shape[1], sms)
         self.plan = plan
@@ -263,19 +249,22 @@ class DecodeStepFp8:
 
 
 class MultiTokenStep:
-    """Verification of T new tokens per sequence (speculative decoding): the slots of the last T
-    positions (``pkv_slot_mapping_multi``), the append of the B*T new K/V rows (``pkv_append``),
-    then ``pkv_decode_attn_multi`` -- one pass when the (sequence, KV head, 32-row chunk) units
-    cover the SMs, else fixed partitions sized like ``plan_attention``'s and a log-sum-exp merge
-    (in the same launch for the mma.sync column kernel, a second one after the tcgen05 kernel).
-    The workspace is zeroed once here; each call leaves its merge counters at zero.
+    """Verification of T new tokens per sequence (speculative decoding).  By default one
+    ``pkv_decode_step_multi`` call does the whole step: the kernel writes the B*T new K/V rows into
+    their slots as it loads their blocks and records the slots.  ``fused=False`` issues the separate
+    calls: the slots of the last T positions (``pkv_slot_mapping_multi``), the append
+    (``pkv_append``), then ``pkv_decode_attn_multi``.  Attention runs one pass when the (sequence,
+    KV head, 32-row chunk) units cover the SMs, else fixed partitions sized like
+    ``plan_attention``'s and a log-sum-exp merge (in the same launch for the mma.sync column
+    kernel, a second one after the tcgen05 kernel).  The workspace is zeroed once here; each call
+    leaves its merge counters at zero.
 
     q [B, T, N, H] bf16; k_new/v_new [B, T, K, H]; pools, tables and lengths as ``DecodeStep``
     (context_lens counts the T new tokens).
     """
 
     def __init__(self, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
-                 partition_blocks: int | None = None, err_flag=None):
+                 partition_blocks: int | None = None, err_flag=None, fused: bool = True):
         self.q, self.k_new, self.v_new = q, k_new, v_new
         self.k_cache, self.v_cache = k_cache, v_cache
         self.block_tables, self.context_lens = block_tables, context_lens
@@ -292,7 +281,7 @@ class MultiTokenStep:
         tc = bool(B.pkv_multi_uses_tcgen05(T, N, K, H))
         self.plan = plan_attention(nseq * chunks, K, block_tables.shape[1], sms,
                                    partition_blocks=partition_blocks, taper=not tc)
-        self.fused = False
+        self.fused = fused
         self.slot_mapping = torch.empty(nseq, T, dtype=torch.int64, device=dev)
         self.out = torch.empty(tuple(q.shape), dtype=q.dtype, device=dev)
         self.lse = torch.empty(nseq, T, N, dtype=torch.float32, device=dev)
@@ -320,15 +309,25 @@ class MultiTokenStep:
                                         self.err_flag, stream))
 
     def run(self, stream=None) -> None:
+        if self.fused:
+            split = self.plan.mode == "split"
+            B.check(B.pkv_decode_step_multi(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
+                                            self.block_tables, self.context_lens, self.scale, self.out,
+                                            self.lse, self.slot_mapping,
+                                            self.plan.partition_blocks if split else 0,
+                                            self.plan.max_partitions if split else 0, self.workspace,
+                                            self.err_flag, stream))
+            return
         self.slot_and_append(stream)
         self.attention(stream)
 
     def launches_per_step(self) -> int:
-        if self.plan.mode != "split":
-            return 3
-        _, T, N, H = self.q.shape
-        tc = bool(B.pkv_multi_uses_tcgen05(T, N, self.k_cache.shape[2], H))
-        return 2 + B.multi_attention_launches(self.plan.max_partitions, tc)
+        attn = 1
+        if self.plan.mode == "split":
+            _, T, N, H = self.q.shape
+            tc = bool(B.pkv_multi_uses_tcgen05(T, N, self.k_cache.shape[2], H))
+            attn = B.multi_attention_launches(self.plan.max_partitions, tc)
+        return attn if self.fused else 2 + attn
 
     def input_names(self):
         return ("q", "k_new", "v_new", "block_tables", "context_lens")

@@ -152,7 +152,6 @@ def test_attention_plan():
     assert p.mode == "split" and p.partition_blocks == 128 and p.max_partitions == 4
     p = plan_attention(1, 40, 64, 152)                                  # at least 8 blocks
     assert p.mode == "split" and p.partition_blocks == 8
-    assert plan_attention(64, 8, 512, 152, mode="balanced").mode == "balanced"
     p = plan_attention(64, 8, 512, 152, partition_blocks=64)            # several waves: tapered
     assert p.mode == "split" and p.max_partitions == 9
     p = plan_attention(16, 8, 512, 152, partition_blocks=64)            # one wave: uniform
@@ -184,20 +183,6 @@ def test_tapered_partition_count():
     assert pkv.tapered_partitions_for(5, 1) == 5   # no taper below two blocks a partition
 
 
-def test_balanced_host_validation(lib):
-    cdll, _ = lib
-    f = cdll.pkv_decode_attn_balanced
-    f.argtypes = [P, P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, P, P,
-                  Desc, P, ctypes.c_size_t, P, P]
-    args = lambda B=4, ws=FAKE, q=FAKE: (q, FAKE, FAKE, FAKE, 4, FAKE, B, 8, 0.125, FAKE, None,
-                                         Desc(64, 16, 2, 64), ws, 1 << 20, None, None)
-    assert f(*args(q=None)) == -1
-    assert f(*args(B=1025)) == -3                                     # beyond the shared-memory prefix
-    assert f(*args(ws=None)) == -7
-    assert f(*args(ws=FAKE + 64)) == -6
-    assert f(*args(B=0)) == 0
-
-
 def test_decode_step_host_validation(lib):
     cdll, _ = lib
     f = cdll.pkv_decode_step
@@ -227,3 +212,43 @@ def test_multi_kernel_choice():
     assert not B.pkv_multi_uses_tcgen05(8, 32, 8, 64)     # H = 64
     assert not B.pkv_multi_uses_tcgen05(1, 64, 8, 128)    # one token, G = 8: 8 rows
     assert not B.pkv_multi_uses_tcgen05(0, 32, 8, 128)
+
+
+def test_noalloc_refuses_before_any_cuda_call(lib):
+    """Every refusal of the no-alloc entry point comes from host validation, before the scratch
+    lookup or a launch (this machine has no GPU, so any CUDA call would fail instead)."""
+    cdll, _ = lib
+    f = cdll.pkv_decode_attn_splitk_noalloc
+    f.argtypes = [P, P, P, P, ctypes.c_int32, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, P, P,
+                  Desc, ctypes.c_int32, ctypes.c_int32, P, P]
+    cdll.pkv_last_error.restype = ctypes.c_char_p
+
+    def call(B=1, N=1, max_nb=1, pb=1, parts=4, desc=(64, 16, 1, 64)):
+        return f(FAKE, FAKE, FAKE, FAKE, max_nb, FAKE, B, N, 0.125, FAKE, None, Desc(*desc), pb, parts,
+                 None, None)
+    assert call(parts=13000) == -3                 # more partitions than the separate merge takes
+    assert call(max_nb=8, pb=1, parts=4) == -2     # the partitions do not cover the table
+    assert call(B=8, N=32, parts=1024, desc=(64, 16, 8, 128)) == -7   # partials beyond the scratch
+    assert b"static scratch" in cdll.pkv_last_error()
+    assert call(pb=0) == -2
+
+
+def test_product_library_has_no_test_hook(lib):
+    cdll, _ = lib
+    assert not hasattr(cdll, "pkv_debug_withhold_tile")
+
+
+def test_test_build_exports_the_hook(tmp_path):
+    """The -DPKV_TEST_HOOKS variant (used by the GPU failure tests) exports the tile-withholding
+    hook declared in tests/pkv_test_hooks.h, and nothing else beyond the product's exports."""
+    from paged_kv_decode_slot_gb300.build import build_library
+    path = build_library(out=str(tmp_path / "libpagedkv_test_hooks.so"), defines=("PKV_TEST_HOOKS",),
+                         build_dir=str(tmp_path / "obj"))
+    hooks = ctypes.CDLL(path)
+    hooks.pkv_debug_withhold_tile.argtypes = [ctypes.c_int64]
+    hooks.pkv_debug_withhold_tile.restype = ctypes.c_int64
+    assert hooks.pkv_debug_withhold_tile(3) == -1 and hooks.pkv_debug_withhold_tile(-1) == 3
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True)
+    if out.returncode == 0:
+        exported = set(re.findall(r"\s[TW]\s+(pkv_\w+)$", out.stdout, flags=re.M))
+        assert exported == set(declared_functions()) | {"pkv_debug_withhold_tile"}

@@ -72,3 +72,21 @@ def test_single_process_keeps_its_own_timings():
     import bench
     assert bench.max_over_ranks([3.5, 1.25]) == [3.5, 1.25]
     assert bench.whole_job_gbs(1, 2_000_000_000, 1000.0) == pytest.approx(2.0)
+
+
+def test_both_arms_describe_the_same_config(monkeypatch, capsys):
+    """The reference arm prints the config dict the GPU arm builds from the same arguments
+    (config_dict(workload, args)): the workload and the timing protocol, nothing arm-specific."""
+    sys.path.insert(0, ROOT)
+    import json
+
+    import bench
+    from paged_kv_decode_slot_gb300 import inputs as gen
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    bench.run_reference(bench.parse_args(["--impl", "reference", "--config", "tiny", "--steps", "1",
+                                          "--warmup", "3"]))
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    ours = bench.config_dict(gen.make_config("tiny"), bench.parse_args(["--config", "tiny"]))
+    assert line["config"] == ours

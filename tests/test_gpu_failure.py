@@ -12,17 +12,34 @@ holds (tensor memory included) and returns, and the unit's result is void.
     count toward the merge, return).  Only PKV_FLAG_TIMEOUT may be flagged, and it must be.
     The same step then runs again with the defaults and must match the oracle: the context
     works, the fused append lands, and the split workspace's merge counters are back at zero.
+    The hook exists only in a test build of the library (-DPKV_TEST_HOOKS, built here next to
+    the product library); each of these cases runs in a child process that loads that build
+    through PKV_LIBRARY, so the product library the other tests load carries no hook.
 """
 from __future__ import annotations
+
+import os
+import subprocess
+import sys
 
 import numpy as np
 import pytest
 import torch
 
-from devutil import assert_close, bf16_dev, i32_dev, out_f64, upload
-from paged_kv_decode_slot_gb300 import inputs as gen
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+for _p in (ROOT, HERE):
+    if _p not in sys.path:
+        sys.path.insert(0, _p)
+
+from devutil import assert_close, bf16_dev, i32_dev, out_f64, upload  # noqa: E402
+from paged_kv_decode_slot_gb300 import inputs as gen  # noqa: E402
 
 pytestmark = pytest.mark.gpu
+
+HOOKS_DIR = os.path.join(ROOT, "_build", "test_hooks")
+HOOKS_LIB = os.path.join(HOOKS_DIR, "libpagedkv_test_hooks.so")
+KINDS = ["single", "split", "split_fp8", "multi_tc", "multi_mma", "prefix"]
 
 
 @pytest.fixture(scope="module")
@@ -66,10 +83,28 @@ def _flags_with_withheld_tile(pkv, run):
     return flag
 
 
-@pytest.mark.parametrize("kind", ["single", "split", "split_fp8", "multi_tc", "multi_mma", "prefix"])
-def test_kernels_survive_expired_waits_and_recover(pkv, oracle, kind):
+@pytest.fixture(scope="module")
+def hooks_lib():
+    from paged_kv_decode_slot_gb300.build import build_library
+    return build_library(out=HOOKS_LIB, defines=("PKV_TEST_HOOKS",), build_dir=HOOKS_DIR)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_kernels_survive_expired_waits_and_recover(hooks_lib, kind):
+    env = dict(os.environ, PKV_LIBRARY=hooks_lib)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), kind], env=env, cwd=ROOT,
+                       capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0 and "RECOVERED" in r.stdout, (r.stdout[-4000:], r.stderr[-4000:])
+
+
+def expired_waits_case(kind: str) -> None:
+    """One case, in a process whose library is the test build (PKV_LIBRARY)."""
+    import oracle as oracle_mod
+    import paged_kv_decode_slot_gb300 as pkv
     from paged_kv_decode_slot_gb300.step import (AttentionPlan, DecodeStep, DecodeStepFp8, MultiTokenStep,
                                                  PrefixDecodeStep, plan_attention)
+    assert pkv.binding.HAS_TEST_HOOKS, "the child must load the -DPKV_TEST_HOOKS build"
+    oracle = oracle_mod.default()
     w = gen.make_config("l3_8b_b16")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     if kind in ("single", "split"):
@@ -81,8 +116,7 @@ def test_kernels_survive_expired_waits_and_recover(pkv, oracle, kind):
                               d["context_lens"], w.scale, plan=plan, err_flag=err)
         kc, vc = w.k_cache.copy(), w.v_cache.copy()
         oracle.append(w.k_new, w.v_new, oracle.slot_mapping(w.block_tables, w.context_lens), kc, vc)
-        rows = [0, 5, 15]
-        ref, _ = oracle.decode(w.q[rows], kc, vc, w.block_tables[rows], w.context_lens[rows], w.scale)
+        ref, _ = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
     elif kind == "split_fp8":
         ks = np.full(w.K, 0.02, dtype=np.float32)
         vs = np.full(w.K, 0.02, dtype=np.float32)
@@ -95,9 +129,7 @@ def test_kernels_survive_expired_waits_and_recover(pkv, oracle, kind):
                                  i32_dev(w.block_tables), i32_dev(w.context_lens), w.scale, err_flag=err)
         kc8a, vc8a = kc8.copy(), vc8.copy()
         oracle.append_fp8(w.k_new, w.v_new, ks, vs, oracle.slot_mapping(w.block_tables, w.context_lens), kc8a, vc8a)
-        rows = [0, 5, 15]
-        ref, _ = oracle.decode_fp8(w.q[rows], kc8a, vc8a, ks, vs, w.block_tables[rows], w.context_lens[rows],
-                                   w.scale)
+        ref, _ = oracle.decode_fp8(w.q, kc8a, vc8a, ks, vs, w.block_tables, w.context_lens, w.scale)
     elif kind in ("multi_tc", "multi_mma"):
         T = 8 if kind == "multi_tc" else 2
         qm = gen.normal_bf16(7, 1, (w.B, T, w.N, w.H))
@@ -111,8 +143,7 @@ def test_kernels_survive_expired_waits_and_recover(pkv, oracle, kind):
         kc, vc = w.k_cache.copy(), w.v_cache.copy()
         slots = oracle.slot_mapping_multi(w.block_tables, w.context_lens, T)
         oracle.append(knm.reshape(-1, w.K, w.H), vnm.reshape(-1, w.K, w.H), slots.reshape(-1), kc, vc)
-        rows = [0, 5, 15]
-        ref, _ = oracle.decode_multi(qm[rows], kc, vc, w.block_tables[rows], w.context_lens[rows], w.scale)
+        ref, _ = oracle.decode_multi(qm, kc, vc, w.block_tables, w.context_lens, w.scale)
     else:
         w = gen.make_config("prefix_l3_70b")
         gs, pb = w.prefix_groups()
@@ -124,8 +155,7 @@ def test_kernels_survive_expired_waits_and_recover(pkv, oracle, kind):
                                     int(pb.max()), partition_blocks=16, err_flag=err)
         kc, vc = w.k_cache.copy(), w.v_cache.copy()
         oracle.append(w.k_new, w.v_new, oracle.slot_mapping(w.block_tables, w.context_lens), kc, vc)
-        rows = [0, 7, 19]
-        ref, _ = oracle.decode(w.q[rows], kc, vc, w.block_tables[rows], w.context_lens[rows], w.scale)
+        ref, _ = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
 
     err0 = torch.zeros(1, dtype=torch.int32, device="cuda")
     step = make(err0)
@@ -136,4 +166,9 @@ def test_kernels_survive_expired_waits_and_recover(pkv, oracle, kind):
     step.run()
     torch.cuda.synchronize()
     assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
-    assert_close(out_f64(step.out[rows]), ref, f"{kind} after expired waits")
+    assert_close(out_f64(step.out), ref, f"{kind} after expired waits")
+
+
+if __name__ == "__main__":
+    expired_waits_case(sys.argv[1])
+    print("RECOVERED", flush=True)

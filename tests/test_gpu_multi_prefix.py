@@ -201,7 +201,7 @@ def test_multi_with_one_token_is_the_decode_kernel(pkv, oracle, part_blocks):
     assert torch.equal(lse1, lse2.view(w.B, w.N))
 
 
-def test_multi_full_size_sampled(pkv, oracle):
+def test_multi_full_size_every_row(pkv, oracle):
     """Llama-3-8B-shaped batch of 64 verifying 4 tokens each (gamma = 3), one pass and partitions."""
     w = gen.make_config("l3_8b_b64")
     T = 4
@@ -216,13 +216,10 @@ def test_multi_full_size_sampled(pkv, oracle):
     assert step.plan.mode == "split"
     assert step.plan.max_partitions == pkv.tapered_partitions_for(w.max_blocks, step.plan.partition_blocks)
     step.attention()
-    sample = [0, 5, 31, 62]
-    bt = np.ascontiguousarray(w.block_tables[sample])
-    cl = np.ascontiguousarray(w.context_lens[sample])
-    ref, _ = oracle.decode_multi(c.q[sample], c.kc, c.vc, bt, cl, w.scale)
-    assert_close(out_f64(out[sample]), ref, "multi l3_8b_b64 one pass")
-    assert_close(out_f64(out_s[sample]), ref, "multi l3_8b_b64 partitions")
-    assert_close(out_f64(step.out[sample]), ref, "multi l3_8b_b64 step plan (tapered)")
+    ref, _ = c.reference(oracle)
+    assert_close(out_f64(out), ref, "multi l3_8b_b64 one pass")
+    assert_close(out_f64(out_s), ref, "multi l3_8b_b64 partitions")
+    assert_close(out_f64(step.out), ref, "multi l3_8b_b64 step plan (tapered)")
 
 
 # ------------------------------------ copy-on-write ----------------------------------------
@@ -383,7 +380,7 @@ def test_prefix_bounds_are_flagged(pkv, oracle):
 def test_multi_step_full_size_in_bench_plan(pkv, oracle, T):
     """The multi-token step as the benchmark times it (MultiTokenStep with its default plan) on the
     Llama-3-8B-shaped batch of 64: T = 8 and T = 4 new tokens (32 query rows per CTA: the tcgen05
-    column kernel; 16: the mma.sync one), sampled sequences against the oracle."""
+    column kernel; 16: the mma.sync one), every sequence against the oracle."""
     from paged_kv_decode_slot_gb300.step import MultiTokenStep
     w = gen.make_config("l3_8b_b64")
     c = MultiCase(oracle, w, T, 200 + T)
@@ -393,13 +390,9 @@ def test_multi_step_full_size_in_bench_plan(pkv, oracle, T):
                           i32_dev(w.context_lens), w.scale, err_flag=err)
     step.run()
     assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
-    rng = np.random.default_rng(T)
-    sample = sorted({0, w.B - 1, int(np.argmax(w.context_lens))} | set(rng.integers(0, w.B, size=3).tolist()))
-    bt = np.ascontiguousarray(w.block_tables[sample])
-    cl = np.ascontiguousarray(w.context_lens[sample])
-    ref, ref_lse = oracle.decode_multi(c.q[sample], c.kc, c.vc, bt, cl, w.scale)
-    assert_close(out_f64(step.out[sample]), ref, f"multi step T={T} ({step.plan.describe()})")
-    assert_lse_close(step.lse[sample].cpu().numpy().astype(np.float64), ref_lse, f"multi step T={T}")
+    ref, ref_lse = c.reference(oracle)
+    assert_close(out_f64(step.out), ref, f"multi step T={T} ({step.plan.describe()})")
+    assert_lse_close(step.lse.cpu().numpy().astype(np.float64), ref_lse, f"multi step T={T}")
 
 
 def test_multi_skipped_block_is_flagged_and_masked(pkv, oracle):
@@ -422,3 +415,100 @@ def test_multi_skipped_block_is_flagged_and_masked(pkv, oracle):
     ref, _ = c.reference(oracle)
     keep = [0, 1, 3]
     assert_close(out_f64(out)[keep], ref[keep], "multi with a skipped block, other sequences")
+
+
+# ------------------------------- fused multi-token step -------------------------------------
+FUSED_CASES = [
+    # (T, N, K, H, plan): plan "one_pass", "split" (uniform partitions) or "tapered"
+    (2, 16, 4, 128, "one_pass"), (4, 16, 4, 128, "split"), (4, 16, 4, 128, "tapered"),
+    (8, 16, 4, 128, "one_pass"), (8, 16, 4, 128, "split"), (9, 16, 4, 128, "split"),
+    (3, 8, 4, 64, "split"), (20, 4, 4, 64, "one_pass"),
+]
+
+
+@pytest.mark.parametrize("T,N,K,H,plan", FUSED_CASES,
+                         ids=[f"T{c[0]}_G{c[1] // c[2]}_H{c[3]}_{c[4]}" for c in FUSED_CASES])
+def test_fused_multi_step_equals_separate_calls(pkv, oracle, T, N, K, H, plan):
+    """pkv_decode_step_multi (the producers write the new rows into the pools before loading their
+    blocks) equals pkv_slot_mapping_multi + pkv_append + pkv_decode_attn_multi bit for bit: out,
+    lse, slots, both pools and the error flags -- with an empty sequence, contexts shorter than T,
+    new tokens that straddle a block edge, and (in the tapered case) enough units to taper -- and
+    matches the oracle.  T = 8, 9 at G = 4 run the tcgen05 column kernel, the rest mma.sync."""
+    lens = [0, 1, T - 1, T, T + 1, 15, 16, 17, 33, 300, 700, 1000]
+    B = len(lens)
+    if plan == "tapered":
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        B = -(-sms // K) + 2
+    w = gen.make_workload(f"fused_m_{T}_{plan}", 500 + T, N, K, H, [lens[i % len(lens)] for i in range(B)])
+    c = MultiCase(oracle, w, T, 510 + T)
+    pb = 0 if plan == "one_pass" else 4
+    P = 0
+    if plan == "split":
+        P = pkv.max_partitions_for(w.max_blocks, pb)
+    elif plan == "tapered":
+        P = pkv.tapered_partitions_for(w.max_blocks, pb)
+        assert w.B * w.K >= torch.cuda.get_device_properties(0).multi_processor_count
+    q, kn, vn = bf16_dev(c.q), bf16_dev(c.k_new), bf16_dev(c.v_new)
+    bt, cl = i32_dev(w.block_tables), i32_dev(w.context_lens)
+    res = []
+    for fused in (False, True):
+        kc, vc = bf16_dev(w.k_cache), bf16_dev(w.v_cache)
+        out = torch.full_like(q, float("nan"))
+        lse = torch.full((w.B, T, N), float("nan"), dtype=torch.float32, device="cuda")
+        slots = torch.full((w.B, T), -7, dtype=torch.int64, device="cuda")
+        ws = None
+        if P:
+            ws = torch.zeros(pkv.pkv_splitk_workspace_bytes(w.B * T, N, H, P), dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if fused:
+            pkv.check(pkv.pkv_decode_step_multi(q, kn, vn, kc, vc, bt, cl, w.scale, out, lse, slots, pb, P, ws, err))
+        else:
+            pkv.check(pkv.pkv_slot_mapping_multi(bt, cl, w.num_blocks, slots, err))
+            pkv.check(pkv.pkv_append(kn.view(-1, K, H), vn.view(-1, K, H), slots.view(-1), kc, vc, err))
+            pkv.check(pkv.pkv_decode_attn_multi(q, kc, vc, bt, cl, w.scale, out, lse, pb, P, ws, err))
+        res.append((out, lse, slots, kc, vc, pkv.pkv_read_err_flag(err)))
+    (o1, l1, s1, k1, v1, f1), (o2, l2, s2, k2, v2, f2) = res
+    assert f1 == f2 == (pkv.PKV_OK, 0)
+    assert torch.equal(s1, s2) and np.array_equal(s2.cpu().numpy(), c.slots)
+    assert torch.equal(k1.view(torch.int16), k2.view(torch.int16)) and torch.equal(v1.view(torch.int16),
+                                                                                   v2.view(torch.int16))
+    assert np.array_equal(bf16_host(k2), c.kc) and np.array_equal(bf16_host(v2), c.vc)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+    ref, ref_lse = c.reference(oracle)
+    assert_close(out_f64(o2), ref, f"fused multi T={T} {plan}")
+    assert_lse_close(l2.cpu().numpy().astype(np.float64), ref_lse, f"fused multi T={T} {plan}")
+
+
+@pytest.mark.parametrize("T", [4, 8])
+def test_fused_multi_step_bad_block_is_flagged_and_skipped(pkv, oracle, T):
+    """A table entry outside the pool in the block that holds the new tokens: flagged, slots -1,
+    nothing written there, the tile skipped -- as the separate calls do -- and every other
+    sequence matches the oracle."""
+    w = gen.make_workload(f"fused_bad_{T}", 520 + T, 16, 4, 128, [40, 90, 300, 17])
+    c = MultiCase(oracle, w, T, 530 + T)
+    bt_np = w.block_tables.copy()
+    bt_np[2, (int(w.context_lens[2]) - 1) // 16] = w.num_blocks + 5
+    q, kn, vn = bf16_dev(c.q), bf16_dev(c.k_new), bf16_dev(c.v_new)
+    bt, cl = i32_dev(bt_np), i32_dev(w.context_lens)
+    res = []
+    for fused in (False, True):
+        kc, vc = bf16_dev(w.k_cache), bf16_dev(w.v_cache)
+        out = torch.empty_like(q)
+        slots = torch.full((w.B, T), -7, dtype=torch.int64, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if fused:
+            pkv.check(pkv.pkv_decode_step_multi(q, kn, vn, kc, vc, bt, cl, w.scale, out, None, slots, 0, 0, None,
+                                                err))
+        else:
+            pkv.check(pkv.pkv_slot_mapping_multi(bt, cl, w.num_blocks, slots, err))
+            pkv.check(pkv.pkv_append(kn.view(-1, 4, 128), vn.view(-1, 4, 128), slots.view(-1), kc, vc, err))
+            pkv.check(pkv.pkv_decode_attn_multi(q, kc, vc, bt, cl, w.scale, out, None, 0, 0, None, err))
+        res.append((out, slots, kc, vc, pkv.pkv_read_err_flag(err)))
+    (o1, s1, k1, v1, f1), (o2, s2, k2, v2, f2) = res
+    assert f1 == f2 and f2[1] & pkv.PKV_FLAG_BLOCK_RANGE
+    assert torch.equal(s1, s2) and torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+    assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    ref, _ = c.reference(oracle)
+    keep = [0, 1, 3]
+    assert_close(out_f64(o2)[keep], ref[keep], "fused multi with a bad block, other sequences")
