@@ -1104,7 +1104,23 @@ PKV_EXPORT int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache
     p.max_group = max_group_size;
     p.prefix_parts = prefix_parts;
     p.prefix_ctas = (int32_t)prefix_ctas;
-    cudaError_t e = pkv::launch_attn_cols(cache.head_dim, tk, tv, p, grid, stream);
+    // With more than 16 rows per chunk (the group's members x G) the prefix pass runs on the
+    // tcgen05 column kernel, whose time per 64-token group is set by its MMA count, not its rows;
+    // the suffix pass (G rows) stays on mma.sync, in a second launch over the rest of the work.
+    bool tc = prefix_ctas > 0 && std::min(max_group_size * G, kColsPerCta) >= kColsTcMinRows &&
+              pkv::cols_tc_supported(cache.head_dim, tok_major);
+    CUtensorMap tk_half;
+    if (tc) tc = encode_kv_map(&tk_half, k_cache, cache, 0, 1) == CUDA_SUCCESS;
+    cudaError_t e;
+    if (tc) {
+        e = pkv::launch_attn_cols_tc(cache.head_dim, tk_half, tv, p, prefix_ctas, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "shared-prefix pass launch");
+        p.cta_base = prefix_ctas;
+        e = pkv::launch_attn_cols(cache.head_dim, tk, tv, p, grid - prefix_ctas, stream);
+        p.cta_base = 0;
+    } else {
+        e = pkv::launch_attn_cols(cache.head_dim, tk, tv, p, grid, stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "shared-prefix attention launch");
     e = pkv::launch_cascade_merge(p, cache.head_dim, reinterpret_cast<__nv_bfloat16 *>(out), lse_out, stream);
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "shared-prefix merge launch");

@@ -121,7 +121,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     ColsWork wk;
-    if (!cols_work(p, blockIdx.x, wk)) return;
+    if (!cols_work(p, (int64_t)blockIdx.x + p.cta_base, wk)) return;
     const int nblk = wk.blk_end - wk.blk_begin;
     multi_slots_below_zero(p, wk);
     if (nblk <= 0) {

@@ -103,6 +103,8 @@ struct ColsParams {
     int32_t prefix_part_blocks;    // prefix mode: blocks per prefix-pass partition
     int32_t prefix_parts;          // prefix mode: partitions of the prefix pass (grid)
     int32_t prefix_ctas;           // prefix mode: CTAs of the prefix pass
+    int64_t cta_base;              // work index of the launch's first CTA (a launch may run a
+                                   // part of the work: the prefix pass and the suffix pass apart)
     // multi, fused step: the T new tokens' K/V rows [B][T][K][H] (nullable: no append) are written
     // into their slots by the producer that loads their block, before it loads it
     const uint16_t *k_new;
