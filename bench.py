@@ -301,6 +301,8 @@ def kernel_label(args, plan, step) -> str:
             return name + " (partitions merged in the same launch)"
         return name + " + lse_merge_kernel"
     if args.attn == "prefix":
+        if step.launches_per_step() == 5:
+            return "attn_cols_tc_kernel<128> (prefix pass) + attn_cols_kernel<128> (suffix pass) + cascade_merge_kernel"
         return "attn_cols_kernel<128> (prefix + suffix passes) + cascade_merge_kernel"
     fp8 = "1" if args.kv == "fp8" else "0"
     if plan.mode == "split":
@@ -326,7 +328,7 @@ def config_dict(w, args) -> dict:
         d["new_tokens_per_seq"] = args.tokens
     if opt("layers", 1) > 1:
         d["layers"] = args.layers
-    if opt("attn", "auto") == "prefix":
+    if w.prefix_groups() is not None:
         d["prefix_groups"] = "one group of the whole batch sharing its full prefix blocks"
     if opt("kv", "bf16") == "fp8":
         d["kv_cache"] = ("e4m3, per-KV-head scales (amax / 448)" if opt("fp8_scales", "head") == "head"
@@ -369,6 +371,14 @@ def run_ours(args):
     plan = plan_attention(w.B, w.K, w.max_blocks, sms, partition_blocks=args.partition_blocks)
     if args.mode and args.partition_blocks is None:
         plan = plan_attention(w.B, w.K, w.max_blocks, sms, mode=args.mode)
+    groups = w.prefix_groups()
+    if args.attn == "auto" and groups is not None and args.kv == "bf16" and args.tokens == 1 and not args.unfused:
+        # sequences that share a prompt: the planner's choice between the plain step and the cascade
+        from paged_kv_decode_slot_gb300.step import PREFIX_PARTITION_BLOCKS, plan_prefix_decode
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        if plan_prefix_decode(int(groups[1].max()) * 16, w.K, w.H, l2):
+            args.attn = "prefix"
+            args.prefix_partition_blocks = args.prefix_partition_blocks or PREFIX_PARTITION_BLOCKS
     if args.tokens > 1:
         if args.kv != "bf16" or args.attn != "auto":
             raise SystemExit("--tokens > 1 runs the bf16 cache without --attn prefix")

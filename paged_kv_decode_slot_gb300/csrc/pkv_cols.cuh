@@ -79,11 +79,12 @@ __device__ __forceinline__ bool cols_work(const ColsParams &p, int64_t c, ColsWo
         return w.ncols > 0;
     }
     if (c < p.prefix_ctas / p.K) {
-        // prefix pass: (group, chunk, prefix partition)
-        const int ppart = (int)(c % p.prefix_parts);
-        c /= p.prefix_parts;
+        // prefix pass: (group, prefix partition, chunk) -- the chunks of one partition next to each
+        // other, so the CTAs that read the same prefix tiles run together (the tiles stay in L2)
         const int chunk = (int)(c % p.chunks);
-        const int g = (int)(c / p.chunks);
+        c /= p.chunks;
+        const int ppart = (int)(c % p.prefix_parts);
+        const int g = (int)(c / p.prefix_parts);
         const int gs_raw = p.group_starts[g], ge_raw = p.group_starts[g + 1];
         const int gs = max(0, min(gs_raw, p.B)), ge = max(gs, min(ge_raw, p.B));
         const int cols = (ge - gs) * p.G;

@@ -287,7 +287,7 @@ def make_prefix_workload(name: str, seed: int, N: int, K: int, H: int, B: int, p
 # --------------------------------------------------------------------------------------
 
 CONFIG_NAMES = ("tiny", "l3_8b_b64", "l3_8b_b16", "l2_13b_mha_b1", "l2_13b_mha_b8", "l2_13b_mha_b64",
-                "l2_13b_mha_b128", "prefix_l3_70b", "long_splitk")
+                "l2_13b_mha_b128", "prefix_l3_70b", "prefix_long_l3_70b", "long_splitk")
 
 
 def make_config(name: str, threads: int = 0) -> Workload:
@@ -310,6 +310,12 @@ def make_config(name: str, threads: int = 0) -> Workload:
     if name == "prefix_l3_70b":
         return make_prefix_workload("prefix_l3_70b", 4, 64, 8, 128, 20, 1000, 16, 512,
                                     threads=threads)
+    if name == "prefix_long_l3_70b" or name.startswith("prefix_l3_70b_p"):
+        # The same batch with a longer shared prompt: 32,008 tokens (2,000 full shared blocks, 128 MB
+        # of K/V per layer, about the GB300's L2) for the named workload, any length for
+        # "prefix_l3_70b_p<tokens>" (a partly filled last prefix block: tokens % 16 != 0).
+        prefix = 32008 if name == "prefix_long_l3_70b" else int(name[len("prefix_l3_70b_p"):])
+        return make_prefix_workload(name, 4, 64, 8, 128, 20, prefix, 16, 512, threads=threads)
     if name == "long_splitk":
         return make_workload("long_splitk", 5, 32, 8, 128, [131072, 32768], k_mult=0.5,
                              partition_blocks=256, threads=threads)

@@ -336,6 +336,25 @@ class MultiTokenStep:
         return [getattr(self, n) for n in self.input_names()]
 
 
+# Prefix-pass partitions of the cascade when the planner picks it (measured best at 32K shared tokens)
+PREFIX_PARTITION_BLOCKS = 128
+
+
+def plan_prefix_decode(prefix_tokens: int, num_kv_heads: int, head_dim: int, l2_bytes: int) -> bool:
+    """Whether a batch whose sequences share ``prefix_tokens`` leading tokens is better served by the
+    shared-prefix cascade (``PrefixDecodeStep``) than by the plain decode step.
+
+    Measured on GB300 (20 sequences, 64 query / 8 KV heads, head_dim 128, suffixes of 16..512 tokens;
+    µs per step from a CUDA graph, plain / best cascade): 1,000 shared tokens 30.0 / 41.4, 4,008
+    46.6 / 61.5, 8,008 73.2 / 86.6, 16,008 116.9 / 123.1, 32,008 209.1 / 195.0.  The plain step reads
+    the prefix once per sequence, but its CTAs read the same prefix blocks at nearly the same time,
+    so the re-reads hit L2 while the shared K/V fits there; the cascade reads it once per KV head and
+    query-row chunk and pays for its prefix pass (tcgen05 MMAs, 32 rows a CTA) and its merge.  The
+    crossover lies between 16K and 32K shared tokens (66 and 131 MB of K/V against a 129 MB L2):
+    the cascade from three quarters of the L2 on."""
+    return prefix_tokens * num_kv_heads * head_dim * 2 * 2 * 4 >= 3 * l2_bytes
+
+
 class PrefixDecodeStep:
     """A decode step of a batch whose sequences share leading blocks (copy-on-write prefix
     sharing): slot mapping and append of the new token, then ``pkv_decode_attn_prefix`` -- each
@@ -393,7 +412,11 @@ class PrefixDecodeStep:
         self.attention(stream)
 
     def launches_per_step(self) -> int:
-        return 4
+        # slot mapping, append, the prefix and suffix passes (one launch, or the tcgen05 prefix pass
+        # and the mma.sync suffix pass), the merge
+        _, N, H = self.q.shape
+        tc = B.pkv_multi_uses_tcgen05(self.max_group_size, N, self.k_cache.shape[2], H)
+        return 5 if tc else 4
 
     def input_names(self):
         return ("q", "k_new", "v_new", "block_tables", "context_lens", "group_starts", "prefix_blocks")

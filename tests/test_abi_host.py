@@ -252,3 +252,15 @@ def test_test_build_exports_the_hook(tmp_path):
     if out.returncode == 0:
         exported = set(re.findall(r"\s[TW]\s+(pkv_\w+)$", out.stdout, flags=re.M))
         assert exported == set(declared_functions()) | {"pkv_debug_withhold_tile"}
+
+
+def test_prefix_planner_crossover():
+    """The cascade is planned once the shared prompt's K/V reaches three quarters of the L2 (GB300:
+    129 MB; the measured crossover of the 20-sequence, 8-KV-head batch lies between 16K and 32K
+    tokens)."""
+    from paged_kv_decode_slot_gb300.step import plan_prefix_decode
+    l2 = 129 * 1024 * 1024
+    assert not plan_prefix_decode(1000, 8, 128, l2)
+    assert not plan_prefix_decode(16008, 8, 128, l2)
+    assert plan_prefix_decode(2000 * 16, 8, 128, l2)
+    assert not plan_prefix_decode(2000 * 16, 1, 128, l2)

@@ -512,3 +512,21 @@ def test_fused_multi_step_bad_block_is_flagged_and_skipped(pkv, oracle, T):
     ref, _ = c.reference(oracle)
     keep = [0, 1, 3]
     assert_close(out_f64(o2)[keep], ref[keep], "fused multi with a bad block, other sequences")
+
+
+@pytest.mark.parametrize("prefix_part_blocks", [64, 128])
+def test_prefix_long_cascade_matches_oracle(pkv, oracle, prefix_part_blocks):
+    """20 sequences sharing a 32,008-token prompt (2,000 full shared blocks, about the L2's size in
+    K/V): the cascade (the prefix pass on the tcgen05 column kernel, 160 query rows per KV head in
+    chunks of 32) matches the oracle's plain decode on every row."""
+    w = gen.make_config("prefix_long_l3_70b")
+    starts, pblocks = w.prefix_groups()
+    assert int(pblocks[0]) == 2000
+    kc, vc = appended_host_cache(oracle, w)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_prefix(pkv, w, bf16_dev(kc), bf16_dev(vc), w.block_tables, starts, pblocks, 16, err=err,
+                          prefix_part_blocks=prefix_part_blocks)
+    assert pkv.pkv_read_err_flag(err) == (pkv.PKV_OK, 0)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+    assert_close(out_f64(out), ref, f"long prefix, {prefix_part_blocks}-block prefix partitions")
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), ref_lse, "long prefix")
