@@ -374,11 +374,12 @@ def run_ours(args):
     groups = w.prefix_groups()
     if args.attn == "auto" and groups is not None and args.kv == "bf16" and args.tokens == 1 and not args.unfused:
         # sequences that share a prompt: the planner's choice between the plain step and the cascade
-        from paged_kv_decode_slot_gb300.step import PREFIX_PARTITION_BLOCKS, plan_prefix_decode
+        from paged_kv_decode_slot_gb300.step import plan_prefix_decode
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-        if plan_prefix_decode(int(groups[1].max()) * 16, w.K, w.H, l2):
+        ppb = plan_prefix_decode(int(groups[1].max()) * 16, w.K, w.H, l2)
+        if ppb:
             args.attn = "prefix"
-            args.prefix_partition_blocks = args.prefix_partition_blocks or PREFIX_PARTITION_BLOCKS
+            args.prefix_partition_blocks = args.prefix_partition_blocks or ppb
     if args.tokens > 1:
         if args.kv != "bf16" or args.attn != "auto":
             raise SystemExit("--tokens > 1 runs the bf16 cache without --attn prefix")
@@ -396,7 +397,7 @@ def run_ours(args):
         gs, pb = groups
         step = PrefixDecodeStep(q, kn, vn, kc, vc, bt, cl, w.scale, d32(gs), d32(pb),
                                 int(np.max(np.diff(gs))), int(pb.max()),
-                                partition_blocks=args.partition_blocks or 16,
+                                partition_blocks=args.partition_blocks,
                                 prefix_partition_blocks=args.prefix_partition_blocks, err_flag=err)
         plan = step.plan
     elif args.kv == "fp8":

@@ -825,10 +825,12 @@ pkv::ColsParams cols_params_of(const AttnArgs &a, int tok_major)
 #ifdef PKV_TEST_HOOKS
     p.withhold_tile = g_withhold_tile.load(std::memory_order_relaxed);
 #endif
+    p.chunk_rows = 32;
     return p;
 }
 
-constexpr int kColsPerCta = 32;  // query rows per CTA of the column-parallel kernel
+constexpr int kColsPerCta = 32;   // query rows per CTA of the column-parallel kernel
+constexpr int kColsPerCtaTc = 128;  // of the 128-row tcgen05 form, for rows beyond 32
 // Query rows per CTA from which the tcgen05 column kernel does the work.  Its time per 64-token
 // group is set by its MMA instructions (8 QK^T + 4 PV whatever the row count), the mma.sync
 // kernel's by its per-warp tile updates (one per 8 rows): with 32 rows the tensor cores are 1.5x
@@ -950,6 +952,14 @@ int multi_attention(const AttnArgs &a, int32_t num_new, const pkv_bf16 *k_new, c
               pkv::cols_tc_supported(cache.head_dim, tok_major);
     CUtensorMap tk_half;
     if (tc) tc = encode_kv_map(&tk_half, a.k_cache, cache, 0, 1) == CUDA_SUCCESS;
+    int64_t grid_run = grid;
+    if (tc && num_new * G > kColsPerCta) {
+        // more than 32 rows: the 128-row tcgen05 form (a group's MMAs serve 128 rows for the cost
+        // of 32), chunks of 128 rows
+        p.chunk_rows = kColsPerCtaTc;
+        p.chunks = (num_new * G + kColsPerCtaTc - 1) / kColsPerCtaTc;
+        grid_run = (int64_t)cache.num_kv_heads * num_seqs * p.chunks * parts;
+    }
     // The mma.sync kernel tapers its partitions as the one-token kernel does (partition_range) when
     // its grid runs in several waves and max_partitions has room: Llama-3-8B batch of 64, 4 new
     // tokens 222.5 -> 218.1 us, 2 new tokens 198.7 -> 196.8; the tcgen05 kernel gained nothing.
@@ -966,7 +976,7 @@ int multi_attention(const AttnArgs &a, int32_t num_new, const pkv_bf16 *k_new, c
     if (split && !tc && (int64_t)kColsPerCta * max_partitions <= kInKernelMergeWeights)
         p.counters = split_ws(workspace, (int32_t)(num_seqs * (int64_t)num_new), num_q_heads, cache.head_dim,
                               max_partitions).counters;
-    cudaError_t e = tc ? pkv::launch_attn_cols_tc(cache.head_dim, tk_half, tv, p, grid, stream)
+    cudaError_t e = tc ? pkv::launch_attn_cols_tc(cache.head_dim, tk_half, tv, p, grid_run, stream)
                        : pkv::launch_attn_cols(cache.head_dim, tk, tv, p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "multi-token attention launch");
     if (!split || p.counters) return PKV_OK;
@@ -1113,11 +1123,22 @@ PKV_EXPORT int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache
     if (tc) tc = encode_kv_map(&tk_half, k_cache, cache, 0, 1) == CUDA_SUCCESS;
     cudaError_t e;
     if (tc) {
-        e = pkv::launch_attn_cols_tc(cache.head_dim, tk_half, tv, p, prefix_ctas, stream);
+        // more than 32 rows a group: the 128-row tcgen05 form, chunks of 128 rows
+        int64_t pctas = prefix_ctas;
+        if (max_group_size * G > kColsPerCta) {
+            p.chunk_rows = kColsPerCtaTc;
+            p.chunks = (max_group_size * G + kColsPerCtaTc - 1) / kColsPerCtaTc;
+            pctas = (int64_t)cache.num_kv_heads * num_groups * p.chunks * prefix_parts;
+            p.prefix_ctas = (int32_t)pctas;
+        }
+        e = pkv::launch_attn_cols_tc(cache.head_dim, tk_half, tv, p, pctas, stream);
         if (e != cudaSuccess) return cuda_fail(e, "shared-prefix pass launch");
-        p.cta_base = prefix_ctas;
-        e = pkv::launch_attn_cols(cache.head_dim, tk, tv, p, grid - prefix_ctas, stream);
-        p.cta_base = 0;
+        // the suffix pass alone: with no prefix CTAs in its grid, its CTAs number the suffix work
+        // from 0 (the partial slots and the merge do not depend on the prefix CTA count)
+        pkv::ColsParams ps = p;
+        ps.prefix_ctas = 0;
+        ps.chunk_rows = kColsPerCta;
+        e = pkv::launch_attn_cols(cache.head_dim, tk, tv, ps, grid - prefix_ctas, stream);
     } else {
         e = pkv::launch_attn_cols(cache.head_dim, tk, tv, p, grid, stream);
     }

@@ -129,7 +129,7 @@ attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     const int lane = threadIdx.x & 31;
 
     ColsWork wk;
-    if (!cols_work(p, (int64_t)blockIdx.x + p.cta_base, wk)) return;
+    if (!cols_work(p, blockIdx.x, wk)) return;
     const int nblk = wk.blk_end - wk.blk_begin;
     // Split multi-token units merged in this launch: a sequence held by one partition is written
     // out directly, one held by several leaves partials for the last of its CTAs to merge.

@@ -10,64 +10,79 @@
 // ("Optimización de la inferencia", "Construye el mismo", Step 2), so every K/V byte fetched from
 // HBM serves all rows of the CTA and no warp spends issue slots on the contraction itself.
 //
-// CTA = 5 warps:
-//  * warps 2-3: TMA producers, the same full/empty mbarrier ring as the other attention kernels
-//    (12 stages of a K and a V tile, 128-byte swizzled -- the layout the MMA reads directly).  The
+// Two forms, by the number RW of row warps: 32 query rows a CTA (RW = 1, 5 warps, a 12-stage ring)
+// and 128 (RW = 4, 8 warps, an 8-stage ring, so that two CTAs still fit an SM): the MMA has
+// M = 128 rows whatever the form, and a group costs the same MMA instructions for 32 rows as for
+// 128, so groups of rows wider than 32 (a shared prefix read for every member of its group, or many
+// new tokens) take the 128-row form.  CTA = RW + 4 warps:
+//  * warps RW+2, RW+3: TMA producers, the same full/empty mbarrier ring as the other attention
+//    kernels (K and V tiles, 128-byte swizzled -- the layout the MMA reads directly).  The
 //    two 64-element halves of a K tile land in two separate regions, so the K tiles of four
 //    consecutive stages form one 64-token operand: one MMA per 16-element step covers a whole
 //    group (a tcgen05.mma costs its issuing thread about the same time for N = 16 as for N = 256,
 //    so the number of instructions, not their size, sets the pace);
-//  * warp 1: allocates 256 TMEM columns (O: 128, two S/P buffers of 64) and issues, from one lane,
+//  * warp RW: allocates 256 TMEM columns (O: 128, two S/P buffers of 64) and issues, from one lane,
 //    QK^T of group g (8 MMAs, N = 64) as soon as its tiles landed (and PV(g-2) freed the S buffer);
-//  * warp 2: issues PV of group g (one MMA per tile) from one lane as soon as its P is ready, and
+//  * warp RW+1: issues PV of group g (one MMA per tile) from one lane as soon as every row warp
+//    wrote its part of P, and
 //    one commit that releases the group's four stages.  Two issuing threads: an MMA costs its
 //    issuer a fixed latency, and a PV no longer waits behind the next group's loads;
-//  * warp 0: one thread per query row (TMEM lanes 0..31): reads the row's 64 logits, masks tokens
-//    the row may not see, keeps the lazily rescaled running max and sum, writes P (bf16) over the
-//    logits, and at the end reads O, normalises it and writes out / lse (or the partials).
-// The MMA has M = 128 rows; rows 32..127 are padding whose results are never read.
+//  * warps 0 .. RW-1: one thread per query row (warp w: TMEM lanes 32w .. 32w+31): reads the row's
+//    64 logits, masks tokens the row may not see, keeps the lazily rescaled running max and sum,
+//    writes P (bf16) over the logits, and at the end reads O, normalises it and writes out / lse
+//    (or the partials).
+// The MMA has M = 128 rows; with RW = 1, rows 32..127 are padding whose results are never read.
 #include "pkv_cols.cuh"
 #include "pkv_tcgen05.cuh"
 
 namespace pkv {
 
-constexpr int kTcStages = 12;
 constexpr int kTcGroupTiles = 4;   // tiles per softmax step (64 tokens)
 constexpr int kTcM = 128;          // MMA rows
 constexpr int kTcProducers = 2;
-constexpr int kTcThreads = 160;    // warp 0 rows, warp 1 QK^T MMAs, warp 2 PV MMAs, warps 3-4 producers
 constexpr uint32_t kTcCols = 256;  // TMEM columns: O [0, H), S/P buffers at H and H + 64
-static_assert(kTcStages % kTcProducers == 0, "pipeline depth must be a multiple of the producer warps");
-static_assert(kTcStages >= 2 * kTcGroupTiles, "two groups of tiles must fit in the ring");
-static_assert(kColsPerCta <= 32, "one thread per query row: warp 0 holds the CTA's rows");
 
-template <int H>
+// RW row warps (32 rows each), then the QK^T warp, the PV warp and the two producers.
+template <int RW>
+struct TcRoles {
+    static_assert(RW == 1 || RW == 4, "32 or 128 query rows a CTA");
+    static constexpr int kRows = 32 * RW;
+    static constexpr int kStages = RW == 1 ? 12 : 8;
+    static constexpr int kQkWarp = RW, kPvWarp = RW + 1, kProd0 = RW + 2;
+    static constexpr int kThreads = (RW + 4) * 32;
+    static_assert(kStages % kTcProducers == 0, "pipeline depth must be a multiple of the producer warps");
+    static_assert(kStages >= 2 * kTcGroupTiles, "two groups of tiles must fit in the ring");
+};
+
+template <int H, int RW>
 struct TcLayout {
     static_assert(H == 128, "the tensor-core column kernel is built for H = 128");
-    // Q: the CTA's 32 rows as the K-major A operand, two 64-element halves of 4 atoms each
+    static constexpr int kStages = TcRoles<RW>::kStages;
+    // Q: the CTA's rows as the K-major A operand, two 64-element halves of rows / 8 atoms each
     static constexpr int kQOffset = 0;
-    static constexpr int kQHalfBytes = (kColsPerCta / 8) * 1024;
+    static constexpr int kQHalfBytes = (TcRoles<RW>::kRows / 8) * 1024;
     // K: two regions (one per 64-element half) of [stage][16 tokens][128 bytes]
     static constexpr int kKHalfTile = kBlockSize * 128;
     static constexpr int kKOffset = kQOffset + (H / 64) * kQHalfBytes;
-    static constexpr int kKRegion = kTcStages * kKHalfTile;
+    static constexpr int kKRegion = kStages * kKHalfTile;
     // V: [stage][half][16 tokens][128 bytes]
     static constexpr int kVTile = kBlockSize * H * 2;
     static constexpr int kVOffset = kKOffset + (H / 64) * kKRegion;
     static constexpr int kStageBytes = 2 * kVTile;  // bytes one stage receives (K and V)
     static constexpr int kRingOffset = kKOffset;
     // barriers: full[S], group_free[S / 4], s_full[2], p_ready[2], o_done, fin
-    static constexpr int kGroupSlots = kTcStages / kTcGroupTiles;
-    static constexpr int kBarOffset = kVOffset + kTcStages * kVTile;
-    static constexpr int kMiscOffset = kBarOffset + (kTcStages + kGroupSlots + 6) * 8;  // slot_ok[S], abort, issued[P], tmem
-    static constexpr int kBytes = kMiscOffset + (kTcStages + 2 + kTcProducers) * 4;
+    static constexpr int kGroupSlots = kStages / kTcGroupTiles;
+    static constexpr int kBarOffset = kVOffset + kStages * kVTile;
+    static constexpr int kMiscOffset = kBarOffset + (kStages + kGroupSlots + 6) * 8;  // slot_ok[S], abort, issued[P], tmem
+    static constexpr int kBytes = kMiscOffset + (kStages + 2 + kTcProducers) * 4;
     static constexpr int kAlloc = kBytes + 1024;
-    // The A descriptor spans M = 128 rows: the padding rows read on into the ring (in bounds).
+    // The A descriptor spans M = 128 rows: with 32 rows the padding rows read on into the ring (in
+    // bounds).
     static_assert(kRingOffset + (H / 64 - 1) * kQHalfBytes + (kTcM / 8) * 1024 <= kBarOffset,
                   "the padding rows of the Q operand must stay inside the CTA's shared memory");
     static_assert(kKOffset % 1024 == 0 && kVOffset % 1024 == 0 && kKHalfTile % 1024 == 0 && kVTile % 1024 == 0,
                   "128B-swizzle atoms need 1024-byte alignment");
-    static_assert(kTcStages % kTcGroupTiles == 0, "a group's K tiles must not wrap around the ring");
+    static_assert(kStages % kTcGroupTiles == 0, "a group's K tiles must not wrap around the ring");
     static_assert(2 * (kAlloc + 1024) <= 228 * 1024 && 3 * (kAlloc + 1024) > 228 * 1024,
                   "two CTAs per SM (2 x 256 TMEM columns fill the SM's 512)");
 };
@@ -76,17 +91,17 @@ struct TcLayout {
 // (one commit after that group's PV frees its four stages), then three TMA loads (the two K halves
 // into their regions, the V tile) completing on the stage's full barrier; an out-of-range block
 // id marks the stage skipped.  Returns false when the wait expired.
-template <int H>
+template <int H, int RW>
 __device__ __forceinline__ bool produce_tile_tc(int64_t i, int kvh, int bid, bool ok, uint32_t kreg, uint32_t vreg,
                                                 uint32_t bar_full, uint32_t bar_free, volatile int *slot_ok,
                                                 volatile int *abort_flag, const CUtensorMap *tm_kh,
                                                 const CUtensorMap *tm_v, int32_t *err_flag, uint64_t wait_ns)
 {
-    using L = TcLayout<H>;
-    const int s = (int)(i % kTcStages);
+    using L = TcLayout<H, RW>;
+    constexpr int S = L::kStages;
+    const int s = (int)(i % S);
     const int slot = (int)((i / kTcGroupTiles) % L::kGroupSlots);
-    if (i >= kTcStages &&
-        !mbar_wait_bounded(bar_free + 8 * slot, (uint32_t)(((i / kTcStages) & 1) ^ 1), abort_flag, wait_ns)) {
+    if (i >= S && !mbar_wait_bounded(bar_free + 8 * slot, (uint32_t)(((i / S) & 1) ^ 1), abort_flag, wait_ns)) {
         if (!*abort_flag) set_flag(err_flag, PKV_FLAG_TIMEOUT);
         *abort_flag = 1;
         return false;
@@ -106,13 +121,15 @@ __device__ __forceinline__ bool produce_tile_tc(int64_t i, int kvh, int bid, boo
     return true;
 }
 
-template <int H>
-__global__ void __launch_bounds__(kTcThreads, 2)
+template <int H, int RW>
+__global__ void __launch_bounds__(TcRoles<RW>::kThreads, 2)
 attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const ColsParams p)
 {
-    using L = TcLayout<H>;
-    constexpr int S = kTcStages;
+    using L = TcLayout<H, RW>;
+    using R = TcRoles<RW>;
+    constexpr int S = L::kStages;
+    constexpr int kTcThreads = R::kThreads;
     constexpr int GT = kTcGroupTiles;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -121,7 +138,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     ColsWork wk;
-    if (!cols_work(p, (int64_t)blockIdx.x + p.cta_base, wk)) return;
+    if (!cols_work<R::kRows>(p, blockIdx.x, wk)) return;
     const int nblk = wk.blk_end - wk.blk_begin;
     multi_slots_below_zero(p, wk);
     if (nblk <= 0) {
@@ -161,24 +178,26 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         for (int q = 0; q < L::kGroupSlots; ++q) mbar_init(bar_free + 8 * q, 1);
         mbar_init(bar_sfull, 1);
         mbar_init(bar_sfull + 8, 1);
-        mbar_init(bar_pready, 1);
-        mbar_init(bar_pready + 8, 1);
+        mbar_init(bar_pready, RW);  // every row warp writes its rows of P
+        mbar_init(bar_pready + 8, RW);
         mbar_init(bar_odone, 1);
         mbar_init(bar_fin, 2);  // one commit from each MMA-issuing warp
         fence_barrier_init();
     }
     __syncthreads();  // the barriers are ready: the producers start loading at once
 
-    // Meanwhile warps 0-2 put the CTA's q rows into the K-major, 128B-swizzled A operand (rows
-    // past ncols are zero) and warp 1 allocates the tensor memory; they meet at a named barrier.
+    // Meanwhile the row warps and the two MMA warps put the CTA's q rows into the K-major,
+    // 128B-swizzled A operand (rows past ncols are zero) and the QK^T warp allocates the tensor
+    // memory; they meet at a named barrier.
     uint32_t tm_o = 0, tm_s = 0;  // O at tm_o (lane 0, first allocated column), S/P at tm_s, tm_s + 64
-    if (warp < 3) {
+    constexpr int kQThreads = (RW + 2) * 32;
+    if (warp < RW + 2) {
         // all of a thread's loads first (one round trip), then the stores
-        constexpr int kUnits = kColsPerCta * (H / 8), kPer = (kUnits + 95) / 96;
+        constexpr int kUnits = R::kRows * (H / 8), kPer = (kUnits + kQThreads - 1) / kQThreads;
         uint4 v[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            const int idx = threadIdx.x + 96 * k;
+            const int idx = threadIdx.x + kQThreads * k;
             const int r = idx / (H / 8), u = idx - r * (H / 8);  // row, 16-byte unit of the row
             v[k] = make_uint4(0u, 0u, 0u, 0u);
             if (idx < kUnits && r < wk.ncols) {
@@ -191,7 +210,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            const int idx = threadIdx.x + 96 * k;
+            const int idx = threadIdx.x + kQThreads * k;
             if (idx < kUnits) {
                 const int r = idx / (H / 8), u = idx - r * (H / 8);
                 const int half = u >> 3, cu = u & 7;
@@ -200,20 +219,20 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             }
         }
         fence_proxy_async_shared();
-        if (warp == 1) {
+        if (warp == R::kQkWarp) {
             tmem_alloc(smem_u32((const void *)tmem_slot), kTcCols);
             tmem_relinquish();
         }
         tc_fence_before();
-        asm volatile("bar.sync 1, 96;" ::: "memory");  // warps 0-2
+        asm volatile("bar.sync 1, %0;" ::"n"(kQThreads) : "memory");  // row warps and MMA warps
         tc_fence_after();
         tm_o = *tmem_slot;
         tm_s = tm_o + H;
     }
 
-    if (warp >= 3) {
+    if (warp >= R::kProd0) {
         // ------------------------------ producer warps ------------------------------
-        const int pw = warp - 3;
+        const int pw = warp - R::kProd0;
         if (lane == 0 && pw == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
@@ -223,12 +242,12 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             pw, lane, nblk, [&](int64_t i) { return __ldg(tbl + i); }, p.num_blocks, p.err_flag,
             [&](int64_t i, int bid, bool ok, float2) {
                 if (PKV_TILE_WITHHELD(p, i)) return true;  // test builds: never loaded, never signalled
-                return produce_tile_tc<H>(i, wk.kvh, bid, ok, kreg, vreg, bar_full, bar_free, slot_ok, abort_flag,
+                return produce_tile_tc<H, RW>(i, wk.kvh, bid, ok, kreg, vreg, bar_full, bar_free, slot_ok, abort_flag,
                                           &tm_k, &tm_v, p.err_flag, p.wait_ns);
             },
             NoAux(), false, 0, [&](int64_t i, int bid, bool ok) { append_multi_rows<H>(p, wk, i, bid, ok, lane); });
         if (lane == 0) issued_count[pw] = (int)issued;
-    } else if (warp == 1) {
+    } else if (warp == R::kQkWarp) {
         // ----------------------- QK^T warp (lane 0 issues) -----------------------
         bool ok = true;
         for (int g = 0; g < ngroups && ok; ++g) {
@@ -267,7 +286,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             if (lane == 0 && !*abort_flag) set_flag(p.err_flag, PKV_FLAG_TIMEOUT);
             *abort_flag = 1;
         }
-    } else if (warp == 2) {
+    } else if (warp == R::kPvWarp) {
         // ------------------------- PV warp (lane 0 issues) -------------------------
         constexpr uint32_t kIdPV = idesc_bf16_f32(kTcM, H, 0, 1);  // O: N = H, V MN-major
         // The tile holding the end of the data may carry poison in its later rows: their V rows
@@ -313,8 +332,9 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             *abort_flag = 1;
         }
     } else {
-        // --------------------- row warp: one thread per query row ---------------------
-        const int r = lane;  // TMEM lane r = MMA row r = query row r of the CTA
+        // --------------------- row warps: one thread per query row ---------------------
+        const int r = 32 * warp + lane;  // TMEM lane r = MMA row r = query row r of the CTA
+        const uint32_t lq = (uint32_t)(32 * warp) << 16;  // the warp's TMEM lane quarter
         const bool real = r < wk.ncols;
         int64_t row = 0;
         int vis = 0;
@@ -338,7 +358,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             const uint32_t sb = tm_s + 64 * (g & 1);
             uint32_t sr[GT][16];
 #pragma unroll
-            for (int t = 0; t < GT; ++t) tmem_ld16(sb + 16 * t, sr[t]);
+            for (int t = 0; t < GT; ++t) tmem_ld16(lq + sb + 16 * t, sr[t]);
             tmem_ld_wait();
             const int tok0 = (wk.blk_begin + i0) * kBlockSize;
             float x[GT * 16];
@@ -370,11 +390,11 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll 1
                     for (int c = 0; c < H; c += 16) {
                         uint32_t o[16];
-                        tmem_ld16(tm_o + c, o);
+                        tmem_ld16(lq + tm_o + c, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                        tmem_st16(tm_o + c, o);
+                        tmem_st16(lq + tm_o + c, o);
                     }
                     tmem_st_wait();
                 }
@@ -388,8 +408,8 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                 pk[c >> 4][c & 15] = v;
                 l += bf16x2_lo(v) + bf16x2_hi(v);  // the sum of the weights PV uses
             }
-            tmem_st16(sb, pk[0]);
-            tmem_st16(sb + 16, pk[1]);
+            tmem_st16(lq + sb, pk[0]);
+            tmem_st16(lq + sb + 16, pk[1]);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -406,7 +426,7 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 #pragma unroll 1
             for (int c = 0; c < H; c += 16) {
                 uint32_t o[16];
-                tmem_ld16(tm_o + c, o);
+                tmem_ld16(lq + tm_o + c, o);
                 tmem_ld_wait();
                 if (!real) continue;
                 float v[16];
@@ -440,8 +460,9 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // ------------------------------------ teardown ------------------------------------
     __syncthreads();
     if (*abort_flag) {
-        if (warp >= 3 && lane == 0) drain_ring<S, kTcProducers>(bar_full, warp - 3, issued_count[warp - 3]);
-        if (warp == 1 || warp == 2) {
+        if (warp >= R::kProd0 && lane == 0)
+            drain_ring<S, kTcProducers>(bar_full, warp - R::kProd0, issued_count[warp - R::kProd0]);
+        if (warp == R::kQkWarp || warp == R::kPvWarp) {
             // every MMA this CTA issued completes before its TMEM is released
             if (lane == 0) tc_commit(bar_fin);
             __syncwarp();
@@ -450,27 +471,28 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == R::kQkWarp) {
         tc_fence_after();
         tmem_dealloc(tm_o, kTcCols);
     }
 }
 
-template <int H>
+template <int H, int RW>
 static cudaError_t launch_cols_tc_t(const CUtensorMap &tk, const CUtensorMap &tv, const ColsParams &p,
                                     int64_t grid, cudaStream_t stream)
 {
-    constexpr int smem = TcLayout<H>::kAlloc;
+    constexpr int smem = TcLayout<H, RW>::kAlloc;
     static int cached[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!cached[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(attn_cols_tc_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e =
+            cudaFuncSetAttribute(attn_cols_tc_kernel<H, RW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         cached[dev] = 1;
     }
-    attn_cols_tc_kernel<H><<<(unsigned)grid, kTcThreads, smem, stream>>>(tk, tv, p);
+    attn_cols_tc_kernel<H, RW><<<(unsigned)grid, TcRoles<RW>::kThreads, smem, stream>>>(tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -481,7 +503,9 @@ cudaError_t launch_attn_cols_tc(int H, const CUtensorMap &tk, const CUtensorMap 
 {
     if (grid <= 0) return cudaSuccess;
     if (!cols_tc_supported(H, p.tok_major)) return cudaErrorInvalidValue;
-    return launch_cols_tc_t<128>(tk, tv, p, grid, stream);
+    if (p.chunk_rows == 128) return launch_cols_tc_t<128, 4>(tk, tv, p, grid, stream);
+    if (p.chunk_rows == 32) return launch_cols_tc_t<128, 1>(tk, tv, p, grid, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv

@@ -22,7 +22,7 @@ struct ColsWork {
     int ctx;        // multi: the sequence's context length
     int vis;        // prefix / suffix: tokens every column sees
     int col_base;   // first column of this CTA's chunk
-    int ncols;      // columns of this CTA (1..32)
+    int ncols;      // columns of this CTA (1 .. chunk_rows)
     int table_row;  // block-table row the blocks come from
     int blk_begin, blk_end;
     int data_end;   // tokens [0, data_end) of the block list hold data; later slots may be poison
@@ -47,7 +47,9 @@ __device__ __forceinline__ int group_of(const ColsParams &p, int b)
     return lo;
 }
 
-// Decode CTA c of the grid into its work.  Returns false when the CTA has nothing to do.
+// Decode CTA c of the grid into its work (kChunkRows: the kernel's query rows per CTA, which the
+// caller's p.chunk_rows matches).  Returns false when the CTA has nothing to do.
+template <int kChunkRows = kColsPerCta>
 __device__ __forceinline__ bool cols_work(const ColsParams &p, int64_t c, ColsWork &w)
 {
     const bool first_thread = threadIdx.x == 0;
@@ -68,8 +70,8 @@ __device__ __forceinline__ bool cols_work(const ColsParams &p, int64_t c, ColsWo
         }
         w.ctx = ctx;
         w.vis = ctx;
-        w.col_base = chunk * kColsPerCta;
-        w.ncols = min(kColsPerCta, p.T * p.G - w.col_base);
+        w.col_base = chunk * kChunkRows;
+        w.ncols = min(kChunkRows, p.T * p.G - w.col_base);
         w.table_row = w.b;
         const int nb = (ctx + kBlockSize - 1) / kBlockSize;
         partition_range(part, partition_count(nb, p.part_blocks, p.taper != 0), nb, p.part_blocks, p.taper != 0,
@@ -97,8 +99,8 @@ __device__ __forceinline__ bool cols_work(const ColsParams &p, int64_t c, ColsWo
         w.mode = kModePrefix;
         w.b = gs;
         w.vis = pnb * kBlockSize;
-        w.col_base = chunk * kColsPerCta;
-        w.ncols = min(kColsPerCta, cols - w.col_base);
+        w.col_base = chunk * kChunkRows;
+        w.ncols = min(kChunkRows, cols - w.col_base);
         w.table_row = gs;
         w.blk_begin = ppart * p.prefix_part_blocks;
         w.blk_end = min(pnb, w.blk_begin + p.prefix_part_blocks);
@@ -221,6 +223,7 @@ __device__ void cols_merge_chunk(const ColsParams &p, const ColsWork &wk, int np
     __shared__ int last_one;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
     __syncthreads();  // every partial of this CTA is written
+    // (the mma.sync column kernel, the only one merging here, always runs 32-row chunks)
     int32_t *count = p.counters + ((int64_t)wk.b * p.K + wk.kvh) * p.chunks + wk.col_base / kColsPerCta;
     if (tid == 0) last_one = atomic_add_acq_rel_gpu(count, 1) == nparts - 1;
     __syncthreads();

@@ -89,7 +89,8 @@ struct ColsParams {
     int32_t parts;                 // multi: partitions per sequence
     int32_t split;                 // multi: write partials (1) or final outputs (0, parts == 1)
     int32_t max_parts;             // partition stride of part_out / part_lse
-    int32_t chunks;                // column chunks of 32 per work unit
+    int32_t chunks;                // column chunks of chunk_rows per work unit
+    int32_t chunk_rows;            // query rows per CTA: 32, or 128 on the 128-row tcgen05 kernel
     __nv_bfloat16 *out;            // multi, one pass: [rows][H]
     float *lse_out;                // nullable
     float *part_out;               // [rows][max_parts][H]
@@ -103,8 +104,6 @@ struct ColsParams {
     int32_t prefix_part_blocks;    // prefix mode: blocks per prefix-pass partition
     int32_t prefix_parts;          // prefix mode: partitions of the prefix pass (grid)
     int32_t prefix_ctas;           // prefix mode: CTAs of the prefix pass
-    int64_t cta_base;              // work index of the launch's first CTA (a launch may run a
-                                   // part of the work: the prefix pass and the suffix pass apart)
     // multi, fused step: the T new tokens' K/V rows [B][T][K][H] (nullable: no append) are written
     // into their slots by the producer that loads their block, before it loads it
     const uint16_t *k_new;

@@ -336,23 +336,26 @@ class MultiTokenStep:
         return [getattr(self, n) for n in self.input_names()]
 
 
-# Prefix-pass partitions of the cascade when the planner picks it (measured best at 32K shared tokens)
-PREFIX_PARTITION_BLOCKS = 128
-
-
-def plan_prefix_decode(prefix_tokens: int, num_kv_heads: int, head_dim: int, l2_bytes: int) -> bool:
-    """Whether a batch whose sequences share ``prefix_tokens`` leading tokens is better served by the
-    shared-prefix cascade (``PrefixDecodeStep``) than by the plain decode step.
+def plan_prefix_decode(prefix_tokens: int, num_kv_heads: int, head_dim: int, l2_bytes: int) -> int:
+    """The shared-prefix cascade's prefix-pass partition size (blocks) when it is the better plan for
+    a batch whose sequences share ``prefix_tokens`` leading tokens, else 0 (the plain decode step).
 
     Measured on GB300 (20 sequences, 64 query / 8 KV heads, head_dim 128, suffixes of 16..512 tokens;
-    µs per step from a CUDA graph, plain / best cascade): 1,000 shared tokens 30.0 / 41.4, 4,008
-    46.6 / 61.5, 8,008 73.2 / 86.6, 16,008 116.9 / 123.1, 32,008 209.1 / 195.0.  The plain step reads
-    the prefix once per sequence, but its CTAs read the same prefix blocks at nearly the same time,
-    so the re-reads hit L2 while the shared K/V fits there; the cascade reads it once per KV head and
-    query-row chunk and pays for its prefix pass (tcgen05 MMAs, 32 rows a CTA) and its merge.  The
-    crossover lies between 16K and 32K shared tokens (66 and 131 MB of K/V against a 129 MB L2):
-    the cascade from three quarters of the L2 on."""
-    return prefix_tokens * num_kv_heads * head_dim * 2 * 2 * 4 >= 3 * l2_bytes
+    µs per step from a CUDA graph, plain / cascade with its best prefix partitions): 1,000 shared
+    tokens 30.0 / 44.5, 4,008 46.6 / 53.5, 8,008 73.2 / 61.8, 16,008 116.9 / 78.1, 32,008
+    209.1 / 110.6.  The plain step reads the prefix once per sequence, its CTAs at nearly the same
+    time, so the re-reads mostly hit L2; the cascade reads it once per KV head and 128-row chunk of
+    the group's queries (the tcgen05 column kernel) and pays a second launch and a merge.  The
+    crossover lies between 4K and 8K shared tokens (16 and 33 MB of K/V against a 129 MB L2): the
+    cascade from a sixth of the L2 on, with prefix partitions of about a sixteenth of the prefix
+    (16 .. 128 blocks: 32 measured best at 8K, 64 at 16K, 128 at 32K)."""
+    if prefix_tokens * num_kv_heads * head_dim * 2 * 2 * 6 < l2_bytes:
+        return 0
+    blocks = prefix_tokens // 16
+    pb = 16
+    while pb < 128 and pb * 16 < blocks:
+        pb *= 2
+    return pb
 
 
 class PrefixDecodeStep:
@@ -360,10 +363,12 @@ class PrefixDecodeStep:
     sharing): slot mapping and append of the new token, then ``pkv_decode_attn_prefix`` -- each
     group's shared blocks attended once per KV head for all its members in partitions of
     ``prefix_partition_blocks`` (0: ``partition_blocks``), each sequence's own blocks in partitions
-    of ``partition_blocks``, merged by log-sum-exp.  Every partition leaves fp32 partials for 32
-    query rows, so small prefix partitions cost more in partial traffic and merging than they
-    gain in parallelism (measured on the 1000-token shared prompt: 1-block prefix partitions
-    126 us per step, 16-block 42 us).
+    of ``partition_blocks``, merged by log-sum-exp.  Every prefix partition leaves fp32 partials
+    for a chunk of 32 query rows (128 when a group's rows outnumber 32 and the tcgen05 column
+    kernel runs the prefix pass), so small prefix partitions cost more in partial traffic and
+    merging than they gain in parallelism (measured on the 1000-token shared prompt with 32-row
+    chunks: 1-block prefix partitions 126 us per step, 16-block 42 us).  ``plan_prefix_decode``
+    says when the cascade beats the plain step and picks ``prefix_partition_blocks``.
 
     group_starts int32 [G+1] and prefix_blocks int32 [G] on the device; max_group_size and
     max_prefix_blocks are host-side bounds on them.
@@ -371,12 +376,20 @@ class PrefixDecodeStep:
 
     def __init__(self, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
                  group_starts, prefix_blocks, max_group_size: int, max_prefix_blocks: int,
-                 partition_blocks: int = 16, prefix_partition_blocks: int = 0, err_flag=None):
+                 partition_blocks: int | None = None, prefix_partition_blocks: int = 0, err_flag=None):
         self.q, self.k_new, self.v_new = q, k_new, v_new
         self.k_cache, self.v_cache = k_cache, v_cache
         self.block_tables, self.context_lens = block_tables, context_lens
         self.group_starts, self.prefix_blocks = group_starts, prefix_blocks
         self.max_group_size, self.max_prefix_blocks = int(max_group_size), int(max_prefix_blocks)
+        if partition_blocks is None:
+            # The suffix pass's grid covers the table's width (the library cannot bound a suffix by
+            # the prefix it follows), so its partitions grow with the table: at most 8 per sequence,
+            # at least 16 blocks (a 32K-token shared prompt: 256-block partitions, 1,280 suffix CTAs
+            # instead of 20,320 mostly empty ones at 16 blocks).
+            partition_blocks = 16
+            while partition_blocks * 8 < block_tables.shape[1]:
+                partition_blocks *= 2
         self.partition_blocks = int(partition_blocks)
         self.prefix_partition_blocks = int(prefix_partition_blocks)
         self.scale = float(scale)

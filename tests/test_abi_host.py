@@ -255,12 +255,15 @@ def test_test_build_exports_the_hook(tmp_path):
 
 
 def test_prefix_planner_crossover():
-    """The cascade is planned once the shared prompt's K/V reaches three quarters of the L2 (GB300:
-    129 MB; the measured crossover of the 20-sequence, 8-KV-head batch lies between 16K and 32K
-    tokens)."""
+    """The cascade is planned once the shared prompt's K/V reaches a sixth of the L2 (GB300: 129 MB;
+    the measured crossover of the 20-sequence, 8-KV-head batch lies between 4K and 8K tokens), with
+    prefix partitions of about a sixteenth of the prefix."""
     from paged_kv_decode_slot_gb300.step import plan_prefix_decode
     l2 = 129 * 1024 * 1024
-    assert not plan_prefix_decode(1000, 8, 128, l2)
-    assert not plan_prefix_decode(16008, 8, 128, l2)
-    assert plan_prefix_decode(2000 * 16, 8, 128, l2)
-    assert not plan_prefix_decode(2000 * 16, 1, 128, l2)
+    assert plan_prefix_decode(1000, 8, 128, l2) == 0
+    assert plan_prefix_decode(4000, 8, 128, l2) == 0
+    assert plan_prefix_decode(8000, 8, 128, l2) == 32
+    assert plan_prefix_decode(16000, 8, 128, l2) == 64
+    assert plan_prefix_decode(32000, 8, 128, l2) == 128
+    assert plan_prefix_decode(100000, 8, 128, l2) == 128
+    assert plan_prefix_decode(8000, 1, 128, l2) == 0
