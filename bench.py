@@ -301,7 +301,7 @@ def kernel_label(args, plan, step) -> str:
             return name + " (partitions merged in the same launch)"
         return name + " + lse_merge_kernel"
     if args.attn == "prefix":
-        if step.launches_per_step() == 5:
+        if step.launches_per_step() - (0 if step.fused else 2) == 3:
             return "attn_cols_tc_kernel<128> (prefix pass) + attn_cols_kernel<128> (suffix pass) + cascade_merge_kernel"
         return "attn_cols_kernel<128> (prefix + suffix passes) + cascade_merge_kernel"
     fp8 = "1" if args.kv == "fp8" else "0"
@@ -372,16 +372,15 @@ def run_ours(args):
     if args.mode and args.partition_blocks is None:
         plan = plan_attention(w.B, w.K, w.max_blocks, sms, mode=args.mode)
     groups = w.prefix_groups()
-    if args.attn == "auto" and groups is not None and args.kv == "bf16" and args.tokens == 1 and not args.unfused:
+    if args.attn == "auto" and groups is not None and args.kv == "bf16" and args.tokens == 1 and args.layers == 1:
         # sequences that share a prompt: the planner's choice between the plain step and the cascade
         from paged_kv_decode_slot_gb300.step import plan_prefix_decode
-        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-        ppb = plan_prefix_decode(int(groups[1].max()) * 16, w.K, w.H, l2)
+        ppb = plan_prefix_decode(int(groups[1].max()) * 16, int(np.max(np.diff(groups[0]))) * (w.N // w.K))
         if ppb:
             args.attn = "prefix"
             args.prefix_partition_blocks = args.prefix_partition_blocks or ppb
     if args.tokens > 1:
-        if args.kv != "bf16" or args.attn != "auto":
+        if args.kv != "bf16" or args.attn == "prefix":
             raise SystemExit("--tokens > 1 runs the bf16 cache without --attn prefix")
         T = args.tokens
         qm = d16(gen.normal_bf16(w.seed, 900, (w.B, T, w.N, w.H)))
@@ -398,7 +397,8 @@ def run_ours(args):
         step = PrefixDecodeStep(q, kn, vn, kc, vc, bt, cl, w.scale, d32(gs), d32(pb),
                                 int(np.max(np.diff(gs))), int(pb.max()),
                                 partition_blocks=args.partition_blocks,
-                                prefix_partition_blocks=args.prefix_partition_blocks, err_flag=err)
+                                prefix_partition_blocks=args.prefix_partition_blocks, err_flag=err,
+                                fused=not args.unfused)
         plan = step.plan
     elif args.kv == "fp8":
         if args.unfused:
@@ -424,7 +424,7 @@ def run_ours(args):
     if args.layers > 1:
         # a multi-layer step: every layer its own copy of the pools and of q / k_new / v_new,
         # the same block tables and context lengths (the same sequences)
-        if args.tokens > 1 or args.attn != "auto" or args.unfused:
+        if args.tokens > 1 or args.attn == "prefix" or args.unfused:
             raise SystemExit("--layers runs the fused one-token step (bf16 or e4m3)")
         from paged_kv_decode_slot_gb300.step import LayerStack
         layers = [step]
@@ -649,8 +649,9 @@ def parse_args(argv=None):
                     help="with --kv fp8: one scale per KV head, or one per (physical block, KV head)")
     ap.add_argument("--tokens", type=int, default=1,
                     help="new tokens per sequence (> 1: speculative verification of that many)")
-    ap.add_argument("--attn", choices=("auto", "prefix"), default="auto",
-                    help="prefix: shared-prefix decode on a workload whose sequences share blocks")
+    ap.add_argument("--attn", choices=("auto", "prefix", "plain"), default="auto",
+                    help="prefix: shared-prefix decode on a workload whose sequences share blocks; "
+                         "plain: the plain step there (auto: the planner's choice)")
     ap.add_argument("--prefix-partition-blocks", type=int, default=0,
                     help="with --attn prefix: blocks per partition of the shared-prefix pass")
     ap.add_argument("--unfused", action="store_true",

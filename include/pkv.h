@@ -425,9 +425,12 @@ size_t pkv_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t
    blocks that every member's table shares with the group's first member (full blocks: a partly
    filled prefix block is copied on write and belongs to each member).  Sequences outside every
    group have no shared prefix.  The shared blocks are attended once per KV head for all the
-   group's queries (up to 32 query rows per loaded tile) in partitions of prefix_partition_blocks
-   (0: partition_blocks), each sequence's own blocks separately in partitions of
-   partition_blocks, and the partials are merged by their log-sum-exp.
+   group's queries (32 query rows per loaded tile; 128 on the tensor cores when a group holds more
+   than 32 rows) in partitions of prefix_partition_blocks (0: partition_blocks), each sequence's
+   own blocks separately in partitions of partition_blocks, and the partials are merged by their
+   log-sum-exp.  With the tensor-core prefix pass the two passes are two launches that may run
+   at the same time on the GPU (the second is launched with programmatic stream serialization);
+   the merge after them is ordered behind both, so the call is ordered on the stream as usual.
    Host-side bounds: every group has at most max_group_size members and at most
    max_prefix_blocks (<= max_blocks_per_seq) shared blocks; a group beyond them, or a member
    shorter than its prefix, sets PKV_FLAG_GROUP_RANGE (that member's result is then void).  The
@@ -442,6 +445,28 @@ int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
                            pkv_bf16 *out, float *lse_out, pkv_cache_desc cache,
                            int32_t partition_blocks, int32_t prefix_partition_blocks, void *workspace,
                            size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream);
+
+/* A whole shared-prefix decode step: pkv_slot_mapping + pkv_append + pkv_decode_attn_prefix, with
+   the append done by the attention launch itself (copy-on-write sharing, "Optimización de la
+   inferencia", "Página Atención"; the fused block-read + attention kernel of CS336 Lecture 10
+   notes).  Each sequence's new K/V row (k_new / v_new [num_seqs][K][H], 16-byte aligned) is
+   written into the slot of its position ctx - 1 by the suffix-pass CTA that loads that block,
+   before it loads it; slot_mapping_out [num_seqs] (nullable, 8-byte aligned) receives the slots
+   (-1 for ctx 0 or an out-of-range block id, as pkv_slot_mapping).  The new token must lie in the
+   sequence's own blocks: a member whose context ends inside its group's shared blocks
+   (ctx = 16 * prefix_blocks[g]) would write into a block every member reads, so its row is not
+   written (slot -1) and PKV_FLAG_GROUP_RANGE is set.  Otherwise arguments and results as
+   pkv_decode_attn_prefix, bit for bit equal to the three separate calls (outputs, lse, slots,
+   pools, flags). */
+int pkv_decode_step_prefix(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                           pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, float scale, const int32_t *group_starts,
+                           const int32_t *prefix_blocks, int32_t num_groups, int32_t max_group_size,
+                           int32_t max_prefix_blocks, pkv_bf16 *out, float *lse_out,
+                           int64_t *slot_mapping_out, pkv_cache_desc cache, int32_t partition_blocks,
+                           int32_t prefix_partition_blocks, void *workspace, size_t workspace_bytes,
+                           int32_t *err_flag, pkv_stream_t stream);
 
 /* Synchronise the stream, copy *err_flag to *host_value; PKV_ERR_RANGE if it is non-zero. */
 int pkv_read_err_flag(const int32_t *err_flag, int32_t *host_value, pkv_stream_t stream);

@@ -580,6 +580,46 @@ def pkv_decode_attn_prefix(q, k_cache, v_cache, block_tables, context_lens, scal
                                        _ptr(err_flag), _stream(stream))
 
 
+_lib.pkv_decode_step_prefix.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, ctypes.c_float, _P, _P,
+                                        _I32, _I32, _I32, _P, _P, _P, CacheDesc, _I32, _I32, _P,
+                                        ctypes.c_size_t, _P, _P]
+
+
+def pkv_decode_step_prefix(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale: float,
+                           group_starts, prefix_blocks, max_group_size: int, max_prefix_blocks: int, out,
+                           lse_out=None, slot_mapping=None, partition_blocks: int = 16, workspace=None,
+                           err_flag=None, stream=None, prefix_partition_blocks: int = 0) -> int:
+    """Slot mapping + append + shared-prefix decode attention, the append done by the attention
+    launch: k_new, v_new bf16 [B, K, H]; slot_mapping int64 [B] (written)."""
+    _need(q, torch.bfloat16, 3, "q")
+    _need(k_new, torch.bfloat16, 3, "k_new")
+    _need(v_new, torch.bfloat16, 3, "v_new")
+    _need(k_cache, torch.bfloat16, 4, "k_cache")
+    _need(v_cache, torch.bfloat16, 4, "v_cache")
+    _need(block_tables, torch.int32, 2, "block_tables")
+    _need(context_lens, torch.int32, 1, "context_lens")
+    _need(group_starts, torch.int32, 1, "group_starts")
+    _need(prefix_blocks, torch.int32, 1, "prefix_blocks")
+    _need(out, torch.bfloat16, 3, "out")
+    _opt(lse_out, torch.float32, 2, "lse_out")
+    _opt(slot_mapping, torch.int64, 1, "slot_mapping")
+    _opt(workspace, torch.uint8, 1, "workspace")
+    _opt(err_flag, torch.int32, 1, "err_flag")
+    if group_starts.numel() != prefix_blocks.numel() + 1:
+        raise ValueError("group_starts needs one more entry than prefix_blocks")
+    B, N, _ = q.shape
+    if tuple(k_new.shape) != (B, k_cache.shape[2], k_cache.shape[3]) or k_new.shape != v_new.shape:
+        raise ValueError("k_new / v_new must be [B, K, H]")
+    return _lib.pkv_decode_step_prefix(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, N,
+                                       float(scale), _ptr(group_starts), _ptr(prefix_blocks),
+                                       prefix_blocks.numel(), max_group_size, max_prefix_blocks, _ptr(out),
+                                       _ptr(lse_out), _ptr(slot_mapping), cache_desc(k_cache), partition_blocks,
+                                       prefix_partition_blocks, _ptr(workspace),
+                                       0 if workspace is None else workspace.numel(), _ptr(err_flag),
+                                       _stream(stream))
+
+
 def pkv_gather(k_cache, v_cache, block_tables, context_lens, cu_seqlens, k_out, v_out, err_flag=None,
                stream=None) -> int:
     _need(k_cache, torch.bfloat16, 4, "k_cache")

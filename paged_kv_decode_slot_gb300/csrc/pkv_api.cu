@@ -1058,22 +1058,25 @@ PKV_EXPORT size_t pkv_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_hea
     return pkv_splitk_workspace_bytes(num_seqs, num_q_heads, head_dim, parts);
 }
 
-PKV_EXPORT int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
-                                      const int32_t *block_tables, int32_t max_blocks_per_seq,
-                                      const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
-                                      float scale, const int32_t *group_starts,
-                                      const int32_t *prefix_blocks, int32_t num_groups,
-                                      int32_t max_group_size, int32_t max_prefix_blocks, pkv_bf16 *out,
-                                      float *lse_out, pkv_cache_desc cache, int32_t partition_blocks,
-                                      int32_t prefix_partition_blocks, void *workspace,
-                                      size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream)
+namespace {
+
+// pkv_decode_attn_prefix, and with k_new != nullptr the fused step pkv_decode_step_prefix (the
+// suffix pass's producers write each sequence's new row into its slot before loading its block).
+int prefix_attention(const AttnArgs &a, const int32_t *group_starts, const int32_t *prefix_blocks,
+                     int32_t num_groups, int32_t max_group_size, int32_t max_prefix_blocks,
+                     const pkv_bf16 *k_new, const pkv_bf16 *v_new, pkv_bf16 *k_cache_w, pkv_bf16 *v_cache_w,
+                     int64_t *slot_out, pkv_bf16 *out, float *lse_out, int32_t partition_blocks,
+                     int32_t prefix_partition_blocks, void *workspace, size_t workspace_bytes,
+                     cudaStream_t stream)
 {
+    const pkv_cache_desc &cache = a.d;
+    const int32_t num_seqs = a.B, num_q_heads = a.N, max_blocks_per_seq = a.max_nb;
+    const pkv_bf16 *k_cache = a.k_cache, *v_cache = a.v_cache;
     if (prefix_partition_blocks == 0) prefix_partition_blocks = partition_blocks;
-    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-               num_q_heads, scale, cache, err_flag};
     int st = validate_attn(a);
     if (st != PKV_OK) return st;
     if (!out || !workspace) return PKV_ERR_NULL;
+    if (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_out, 8))) return PKV_ERR_ALIGN;
     if (num_groups < 0 || partition_blocks <= 0 || prefix_partition_blocks <= 0 || max_prefix_blocks < 0 ||
         max_prefix_blocks > max_blocks_per_seq)
         return PKV_ERR_SHAPE;
@@ -1114,6 +1117,11 @@ PKV_EXPORT int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache
     p.max_group = max_group_size;
     p.prefix_parts = prefix_parts;
     p.prefix_ctas = (int32_t)prefix_ctas;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache_w = k_cache_w;
+    p.v_cache_w = v_cache_w;
+    p.slot_out = slot_out;
     // With more than 16 rows per chunk (the group's members x G) the prefix pass runs on the
     // tcgen05 column kernel, whose time per 64-token group is set by its MMA count, not its rows;
     // the suffix pass (G rows) stays on mma.sync, in a second launch over the rest of the work.
@@ -1135,14 +1143,57 @@ PKV_EXPORT int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache
         if (e != cudaSuccess) return cuda_fail(e, "shared-prefix pass launch");
         // the suffix pass alone: with no prefix CTAs in its grid, its CTAs number the suffix work
         // from 0 (the partial slots and the merge do not depend on the prefix CTA count)
+        // It shares no data with the prefix pass (only the merge reads both), so it is launched
+        // with programmatic serialization: its CTAs start on the SMs the prefix pass leaves free
+        // once every prefix CTA is running, and its last CTA waits for the prefix grid before it
+        // exits, so the merge after it sees both passes.
         pkv::ColsParams ps = p;
         ps.prefix_ctas = 0;
         ps.chunk_rows = kColsPerCta;
-        e = pkv::launch_attn_cols(cache.head_dim, tk, tv, ps, grid - prefix_ctas, stream);
+        ps.pdl_wait = 1;
+        e = pkv::launch_attn_cols(cache.head_dim, tk, tv, ps, grid - prefix_ctas, stream, true);
     } else {
         e = pkv::launch_attn_cols(cache.head_dim, tk, tv, p, grid, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "shared-prefix attention launch");
     e = pkv::launch_cascade_merge(p, cache.head_dim, reinterpret_cast<__nv_bfloat16 *>(out), lse_out, stream);
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "shared-prefix merge launch");
+}
+
+}  // namespace
+
+PKV_EXPORT int pkv_decode_attn_prefix(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                      float scale, const int32_t *group_starts,
+                                      const int32_t *prefix_blocks, int32_t num_groups,
+                                      int32_t max_group_size, int32_t max_prefix_blocks, pkv_bf16 *out,
+                                      float *lse_out, pkv_cache_desc cache, int32_t partition_blocks,
+                                      int32_t prefix_partition_blocks, void *workspace,
+                                      size_t workspace_bytes, int32_t *err_flag, pkv_stream_t stream)
+{
+    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+               num_q_heads, scale, cache, err_flag};
+    return prefix_attention(a, group_starts, prefix_blocks, num_groups, max_group_size, max_prefix_blocks,
+                            nullptr, nullptr, nullptr, nullptr, nullptr, out, lse_out, partition_blocks,
+                            prefix_partition_blocks, workspace, workspace_bytes, stream);
+}
+
+PKV_EXPORT int pkv_decode_step_prefix(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                                      pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                      int32_t num_seqs, int32_t num_q_heads, float scale,
+                                      const int32_t *group_starts, const int32_t *prefix_blocks,
+                                      int32_t num_groups, int32_t max_group_size, int32_t max_prefix_blocks,
+                                      pkv_bf16 *out, float *lse_out, int64_t *slot_mapping_out,
+                                      pkv_cache_desc cache, int32_t partition_blocks,
+                                      int32_t prefix_partition_blocks, void *workspace, size_t workspace_bytes,
+                                      int32_t *err_flag, pkv_stream_t stream)
+{
+    if (!k_new || !v_new) return PKV_ERR_NULL;
+    AttnArgs a{q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+               num_q_heads, scale, cache, err_flag};
+    return prefix_attention(a, group_starts, prefix_blocks, num_groups, max_group_size, max_prefix_blocks,
+                            k_new, v_new, k_cache, v_cache, slot_mapping_out, out, lse_out, partition_blocks,
+                            prefix_partition_blocks, workspace, workspace_bytes, stream);
 }

@@ -114,9 +114,8 @@ __device__ __forceinline__ void tile_update_cols(WarpAcc<H> &a, const uint32_t (
 }
 
 template <int H>
-__global__ void __launch_bounds__(kAttnThreads, PKV_CTAS_PER_SM)
-attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 const ColsParams p)
+__device__ __forceinline__ void attn_cols_body(const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                               const ColsParams &p)
 {
     constexpr int S = kStages;
     using L = AttnLayout<H, S>;
@@ -285,9 +284,27 @@ attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (merge_here) cols_merge_chunk<H>(p, wk, nparts, reinterpret_cast<float *>(base), kAttnThreads);
 }
 
+template <int H>
+__global__ void __launch_bounds__(kAttnThreads, PKV_CTAS_PER_SM)
+attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                 const ColsParams p)
+{
+    attn_cols_body<H>(tm_k, tm_v, p);
+    // the suffix pass launched behind the tcgen05 prefix pass: its last CTA (scheduled last, so its
+    // wait holds no slot another CTA of this grid needs) waits for that grid, so this one completes
+    // only after it and the merge launched next reads both passes' partials
+    if (p.pdl_wait && blockIdx.x == gridDim.x - 1) pdl_wait_primary();
+}
+
 // Merge of the prefix pass and the suffix pass of one (sequence, query head): slots
 // [0, ceil(pnb / prefix PB)) hold the shared prefix, the next ceil((nb - pnb) / PB) the
 // sequence's own blocks; one warp computes the log-sum-exp weights, every thread one element.
+// Which slots hold data takes dependent reads (the length, the group, its prefix), so the row's
+// partial lse of every slot and each thread's partial values of the first kCascadePrefetch slots
+// are loaded before them, independently (the workspace holds max_parts slots a row; slots that
+// hold no data are read but never used).
+constexpr int kCascadePrefetch = 8;
+
 __global__ void cascade_merge_kernel(const ColsParams p, __nv_bfloat16 *__restrict__ out,
                                      float *__restrict__ lse_out)
 {
@@ -296,6 +313,11 @@ __global__ void cascade_merge_kernel(const ColsParams p, __nv_bfloat16 *__restri
     const int n = blockIdx.x, b = blockIdx.y, h = threadIdx.x;
     const int H = blockDim.x;
     const int64_t row = (int64_t)b * p.N + n;
+    const float *po = p.part_out + row * p.max_parts * H + h;
+    float v[kCascadePrefetch];
+#pragma unroll
+    for (int q = 0; q < kCascadePrefetch; ++q) v[q] = q < p.max_parts ? __ldcg(po + (size_t)q * H) : 0.f;
+    for (int q = h; q < p.max_parts; q += H) wts[q] = __ldcg(p.part_lse + row * p.max_parts + q);
     const int ctx = p.context_lens[b];
     const int g = group_of(p, b);
     const int pnb = g >= 0 ? prefix_blocks_of(p, g) : 0;
@@ -304,15 +326,19 @@ __global__ void cascade_merge_kernel(const ColsParams p, __nv_bfloat16 *__restri
     const int np = ok ? (pnb + p.prefix_part_blocks - 1) / p.prefix_part_blocks +
                             (nb - pnb + p.part_blocks - 1) / p.part_blocks
                       : 0;
-    // the row's partial lse first (one round trip), then its weights from that copy, in place
-    for (int q = h; q < np; q += H) wts[q] = __ldcg(p.part_lse + row * p.max_parts + q);
     __syncthreads();
     if (h < 32) {
         const float L = lse_merge_weights<true>(wts, np, wts, h);
         if (h == 0) row_lse = L;
     }
     __syncthreads();
-    out[row * H + h] = __float2bfloat16_rn(lse_merge_value(wts, p.part_out + row * p.max_parts * H + h, np, H));
+    // sum_q w_q o_q in slot order (lse_merge_value's arithmetic), the first slots from registers
+    float val = 0.f;
+#pragma unroll
+    for (int q = 0; q < kCascadePrefetch; ++q)
+        if (q < np) val += wts[q] * v[q];
+    for (int q = kCascadePrefetch; q < np; ++q) val += wts[q] * __ldcg(po + (size_t)q * H);
+    out[row * H + h] = __float2bfloat16_rn(val);
     if (h == 0 && lse_out) lse_out[row] = row_lse;
 }
 
@@ -330,22 +356,36 @@ static cudaError_t ensure_cols_smem(Kern kern, int smem, int *cached)
 
 template <int H>
 static cudaError_t launch_cols_t(const CUtensorMap &tk, const CUtensorMap &tv, const ColsParams &p,
-                                 int64_t grid, cudaStream_t stream)
+                                 int64_t grid, cudaStream_t stream, bool pdl)
 {
     constexpr int smem = AttnLayout<H>::kAlloc;
     static int cached[64] = {};
     cudaError_t e = ensure_cols_smem(attn_cols_kernel<H>, smem, cached);
     if (e != cudaSuccess) return e;
-    attn_cols_kernel<H><<<(unsigned)grid, kAttnThreads, smem, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    if (!pdl) {
+        attn_cols_kernel<H><<<(unsigned)grid, kAttnThreads, smem, stream>>>(tk, tv, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_cols_kernel<H>, tk, tv, p);
 }
 
 cudaError_t launch_attn_cols(int H, const CUtensorMap &tk, const CUtensorMap &tv, const ColsParams &p,
-                             int64_t grid, cudaStream_t stream)
+                             int64_t grid, cudaStream_t stream, bool pdl)
 {
     if (grid <= 0) return cudaSuccess;
-    if (H == 64) return launch_cols_t<64>(tk, tv, p, grid, stream);
-    if (H == 128) return launch_cols_t<128>(tk, tv, p, grid, stream);
+    if (pdl && !p.pdl_wait) return cudaErrorInvalidValue;
+    if (H == 64) return launch_cols_t<64>(tk, tv, p, grid, stream, pdl);
+    if (H == 128) return launch_cols_t<128>(tk, tv, p, grid, stream, pdl);
     return cudaErrorInvalidValue;
 }
 

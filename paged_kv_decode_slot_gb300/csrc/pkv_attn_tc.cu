@@ -136,6 +136,9 @@ attn_cols_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_u32 - raw_u32);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // a suffix pass launched behind this grid (programmatic serialization) may start as soon as
+    // every CTA of this one is running: the two passes share no data until the merge
+    pdl_launch_dependents();
 
     ColsWork wk;
     if (!cols_work<R::kRows>(p, blockIdx.x, wk)) return;

@@ -19,7 +19,7 @@ struct ColsWork {
     int mode;
     int kvh;
     int b;          // multi / suffix: the sequence; prefix: the group's first member
-    int ctx;        // multi: the sequence's context length
+    int ctx;        // multi / suffix: the sequence's context length
     int vis;        // prefix / suffix: tokens every column sees
     int col_base;   // first column of this CTA's chunk
     int ncols;      // columns of this CTA (1 .. chunk_rows)
@@ -108,24 +108,41 @@ __device__ __forceinline__ bool cols_work(const ColsParams &p, int64_t c, ColsWo
         w.slot = ppart;
         return w.ncols > 0 && w.blk_begin < w.blk_end;
     }
-    // suffix pass: (sequence, suffix partition)
+    // suffix pass: (suffix partition, sequence), partitions slowest and in ascending order: the
+    // grid covers the table's whole width, so the partitions past the shorter suffixes (empty
+    // CTAs that return at once) come after all the work
     c -= p.prefix_ctas / p.K;
-    const int sparts = (p.max_nb + p.part_blocks - 1) / p.part_blocks;
-    const int spart = (int)(c % sparts);
+    const int spart = (int)(c / p.B);
     w.mode = kModeSuffix;
-    w.b = (int)(c / sparts);
+    w.b = (int)(c % p.B);
+    // the sequence's reporter: flags, and in the fused step the slot of a new token nobody writes
+    const bool report = first_thread && w.kvh == 0 && spart == 0;
+    int64_t *const no_slot = p.k_new ? p.slot_out : nullptr;
     int ctx = p.context_lens[w.b];
     if (ctx < 0 || ctx > p.max_nb * kBlockSize) {
-        if (first_thread && w.kvh == 0 && spart == 0) set_flag(p.err_flag, PKV_FLAG_CTX_RANGE);
+        if (report) {
+            set_flag(p.err_flag, PKV_FLAG_CTX_RANGE);
+            if (no_slot) no_slot[w.b] = -1;
+        }
         return false;
     }
     const int g = group_of(p, w.b);
     const int pnb = g >= 0 ? prefix_blocks_of(p, g) : 0;
     if (pnb * kBlockSize > ctx) {
-        if (first_thread && w.kvh == 0 && spart == 0) set_flag(p.err_flag, PKV_FLAG_GROUP_RANGE);
+        if (report) {
+            set_flag(p.err_flag, PKV_FLAG_GROUP_RANGE);
+            if (no_slot) no_slot[w.b] = -1;
+        }
         return false;
     }
+    // fused step: the new token (position ctx - 1) goes into the sequence's own blocks, past the
+    // shared ones (writing it into a shared block would change every member's prefix)
+    if (report && p.k_new && (ctx == 0 || pnb * kBlockSize == ctx)) {
+        if (ctx > 0) set_flag(p.err_flag, PKV_FLAG_GROUP_RANGE);
+        if (no_slot) no_slot[w.b] = -1;
+    }
     const int nb = (ctx + kBlockSize - 1) / kBlockSize;
+    w.ctx = ctx;
     w.vis = ctx;
     w.col_base = 0;
     w.ncols = p.G;
@@ -157,18 +174,19 @@ __device__ __forceinline__ void col_of(const ColsParams &p, const ColsWork &w, i
     }
 }
 
-// Fused multi-token step: right before the producer warp loads tile i (logical block
-// blk_begin + i) of a multi-token unit, it writes the new tokens whose positions fall in that
-// block -- token t of the last T sits at position ctx - T + t -- from k_new / v_new into their
-// slots (this KV head's H elements of each row), fences those writes against the TMA load that
-// follows, and (KV head 0, first chunk) records their slots.  The CTAs of the unit's other chunks
-// write the same bytes.  A block id outside the pool (flagged by the producer) is not written and
-// its slots are -1.  The same rows land where pkv_slot_mapping_multi + pkv_append put them.
+// Fused steps (several new tokens, or the suffix pass of shared-prefix decode with T = 1): right
+// before the producer warp loads tile i (logical block blk_begin + i) of a multi-token or suffix
+// unit, it writes the new tokens whose positions fall in that block -- token t of the last T sits
+// at position ctx - T + t -- from k_new / v_new into their slots (this KV head's H elements of each
+// row), fences those writes against the TMA load that follows, and (KV head 0, first chunk)
+// records their slots.  The CTAs of the unit's other chunks write the same bytes.  A block id
+// outside the pool (flagged by the producer) is not written and its slots are -1.  The same rows
+// land where pkv_slot_mapping(_multi) + pkv_append put them.
 template <int H>
 __device__ __forceinline__ void append_multi_rows(const ColsParams &p, const ColsWork &wk, int64_t i, int bid,
                                                   bool ok, int lane)
 {
-    if (!p.k_new || wk.mode != kModeMulti) return;
+    if (!p.k_new || wk.mode == kModePrefix) return;
     const int j = wk.blk_begin + (int)i;
     const int first = wk.ctx - p.T;
     const int lo = max(max(first, 0), j * kBlockSize), hi = min(wk.ctx, (j + 1) * kBlockSize);

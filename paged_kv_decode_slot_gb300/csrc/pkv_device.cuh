@@ -113,6 +113,21 @@ __device__ __forceinline__ void fence_proxy_async_global()
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Programmatic dependent launch (sm_90 and later).  launch_dependents: the grid launched next on
+// the stream with the programmatic-serialization attribute may start once every CTA of this grid
+// has executed it or exited (a no-op when the next grid is launched plainly).  wait_primary: block
+// until the grid this one was launched behind has completed and its writes are visible (returns at
+// once in a grid launched plainly).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_primary()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2(const void *ptr)
 {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));

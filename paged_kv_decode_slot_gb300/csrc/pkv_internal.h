@@ -104,6 +104,8 @@ struct ColsParams {
     int32_t prefix_part_blocks;    // prefix mode: blocks per prefix-pass partition
     int32_t prefix_parts;          // prefix mode: partitions of the prefix pass (grid)
     int32_t prefix_ctas;           // prefix mode: CTAs of the prefix pass
+    int32_t pdl_wait;              // launched behind the prefix pass with programmatic
+                                   // serialization: the last CTA waits for that grid before it exits
     // multi, fused step: the T new tokens' K/V rows [B][T][K][H] (nullable: no append) are written
     // into their slots by the producer that loads their block, before it loads it
     const uint16_t *k_new;
@@ -118,8 +120,11 @@ struct ColsParams {
 #endif
 };
 
+// pdl: launch with programmatic stream serialization, so that the grid may start while the grid
+// before it on the stream still runs (p.pdl_wait must then be set: the grid's last CTA waits for
+// that grid at its end, so the next plain launch sees both grids' writes).
 cudaError_t launch_attn_cols(int H, const CUtensorMap &tk, const CUtensorMap &tv, const ColsParams &p,
-                             int64_t grid, cudaStream_t stream);
+                             int64_t grid, cudaStream_t stream, bool pdl = false);
 // tcgen05 form of the same column kernel (H = 128, half-major tensor maps only; the K map's box
 // is one 64-element half of a tile, the V map's the whole tile).
 bool cols_tc_supported(int H, int tok_major);

@@ -336,31 +336,36 @@ class MultiTokenStep:
         return [getattr(self, n) for n in self.input_names()]
 
 
-def plan_prefix_decode(prefix_tokens: int, num_kv_heads: int, head_dim: int, l2_bytes: int) -> int:
+def plan_prefix_decode(prefix_tokens: int, group_rows: int) -> int:
     """The shared-prefix cascade's prefix-pass partition size (blocks) when it is the better plan for
-    a batch whose sequences share ``prefix_tokens`` leading tokens, else 0 (the plain decode step).
+    a batch whose groups share ``prefix_tokens`` leading tokens and hold ``group_rows`` query rows
+    (members x query heads per KV head), else 0 (the plain decode step).
 
-    Measured on GB300 (20 sequences, 64 query / 8 KV heads, head_dim 128, suffixes of 16..512 tokens;
-    µs per step from a CUDA graph, plain / cascade with its best prefix partitions): 1,000 shared
-    tokens 30.0 / 44.5, 4,008 46.6 / 53.5, 8,008 73.2 / 61.8, 16,008 116.9 / 78.1, 32,008
-    209.1 / 110.6.  The plain step reads the prefix once per sequence, its CTAs at nearly the same
-    time, so the re-reads mostly hit L2; the cascade reads it once per KV head and 128-row chunk of
-    the group's queries (the tcgen05 column kernel) and pays a second launch and a merge.  The
-    crossover lies between 4K and 8K shared tokens (16 and 33 MB of K/V against a 129 MB L2): the
-    cascade from a sixth of the L2 on, with prefix partitions of about a sixteenth of the prefix
-    (16 .. 128 blocks: 32 measured best at 8K, 64 at 16K, 128 at 32K)."""
-    if prefix_tokens * num_kv_heads * head_dim * 2 * 2 * 6 < l2_bytes:
+    Measured on GB300 (20 sequences, 64 query / 8 KV heads, head_dim 128, suffixes of 16..512 tokens:
+    160 rows a group; fused steps, µs per step in a CUDA graph, plain / cascade with its best prefix
+    partitions): 1,000 shared tokens 29.0 / 30.0 (16 blocks), 2,008 33.5 / 32.7 (16), 4,008
+    45.5 / 36.7 (32), 8,008 73.2 / 49.1 (32), 16,008 116.9 / 62.4 (64), 32,008 209.0 / 88.8 (128).
+    The plain step reads the prefix once per sequence, mostly from L2, but each of its CTAs streams
+    the whole prefix; the cascade spreads the prefix over partitions read once per KV head and
+    128-row chunk (the tcgen05 column kernel, from 17 rows a group) and pays two more launches.  So
+    the cascade from 3,000 shared tokens on, with partitions of 16 blocks up to 160 shared blocks,
+    32 up to 600, 64 up to 1,200, then 128 (about 8 to 16 partitions).  Groups of 16 rows or fewer
+    run the cascade on mma.sync, which does not save tile updates (1,000 tokens, 8-row chunks:
+    41 vs 30 us): plain."""
+    if group_rows <= 16 or prefix_tokens < 3000:
         return 0
     blocks = prefix_tokens // 16
-    pb = 16
-    while pb < 128 and pb * 16 < blocks:
-        pb *= 2
-    return pb
+    for limit, pb in ((160, 16), (600, 32), (1200, 64)):
+        if blocks <= limit:
+            return pb
+    return 128
 
 
 class PrefixDecodeStep:
     """A decode step of a batch whose sequences share leading blocks (copy-on-write prefix
-    sharing): slot mapping and append of the new token, then ``pkv_decode_attn_prefix`` -- each
+    sharing): by default ``pkv_decode_step_prefix``, whose suffix pass appends each sequence's new
+    token as it loads its block (``fused=False``: slot mapping and append of the new token, then
+    ``pkv_decode_attn_prefix``, bit for bit the same results) -- each
     group's shared blocks attended once per KV head for all its members in partitions of
     ``prefix_partition_blocks`` (0: ``partition_blocks``), each sequence's own blocks in partitions
     of ``partition_blocks``, merged by log-sum-exp.  Every prefix partition leaves fp32 partials
@@ -376,7 +381,8 @@ class PrefixDecodeStep:
 
     def __init__(self, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale,
                  group_starts, prefix_blocks, max_group_size: int, max_prefix_blocks: int,
-                 partition_blocks: int | None = None, prefix_partition_blocks: int = 0, err_flag=None):
+                 partition_blocks: int | None = None, prefix_partition_blocks: int = 0, err_flag=None,
+                 fused: bool = True):
         self.q, self.k_new, self.v_new = q, k_new, v_new
         self.k_cache, self.v_cache = k_cache, v_cache
         self.block_tables, self.context_lens = block_tables, context_lens
@@ -397,7 +403,7 @@ class PrefixDecodeStep:
         nseq, N, H = q.shape
         self.num_blocks = k_cache.shape[0]
         self.plan = AttentionPlan("prefix", self.partition_blocks, 0)
-        self.fused = False
+        self.fused = fused
         self.slot_mapping = torch.empty(nseq, dtype=torch.int64, device=dev)
         self.out = torch.empty(tuple(q.shape), dtype=q.dtype, device=dev)
         self.lse = torch.empty(nseq, N, dtype=torch.float32, device=dev)
@@ -421,15 +427,24 @@ class PrefixDecodeStep:
                                          prefix_partition_blocks=self.prefix_partition_blocks))
 
     def run(self, stream=None) -> None:
+        if self.fused:
+            B.check(B.pkv_decode_step_prefix(self.q, self.k_new, self.v_new, self.k_cache, self.v_cache,
+                                             self.block_tables, self.context_lens, self.scale,
+                                             self.group_starts, self.prefix_blocks, self.max_group_size,
+                                             self.max_prefix_blocks, self.out, self.lse, self.slot_mapping,
+                                             self.partition_blocks, self.workspace, self.err_flag, stream,
+                                             prefix_partition_blocks=self.prefix_partition_blocks))
+            return
         self.slot_and_append(stream)
         self.attention(stream)
 
     def launches_per_step(self) -> int:
-        # slot mapping, append, the prefix and suffix passes (one launch, or the tcgen05 prefix pass
-        # and the mma.sync suffix pass), the merge
+        # the prefix and suffix passes (one launch, or the tcgen05 prefix pass and the mma.sync
+        # suffix pass), the merge; unfused, slot mapping and append before them
         _, N, H = self.q.shape
         tc = B.pkv_multi_uses_tcgen05(self.max_group_size, N, self.k_cache.shape[2], H)
-        return 5 if tc else 4
+        attn = 3 if tc else 2
+        return attn if self.fused else 2 + attn
 
     def input_names(self):
         return ("q", "k_new", "v_new", "block_tables", "context_lens", "group_starts", "prefix_blocks")

@@ -200,6 +200,31 @@ def test_decode_step_host_validation(lib):
     assert f(*args(B=0)) == 0
 
 
+def test_decode_step_prefix_host_validation(lib):
+    """pkv_decode_step_prefix: the fused step's own arguments are checked on the host (no GPU)."""
+    cdll, _ = lib
+    f = cdll.pkv_decode_step_prefix
+    I = ctypes.c_int32
+    f.argtypes = [P, P, P, P, P, P, I, P, I, I, ctypes.c_float, P, P, I, I, I, P, P, P, Desc, I, I, P,
+                  ctypes.c_size_t, P, P]
+    cdll.pkv_prefix_workspace_bytes.restype = ctypes.c_size_t
+    cdll.pkv_prefix_workspace_bytes.argtypes = [I] * 7
+    wsb = cdll.pkv_prefix_workspace_bytes(4, 8, 64, 4, 2, 2, 0)
+    assert wsb > 0
+    args = lambda kn=FAKE, vn=FAKE, slot=None, B=4, groups=1, ws=FAKE, nbytes=wsb: (
+        FAKE, kn, vn, FAKE, FAKE, FAKE, 4, FAKE, B, 8, 0.125, FAKE, FAKE, groups, 4, 2, FAKE, None, slot,
+        Desc(64, 16, 2, 64), 2, 0, ws, nbytes, None, None)
+    assert f(*args(kn=None)) == -1
+    assert f(*args(vn=None)) == -1
+    assert f(*args(kn=FAKE + 8)) == -6                  # new rows move as 16-byte vectors
+    assert f(*args(slot=FAKE + 4)) == -6
+    assert f(*args(ws=None)) == -1
+    assert f(*args(nbytes=wsb - 1)) == -7
+    assert f(*args(groups=-1)) == -2
+    assert f(*args(B=0)) == -2                          # a group of 4 in a batch of none
+    assert f(*args(B=0, groups=0)) == 0
+
+
 def test_multi_kernel_choice():
     """pkv_decode_attn_multi runs the tcgen05 column kernel from 17 query rows per CTA at H = 128
     (rows = min(T * G, 32)), the mma.sync one below that and at H = 64; no GPU work."""
@@ -255,15 +280,16 @@ def test_test_build_exports_the_hook(tmp_path):
 
 
 def test_prefix_planner_crossover():
-    """The cascade is planned once the shared prompt's K/V reaches a sixth of the L2 (GB300: 129 MB;
-    the measured crossover of the 20-sequence, 8-KV-head batch lies between 4K and 8K tokens), with
-    prefix partitions of about a sixteenth of the prefix."""
+    """The cascade is planned from 3,000 shared tokens for groups of more than 16 query rows (the
+    measured crossover of the 20-sequence, 160-row batch lies between 2K and 4K tokens), with
+    prefix partitions growing with the prefix (16 to 128 blocks)."""
     from paged_kv_decode_slot_gb300.step import plan_prefix_decode
-    l2 = 129 * 1024 * 1024
-    assert plan_prefix_decode(1000, 8, 128, l2) == 0
-    assert plan_prefix_decode(4000, 8, 128, l2) == 0
-    assert plan_prefix_decode(8000, 8, 128, l2) == 32
-    assert plan_prefix_decode(16000, 8, 128, l2) == 64
-    assert plan_prefix_decode(32000, 8, 128, l2) == 128
-    assert plan_prefix_decode(100000, 8, 128, l2) == 128
-    assert plan_prefix_decode(8000, 1, 128, l2) == 0
+    assert plan_prefix_decode(1000, 160) == 0
+    assert plan_prefix_decode(2000, 160) == 0
+    assert plan_prefix_decode(4000, 160) == 32
+    assert plan_prefix_decode(8000, 160) == 32
+    assert plan_prefix_decode(16000, 160) == 64
+    assert plan_prefix_decode(32000, 160) == 128
+    assert plan_prefix_decode(100000, 160) == 128
+    assert plan_prefix_decode(3000, 24) == 32          # 187 shared blocks
+    assert plan_prefix_decode(32000, 16) == 0

@@ -530,3 +530,104 @@ def test_prefix_long_cascade_matches_oracle(pkv, oracle, prefix_part_blocks):
     ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
     assert_close(out_f64(out), ref, f"long prefix, {prefix_part_blocks}-block prefix partitions")
     assert_lse_close(lse.cpu().numpy().astype(np.float64), ref_lse, "long prefix")
+
+
+# ------------------------------- fused shared-prefix step -------------------------------------
+FUSED_PREFIX_CASES = [
+    # name, N, K, H, context lengths, groups (start, end, shared blocks).  Rows of a group = members
+    # x G: up to 16 on mma.sync (both passes in one launch), 17..32 on the 32-row tcgen05 prefix pass,
+    # more on the 128-row one (the suffix pass then a second launch, overlapping the first)
+    ("mma_two_groups_empty_single", 16, 2, 128, [100, 120, 0, 300, 260, 33, 35], [(0, 2, 6), (3, 5, 16)]),
+    ("tc32_g8", 64, 8, 128, [150, 170, 190, 210, 77], [(0, 4, 9)]),
+    ("tc128_g8_edges", 64, 8, 128, [130 + 7 * i for i in range(11)] + [129], [(0, 12, 8)]),
+    ("tc128_long_suffix", 64, 8, 128, [700 + 90 * i for i in range(20)], [(0, 20, 40)]),
+]
+
+
+@pytest.mark.parametrize("part_blocks,prefix_part_blocks", [(16, 0), (4, 3)])
+@pytest.mark.parametrize("name,N,K,H,ctx,groups", FUSED_PREFIX_CASES, ids=[c[0] for c in FUSED_PREFIX_CASES])
+def test_fused_prefix_step_equals_separate_calls(pkv, oracle, name, N, K, H, ctx, groups, part_blocks,
+                                                 prefix_part_blocks):
+    """pkv_decode_step_prefix (the suffix pass's producers append each new row before loading its
+    block) equals pkv_slot_mapping + pkv_append + pkv_decode_attn_prefix bit for bit -- out, lse,
+    slots, both pools, flags -- on the mma.sync path and on both tcgen05 forms (whose suffix pass
+    overlaps the prefix pass on the GPU), with an empty sequence outside every group, a member whose
+    new token opens a block (ctx = 16 k + 1) and suffixes that span several partitions; and matches
+    the oracle's plain decode on every row."""
+    w = gen.make_workload(f"fp_{name}", 171, N, K, H, ctx)
+    tables, starts, pblocks = share_prefixes(w, groups)
+    q, kn, vn = bf16_dev(w.q), bf16_dev(w.k_new), bf16_dev(w.v_new)
+    bt, cl = i32_dev(tables), i32_dev(w.context_lens)
+    gs, pbd = i32_dev(starts), i32_dev(pblocks)
+    max_group, max_prefix = int(np.max(np.diff(starts))), int(pblocks.max())
+    nbytes = pkv.pkv_prefix_workspace_bytes(w.B, N, H, tables.shape[1], max_prefix, part_blocks,
+                                            prefix_part_blocks)
+    res = []
+    for fused in (False, True):
+        kc, vc = bf16_dev(w.k_cache), bf16_dev(w.v_cache)
+        out = torch.full_like(q, float("nan"))
+        lse = torch.full((w.B, N), float("nan"), dtype=torch.float32, device="cuda")
+        slots = torch.full((w.B,), -7, dtype=torch.int64, device="cuda")
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if fused:
+            pkv.check(pkv.pkv_decode_step_prefix(q, kn, vn, kc, vc, bt, cl, w.scale, gs, pbd, max_group,
+                                                 max_prefix, out, lse, slots, part_blocks, ws, err,
+                                                 prefix_partition_blocks=prefix_part_blocks))
+        else:
+            pkv.check(pkv.pkv_slot_mapping(bt, cl, w.num_blocks, slots, err))
+            pkv.check(pkv.pkv_append(kn, vn, slots, kc, vc, err))
+            pkv.check(pkv.pkv_decode_attn_prefix(q, kc, vc, bt, cl, w.scale, gs, pbd, max_group, max_prefix,
+                                                 out, lse, part_blocks, ws, err,
+                                                 prefix_partition_blocks=prefix_part_blocks))
+        res.append((out, lse, slots, kc, vc, pkv.pkv_read_err_flag(err)))
+    (o1, l1, s1, k1, v1, f1), (o2, l2, s2, k2, v2, f2) = res
+    assert f1 == f2 == (pkv.PKV_OK, 0)
+    ref_slots = oracle.slot_mapping(tables, w.context_lens)
+    assert torch.equal(s1, s2) and np.array_equal(s2.cpu().numpy(), ref_slots)
+    assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
+    assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.append(w.k_new, w.v_new, ref_slots, kc, vc)
+    assert np.array_equal(bf16_host(k2), kc) and np.array_equal(bf16_host(v2), vc)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, tables, w.context_lens, w.scale)
+    assert_close(out_f64(o2), ref, f"fused prefix step {name}")
+    assert_lse_close(l2.cpu().numpy().astype(np.float64), ref_lse, f"fused prefix step {name}")
+
+
+def test_fused_prefix_step_refuses_a_write_into_shared_blocks(pkv, oracle):
+    """A member whose context ends exactly at its group's shared blocks would append into a block
+    every member reads: the fused step flags it (PKV_FLAG_GROUP_RANGE), writes no row (slot -1, both
+    pools unchanged there) and still computes every other sequence as the oracle does."""
+    w = gen.make_workload("fp_shared_end", 172, 32, 8, 128, [200, 96, 250, 300])
+    tables, starts, pblocks = share_prefixes(w, [(0, 1, 6), (2, 4, 6)])
+    # sequence 1 joins group 0 with ctx = 96 = 16 * 6: its new token would land in a shared block
+    starts = np.array([0, 2, 4], dtype=np.int32)
+    pblocks = np.array([6, 6], dtype=np.int32)
+    tables[1, :6] = tables[0, :6]
+    q, kn, vn = bf16_dev(w.q), bf16_dev(w.k_new), bf16_dev(w.v_new)
+    kc, vc = bf16_dev(w.k_cache), bf16_dev(w.v_cache)
+    k_before, v_before = kc.clone(), vc.clone()
+    out = torch.empty_like(q)
+    slots = torch.full((w.B,), -7, dtype=torch.int64, device="cuda")
+    ws = torch.empty(pkv.pkv_prefix_workspace_bytes(w.B, w.N, w.H, tables.shape[1], 6, 16, 0),
+                     dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.check(pkv.pkv_decode_step_prefix(q, kn, vn, kc, vc, i32_dev(tables), i32_dev(w.context_lens), w.scale,
+                                         i32_dev(starts), i32_dev(pblocks), 2, 6, out, None, slots, 16, ws, err))
+    st, flag = pkv.pkv_read_err_flag(err)
+    assert st == pkv.PKV_ERR_RANGE and flag == pkv.PKV_FLAG_GROUP_RANGE
+    s = slots.cpu().numpy()
+    ref_slots = oracle.slot_mapping(tables, w.context_lens)
+    assert s[1] == -1 and np.array_equal(s[[0, 2, 3]], ref_slots[[0, 2, 3]])
+    # only the other sequences' rows were written, in both pools
+    written = sorted(int(x) for x in ref_slots[[0, 2, 3]])
+    for after, before in ((kc, k_before), (vc, v_before)):
+        rows = (after.view(torch.int16) != before.view(torch.int16)).any(-1).any(-1).view(-1)
+        assert torch.nonzero(rows).view(-1).cpu().tolist() == written
+    kh, vh = w.k_cache.copy(), w.v_cache.copy()
+    keep = [0, 2, 3]
+    oracle.append(w.k_new[keep], w.v_new[keep], ref_slots[keep], kh, vh)
+    ref, _ = oracle.decode(w.q, kh, vh, tables, w.context_lens, w.scale)
+    assert_close(out_f64(out)[keep], ref[keep], "fused prefix step, other sequences")
