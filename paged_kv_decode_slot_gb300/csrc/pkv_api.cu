@@ -363,9 +363,11 @@ PKV_EXPORT int pkv_decode_attn_partitions(const pkv_bf16 *q, const pkv_bf16 *k_c
 namespace {
 
 // pkv_lse_merge, for partials in the uniform (taper false) or the tapered partition layout.
+// pdl: the partials come from the launch just before on the stream, which lets the merge be
+// scheduled early (griddepcontrol.launch_dependents); the merge waits for it in the kernel.
 int lse_merge_impl(const float *part_out, const float *part_lse, const int32_t *context_lens, int32_t num_seqs,
                    int32_t num_q_heads, int32_t head_dim, int32_t max_partitions, int32_t partition_blocks,
-                   pkv_bf16 *out, float *lse_out, bool taper, cudaStream_t stream)
+                   pkv_bf16 *out, float *lse_out, bool taper, cudaStream_t stream, bool pdl = false)
 {
     if (!part_out || !part_lse || !context_lens || !out) return PKV_ERR_NULL;
     if (num_seqs < 0 || num_q_heads <= 0 || max_partitions <= 0 || partition_blocks <= 0)
@@ -377,7 +379,7 @@ int lse_merge_impl(const float *part_out, const float *part_lse, const int32_t *
     if (num_seqs == 0) return PKV_OK;
     cudaError_t e = pkv::launch_lse_merge(part_out, part_lse, context_lens, num_seqs, num_q_heads,
                                           head_dim, max_partitions, partition_blocks, taper, out, lse_out,
-                                          stream);
+                                          stream, pdl);
     return e == cudaSuccess ? PKV_OK : cuda_fail(e, "lse merge launch");
 }
 
@@ -981,8 +983,9 @@ int multi_attention(const AttnArgs &a, int32_t num_new, const pkv_bf16 *k_new, c
     if (e != cudaSuccess) return cuda_fail(e, "multi-token attention launch");
     if (!split || p.counters) return PKV_OK;
     // rows of one sequence: its T tokens x N heads, all with the sequence's context length
+    // (the tcgen05 kernel lets the merge be scheduled while its last CTAs run)
     return lse_merge_impl(part_out, part_lse, a.context_lens, num_seqs, num_new * num_q_heads,
-                          cache.head_dim, max_partitions, partition_blocks, out, lse_out, p.taper != 0, stream);
+                          cache.head_dim, max_partitions, partition_blocks, out, lse_out, p.taper != 0, stream, tc);
 }
 
 }  // namespace

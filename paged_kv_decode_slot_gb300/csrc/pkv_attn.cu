@@ -382,6 +382,7 @@ lse_merge_kernel(const float *__restrict__ part_out, const float *__restrict__ p
                  __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out)
 {
     extern __shared__ float smem_f[];  // weights [R][np], then the warps' sums [kMergeWarps][R][H]
+    pdl_wait_primary();  // launched behind the attention grid (programmatic serialization): its partials
     const int n0 = blockIdx.x * R, b = blockIdx.y, t = threadIdx.x;
     const int nrows = min(R, N - n0);
     const size_t bn0 = (size_t)b * N + n0;
@@ -461,31 +462,30 @@ cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensor
 template <int H, int R>
 static cudaError_t launch_lse_merge_t(const float *part_out, const float *part_lse, const int32_t *context_lens,
                                       int B, int N, int max_parts, int part_blocks, int taper, uint16_t *out,
-                                      float *lse_out, cudaStream_t stream)
+                                      float *lse_out, cudaStream_t stream, bool pdl)
 {
     const size_t smem = (((size_t)R * max_parts + 3) / 4 * 4 + (size_t)kMergeWarps * R * H) * sizeof(float);
     static int cached[64] = {};
     cudaError_t e = ensure_smem(lse_merge_kernel<H, R>, (int)smem, cached);
     if (e != cudaSuccess) return e;
-    lse_merge_kernel<H, R><<<dim3((N + R - 1) / R, B), kMergeWarps * 32, smem, stream>>>(
-        part_out, part_lse, context_lens, N, max_parts, part_blocks, taper, reinterpret_cast<__nv_bfloat16 *>(out),
-        lse_out);
-    return cudaGetLastError();
+    return launch_kernel(lse_merge_kernel<H, R>, dim3((N + R - 1) / R, B), dim3(kMergeWarps * 32), smem, stream,
+                         pdl, part_out, part_lse, context_lens, N, max_parts, part_blocks, taper,
+                         reinterpret_cast<__nv_bfloat16 *>(out), lse_out);
 }
 
 cudaError_t launch_lse_merge(const float *part_out, const float *part_lse, const int32_t *context_lens,
                              int B, int N, int H, int max_parts, int part_blocks, bool taper, uint16_t *out,
-                             float *lse_out, cudaStream_t stream)
+                             float *lse_out, cudaStream_t stream, bool pdl)
 {
     const int tp = taper ? 1 : 0;
     // eight rows per CTA while their weights stay within 32 KB
     const bool eight = (int64_t)8 * max_parts <= 8192;
     if (H == 128)
-        return eight ? launch_lse_merge_t<128, 8>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, tp, out, lse_out, stream)
-                     : launch_lse_merge_t<128, 1>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, tp, out, lse_out, stream);
+        return eight ? launch_lse_merge_t<128, 8>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, tp, out, lse_out, stream, pdl)
+                     : launch_lse_merge_t<128, 1>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, tp, out, lse_out, stream, pdl);
     if (H == 64)
-        return eight ? launch_lse_merge_t<64, 8>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, tp, out, lse_out, stream)
-                     : launch_lse_merge_t<64, 1>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, tp, out, lse_out, stream);
+        return eight ? launch_lse_merge_t<64, 8>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, tp, out, lse_out, stream, pdl)
+                     : launch_lse_merge_t<64, 1>(part_out, part_lse, context_lens, B, N, max_parts, part_blocks, tp, out, lse_out, stream, pdl);
     return cudaErrorInvalidValue;
 }
 

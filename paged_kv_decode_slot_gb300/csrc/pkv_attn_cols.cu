@@ -289,6 +289,9 @@ __global__ void __launch_bounds__(kAttnThreads, PKV_CTAS_PER_SM)
 attn_cols_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const ColsParams p)
 {
+    // the merge launched behind this grid (programmatic serialization) may be scheduled once every
+    // CTA of it runs; it waits for this grid's completion before it reads the partials
+    pdl_launch_dependents();
     attn_cols_body<H>(tm_k, tm_v, p);
     // the suffix pass launched behind the tcgen05 prefix pass: its last CTA (scheduled last, so its
     // wait holds no slot another CTA of this grid needs) waits for that grid, so this one completes
@@ -310,6 +313,7 @@ __global__ void cascade_merge_kernel(const ColsParams p, __nv_bfloat16 *__restri
 {
     extern __shared__ float wts[];  // [max_parts]
     __shared__ float row_lse;
+    pdl_wait_primary();  // launched behind the attention launch (programmatic serialization)
     const int n = blockIdx.x, b = blockIdx.y, h = threadIdx.x;
     const int H = blockDim.x;
     const int64_t row = (int64_t)b * p.N + n;
@@ -362,21 +366,7 @@ static cudaError_t launch_cols_t(const CUtensorMap &tk, const CUtensorMap &tv, c
     static int cached[64] = {};
     cudaError_t e = ensure_cols_smem(attn_cols_kernel<H>, smem, cached);
     if (e != cudaSuccess) return e;
-    if (!pdl) {
-        attn_cols_kernel<H><<<(unsigned)grid, kAttnThreads, smem, stream>>>(tk, tv, p);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_cols_kernel<H>, tk, tv, p);
+    return launch_kernel(attn_cols_kernel<H>, dim3((unsigned)grid), dim3(kAttnThreads), smem, stream, pdl, tk, tv, p);
 }
 
 cudaError_t launch_attn_cols(int H, const CUtensorMap &tk, const CUtensorMap &tv, const ColsParams &p,
@@ -393,8 +383,10 @@ cudaError_t launch_cascade_merge(const ColsParams &p, int H, __nv_bfloat16 *out,
                                  cudaStream_t stream)
 {
     if (p.B <= 0) return cudaSuccess;
-    cascade_merge_kernel<<<dim3(p.N, p.B), H, (size_t)p.max_parts * sizeof(float), stream>>>(p, out, lse_out);
-    return cudaGetLastError();
+    // behind the attention launch that wrote the partials (whose completion implies the prefix
+    // pass's when the two passes are two launches)
+    return launch_kernel(cascade_merge_kernel, dim3(p.N, p.B), dim3(H), (size_t)p.max_parts * sizeof(float),
+                         stream, true, p, out, lse_out);
 }
 
 }  // namespace pkv

@@ -7,7 +7,33 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace pkv {
+
+// Launch `kernel`; with pdl, with programmatic stream serialization: its CTAs may be scheduled once
+// every CTA of the grid ahead of it on the stream has executed griddepcontrol.launch_dependents
+// (or exited), so the kernel must execute griddepcontrol.wait before it reads that grid's results.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, bool pdl, Args &&...args)
+{
+    if (!pdl) {
+        kernel<<<grid, block, smem, stream>>>(std::forward<Args>(args)...);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // The log-sum-exp merge of a row's partitions (merge_rows): kMergeWarps warps split the
 // partitions; the last partition CTA of a split runs it inside the attention kernel when the
@@ -151,9 +177,12 @@ cudaError_t launch_append_fp8(const uint16_t *k_new, const uint16_t *v_new, cons
                               cudaStream_t stream);
 
 // taper: the partials come from partition_range's tapered layout (partition_count partitions).
+// pdl: launched with programmatic stream serialization behind the kernel that wrote the partials
+// (which executes griddepcontrol.launch_dependents); the merge waits for it in the kernel.
 cudaError_t launch_lse_merge(const float *part_out, const float *part_lse,
                              const int32_t *context_lens, int B, int N, int H, int max_parts,
-                             int part_blocks, bool taper, uint16_t *out, float *lse_out, cudaStream_t stream);
+                             int part_blocks, bool taper, uint16_t *out, float *lse_out, cudaStream_t stream,
+                             bool pdl = false);
 
 cudaError_t launch_slot_mapping(const int32_t *block_tables, int max_nb, const int32_t *context_lens,
                                 int B, int num_blocks, int64_t *slots, int32_t *err_flag,
