@@ -459,6 +459,76 @@ cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensor
                  : launch_attn_t<64, false, false>(tk, tv, p, grid, stream);
 }
 
+// pkv_lse_merge for rows of at most kFewParts partition slots (max_parts <= kFewParts): one warp per
+// row, six rows a CTA.  Every load -- the length, the row's partial lse and partials of every slot
+// -- is issued at once (slots past the row's partitions are read and never used), then the weights
+// (lse_merge_weights, on the warp's copy of the lse) and the sum in merge_rows' order: merge slot s
+// adds partitions s, s + kMergeWarps, ... with fused multiply-adds, the slots' sums are added in slot
+// order -- the same bits as merge_rows and the in-kernel merges.  Few registers, so many CTAs per SM
+// (merge_rows keeps eight rows a warp in flight: 96 registers, three 192-thread CTAs per SM; eight
+// new tokens on the Llama-3-8B batch of 64 merge 16,384 rows).
+constexpr int kFewParts = 8;
+
+template <int H>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+lse_merge_few_kernel(const float *__restrict__ part_out, const float *__restrict__ part_lse,
+                     const int32_t *__restrict__ context_lens, int N, int max_parts, int part_blocks, int taper,
+                     __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out)
+{
+    constexpr int E = H / 32;
+    static_assert(E == 2 || E == 4, "H = 64 or 128");
+    __shared__ float wsm[kMergeWarps][kFewParts];
+    pdl_wait_primary();  // launched behind the attention grid (programmatic serialization): its partials
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = blockIdx.x * kMergeWarps + warp, b = blockIdx.y;
+    if (n >= N) return;  // the whole warp
+    const size_t row = (size_t)b * N + n;
+    const float *po = part_out + row * max_parts * H + lane * E;
+    float v[kFewParts][E];
+#pragma unroll
+    for (int q = 0; q < kFewParts; ++q) {
+        if (q < max_parts) {
+            if constexpr (E == 4) {
+                const float4 x = __ldcg(reinterpret_cast<const float4 *>(po + (size_t)q * H));
+                v[q][0] = x.x, v[q][1] = x.y, v[q][2] = x.z, v[q][3] = x.w;
+            } else {
+                const float2 x = __ldcg(reinterpret_cast<const float2 *>(po + (size_t)q * H));
+                v[q][0] = x.x, v[q][1] = x.y;
+            }
+        }
+    }
+    const float lp = lane < max_parts ? __ldcg(part_lse + row * max_parts + lane) : 0.f;
+    const int ctx = context_lens[b];
+    const int nb = ctx > 0 ? (ctx + kBlockSize - 1) / kBlockSize : 0;
+    const int np = min(partition_count(nb, part_blocks, taper != 0), max_parts);
+    float *w = wsm[warp];
+    if (lane < kFewParts) w[lane] = lp;
+    __syncwarp();
+    const float L = lse_merge_weights<true>(w, np, w, lane);
+    if (lane == 0 && lse_out) lse_out[row] = L;
+    float sum[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) sum[e] = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMergeWarps; ++s) {
+        float acc[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int q = s; q < kFewParts; q += kMergeWarps) {
+            if (q < np) {
+                const float wq = w[q];
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = __fmaf_rn(wq, v[q][e], acc[e]);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) sum[e] += acc[e];
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[row * H + lane * E + e] = __float2bfloat16_rn(sum[e]);
+}
+
 template <int H, int R>
 static cudaError_t launch_lse_merge_t(const float *part_out, const float *part_lse, const int32_t *context_lens,
                                       int B, int N, int max_parts, int part_blocks, int taper, uint16_t *out,
@@ -478,6 +548,14 @@ cudaError_t launch_lse_merge(const float *part_out, const float *part_lse, const
                              float *lse_out, cudaStream_t stream, bool pdl)
 {
     const int tp = taper ? 1 : 0;
+    if (max_parts <= kFewParts && (H == 128 || H == 64)) {
+        const dim3 grid((N + kMergeWarps - 1) / kMergeWarps, B);
+        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(out);
+        return H == 128 ? launch_kernel(lse_merge_few_kernel<128>, grid, dim3(kMergeWarps * 32), 0, stream, pdl,
+                                        part_out, part_lse, context_lens, N, max_parts, part_blocks, tp, o, lse_out)
+                        : launch_kernel(lse_merge_few_kernel<64>, grid, dim3(kMergeWarps * 32), 0, stream, pdl,
+                                        part_out, part_lse, context_lens, N, max_parts, part_blocks, tp, o, lse_out);
+    }
     // eight rows per CTA while their weights stay within 32 KB
     const bool eight = (int64_t)8 * max_parts <= 8192;
     if (H == 128)
