@@ -42,12 +42,21 @@ constexpr int kTcM = 128;          // MMA rows
 constexpr int kTcProducers = 2;
 constexpr uint32_t kTcCols = 256;  // TMEM columns: O [0, H), S/P buffers at H and H + 64
 
+// Ring depths of the two forms (stages of one K and one V tile; a multiple of 4): 12 and 8 keep
+// two CTAs per SM, which the tensor memory allows (256 columns each).
+#ifndef PKV_TC_STAGES_32
+#define PKV_TC_STAGES_32 12
+#endif
+#ifndef PKV_TC_STAGES_128
+#define PKV_TC_STAGES_128 8
+#endif
+
 // RW row warps (32 rows each), then the QK^T warp, the PV warp and the two producers.
 template <int RW>
 struct TcRoles {
     static_assert(RW == 1 || RW == 4, "32 or 128 query rows a CTA");
     static constexpr int kRows = 32 * RW;
-    static constexpr int kStages = RW == 1 ? 12 : 8;
+    static constexpr int kStages = RW == 1 ? PKV_TC_STAGES_32 : PKV_TC_STAGES_128;
     static constexpr int kQkWarp = RW, kPvWarp = RW + 1, kProd0 = RW + 2;
     static constexpr int kThreads = (RW + 4) * 32;
     static_assert(kStages % kTcProducers == 0, "pipeline depth must be a multiple of the producer warps");
@@ -83,8 +92,8 @@ struct TcLayout {
     static_assert(kKOffset % 1024 == 0 && kVOffset % 1024 == 0 && kKHalfTile % 1024 == 0 && kVTile % 1024 == 0,
                   "128B-swizzle atoms need 1024-byte alignment");
     static_assert(kStages % kTcGroupTiles == 0, "a group's K tiles must not wrap around the ring");
-    static_assert(2 * (kAlloc + 1024) <= 228 * 1024 && 3 * (kAlloc + 1024) > 228 * 1024,
-                  "two CTAs per SM (2 x 256 TMEM columns fill the SM's 512)");
+    static_assert(kAlloc + 1024 <= 228 * 1024 && 3 * (kAlloc + 1024) > 228 * 1024,
+                  "at most two CTAs per SM (2 x 256 TMEM columns fill the SM's 512)");
 };
 
 // Producer side of one tile: wait until the previous group in the tile's group slot is released
