@@ -541,6 +541,7 @@ FUSED_PREFIX_CASES = [
     ("tc32_g8", 64, 8, 128, [150, 170, 190, 210, 77], [(0, 4, 9)]),
     ("tc128_g8_edges", 64, 8, 128, [130 + 7 * i for i in range(11)] + [129], [(0, 12, 8)]),
     ("tc128_long_suffix", 64, 8, 128, [700 + 90 * i for i in range(20)], [(0, 20, 40)]),
+    ("mma_mha_h64", 8, 8, 64, [70, 90, 110, 130, 150, 33], [(0, 5, 4)]),
 ]
 
 
