@@ -87,12 +87,12 @@ __device__ __forceinline__ void append_new_token_fp8(const AttnParams &p, int b,
 // ------------------------ single pass and fixed partitions --------------------------------
 // kFp8: the pools hold e4m3 codes with per-KV-head scales (H = 128); the K scale is folded into
 // the logit multiplier, the V scale into the final normalisation.
-template <int H, bool kSplit, bool kFp8 = false, bool kPairs = false, bool kBScale = false>
-__global__ void __launch_bounds__(kAttnThreads, PKV_CTAS_PER_SM)
+template <int H, bool kSplit, bool kFp8 = false, bool kPairs = false, bool kBScale = false, bool kDeep = false>
+__global__ void __launch_bounds__(kAttnThreads, kDeep ? 2 : PKV_CTAS_PER_SM)
 attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
             const AttnParams p)
 {
-    constexpr int S = kFp8 ? kStagesFp8 : kStages;
+    constexpr int S = kFp8 ? kStagesFp8 : (kDeep ? kStagesDeep : kStages);
     using L = AttnLayout<H, S, kConsumerWarps, kProducers, kFp8 ? 1 : 2>;
 
     extern __shared__ uint8_t smem_raw[];
@@ -421,17 +421,28 @@ static cudaError_t ensure_smem(Kern kern, int smem, int *cached)
     return e;
 }
 
-template <int H, bool kSplit, bool kFp8, bool kPairs = false, bool kBScale = false>
+template <int H, bool kSplit, bool kFp8, bool kPairs = false, bool kBScale = false, bool kDeep = false>
 static cudaError_t launch_attn_t(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &p,
                                  dim3 grid, cudaStream_t stream)
 {
-    constexpr int smem = AttnLayout<H, kFp8 ? kStagesFp8 : kStages, kConsumerWarps, kProducers,
-                                    kFp8 ? 1 : 2>::kAlloc;
+    constexpr int smem = AttnLayout<H, kFp8 ? kStagesFp8 : (kDeep ? kStagesDeep : kStages), kConsumerWarps,
+                                    kProducers, kFp8 ? 1 : 2>::kAlloc;
     static int cached[64] = {};
-    cudaError_t e = ensure_smem(attn_kernel<H, kSplit, kFp8, kPairs, kBScale>, smem, cached);
+    cudaError_t e = ensure_smem(attn_kernel<H, kSplit, kFp8, kPairs, kBScale, kDeep>, smem, cached);
     if (e != cudaSuccess) return e;
-    attn_kernel<H, kSplit, kFp8, kPairs, kBScale><<<grid, kAttnThreads, smem, stream>>>(tk, tv, p);
+    attn_kernel<H, kSplit, kFp8, kPairs, kBScale, kDeep><<<grid, kAttnThreads, smem, stream>>>(tk, tv, p);
     return cudaGetLastError();
+}
+
+// SMs of the current device (cached per device).
+static int device_sms()
+{
+    static int sms[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 0;
+    if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    return sms[dev];
 }
 
 cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensorMap &tv,
@@ -451,6 +462,16 @@ cudaError_t launch_attn(int H, bool split, const CUtensorMap &tk, const CUtensor
                          : launch_attn_t<128, false, true, true>(tk, tv, p, grid, stream);
         return split ? launch_attn_t<128, true, true>(tk, tv, p, grid, stream)
                      : launch_attn_t<128, false, true>(tk, tv, p, grid, stream);
+    }
+    // bf16: a grid that fits in one wave at two CTAs per SM takes the deeper ring (kStagesDeep)
+    const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
+    const int sms = device_sms();
+    if (sms > 0 && ctas <= 2 * (int64_t)sms) {
+        if (H == 128)
+            return split ? launch_attn_t<128, true, false, false, false, true>(tk, tv, p, grid, stream)
+                         : launch_attn_t<128, false, false, false, false, true>(tk, tv, p, grid, stream);
+        return split ? launch_attn_t<64, true, false, false, false, true>(tk, tv, p, grid, stream)
+                     : launch_attn_t<64, false, false, false, false, true>(tk, tv, p, grid, stream);
     }
     if (H == 128)
         return split ? launch_attn_t<128, true, false>(tk, tv, p, grid, stream)

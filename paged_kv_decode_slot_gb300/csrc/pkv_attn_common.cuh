@@ -31,8 +31,15 @@ namespace pkv {
 #ifndef PKV_CONSUMERS
 #define PKV_CONSUMERS 4
 #endif
+// A grid that fits in one wave at two CTAs per SM leaves the third CTA slot of every SM empty;
+// there the bf16 kernel takes a deeper ring at two CTAs per SM instead (more bytes in flight per
+// CTA for the same bytes per SM): the 20-sequence shared-prompt batch, 160 CTAs, 30.5 -> 26.6 us.
+#ifndef PKV_STAGES_DEEP
+#define PKV_STAGES_DEEP 12
+#endif
 constexpr int kConsumerWarps = PKV_CONSUMERS;
 constexpr int kStages = PKV_STAGES;
+constexpr int kStagesDeep = PKV_STAGES_DEEP;
 constexpr int kStagesFp8 = PKV_FP8_STAGES;  // e4m3 tiles are half the bytes: twice the depth
 constexpr int kProducers = PKV_PRODUCERS;
 constexpr int kAttnThreads = (kConsumerWarps + kProducers) * 32;
@@ -43,6 +50,8 @@ constexpr int kAttnThreads = (kConsumerWarps + kProducers) * 32;
 static_assert(kStages % kConsumerWarps == 0, "pipeline depth must be a multiple of the consumer warps");
 static_assert(kStages % kProducers == 0, "pipeline depth must be a multiple of the producer warps");
 static_assert(kStagesFp8 % kConsumerWarps == 0 && kStagesFp8 % kProducers == 0,
+              "pipeline depth must be a multiple of the consumer and producer warps");
+static_assert(kStagesDeep % kConsumerWarps == 0 && kStagesDeep % kProducers == 0,
               "pipeline depth must be a multiple of the consumer and producer warps");
 
 // Lazy rescaling: keep the running maximum until a new logit exceeds it by this much
