@@ -269,14 +269,21 @@ __device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&
         uint32_t r[4];
         ldsm_x4(r, kt + fp8_chunk_offset(tok, kk + coff));
         uint32_t a0[4], a1[4];
-        a0[0] = e4m3x2_to_f16x2((uint16_t)(r[0] & 0xFFFFu));
-        a0[1] = e4m3x2_to_f16x2((uint16_t)(r[1] & 0xFFFFu));
-        a0[2] = e4m3x2_to_f16x2((uint16_t)(r[0] >> 16));
-        a0[3] = e4m3x2_to_f16x2((uint16_t)(r[1] >> 16));
-        a1[0] = e4m3x2_to_f16x2((uint16_t)(r[2] & 0xFFFFu));
-        a1[1] = e4m3x2_to_f16x2((uint16_t)(r[3] & 0xFFFFu));
-        a1[2] = e4m3x2_to_f16x2((uint16_t)(r[2] >> 16));
-        a1[3] = e4m3x2_to_f16x2((uint16_t)(r[3] >> 16));
+        if constexpr (kBS) {  // (per-half conversions: the register allocation measured faster here)
+            a0[0] = e4m3x2_to_f16x2((uint16_t)(r[0] & 0xFFFFu));
+            a0[1] = e4m3x2_to_f16x2((uint16_t)(r[1] & 0xFFFFu));
+            a0[2] = e4m3x2_to_f16x2((uint16_t)(r[0] >> 16));
+            a0[3] = e4m3x2_to_f16x2((uint16_t)(r[1] >> 16));
+            a1[0] = e4m3x2_to_f16x2((uint16_t)(r[2] & 0xFFFFu));
+            a1[1] = e4m3x2_to_f16x2((uint16_t)(r[3] & 0xFFFFu));
+            a1[2] = e4m3x2_to_f16x2((uint16_t)(r[2] >> 16));
+            a1[3] = e4m3x2_to_f16x2((uint16_t)(r[3] >> 16));
+        } else {
+            e4m3x4_to_f16x2x2(r[0], a0[0], a0[2]);
+            e4m3x4_to_f16x2x2(r[1], a0[1], a0[3]);
+            e4m3x4_to_f16x2x2(r[2], a1[0], a1[2]);
+            e4m3x4_to_f16x2x2(r[3], a1[1], a1[3]);
+        }
         mma_f16_16816(sa, a0, qf[kk][0], qf[kk][1]);
         mma_f16_16816(sb, a1, qf[kk + 1][0], qf[kk + 1][1]);
     }
@@ -344,10 +351,15 @@ __device__ __forceinline__ void tile_update_fp8(WarpAcc<H> &a, const uint32_t (&
             const uint32_t lo = byte_perm(r[2 * hf], 0u, 0x3120u);      // tokens 0-7 of the tile
             const uint32_t hi = byte_perm(r[2 * hf + 1], 0u, 0x3120u);  // tokens 8-15
             uint32_t av[4];
-            av[0] = e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu));
-            av[1] = e4m3x2_to_f16x2((uint16_t)(lo >> 16));
-            av[2] = e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu));
-            av[3] = e4m3x2_to_f16x2((uint16_t)(hi >> 16));
+            if constexpr (kBS) {
+                av[0] = e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu));
+                av[1] = e4m3x2_to_f16x2((uint16_t)(lo >> 16));
+                av[2] = e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu));
+                av[3] = e4m3x2_to_f16x2((uint16_t)(hi >> 16));
+            } else {
+                e4m3x4_to_f16x2x2(lo, av[0], av[1]);
+                e4m3x4_to_f16x2x2(hi, av[2], av[3]);
+            }
             if (partial) {
                 const uint32_t lo0 = tc < valid ? 0x0000FFFFu : 0u;
                 const uint32_t hi0 = tc + 1 < valid ? 0xFFFF0000u : 0u;
@@ -392,14 +404,21 @@ __device__ __forceinline__ void tile_update_fp8_n(WarpAcc<H> &a, const uint32_t 
             uint32_t r[4];
             ldsm_x4(r, kt[t] + fp8_chunk_offset(tok, kk + coff));
             uint32_t a0[4], a1[4];
-            a0[0] = e4m3x2_to_f16x2((uint16_t)(r[0] & 0xFFFFu));
-            a0[1] = e4m3x2_to_f16x2((uint16_t)(r[1] & 0xFFFFu));
-            a0[2] = e4m3x2_to_f16x2((uint16_t)(r[0] >> 16));
-            a0[3] = e4m3x2_to_f16x2((uint16_t)(r[1] >> 16));
-            a1[0] = e4m3x2_to_f16x2((uint16_t)(r[2] & 0xFFFFu));
-            a1[1] = e4m3x2_to_f16x2((uint16_t)(r[3] & 0xFFFFu));
-            a1[2] = e4m3x2_to_f16x2((uint16_t)(r[2] >> 16));
-            a1[3] = e4m3x2_to_f16x2((uint16_t)(r[3] >> 16));
+            if constexpr (kBS) {  // (as in tile_update_fp8)
+                a0[0] = e4m3x2_to_f16x2((uint16_t)(r[0] & 0xFFFFu));
+                a0[1] = e4m3x2_to_f16x2((uint16_t)(r[1] & 0xFFFFu));
+                a0[2] = e4m3x2_to_f16x2((uint16_t)(r[0] >> 16));
+                a0[3] = e4m3x2_to_f16x2((uint16_t)(r[1] >> 16));
+                a1[0] = e4m3x2_to_f16x2((uint16_t)(r[2] & 0xFFFFu));
+                a1[1] = e4m3x2_to_f16x2((uint16_t)(r[3] & 0xFFFFu));
+                a1[2] = e4m3x2_to_f16x2((uint16_t)(r[2] >> 16));
+                a1[3] = e4m3x2_to_f16x2((uint16_t)(r[3] >> 16));
+            } else {
+                e4m3x4_to_f16x2x2(r[0], a0[0], a0[2]);
+                e4m3x4_to_f16x2x2(r[1], a0[1], a0[3]);
+                e4m3x4_to_f16x2x2(r[2], a1[0], a1[2]);
+                e4m3x4_to_f16x2x2(r[3], a1[1], a1[3]);
+            }
             mma_f16_16816(sa, a0, qf[kk][0], qf[kk][1]);
             mma_f16_16816(sb, a1, qf[kk + 1][0], qf[kk + 1][1]);
         }
@@ -485,10 +504,15 @@ __device__ __forceinline__ void tile_update_fp8_n(WarpAcc<H> &a, const uint32_t 
                 const uint32_t lo = byte_perm(r[2 * hf], 0u, 0x3120u);
                 const uint32_t hi = byte_perm(r[2 * hf + 1], 0u, 0x3120u);
                 uint32_t av[4];
-                av[0] = e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu));
-                av[1] = e4m3x2_to_f16x2((uint16_t)(lo >> 16));
-                av[2] = e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu));
-                av[3] = e4m3x2_to_f16x2((uint16_t)(hi >> 16));
+                if constexpr (kBS) {
+                    av[0] = e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu));
+                    av[1] = e4m3x2_to_f16x2((uint16_t)(lo >> 16));
+                    av[2] = e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu));
+                    av[3] = e4m3x2_to_f16x2((uint16_t)(hi >> 16));
+                } else {
+                    e4m3x4_to_f16x2x2(lo, av[0], av[1]);
+                    e4m3x4_to_f16x2x2(hi, av[2], av[3]);
+                }
                 if (partial) {
                     const uint32_t lo0 = tc < valid[t] ? 0x0000FFFFu : 0u;
                     const uint32_t hi0 = tc + 1 < valid[t] ? 0xFFFF0000u : 0u;

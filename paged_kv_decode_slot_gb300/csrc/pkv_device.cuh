@@ -179,6 +179,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes)
     return out;
 }
 
+// Four e4m3 codes (bytes 0..3 of x) -> two f16x2, lo = codes 0 and 1, hi = codes 2 and 3 (exact).
+// Both halves of the register go straight to the conversions in one asm block, so no separate
+// half extraction is needed.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t &lo, uint32_t &hi)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
+
 // Two floats -> two e4m3 codes, round to nearest even, saturating at +-448 (lo in the low byte).
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi)
 {
