@@ -632,3 +632,88 @@ def test_fused_prefix_step_refuses_a_write_into_shared_blocks(pkv, oracle):
     oracle.append(w.k_new[keep], w.v_new[keep], ref_slots[keep], kh, vh)
     ref, _ = oracle.decode(w.q, kh, vh, tables, w.context_lens, w.scale)
     assert_close(out_f64(out)[keep], ref[keep], "fused prefix step, other sequences")
+
+
+@pytest.mark.parametrize("kind", ["prefix_tc128", "prefix_tc32", "multi_T8"])
+def test_graph_replay_of_overlapped_launches_equals_eager(pkv, oracle, kind):
+    """Steps whose launches overlap on the GPU through programmatic serialization -- the tcgen05
+    prefix pass with the suffix pass launched behind it and the merge behind both, and the tcgen05
+    multi-token kernel with its merge behind it -- captured in a CUDA graph and replayed three times
+    give bit for bit what the eager launches give (the graph keeps the programmatic dependencies),
+    and match the oracle."""
+    from paged_kv_decode_slot_gb300.step import MultiTokenStep, PrefixDecodeStep, StepGraph
+    if kind.startswith("prefix"):
+        groups = [(0, 12, 8)] if kind == "prefix_tc128" else [(0, 4, 9)]
+        ctx = [130 + 7 * i for i in range(12)] if kind == "prefix_tc128" else [150, 170, 190, 210, 77]
+        w = gen.make_workload(f"g_{kind}", 181, 64, 8, 128, ctx)
+        tables, starts, pblocks = share_prefixes(w, groups)
+
+        def make():
+            return PrefixDecodeStep(bf16_dev(w.q), bf16_dev(w.k_new), bf16_dev(w.v_new), bf16_dev(w.k_cache),
+                                    bf16_dev(w.v_cache), i32_dev(tables), i32_dev(w.context_lens), w.scale,
+                                    i32_dev(starts), i32_dev(pblocks), int(np.max(np.diff(starts))),
+                                    int(pblocks.max()), partition_blocks=4, prefix_partition_blocks=3)
+        kc, vc = w.k_cache.copy(), w.v_cache.copy()
+        oracle.append(w.k_new, w.v_new, oracle.slot_mapping(tables, w.context_lens), kc, vc)
+        ref, _ = oracle.decode(w.q, kc, vc, tables, w.context_lens, w.scale)
+    else:
+        w = gen.make_workload("g_multi", 182, 16, 4, 128, [0, 3, 17, 300, 700, 1000])
+        c = MultiCase(oracle, w, 8, 183)
+
+        def make():
+            return MultiTokenStep(bf16_dev(c.q), bf16_dev(c.k_new), bf16_dev(c.v_new), bf16_dev(w.k_cache),
+                                  bf16_dev(w.v_cache), i32_dev(w.block_tables), i32_dev(w.context_lens), w.scale,
+                                  partition_blocks=8)
+        ref, _ = c.reference(oracle)
+    eager = make()
+    assert eager.launches_per_step() >= 2
+    eager.run()
+    graphed = make()
+    g = StepGraph(graphed)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager.out.view(torch.int16), graphed.out.view(torch.int16)), kind
+    assert torch.equal(eager.lse, graphed.lse) and torch.equal(eager.slot_mapping, graphed.slot_mapping)
+    assert torch.equal(eager.k_cache.view(torch.int16), graphed.k_cache.view(torch.int16))
+    assert_close(out_f64(graphed.out), ref, f"graph replay {kind}")
+
+
+def test_fused_prefix_step_bad_block_is_flagged_and_skipped(pkv, oracle):
+    """A table entry outside the pool in the block that holds a sequence's new token (past the
+    shared prefix): the fused shared-prefix step flags it, writes nothing there and reports slot -1,
+    as pkv_slot_mapping + pkv_append do, and computes every other sequence as the oracle does."""
+    w = gen.make_workload("fp_bad", 184, 64, 8, 128, [150, 170, 190, 210, 77])
+    tables, starts, pblocks = share_prefixes(w, [(0, 4, 9)])
+    tables = tables.copy()
+    tables[2, (int(w.context_lens[2]) - 1) // 16] = w.num_blocks + 3
+    q, kn, vn = bf16_dev(w.q), bf16_dev(w.k_new), bf16_dev(w.v_new)
+    bt, cl = i32_dev(tables), i32_dev(w.context_lens)
+    res = []
+    for fused in (False, True):
+        kc, vc = bf16_dev(w.k_cache), bf16_dev(w.v_cache)
+        out = torch.empty_like(q)
+        slots = torch.full((w.B,), -7, dtype=torch.int64, device="cuda")
+        ws = torch.empty(pkv.pkv_prefix_workspace_bytes(w.B, w.N, w.H, tables.shape[1], 9, 4, 0),
+                         dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if fused:
+            pkv.check(pkv.pkv_decode_step_prefix(q, kn, vn, kc, vc, bt, cl, w.scale, i32_dev(starts), i32_dev(pblocks),
+                                                 4, 9, out, None, slots, 4, ws, err))
+        else:
+            pkv.check(pkv.pkv_slot_mapping(bt, cl, w.num_blocks, slots, err))
+            pkv.check(pkv.pkv_append(kn, vn, slots, kc, vc, err))
+            pkv.check(pkv.pkv_decode_attn_prefix(q, kc, vc, bt, cl, w.scale, i32_dev(starts), i32_dev(pblocks), 4, 9,
+                                                 out, None, 4, ws, err))
+        res.append((out, slots, kc, vc, pkv.pkv_read_err_flag(err)))
+    (o1, s1, k1, v1, f1), (o2, s2, k2, v2, f2) = res
+    assert f1 == f2 and f2[1] & pkv.PKV_FLAG_BLOCK_RANGE
+    assert torch.equal(s1, s2) and int(s2[2]) == -1
+    assert torch.equal(k1.view(torch.int16), k2.view(torch.int16)) and torch.equal(v1.view(torch.int16),
+                                                                                   v2.view(torch.int16))
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    kh, vh = w.k_cache.copy(), w.v_cache.copy()
+    keep = [0, 1, 3, 4]
+    oracle.append(w.k_new[keep], w.v_new[keep], oracle.slot_mapping(tables, w.context_lens)[keep], kh, vh)
+    ref, _ = oracle.decode(w.q, kh, vh, tables, w.context_lens, w.scale)
+    assert_close(out_f64(o2)[keep], ref[keep], "fused prefix step with a bad block, other sequences")
