@@ -348,11 +348,14 @@ int pkv_slot_mapping_multi(const int32_t *block_tables, int32_t max_blocks_per_s
    for bit) and leaves its counter (in the workspace's counter area) at zero again, so the
    workspace can be reused and captured in a CUDA graph.  The tcgen05 kernel and larger splits
    merge in a second launch (pkv_lse_merge).  Calls that share a workspace must not overlap on
-   the GPU.  Each CTA loads a K/V tile once for up to 32 of a
-   sequence's (token, head) rows of one KV head.  H in {64, 128}; G in {1, 2, 4, 8}.  With more
-   than 16 rows per CTA (min(T * G, 32) > 16) and H = 128 the contraction runs on the tcgen05
-   tensor cores (accumulators in tensor memory), otherwise on warp-level mma.sync; both compute
-   the same definition (results agree within rounding, not bit for bit). */
+   the GPU.  Each CTA loads a K/V tile once for up to 32 of a sequence's (token, head) rows of
+   one KV head (128 on the tensor cores when T * G > 32).  H in {64, 128}; G in {1, 2, 4, 8}.
+   With more than 16 rows per CTA (min(T * G, 32) > 16) and H = 128 the contraction runs on the
+   tcgen05 tensor cores (accumulators in tensor memory), otherwise on warp-level mma.sync; both
+   compute the same definition (results agree within rounding, not bit for bit).  The tcgen05
+   kernel's separate merge is launched with programmatic stream serialization (it may start while
+   the attention grid's last CTAs run and waits for that grid in the kernel); the call is ordered
+   on the stream as usual. */
 int pkv_decode_attn_multi(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
                           const int32_t *block_tables, int32_t max_blocks_per_seq,
                           const int32_t *context_lens, int32_t num_seqs, int32_t num_new,
