@@ -303,6 +303,12 @@ def make_config(name: str, threads: int = 0) -> Workload:
         # small enough for full profiler captures.
         ctx = uniform_int(2, _S_CTX, 16, 512, 8192)
         return make_workload("l3_8b_b16", 2, 32, 8, 128, ctx, threads=threads)
+    if name.startswith("l3_8b_b") and name[len("l3_8b_b"):].isdigit():
+        # Any batch size of the same draw (the first B context lengths of the stream above; B = 64
+        # and 16 are the two named workloads), for throughput-versus-batch measurements.
+        B = int(name[len("l3_8b_b"):])
+        ctx = uniform_int(2, _S_CTX, B, 512, 8192)
+        return make_workload(name, 2, 32, 8, 128, ctx, threads=threads)
     if name.startswith("l2_13b_mha_b"):
         B = int(name[len("l2_13b_mha_b"):])
         assert B in (1, 8, 64, 128)
